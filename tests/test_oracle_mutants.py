@@ -1,0 +1,63 @@
+"""Plant a plausible mistake in a copy of the C oracle and check that at least
+one pin fails on it.  The mistakes are planted on the CPU, in a temporary build
+of the oracle; the real oracle is untouched."""
+import os
+import subprocess
+
+import pytest
+
+from oracle_pins import ALL_PINS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "nvfp4_oracle.c")
+
+# (name, text in the oracle source, replacement, which occurrence (0-based))
+MUTANTS = [
+    ("e2m1_ties_to_lower", "(d == bestd && (c & 1) == 0 && (best & 1) == 1)", "0", 0),
+    ("e4m3_ties_to_lower", "(d == bestd && (c & 1) == 0 && (best & 1) == 1)", "0", 1),
+    ("e2m1_sign_dropped", "int sign = signbit(v) ? 8 : 0;", "int sign = 0;", 0),
+    ("e4m3_bias_off_by_one", "ldexp(8.0 + m, e - 10)", "ldexp(8.0 + m, e - 11)", 0),
+    ("scale_divisor_dropped", "float t = ga / 6.0f;", "float t = ga;", 0),
+    ("scale_without_global", "float ga = g * amax;", "float ga = amax;", 0),
+    ("data_without_global", "float y = x[i] * g;", "float y = x[i];", 0),
+    ("nibbles_swapped", "((lo_code & 15) | ((hi_code & 15) << 4))", "((hi_code & 15) | ((lo_code & 15) << 4))", 0),
+    ("gemm_weight_scale_dropped", "((double)c->ga[m] * (double)c->gw)", "((double)c->ga[m])", 0),
+    ("gemm_nibble_order", "uint8_t code = (kk & 1) ? (byte >> 4) : (byte & 15);",
+     "uint8_t code = (kk & 1) ? (byte & 15) : (byte >> 4);", 0),
+    ("gemm_block_scale_index", "deq_int(code, c->asf[m * (K / 16) + kk / 16])", "deq_int(code, c->asf[m * (K / 16) + kk / 32])", 0),
+    ("gate_up_swapped", "double gate = y1[m * 2 * I + i];\n            double up = y1[m * 2 * I + I + i];",
+     "double up = y1[m * 2 * I + i];\n            double gate = y1[m * 2 * I + I + i];", 0),
+    ("silu_sign", "gate / (1.0 + exp(-gate))", "gate / (1.0 + exp(gate))", 0),
+    ("route_unstable", "for (int64_t f = 0; f < R; ++f) perm[cursor[ids[f]]++] = (int32_t)f;",
+     "for (int64_t f = R - 1; f >= 0; --f) perm[cursor[ids[f]]++] = (int32_t)f;", 0),
+    ("validate_no_reciprocal_check", "if (!isfinite(r) || !isnormal(r)) ok = 0;", "(void)r;", 0),
+    ("rmsnorm_eps_outside", "sqrt(ss / (double)H + eps)", "(sqrt(ss / (double)H) + eps)", 0),
+]
+
+
+def _mutate(text, old, new, which):
+    pos = -1
+    for _ in range(which + 1):
+        pos = text.index(old, pos + 1)
+    return text[:pos] + new + text[pos + len(old):]
+
+
+@pytest.mark.parametrize("name,old,new,which", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(orc, tmp_path, name, old, new, which):
+    with open(SRC, encoding="utf-8") as f:
+        src = f.read()
+    mutated = _mutate(src, old, new, which)
+    assert mutated != src
+    c = tmp_path / f"{name}.c"
+    so = tmp_path / f"lib{name}.so"
+    c.write_text(mutated, encoding="utf-8")
+    subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                    str(c), "-o", str(so), "-lm"], check=True)
+    failed = []
+    with orc.use_library(str(so)):
+        for pin in ALL_PINS:
+            try:
+                pin(orc)
+            except Exception:  # an AssertionError, or a crash of the broken maths
+                failed.append(pin.__name__)
+    assert failed, f"no pin caught mutant {name}"
