@@ -1,0 +1,283 @@
+/*
+ * nvfp4_moe.h -- C ABI of the NVFP4 (W4A4) MoE expert forward for GB300 (sm_103a).
+ *
+ * What the library computes is the expert path described on the page
+ * "Gemma 4 NVFP4 MoE 空输出" (taking-lying-flat.github.io, a write-up of vLLM
+ * issue #51525), cited below as [page, section / figure]:
+ *
+ *   token reorder -> a1 quantisation -> grouped w13 GEMM
+ *     -> SiLU(gate)*up + a2 quantisation -> grouped w2 GEMM
+ *     -> restore token order and sum with the routing weights
+ *                                  [page, §矩阵融合 "MoE FFN", pipeline figure]
+ *
+ * preceded by the check the page says was missing: every expert's stored
+ * input-scale slot must be written and finite before its reciprocal is taken
+ * [page, ROOT CAUSE].
+ *
+ * Common rules for every entry point
+ *   - Pointers named *_host are host memory; every other pointer is DEVICE
+ *     memory on the current CUDA device.  All memory is owned by the caller;
+ *     the library allocates no device memory and keeps no per-call state.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *     stream-ordered and asynchronous unless the entry point says otherwise.
+ *   - The return value is an nvfp4_status.  On any status other than
+ *     NVFP4_OK no output buffer has been written, except where noted.
+ *     nvfp4_last_error_string() gives a one-line reason (thread-local).
+ *   - BF16 tensors are passed as uint16_t bit patterns.
+ *   - Shapes: E experts, H hidden size, I expert intermediate size, T tokens,
+ *     k experts per token, R = T*k routed rows.  Supported: 1 <= E <= 1024,
+ *     1 <= k <= min(32, E), H % 256 == 0, I % 64 == 0 (nvfp4_quantize_experts
+ *     alone needs only H % 64 == 0), 0 <= T, R < 2^30.
+ *
+ * Data formats [page, §NVFP4]
+ *   - FP4 E2M1 codes, two per byte: element 2i in the low nibble of byte i,
+ *     element 2i+1 in the high nibble.
+ *   - One FP8 E4M3 (OCP E4M3FN) block scale per 16 consecutive elements of a
+ *     row.  Two scale layouts exist:
+ *       NVFP4_SF_LINEAR    [rows, K/16] row-major bytes;
+ *       NVFP4_SF_SWIZZLED  the tensor-core layout: the matrix is cut into
+ *                          tiles of 128 rows x 64 elements (4 scales per row),
+ *                          each stored as 512 contiguous bytes, tiles ordered
+ *                          row-tile-major; inside a tile the scale of row r,
+ *                          block j sits at byte (r%32)*16 + (r/32)*4 + j.
+ *                          Rows are padded to a multiple of 128 and the
+ *                          64-element columns to a whole number of tiles; the
+ *                          padding holds zero bytes.
+ *   - Per-expert FP32 scales are stored in the dequantisation direction, as a
+ *     calibration writes them: input_scale (activations) and weight_scale_2
+ *     (weights).  The quantiser's global scale is their FP32 reciprocal.
+ */
+#ifndef NVFP4_MOE_H
+#define NVFP4_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *nvfp4_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,         /* null pointer, bad shape, id outside [0, E) */
+    NVFP4_ERR_SCALE_INVALID = 2,       /* an input / weight scale slot failed validation */
+    NVFP4_ERR_UNSUPPORTED_SHAPE = 3,   /* shape outside the supported set above */
+    NVFP4_ERR_CUDA = 4,                /* a CUDA runtime / driver call failed */
+    NVFP4_ERR_DEVICE_TIMEOUT = 5,      /* a bounded device-side wait expired */
+    NVFP4_ERR_WORKSPACE_TOO_SMALL = 6, /* ws_bytes below the size query's answer */
+} nvfp4_status;
+
+enum { NVFP4_SF_LINEAR = 0, NVFP4_SF_SWIZZLED = 1 };
+
+/* Flags of nvfp4_moe_forward / nvfp4_moe_forward_host. */
+enum {
+    /* Skip the synchronous host check of the scales.  The device still
+     * validates them, and on a bad slot every later kernel of the call exits
+     * without writing; nvfp4_moe_status() then reports NVFP4_ERR_SCALE_INVALID. */
+    NVFP4_SCALES_PREVALIDATED = 1u,
+    /* Synchronise at the end of the call and report device-side errors
+     * (a bad scale slot or an expired wait) in the return value. */
+    NVFP4_SYNC_CHECK = 2u,
+};
+
+/* One-line description of the last error raised on the calling thread. */
+const char *nvfp4_last_error_string(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int nvfp4_version(void);
+
+/*
+ * nvfp4_validate_scales -- the completeness check [page, ROOT CAUSE].
+ *
+ * A slot i of scales[n] (device, FP32, dequantisation direction) is bad if
+ * written (device, one byte per slot, nullable) holds 0 at i, or the value is
+ * NaN, +-inf, <= 0 or subnormal, or its FP32 reciprocal is not a finite normal
+ * number.  ws: 256 bytes of device memory (256-byte aligned) for the
+ * device-side result.  SYNCHRONOUS: waits for `stream`.  Results go to host
+ * memory: *bad_count_host = number of bad slots, *first_bad_host = lowest bad
+ * index or -1.  Returns NVFP4_OK when the check ran (whatever it found),
+ * NVFP4_ERR_INVALID_ARG for n < 0, a null ws or null result pointers.
+ */
+int nvfp4_validate_scales(const float *scales, const uint8_t *written, int n, void *ws, nvfp4_stream_t stream,
+                          int *bad_count_host, int *first_bad_host);
+
+/*
+ * nvfp4_quantize_experts -- dynamic activation quantisation of the routed
+ * rows [page, §NVFP4 runtime-order figure; MoE section: SFScale[expert_idx]].
+ *
+ * x [T, H] BF16; topk_ids [T, k] int32 in [0, E); input_scale [E] FP32.
+ * Routed row f = t*k + j goes to permuted row p (expert-major, ascending f
+ * inside an expert) and is quantised with g = fl(1 / input_scale[e]):
+ * per 16-block, s = e4m3(fl(fl(g*amax)/6)), q = e2m1(fl(fl(x*g)/s)), with
+ * round-to-nearest-even and saturation; an all-zero-scale block gets code 0.
+ * Outputs: q_out [R, H/2] packed codes; sf_out scales in `sf_layout`
+ * (LINEAR: [R, H/16]; SWIZZLED: ceil(R/128) * ceil(H/64) * 512 bytes);
+ * expert_offsets [E+1] (first permuted row of each expert, [E] = R);
+ * perm [R] (permuted row -> f).
+ * SYNCHRONOUS: input_scale is validated first and the call waits for the
+ * check; a bad slot returns NVFP4_ERR_SCALE_INVALID with no output written.
+ * The call also waits for the quantiser and returns NVFP4_ERR_INVALID_ARG,
+ * with no output written, if an expert id is outside [0, E).  Pointer
+ * alignment: x 16 B, q_out 8 B, sf_out 4 B.  Workspace:
+ * nvfp4_quantize_workspace_size(T, k, E) bytes of device memory, 256-byte
+ * aligned.
+ */
+size_t nvfp4_quantize_workspace_size(int T, int k, int E);
+int nvfp4_quantize_experts(const uint16_t *x, int T, int H, const int32_t *topk_ids, int k, int E,
+                           const float *input_scale, uint8_t *q_out, uint8_t *sf_out, int sf_layout,
+                           int32_t *expert_offsets, int32_t *perm, void *ws, size_t ws_bytes,
+                           nvfp4_stream_t stream);
+
+/*
+ * Expert weights of one MoE layer, canonical (checkpoint) layout
+ * [page, glossary "Static weight quantization": packed FP4 weight, E4M3
+ * weight_scale, FP32 weight_scale_2; §矩阵融合 "Gated FFN": gate and up fused
+ * along the output dimension into w13].  All device pointers, [out, in] rows:
+ *   w13_q [E, 2I, H/2]   rows 0..I-1 = gate, rows I..2I-1 = up
+ *   w13_sf [E, 2I, H/16] linear E4M3 scales
+ *   w13_scale2 [E]       weight_scale_2 (FP32)
+ *   w13_input_scale [E]  stored activation scale of the w13 input
+ *   w2_q [E, H, I/2], w2_sf [E, H, I/16], w2_scale2 [E], w2_input_scale [E]
+ *   w13_input_written, w2_input_written: nullable [E] bytes, 0 = slot never
+ *     written by the loader (checked with the values themselves).
+ */
+typedef struct {
+    int E, H, I;
+    const uint8_t *w13_q;
+    const uint8_t *w13_sf;
+    const float *w13_scale2;
+    const float *w13_input_scale;
+    const uint8_t *w13_input_written;
+    const uint8_t *w2_q;
+    const uint8_t *w2_sf;
+    const float *w2_scale2;
+    const float *w2_input_scale;
+    const uint8_t *w2_input_written;
+} nvfp4_moe_weights;
+
+/*
+ * nvfp4_prepare_weights -- one-time layout conversion of the weight scales
+ * [page, "Kernel Backend": after choosing a backend the packed weights and
+ * scales are converted to the layout that kernel wants].  Writes the w13 and
+ * w2 block scales into `prepared` (device, nvfp4_prepared_weights_size bytes,
+ * 256-byte aligned) in the swizzled tensor-core layout, w13 rows reordered so
+ * that each 128-row tile holds 64 gate rows and the 64 matching up rows.
+ * The packed codes are used in place from nvfp4_moe_weights.  Asynchronous.
+ */
+size_t nvfp4_prepared_weights_size(int E, int H, int I);
+int nvfp4_prepare_weights(const nvfp4_moe_weights *w, void *prepared, size_t prepared_bytes,
+                          nvfp4_stream_t stream);
+
+/*
+ * nvfp4_moe_forward -- the expert path of one MoE layer.
+ *
+ * x [T, H] BF16, topk_ids [T, k] int32, topk_weights [T, k] FP32 (device).
+ * out [T, H] FP32 (device):
+ *   out[t] = sum_j topk_weights[t, j] * W2_e(q2(silu(gate_e) * up_e))
+ * with gate_e, up_e = W13_e(q1(x[t])), e = topk_ids[t, j], q1/q2 the NVFP4
+ * activation quantisation with a1_gscale = 1/w13_input_scale[e] and
+ * a2_gscale = 1/w2_input_scale[e], and every GEMM a block-scaled FP4 x FP4
+ * product accumulated in FP32 and scaled by 1/(a_gscale * w_gscale).
+ * Before any reciprocal is taken the 4E scale slots (w13/w2 input scales and
+ * weight_scale_2) are validated; unless NVFP4_SCALES_PREVALIDATED is set the
+ * call SYNCHRONISES on that check and returns NVFP4_ERR_SCALE_INVALID with
+ * nothing launched after it and `out` untouched.
+ * `prepared` is the output of nvfp4_prepare_weights for the same weights.
+ * An expert id outside [0, E) stops the call on the device before anything
+ * is written to `out` (reported by nvfp4_moe_status / NVFP4_SYNC_CHECK as
+ * NVFP4_ERR_INVALID_ARG).  Alignment: x and out 16 B, ws and prepared 256 B,
+ * weight codes 16 B.  Workspace: nvfp4_moe_workspace_size(T, H, I, E, k)
+ * bytes of device memory, 256-byte aligned; its contents after the call are
+ * internal.  T == 0 is valid (nothing is written).
+ */
+size_t nvfp4_moe_workspace_size(int T, int H, int I, int E, int k);
+int nvfp4_moe_forward(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x, int T,
+                      const int32_t *topk_ids, const float *topk_weights, int k, float *out, void *ws,
+                      size_t ws_bytes, unsigned flags, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_moe_forward_host -- the same layer with HOST activations and routing:
+ * copies x_host [T, H] BF16, topk_ids_host [T, k], topk_weights_host [T, k]
+ * into the workspace, runs nvfp4_moe_forward and copies out [T, H] FP32 back
+ * to out_host.  Host buffers should be page-locked for the copies to be
+ * asynchronous.  SYNCHRONOUS: returns after out_host is written.
+ * Workspace: nvfp4_moe_host_workspace_size(T, H, I, E, k) bytes.
+ */
+size_t nvfp4_moe_host_workspace_size(int T, int H, int I, int E, int k);
+int nvfp4_moe_forward_host(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x_host,
+                           int T, const int32_t *topk_ids_host, const float *topk_weights_host, int k,
+                           float *out_host, void *ws, size_t ws_bytes, unsigned flags,
+                           nvfp4_stream_t stream);
+
+/*
+ * nvfp4_moe_status -- SYNCHRONOUS: waits for `stream`, then reports the
+ * device-side status of the last nvfp4_moe_forward that used `ws`:
+ * NVFP4_OK, NVFP4_ERR_SCALE_INVALID (bad slot found on the device; then
+ * *first_bad_host is its index in the order w13_input_scale[E],
+ * w2_input_scale[E], w13_scale2[E], w2_scale2[E]), NVFP4_ERR_INVALID_ARG
+ * (an expert id outside [0, E)) or NVFP4_ERR_DEVICE_TIMEOUT.
+ * first_bad_host is nullable.
+ */
+int nvfp4_moe_status(const void *ws, nvfp4_stream_t stream, int *first_bad_host);
+
+/*
+ * Intermediates of the last nvfp4_moe_forward on `ws`, for inspection
+ * (device pointers into ws; valid until the next call on ws):
+ *   a1q [rows_cap, H/2], sf1 (swizzled, ceil(H/64) tiles per 128 rows),
+ *   a2q [rows_cap, I/2], sf2 (swizzled, 4*ceil(I/256) tiles per 128 rows),
+ *   row_of [R] (routed row f -> padded permuted row), offsets [E+1] (compact),
+ *   pad_offsets [E+1] (padded: every expert starts on a 128-row boundary),
+ *   h [rows_cap, I] FP32, the SiLU(gate)*up intermediate (written only when
+ *   a forward ran with NVFP4_DEBUG_KEEP_H, which needs
+ *   nvfp4_moe_host_workspace_size(...) + rows_cap*I*4 bytes of workspace).
+ * Returns NVFP4_ERR_INVALID_ARG if ws is null.
+ */
+enum { NVFP4_DEBUG_KEEP_H = 4u };
+typedef struct {
+    int rows_cap;
+    uint8_t *a1q, *sf1, *a2q, *sf2;
+    int32_t *row_of, *offsets, *pad_offsets;
+    float *h;
+} nvfp4_moe_intermediates;
+int nvfp4_moe_intermediates_of(void *ws, int T, int H, int I, int E, int k,
+                               nvfp4_moe_intermediates *out_host);
+
+/*
+ * nvfp4_residual_rmsnorm -- between stacked layers (not on the page):
+ * x_next = bf16(r / sqrt(mean(r^2) + eps)), r = x + out, gamma = 1, per token.
+ * x [T, H] BF16, out [T, H] FP32, x_next [T, H] BF16 (may alias x).
+ */
+int nvfp4_residual_rmsnorm(const uint16_t *x, const float *out, int T, int H, float eps,
+                           uint16_t *x_next, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_quantize_weights -- static weight quantisation on the device
+ * [page, glossary "Static weight quantization"]: for each of `count` tensors
+ * w [count, N, K] BF16 (K % 16 == 0), weight_scale_2[c] = fl(amax_c / 2688)
+ * (2688 = 6 * 448, [page, §NVFP4 two-level scale]), then every row is block
+ * quantised with g = fl(1 / weight_scale_2[c]) exactly as activations are.
+ * Outputs q [count, N, K/2], sf [count, N, K/16] (linear), scale2 [count].
+ * Workspace: nvfp4_quantize_weights_workspace_size(count) bytes.
+ */
+size_t nvfp4_quantize_weights_workspace_size(int count);
+int nvfp4_quantize_weights(const uint16_t *w, int count, int N, int K, uint8_t *q, uint8_t *sf,
+                           float *scale2, void *ws, size_t ws_bytes, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_selftest_block_division -- host-side exhaustive check of the exact
+ * block-scale division used by the quantisers: for every finite non-zero
+ * E4M3 scale s and every FP32 significand y in [1, 2), the two-constant
+ * product fma(y, zh(s), y*zl(s)) must equal the correctly rounded y / s
+ * (N. Brisebarre, J.-M. Muller, S. K. Raina, "Accelerating correctly rounded
+ * floating-point division when the divisor is known in advance", IEEE Trans.
+ * Computers 53(8), 2004).  Returns the number of mismatches (0 = exact);
+ * nthreads <= 0 uses every host core.  Runs on the CPU only.
+ */
+long long nvfp4_selftest_block_division(int nthreads);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_MOE_H */

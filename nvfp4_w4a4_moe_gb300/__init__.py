@@ -1,0 +1,297 @@
+"""Python binding of libnvfp4moe (the NVFP4 W4A4 MoE expert forward for GB300).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  PyTorch supplies device memory and streams.  The functions carry the
+names of the C entry points in include/nvfp4_moe.h without the ``nvfp4_``
+prefix.  There is no fallback: if the library is missing, or a call fails, a
+``Nvfp4Error`` is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnvfp4moe.so")
+
+OK, ERR_INVALID_ARG, ERR_SCALE_INVALID, ERR_UNSUPPORTED_SHAPE, ERR_CUDA, ERR_DEVICE_TIMEOUT, \
+    ERR_WORKSPACE_TOO_SMALL = range(7)
+SF_LINEAR, SF_SWIZZLED = 0, 1
+SCALES_PREVALIDATED, SYNC_CHECK, DEBUG_KEEP_H = 1, 2, 4
+
+_lib = None
+_lock = threading.Lock()
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"nvfp4 status {status}: {msg}")
+        self.status = status
+
+
+class _Weights(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
+                ("w13_q", ctypes.c_void_p), ("w13_sf", ctypes.c_void_p), ("w13_scale2", ctypes.c_void_p),
+                ("w13_input_scale", ctypes.c_void_p), ("w13_input_written", ctypes.c_void_p),
+                ("w2_q", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p), ("w2_scale2", ctypes.c_void_p),
+                ("w2_input_scale", ctypes.c_void_p), ("w2_input_written", ctypes.c_void_p)]
+
+
+class _Intermediates(ctypes.Structure):
+    _fields_ = [("rows_cap", ctypes.c_int), ("a1q", ctypes.c_void_p), ("sf1", ctypes.c_void_p),
+                ("a2q", ctypes.c_void_p), ("sf2", ctypes.c_void_p), ("row_of", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("pad_offsets", ctypes.c_void_p), ("h", ctypes.c_void_p)]
+
+
+def build(force: bool = False) -> str:
+    """Compile the library in-tree (nvcc, sm_103a)."""
+    from . import builder
+    return builder.build(force=force)
+
+
+def load():
+    """Load libnvfp4moe.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise Nvfp4Error(ERR_CUDA, f"{LIB_PATH} is missing: build it with nvfp4_w4a4_moe_gb300.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, SZ, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint
+        sig = {
+            "nvfp4_last_error_string": (ctypes.c_char_p, []),
+            "nvfp4_version": (I, []),
+            "nvfp4_validate_scales": (I, [P, P, I, P, P, P, P]),
+            "nvfp4_quantize_workspace_size": (SZ, [I, I, I]),
+            "nvfp4_quantize_experts": (I, [P, I, I, P, I, I, P, P, P, I, P, P, P, SZ, P]),
+            "nvfp4_prepared_weights_size": (SZ, [I, I, I]),
+            "nvfp4_prepare_weights": (I, [P, P, SZ, P]),
+            "nvfp4_moe_workspace_size": (SZ, [I, I, I, I, I]),
+            "nvfp4_moe_forward": (I, [P, P, P, I, P, P, I, P, P, SZ, U, P]),
+            "nvfp4_moe_host_workspace_size": (SZ, [I, I, I, I, I]),
+            "nvfp4_moe_forward_host": (I, [P, P, P, I, P, P, I, P, P, SZ, U, P]),
+            "nvfp4_moe_status": (I, [P, P, P]),
+            "nvfp4_moe_intermediates_of": (I, [P, I, I, I, I, I, P]),
+            "nvfp4_residual_rmsnorm": (I, [P, P, I, I, ctypes.c_float, P, P]),
+            "nvfp4_quantize_weights_workspace_size": (SZ, [I]),
+            "nvfp4_quantize_weights": (I, [P, I, I, I, P, P, P, P, SZ, P]),
+            "nvfp4_selftest_block_division": (ctypes.c_longlong, [I]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != OK:
+        raise Nvfp4Error(rc, load().nvfp4_last_error_string().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _empty_ws(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def version() -> int:
+    return int(load().nvfp4_version())
+
+
+def selftest_block_division(nthreads: int = 0) -> int:
+    return int(load().nvfp4_selftest_block_division(nthreads))
+
+
+# ---------------------------------------------------------------------------
+def validate_scales(scales: torch.Tensor, written: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                    stream=None):
+    """Returns (bad_count, first_bad or -1).  Synchronous."""
+    ws = _empty_ws(256, scales.device) if ws is None else ws
+    bad, first = ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().nvfp4_validate_scales(_ptr(scales), _ptr(written), scales.numel(), _ptr(ws), _stream(stream),
+                                        ctypes.byref(bad), ctypes.byref(first)))
+    return bad.value, first.value
+
+
+def quantize_workspace_size(T: int, k: int, E: int) -> int:
+    return int(load().nvfp4_quantize_workspace_size(T, k, E))
+
+
+def quantize_experts(x: torch.Tensor, topk_ids: torch.Tensor, input_scale: torch.Tensor, E: int,
+                     sf_layout: int = SF_LINEAR, ws: torch.Tensor | None = None, stream=None):
+    """x [T, H] bf16, topk_ids [T, k] int32, input_scale [E] f32 (device).
+    Returns (q [R, H/2] u8, sf u8, expert_offsets [E+1] i32, perm [R] i32)."""
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    R = T * k
+    dev = x.device
+    q = torch.empty((R, H // 2), dtype=torch.uint8, device=dev)
+    if sf_layout == SF_SWIZZLED:
+        sf = torch.empty(((R + 127) // 128) * ((H + 63) // 64) * 512, dtype=torch.uint8, device=dev)
+    else:
+        sf = torch.empty((R, H // 16), dtype=torch.uint8, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(max(R, 1), dtype=torch.int32, device=dev)
+    need = quantize_workspace_size(T, k, E)
+    ws = _empty_ws(need, dev) if ws is None else ws
+    _check(load().nvfp4_quantize_experts(_ptr(x), T, H, _ptr(topk_ids), k, E, _ptr(input_scale), _ptr(q), _ptr(sf),
+                                         sf_layout, _ptr(offsets), _ptr(perm), _ptr(ws), ws.numel(),
+                                         _stream(stream)))
+    return q, sf, offsets, perm[:R]
+
+
+class MoEWeights:
+    """Device tensors of one layer's NVFP4 expert weights (canonical layout,
+    see nvfp4_moe_weights in the C header) plus their prepared scale layout."""
+
+    def __init__(self, E, H, I, w13_q, w13_sf, w13_scale2, w13_input_scale, w2_q, w2_sf, w2_scale2,
+                 w2_input_scale, w13_input_written=None, w2_input_written=None):
+        self.E, self.H, self.I = E, H, I
+        self.w13_q, self.w13_sf, self.w13_scale2, self.w13_input_scale = w13_q, w13_sf, w13_scale2, w13_input_scale
+        self.w2_q, self.w2_sf, self.w2_scale2, self.w2_input_scale = w2_q, w2_sf, w2_scale2, w2_input_scale
+        self.w13_input_written, self.w2_input_written = w13_input_written, w2_input_written
+        self.prepared = None
+
+    def cstruct(self) -> _Weights:
+        return _Weights(self.E, self.H, self.I, _ptr(self.w13_q), _ptr(self.w13_sf), _ptr(self.w13_scale2),
+                        _ptr(self.w13_input_scale), _ptr(self.w13_input_written), _ptr(self.w2_q), _ptr(self.w2_sf),
+                        _ptr(self.w2_scale2), _ptr(self.w2_input_scale), _ptr(self.w2_input_written))
+
+
+def prepared_weights_size(E: int, H: int, I: int) -> int:
+    return int(load().nvfp4_prepared_weights_size(E, H, I))
+
+
+def prepare_weights(w: MoEWeights, stream=None) -> torch.Tensor:
+    n = prepared_weights_size(w.E, w.H, w.I)
+    prep = torch.empty(n, dtype=torch.uint8, device=w.w13_q.device)
+    cw = w.cstruct()
+    _check(load().nvfp4_prepare_weights(ctypes.byref(cw), _ptr(prep), n, _stream(stream)))
+    w.prepared = prep
+    return prep
+
+
+def moe_workspace_size(T: int, H: int, I: int, E: int, k: int) -> int:
+    return int(load().nvfp4_moe_workspace_size(T, H, I, E, k))
+
+
+def moe_host_workspace_size(T: int, H: int, I: int, E: int, k: int) -> int:
+    return int(load().nvfp4_moe_host_workspace_size(T, H, I, E, k))
+
+
+def moe_forward(w: MoEWeights, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                out: torch.Tensor | None = None, ws: torch.Tensor | None = None, flags: int = 0, stream=None):
+    """out [T, H] f32 = the expert path of one layer (device tensors)."""
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    if w.prepared is None:
+        prepare_weights(w, stream)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    if ws is None:
+        n = moe_workspace_size(T, H, w.I, w.E, k)
+        if flags & DEBUG_KEEP_H:
+            n = moe_host_workspace_size(T, H, w.I, w.E, k) + intermediates_rows_cap(T, w.E, k) * w.I * 4
+        ws = _empty_ws(n, x.device)
+    cw = w.cstruct()
+    _check(load().nvfp4_moe_forward(ctypes.byref(cw), _ptr(w.prepared), _ptr(x), T, _ptr(topk_ids),
+                                    _ptr(topk_weights), k, _ptr(out), _ptr(ws), ws.numel(), flags, _stream(stream)))
+    return out, ws
+
+
+def moe_forward_host(w: MoEWeights, x_host: torch.Tensor, topk_ids_host: torch.Tensor,
+                     topk_weights_host: torch.Tensor, out_host: torch.Tensor | None = None,
+                     ws: torch.Tensor | None = None, flags: int = 0, stream=None):
+    """Same layer from host (ideally pinned) tensors; returns out_host [T, H] f32."""
+    T, H = x_host.shape
+    k = topk_ids_host.shape[1]
+    if w.prepared is None:
+        prepare_weights(w, stream)
+    if out_host is None:
+        out_host = torch.empty((T, H), dtype=torch.float32, pin_memory=True)
+    if ws is None:
+        ws = _empty_ws(moe_host_workspace_size(T, H, w.I, w.E, k), w.w13_q.device)
+    cw = w.cstruct()
+    _check(load().nvfp4_moe_forward_host(ctypes.byref(cw), _ptr(w.prepared), _ptr(x_host), T, _ptr(topk_ids_host),
+                                         _ptr(topk_weights_host), k, _ptr(out_host), _ptr(ws), ws.numel(), flags,
+                                         _stream(stream)))
+    return out_host, ws
+
+
+def moe_status(ws: torch.Tensor, stream=None):
+    """(status, first_bad) of the last forward on ws.  Synchronous; does not raise."""
+    first = ctypes.c_int(-1)
+    rc = load().nvfp4_moe_status(_ptr(ws), _stream(stream), ctypes.byref(first))
+    return int(rc), first.value
+
+
+def intermediates_rows_cap(T: int, E: int, k: int) -> int:
+    R = T * k
+    if R == 0:
+        return 0
+    return ((R + min(R, E) * 127) + 127) // 128 * 128
+
+
+def intermediates_of(ws: torch.Tensor, T: int, H: int, I: int, E: int, k: int) -> dict:
+    """Views (device tensors) of the workspace intermediates of the last forward."""
+    o = _Intermediates()
+    _check(load().nvfp4_moe_intermediates_of(_ptr(ws), T, H, I, E, k, ctypes.byref(o)))
+    base = ws.data_ptr()
+    rc = o.rows_cap
+    mt = rc // 128
+
+    def view(addr, n, dtype, shape):
+        off = addr - base
+        esz = torch.tensor([], dtype=dtype).element_size()
+        return ws[off:off + n * esz].view(dtype).view(shape)
+
+    kc1, kc2 = 4 * ((H + 255) // 256), 4 * ((I + 255) // 256)
+    R = T * k
+    d = dict(rows_cap=rc,
+             a1q=view(o.a1q, rc * H // 2, torch.uint8, (rc, H // 2)),
+             sf1=view(o.sf1, mt * kc1 * 512, torch.uint8, (mt * kc1 * 512,)),
+             a2q=view(o.a2q, rc * I // 2, torch.uint8, (rc, I // 2)),
+             sf2=view(o.sf2, mt * kc2 * 512, torch.uint8, (mt * kc2 * 512,)),
+             row_of=view(o.row_of, R, torch.int32, (R,)),
+             offsets=view(o.offsets, E + 1, torch.int32, (E + 1,)),
+             pad_offsets=view(o.pad_offsets, E + 1, torch.int32, (E + 1,)),
+             kc1=kc1, kc2=kc2)
+    if (o.h - base) + rc * I * 4 <= ws.numel():
+        d["h"] = view(o.h, rc * I, torch.float32, (rc, I))
+    return d
+
+
+def residual_rmsnorm(x: torch.Tensor, out: torch.Tensor, eps: float = 1e-6, x_next: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    T, H = x.shape
+    if x_next is None:
+        x_next = torch.empty_like(x)
+    _check(load().nvfp4_residual_rmsnorm(_ptr(x), _ptr(out), T, H, float(eps), _ptr(x_next), _stream(stream)))
+    return x_next
+
+
+def quantize_weights(w: torch.Tensor, stream=None):
+    """w [count, N, K] bf16 (device) -> (q [count, N, K/2] u8, sf [count, N, K/16] u8, scale2 [count] f32)."""
+    count, N, K = w.shape
+    dev = w.device
+    q = torch.empty((count, N, K // 2), dtype=torch.uint8, device=dev)
+    sf = torch.empty((count, N, K // 16), dtype=torch.uint8, device=dev)
+    s2 = torch.empty(count, dtype=torch.float32, device=dev)
+    n = int(load().nvfp4_quantize_weights_workspace_size(count))
+    ws = _empty_ws(n, dev)
+    _check(load().nvfp4_quantize_weights(_ptr(w), count, N, K, _ptr(q), _ptr(sf), _ptr(s2), _ptr(ws), ws.numel(),
+                                         _stream(stream)))
+    return q, sf, s2

@@ -1,0 +1,634 @@
+// C ABI of libnvfp4moe: argument checks, workspace layout and the launch
+// sequence of the NVFP4 MoE expert path.  Declared in include/nvfp4_moe.h.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <thread>
+#include <vector>
+
+#include "../../include/nvfp4_moe.h"
+#include "internal.h"
+
+namespace nvfp4 {
+
+// ------------------------------------------------------------------ errors
+static thread_local char g_err[512] = "no error";
+
+void set_error(const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+}
+
+static int fail(int status, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+static int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(NVFP4_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define NV_CUDA(call, what)                                  \
+    do {                                                     \
+        cudaError_t _e = (call);                             \
+        if (_e != cudaSuccess) return cuda_fail(_e, (what)); \
+    } while (0)
+
+// ------------------------------------------------------------------ device facts
+int sm_count()
+{
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// ------------------------------------------------------------------ block-scale division table
+static double e4m3_value(int b)
+{
+    const int e = (b >> 3) & 15, m = b & 7;
+    return e == 0 ? std::ldexp((double)m, -9) : std::ldexp(8.0 + m, e - 10);
+}
+
+// zh = RN(1/s), zl = RN(1/s - zh) for each finite non-zero E4M3 scale s
+// (Brisebarre-Muller-Raina two-constant division; see common.cuh).
+static DivTable build_div_table()
+{
+    DivTable t;
+    std::memset(&t, 0, sizeof(t));
+    for (int b = 1; b <= 0x7E; ++b) {
+        const double s = e4m3_value(b);
+        const float zh = (float)(1.0 / s);
+        const double rem = std::fma(-s, (double)zh, 1.0);  // exact: 1 - s*zh
+        const float zl = (float)(rem / s);
+        t.z[b] = make_float2(zh, zl);
+    }
+    return t;
+}
+
+const DivTable &div_table()
+{
+    static const DivTable t = build_div_table();
+    return t;
+}
+
+// ------------------------------------------------------------------ workspace layout
+static size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+WsLayout make_layout(int T, int H, int I, int E, int k)
+{
+    WsLayout L;
+    std::memset(&L, 0, sizeof(L));
+    L.T = T, L.H = H, L.I = I, L.E = E, L.k = k;
+    L.R = T * k;
+    const long long R = L.R;
+    const long long busy = R < E ? R : E;
+    L.rows_cap = R == 0 ? 0 : (int)(((R + busy * 127) + 127) / 128 * 128);
+    L.mtiles_cap = L.rows_cap / 128;
+    L.nchunks = (int)((R + kRouteChunk - 1) / kRouteChunk);
+    if (L.nchunks < 1) L.nchunks = 1;
+    L.kc1 = 4 * ((H + 255) / 256);
+    L.kc2 = 4 * ((I + 255) / 256);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = up256(o + bytes);
+        return at;
+    };
+    L.hdr = take(sizeof(DevHeader));
+    L.g1 = take(sizeof(float) * 4 * (size_t)E);  // g1, g2, gw13, gw2
+    L.g2 = L.g1 + sizeof(float) * (size_t)E;
+    L.alpha1 = take(sizeof(float) * 2 * (size_t)E);
+    L.alpha2 = L.alpha1 + sizeof(float) * (size_t)E;
+    L.counts = take(sizeof(int) * (size_t)E);
+    L.offsets = take(sizeof(int) * (size_t)(E + 1));
+    L.pad_off = take(sizeof(int) * (size_t)(E + 1));
+    L.chunk_hist = take(sizeof(int) * (size_t)L.nchunks * E);
+    L.row_of = take(sizeof(int) * (size_t)R);
+    L.perm = take(sizeof(int) * (size_t)R);
+    L.row_src = take(sizeof(int) * (size_t)L.rows_cap);
+    L.tile_expert = take(sizeof(int) * (size_t)L.mtiles_cap);
+    L.a1q = take((size_t)L.rows_cap * (H / 2));
+    L.sf1 = take((size_t)L.mtiles_cap * L.kc1 * 512);
+    L.a2q = take((size_t)L.rows_cap * (I / 2));
+    L.sf2 = take((size_t)L.mtiles_cap * L.kc2 * 512);
+    L.end = o;
+    L.x_stage = take(sizeof(uint16_t) * (size_t)T * H);
+    L.ids_stage = take(sizeof(int32_t) * (size_t)R);
+    L.w_stage = take(sizeof(float) * (size_t)R);
+    L.out_stage = take(sizeof(float) * (size_t)T * H);
+    L.host_end = o;
+    return L;
+}
+
+static size_t prepared_w13_bytes(int E, int H, int I)
+{
+    return (size_t)E * (2 * I / 128) * (4 * ((H + 255) / 256)) * 512;
+}
+static size_t prepared_w2_bytes(int E, int H, int I)
+{
+    return (size_t)E * (H / 128) * (4 * ((I + 255) / 256)) * 512;
+}
+
+static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static int check_layer_shape(int E, int H, int I, int k)
+{
+    if (E < 1 || E > 1024) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "E=%d outside [1, 1024]", E);
+    if (k < 1 || k > 32 || k > E) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "k=%d outside [1, min(32, E)]", k);
+    if (H <= 0 || H % 256 != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "H=%d is not a positive multiple of 256", H);
+    if (I <= 0 || I % 64 != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "I=%d is not a positive multiple of 64", I);
+    return NVFP4_OK;
+}
+
+static int read_header(const void *ws, cudaStream_t st, DevHeader *h)
+{
+    NV_CUDA(cudaMemcpyAsync(h, ws, sizeof(DevHeader), cudaMemcpyDeviceToHost, st), "reading the status block");
+    NV_CUDA(cudaStreamSynchronize(st), "synchronising the stream");
+    return NVFP4_OK;
+}
+
+static int header_status(const DevHeader &h, int *first_bad)
+{
+    if (first_bad) *first_bad = h.first_bad == 0x7fffffff ? -1 : h.first_bad;
+    if (h.status == 2)
+        return fail(NVFP4_ERR_SCALE_INVALID, "%d scale slot(s) failed validation; first bad slot %d", h.bad_count,
+                    h.first_bad);
+    if (h.status == 3 || (h.error_flags & kErrBadExpertId))
+        return fail(NVFP4_ERR_INVALID_ARG, "an expert id is outside [0, E)");
+    if (h.error_flags & (kErrTimeoutProducer | kErrTimeoutMma | kErrTimeoutEpilogue))
+        return fail(NVFP4_ERR_DEVICE_TIMEOUT, "a device-side wait expired (flags 0x%x)", h.error_flags);
+    return NVFP4_OK;
+}
+
+// ------------------------------------------------------------------ self-test of the division
+long long selftest_division(int nthreads)
+{
+    const DivTable &t = div_table();
+    if (nthreads <= 0) nthreads = (int)std::thread::hardware_concurrency();
+    if (nthreads <= 0) nthreads = 1;
+    std::atomic<long long> bad{0};
+    std::atomic<int> next{1};
+    auto work = [&]() {
+        for (;;) {
+            const int b = next.fetch_add(1);
+            if (b > 0x7E) return;
+            const double s = e4m3_value(b);
+            // s = D * 2^es with D odd
+            int es = 0;
+            double D = s;
+            while (D != std::floor(D)) D *= 2, --es;
+            while (std::fmod(D, 2.0) == 0.0) D /= 2, ++es;
+            const uint64_t d = (uint64_t)D;
+            const float zh = t.z[b].x, zl = t.z[b].y;
+            long long local = 0;
+            for (uint32_t Y = 1u << 23; Y < (1u << 24); ++Y) {
+                const float y = std::ldexp((float)Y, -23);
+                volatile float prod = y * zl;  // one rounding, no contraction
+                const float q = std::fmaf(y, zh, prod);
+                int sh = 0;
+                while ((((uint64_t)Y << sh) / d) < (1u << 23)) ++sh;
+                const uint64_t N = (uint64_t)Y << sh;
+                uint64_t Q = N / d;
+                const uint64_t R = N % d;
+                if (2 * R > d || (2 * R == d && (Q & 1))) ++Q;
+                const double want = std::ldexp((double)Q, -sh - 23 - es);
+                if ((double)q != want) ++local;
+            }
+            bad += local;
+        }
+    };
+    std::vector<std::thread> pool;
+    for (int i = 0; i < nthreads; ++i) pool.emplace_back(work);
+    for (auto &th : pool) th.join();
+    return bad.load();
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+// ====================================================================== C ABI
+extern "C" {
+
+const char *nvfp4_last_error_string(void) { return g_err; }
+
+int nvfp4_version(void) { return 100; }
+
+long long nvfp4_selftest_block_division(int nthreads) { return selftest_division(nthreads); }
+
+int nvfp4_validate_scales(const float *scales, const uint8_t *written, int n, void *ws, nvfp4_stream_t stream,
+                          int *bad_count_host, int *first_bad_host)
+{
+    if (n < 0 || !bad_count_host || !first_bad_host || !ws || (n > 0 && !scales))
+        return fail(NVFP4_ERR_INVALID_ARG, "nvfp4_validate_scales: bad arguments");
+    if (!aligned(ws, 256)) return fail(NVFP4_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    DevHeader *hdr = reinterpret_cast<DevHeader *>(ws);
+    ValidateArgs va;
+    std::memset(&va, 0, sizeof(va));
+    va.s[0] = scales;
+    va.written[0] = written;
+    va.E = n;
+    va.narrays = 1;
+    va.hdr = hdr;
+    NV_CUDA(launch_validate(va, st), "launching the scale check");
+    DevHeader h;
+    int rc = read_header(ws, st, &h);
+    if (rc) return rc;
+    *bad_count_host = h.bad_count;
+    *first_bad_host = h.bad_count ? h.first_bad : -1;
+    return NVFP4_OK;
+}
+
+size_t nvfp4_quantize_workspace_size(int T, int k, int E)
+{
+    if (T < 0 || k < 1 || E < 1) return 0;
+    return make_layout(T, 256, 64, E, k).row_src;  // header .. perm
+}
+
+int nvfp4_quantize_experts(const uint16_t *x, int T, int H, const int32_t *topk_ids, int k, int E,
+                           const float *input_scale, uint8_t *q_out, uint8_t *sf_out, int sf_layout,
+                           int32_t *expert_offsets, int32_t *perm, void *ws, size_t ws_bytes,
+                           nvfp4_stream_t stream)
+{
+    if (E < 1 || E > 1024 || k < 1 || k > 32 || k > E || T < 0)
+        return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "quantize: E=%d k=%d T=%d unsupported", E, k, T);
+    if (H <= 0 || H % 64 != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "quantize: H=%d is not a multiple of 64", H);
+    if (sf_layout != NVFP4_SF_LINEAR && sf_layout != NVFP4_SF_SWIZZLED)
+        return fail(NVFP4_ERR_INVALID_ARG, "unknown scale layout %d", sf_layout);
+    if (!input_scale || !expert_offsets || !ws || (T > 0 && (!x || !topk_ids || !q_out || !sf_out || !perm)))
+        return fail(NVFP4_ERR_INVALID_ARG, "quantize: null pointer");
+    if (!aligned(ws, 256) || (T > 0 && (!aligned(x, 16) || !aligned(q_out, 8) || !aligned(sf_out, 4))))
+        return fail(NVFP4_ERR_INVALID_ARG, "quantize: misaligned pointer (x 16 B, q 8 B, sf 4 B, ws 256 B)");
+    const size_t need = nvfp4_quantize_workspace_size(T, k, E);
+    if (ws_bytes < need) return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "quantize: workspace %zu < %zu", ws_bytes, need);
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    WsLayout L = make_layout(T, 256, 64, E, k);
+    DevHeader *hdr = reinterpret_cast<DevHeader *>(base + L.hdr);
+    float *g = reinterpret_cast<float *>(base + L.g1);
+
+    ValidateArgs va;
+    std::memset(&va, 0, sizeof(va));
+    va.s[0] = input_scale;
+    va.recip[0] = g;
+    va.E = E;
+    va.narrays = 1;
+    va.hdr = hdr;
+    NV_CUDA(launch_validate(va, st), "launching the scale check");
+    DevHeader h;
+    int rc = read_header(hdr, st, &h);
+    if (rc) return rc;
+    if (h.status) return header_status(h, nullptr);
+    if (T == 0) {
+        NV_CUDA(cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), st), "zeroing offsets");
+        NV_CUDA(cudaStreamSynchronize(st), "synchronising the stream");
+        return NVFP4_OK;
+    }
+    const int R = T * k;
+    RouteArgs ra;
+    std::memset(&ra, 0, sizeof(ra));
+    ra.ids = topk_ids;
+    ra.R = R;
+    ra.k = k;
+    ra.E = E;
+    ra.nchunks = L.nchunks;
+    ra.chunk_hist = reinterpret_cast<int *>(base + L.chunk_hist);
+    ra.counts = reinterpret_cast<int *>(base + L.counts);
+    ra.offsets = reinterpret_cast<int *>(base + L.offsets);
+    ra.pad_off = reinterpret_cast<int *>(base + L.pad_off);
+    ra.tile_expert = nullptr;
+    ra.row_of = reinterpret_cast<int *>(base + L.row_of);
+    ra.perm = perm;
+    ra.row_src = nullptr;
+    ra.offsets_out = expert_offsets;
+    ra.padded = 0;
+    ra.hdr = hdr;
+    NV_CUDA(launch_route(ra, st), "launching the token reorder");
+    const int kc = (H + 63) / 64;
+    if (sf_layout == NVFP4_SF_SWIZZLED)
+        NV_CUDA(cudaMemsetAsync(sf_out, 0, (size_t)((R + 127) / 128) * kc * 512, st), "zeroing scale padding");
+    QuantArgs qa;
+    std::memset(&qa, 0, sizeof(qa));
+    qa.x = x;
+    qa.ids = topk_ids;
+    qa.row_of = ra.row_of;
+    qa.g = g;
+    qa.T = T;
+    qa.H = H;
+    qa.k = k;
+    qa.q = q_out;
+    qa.sf = sf_out;
+    qa.sf_swizzled = sf_layout == NVFP4_SF_SWIZZLED;
+    qa.sf_kc = kc;
+    qa.hdr = hdr;
+    NV_CUDA(launch_quant_experts(qa, st), "launching the quantiser");
+    rc = read_header(hdr, st, &h);
+    if (rc) return rc;
+    return header_status(h, nullptr);
+}
+
+size_t nvfp4_prepared_weights_size(int E, int H, int I)
+{
+    if (E < 1 || H <= 0 || I <= 0) return 0;
+    return up256(prepared_w13_bytes(E, H, I)) + up256(prepared_w2_bytes(E, H, I));
+}
+
+static int check_weights(const nvfp4_moe_weights *w)
+{
+    if (!w) return fail(NVFP4_ERR_INVALID_ARG, "weights struct is null");
+    if (!w->w13_q || !w->w13_sf || !w->w13_scale2 || !w->w13_input_scale || !w->w2_q || !w->w2_sf ||
+        !w->w2_scale2 || !w->w2_input_scale)
+        return fail(NVFP4_ERR_INVALID_ARG, "a weight or scale pointer is null");
+    if (!aligned(w->w13_q, 16) || !aligned(w->w2_q, 16) || !aligned(w->w13_sf, 4) || !aligned(w->w2_sf, 4))
+        return fail(NVFP4_ERR_INVALID_ARG, "weight codes must be 16-byte aligned, scales 4-byte aligned");
+    return NVFP4_OK;
+}
+
+int nvfp4_prepare_weights(const nvfp4_moe_weights *w, void *prepared, size_t prepared_bytes, nvfp4_stream_t stream)
+{
+    int rc = check_weights(w);
+    if (rc) return rc;
+    rc = check_layer_shape(w->E, w->H, w->I, 1);
+    if (rc) return rc;
+    if (!prepared || !aligned(prepared, 256)) return fail(NVFP4_ERR_INVALID_ARG, "prepared buffer null or misaligned");
+    const size_t need = nvfp4_prepared_weights_size(w->E, w->H, w->I);
+    if (prepared_bytes < need)
+        return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "prepared buffer %zu < %zu", prepared_bytes, need);
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *base = static_cast<uint8_t *>(prepared);
+    PrepArgs a13 = {w->w13_sf, base, w->E, 2 * w->I, w->H, 4 * ((w->H + 255) / 256), w->I};
+    NV_CUDA(launch_prep_sf(a13, st), "launching the w13 scale conversion");
+    PrepArgs a2 = {w->w2_sf, base + up256(prepared_w13_bytes(w->E, w->H, w->I)), w->E, w->H, w->I,
+                   4 * ((w->I + 255) / 256), 0};
+    NV_CUDA(launch_prep_sf(a2, st), "launching the w2 scale conversion");
+    return NVFP4_OK;
+}
+
+size_t nvfp4_moe_workspace_size(int T, int H, int I, int E, int k)
+{
+    if (T < 0 || H <= 0 || I <= 0 || E < 1 || k < 1) return 0;
+    return make_layout(T, H, I, E, k).end;
+}
+
+size_t nvfp4_moe_host_workspace_size(int T, int H, int I, int E, int k)
+{
+    if (T < 0 || H <= 0 || I <= 0 || E < 1 || k < 1) return 0;
+    return make_layout(T, H, I, E, k).host_end;
+}
+
+static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x, int T,
+                        const int32_t *ids, const float *topk_w, int k, float *out, void *ws, size_t ws_bytes,
+                        unsigned flags, cudaStream_t st)
+{
+    int rc = check_weights(w);
+    if (rc) return rc;
+    rc = check_layer_shape(w->E, w->H, w->I, k);
+    if (rc) return rc;
+    const int E = w->E, H = w->H, I = w->I;
+    if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "T=%d < 0", T);
+    if ((long long)T * k >= (1ll << 31) / 2) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "T*k too large");
+    if (!prepared || !ws || (T > 0 && (!x || !ids || !topk_w || !out)))
+        return fail(NVFP4_ERR_INVALID_ARG, "forward: null pointer");
+    if (!aligned(ws, 256) || !aligned(prepared, 256) || (T > 0 && (!aligned(x, 16) || !aligned(out, 16))))
+        return fail(NVFP4_ERR_INVALID_ARG, "forward: misaligned pointer (x, out 16 B; ws, prepared 256 B)");
+    const WsLayout L = make_layout(T, H, I, E, k);
+    if (ws_bytes < L.end) return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu", ws_bytes, L.end);
+    const bool keep_h = (flags & NVFP4_DEBUG_KEEP_H) != 0;
+    if (keep_h && ws_bytes < L.host_end + (size_t)L.rows_cap * I * sizeof(float))
+        return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "NVFP4_DEBUG_KEEP_H needs the host workspace size + rows_cap*I*4");
+    if (T == 0) return NVFP4_OK;
+
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    DevHeader *hdr = reinterpret_cast<DevHeader *>(base + L.hdr);
+    float *g = reinterpret_cast<float *>(base + L.g1);  // g1 | g2 | gw13 | gw2
+    float *alpha1 = reinterpret_cast<float *>(base + L.alpha1);
+    float *alpha2 = reinterpret_cast<float *>(base + L.alpha2);
+
+    ValidateArgs va;
+    std::memset(&va, 0, sizeof(va));
+    va.s[0] = w->w13_input_scale;
+    va.s[1] = w->w2_input_scale;
+    va.s[2] = w->w13_scale2;
+    va.s[3] = w->w2_scale2;
+    va.written[0] = w->w13_input_written;
+    va.written[1] = w->w2_input_written;
+    for (int i = 0; i < 4; ++i) va.recip[i] = g + (size_t)i * E;
+    va.E = E;
+    va.narrays = 4;
+    va.alpha1 = alpha1;
+    va.alpha2 = alpha2;
+    va.hdr = hdr;
+    NV_CUDA(launch_validate(va, st), "launching the scale check");
+    if (!(flags & NVFP4_SCALES_PREVALIDATED)) {
+        DevHeader h;
+        rc = read_header(hdr, st, &h);
+        if (rc) return rc;
+        if (h.status) return header_status(h, nullptr);
+    }
+
+    const int R = T * k;
+    RouteArgs ra;
+    std::memset(&ra, 0, sizeof(ra));
+    ra.ids = ids;
+    ra.R = R;
+    ra.k = k;
+    ra.E = E;
+    ra.nchunks = L.nchunks;
+    ra.chunk_hist = reinterpret_cast<int *>(base + L.chunk_hist);
+    ra.counts = reinterpret_cast<int *>(base + L.counts);
+    ra.offsets = reinterpret_cast<int *>(base + L.offsets);
+    ra.pad_off = reinterpret_cast<int *>(base + L.pad_off);
+    ra.tile_expert = reinterpret_cast<int *>(base + L.tile_expert);
+    ra.row_of = reinterpret_cast<int *>(base + L.row_of);
+    ra.perm = reinterpret_cast<int *>(base + L.perm);
+    ra.row_src = reinterpret_cast<int *>(base + L.row_src);
+    ra.padded = 1;
+    ra.hdr = hdr;
+    NV_CUDA(launch_route(ra, st), "launching the token reorder");
+
+    QuantArgs qa;
+    std::memset(&qa, 0, sizeof(qa));
+    qa.x = x;
+    qa.ids = ids;
+    qa.row_of = ra.row_of;
+    qa.g = g;
+    qa.T = T;
+    qa.H = H;
+    qa.k = k;
+    qa.q = base + L.a1q;
+    qa.sf = base + L.sf1;
+    qa.sf_swizzled = 1;
+    qa.sf_kc = L.kc1;
+    qa.zero_out = out;
+    qa.hdr = hdr;
+    NV_CUDA(launch_quant_experts(qa, st), "launching the a1 quantiser");
+
+    const uint8_t *pw = static_cast<const uint8_t *>(prepared);
+    GemmArgs ga;
+    std::memset(&ga, 0, sizeof(ga));
+    ga.a_q = base + L.a1q;
+    ga.b_q = w->w13_q;
+    ga.a_sf = base + L.sf1;
+    ga.b_sf = pw;
+    ga.rows_cap = L.rows_cap;
+    ga.K = H;
+    ga.N = 2 * I;
+    ga.E = E;
+    ga.a_kc = L.kc1;
+    ga.b_kc = L.kc1;
+    ga.gate_up_I = I;
+    ga.tile_expert = ra.tile_expert;
+    ga.pad_off = ra.pad_off;
+    ga.counts = ra.counts;
+    ga.alpha = alpha1;
+    ga.g2 = g + E;
+    ga.a2q = base + L.a2q;
+    ga.sf2 = base + L.sf2;
+    ga.I = I;
+    ga.kc2 = L.kc2;
+    ga.h_dump = keep_h ? reinterpret_cast<float *>(base + L.host_end) : nullptr;
+    ga.k = k;
+    ga.H = H;
+    ga.hdr = hdr;
+    ga.mtiles_cap = L.mtiles_cap;
+    NV_CUDA(launch_gemm_w13(ga, st), "launching the w13 GEMM");
+
+    GemmArgs gb = ga;
+    gb.a_q = base + L.a2q;
+    gb.b_q = w->w2_q;
+    gb.a_sf = base + L.sf2;
+    gb.b_sf = pw + up256(prepared_w13_bytes(E, H, I));
+    gb.K = I;
+    gb.N = H;
+    gb.a_kc = L.kc2;
+    gb.b_kc = L.kc2;
+    gb.gate_up_I = 0;
+    gb.alpha = alpha2;
+    gb.h_dump = nullptr;
+    gb.row_src = ra.row_src;
+    gb.topk_w = topk_w;
+    gb.out = out;
+    NV_CUDA(launch_gemm_w2(gb, st), "launching the w2 GEMM");
+
+    if (flags & NVFP4_SYNC_CHECK) {
+        DevHeader h;
+        rc = read_header(hdr, st, &h);
+        if (rc) return rc;
+        return header_status(h, nullptr);
+    }
+    return NVFP4_OK;
+}
+
+int nvfp4_moe_forward(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x, int T,
+                      const int32_t *topk_ids, const float *topk_weights, int k, float *out, void *ws,
+                      size_t ws_bytes, unsigned flags, nvfp4_stream_t stream)
+{
+    return forward_impl(w, prepared, x, T, topk_ids, topk_weights, k, out, ws, ws_bytes, flags,
+                        (cudaStream_t)stream);
+}
+
+int nvfp4_moe_forward_host(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x_host, int T,
+                           const int32_t *topk_ids_host, const float *topk_weights_host, int k, float *out_host,
+                           void *ws, size_t ws_bytes, unsigned flags, nvfp4_stream_t stream)
+{
+    int rc = check_weights(w);
+    if (rc) return rc;
+    rc = check_layer_shape(w->E, w->H, w->I, k);
+    if (rc) return rc;
+    if (T < 0 || !ws || (T > 0 && (!x_host || !topk_ids_host || !topk_weights_host || !out_host)))
+        return fail(NVFP4_ERR_INVALID_ARG, "forward_host: bad arguments");
+    const WsLayout L = make_layout(T, w->H, w->I, w->E, k);
+    if (ws_bytes < L.host_end)
+        return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "host workspace %zu < %zu", ws_bytes, L.host_end);
+    if (T == 0) return NVFP4_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    uint16_t *x = reinterpret_cast<uint16_t *>(base + L.x_stage);
+    int32_t *ids = reinterpret_cast<int32_t *>(base + L.ids_stage);
+    float *tw = reinterpret_cast<float *>(base + L.w_stage);
+    float *out = reinterpret_cast<float *>(base + L.out_stage);
+    const size_t R = (size_t)T * k;
+    NV_CUDA(cudaMemcpyAsync(x, x_host, sizeof(uint16_t) * (size_t)T * w->H, cudaMemcpyHostToDevice, st), "copying x");
+    NV_CUDA(cudaMemcpyAsync(ids, topk_ids_host, sizeof(int32_t) * R, cudaMemcpyHostToDevice, st), "copying ids");
+    NV_CUDA(cudaMemcpyAsync(tw, topk_weights_host, sizeof(float) * R, cudaMemcpyHostToDevice, st), "copying weights");
+    rc = forward_impl(w, prepared, x, T, ids, tw, k, out, ws, ws_bytes, flags & ~NVFP4_DEBUG_KEEP_H, st);
+    if (rc) return rc;
+    NV_CUDA(cudaMemcpyAsync(out_host, out, sizeof(float) * (size_t)T * w->H, cudaMemcpyDeviceToHost, st),
+            "copying out");
+    DevHeader h;
+    rc = read_header(base + L.hdr, st, &h);
+    if (rc) return rc;
+    return header_status(h, nullptr);
+}
+
+int nvfp4_moe_status(const void *ws, nvfp4_stream_t stream, int *first_bad_host)
+{
+    if (!ws) return fail(NVFP4_ERR_INVALID_ARG, "ws is null");
+    DevHeader h;
+    int rc = read_header(ws, (cudaStream_t)stream, &h);
+    if (rc) return rc;
+    return header_status(h, first_bad_host);
+}
+
+int nvfp4_moe_intermediates_of(void *ws, int T, int H, int I, int E, int k, nvfp4_moe_intermediates *o)
+{
+    if (!ws || !o) return fail(NVFP4_ERR_INVALID_ARG, "null argument");
+    const WsLayout L = make_layout(T, H, I, E, k);
+    uint8_t *b = static_cast<uint8_t *>(ws);
+    o->rows_cap = L.rows_cap;
+    o->a1q = b + L.a1q;
+    o->sf1 = b + L.sf1;
+    o->a2q = b + L.a2q;
+    o->sf2 = b + L.sf2;
+    o->row_of = reinterpret_cast<int32_t *>(b + L.row_of);
+    o->offsets = reinterpret_cast<int32_t *>(b + L.offsets);
+    o->pad_offsets = reinterpret_cast<int32_t *>(b + L.pad_off);
+    o->h = reinterpret_cast<float *>(b + L.host_end);
+    return NVFP4_OK;
+}
+
+int nvfp4_residual_rmsnorm(const uint16_t *x, const float *out, int T, int H, float eps, uint16_t *x_next,
+                           nvfp4_stream_t stream)
+{
+    if (T < 0 || H <= 0 || (T > 0 && (!x || !out || !x_next)))
+        return fail(NVFP4_ERR_INVALID_ARG, "rmsnorm: bad arguments");
+    if (T == 0) return NVFP4_OK;
+    NV_CUDA(launch_rmsnorm(x, out, T, H, eps, x_next, (cudaStream_t)stream), "launching residual + RMSNorm");
+    return NVFP4_OK;
+}
+
+size_t nvfp4_quantize_weights_workspace_size(int count) { return count > 0 ? up256(sizeof(unsigned) * count) : 0; }
+
+int nvfp4_quantize_weights(const uint16_t *w, int count, int N, int K, uint8_t *q, uint8_t *sf, float *scale2,
+                           void *ws, size_t ws_bytes, nvfp4_stream_t stream)
+{
+    if (count < 1 || count > 65535 || N < 1 || K < 16 || K % 16 != 0 || !w || !q || !sf || !scale2 || !ws)
+        return fail(NVFP4_ERR_INVALID_ARG, "quantize_weights: bad arguments");
+    if (!aligned(q, 8)) return fail(NVFP4_ERR_INVALID_ARG, "quantize_weights: q must be 8-byte aligned");
+    if (ws_bytes < nvfp4_quantize_weights_workspace_size(count))
+        return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "quantize_weights: workspace too small");
+    NV_CUDA(launch_quantize_weights(w, count, N, K, q, sf, scale2, static_cast<unsigned *>(ws),
+                                    (cudaStream_t)stream),
+            "launching the weight quantiser");
+    return NVFP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,111 @@
+// Host-side declarations shared by the translation units of libnvfp4moe.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace nvfp4 {
+
+// ---------------------------------------------------------------- workspace
+// Every region starts on a 256-byte boundary.
+struct WsLayout {
+    int T, H, I, E, k, R;
+    int rows_cap, mtiles_cap, nchunks;
+    int kc1, kc2;  // 64-element scale chunks per 128-row tile for a1 (H) and a2 (I)
+    size_t hdr, g1, g2, alpha1, alpha2, counts, offsets, pad_off, chunk_hist, row_of, perm, row_src,
+        tile_expert, a1q, sf1, a2q, sf2, end;
+    // forward_host staging (after `end`), and the optional FP32 h dump
+    size_t x_stage, ids_stage, w_stage, out_stage, host_end;
+};
+
+constexpr int kRouteChunk = 2048;  // routed rows per routing CTA
+
+WsLayout make_layout(int T, int H, int I, int E, int k);
+
+// ---------------------------------------------------------------- kernels
+struct ValidateArgs {
+    const float *s[4];
+    const uint8_t *written[4];
+    float *recip[4];  // FP32 reciprocal of each slot (nullable per array)
+    int E, narrays;
+    float *alpha1, *alpha2;  // 1/(g_a * g_w) per expert (forward only; nullable)
+    DevHeader *hdr;
+};
+cudaError_t launch_validate(const ValidateArgs &a, cudaStream_t st);
+
+struct RouteArgs {
+    const int32_t *ids;
+    int R, k, E, nchunks;
+    int *chunk_hist, *counts, *offsets, *pad_off, *tile_expert;
+    int *row_of;       // f -> output row (padded rows when `padded`, else compact)
+    int *perm;         // compact permuted row -> f (nullable)
+    int *row_src;      // padded row -> f, -1 for padding (nullable)
+    int *offsets_out;  // caller copy of the compact offsets (nullable)
+    int padded;
+    DevHeader *hdr;
+};
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t st);
+
+struct QuantArgs {
+    const uint16_t *x;
+    const int32_t *ids;
+    const int *row_of;
+    const float *g;  // per-expert global scale
+    int T, H, k;
+    uint8_t *q;
+    uint8_t *sf;
+    int sf_swizzled, sf_kc;
+    float *zero_out;  // [T, H] FP32 zeroed on the way (nullable)
+    const DevHeader *hdr;
+};
+cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st);
+
+struct PrepArgs {
+    const uint8_t *sf;  // canonical [E, N, K/16]
+    uint8_t *out;       // [E][N/128][kc][512]
+    int E, N, K, kc;
+    int gate_up_I;      // > 0: rows interleaved 64 gate / 64 up per 128-row tile
+};
+cudaError_t launch_prep_sf(const PrepArgs &a, cudaStream_t st);
+
+cudaError_t launch_rmsnorm(const uint16_t *x, const float *out, int T, int H, float eps, uint16_t *xn,
+                           cudaStream_t st);
+
+cudaError_t launch_quantize_weights(const uint16_t *w, int count, int N, int K, uint8_t *q, uint8_t *sf,
+                                    float *scale2, unsigned *amax_bits, cudaStream_t st);
+
+struct GemmArgs {
+    // A: activations [rows_cap, K/2]; B: weights [E * Nrows, K/2]
+    const uint8_t *a_q, *b_q;
+    const uint8_t *a_sf, *b_sf;  // swizzled scale tiles
+    int rows_cap, K, N, E;
+    int a_kc, b_kc;
+    int gate_up_I;  // w13: > 0 (B tile = 64 gate rows + 64 up rows)
+    const int *tile_expert, *pad_off, *counts;
+    const float *alpha;
+    // w13 epilogue (SiLU * up, requantise)
+    const float *g2;
+    uint8_t *a2q, *sf2;
+    int I, kc2;
+    float *h_dump;
+    // w2 epilogue (weighted combine)
+    const int *row_src;
+    const float *topk_w;
+    int k, H;
+    float *out;
+    DevHeader *hdr;
+    int mtiles_cap;
+};
+cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st);
+cudaError_t launch_gemm_w2(const GemmArgs &a, cudaStream_t st);
+
+// ---------------------------------------------------------------- helpers
+const DivTable &div_table();
+int sm_count();
+void set_error(const char *fmt, ...);
+
+}  // namespace nvfp4

@@ -1,0 +1,451 @@
+// Memory-bound kernels of the NVFP4 MoE expert path (sm_103a):
+//   scale validation, token reorder (histogram + scan + stable scatter),
+//   the routed activation quantiser, the weight-scale layout conversion,
+//   residual + RMSNorm, and the static weight quantiser.
+//
+// Page cited: "Gemma 4 NVFP4 MoE 空输出" (taking-lying-flat.github.io).
+#include <climits>
+#include <cfloat>
+
+#include "internal.h"
+
+namespace nvfp4 {
+namespace {
+
+// ------------------------------------------------------------------ validate
+// [page, ROOT CAUSE]: a per-expert scale slot left unwritten by the loader is
+// reciprocated into an inf / NaN / garbage global scale.  Every slot must be
+// written, finite, positive and normal, and so must its FP32 reciprocal.
+__global__ void __launch_bounds__(256) validate_kernel(ValidateArgs a)
+{
+    __shared__ int s_bad, s_first;
+    if (threadIdx.x == 0) {
+        s_bad = 0;
+        s_first = INT_MAX;
+    }
+    __syncthreads();
+    const int n = a.narrays * a.E;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int arr = i / a.E, e = i - arr * a.E;
+        const float x = a.s[arr][e];
+        bool ok = true;
+        if (a.written[arr] && a.written[arr][e] == 0) ok = false;
+        const float ax = fabsf(x);
+        if (!(x > 0.0f) || !(ax <= FLT_MAX) || ax < FLT_MIN) ok = false;
+        const float r = __frcp_rn(x);  // the reciprocal the format conversion takes
+        const float ar = fabsf(r);
+        if (!(ar <= FLT_MAX) || ar < FLT_MIN) ok = false;
+        if (a.recip[arr]) a.recip[arr][e] = r;
+        if (!ok) {
+            atomicAdd(&s_bad, 1);
+            atomicMin(&s_first, i);
+        }
+    }
+    __syncthreads();
+    // GEMM output scale 1/(g_a * g_w) per expert [page, §NVFP4 runtime-order
+    // figure: the GEMM's scaling takes in both FP32 global scales].
+    if (a.alpha1 && a.narrays == 4) {
+        for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+            a.alpha1[e] = __frcp_rn(__fmul_rn(a.recip[0][e], a.recip[2][e]));
+            a.alpha2[e] = __frcp_rn(__fmul_rn(a.recip[1][e], a.recip[3][e]));
+        }
+    }
+    if (threadIdx.x == 0) {
+        a.hdr->bad_count = s_bad;
+        a.hdr->first_bad = s_first;
+        a.hdr->status = s_bad ? 2 : 0;
+        a.hdr->error_flags = 0;
+        a.hdr->num_mtiles = 0;
+        a.hdr->done_count = 0u;
+    }
+}
+
+// ------------------------------------------------------------------ routing
+// [page, §矩阵融合 "MoE FFN"]: rows are reordered by expert so all experts'
+// GEMMs run as one grouped GEMM.  Order inside an expert: ascending routed
+// row f = t*k + j (stable), which makes the permutation unique.
+//
+// route_hist_kernel: per-chunk expert histogram; the last CTA to finish scans
+// them (exclusive over chunks per expert, then over experts), producing the
+// compact offsets, the 128-row-padded offsets used by the grouped GEMM, the
+// m-tile -> expert map and the padding entries of row_src.
+__global__ void __launch_bounds__(256) route_hist_kernel(RouteArgs a)
+{
+    extern __shared__ int sh[];
+    __shared__ int s_last;
+    int *hist = sh;
+    const int E = a.E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    if (a.hdr->status != 0) return;
+    const int f0 = blockIdx.x * kRouteChunk, f1 = min(a.R, f0 + kRouteChunk);
+    for (int f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
+        const int e = a.ids[f];
+        if (e < 0 || e >= E)
+            atomicOr(&a.hdr->error_flags, kErrBadExpertId);
+        else
+            atomicAdd(&hist[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) a.chunk_hist[(size_t)blockIdx.x * E + e] = hist[e];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(&a.hdr->done_count, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (__ldcg(&a.hdr->error_flags) & kErrBadExpertId) {
+        if (threadIdx.x == 0) a.hdr->status = 3;  // nothing after this writes
+        return;
+    }
+
+    int *cnt = sh;            // [E]
+    int *off = sh + E;        // [E + 1]
+    int *poff = sh + 2 * E + 1;  // [E + 1]
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int c = 0; c < a.nchunks; ++c) {
+            int *p = &a.chunk_hist[(size_t)c * E + e];
+            const int v = __ldcg(p);
+            *p = run;
+            run += v;
+        }
+        cnt[e] = run;
+        a.counts[e] = run;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int o = 0, po = 0;
+        for (int e = 0; e < E; ++e) {
+            off[e] = o;
+            poff[e] = po;
+            o += cnt[e];
+            po += (cnt[e] + 127) & ~127;
+        }
+        off[E] = o;
+        poff[E] = po;
+        a.hdr->num_mtiles = po >> 7;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        a.offsets[e] = off[e];
+        a.pad_off[e] = poff[e];
+        if (a.offsets_out) a.offsets_out[e] = off[e];
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        if (a.tile_expert)
+            for (int m = poff[e] >> 7; m < (poff[e + 1] >> 7); ++m) a.tile_expert[m] = e;
+        if (a.row_src)
+            for (int r = poff[e] + cnt[e]; r < poff[e + 1]; ++r) a.row_src[r] = -1;
+    }
+}
+
+// route_scatter_kernel: stable ranks.  Each of the 8 warps owns a contiguous
+// 256-row slice of the chunk; per-warp histograms give each warp's starting
+// rank per expert, and the warp walks its slice in order, ranking equal
+// experts inside each 32-row step with __match_any_sync.
+__global__ void __launch_bounds__(256) route_scatter_kernel(RouteArgs a)
+{
+    extern __shared__ int sh[];  // [8][E]
+    const int E = a.E;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int *wb = sh + warp * E;
+    for (int e = lane; e < E; e += 32) wb[e] = 0;
+    __syncthreads();
+    if (a.hdr->status != 0) return;
+    const int f0 = blockIdx.x * kRouteChunk;
+    const int wf0 = f0 + warp * (kRouteChunk / 8);
+    const int wf1 = min(a.R, wf0 + kRouteChunk / 8);
+    for (int f = wf0 + lane; f < wf1; f += 32) {
+        const int e = a.ids[f];
+        if (e >= 0 && e < E) atomicAdd(&wb[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = a.chunk_hist[(size_t)blockIdx.x * E + e];
+        for (int w = 0; w < 8; ++w) {
+            const int v = sh[w * E + e];
+            sh[w * E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    for (int base = wf0; base < wf1; base += 32) {
+        const int f = base + lane;
+        int e = (f < wf1) ? a.ids[f] : -1;
+        if (e >= E) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        const int pos = (e >= 0) ? wb[e] + rank : 0;
+        __syncwarp();
+        if (e >= 0 && rank == 0) wb[e] += __popc(peers);
+        __syncwarp();
+        if (e >= 0) {
+            const int compact = a.offsets[e] + pos;
+            const int padded = a.pad_off[e] + pos;
+            a.row_of[f] = a.padded ? padded : compact;
+            if (a.perm) a.perm[compact] = f;
+            if (a.row_src) a.row_src[padded] = f;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ quantiser
+// [page, §NVFP4 runtime-order figure; MoE section: SFScale[expert_idx]]:
+// one thread per (token, 16-element block).  The block's BF16 values and amax
+// are read once and quantised for each of the token's k experts with that
+// expert's global scale, into the expert's permuted row.  Four lanes pack
+// their four scale bytes into one 32-bit store.
+__global__ void __launch_bounds__(256) quant_experts_kernel(QuantArgs a, DivTable tab_in)
+{
+    __shared__ float2 tab[128];
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) tab[i] = tab_in.z[i];
+    __syncthreads();
+    if (a.hdr && a.hdr->status != 0) return;
+    const int nb = a.H >> 4;
+    const long long total = (long long)a.T * nb;
+    const int lane = threadIdx.x & 31;
+    const long long warp_stride = (long long)gridDim.x * blockDim.x;
+    for (long long wbase = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); wbase < total;
+         wbase += warp_stride) {
+        const long long idx = wbase + lane;
+        const bool valid = idx < total;
+        const int t = valid ? (int)(idx / nb) : 0;
+        const int b = valid ? (int)(idx - (long long)t * nb) : 0;
+        float x[16];
+        float amax = 0.0f;
+        if (valid) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + (size_t)b * 16);
+            const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+            const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                x[2 * i] = bf16_lo(w[i]);
+                x[2 * i + 1] = bf16_hi(w[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+            if (a.zero_out) {
+                float4 *z = reinterpret_cast<float4 *>(a.zero_out + (size_t)t * a.H + (size_t)b * 16);
+                const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+                z[0] = zero;
+                z[1] = zero;
+                z[2] = zero;
+                z[3] = zero;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = 0.0f;
+        }
+        for (int j = 0; j < a.k; ++j) {
+            int row = 0;
+            float g = 1.0f;
+            if (valid) {
+                const int f = t * a.k + j;
+                row = a.row_of[f];
+                g = a.g[a.ids[f]];
+            }
+            uint32_t sb;
+            const uint2 pk = quant_block16(x, amax, g, tab, sb);
+            uint32_t word = sb;
+            word |= __shfl_down_sync(0xffffffffu, sb, 1) << 8;
+            word |= __shfl_down_sync(0xffffffffu, sb, 2) << 16;
+            word |= __shfl_down_sync(0xffffffffu, sb, 3) << 24;
+            if (valid) {
+                *reinterpret_cast<uint2 *>(a.q + (size_t)row * (a.H >> 1) + (size_t)b * 8) = pk;
+                if ((b & 3) == 0) {
+                    uint8_t *dst = a.sf_swizzled ? a.sf + swz_sf_offset(row, b >> 2, a.sf_kc)
+                                                 : a.sf + (size_t)row * nb + b;
+                    *reinterpret_cast<uint32_t *>(dst) = word;
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ weight-scale layout
+// [page, "Kernel Backend": packed weights and scales are converted to the
+// layout the chosen kernel wants].  One thread per output word (one row's four
+// scales of a 64-element chunk).  For w13 every 128-row tile holds 64 gate rows
+// followed by the 64 matching up rows, so one tile yields 64 SiLU(gate)*up
+// columns.
+__global__ void __launch_bounds__(256) prep_sf_kernel(PrepArgs a)
+{
+    const int NT = a.N / 128;
+    const long long total = (long long)a.E * NT * a.kc * 128;
+    const int nsf = a.K / 16;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int v = (int)(i & 127);
+        long long rest = i >> 7;
+        const int c = (int)(rest % a.kc);
+        rest /= a.kc;
+        const int nt = (int)(rest % NT);
+        const int e = (int)(rest / NT);
+        int row;
+        if (a.gate_up_I > 0)
+            row = v < 64 ? nt * 64 + v : a.gate_up_I + nt * 64 + (v - 64);
+        else
+            row = nt * 128 + v;
+        const uint8_t *src = a.sf + ((size_t)e * a.N + row) * nsf;
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int col = 4 * c + j;
+            if (col < nsf) word |= (uint32_t)src[col] << (8 * j);
+        }
+        uint8_t *dst = a.out + (((size_t)e * NT + nt) * a.kc + c) * 512 + (size_t)(v & 31) * 16 + (v >> 5) * 4;
+        *reinterpret_cast<uint32_t *>(dst) = word;
+    }
+}
+
+// ------------------------------------------------------------------ residual + RMSNorm
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t *x, const float *out, int H, float eps,
+                                                       uint16_t *xn)
+{
+    const int t = blockIdx.x;
+    const uint16_t *xr = x + (size_t)t * H;
+    const float *orow = out + (size_t)t * H;
+    float ss = 0.0f;
+    for (int i = threadIdx.x; i < H; i += blockDim.x) {
+        const float r = __uint_as_float((uint32_t)xr[i] << 16) + orow[i];
+        ss = fmaf(r, r, ss);
+    }
+    __shared__ float red[8];
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
+    const float inv = 1.0f / sqrtf(tot / (float)H + eps);
+    __syncthreads();  // every thread has read `red` before x_next may overwrite x
+    for (int i = threadIdx.x; i < H; i += blockDim.x) {
+        const float r = __uint_as_float((uint32_t)xr[i] << 16) + orow[i];
+        const float y = r * inv;
+        uint32_t u = __float_as_uint(y);
+        u += 0x7FFFu + ((u >> 16) & 1u);  // nearest BF16, ties to even (finite inputs)
+        xn[(size_t)t * H + i] = (uint16_t)(u >> 16);
+    }
+}
+
+// ------------------------------------------------------------------ static weight quantiser
+// [page, glossary "Static weight quantization"; §NVFP4 two-level scale:
+// 2688 = 6 * 448].  Pass 1: amax per tensor (non-negative floats order like
+// their bit patterns, so an unsigned atomicMax is exact).
+__global__ void __launch_bounds__(256) weight_amax_kernel(const uint16_t *w, long long per, unsigned *amax_bits)
+{
+    const int c = blockIdx.y;
+    const uint16_t *src = w + (size_t)c * per;
+    float m = 0.0f;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < per;
+         i += (long long)gridDim.x * blockDim.x)
+        m = fmaxf(m, fabsf(__uint_as_float((uint32_t)src[i] << 16)));
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(&amax_bits[c], __float_as_uint(m));
+}
+
+// Pass 2: weight_scale_2 = fl(amax / 2688), g = fl(1 / weight_scale_2), then
+// the same block quantisation as activations.  A tensor of zeros has no
+// usable scale: it gets weight_scale_2 = 0 (rejected by validation) and zero
+// codes and scales.
+__global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t *w, int N, int K, uint8_t *q,
+                                                           uint8_t *sf, float *scale2,
+                                                           const unsigned *amax_bits, DivTable tab_in)
+{
+    __shared__ float2 tab[128];
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) tab[i] = tab_in.z[i];
+    __syncthreads();
+    const int c = blockIdx.y;
+    const float amax_t = __uint_as_float(amax_bits[c]);
+    const float s2 = __fdiv_rn(amax_t, 2688.0f);
+    const float g = __frcp_rn(s2);
+    if (blockIdx.x == 0 && threadIdx.x == 0) scale2[c] = s2;
+    const int nb = K >> 4;
+    const long long total = (long long)N * nb;
+    const uint16_t *src = w + (size_t)c * N * K;
+    uint8_t *qc = q + (size_t)c * N * (K >> 1);
+    uint8_t *sfc = sf + (size_t)c * N * nb;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int n = (int)(i / nb), b = (int)(i - (long long)n * nb);
+        float x[16];
+        float amax = 0.0f;
+        const uint16_t *p = src + (size_t)n * K + (size_t)b * 16;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            x[j] = __uint_as_float((uint32_t)p[j] << 16);
+            amax = fmaxf(amax, fabsf(x[j]));
+        }
+        uint32_t sb = 0;
+        uint2 pk = make_uint2(0u, 0u);
+        if (amax_t > 0.0f) pk = quant_block16(x, amax, g, tab, sb);
+        *reinterpret_cast<uint2 *>(qc + (size_t)n * (K >> 1) + (size_t)b * 8) = pk;
+        sfc[(size_t)n * nb + b] = (uint8_t)sb;
+    }
+}
+
+int grid_for(long long work, int per_block, int waves_cap)
+{
+    long long g = (work + per_block - 1) / per_block;
+    const long long cap = (long long)sm_count() * waves_cap;
+    if (g > cap) g = cap;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_validate(const ValidateArgs &a, cudaStream_t st)
+{
+    validate_kernel<<<1, 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t st)
+{
+    const size_t sh1 = sizeof(int) * (3 * (size_t)a.E + 2);
+    route_hist_kernel<<<a.nchunks, 256, sh1, st>>>(a);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const size_t sh2 = sizeof(int) * 8 * (size_t)a.E;
+    route_scatter_kernel<<<a.nchunks, 256, sh2, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st)
+{
+    const long long work = (long long)a.T * (a.H >> 4);
+    quant_experts_kernel<<<grid_for(work, 256, 8), 256, 0, st>>>(a, div_table());
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep_sf(const PrepArgs &a, cudaStream_t st)
+{
+    const long long work = (long long)a.E * (a.N / 128) * a.kc * 128;
+    prep_sf_kernel<<<grid_for(work, 256, 16), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const uint16_t *x, const float *out, int T, int H, float eps, uint16_t *xn,
+                           cudaStream_t st)
+{
+    rmsnorm_kernel<<<T, 256, 0, st>>>(x, out, H, eps, xn);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_weights(const uint16_t *w, int count, int N, int K, uint8_t *q, uint8_t *sf,
+                                    float *scale2, unsigned *amax_bits, cudaStream_t st)
+{
+    cudaError_t err = cudaMemsetAsync(amax_bits, 0, sizeof(unsigned) * (size_t)count, st);
+    if (err != cudaSuccess) return err;
+    const long long per = (long long)N * K;
+    dim3 g1(grid_for(per, 256 * 8, 4), count);
+    weight_amax_kernel<<<g1, 256, 0, st>>>(w, per, amax_bits);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    dim3 g2(grid_for((long long)N * (K / 16), 256, 4), count);
+    weight_quant_kernel<<<g2, 256, 0, st>>>(w, N, K, q, sf, scale2, amax_bits, div_table());
+    return cudaGetLastError();
+}
+
+}  // namespace nvfp4

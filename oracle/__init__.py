@@ -218,6 +218,9 @@ def quantize_weight(w_bf16: np.ndarray):
     Returns (q [N, K/2], sf [N, K/16], weight_scale_2 float32)."""
     wf = (np.asarray(w_bf16, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
     amax = np.float32(np.abs(wf).max())
+    if amax == 0:  # no usable scale: zero codes and scales, weight_scale_2 = 0
+        N, K = wf.shape
+        return np.zeros((N, K // 2), np.uint8), np.zeros((N, K // 16), np.uint8), np.float32(0.0)
     scale2 = np.float32(amax / np.float32(2688.0))
     g = reciprocal_f32(np.array([scale2]))[0]
     q, sf = quant_rows(wf, np.full(wf.shape[0], g, dtype=np.float32))

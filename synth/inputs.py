@@ -39,10 +39,9 @@ RANGE_2688 = np.float32(2688.0)
 
 def bf16_bits_from_f32(a: np.ndarray) -> np.ndarray:
     """Round FP32 values to BF16 (nearest, ties to even); returns uint16 bits."""
-    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    lsb = (u >> 16) & 1
-    r = (u + 0x7FFF + lsb) >> 16
-    return r.astype(np.uint16)
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    r = u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))  # finite inputs: no wrap-around
+    return (r >> np.uint32(16)).astype(np.uint16)
 
 
 def f32_from_bf16_bits(b: np.ndarray) -> np.ndarray:

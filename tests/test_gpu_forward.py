@@ -1,0 +1,183 @@
+"""GPU parity of the whole expert path (through the C ABI) against the oracle.
+
+Bit-exact: the a1 codes and scales, the routing, and the a2 codes and scales
+given the GPU's own FP32 SiLU(gate)*up (both sides then decide every code in
+FP32).  Within tolerance (max |d| <= 2e-3 max |ref|, Frobenius <= 1e-3): the
+FP32-accumulated outputs and the intermediate h."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import inputs as S
+
+from gpu_helpers import assert_close, dev, dev_bf16, device_weights, host, layer_with_weights, unswizzle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def m():
+    import nvfp4_w4a4_moe_gb300 as mod
+    mod.load()
+    return mod
+
+
+def run_gpu(m, layer, W, flags=None, w=None):
+    if flags is None:
+        flags = m.SYNC_CHECK | m.DEBUG_KEEP_H
+    w = device_weights(W) if w is None else w
+    out, ws = m.moe_forward(w, dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w), flags=flags)
+    torch.cuda.synchronize()
+    return out, ws, w
+
+
+def check_layer(m, layer, W, tokens=None):
+    out, ws, _ = run_gpu(m, layer, W)
+    ref = oracle.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W, tokens=tokens)
+    toks = np.arange(layer.T) if tokens is None else np.asarray(tokens)
+    stats = {"out": assert_close(host(out)[toks], ref["out"][toks], "out")}
+
+    T, H, I, E, k = layer.T, layer.H, layer.I, layer.E, layer.k
+    it = m.intermediates_of(ws, T, H, I, E, k)
+    assert np.array_equal(host(it["offsets"]), ref["offsets"])
+    row_of = host(it["row_of"])
+    prow = row_of[ref["perm"][ref["rows"]]]
+    # padded layout: each expert starts on a 128-row tile, rows keep the oracle's order
+    pad = host(it["pad_offsets"])
+    assert np.all(pad[1:] - pad[:-1] == ((np.diff(ref["offsets"]) + 127) // 128) * 128)
+    assert np.array_equal(host(it["a1q"])[prow], ref["a1q"]), "a1 codes"
+    assert np.array_equal(unswizzle(host(it["sf1"]), prow, H // 16, it["kc1"]), ref["sf1"]), "a1 scales"
+    h_gpu = host(it["h"])[prow]
+    stats["h"] = assert_close(h_gpu, ref["h"], "h")
+    g2 = oracle.reciprocal_f32(W.w2_input_scale)[ref["row_expert"][ref["rows"]]]
+    q2, s2 = oracle.quant_rows(h_gpu, g2)
+    a2q = host(it["a2q"])[prow]
+    assert np.array_equal(a2q, q2), "a2 codes (requantisation of the GPU's h)"
+    assert np.array_equal(unswizzle(host(it["sf2"]), prow, I // 16, it["kc2"]), s2), "a2 scales"
+    # against the oracle's own h the codes may differ where h sits on a
+    # rounding boundary; that must stay rare
+    diff = (oracle.unpack_codes(a2q) != oracle.unpack_codes(ref["a2q"])).mean()
+    assert diff <= 1e-3, f"{diff:.2e} of a2 codes differ from the oracle's"
+    stats["a2_code_diff"] = diff
+    return stats
+
+
+def test_tiny_layer(m):
+    layer, W = layer_with_weights(S.tiny())
+    check_layer(m, layer, W)
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 64])
+def test_decode_layer(m, T):
+    layer, W = layer_with_weights(S.decode(T))
+    check_layer(m, layer, W)
+
+
+@pytest.fixture(scope="module")
+def prefill(m):
+    return layer_with_weights(S.prefill(), max_rows=32)
+
+
+def test_prefill_layer_sampled_tokens(m, prefill):
+    layer, W = prefill
+    tokens = np.sort(np.random.default_rng([layer.seed, 1]).choice(layer.T, 48, replace=False))
+    check_layer(m, layer, W, tokens=tokens)
+
+
+def test_prefill_unwritten_slots_rejected_before_launch(m, prefill):
+    layer, W = prefill
+    slots = S.unwritten_slots(layer.seed, layer.E)
+    w = device_weights(W, w13_in=S.with_unwritten(W.w13_input_scale, slots),
+                       w2_in=S.with_unwritten(W.w2_input_scale, slots[:1]))
+    out = torch.full((layer.T, layer.H), 7.0, device="cuda")
+    with pytest.raises(m.Nvfp4Error) as ei:
+        m.moe_forward(w, dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w), out=out)
+    assert ei.value.status == m.ERR_SCALE_INVALID
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all()), "out was written although the call was rejected"
+    # without the host check the device still refuses, and reports the slot
+    _, ws = m.moe_forward(w, dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w), out=out,
+                          flags=m.SCALES_PREVALIDATED)
+    status, first = m.moe_status(ws)
+    assert status == m.ERR_SCALE_INVALID and first == int(slots[0])
+    assert bool((out == 7.0).all())
+
+
+def test_bad_expert_id_refused_on_device(m):
+    layer, W = layer_with_weights(S.tiny())
+    ids = layer.topk_ids.copy()
+    ids[3, 0] = -1
+    out = torch.full((layer.T, layer.H), 5.0, device="cuda")
+    with pytest.raises(m.Nvfp4Error) as ei:
+        m.moe_forward(device_weights(W), dev_bf16(layer.x), dev(ids), dev(layer.topk_w), out=out,
+                      flags=m.SYNC_CHECK)
+    assert ei.value.status == m.ERR_INVALID_ARG
+    assert bool((out == 5.0).all())
+
+
+def test_empty_batch(m):
+    layer, W = layer_with_weights(S.tiny())
+    x = torch.zeros((0, layer.H), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((0, layer.k), dtype=torch.int32, device="cuda")
+    tw = torch.zeros((0, layer.k), dtype=torch.float32, device="cuda")
+    out, _ = m.moe_forward(device_weights(W), x, ids, tw, flags=m.SYNC_CHECK)
+    assert out.shape == (0, layer.H)
+
+
+def test_one_expert_per_token_and_skew(m):
+    """k = 1 with unit weights (out is one expert's w2 output), and every token
+    routed to the same expert (one expert spanning many 128-row tiles)."""
+    base = S.tiny()
+    r = np.random.default_rng(9)
+    for ids in (r.integers(0, base.E, (base.T, 1)).astype(np.int32),
+                np.full((base.T * 5, 1), 2, np.int32)):
+        T = ids.shape[0]
+        layer = S.Layer("tiny", base.E, base.H, base.I, T, 1, base.seed, S.normal_bf16(r, (T, base.H)), ids,
+                        np.ones((T, 1), np.float32))
+        layer.w13_input_scale = S.input_scale_from_amax(S.amax_per_expert(S.f32_from_bf16_bits(layer.x), ids,
+                                                                            base.E))
+        layer, W = layer_with_weights(layer)
+        check_layer(m, layer, W)
+
+
+def test_host_entry_point_matches_device_path(m):
+    layer, W = layer_with_weights(S.decode(32))
+    out_d, _, w = run_gpu(m, layer, W, flags=m.SYNC_CHECK)
+    xh = torch.from_numpy(layer.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ih = torch.from_numpy(layer.topk_ids).pin_memory()
+    wh = torch.from_numpy(layer.topk_w).pin_memory()
+    out_h, _ = m.moe_forward_host(w, xh, ih, wh)
+    ref = oracle.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W)["out"]
+    assert_close(out_h.numpy(), ref, "host entry point")
+    assert_close(out_h.numpy(), host(out_d).astype(np.float64), "host vs device entry point")
+
+
+def test_weight_quantiser_matches_oracle_weight_path(m):
+    """The device weight quantiser against the oracle's static weight path."""
+    r = np.random.default_rng(11)
+    layer = S.decode(1)
+    w = np.stack([layer.weight_bf16(0, "w13"), layer.weight_bf16(1, "w13")])
+    small = S.normal_bf16(r, (3, 64, 256), 0.02)
+    small[2] = 0  # a tensor of zeros
+    for t in (w, small):
+        q, sf, s2 = m.quantize_weights(dev_bf16(t))
+        torch.cuda.synchronize()
+        for c in range(t.shape[0]):
+            q_ref, sf_ref, s2_ref = oracle.quantize_weight(t[c])
+            assert host(s2)[c] == s2_ref
+            assert np.array_equal(host(q)[c], q_ref) and np.array_equal(host(sf)[c], sf_ref)
+
+
+def test_residual_rmsnorm(m):
+    r = np.random.default_rng(12)
+    T, H = 33, 2816
+    x = S.normal_bf16(r, (T, H))
+    out = r.standard_normal((T, H)).astype(np.float32)
+    got = host(m.residual_rmsnorm(dev_bf16(x), dev(out)).view(torch.int16)).view(np.uint16)
+    ref = oracle.residual_rmsnorm(x, out)
+    gf, rf = S.f32_from_bf16_bits(got), S.f32_from_bf16_bits(ref)
+    # FP32 on the device vs fp64 in the oracle: at most one BF16 step apart, rarely
+    step = np.abs(rf) * 2.0 ** -7
+    assert np.all(np.abs(gf - rf) <= step * 1.0001)
+    assert (got != ref).mean() < 1e-3

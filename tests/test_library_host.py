@@ -1,0 +1,107 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, its host-side logic (sizes, argument checks) answers, and the
+exact block-scale division it relies on holds for every E4M3 divisor."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4_moe.h")
+
+
+@pytest.fixture(scope="session")
+def lib():
+    import nvfp4_w4a4_moe_gb300 as m
+    m.build()
+    return m.load()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for must in ("nvfp4_validate_scales", "nvfp4_quantize_experts", "nvfp4_moe_forward"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_error_string(lib):
+    assert lib.nvfp4_version() >= 100
+    assert isinstance(lib.nvfp4_last_error_string(), bytes)
+
+
+def test_block_division_is_exact_for_every_e4m3_scale(lib):
+    assert lib.nvfp4_selftest_block_division(0) == 0
+
+
+def test_workspace_sizes(lib):
+    import nvfp4_w4a4_moe_gb300 as m
+    H, I, E, k = 2816, 704, 128, 8
+    prev = 0
+    for T in (0, 1, 8, 64, 512, 8192):
+        n = m.moe_workspace_size(T, H, I, E, k)
+        assert n >= prev and n % 256 == 0
+        assert m.moe_host_workspace_size(T, H, I, E, k) >= n
+        prev = n
+    # the padded row capacity covers the worst case: every busy expert ends
+    # on a partial 128-row tile
+    R = 8192 * k
+    assert m.intermediates_rows_cap(8192, E, k) >= R + E * 127
+    assert m.intermediates_rows_cap(1, E, k) == 8 * 128
+    assert m.prepared_weights_size(E, H, I) == E * 11 * 44 * 512 + E * 22 * 12 * 512
+    assert m.quantize_workspace_size(4096, 8, 128) > 0
+    assert m.moe_workspace_size(-1, H, I, E, k) == 0
+
+
+def test_argument_errors_need_no_gpu(lib):
+    import nvfp4_w4a4_moe_gb300 as m
+    P = ctypes.c_void_p
+    # null weights struct
+    rc = lib.nvfp4_moe_forward(None, None, None, 4, None, None, 8, None, None, 0, 0, None)
+    assert rc == m.ERR_INVALID_ARG
+    # unsupported shapes
+    w = m._Weights(128, 2816 + 64, 704, *([P(256)] * 10))
+    rc = lib.nvfp4_moe_forward(ctypes.byref(w), P(256), P(256), 1, P(256), P(256), 8, P(256), P(256), 1 << 30, 0, None)
+    assert rc == m.ERR_UNSUPPORTED_SHAPE
+    assert b"256" in lib.nvfp4_last_error_string()
+    w = m._Weights(128, 2816, 700, *([P(256)] * 10))
+    rc = lib.nvfp4_moe_forward(ctypes.byref(w), P(256), P(256), 1, P(256), P(256), 8, P(256), P(256), 1 << 30, 0, None)
+    assert rc == m.ERR_UNSUPPORTED_SHAPE
+    w = m._Weights(2000, 2816, 704, *([P(256)] * 10))
+    rc = lib.nvfp4_moe_forward(ctypes.byref(w), P(256), P(256), 1, P(256), P(256), 8, P(256), P(256), 1 << 30, 0, None)
+    assert rc == m.ERR_UNSUPPORTED_SHAPE
+    # workspace too small
+    w = m._Weights(128, 2816, 704, *([P(256)] * 10))
+    rc = lib.nvfp4_moe_forward(ctypes.byref(w), P(256), P(256), 64, P(256), P(256), 8, P(256), P(256), 1024, 0, None)
+    assert rc == m.ERR_WORKSPACE_TOO_SMALL
+    # misaligned workspace
+    rc = lib.nvfp4_moe_forward(ctypes.byref(w), P(256), P(256), 64, P(256), P(256), 8, P(256), P(264), 1 << 40, 0, None)
+    assert rc == m.ERR_INVALID_ARG
+    # quantiser: unknown scale layout, H not a multiple of 64
+    rc = lib.nvfp4_quantize_experts(P(256), 4, 256, P(256), 2, 4, P(256), P(256), P(256), 7, P(256), P(256), P(256),
+                                    1 << 20, None)
+    assert rc == m.ERR_INVALID_ARG
+    rc = lib.nvfp4_quantize_experts(P(256), 4, 100, P(256), 2, 4, P(256), P(256), P(256), 0, P(256), P(256), P(256),
+                                    1 << 20, None)
+    assert rc == m.ERR_UNSUPPORTED_SHAPE
+    # validate: null result pointers
+    rc = lib.nvfp4_validate_scales(P(256), None, 4, P(256), None, None, None)
+    assert rc == m.ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    import nvfp4_w4a4_moe_gb300 as m
+    monkeypatch.setattr(m, "_lib", None)
+    monkeypatch.setattr(m, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(m.Nvfp4Error):
+        m.load()
