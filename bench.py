@@ -1,0 +1,435 @@
+"""Benchmark of the NVFP4 W4A4 MoE expert forward on GB300.
+
+One step = one pass of the whole expert path (scale check, token reorder,
+a1 quantisation, w13 GEMM + SiLU*up + a2 quantisation, w2 GEMM + weighted
+combine) over one batch: the prefill-shaped layer of 8192 tokens, 128
+experts, hidden 2816, intermediate 704, top-8 with Zipf(1.1) routing.  Inputs
+are synthetic and seeded; weights are N(0, 0.02) BF16 draws quantised to NVFP4
+on the device.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (the reference arm).  Under torchrun (N > 1) each rank runs an
+independent replica of the layer on its own GPU (the path has no exchange
+step); value = tokens of all ranks / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synth import inputs as S  # noqa: E402
+
+METRIC = "NVFP4 MoE layer tokens/s; quant GB/s and expert-GEMM FP4 TFLOPS vs GB300 peak"
+WORKLOAD = ("prefill MoE layer: 8192 tokens, 128 experts, hidden 2816, intermediate 704, top-8, "
+            "Zipf(1.1) routing with 8 idle experts")
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
+
+
+def peaks():
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        p.update({k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained") if k in d})
+        p["source"] = "measured"
+    return p
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- workload
+def make_layer_device(layer, m, torch, seed: int):
+    """Device weights: N(0, 0.02) BF16 draws quantised on the device."""
+    E, H, I = layer.E, layer.H, layer.I
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    w13 = (torch.randn((E, 2 * I, H), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+    w2 = (torch.randn((E, H, I), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+    q13, sf13, s13 = m.quantize_weights(w13)
+    q2, sf2, s2 = m.quantize_weights(w2)
+    in13 = torch.from_numpy(layer.w13_input_scale).cuda()
+    w = m.MoEWeights(E, H, I, q13, sf13, s13, in13, q2, sf2, s2, torch.ones(E, device="cuda"))
+    return w, (w13, w2)
+
+
+def calibrate_w2_on_device(m, torch, w, x, ids, tw, layer):
+    """w2 input scale = amax of SiLU(gate)*up per expert / 2688, from one
+    forward that keeps h (calibration stand-in; outside the timed region)."""
+    T, k, E, I = layer.T, layer.k, layer.E, layer.I
+    _, ws = m.moe_forward(w, x, ids, tw, flags=m.DEBUG_KEEP_H | m.SYNC_CHECK)
+    it = m.intermediates_of(ws, T, layer.H, I, E, k)
+    pad = it["pad_offsets"].cpu().numpy()
+    counts = np.diff(np.concatenate([[0], np.bincount(layer.topk_ids.ravel(), minlength=E).cumsum()]))
+    h = it["h"]
+    amax = np.zeros(E, np.float32)
+    for e in range(E):
+        if counts[e]:
+            amax[e] = float(h[pad[e]:pad[e] + counts[e]].abs().max())
+    amax[amax == 0] = amax.max()
+    w.w2_input_scale = torch.from_numpy(S.input_scale_from_amax(amax)).cuda()
+    del ws
+
+
+def algorithmic(layer, n_active):
+    """Algorithmic bytes / FLOPs per launch of each stage (minimum traffic)."""
+    T, H, I, k, E = layer.T, layer.H, layer.I, layer.k, layer.E
+    R = T * k
+    fp4 = 0.5 + 1.0 / 16.0  # bytes per element: packed code + its share of a scale byte
+    return {
+        "validate": {"bytes": 4 * 4 * E},
+        "route": {"bytes": R * 4 * 3 + R * 4},
+        "quant_a1": {"bytes": T * H * 2 + R * H * fp4 + R * 4 * 2 + T * H * 4},
+        "gemm_w13": {"bytes": R * H * fp4 + n_active * 2 * I * H * fp4 + R * I * fp4,
+                     "flops": 2.0 * R * 2 * I * H},
+        "gemm_w2": {"bytes": R * I * fp4 + n_active * H * I * fp4 + T * H * 4, "flops": 2.0 * R * H * I},
+    }
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import nvfp4_w4a4_moe_gb300 as m
+
+    m.load()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    layer = S.prefill()
+    T, H, I, E, k = layer.T, layer.H, layer.I, layer.E, layer.k
+    w, _bf16 = make_layer_device(layer, m, torch, seed=1003 + 17 * rank)
+    x = torch.from_numpy(layer.x.view(np.int16)).cuda().view(torch.bfloat16)
+    ids = torch.from_numpy(layer.topk_ids).cuda()
+    tw = torch.from_numpy(layer.topk_w).cuda()
+    calibrate_w2_on_device(m, torch, w, x, ids, tw, layer)
+    del _bf16
+    m.prepare_weights(w)
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(m.moe_workspace_size(T, H, I, E, k), dtype=torch.uint8, device="cuda")
+    flags = m.SCALES_PREVALIDATED
+    stream = torch.cuda.current_stream()
+
+    # one checked call first: scale check with the host sync, device status clean
+    m.moe_forward(w, x, ids, tw, out=out, ws=ws, flags=m.SYNC_CHECK)
+
+    K, W = args.steps, args.warmup
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for _ in range(W):
+        m.moe_forward(w, x, ids, tw, out=out, ws=ws, flags=flags)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(0).uuid)
+    except Exception:
+        uuid = None
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(uuid if rank == 0 else None) as clocks:
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        start.record(stream)
+        for i in range(K):
+            m.moe_forward_profiled(w, x, ids, tw, evs[i], out=out, ws=ws, flags=flags)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    status, _ = m.moe_status(ws)
+    if status != m.OK:
+        raise RuntimeError(f"device status {status} after the timed steps")
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / K
+    stage_ms = {name: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
+                for j, name in enumerate(m.STAGES)}
+
+    # host-checked step (scale check synchronised on the host), for reference
+    t0 = time.perf_counter()
+    for _ in range(5):
+        m.moe_forward(w, x, ids, tw, out=out, ws=ws, flags=0)
+    torch.cuda.synchronize()
+    ms_checked = (time.perf_counter() - t0) * 1e3 / 5
+
+    # quantiser workload: 4096 tokens x 2816, uniform top-8, 1% outliers x50
+    qres = quant_workload(m, torch, w, args)
+
+    # e2e: host buffers in, host buffers out, through the host entry point
+    e2e = e2e_host(m, torch, w, layer, args)
+
+    pk = peaks()
+    n_active = int((np.bincount(layer.topk_ids.ravel(), minlength=E) > 0).sum())
+    alg = algorithmic(layer, n_active)
+    fp4_peak = pk["bf16_tflops"] * FP4_OVER_BF16
+    dom = max(stage_ms, key=stage_ms.get)
+    a = alg[dom]
+    t_s = stage_ms[dom] * 1e-3
+    if "flops" in a and a["flops"] / (fp4_peak * 1e12) > a["bytes"] / (pk["hbm_gbs"] * 1e9):
+        roof = {"bound": "tensor", "achieved": a["flops"] / t_s / 1e12, "peak": fp4_peak, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": a["bytes"] / t_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = dom
+    roof["peak_source"] = (f"{pk['source']} HBM copy" if roof["bound"] == "hbm" else
+                           f"{pk['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4:BF16)")
+
+    tokens = T * world
+    line = {
+        "metric": METRIC,
+        "value": tokens / (ms_step * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4 e2m1 x e2m1 (e4m3 block scales), fp32 accumulate",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T, "E": E, "H": H, "I": I, "k": k,
+                   "routed_rows": T * k, "active_experts": n_active,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (0.43 GB of weights + 0.2 GB activations per step)",
+                   "scale_check": "device-side each step; host sync skipped in the timed steps",
+                   "ms_per_step_with_host_scale_check": ms_checked},
+        "roofline": roof,
+        "kernels": {n: {"ms": v, "share": v / sum(stage_ms.values())} for n, v in stage_ms.items()},
+        "gemm": {
+            "w13_tflops": alg["gemm_w13"]["flops"] / (stage_ms["gemm_w13"] * 1e-3) / 1e12,
+            "w2_tflops": alg["gemm_w2"]["flops"] / (stage_ms["gemm_w2"] * 1e-3) / 1e12,
+            "fp4_peak_tflops": fp4_peak,
+            "w13_frac_fp4_peak": alg["gemm_w13"]["flops"] / (stage_ms["gemm_w13"] * 1e-3) / 1e12 / fp4_peak,
+            "w2_frac_fp4_peak": alg["gemm_w2"]["flops"] / (stage_ms["gemm_w2"] * 1e-3) / 1e12 / fp4_peak,
+        },
+        "quant": qres,
+        "e2e": e2e,
+        "gpu_launches": 6 * K,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    if dist:
+        dist.destroy_process_group()
+    return line
+
+
+def quant_workload(m, torch, w, args):
+    """The activation quantiser on the quantiser workload (4096 x 2816, 128
+    experts, uniform top-8, input_scale = U(0.5,2) amax/2688), timed as the
+    a1-quantiser stage of the expert path."""
+    L = S.quantiser()
+    T, H, E, k = L.T, L.H, L.E, L.k
+    x = torch.from_numpy(L.x.view(np.int16)).cuda().view(torch.bfloat16)
+    ids = torch.from_numpy(L.topk_ids).cuda()
+    tw = torch.from_numpy(L.topk_w).cuda()
+    wq = m.MoEWeights(E, H, w.I, w.w13_q, w.w13_sf, w.w13_scale2, torch.from_numpy(L.w13_input_scale).cuda(),
+                      w.w2_q, w.w2_sf, w.w2_scale2, w.w2_input_scale)
+    wq.prepared = w.prepared
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(m.moe_workspace_size(T, H, w.I, E, k), dtype=torch.uint8, device="cuda")
+    m.moe_forward(wq, x, ids, tw, out=out, ws=ws, flags=m.SYNC_CHECK)
+    n = max(20, args.steps // 2)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n)]
+    for i in range(n):
+        m.moe_forward_profiled(wq, x, ids, tw, evs[i], out=out, ws=ws, flags=m.SCALES_PREVALIDATED)
+    torch.cuda.synchronize()
+    ms = sum(evs[i][2].elapsed_time(evs[i][3]) for i in range(n)) / n  # the a1-quantiser stage
+    R = T * k
+    nbytes = T * H * 2 + R * H * (0.5 + 1 / 16) + R * 8
+    pk = peaks()
+    return {"workload": "4096 tokens x 2816, 128 experts, uniform top-8, 1% outliers x50",
+            "ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+            "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "note": "bytes = x read once + codes and scales written + routing; the fused zeroing of the "
+                    "FP32 output (T*H*4 bytes) is extra traffic not counted"}
+
+
+def e2e_host(m, torch, w, layer, args):
+    T, H, k = layer.T, layer.H, layer.k
+    xh = torch.from_numpy(layer.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ih = torch.from_numpy(layer.topk_ids).pin_memory()
+    wh = torch.from_numpy(layer.topk_w).pin_memory()
+    oh = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    ws = torch.empty(m.moe_host_workspace_size(T, H, w.I, w.E, k), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        m.moe_forward_host(w, xh, ih, wh, out_host=oh, ws=ws, flags=m.SCALES_PREVALIDATED)
+    n = max(10, args.steps // 10)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(n):
+        m.moe_forward_host(w, xh, ih, wh, out_host=oh, ws=ws, flags=m.SCALES_PREVALIDATED)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    return {"value": T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": T * H * 2 + T * k * 8, "d2h_bytes_per_step": T * H * 4,
+            "entry_point": "nvfp4_moe_forward_host (pinned host buffers)"}
+
+
+# --------------------------------------------------------------------------- oracle arm
+def oracle_sample_setup(n_tokens: int):
+    """The oracle's inputs for a bounded sample of the prefill workload: the
+    first n_tokens tokens, oracle-quantised weights of the experts they use
+    (same N(0, 0.02) distribution, the generator's own draws), and a fixed
+    w2 input scale (the oracle's time does not depend on the scale values)."""
+    import oracle
+    layer = S.prefill()
+    toks = np.arange(n_tokens)
+    W = oracle.Weights(layer.E, layer.H, layer.I)
+    used = np.unique(layer.topk_ids[toks])
+    for e in used:
+        W.w13_q[e], W.w13_sf[e], W.w13_scale2[e] = oracle.quantize_weight(layer.weight_bf16(int(e), "w13"))
+        W.w2_q[e], W.w2_sf[e], W.w2_scale2[e] = oracle.quantize_weight(layer.weight_bf16(int(e), "w2"))
+    for e in range(layer.E):
+        if e not in used:
+            W.w13_scale2[e] = W.w2_scale2[e] = np.float32(1.0)
+    W.w13_input_scale = layer.w13_input_scale.copy()
+    W.w2_input_scale = np.full(layer.E, np.float32(16.0 / 2688.0))
+    return oracle, layer, W, toks
+
+
+def cpu_baseline(args):
+    orc, layer, W, toks = oracle_sample_setup(args.cpu_tokens)
+    t0 = time.perf_counter()
+    orc.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W, tokens=toks)
+    dt = time.perf_counter() - t0
+    return {"value": len(toks) / dt, "unit": "tokens/s", "cores": orc.threads(), "kind": "oracle",
+            "sample": f"{len(toks)} of 8192 prefill tokens ({len(toks) * layer.k} routed rows), whole expert "
+                      f"path, {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, as it stands, on the host cores; each
+    step is the whole expert path for a bounded token sample of the workload,
+    sized from a calibration run so that all steps take about two minutes."""
+    if rank != 0:
+        return None
+    orc, layer, W, toks = oracle_sample_setup(args.cpu_tokens)
+    t0 = time.perf_counter()
+    orc.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W, tokens=toks[:64])
+    rate = 64 / (time.perf_counter() - t0)
+    n = int(min(len(toks), max(8, rate * 120.0 / max(1, args.steps + args.warmup))))
+    toks = toks[:n]
+    for _ in range(args.warmup):
+        orc.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W, tokens=toks)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        orc.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W, tokens=toks)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = len(toks) / (ms * 1e-3)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int64 exact products, fp64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": layer.T, "E": layer.E, "H": layer.H, "I": layer.I,
+                       "k": layer.k, "sample_tokens_per_step": len(toks)},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": orc.threads(), "kind": "oracle",
+                             "sample": f"{len(toks)} of 8192 prefill tokens per step, whole expert path"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    line = run_reference(args, rank, world) if args.impl == "reference" else run_ours(args, rank, world)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

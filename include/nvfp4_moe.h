@@ -198,6 +198,18 @@ int nvfp4_moe_forward(const nvfp4_moe_weights *w, const void *prepared, const ui
                       size_t ws_bytes, unsigned flags, nvfp4_stream_t stream);
 
 /*
+ * nvfp4_moe_forward_profiled -- nvfp4_moe_forward that also records six
+ * caller-created CUDA events (events[i] is a cudaEvent_t) on `stream`:
+ * [0] before the scale check, [1] after it, [2] after the token reorder,
+ * [3] after the a1 quantiser, [4] after the w13 GEMM, [5] after the w2 GEMM,
+ * so that each stage's device time is the gap between consecutive events.
+ * A call that returns early records only the events before its exit point.
+ */
+int nvfp4_moe_forward_profiled(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x, int T,
+                               const int32_t *topk_ids, const float *topk_weights, int k, float *out, void *ws,
+                               size_t ws_bytes, unsigned flags, nvfp4_stream_t stream, void *const *events);
+
+/*
  * nvfp4_moe_forward_host -- the same layer with HOST activations and routing:
  * copies x_host [T, H] BF16, topk_ids_host [T, k], topk_weights_host [T, k]
  * into the workspace, runs nvfp4_moe_forward and copies out [T, H] FP32 back

@@ -72,6 +72,7 @@ def load():
             "nvfp4_prepare_weights": (I, [P, P, SZ, P]),
             "nvfp4_moe_workspace_size": (SZ, [I, I, I, I, I]),
             "nvfp4_moe_forward": (I, [P, P, P, I, P, P, I, P, P, SZ, U, P]),
+            "nvfp4_moe_forward_profiled": (I, [P, P, P, I, P, P, I, P, P, SZ, U, P, P]),
             "nvfp4_moe_host_workspace_size": (SZ, [I, I, I, I, I]),
             "nvfp4_moe_forward_host": (I, [P, P, P, I, P, P, I, P, P, SZ, U, P]),
             "nvfp4_moe_status": (I, [P, P, P]),
@@ -210,6 +211,26 @@ def moe_forward(w: MoEWeights, x: torch.Tensor, topk_ids: torch.Tensor, topk_wei
     _check(load().nvfp4_moe_forward(ctypes.byref(cw), _ptr(w.prepared), _ptr(x), T, _ptr(topk_ids),
                                     _ptr(topk_weights), k, _ptr(out), _ptr(ws), ws.numel(), flags, _stream(stream)))
     return out, ws
+
+
+STAGES = ("validate", "route", "quant_a1", "gemm_w13", "gemm_w2")
+
+
+def moe_forward_profiled(w: MoEWeights, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                         events, out: torch.Tensor, ws: torch.Tensor, flags: int = 0, stream=None):
+    """moe_forward recording six torch.cuda.Event (enable_timing) around its
+    stages on the launching stream; stage i lasts events[i] -> events[i + 1]."""
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    for e in events:  # torch creates the CUDA event on its first record
+        if e.cuda_event == 0:
+            e.record(stream)
+    arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    cw = w.cstruct()
+    _check(load().nvfp4_moe_forward_profiled(ctypes.byref(cw), _ptr(w.prepared), _ptr(x), T, _ptr(topk_ids),
+                                             _ptr(topk_weights), k, _ptr(out), _ptr(ws), ws.numel(), flags,
+                                             _stream(stream), arr))
+    return out
 
 
 def moe_forward_host(w: MoEWeights, x_host: torch.Tensor, topk_ids_host: torch.Tensor,

@@ -396,8 +396,11 @@ size_t nvfp4_moe_host_workspace_size(int T, int H, int I, int E, int k)
 
 static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x, int T,
                         const int32_t *ids, const float *topk_w, int k, float *out, void *ws, size_t ws_bytes,
-                        unsigned flags, cudaStream_t st)
+                        unsigned flags, cudaStream_t st, void *const *events = nullptr)
 {
+    auto mark = [&](int i) -> cudaError_t {
+        return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st) : cudaSuccess;
+    };
     int rc = check_weights(w);
     if (rc) return rc;
     rc = check_layer_shape(w->E, w->H, w->I, k);
@@ -436,7 +439,9 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     va.alpha1 = alpha1;
     va.alpha2 = alpha2;
     va.hdr = hdr;
+    NV_CUDA(mark(0), "recording an event");
     NV_CUDA(launch_validate(va, st), "launching the scale check");
+    NV_CUDA(mark(1), "recording an event");
     if (!(flags & NVFP4_SCALES_PREVALIDATED)) {
         DevHeader h;
         rc = read_header(hdr, st, &h);
@@ -463,6 +468,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     ra.padded = 1;
     ra.hdr = hdr;
     NV_CUDA(launch_route(ra, st), "launching the token reorder");
+    NV_CUDA(mark(2), "recording an event");
 
     QuantArgs qa;
     std::memset(&qa, 0, sizeof(qa));
@@ -480,6 +486,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     qa.zero_out = out;
     qa.hdr = hdr;
     NV_CUDA(launch_quant_experts(qa, st), "launching the a1 quantiser");
+    NV_CUDA(mark(3), "recording an event");
 
     const uint8_t *pw = static_cast<const uint8_t *>(prepared);
     GemmArgs ga;
@@ -510,6 +517,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     ga.hdr = hdr;
     ga.mtiles_cap = L.mtiles_cap;
     NV_CUDA(launch_gemm_w13(ga, st), "launching the w13 GEMM");
+    NV_CUDA(mark(4), "recording an event");
 
     GemmArgs gb = ga;
     gb.a_q = base + L.a2q;
@@ -527,6 +535,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     gb.topk_w = topk_w;
     gb.out = out;
     NV_CUDA(launch_gemm_w2(gb, st), "launching the w2 GEMM");
+    NV_CUDA(mark(5), "recording an event");
 
     if (flags & NVFP4_SYNC_CHECK) {
         DevHeader h;
@@ -543,6 +552,17 @@ int nvfp4_moe_forward(const nvfp4_moe_weights *w, const void *prepared, const ui
 {
     return forward_impl(w, prepared, x, T, topk_ids, topk_weights, k, out, ws, ws_bytes, flags,
                         (cudaStream_t)stream);
+}
+
+int nvfp4_moe_forward_profiled(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x, int T,
+                               const int32_t *topk_ids, const float *topk_weights, int k, float *out, void *ws,
+                               size_t ws_bytes, unsigned flags, nvfp4_stream_t stream, void *const *events)
+{
+    if (!events) return fail(NVFP4_ERR_INVALID_ARG, "events is null");
+    for (int i = 0; i < 6; ++i)
+        if (!events[i]) return fail(NVFP4_ERR_INVALID_ARG, "event %d is null", i);
+    return forward_impl(w, prepared, x, T, topk_ids, topk_weights, k, out, ws, ws_bytes, flags,
+                        (cudaStream_t)stream, events);
 }
 
 int nvfp4_moe_forward_host(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x_host, int T,

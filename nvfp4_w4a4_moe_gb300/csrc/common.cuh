@@ -15,7 +15,8 @@
 // correctly rounded y/s for every E4M3 divisor and every FP32 significand
 // (nvfp4_selftest_block_division); exponents only shift both sides, and
 // results that leave the normal range are far below the smallest E2M1 step or
-// saturate.  One FMUL + one FFMA replaces a full IEEE division per element.
+// saturate; zero dividends keep their sign.  One FMUL, one FFMA and a sign
+// copy replace a full IEEE division per element.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -75,9 +76,12 @@ __device__ __forceinline__ uint32_t e2m1_rn_sat4(float a, float b, float c, floa
 }
 
 // Correctly rounded y / s for an E4M3 divisor with constants z = (zh, zl).
+// The two-constant form loses the sign of a zero dividend when zl < 0
+// ((-0)*zl = +0, and -0 + +0 = +0); the quotient always has the dividend's
+// sign, so it is put back.
 __device__ __forceinline__ float div_by_scale(float y, float2 z)
 {
-    return __fmaf_rn(y, z.x, __fmul_rn(y, z.y));
+    return copysignf(__fmaf_rn(y, z.x, __fmul_rn(y, z.y)), y);
 }
 
 // One 16-element block: returns the 64-bit packed codes (element i in nibble
