@@ -131,6 +131,33 @@ int nvfp4_quantize_experts(const uint16_t *x, int T, int H, const int32_t *topk_
                            nvfp4_stream_t stream);
 
 /*
+ * nvfp4_quantize_experts_static_scratch -- nvfp4_quantize_experts for callers
+ * that cannot allocate device memory: a serving process whose memory pool has
+ * already claimed the device (a cudaMalloc would fail or fragment it), or a
+ * latency-critical path that must not call cudaMalloc / cudaFree because they
+ * can synchronise the device.  The page has no counterpart; this is an
+ * interface convenience of this library.
+ *
+ * Same arguments, outputs, checks and SYNCHRONOUS behaviour as
+ * nvfp4_quantize_experts, minus the workspace: the scratch is one static
+ * 4 MiB device array per GPU that loads the library, held until the process
+ * exits.  That covers nvfp4_quantize_workspace_size(T, k, E) <= 4 MiB (about
+ * 500,000 routed rows T*k with 128 experts); larger calls return
+ * NVFP4_ERR_WORKSPACE_TOO_SMALL and write nothing.  The library calls no
+ * cudaMalloc, cudaFree or other allocating routine on this path.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents (each call resets what it needs).  Calls whose work
+ *     overlaps on the GPU -- e.g. from two host threads or on two streams --
+ *     race on it and must be serialised by the caller.
+ */
+int nvfp4_quantize_experts_static_scratch(const uint16_t *x, int T, int H, const int32_t *topk_ids, int k, int E,
+                                          const float *input_scale, uint8_t *q_out, uint8_t *sf_out, int sf_layout,
+                                          int32_t *expert_offsets, int32_t *perm, nvfp4_stream_t stream);
+
+/*
  * Expert weights of one MoE layer, canonical (checkpoint) layout
  * [page, glossary "Static weight quantization": packed FP4 weight, E4M3
  * weight_scale, FP32 weight_scale_2; §矩阵融合 "Gated FFN": gate and up fused

@@ -68,6 +68,7 @@ def load():
             "nvfp4_validate_scales": (I, [P, P, I, P, P, P, P]),
             "nvfp4_quantize_workspace_size": (SZ, [I, I, I]),
             "nvfp4_quantize_experts": (I, [P, I, I, P, I, I, P, P, P, I, P, P, P, SZ, P]),
+            "nvfp4_quantize_experts_static_scratch": (I, [P, I, I, P, I, I, P, P, P, I, P, P, P]),
             "nvfp4_prepared_weights_size": (SZ, [I, I, I]),
             "nvfp4_prepare_weights": (I, [P, P, SZ, P]),
             "nvfp4_moe_workspace_size": (SZ, [I, I, I, I, I]),
@@ -151,6 +152,29 @@ def quantize_experts(x: torch.Tensor, topk_ids: torch.Tensor, input_scale: torch
     _check(load().nvfp4_quantize_experts(_ptr(x), T, H, _ptr(topk_ids), k, E, _ptr(input_scale), _ptr(q), _ptr(sf),
                                          sf_layout, _ptr(offsets), _ptr(perm), _ptr(ws), ws.numel(),
                                          _stream(stream)))
+    return q, sf, offsets, perm[:R]
+
+
+def quantize_experts_static_scratch(x: torch.Tensor, topk_ids: torch.Tensor, input_scale: torch.Tensor, E: int,
+                                    sf_layout: int = SF_LINEAR, stream=None):
+    """quantize_experts without a workspace: for callers that cannot allocate
+    device memory, the library's fixed per-device scratch array is used (see
+    nvfp4_quantize_experts_static_scratch in the C header for its limit and
+    the rule that overlapping calls race).  Outputs are still the caller's."""
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    R = T * k
+    dev = x.device
+    q = torch.empty((R, H // 2), dtype=torch.uint8, device=dev)
+    if sf_layout == SF_SWIZZLED:
+        sf = torch.empty(((R + 127) // 128) * ((H + 63) // 64) * 512, dtype=torch.uint8, device=dev)
+    else:
+        sf = torch.empty((R, H // 16), dtype=torch.uint8, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(max(R, 1), dtype=torch.int32, device=dev)
+    _check(load().nvfp4_quantize_experts_static_scratch(_ptr(x), T, H, _ptr(topk_ids), k, E, _ptr(input_scale),
+                                                        _ptr(q), _ptr(sf), sf_layout, _ptr(offsets), _ptr(perm),
+                                                        _stream(stream)))
     return q, sf, offsets, perm[:R]
 
 
