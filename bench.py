@@ -171,7 +171,7 @@ def run_ours(args, rank, world):
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    layer = S.prefill()
+    layer = S.prefill(args.tokens)
     T, H, I, E, k = layer.T, layer.H, layer.I, layer.E, layer.k
     w, _bf16 = make_layer_device(layer, m, torch, seed=1003 + 17 * rank)
     x = torch.from_numpy(layer.x.view(np.int16)).cuda().view(torch.bfloat16)
@@ -223,6 +223,11 @@ def run_ours(args, rank, world):
     ms_step = total_ms / K
     stage_ms = {name: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
                 for j, name in enumerate(m.STAGES)}
+
+    if args.only_layer:
+        return {"metric": METRIC, "value": T * world / (ms_step * 1e-3), "unit": "tokens/s", "n_gpus": world,
+                "steps": K, "warmup": W, "ms_per_step": ms_step, "config": {"T": T},
+                "kernels": {n: {"ms": v} for n, v in stage_ms.items()}, "note": "layer only (profiling run)"}
 
     # host-checked step (scale check synchronised on the host), for reference
     t0 = time.perf_counter()
@@ -421,6 +426,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=8192,
+                    help="prefill tokens (8192 is the benchmark workload; smaller values for ncu captures)")
+    ap.add_argument("--only-layer", action="store_true",
+                    help="time only the layer steps (no quantiser workload, e2e or CPU baseline)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))

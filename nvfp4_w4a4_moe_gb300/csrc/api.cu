@@ -66,16 +66,18 @@ static double e4m3_value(int b)
     return e == 0 ? std::ldexp((double)m, -9) : std::ldexp(8.0 + m, e - 10);
 }
 
-// zh = RN(1/s), zl = RN(1/s - zh) for each finite non-zero E4M3 scale s
-// (Brisebarre-Muller-Raina two-constant division; see common.cuh).
+// zh = 1/s rounded toward zero, zl = RN(1/s - zh) >= 0, for each finite
+// non-zero E4M3 scale s (two-constant division; see common.cuh).
 static DivTable build_div_table()
 {
     DivTable t;
     std::memset(&t, 0, sizeof(t));
     for (int b = 1; b <= 0x7E; ++b) {
         const double s = e4m3_value(b);
-        const float zh = (float)(1.0 / s);
-        const double rem = std::fma(-s, (double)zh, 1.0);  // exact: 1 - s*zh
+        const double r = 1.0 / s;  // 1/s = m * 2^e with m a short odd fraction; r is its nearest double
+        float zh = (float)r;
+        if ((double)zh > r) zh = std::nextafterf(zh, 0.0f);
+        const double rem = std::fma(-s, (double)zh, 1.0);  // exact: 1 - s*zh >= 0
         const float zl = (float)(rem / s);
         t.z[b] = make_float2(zh, zl);
     }
@@ -483,7 +485,6 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     qa.sf = base + L.sf1;
     qa.sf_swizzled = 1;
     qa.sf_kc = L.kc1;
-    qa.zero_out = out;
     qa.hdr = hdr;
     NV_CUDA(launch_quant_experts(qa, st), "launching the a1 quantiser");
     NV_CUDA(mark(3), "recording an event");
@@ -512,6 +513,8 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     ga.I = I;
     ga.kc2 = L.kc2;
     ga.h_dump = keep_h ? reinterpret_cast<float *>(base + L.host_end) : nullptr;
+    ga.zero_out = out;  // the w13 kernel clears out for the w2 kernel's reductions
+    ga.zero_floats = (long long)T * H;
     ga.k = k;
     ga.H = H;
     ga.hdr = hdr;
@@ -531,6 +534,8 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     gb.gate_up_I = 0;
     gb.alpha = alpha2;
     gb.h_dump = nullptr;
+    gb.zero_out = nullptr;
+    gb.zero_floats = 0;
     gb.row_src = ra.row_src;
     gb.topk_w = topk_w;
     gb.out = out;

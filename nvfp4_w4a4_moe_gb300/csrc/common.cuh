@@ -8,15 +8,17 @@
 //
 // Exact division by a block scale.  Both divisions above must be the correctly
 // rounded FP32 quotient.  The divisor s is one of 126 E4M3 values (and 6 is one
-// of them), so each division uses two per-divisor constants zh = RN(1/s) and
-// zl = RN(1/s - zh) and computes fma(y, zh, y * zl) -- the "division by a
-// constant known in advance" of Brisebarre, Muller and Raina (IEEE Trans.
-// Computers 53(8), 2004).  The host checks exhaustively that this equals the
-// correctly rounded y/s for every E4M3 divisor and every FP32 significand
-// (nvfp4_selftest_block_division); exponents only shift both sides, and
-// results that leave the normal range are far below the smallest E2M1 step or
-// saturate; zero dividends keep their sign.  One FMUL, one FFMA and a sign
-// copy replace a full IEEE division per element.
+// of them), so each division uses two per-divisor constants and computes
+// fma(y, zh, y * zl) -- the "division by a constant known in advance" of
+// Brisebarre, Muller and Raina (IEEE Trans. Computers 53(8), 2004), here with
+// zh = 1/s rounded toward zero and zl = RN(1/s - zh) >= 0.  With zl never
+// negative a zero dividend keeps its sign ((-0)*zl + (-0)*zh = -0), so the
+// quotient of -0 is -0 as IEEE division gives.  The host checks exhaustively
+// that this equals the correctly rounded y/s for every E4M3 divisor and every
+// FP32 significand (nvfp4_selftest_block_division); exponents only shift both
+// sides, and results that leave the normal range are far below the smallest
+// E2M1 step or saturate.  Two packed FP32x2 operations per pair of elements
+// (plus the x*g product) replace two full IEEE divisions.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -59,38 +61,57 @@ __device__ __forceinline__ uint32_t e4m3_rn_sat(float t)
     return (uint32_t)r & 0xFFu;
 }
 
-// RN, saturating FP32 -> E2M1 for four values: a in bits 0-3, b in 4-7,
-// c in 8-11, d in 12-15 (the x2 conversion puts its first source in the upper
-// nibble, so the pair (a, b) is passed as (b, a)).
-__device__ __forceinline__ uint32_t e2m1_rn_sat4(float a, float b, float c, float d)
+// Correctly rounded y / s for an E4M3 divisor with constants z = (zh, zl).
+__device__ __forceinline__ float div_by_scale(float y, float2 z)
 {
-    uint32_t r;
-    asm("{\n\t.reg .b8 ab, cd;\n\t.reg .b16 w;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 ab, %2, %1;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 cd, %4, %3;\n\t"
-        "mov.b16 w, {ab, cd};\n\t"
-        "cvt.u32.u16 %0, w;\n\t}"
-        : "=r"(r)
-        : "f"(a), "f"(b), "f"(c), "f"(d));
+    return __fmaf_rn(y, z.x, __fmul_rn(y, z.y));
+}
+
+// Packed FP32x2 arithmetic (one instruction, two IEEE round-to-nearest results).
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pr;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "mul.rn.f32x2 pr, pa, pb;\n\tmov.b64 {%0, %1}, pr;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c)
+{
+    float2 r;
+    asm("{\n\t.reg .b64 pa, pb, pc, pr;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+        "mov.b64 pc, {%6, %7};\n\tfma.rn.f32x2 pr, pa, pb, pc;\n\tmov.b64 {%0, %1}, pr;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
     return r;
 }
 
-// Correctly rounded y / s for an E4M3 divisor with constants z = (zh, zl).
-// The two-constant form loses the sign of a zero dividend when zl < 0
-// ((-0)*zl = +0, and -0 + +0 = +0); the quotient always has the dividend's
-// sign, so it is put back.
-__device__ __forceinline__ float div_by_scale(float y, float2 z)
+// Four quotient pairs -> 32 bits of codes (pair i in byte i, first element of
+// each pair in the low nibble).
+__device__ __forceinline__ uint32_t e2m1_rn_sat8(float2 a, float2 b, float2 c, float2 d)
 {
-    return copysignf(__fmaf_rn(y, z.x, __fmul_rn(y, z.y)), y);
+    uint32_t r;
+    asm("{\n\t.reg .b8 ba, bb, bc, bd;\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 ba, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 bb, %4, %3;\n\t"
+        "mov.b16 lo, {ba, bb};\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 bc, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 bd, %8, %7;\n\t"
+        "mov.b16 hi, {bc, bd};\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y), "f"(d.x), "f"(d.y));
+    return r;
 }
 
-// One 16-element block: returns the 64-bit packed codes (element i in nibble
-// i) and writes the E4M3 scale byte.  `amax` is max |x_i|; `g` the global
-// scale; `tab` the division table (any address space).
-__device__ __forceinline__ uint2 quant_block16(const float (&x)[16], float amax, float g,
-                                               const float2 *tab, uint32_t &sf_byte)
+// One 16-element block given as 8 pairs: returns the 64-bit packed codes
+// (element i in nibble i) and writes the E4M3 scale byte.  `amax` is
+// max |x_i|; `g` the global scale; `tab` the division table.
+__device__ __forceinline__ uint2 quant_block16(const float2 (&x)[8], float amax, float g, const float2 *tab,
+                                               uint32_t &sf_byte)
 {
-    float q[16];
+    float2 q[8];
     const float ga = __fmul_rn(g, amax);
     uint32_t sb;
     if (ga <= kFltMax) {
@@ -101,21 +122,22 @@ __device__ __forceinline__ uint2 quant_block16(const float (&x)[16], float amax,
             return make_uint2(0u, 0u);
         }
         const float2 z = tab[sb];
+        const float2 gg = make_float2(g, g), zh = make_float2(z.x, z.x), zl = make_float2(z.y, z.y);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) q[i] = div_by_scale(__fmul_rn(x[i], g), z);
+        for (int i = 0; i < 8; ++i) {
+            const float2 y = mul_f32x2(x[i], gg);
+            q[i] = fma_f32x2(y, zh, mul_f32x2(y, zl));
+        }
     } else {
         // g * amax overflowed: the scale saturates to 448 and the rare block
         // takes the plain IEEE division (infinite products stay infinite).
         sb = e4m3_rn_sat(__fdiv_rn(ga, 6.0f));
-        const float s = 448.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) q[i] = __fdiv_rn(__fmul_rn(x[i], g), s);
+        for (int i = 0; i < 8; ++i)
+            q[i] = make_float2(__fdiv_rn(__fmul_rn(x[i].x, g), 448.0f), __fdiv_rn(__fmul_rn(x[i].y, g), 448.0f));
     }
     sf_byte = sb;
-    uint2 r;
-    r.x = e2m1_rn_sat4(q[0], q[1], q[2], q[3]) | (e2m1_rn_sat4(q[4], q[5], q[6], q[7]) << 16);
-    r.y = e2m1_rn_sat4(q[8], q[9], q[10], q[11]) | (e2m1_rn_sat4(q[12], q[13], q[14], q[15]) << 16);
-    return r;
+    return make_uint2(e2m1_rn_sat8(q[0], q[1], q[2], q[3]), e2m1_rn_sat8(q[4], q[5], q[6], q[7]));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -59,7 +59,6 @@ struct QuantArgs {
     uint8_t *q;
     uint8_t *sf;
     int sf_swizzled, sf_kc;
-    float *zero_out;  // [T, H] FP32 zeroed on the way (nullable)
     const DevHeader *hdr;
 };
 cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st);
@@ -92,6 +91,8 @@ struct GemmArgs {
     uint8_t *a2q, *sf2;
     int I, kc2;
     float *h_dump;
+    float *zero_out;  // w13 kernel: [T, H] FP32 output zeroed by the epilogue warps before the first tile
+    long long zero_floats;
     // w2 epilogue (weighted combine)
     const int *row_src;
     const float *topk_w;

@@ -11,7 +11,7 @@
 //   pipeline figure: SiLU/mul + a2_gscale quantisation after w13, and the
 //   token order restored and summed with the routing weights after w2.
 //
-// Kernel shape (one persistent CTA per SM, 6 warps):
+// Kernel shape (one persistent CTA per SM, 10 warps):
 //   warp 0     TMA producer: A tile 128 rows x 256 FP4 (128-byte swizzle),
 //              B tile 128 rows x 256 FP4, and both 128x4-scale tiles (2 KB
 //              each, plain bulk copies) per stage into a 5-stage ring.
@@ -19,9 +19,12 @@
 //              8 scale chunks smem -> TMEM (tcgen05.cp 32x128b.warpx4) and
 //              issues 4 x tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
 //              (M128 N128 K64) into one of two FP32 accumulators.
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, then either
+//   warps 2-9  epilogue, two warps per TMEM lane quarter, each on half of the
+//              tile's columns: tcgen05.ld of the accumulator, then either
 //              SiLU(gate)*up + NVFP4 requantisation (w13) or the weighted
-//              scatter-add into the token-order output (w2).
+//              scatter-add into the token-order output (w2), transposed
+//              through shared memory so the FP32 reductions are coalesced.
+//              In the w13 kernel they first clear the output for w2.
 // Every wait is bounded (%globaltimer); on expiry the kernel records the
 // error in the workspace header, drains what it has in flight and exits.
 #include <climits>
@@ -40,7 +43,10 @@ constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + 2 * SF_BYTES;
 constexpr int ACC_COLS = BN;
 constexpr int SF_TMEM_COL = 2 * ACC_COLS;  // 32 columns per stage after the accumulators
 constexpr int TMEM_COLS = 512;
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 8;  // two per TMEM lane quarter, each on half of the tile's columns
+constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
+constexpr int NUM_THREADS = 64 + EPI_THREADS;
+constexpr int XPOSE_LD = 33;  // padded row of the per-warp 32 x 32 transpose buffer
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
@@ -51,7 +57,8 @@ constexpr int OFF_SFB = OFF_SFA + STAGES * SF_BYTES;
 constexpr int OFF_BAR = OFF_SFB + STAGES * SF_BYTES;
 constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+constexpr int OFF_XPOSE = (OFF_MISC + 16 + 15) & ~15;
+constexpr int SMEM_BYTES = OFF_XPOSE + NUM_EPI_WARPS * 32 * XPOSE_LD * 4 + 1024;  // + alignment slack
 
 // Instruction descriptor, block-scaled kinds: E2M1 A and B (code 1 at bits
 // 7-9 and 10-12), K-major both, N>>3 at 17-22, scale type UE4M3 (bit 23 = 0),
@@ -146,7 +153,7 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
         "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate), "r"(sfa), "r"(sfb)
         : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v)
 {
     uint32_t r[16];
     asm volatile(
@@ -166,7 +173,9 @@ __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, 
                  : "memory");
 }
 
-__device__ __forceinline__ float silu(float z) { return __fdiv_rn(z, 1.0f + expf(-z)); }
+// z * sigmoid(z) with the fast exponential and division (a few ulp; the
+// requantisation that follows is exact for whatever FP32 h results).
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(fminf(-z, 80.0f))); }
 
 // ---------------------------------------------------------------- kernel
 template <int EPI>  // 0: w13 (SiLU*up + requantise), 1: w2 (weighted combine)
@@ -199,7 +208,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], 128);
+            mbar_init(&acc_empty[i], EPI_THREADS);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -315,9 +324,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_wait(drain, 0, nullptr, kDrainLimitNs);
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue
-        const int quarter = warp & 3;
+        const int ew = warp - 2;          // 0..7
+        const int quarter = warp & 3;     // TMEM lanes this warp may read
+        const int half = ew >> 2;         // which half of the tile's columns it owns
         const int r_in = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        if (EPI == 0 && p.zero_out) {
+            // Clear the FP32 output for the w2 kernel's reductions while the
+            // first accumulator is being produced.
+            const long long active = min((long long)gridDim.x, (long long)ntiles);
+            const long long n4 = p.zero_floats >> 2;
+            float4 *z = reinterpret_cast<float4 *>(p.zero_out);
+            for (long long i = (long long)blockIdx.x * EPI_THREADS + (threadIdx.x - 64); i < n4;
+                 i += active * EPI_THREADS)
+                z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float *xp = reinterpret_cast<float *>(smem + OFF_XPOSE) + ew * 32 * XPOSE_LD;
         uint32_t acc = 0, acc_phase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
@@ -332,40 +354,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const uint32_t col0 = lane_base + acc * ACC_COLS;
             if (EPI == 0) {
-                // SiLU(gate) * up on the 64 columns of this tile, then the a2
-                // quantisation of the result (16-column blocks).
+                // SiLU(gate) * up on this warp's 32 of the tile's 64 h columns
+                // (gate columns 0..63 of the tile, up columns 64..127), then the
+                // a2 quantisation of the result, 16 columns per block.
                 const float alpha = p.alpha[e], g2 = p.g2[e];
+                const float2 aa = make_float2(alpha, alpha);
                 uint32_t sfw = 0;
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    float gate[16], up[16], h[16];
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int c = half * 2 + c2;
+                    float gate[16], up[16];
                     tmem_ld16(col0 + 16 * c, gate);
                     tmem_ld16(col0 + 64 + 16 * c, up);
                     tmem_wait_ld();
+                    float2 h[8];
                     float amax = 0.0f;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        h[i] = __fmul_rn(silu(__fmul_rn(gate[i], alpha)), __fmul_rn(up[i], alpha));
-                        amax = fmaxf(amax, fabsf(h[i]));
+                    for (int i = 0; i < 8; ++i) {
+                        const float2 gs = mul_f32x2(make_float2(gate[2 * i], gate[2 * i + 1]), aa);
+                        const float2 us = mul_f32x2(make_float2(up[2 * i], up[2 * i + 1]), aa);
+                        h[i] = mul_f32x2(make_float2(silu(gs.x), silu(gs.y)), us);
+                        amax = fmaxf(amax, fmaxf(fabsf(h[i].x), fabsf(h[i].y)));
                     }
                     if (p.h_dump && valid) {
                         float4 *hd = reinterpret_cast<float4 *>(p.h_dump + (size_t)row * p.I + nt * 64 + 16 * c);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) hd[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i) hd[i] = make_float4(h[2 * i].x, h[2 * i].y, h[2 * i + 1].x, h[2 * i + 1].y);
                     }
                     uint32_t sb;
                     const uint2 pk = quant_block16(h, amax, g2, tab, sb);
                     if (valid) *reinterpret_cast<uint2 *>(p.a2q + (size_t)row * (p.I >> 1) + nt * 32 + 8 * c) = pk;
-                    sfw |= sb << (8 * c);
+                    sfw |= sb << (8 * c2);
                 }
                 if (valid) {
-                    *reinterpret_cast<uint32_t *>(p.sf2 + swz_sf_offset(row, nt, p.kc2)) = sfw;
-                    if (nt == NT - 1)
+                    *reinterpret_cast<uint16_t *>(p.sf2 + swz_sf_offset(row, nt, p.kc2) + 2 * half) = (uint16_t)sfw;
+                    if (nt == NT - 1 && half == 0)
                         for (int cc = NT; cc < p.kc2; ++cc)
                             *reinterpret_cast<uint32_t *>(p.sf2 + swz_sf_offset(row, cc, p.kc2)) = 0u;
                 }
             } else {
-                // out[t, cols] += w[t, j] * alpha2 * y2 (scatter back to token order)
+                // out[t, cols] += w[t, j] * alpha2 * y2: this warp's 64 columns,
+                // 32 at a time, transposed through shared memory so that each
+                // reduction instruction covers four contiguous 128-byte row
+                // segments.
                 int t = 0;
                 float scale = 0.0f;
                 if (valid) {
@@ -373,18 +404,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     t = f / p.k;
                     scale = __fmul_rn(p.topk_w[f], p.alpha[e]);
                 }
-                float *dst = p.out + (size_t)t * p.H + nt * BN;
+                const int sub = lane >> 3, cc = (lane & 7) * 4;
 #pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
-                    float v[16];
-                    tmem_ld16(col0 + 16 * c, v);
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int cbase = 64 * half + 32 * c2;
+                    float v[32];
+                    tmem_ld16(col0 + cbase, v);
+                    tmem_ld16(col0 + cbase + 16, v + 16);
                     tmem_wait_ld();
-                    if (valid) {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            red_add_v4(dst + 16 * c + 4 * i, v[4 * i] * scale, v[4 * i + 1] * scale,
-                                       v[4 * i + 2] * scale, v[4 * i + 3] * scale);
+                    for (int i = 0; i < 32; ++i) xp[lane * XPOSE_LD + i] = v[i] * scale;
+                    __syncwarp();
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = it * 4 + sub;
+                        const int t_r = __shfl_sync(0xffffffffu, t, rr);
+                        const int ok_r = __shfl_sync(0xffffffffu, (int)valid, rr);
+                        const float *src = xp + rr * XPOSE_LD + cc;
+                        if (ok_r)
+                            red_add_v4(p.out + (size_t)t_r * p.H + nt * BN + cbase + cc, src[0], src[1], src[2], src[3]);
                     }
+                    __syncwarp();
                 }
             }
             tc_fence_before();

@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(256) quant_experts_kernel(QuantArgs a, DivTabl
         const bool valid = idx < total;
         const int t = valid ? (int)(idx / nb) : 0;
         const int b = valid ? (int)(idx - (long long)t * nb) : 0;
-        float x[16];
+        float2 x[8];
         float amax = 0.0f;
         if (valid) {
             const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + (size_t)b * 16);
@@ -220,22 +220,12 @@ __global__ void __launch_bounds__(256) quant_experts_kernel(QuantArgs a, DivTabl
             const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                x[2 * i] = bf16_lo(w[i]);
-                x[2 * i + 1] = bf16_hi(w[i]);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-            if (a.zero_out) {
-                float4 *z = reinterpret_cast<float4 *>(a.zero_out + (size_t)t * a.H + (size_t)b * 16);
-                const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-                z[0] = zero;
-                z[1] = zero;
-                z[2] = zero;
-                z[3] = zero;
+                x[i] = make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
+                amax = fmaxf(amax, fmaxf(fabsf(x[i].x), fabsf(x[i].y)));
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = 0.0f;
+            for (int i = 0; i < 8; ++i) x[i] = make_float2(0.0f, 0.0f);
         }
         for (int j = 0; j < a.k; ++j) {
             int row = 0;
@@ -368,13 +358,14 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t *w, in
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
         const int n = (int)(i / nb), b = (int)(i - (long long)n * nb);
-        float x[16];
+        float2 x[8];
         float amax = 0.0f;
-        const uint16_t *p = src + (size_t)n * K + (size_t)b * 16;
+        const uint32_t *p = reinterpret_cast<const uint32_t *>(src + (size_t)n * K + (size_t)b * 16);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            x[j] = __uint_as_float((uint32_t)p[j] << 16);
-            amax = fmaxf(amax, fabsf(x[j]));
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t wv = p[j];
+            x[j] = make_float2(bf16_lo(wv), bf16_hi(wv));
+            amax = fmaxf(amax, fmaxf(fabsf(x[j].x), fabsf(x[j].y)));
         }
         uint32_t sb = 0;
         uint2 pk = make_uint2(0u, 0u);
