@@ -152,7 +152,7 @@ def algorithmic(layer, n_active):
     return {
         "validate": {"bytes": 4 * 4 * E},
         "route": {"bytes": R * 4 * 3 + R * 4},
-        "quant_a1": {"bytes": T * H * 2 + R * H * fp4 + R * 4 * 2 + T * H * 4},
+        "quant_a1": {"bytes": T * H * 2 + R * H * fp4 + R * 4 * 2},
         "gemm_w13": {"bytes": R * H * fp4 + n_active * 2 * I * H * fp4 + R * I * fp4,
                      "flops": 2.0 * R * 2 * I * H},
         "gemm_w2": {"bytes": R * I * fp4 + n_active * H * I * fp4 + T * H * 4, "flops": 2.0 * R * H * I},
@@ -327,8 +327,7 @@ def quant_workload(m, torch, w, args):
     return {"workload": "4096 tokens x 2816, 128 experts, uniform top-8, 1% outliers x50",
             "ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
             "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
-            "note": "bytes = x read once + codes and scales written + routing; the fused zeroing of the "
-                    "FP32 output (T*H*4 bytes) is extra traffic not counted"}
+            "note": "bytes = x read once + codes and scales written + routing reads"}
 
 
 def e2e_host(m, torch, w, layer, args):

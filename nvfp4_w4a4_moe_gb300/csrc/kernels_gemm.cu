@@ -14,7 +14,8 @@
 // Kernel shape (one persistent CTA per SM, 10 warps):
 //   warp 0     TMA producer: A tile 128 rows x 256 FP4 (128-byte swizzle),
 //              B tile 128 rows x 256 FP4, and both 128x4-scale tiles (2 KB
-//              each, plain bulk copies) per stage into a 5-stage ring.
+//              each, plain bulk copies) per stage into a 6-stage (w13) or
+//              5-stage (w2) ring.
 //   warp 1     TMEM owner (512 columns) and MMA issuer: per stage, copies the
 //              8 scale chunks smem -> TMEM (tcgen05.cp 32x128b.warpx4) and
 //              issues 4 x tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
@@ -35,30 +36,44 @@ namespace nvfp4 {
 namespace {
 
 constexpr int BM = 128, BN = 128, BK = 256;  // BK in FP4 elements (128 bytes per row)
-constexpr int STAGES = 5;
 constexpr int A_BYTES = BM * BK / 2;
 constexpr int B_BYTES = BN * BK / 2;
 constexpr int SF_BYTES = 4 * 512;  // four 128x4-scale tiles = 256 K per stage
 constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + 2 * SF_BYTES;
 constexpr int ACC_COLS = BN;
-constexpr int SF_TMEM_COL = 2 * ACC_COLS;  // 32 columns per stage after the accumulators
+constexpr int SF_TMEM_COL = 2 * ACC_COLS;  // 32 scale columns per stage after the accumulators
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;  // two per TMEM lane quarter, each on half of the tile's columns
 constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
-constexpr int NUM_THREADS = 64 + EPI_THREADS;
+constexpr int COPY_WARP = 2 + NUM_EPI_WARPS;  // issues the smem -> TMEM scale copies
+constexpr int NUM_THREADS = 64 + EPI_THREADS + 32;
 constexpr int XPOSE_LD = 33;  // padded row of the per-warp 32 x 32 transpose buffer
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-constexpr int OFF_SFB = OFF_SFA + STAGES * SF_BYTES;
-constexpr int OFF_BAR = OFF_SFB + STAGES * SF_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 4 + 1;
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int OFF_XPOSE = (OFF_MISC + 16 + 15) & ~15;
-constexpr int SMEM_BYTES = OFF_XPOSE + NUM_EPI_WARPS * 32 * XPOSE_LD * 4 + 1024;  // + alignment slack
+// Shared-memory plan per kernel: the w13 kernel spends it all on a 6-stage
+// ring (the loads of a stage take longer than its MMAs, so more bytes in
+// flight hide more latency); the w2 kernel keeps 5 stages and a transpose
+// buffer for its epilogue.
+#ifndef NVFP4_W13_STAGES
+#define NVFP4_W13_STAGES 6
+#endif
+template <int EPI>
+struct Plan {
+    static constexpr int STAGES = EPI == 0 ? NVFP4_W13_STAGES : 5;
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SF_BYTES;
+    static constexpr int OFF_BAR = OFF_SFB + STAGES * SF_BYTES;
+    static constexpr int NUM_BARS = 3 * STAGES + 4 + 2;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_XPOSE = (OFF_MISC + 16 + 15) & ~15;
+    static constexpr int XPOSE_BYTES = EPI == 1 ? NUM_EPI_WARPS * 32 * XPOSE_LD * 4 : 0;
+    static constexpr int SMEM_BYTES = OFF_XPOSE + XPOSE_BYTES + 1024;  // + alignment slack
+    static_assert(SF_TMEM_COL + STAGES * 32 <= TMEM_COLS, "scale slots exceed TMEM");
+    static_assert(SMEM_BYTES + 1024 <= 232448, "shared memory plan exceeds the opt-in limit");
+};
 
 // Instruction descriptor, block-scaled kinds: E2M1 A and B (code 1 at bits
 // 7-9 and 10-12), K-major both, N>>3 at 17-22, scale type UE4M3 (bit 23 = 0),
@@ -183,12 +198,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const GemmArgs p, const DivTable tab_in)
 {
+    using P = Plan<EPI>;
+    constexpr int STAGES = P::STAGES, OFF_A = P::OFF_A, OFF_B = P::OFF_B, OFF_SFA = P::OFF_SFA,
+                  OFF_SFB = P::OFF_SFB, OFF_BAR = P::OFF_BAR, OFF_MISC = P::OFF_MISC, OFF_XPOSE = P::OFF_XPOSE;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ float2 tab[128];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint64_t *full = bars, *empty = bars + STAGES, *acc_full = bars + 2 * STAGES,
-             *acc_empty = bars + 2 * STAGES + 2, *drain = bars + 2 * STAGES + 4;
+             *acc_empty = bars + 2 * STAGES + 2, *drain = bars + 2 * STAGES + 4, *sf_ready = bars + 2 * STAGES + 5,
+             *drain_cp = bars + 3 * STAGES + 5;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
@@ -205,7 +224,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_ready[s], 1);
         }
+        mbar_init(drain_cp, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], EPI_THREADS);
@@ -284,7 +305,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             const uint32_t d = tmem + acc * ACC_COLS;
             for (int kt = 0; kt < KT; ++kt) {
-                if (!mbar_wait(&full[stage], phase, abort_flag, kWaitLimitNs)) {
+                // operands landed (full) and their scales are in TMEM (sf_ready)
+                if (!mbar_wait(&full[stage], phase, abort_flag, kWaitLimitNs) ||
+                    !mbar_wait(&sf_ready[stage], phase, abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
@@ -293,12 +316,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t sfa_t = tmem + SF_TMEM_COL + stage * 32, sfb_t = sfa_t + 16;
                 const uint32_t sa = su32(smem + OFF_A + stage * A_BYTES);
                 const uint32_t sb = su32(smem + OFF_B + stage * B_BYTES);
-                const uint32_t ssfa = su32(smem + OFF_SFA + stage * SF_BYTES);
-                const uint32_t ssfb = su32(smem + OFF_SFB + stage * SF_BYTES);
-                for (int j = 0; j < ksteps; ++j) {
-                    tc_cp_sf(sfa_t + 4 * j, desc_sf(ssfa + 512 * j));
-                    tc_cp_sf(sfb_t + 4 * j, desc_sf(ssfb + 512 * j));
-                }
                 for (int j = 0; j < ksteps; ++j)
                     tc_mma(d, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j), sfa_t + 4 * j, sfb_t + 4 * j,
                            (kt | j) != 0);
@@ -322,7 +339,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Drain: all issued tcgen05 work completes before TMEM is released.
         tc_commit(drain);
         mbar_wait(drain, 0, nullptr, kDrainLimitNs);
-    } else if (warp >= 2) {
+    } else if (warp == COPY_WARP && lane == 0) {
+        // ------------------------------------------------ scale copier
+        // Moves each stage's scale tiles smem -> TMEM (tcgen05.cp
+        // 32x128b.warpx4, one per K step and operand) ahead of the MMA issuer,
+        // and signals sf_ready[stage] when the copies have completed.  The
+        // stage's TMEM scale slot is only rewritten after the producer has
+        // refilled the stage, i.e. after the MMAs that read it have finished.
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            for (int kt = 0; kt < KT; ++kt) {
+                if (!mbar_wait(&full[stage], phase, abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int ksteps = min(4, (p.K - kt * BK + 63) / 64);
+                const uint32_t sfa_t = tmem + SF_TMEM_COL + stage * 32, sfb_t = sfa_t + 16;
+                const uint32_t ssfa = su32(smem + OFF_SFA + stage * SF_BYTES);
+                const uint32_t ssfb = su32(smem + OFF_SFB + stage * SF_BYTES);
+                for (int j = 0; j < ksteps; ++j) {
+                    tc_cp_sf(sfa_t + 4 * j, desc_sf(ssfa + 512 * j));
+                    tc_cp_sf(sfb_t + 4 * j, desc_sf(ssfb + 512 * j));
+                }
+                tc_commit(&sf_ready[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            atomicOr(&p.hdr->error_flags, kErrTimeoutMma);
+        }
+        tc_commit(drain_cp);
+        mbar_wait(drain_cp, 0, nullptr, kDrainLimitNs);
+    } else if (warp >= 2 && warp < COPY_WARP) {
         // ------------------------------------------------ epilogue
         const int ew = warp - 2;          // 0..7
         const int quarter = warp & 3;     // TMEM lanes this warp may read
@@ -498,8 +552,8 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
 {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t err =
-            cudaFuncSetAttribute(moe_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               Plan<EPI>::SMEM_BYTES);
         if (err != cudaSuccess) return err;
         attr_set = true;
     }
@@ -511,7 +565,7 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
     const long long tiles = (long long)a.mtiles_cap * (a.N / BN);
     int grid = sm_count();
     if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
-    moe_gemm_kernel<EPI><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, a, div_table());
+    moe_gemm_kernel<EPI><<<grid, NUM_THREADS, Plan<EPI>::SMEM_BYTES, st>>>(ma, mb, a, div_table());
     return cudaGetLastError();
 }
 
