@@ -102,29 +102,56 @@ __global__ void __launch_bounds__(256) route_hist_kernel(RouteArgs a)
     int *cnt = sh;            // [E]
     int *off = sh + E;        // [E + 1]
     int *poff = sh + 2 * E + 1;  // [E + 1]
+    // Per expert, exclusive prefix over the chunks.  The chunk counts are all
+    // loaded before any is rewritten, so the loads overlap instead of forming
+    // a chain of dependent round trips.
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = 0;
-        for (int c = 0; c < a.nchunks; ++c) {
-            int *p = &a.chunk_hist[(size_t)c * E + e];
-            const int v = __ldcg(p);
-            *p = run;
-            run += v;
+        for (int c0 = 0; c0 < a.nchunks; c0 += 16) {
+            int v[16];
+            const int n = min(16, a.nchunks - c0);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = i < n ? __ldcg(&a.chunk_hist[(size_t)(c0 + i) * E + e]) : 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (i < n) a.chunk_hist[(size_t)(c0 + i) * E + e] = run;
+                run += v[i];
+            }
         }
         cnt[e] = run;
         a.counts[e] = run;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int o = 0, po = 0;
-        for (int e = 0; e < E; ++e) {
-            off[e] = o;
-            poff[e] = po;
-            o += cnt[e];
-            po += (cnt[e] + 127) & ~127;
+    // Exclusive scans over experts (compact, and padded to 128-row tiles) by
+    // warp 0, 32 experts per step.
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int base_o = 0, base_p = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            const int c = e < E ? cnt[e] : 0;
+            const int cp = (c + 127) & ~127;
+            int io = c, ip = cp;  // inclusive warp scans
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int to = __shfl_up_sync(0xffffffffu, io, o), tp = __shfl_up_sync(0xffffffffu, ip, o);
+                if (lane >= o) {
+                    io += to;
+                    ip += tp;
+                }
+            }
+            if (e < E) {
+                off[e] = base_o + io - c;
+                poff[e] = base_p + ip - cp;
+            }
+            base_o += __shfl_sync(0xffffffffu, io, 31);
+            base_p += __shfl_sync(0xffffffffu, ip, 31);
         }
-        off[E] = o;
-        poff[E] = po;
-        a.hdr->num_mtiles = po >> 7;
+        if (lane == 0) {
+            off[E] = base_o;
+            poff[E] = base_p;
+            a.hdr->num_mtiles = base_p >> 7;
+        }
     }
     __syncthreads();
     for (int e = threadIdx.x; e <= E; e += blockDim.x) {
@@ -132,11 +159,28 @@ __global__ void __launch_bounds__(256) route_hist_kernel(RouteArgs a)
         a.pad_off[e] = poff[e];
         if (a.offsets_out) a.offsets_out[e] = off[e];
     }
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        if (a.tile_expert)
-            for (int m = poff[e] >> 7; m < (poff[e + 1] >> 7); ++m) a.tile_expert[m] = e;
-        if (a.row_src)
-            for (int r = poff[e] + cnt[e]; r < poff[e + 1]; ++r) a.row_src[r] = -1;
+    // m-tile -> expert map: every thread takes m-tiles and finds the expert
+    // whose padded range holds the tile (binary search over the offsets).
+    if (a.tile_expert) {
+        const int ntile = poff[E] >> 7;
+        for (int mtile = threadIdx.x; mtile < ntile; mtile += blockDim.x) {
+            const int row = mtile << 7;
+            int lo = 0, hi = E - 1;  // last e with poff[e] <= row
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (poff[mid] <= row)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            a.tile_expert[mtile] = lo;
+        }
+    }
+    // padding rows of each expert's last tile: one warp per expert at a time
+    if (a.row_src) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+        for (int e = warp; e < E; e += nwarps)
+            for (int r = poff[e] + cnt[e] + lane; r < poff[e + 1]; r += 32) a.row_src[r] = -1;
     }
 }
 
@@ -194,8 +238,11 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(RouteArgs a)
 // [page, §NVFP4 runtime-order figure; MoE section: SFScale[expert_idx]]:
 // one thread per (token, 16-element block).  The block's BF16 values and amax
 // are read once and quantised for each of the token's k experts with that
-// expert's global scale, into the expert's permuted row.  Four lanes pack
-// their four scale bytes into one 32-bit store.
+// expert's global scale, into the expert's permuted row.  The token's k
+// destination rows and global scales are loaded up front (KMAX >= k, so the
+// expert loop unrolls and its loads overlap); four lanes pack their four
+// scale bytes into one 32-bit store.
+template <int KMAX>
 __global__ void __launch_bounds__(256) quant_experts_kernel(QuantArgs a, DivTable tab_in)
 {
     __shared__ float2 tab[128];
@@ -203,15 +250,31 @@ __global__ void __launch_bounds__(256) quant_experts_kernel(QuantArgs a, DivTabl
     __syncthreads();
     if (a.hdr && a.hdr->status != 0) return;
     const int nb = a.H >> 4;
+    const int k = a.k;
     const long long total = (long long)a.T * nb;
     const int lane = threadIdx.x & 31;
     const long long warp_stride = (long long)gridDim.x * blockDim.x;
+    const int32_t *__restrict__ ids = a.ids;
+    const int *__restrict__ row_of = a.row_of;
+    const float *__restrict__ gsc = a.g;
     for (long long wbase = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); wbase < total;
          wbase += warp_stride) {
         const long long idx = wbase + lane;
         const bool valid = idx < total;
         const int t = valid ? (int)(idx / nb) : 0;
         const int b = valid ? (int)(idx - (long long)t * nb) : 0;
+        int rows[KMAX];
+        float gs[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            rows[j] = 0;
+            gs[j] = 1.0f;
+            if (j < k && valid) {
+                const int f = t * k + j;
+                rows[j] = __ldg(row_of + f);
+                gs[j] = __ldg(gsc + __ldg(ids + f));
+            }
+        }
         float2 x[8];
         float amax = 0.0f;
         if (valid) {
@@ -227,21 +290,17 @@ __global__ void __launch_bounds__(256) quant_experts_kernel(QuantArgs a, DivTabl
 #pragma unroll
             for (int i = 0; i < 8; ++i) x[i] = make_float2(0.0f, 0.0f);
         }
-        for (int j = 0; j < a.k; ++j) {
-            int row = 0;
-            float g = 1.0f;
-            if (valid) {
-                const int f = t * a.k + j;
-                row = a.row_of[f];
-                g = a.g[a.ids[f]];
-            }
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            if (j >= k) break;
             uint32_t sb;
-            const uint2 pk = quant_block16(x, amax, g, tab, sb);
+            const uint2 pk = quant_block16(x, amax, gs[j], tab, sb);
             uint32_t word = sb;
             word |= __shfl_down_sync(0xffffffffu, sb, 1) << 8;
             word |= __shfl_down_sync(0xffffffffu, sb, 2) << 16;
             word |= __shfl_down_sync(0xffffffffu, sb, 3) << 24;
             if (valid) {
+                const int row = rows[j];
                 *reinterpret_cast<uint2 *>(a.q + (size_t)row * (a.H >> 1) + (size_t)b * 8) = pk;
                 if ((b & 3) == 0) {
                     uint8_t *dst = a.sf_swizzled ? a.sf + swz_sf_offset(row, b >> 2, a.sf_kc)
@@ -406,7 +465,17 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t st)
 cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st)
 {
     const long long work = (long long)a.T * (a.H >> 4);
-    quant_experts_kernel<<<grid_for(work, 256, 8), 256, 0, st>>>(a, div_table());
+    const int grid = grid_for(work, 256, 8);
+    if (a.k <= 1)
+        quant_experts_kernel<1><<<grid, 256, 0, st>>>(a, div_table());
+    else if (a.k <= 2)
+        quant_experts_kernel<2><<<grid, 256, 0, st>>>(a, div_table());
+    else if (a.k <= 4)
+        quant_experts_kernel<4><<<grid, 256, 0, st>>>(a, div_table());
+    else if (a.k <= 8)
+        quant_experts_kernel<8><<<grid, 256, 0, st>>>(a, div_table());
+    else
+        quant_experts_kernel<32><<<grid, 256, 0, st>>>(a, div_table());
     return cudaGetLastError();
 }
 
