@@ -67,66 +67,93 @@ __device__ __forceinline__ float div_by_scale(float y, float2 z)
     return __fmaf_rn(y, z.x, __fmul_rn(y, z.y));
 }
 
-// Packed FP32x2 arithmetic (one instruction, two IEEE round-to-nearest results).
-__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b)
+// Packed FP32x2 arithmetic on 64-bit register pairs (one instruction, two
+// IEEE round-to-nearest results); element 0 in the low half.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pack_f32x2(float lo, float hi)
 {
-    float2 r;
-    asm("{\n\t.reg .b64 pa, pb, pr;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
-        "mul.rn.f32x2 pr, pa, pb;\n\tmov.b64 {%0, %1}, pr;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
     return r;
 }
-__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c)
+__device__ __forceinline__ f32x2 mul_f32x2(f32x2 a, f32x2 b)
 {
-    float2 r;
-    asm("{\n\t.reg .b64 pa, pb, pc, pr;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
-        "mov.b64 pc, {%6, %7};\n\tfma.rn.f32x2 pr, pa, pb, pc;\n\tmov.b64 {%0, %1}, pr;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    f32x2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
     return r;
+}
+__device__ __forceinline__ f32x2 fma_f32x2(f32x2 a, f32x2 b, f32x2 c)
+{
+    f32x2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ float lo_f32(f32x2 v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi_f32(f32x2 v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
+// Two BF16 values (one 32-bit word, element 0 in the low half) widened to FP32.
+__device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w)
+{
+    return ((f32x2)(w & 0xFFFF0000u) << 32) | (f32x2)(w << 16);
 }
 
-// Four quotient pairs -> 32 bits of codes (pair i in byte i, first element of
-// each pair in the low nibble).
-__device__ __forceinline__ uint32_t e2m1_rn_sat8(float2 a, float2 b, float2 c, float2 d)
+// Four quotient pairs -> 32 bits of codes (pair i in byte i, the low element
+// of each pair in the low nibble).
+__device__ __forceinline__ uint32_t e2m1_rn_sat8(f32x2 a, f32x2 b, f32x2 c, f32x2 d)
 {
     uint32_t r;
-    asm("{\n\t.reg .b8 ba, bb, bc, bd;\n\t.reg .b16 lo, hi;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 ba, %2, %1;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 bb, %4, %3;\n\t"
+    asm("{\n\t.reg .f32 a0, a1, b0, b1, c0, c1, d0, d1;\n\t.reg .b8 ba, bb, bc, bd;\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b64 {a0, a1}, %1;\n\tmov.b64 {b0, b1}, %2;\n\tmov.b64 {c0, c1}, %3;\n\tmov.b64 {d0, d1}, %4;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 ba, a1, a0;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 bb, b1, b0;\n\t"
         "mov.b16 lo, {ba, bb};\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 bc, %6, %5;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 bd, %8, %7;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 bc, c1, c0;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 bd, d1, d0;\n\t"
         "mov.b16 hi, {bc, bd};\n\t"
         "mov.b32 %0, {lo, hi};\n\t}"
         : "=r"(r)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y), "f"(d.x), "f"(d.y));
+        : "l"(a), "l"(b), "l"(c), "l"(d));
     return r;
+}
+
+// The division table in the form the kernels keep in shared memory: the two
+// constants of each E4M3 divisor duplicated into FP32x2 pairs, and those of 6.
+struct DivTable2 {
+    ulonglong2 z[128];
+    float2 six;
+};
+__device__ __forceinline__ void load_div_table(DivTable2 *dst, const DivTable &src)
+{
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+        const float2 z = src.z[i];
+        dst->z[i] = make_ulonglong2(pack_f32x2(z.x, z.x), pack_f32x2(z.y, z.y));
+    }
+    if (threadIdx.x == 0) dst->six = src.z[kE4M3Six];
 }
 
 // One 16-element block given as 8 pairs: returns the 64-bit packed codes
 // (element i in nibble i) and writes the E4M3 scale byte.  `amax` is
 // max |x_i|; `g` the global scale; `tab` the division table.
-__device__ __forceinline__ uint2 quant_block16(const float2 (&x)[8], float amax, float g, const float2 *tab,
+__device__ __forceinline__ uint2 quant_block16(const f32x2 (&x)[8], float amax, float g, const DivTable2 *tab,
                                                uint32_t &sf_byte)
 {
-    float2 q[8];
+    f32x2 q[8];
     const float ga = __fmul_rn(g, amax);
     uint32_t sb;
     if (ga <= kFltMax) {
-        const float t = div_by_scale(ga, tab[kE4M3Six]);  // fl(ga / 6)
+        const float t = div_by_scale(ga, tab->six);  // fl(ga / 6)
         sb = e4m3_rn_sat(t);
         if (sb == 0) {
             sf_byte = 0;
             return make_uint2(0u, 0u);
         }
-        const float2 z = tab[sb];
-        const float2 gg = make_float2(g, g), zh = make_float2(z.x, z.x), zl = make_float2(z.y, z.y);
+        const ulonglong2 z = tab->z[sb];  // (zh, zh), (zl, zl)
+        const f32x2 gg = pack_f32x2(g, g);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float2 y = mul_f32x2(x[i], gg);
-            q[i] = fma_f32x2(y, zh, mul_f32x2(y, zl));
+            const f32x2 y = mul_f32x2(x[i], gg);
+            q[i] = fma_f32x2(y, z.x, mul_f32x2(y, z.y));
         }
     } else {
         // g * amax overflowed: the scale saturates to 448 and the rare block
@@ -134,7 +161,7 @@ __device__ __forceinline__ uint2 quant_block16(const float2 (&x)[8], float amax,
         sb = e4m3_rn_sat(__fdiv_rn(ga, 6.0f));
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            q[i] = make_float2(__fdiv_rn(__fmul_rn(x[i].x, g), 448.0f), __fdiv_rn(__fmul_rn(x[i].y, g), 448.0f));
+            q[i] = pack_f32x2(__fdiv_rn(__fmul_rn(lo_f32(x[i]), g), 448.0f), __fdiv_rn(__fmul_rn(hi_f32(x[i]), g), 448.0f));
     }
     sf_byte = sb;
     return make_uint2(e2m1_rn_sat8(q[0], q[1], q[2], q[3]), e2m1_rn_sat8(q[4], q[5], q[6], q[7]));

@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int STAGES = P::STAGES, OFF_A = P::OFF_A, OFF_B = P::OFF_B, OFF_SFA = P::OFF_SFA,
                   OFF_SFB = P::OFF_SFB, OFF_BAR = P::OFF_BAR, OFF_MISC = P::OFF_MISC, OFF_XPOSE = P::OFF_XPOSE;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ float2 tab[128];
+    __shared__ DivTable2 tab;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint64_t *full = bars, *empty = bars + STAGES, *acc_full = bars + 2 * STAGES,
@@ -218,8 +218,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if ((int)blockIdx.x >= ntiles) return;
     const int KT = (p.K + BK - 1) / BK;
 
-    if (EPI == 0)
-        for (int i = threadIdx.x; i < 128; i += NUM_THREADS) tab[i] = tab_in.z[i];
+    if (EPI == 0) load_div_table(&tab, tab_in);
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -412,7 +411,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // (gate columns 0..63 of the tile, up columns 64..127), then the
                 // a2 quantisation of the result, 16 columns per block.
                 const float alpha = p.alpha[e], g2 = p.g2[e];
-                const float2 aa = make_float2(alpha, alpha);
+                const f32x2 aa = pack_f32x2(alpha, alpha);
                 uint32_t sfw = 0;
 #pragma unroll 1
                 for (int c2 = 0; c2 < 2; ++c2) {
@@ -421,22 +420,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_ld16(col0 + 16 * c, gate);
                     tmem_ld16(col0 + 64 + 16 * c, up);
                     tmem_wait_ld();
-                    float2 h[8];
+                    f32x2 h[8];
                     float amax = 0.0f;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float2 gs = mul_f32x2(make_float2(gate[2 * i], gate[2 * i + 1]), aa);
-                        const float2 us = mul_f32x2(make_float2(up[2 * i], up[2 * i + 1]), aa);
-                        h[i] = mul_f32x2(make_float2(silu(gs.x), silu(gs.y)), us);
-                        amax = fmaxf(amax, fmaxf(fabsf(h[i].x), fabsf(h[i].y)));
+                        const f32x2 gs = mul_f32x2(pack_f32x2(gate[2 * i], gate[2 * i + 1]), aa);
+                        const f32x2 us = mul_f32x2(pack_f32x2(up[2 * i], up[2 * i + 1]), aa);
+                        h[i] = mul_f32x2(pack_f32x2(silu(lo_f32(gs)), silu(hi_f32(gs))), us);
+                        amax = fmaxf(amax, fmaxf(fabsf(lo_f32(h[i])), fabsf(hi_f32(h[i]))));
                     }
                     if (p.h_dump && valid) {
                         float4 *hd = reinterpret_cast<float4 *>(p.h_dump + (size_t)row * p.I + nt * 64 + 16 * c);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) hd[i] = make_float4(h[2 * i].x, h[2 * i].y, h[2 * i + 1].x, h[2 * i + 1].y);
+                        for (int i = 0; i < 4; ++i)
+                            hd[i] = make_float4(lo_f32(h[2 * i]), hi_f32(h[2 * i]), lo_f32(h[2 * i + 1]), hi_f32(h[2 * i + 1]));
                     }
                     uint32_t sb;
-                    const uint2 pk = quant_block16(h, amax, g2, tab, sb);
+                    const uint2 pk = quant_block16(h, amax, g2, &tab, sb);
                     if (valid) *reinterpret_cast<uint2 *>(p.a2q + (size_t)row * (p.I >> 1) + nt * 32 + 8 * c) = pk;
                     sfw |= sb << (8 * c2);
                 }

@@ -240,74 +240,57 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(RouteArgs a)
 // are read once and quantised for each of the token's k experts with that
 // expert's global scale, into the expert's permuted row.  The token's k
 // destination rows and global scales are loaded up front (KMAX >= k, so the
-// expert loop unrolls and its loads overlap); four lanes pack their four
-// scale bytes into one 32-bit store.
+// expert loop unrolls and its loads overlap).
 template <int KMAX>
 __global__ void __launch_bounds__(256) quant_experts_kernel(QuantArgs a, DivTable tab_in)
 {
-    __shared__ float2 tab[128];
-    for (int i = threadIdx.x; i < 128; i += blockDim.x) tab[i] = tab_in.z[i];
+    __shared__ DivTable2 tab;
+    load_div_table(&tab, tab_in);
     __syncthreads();
     if (a.hdr && a.hdr->status != 0) return;
     const int nb = a.H >> 4;
     const int k = a.k;
     const long long total = (long long)a.T * nb;
-    const int lane = threadIdx.x & 31;
-    const long long warp_stride = (long long)gridDim.x * blockDim.x;
+    const long long stride = (long long)gridDim.x * blockDim.x;
     const int32_t *__restrict__ ids = a.ids;
     const int *__restrict__ row_of = a.row_of;
     const float *__restrict__ gsc = a.g;
-    for (long long wbase = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); wbase < total;
-         wbase += warp_stride) {
-        const long long idx = wbase + lane;
-        const bool valid = idx < total;
-        const int t = valid ? (int)(idx / nb) : 0;
-        const int b = valid ? (int)(idx - (long long)t * nb) : 0;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+        const int t = (int)(idx / nb);
+        const int b = (int)(idx - (long long)t * nb);
         int rows[KMAX];
         float gs[KMAX];
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
             rows[j] = 0;
             gs[j] = 1.0f;
-            if (j < k && valid) {
+            if (j < k) {
                 const int f = t * k + j;
                 rows[j] = __ldg(row_of + f);
                 gs[j] = __ldg(gsc + __ldg(ids + f));
             }
         }
-        float2 x[8];
-        float amax = 0.0f;
-        if (valid) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + (size_t)b * 16);
-            const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-            const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + (size_t)b * 16);
+        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        f32x2 x[8];
+        uint32_t amax_bits = 0;  // max |x| on the bit patterns (non-negative floats order as integers)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                x[i] = make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
-                amax = fmaxf(amax, fmaxf(fabsf(x[i].x), fabsf(x[i].y)));
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = make_float2(0.0f, 0.0f);
+        for (int i = 0; i < 8; ++i) {
+            x[i] = bf16x2_to_f32x2(w[i]);
+            amax_bits = max(amax_bits, max((w[i] << 16) & 0x7FFFFFFFu, w[i] & 0x7FFF0000u));
         }
+        const float amax = __uint_as_float(amax_bits);
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
             if (j >= k) break;
             uint32_t sb;
-            const uint2 pk = quant_block16(x, amax, gs[j], tab, sb);
-            uint32_t word = sb;
-            word |= __shfl_down_sync(0xffffffffu, sb, 1) << 8;
-            word |= __shfl_down_sync(0xffffffffu, sb, 2) << 16;
-            word |= __shfl_down_sync(0xffffffffu, sb, 3) << 24;
-            if (valid) {
-                const int row = rows[j];
-                *reinterpret_cast<uint2 *>(a.q + (size_t)row * (a.H >> 1) + (size_t)b * 8) = pk;
-                if ((b & 3) == 0) {
-                    uint8_t *dst = a.sf_swizzled ? a.sf + swz_sf_offset(row, b >> 2, a.sf_kc)
-                                                 : a.sf + (size_t)row * nb + b;
-                    *reinterpret_cast<uint32_t *>(dst) = word;
-                }
-            }
+            const uint2 pk = quant_block16(x, amax, gs[j], &tab, sb);
+            const int row = rows[j];
+            *reinterpret_cast<uint2 *>(a.q + (size_t)row * (a.H >> 1) + (size_t)b * 8) = pk;
+            uint8_t *dst = a.sf_swizzled ? a.sf + swz_sf_offset(row, b >> 2, a.sf_kc) + (b & 3)
+                                         : a.sf + (size_t)row * nb + b;
+            *dst = (uint8_t)sb;
         }
     }
 }
@@ -401,8 +384,8 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t *w, in
                                                            uint8_t *sf, float *scale2,
                                                            const unsigned *amax_bits, DivTable tab_in)
 {
-    __shared__ float2 tab[128];
-    for (int i = threadIdx.x; i < 128; i += blockDim.x) tab[i] = tab_in.z[i];
+    __shared__ DivTable2 tab;
+    load_div_table(&tab, tab_in);
     __syncthreads();
     const int c = blockIdx.y;
     const float amax_t = __uint_as_float(amax_bits[c]);
@@ -417,18 +400,18 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t *w, in
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
         const int n = (int)(i / nb), b = (int)(i - (long long)n * nb);
-        float2 x[8];
+        f32x2 x[8];
         float amax = 0.0f;
         const uint32_t *p = reinterpret_cast<const uint32_t *>(src + (size_t)n * K + (size_t)b * 16);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const uint32_t wv = p[j];
-            x[j] = make_float2(bf16_lo(wv), bf16_hi(wv));
-            amax = fmaxf(amax, fmaxf(fabsf(x[j].x), fabsf(x[j].y)));
+            x[j] = bf16x2_to_f32x2(wv);
+            amax = fmaxf(amax, fmaxf(fabsf(lo_f32(x[j])), fabsf(hi_f32(x[j]))));
         }
         uint32_t sb = 0;
         uint2 pk = make_uint2(0u, 0u);
-        if (amax_t > 0.0f) pk = quant_block16(x, amax, g, tab, sb);
+        if (amax_t > 0.0f) pk = quant_block16(x, amax, g, &tab, sb);
         *reinterpret_cast<uint2 *>(qc + (size_t)n * (K >> 1) + (size_t)b * 8) = pk;
         sfc[(size_t)n * nb + b] = (uint8_t)sb;
     }
@@ -465,17 +448,27 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t st)
 cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st)
 {
     const long long work = (long long)a.T * (a.H >> 4);
-    const int grid = grid_for(work, 256, 8);
+    // One full wave of resident CTAs, grid-striding over the work.
+    auto launch = [&](auto kernel) {
+        int per_sm = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0) != cudaSuccess || per_sm < 1)
+            per_sm = 1;
+        long long grid = (long long)sm_count() * per_sm;
+        const long long need = (work + 255) / 256;
+        if (grid > need) grid = need;
+        if (grid < 1) grid = 1;
+        kernel<<<(int)grid, 256, 0, st>>>(a, div_table());
+    };
     if (a.k <= 1)
-        quant_experts_kernel<1><<<grid, 256, 0, st>>>(a, div_table());
+        launch(quant_experts_kernel<1>);
     else if (a.k <= 2)
-        quant_experts_kernel<2><<<grid, 256, 0, st>>>(a, div_table());
+        launch(quant_experts_kernel<2>);
     else if (a.k <= 4)
-        quant_experts_kernel<4><<<grid, 256, 0, st>>>(a, div_table());
+        launch(quant_experts_kernel<4>);
     else if (a.k <= 8)
-        quant_experts_kernel<8><<<grid, 256, 0, st>>>(a, div_table());
+        launch(quant_experts_kernel<8>);
     else
-        quant_experts_kernel<32><<<grid, 256, 0, st>>>(a, div_table());
+        launch(quant_experts_kernel<32>);
     return cudaGetLastError();
 }
 
