@@ -189,8 +189,10 @@ typedef struct {
  * [page, "Kernel Backend": after choosing a backend the packed weights and
  * scales are converted to the layout that kernel wants].  Writes the w13 and
  * w2 block scales into `prepared` (device, nvfp4_prepared_weights_size bytes,
- * 256-byte aligned) in the swizzled tensor-core layout, w13 rows reordered so
- * that each 128-row tile holds 64 gate rows and the 64 matching up rows.
+ * 256-byte aligned) in the swizzled tensor-core layout: 128-row x 64-K
+ * tiles; for w13, the gate block and the up block of each 128 h columns
+ * interleaved per 64-K step (a final 64 gate + 64 up block when I is an odd
+ * multiple of 64).
  * The packed codes are used in place from nvfp4_moe_weights.  Asynchronous.
  */
 size_t nvfp4_prepared_weights_size(int E, int H, int I);

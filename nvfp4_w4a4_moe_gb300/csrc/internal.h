@@ -65,9 +65,9 @@ cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st);
 
 struct PrepArgs {
     const uint8_t *sf;  // canonical [E, N, K/16]
-    uint8_t *out;       // [E][N/128][kc][512]
+    uint8_t *out;       // [E][N/128 blocks][kc][512]; w13 blocks of one tile interleaved per K step
     int E, N, K, kc;
-    int gate_up_I;      // > 0: rows interleaved 64 gate / 64 up per 128-row tile
+    int gate_up_I;      // w13: I > 0 (blocks of 128 gate rows and 128 up rows; a 64 + 64 tail block)
 };
 cudaError_t launch_prep_sf(const PrepArgs &a, cudaStream_t st);
 
@@ -83,7 +83,7 @@ struct GemmArgs {
     const uint8_t *a_sf, *b_sf;  // swizzled scale tiles
     int rows_cap, K, N, E;
     int a_kc, b_kc;
-    int gate_up_I;  // w13: > 0 (B tile = 64 gate rows + 64 up rows)
+    int gate_up_I;  // w13: I > 0 (B tile = up to 128 gate rows + the matching up rows)
     const int *tile_expert, *pad_off, *counts;
     const float *alpha;
     // w13 epilogue (SiLU * up, requantise)

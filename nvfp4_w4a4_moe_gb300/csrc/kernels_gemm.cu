@@ -11,15 +11,16 @@
 //   pipeline figure: SiLU/mul + a2_gscale quantisation after w13, and the
 //   token order restored and summed with the routing weights after w2.
 //
-// Kernel shape (one persistent CTA per SM, 10 warps):
+// Kernel shape (one persistent CTA per SM, 14 warps):
 //   warp 0     TMA producer: A tile 128 rows x 256 FP4 (128-byte swizzle),
 //              B tile 128 rows x 256 FP4, and both 128x4-scale tiles (2 KB
 //              each, plain bulk copies) per stage into a 6-stage (w13) or
 //              5-stage (w2) ring.
-//   warp 1     TMEM owner (512 columns) and MMA issuer: per stage, copies the
-//              8 scale chunks smem -> TMEM (tcgen05.cp 32x128b.warpx4) and
-//              issues 4 x tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
+//   warp 1     TMEM owner (512 columns) and MMA issuer: per stage, 4 x
+//              tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
 //              (M128 N128 K64) into one of two FP32 accumulators.
+//   warps 10-13 scale writers, one per TMEM lane quarter: per stage they
+//              move both scale tiles smem -> registers -> TMEM (tcgen05.st).
 //   warps 2-9  epilogue, two warps per TMEM lane quarter, each on half of the
 //              tile's columns: tcgen05.ld of the accumulator, then either
 //              SiLU(gate)*up + NVFP4 requantisation (w13) or the weighted
@@ -35,50 +36,60 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 256;  // BK in FP4 elements (128 bytes per row)
+constexpr int BM = 128, BK = 256;  // BK in FP4 elements (128 bytes per row)
 constexpr int A_BYTES = BM * BK / 2;
-constexpr int B_BYTES = BN * BK / 2;
-constexpr int SF_BYTES = 4 * 512;  // four 128x4-scale tiles = 256 K per stage
-constexpr uint32_t TX_BYTES = A_BYTES + B_BYTES + 2 * SF_BYTES;
-constexpr int ACC_COLS = BN;
-constexpr int SF_TMEM_COL = 2 * ACC_COLS;  // 32 scale columns per stage after the accumulators
+constexpr int SF_TILE = 512;                 // one 128x4-scale tile: 128 rows x 64 K
+constexpr int SFA_BYTES = 4 * SF_TILE;       // 256 K per stage
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_EPI_WARPS = 8;  // two per TMEM lane quarter, each on half of the tile's columns
 constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
-constexpr int COPY_WARP = 2 + NUM_EPI_WARPS;  // issues the smem -> TMEM scale copies
-constexpr int NUM_THREADS = 64 + EPI_THREADS + 32;
+constexpr int SCALE_WARP0 = 2 + NUM_EPI_WARPS;  // four warps write the scales into TMEM
+constexpr int NUM_SCALE_WARPS = 4;                // one per TMEM lane quarter
+constexpr int NUM_THREADS = 64 + EPI_THREADS + 32 * NUM_SCALE_WARPS;
 constexpr int XPOSE_LD = 33;  // padded row of the per-warp 32 x 32 transpose buffer
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
-// Shared-memory plan per kernel: the w13 kernel spends it all on a 6-stage
-// ring (the loads of a stage take longer than its MMAs, so more bytes in
-// flight hide more latency); the w2 kernel keeps 5 stages and a transpose
-// buffer for its epilogue.
-#ifndef NVFP4_W13_STAGES
-#define NVFP4_W13_STAGES 6
-#endif
+// Per-kernel plan.
+//  w13: tiles of 128 rows x (128 gate + 128 up) columns, one M128 N256 MMA per
+//       64-K step (the last tile of an I that is an odd multiple of 64 is
+//       64 gate + 64 up wide, N128).  The 256-column FP32 accumulator leaves no
+//       TMEM for a second one, so the epilogue copies it to registers and
+//       releases it before computing; a 4-stage ring of 54 KB stages.
+//  w2:  tiles of 128 x 128, M128 N128 MMAs into two alternating accumulators,
+//       a 5-stage ring and a transpose buffer for the combine.
 template <int EPI>
 struct Plan {
-    static constexpr int STAGES = EPI == 0 ? NVFP4_W13_STAGES : 5;
+    static constexpr int BN = EPI == 0 ? 256 : 128;  // widest tile (MMA N)
+    static constexpr int STAGES = EPI == 0 ? 4 : 5;
+    static constexpr int ACC_BUFS = EPI == 0 ? 1 : 2;
+    static constexpr int B_BYTES = BN * BK / 2;
+    static constexpr int SFB_BYTES = (BN / 128) * 4 * SF_TILE;
+    static constexpr int SFB_STEP = BN / 32;               // TMEM columns per 64-K step of B scales
+    static constexpr int SF_COLS = 16 + 4 * SFB_STEP;      // TMEM scale columns per stage
+    static constexpr int SF_TMEM_COL = ACC_BUFS * BN;      // scale slots after the accumulator(s)
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_SFB = OFF_SFA + STAGES * SF_BYTES;
-    static constexpr int OFF_BAR = OFF_SFB + STAGES * SF_BYTES;
-    static constexpr int NUM_BARS = 3 * STAGES + 4 + 2;
+    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_XPOSE = (OFF_MISC + 16 + 15) & ~15;
     static constexpr int XPOSE_BYTES = EPI == 1 ? NUM_EPI_WARPS * 32 * XPOSE_LD * 4 : 0;
     static constexpr int SMEM_BYTES = OFF_XPOSE + XPOSE_BYTES + 1024;  // + alignment slack
-    static_assert(SF_TMEM_COL + STAGES * 32 <= TMEM_COLS, "scale slots exceed TMEM");
-    static_assert(SMEM_BYTES + 1024 <= 232448, "shared memory plan exceeds the opt-in limit");
+    static_assert(SF_TMEM_COL + STAGES * SF_COLS <= TMEM_COLS, "scale slots exceed TMEM");
+    static_assert(SMEM_BYTES + (EPI == 0 ? (int)sizeof(DivTable2) : 0) <= 232448,
+                  "shared memory plan exceeds the opt-in limit");
 };
 
 // Instruction descriptor, block-scaled kinds: E2M1 A and B (code 1 at bits
 // 7-9 and 10-12), K-major both, N>>3 at 17-22, scale type UE4M3 (bit 23 = 0),
 // M>>4 at 24-28, scale-factor ids 0.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_for(int n)
+{
+    return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -149,23 +160,14 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr)
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// One 128x4-scale tile as 32 rows x 16 bytes, no swizzle (8-row groups 128 B apart).
-__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr)
-{
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
-}
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb,
-                                       uint32_t accumulate)
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
             d),
-        "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
         : "memory");
 }
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v)
@@ -181,6 +183,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v)
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Four 16-byte rows to 16 consecutive columns of this warp's lane quarter.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint4 (&v)[4])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z), "r"(v[1].w),
+        "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y), "r"(v[3].z), "r"(v[3].w)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d)
 {
@@ -192,6 +205,34 @@ __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, 
 // requantisation that follows is exact for whatever FP32 h results).
 __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(fminf(-z, 80.0f))); }
 
+// ---------------------------------------------------------------- tiles
+// Tile geometry shared by every role.  w13: tile t covers h columns
+// [128 t, 128 t + hc) with hc = min(128, I - 128 t); its B rows are hc gate
+// rows then hc up rows, and its weight scales are hc*2/128 tiles per 64-K
+// step.  w2: tile t covers output columns [128 t, 128 t + 128).
+template <int EPI>
+struct TileInfo {
+    int mt, nt, e;
+    int hc;    // w13: h columns of the tile (128 or 64)
+    int nblk;  // 128-row scale blocks of the B tile (w13 full: 2, else 1)
+};
+template <int EPI>
+__device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, int NT)
+{
+    TileInfo<EPI> ti;
+    ti.mt = tile / NT;
+    ti.nt = tile - ti.mt * NT;
+    ti.e = p.tile_expert[ti.mt];
+    if (EPI == 0) {
+        ti.hc = min(128, p.gate_up_I - 128 * ti.nt);
+        ti.nblk = ti.hc == 128 ? 2 : 1;
+    } else {
+        ti.hc = 0;
+        ti.nblk = 1;
+    }
+    return ti;
+}
+
 // ---------------------------------------------------------------- kernel
 template <int EPI>  // 0: w13 (SiLU*up + requantise), 1: w2 (weighted combine)
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -199,21 +240,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const GemmArgs p, const DivTable tab_in)
 {
     using P = Plan<EPI>;
-    constexpr int STAGES = P::STAGES, OFF_A = P::OFF_A, OFF_B = P::OFF_B, OFF_SFA = P::OFF_SFA,
-                  OFF_SFB = P::OFF_SFB, OFF_BAR = P::OFF_BAR, OFF_MISC = P::OFF_MISC, OFF_XPOSE = P::OFF_XPOSE;
+    constexpr int STAGES = P::STAGES, ACC_BUFS = P::ACC_BUFS, OFF_A = P::OFF_A, OFF_B = P::OFF_B,
+                  OFF_SFA = P::OFF_SFA, OFF_SFB = P::OFF_SFB, OFF_BAR = P::OFF_BAR, OFF_MISC = P::OFF_MISC,
+                  OFF_XPOSE = P::OFF_XPOSE, B_BYTES = P::B_BYTES, SFB_BYTES = P::SFB_BYTES,
+                  SFB_STEP = P::SFB_STEP, SF_COLS = P::SF_COLS, SF_TMEM_COL = P::SF_TMEM_COL;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ DivTable2 tab;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-    uint64_t *full = bars, *empty = bars + STAGES, *acc_full = bars + 2 * STAGES,
-             *acc_empty = bars + 2 * STAGES + 2, *drain = bars + 2 * STAGES + 4, *sf_ready = bars + 2 * STAGES + 5,
-             *drain_cp = bars + 3 * STAGES + 5;
+    uint64_t *full = bars, *empty = bars + STAGES, *sf_ready = bars + 2 * STAGES, *acc_full = bars + 3 * STAGES,
+             *acc_empty = acc_full + ACC_BUFS, *drain = acc_empty + ACC_BUFS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (p.hdr->status != 0) return;
-    const int NT = p.N / BN;
+    const int NT = EPI == 0 ? (p.gate_up_I + 127) / 128 : p.N / 128;
     const int ntiles = p.hdr->num_mtiles * NT;
     if ((int)blockIdx.x >= ntiles) return;
     const int KT = (p.K + BK - 1) / BK;
@@ -223,10 +265,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&sf_ready[s], 1);
+            mbar_init(&sf_ready[s], NUM_SCALE_WARPS);
         }
-        mbar_init(drain_cp, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < ACC_BUFS; ++i) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], EPI_THREADS);
         }
@@ -252,31 +293,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t issued = 0;           // bit s: stage s has had a load issued
         uint32_t last_parity = 0;      // bit s: parity of that last load's phase
         bool ok = true;
+        const size_t b_sf_expert = (size_t)(p.N / 128) * p.b_kc * SF_TILE;  // prepared scale bytes per expert
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            const int mt = tile / NT, nt = tile - mt * NT;
-            const int e = p.tile_expert[mt];
+            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT);
+            const uint8_t *b_sf = p.b_sf + (size_t)ti.e * b_sf_expert +
+                                  (size_t)(EPI == 0 ? 2 * ti.nt : ti.nt) * p.b_kc * SF_TILE;
+            const uint32_t b_bytes = EPI == 0 ? (uint32_t)ti.hc * 2 * (BK / 2) : (uint32_t)B_BYTES;
+            const uint32_t sfb_bytes = (uint32_t)ti.nblk * 4 * SF_TILE;
             for (int kt = 0; kt < KT; ++kt) {
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 uint64_t *fb = &full[stage];
-                mbar_expect_tx(fb, TX_BYTES);
+                mbar_expect_tx(fb, A_BYTES + b_bytes + SFA_BYTES + sfb_bytes);
                 const int kx = kt * (BK / 2);
                 uint8_t *sa = smem + OFF_A + stage * A_BYTES;
                 uint8_t *sb = smem + OFF_B + stage * B_BYTES;
-                tma_2d(sa, &tmap_a, kx, mt * BM, fb);
-                if (p.gate_up_I > 0) {
-                    const int brow = e * 2 * p.gate_up_I + nt * 64;
-                    tma_2d(sb, &tmap_b, kx, brow, fb);
-                    tma_2d(sb + B_BYTES / 2, &tmap_b, kx, brow + p.gate_up_I, fb);
+                tma_2d(sa, &tmap_a, kx, ti.mt * BM, fb);
+                if (EPI == 0) {
+                    // hc gate rows, then the hc matching up rows, in 64-row boxes
+                    const int gate = ti.e * 2 * p.gate_up_I + 128 * ti.nt;
+                    for (int r = 0; r < ti.hc; r += 64) {
+                        tma_2d(sb + r * (BK / 2), &tmap_b, kx, gate + r, fb);
+                        tma_2d(sb + (ti.hc + r) * (BK / 2), &tmap_b, kx, gate + p.gate_up_I + r, fb);
+                    }
                 } else {
-                    tma_2d(sb, &tmap_b, kx, e * p.N + nt * BN, fb);
+                    tma_2d(sb, &tmap_b, kx, ti.e * p.N + ti.nt * 128, fb);
                 }
-                bulk_g2s(smem + OFF_SFA + stage * SF_BYTES, p.a_sf + ((size_t)mt * p.a_kc + 4 * kt) * 512,
-                         SF_BYTES, fb);
-                bulk_g2s(smem + OFF_SFB + stage * SF_BYTES,
-                         p.b_sf + (((size_t)e * NT + nt) * p.b_kc + 4 * kt) * 512, SF_BYTES, fb);
+                bulk_g2s(smem + OFF_SFA + stage * SFA_BYTES,
+                         p.a_sf + ((size_t)ti.mt * p.a_kc + 4 * kt) * SF_TILE, SFA_BYTES, fb);
+                bulk_g2s(smem + OFF_SFB + stage * SFB_BYTES, b_sf + (size_t)4 * kt * ti.nblk * SF_TILE, sfb_bytes,
+                         fb);
                 issued |= 1u << stage;
                 last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
                 if (++stage == STAGES) {
@@ -297,27 +345,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT);
+            const uint32_t idesc = idesc_for(EPI == 0 ? 2 * ti.hc : 128);
             if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t d = tmem + acc * ACC_COLS;
+            const uint32_t d = tmem + acc * P::BN;
             for (int kt = 0; kt < KT; ++kt) {
-                // operands landed (full) and their scales are in TMEM (sf_ready)
-                if (!mbar_wait(&full[stage], phase, abort_flag, kWaitLimitNs) ||
-                    !mbar_wait(&sf_ready[stage], phase, abort_flag, kWaitLimitNs)) {
+                // the scale writers arrive on sf_ready[stage] only after they
+                // have seen the stage's loads land (full[stage])
+                if (!mbar_wait(&sf_ready[stage], phase, abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const int ksteps = min(4, (p.K - kt * BK + 63) / 64);
-                const uint32_t sfa_t = tmem + SF_TMEM_COL + stage * 32, sfb_t = sfa_t + 16;
+                const uint32_t sfa_t = tmem + SF_TMEM_COL + stage * SF_COLS, sfb_t = sfa_t + 16;
                 const uint32_t sa = su32(smem + OFF_A + stage * A_BYTES);
                 const uint32_t sb = su32(smem + OFF_B + stage * B_BYTES);
                 for (int j = 0; j < ksteps; ++j)
-                    tc_mma(d, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j), sfa_t + 4 * j, sfb_t + 4 * j,
-                           (kt | j) != 0);
+                    tc_mma(d, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j), idesc, sfa_t + 4 * j,
+                           sfb_t + SFB_STEP * j, (kt | j) != 0);
                 tc_commit(&empty[stage]);
                 if (++stage == STAGES) {
                     stage = 0;
@@ -326,7 +376,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (!ok) break;
             tc_commit(&acc_full[acc]);
-            if (++acc == 2) {
+            if (++acc == ACC_BUFS) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
@@ -338,44 +388,69 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Drain: all issued tcgen05 work completes before TMEM is released.
         tc_commit(drain);
         mbar_wait(drain, 0, nullptr, kDrainLimitNs);
-    } else if (warp == COPY_WARP && lane == 0) {
-        // ------------------------------------------------ scale copier
-        // Moves each stage's scale tiles smem -> TMEM (tcgen05.cp
-        // 32x128b.warpx4, one per K step and operand) ahead of the MMA issuer,
-        // and signals sf_ready[stage] when the copies have completed.  The
-        // stage's TMEM scale slot is only rewritten after the producer has
-        // refilled the stage, i.e. after the MMAs that read it have finished.
+    } else if (warp >= SCALE_WARP0) {
+        // ------------------------------------------------ scale writers
+        // Each warp owns one TMEM lane quarter and writes the stage's scales
+        // there with tcgen05.st: per 64-K step and 128-row block, the 16 bytes
+        // of row (lane) of the 128x4-scale tile (the scales of rows lane,
+        // lane+32, lane+64, lane+96) go to four consecutive columns of every
+        // lane quarter, the layout the block-scaled MMA reads.  With N256 the
+        // second 128-row block of B follows the first at +4 columns.  Register
+        // stores from four warps in parallel keep the MMA issuer free of the
+        // smem -> TMEM copy queue.  A stage's slot is rewritten only after the
+        // producer has refilled the stage, i.e. after the MMAs that read it
+        // have finished.
+        const int quarter = warp & 3;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         uint32_t stage = 0, phase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT);
             for (int kt = 0; kt < KT; ++kt) {
                 if (!mbar_wait(&full[stage], phase, abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                const int ksteps = min(4, (p.K - kt * BK + 63) / 64);
-                const uint32_t sfa_t = tmem + SF_TMEM_COL + stage * 32, sfb_t = sfa_t + 16;
-                const uint32_t ssfa = su32(smem + OFF_SFA + stage * SF_BYTES);
-                const uint32_t ssfb = su32(smem + OFF_SFB + stage * SF_BYTES);
-                for (int j = 0; j < ksteps; ++j) {
-                    tc_cp_sf(sfa_t + 4 * j, desc_sf(ssfa + 512 * j));
-                    tc_cp_sf(sfb_t + 4 * j, desc_sf(ssfb + 512 * j));
+                const uint32_t sfa_t = tmem + lane_off + SF_TMEM_COL + stage * SF_COLS, sfb_t = sfa_t + 16;
+                const uint4 *ssfa = reinterpret_cast<const uint4 *>(smem + OFF_SFA + stage * SFA_BYTES) + lane;
+                const uint4 *ssfb = reinterpret_cast<const uint4 *>(smem + OFF_SFB + stage * SFB_BYTES) + lane;
+                uint4 v[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[j] = ssfa[32 * j];
+                tmem_st16(sfa_t, v);
+                if (SFB_STEP == 4) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v[j] = ssfb[32 * j];
+                    tmem_st16(sfb_t, v);
+                } else {
+                    // column 4i holds tile i of the stage: (step i/2, block i%2)
+                    // for a full tile; a narrow tile has one block per step
+                    // and leaves the odd slots as copies.
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int i = 4 * h + j;
+                            v[j] = ti.nblk == 2 ? ssfb[32 * i] : ssfb[32 * (i >> 1)];
+                        }
+                        tmem_st16(sfb_t + 16 * h, v);
+                    }
                 }
-                tc_commit(&sf_ready[stage]);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_ready[stage]);
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
         }
-        if (!ok) {
+        if (!ok && lane == 0) {
             *abort_flag = 1;
             atomicOr(&p.hdr->error_flags, kErrTimeoutMma);
         }
-        tc_commit(drain_cp);
-        mbar_wait(drain_cp, 0, nullptr, kDrainLimitNs);
-    } else if (warp >= 2 && warp < COPY_WARP) {
+    } else if (warp >= 2 && warp < SCALE_WARP0) {
         // ------------------------------------------------ epilogue
         const int ew = warp - 2;          // 0..7
         const int quarter = warp & 3;     // TMEM lanes this warp may read
@@ -396,54 +471,80 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t acc = 0, acc_phase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-            const int mt = tile / NT, nt = tile - mt * NT;
-            const int e = p.tile_expert[mt];
-            const int row = mt * BM + r_in;
+            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT);
+            const int e = ti.e, nt = ti.nt;
+            const int row = ti.mt * BM + r_in;
             const bool valid = row < p.pad_off[e] + p.counts[e];
             if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t col0 = lane_base + acc * ACC_COLS;
+            const uint32_t col0 = lane_base + acc * P::BN;
             if (EPI == 0) {
-                // SiLU(gate) * up on this warp's 32 of the tile's 64 h columns
-                // (gate columns 0..63 of the tile, up columns 64..127), then the
-                // a2 quantisation of the result, 16 columns per block.
+                // This warp's h columns: [w0, w0 + hw) of the tile, hw = hc/2,
+                // w0 = half * hw; gate accumulator columns w0.., up columns
+                // hc + w0...  h = SiLU(alpha * gate) * (alpha * up) is formed
+                // 32 columns at a time and the accumulator released once all
+                // of it is in registers.
                 const float alpha = p.alpha[e], g2 = p.g2[e];
                 const f32x2 aa = pack_f32x2(alpha, alpha);
-                uint32_t sfw = 0;
-#pragma unroll 1
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    const int c = half * 2 + c2;
-                    float gate[16], up[16];
-                    tmem_ld16(col0 + 16 * c, gate);
-                    tmem_ld16(col0 + 64 + 16 * c, up);
-                    tmem_wait_ld();
-                    f32x2 h[8];
-                    float amax = 0.0f;
+                const int hw = ti.hc >> 1, w0 = half * hw;
+                const int nblocks = hw >> 4;  // 4 or 2 blocks of 16
+                f32x2 h[4][8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
+                for (int c = 0; c < 2; ++c) {
+                    if (c * 32 >= hw) break;
+                    float gate[32], up[32];
+                    tmem_ld16(col0 + w0 + 32 * c, gate);
+                    tmem_ld16(col0 + w0 + 32 * c + 16, gate + 16);
+                    tmem_ld16(col0 + ti.hc + w0 + 32 * c, up);
+                    tmem_ld16(col0 + ti.hc + w0 + 32 * c + 16, up + 16);
+                    tmem_wait_ld();
+                    if (32 * (c + 1) >= hw) {
+                        // the whole accumulator slice is in registers
+                        tc_fence_before();
+                        mbar_arrive(&acc_empty[acc]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
                         const f32x2 gs = mul_f32x2(pack_f32x2(gate[2 * i], gate[2 * i + 1]), aa);
                         const f32x2 us = mul_f32x2(pack_f32x2(up[2 * i], up[2 * i + 1]), aa);
-                        h[i] = mul_f32x2(pack_f32x2(silu(lo_f32(gs)), silu(hi_f32(gs))), us);
-                        amax = fmaxf(amax, fmaxf(fabsf(lo_f32(h[i])), fabsf(hi_f32(h[i]))));
+                        h[2 * c + (i >> 3)][i & 7] = mul_f32x2(pack_f32x2(silu(lo_f32(gs)), silu(hi_f32(gs))), us);
                     }
+                }
+                uint32_t sfw = 0;
+                const int hcol_tile = 128 * nt + w0;  // first h column of this warp
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    if (b >= nblocks) break;
+                    float amax = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        amax = fmaxf(amax, fmaxf(fabsf(lo_f32(h[b][i])), fabsf(hi_f32(h[b][i]))));
+                    const int hcol = hcol_tile + 16 * b;
                     if (p.h_dump && valid) {
-                        float4 *hd = reinterpret_cast<float4 *>(p.h_dump + (size_t)row * p.I + nt * 64 + 16 * c);
+                        float4 *hd = reinterpret_cast<float4 *>(p.h_dump + (size_t)row * p.I + hcol);
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
-                            hd[i] = make_float4(lo_f32(h[2 * i]), hi_f32(h[2 * i]), lo_f32(h[2 * i + 1]), hi_f32(h[2 * i + 1]));
+                            hd[i] = make_float4(lo_f32(h[b][2 * i]), hi_f32(h[b][2 * i]), lo_f32(h[b][2 * i + 1]),
+                                                hi_f32(h[b][2 * i + 1]));
                     }
                     uint32_t sb;
-                    const uint2 pk = quant_block16(h, amax, g2, &tab, sb);
-                    if (valid) *reinterpret_cast<uint2 *>(p.a2q + (size_t)row * (p.I >> 1) + nt * 32 + 8 * c) = pk;
-                    sfw |= sb << (8 * c2);
+                    const uint2 pk = quant_block16(h[b], amax, g2, &tab, sb);
+                    if (valid) *reinterpret_cast<uint2 *>(p.a2q + (size_t)row * (p.I >> 1) + (hcol >> 1)) = pk;
+                    sfw |= sb << (8 * b);
                 }
                 if (valid) {
-                    *reinterpret_cast<uint16_t *>(p.sf2 + swz_sf_offset(row, nt, p.kc2) + 2 * half) = (uint16_t)sfw;
+                    // four scales = one 64-column chunk (full tile), or two =
+                    // half a chunk (narrow tile)
+                    uint8_t *sfp = p.sf2 + swz_sf_offset(row, hcol_tile >> 6, p.kc2) + ((hcol_tile & 63) >> 4);
+                    if (nblocks == 4)
+                        *reinterpret_cast<uint32_t *>(sfp) = sfw;
+                    else
+                        *reinterpret_cast<uint16_t *>(sfp) = (uint16_t)sfw;
                     if (nt == NT - 1 && half == 0)
-                        for (int cc = NT; cc < p.kc2; ++cc)
+                        for (int cc = p.I >> 6; cc < p.kc2; ++cc)
                             *reinterpret_cast<uint32_t *>(p.sf2 + swz_sf_offset(row, cc, p.kc2)) = 0u;
                 }
             } else {
@@ -466,6 +567,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_ld16(col0 + cbase, v);
                     tmem_ld16(col0 + cbase + 16, v + 16);
                     tmem_wait_ld();
+                    if (c2 == 1) {
+                        tc_fence_before();
+                        mbar_arrive(&acc_empty[acc]);
+                    }
 #pragma unroll
                     for (int i = 0; i < 32; ++i) xp[lane * XPOSE_LD + i] = v[i] * scale;
                     __syncwarp();
@@ -476,14 +581,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const int ok_r = __shfl_sync(0xffffffffu, (int)valid, rr);
                         const float *src = xp + rr * XPOSE_LD + cc;
                         if (ok_r)
-                            red_add_v4(p.out + (size_t)t_r * p.H + nt * BN + cbase + cc, src[0], src[1], src[2], src[3]);
+                            red_add_v4(p.out + (size_t)t_r * p.H + nt * 128 + cbase + cc, src[0], src[1], src[2],
+                                       src[3]);
                     }
                     __syncwarp();
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&acc_empty[acc]);
-            if (++acc == 2) {
+            if (++acc == ACC_BUFS) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
@@ -562,7 +666,8 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
     if (!make_map(&ma, a.a_q, kbytes, (uint64_t)a.rows_cap, 128)) return cudaErrorInvalidValue;
     const uint64_t brows = (uint64_t)a.E * (uint64_t)a.N;
     if (!make_map(&mb, a.b_q, kbytes, brows, a.gate_up_I > 0 ? 64 : 128)) return cudaErrorInvalidValue;
-    const long long tiles = (long long)a.mtiles_cap * (a.N / BN);
+    const long long nt = EPI == 0 ? (a.gate_up_I + 127) / 128 : a.N / 128;
+    const long long tiles = (long long)a.mtiles_cap * nt;
     int grid = sm_count();
     if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
     moe_gemm_kernel<EPI><<<grid, NUM_THREADS, Plan<EPI>::SMEM_BYTES, st>>>(ma, mb, a, div_table());

@@ -298,9 +298,7 @@ __global__ void __launch_bounds__(256) quant_experts_kernel(QuantArgs a, DivTabl
 // ------------------------------------------------------------------ weight-scale layout
 // [page, "Kernel Backend": packed weights and scales are converted to the
 // layout the chosen kernel wants].  One thread per output word (one row's four
-// scales of a 64-element chunk).  For w13 every 128-row tile holds 64 gate rows
-// followed by the 64 matching up rows, so one tile yields 64 SiLU(gate)*up
-// columns.
+// scales of a 64-element chunk), in 128x4-scale tiles of 128 rows x 64 K.
 __global__ void __launch_bounds__(256) prep_sf_kernel(PrepArgs a)
 {
     const int NT = a.N / 128;
@@ -314,11 +312,28 @@ __global__ void __launch_bounds__(256) prep_sf_kernel(PrepArgs a)
         rest /= a.kc;
         const int nt = (int)(rest % NT);
         const int e = (int)(rest / NT);
+        // 128-row block nt of the expert.  w13: block 2t holds the gate rows
+        // and block 2t+1 the up rows of h columns [128 t, 128 t + 128); when
+        // I is an odd multiple of 64 the last block holds the final 64 gate
+        // rows then the final 64 up rows.  Blocks of one tile are interleaved
+        // per 64-K step, so a stage's scales are one contiguous run.
         int row;
-        if (a.gate_up_I > 0)
-            row = v < 64 ? nt * 64 + v : a.gate_up_I + nt * 64 + (v - 64);
-        else
+        size_t blk_off;  // byte offset of (block, step c) within the expert
+        if (a.gate_up_I > 0) {
+            const int full = a.gate_up_I / 128;
+            const int t = nt >> 1;
+            if (t < full) {
+                const int up = nt & 1;
+                row = (up ? a.gate_up_I : 0) + 128 * t + v;
+                blk_off = ((size_t)2 * t * a.kc + 2 * c + up) * 512;
+            } else {
+                row = v < 64 ? 128 * t + v : a.gate_up_I + 128 * t + (v - 64);
+                blk_off = ((size_t)2 * t * a.kc + c) * 512;
+            }
+        } else {
             row = nt * 128 + v;
+            blk_off = ((size_t)nt * a.kc + c) * 512;
+        }
         const uint8_t *src = a.sf + ((size_t)e * a.N + row) * nsf;
         uint32_t word = 0;
 #pragma unroll
@@ -326,7 +341,7 @@ __global__ void __launch_bounds__(256) prep_sf_kernel(PrepArgs a)
             const int col = 4 * c + j;
             if (col < nsf) word |= (uint32_t)src[col] << (8 * j);
         }
-        uint8_t *dst = a.out + (((size_t)e * NT + nt) * a.kc + c) * 512 + (size_t)(v & 31) * 16 + (v >> 5) * 4;
+        uint8_t *dst = a.out + (size_t)e * NT * a.kc * 512 + blk_off + (size_t)(v & 31) * 16 + (v >> 5) * 4;
         *reinterpret_cast<uint32_t *>(dst) = word;
     }
 }
