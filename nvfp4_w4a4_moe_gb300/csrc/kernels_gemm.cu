@@ -11,22 +11,24 @@
 //   pipeline figure: SiLU/mul + a2_gscale quantisation after w13, and the
 //   token order restored and summed with the routing weights after w2.
 //
-// Kernel shape (one persistent CTA per SM, 14 warps):
-//   warp 0     TMA producer: A tile 128 rows x 256 FP4 (128-byte swizzle),
-//              B tile 128 rows x 256 FP4, and both 128x4-scale tiles (2 KB
-//              each, plain bulk copies) per stage into a 6-stage (w13) or
-//              5-stage (w2) ring.
+// Kernel shape (one persistent CTA per SM):
+//   warp 0     TMA producer: per 256-K stage the A tile (128 rows, 128-byte
+//              swizzle), the B tile, and the 128x4-scale tiles of both (plain
+//              bulk copies) into a 4-stage ring.
 //   warp 1     TMEM owner (512 columns) and MMA issuer: per stage, 4 x
-//              tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
-//              (M128 N128 K64) into one of two FP32 accumulators.
-//   warps 10-13 scale writers, one per TMEM lane quarter: per stage they
-//              move both scale tiles smem -> registers -> TMEM (tcgen05.st).
-//   warps 2-9  epilogue, two warps per TMEM lane quarter, each on half of the
-//              tile's columns: tcgen05.ld of the accumulator, then either
-//              SiLU(gate)*up + NVFP4 requantisation (w13) or the weighted
-//              scatter-add into the token-order output (w2), transposed
-//              through shared memory so the FP32 reductions are coalesced.
-//              In the w13 kernel they first clear the output for w2.
+//              tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (K64):
+//              M128 N256 into one accumulator (w13), M128 N128 into one of two
+//              (w2).
+//   epilogue   8 (w13) or 16 (w2) warps, two or four per TMEM lane quarter:
+//              tcgen05.ld of the accumulator, released before the heavy work,
+//              then either SiLU(gate)*up + NVFP4 requantisation (w13) or the
+//              weighted scatter-add into the token-order output (w2),
+//              transposed through shared memory so the FP32 reductions are
+//              coalesced.  In the w13 kernel they first clear the output for
+//              w2.
+//   last 4     scale writers, one per TMEM lane quarter: per stage they move
+//              both operands' scale tiles smem -> registers -> TMEM
+//              (tcgen05.st).
 // Every wait is bounded (%globaltimer); on expiry the kernel records the
 // error in the workspace header, drains what it has in flight and exits.
 #include <climits>
@@ -41,11 +43,7 @@ constexpr int A_BYTES = BM * BK / 2;
 constexpr int SF_TILE = 512;                 // one 128x4-scale tile: 128 rows x 64 K
 constexpr int SFA_BYTES = 4 * SF_TILE;       // 256 K per stage
 constexpr int TMEM_COLS = 512;
-constexpr int NUM_EPI_WARPS = 8;  // two per TMEM lane quarter, each on half of the tile's columns
-constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
-constexpr int SCALE_WARP0 = 2 + NUM_EPI_WARPS;  // four warps write the scales into TMEM
-constexpr int NUM_SCALE_WARPS = 4;                // one per TMEM lane quarter
-constexpr int NUM_THREADS = 64 + EPI_THREADS + 32 * NUM_SCALE_WARPS;
+constexpr int NUM_SCALE_WARPS = 4;  // one per TMEM lane quarter
 constexpr int XPOSE_LD = 33;  // padded row of the per-warp 32 x 32 transpose buffer
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
@@ -56,12 +54,19 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 //       64 gate + 64 up wide, N128).  The 256-column FP32 accumulator leaves no
 //       TMEM for a second one, so the epilogue copies it to registers and
 //       releases it before computing; a 4-stage ring of 54 KB stages.
+//       Eight epilogue warps, two per TMEM lane quarter.
 //  w2:  tiles of 128 x 128, M128 N128 MMAs into two alternating accumulators,
-//       a 5-stage ring and a transpose buffer for the combine.
+//       a 4-stage ring, and sixteen epilogue warps (four per lane quarter, 32
+//       columns each) so that enough of them are issuing the combine's
+//       reductions while others wait on TMEM; each has a transpose buffer.
 template <int EPI>
 struct Plan {
     static constexpr int BN = EPI == 0 ? 256 : 128;  // widest tile (MMA N)
-    static constexpr int STAGES = EPI == 0 ? 4 : 5;
+    static constexpr int STAGES = 4;
+    static constexpr int NUM_EPI_WARPS = EPI == 0 ? 8 : 16;
+    static constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
+    static constexpr int SCALE_WARP0 = 2 + NUM_EPI_WARPS;  // then the four scale writers
+    static constexpr int NUM_THREADS = 64 + EPI_THREADS + 32 * NUM_SCALE_WARPS;
     static constexpr int ACC_BUFS = EPI == 0 ? 1 : 2;
     static constexpr int B_BYTES = BN * BK / 2;
     static constexpr int SFB_BYTES = (BN / 128) * 4 * SF_TILE;
@@ -182,7 +187,24 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v)
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Waits for this thread's tcgen05.ld results.  The loaded registers are only
+// defined after the wait, so each is passed through an empty asm that the
+// compiler must order after it: no use of a loaded value can be scheduled
+// ahead of the wait.
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld(float (&v)[N])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i])::"memory");
+}
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld(float (&v)[N], float (&w)[N])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]), "+f"(w[i])::"memory");
+}
 // Four 16-byte rows to 16 consecutive columns of this warp's lane quarter.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint4 (&v)[4])
 {
@@ -235,7 +257,7 @@ __device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, 
 
 // ---------------------------------------------------------------- kernel
 template <int EPI>  // 0: w13 (SiLU*up + requantise), 1: w2 (weighted combine)
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const GemmArgs p, const DivTable tab_in)
 {
@@ -243,7 +265,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr int STAGES = P::STAGES, ACC_BUFS = P::ACC_BUFS, OFF_A = P::OFF_A, OFF_B = P::OFF_B,
                   OFF_SFA = P::OFF_SFA, OFF_SFB = P::OFF_SFB, OFF_BAR = P::OFF_BAR, OFF_MISC = P::OFF_MISC,
                   OFF_XPOSE = P::OFF_XPOSE, B_BYTES = P::B_BYTES, SFB_BYTES = P::SFB_BYTES,
-                  SFB_STEP = P::SFB_STEP, SF_COLS = P::SF_COLS, SF_TMEM_COL = P::SF_TMEM_COL;
+                  SFB_STEP = P::SFB_STEP, SF_COLS = P::SF_COLS, SF_TMEM_COL = P::SF_TMEM_COL,
+                  EPI_THREADS = P::EPI_THREADS, SCALE_WARP0 = P::SCALE_WARP0;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ DivTable2 tab;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -452,9 +475,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp >= 2 && warp < SCALE_WARP0) {
         // ------------------------------------------------ epilogue
-        const int ew = warp - 2;          // 0..7
+        const int ew = warp - 2;          // 0 .. epilogue warps - 1
         const int quarter = warp & 3;     // TMEM lanes this warp may read
-        const int half = ew >> 2;         // which half of the tile's columns it owns
+        const int half = ew >> 2;         // w13: which half of the tile's columns it owns; w2: which quarter
         const int r_in = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         if (EPI == 0 && p.zero_out) {
@@ -500,7 +523,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tmem_ld16(col0 + w0 + 32 * c + 16, gate + 16);
                     tmem_ld16(col0 + ti.hc + w0 + 32 * c, up);
                     tmem_ld16(col0 + ti.hc + w0 + 32 * c + 16, up + 16);
-                    tmem_wait_ld();
+                    tmem_wait_ld(gate, up);
                     if (32 * (c + 1) >= hw) {
                         // the whole accumulator slice is in registers
                         tc_fence_before();
@@ -548,10 +571,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             *reinterpret_cast<uint32_t *>(p.sf2 + swz_sf_offset(row, cc, p.kc2)) = 0u;
                 }
             } else {
-                // out[t, cols] += w[t, j] * alpha2 * y2: this warp's 64 columns,
-                // 32 at a time, transposed through shared memory so that each
-                // reduction instruction covers four contiguous 128-byte row
-                // segments.
+                // out[t, cols] += w[t, j] * alpha2 * y2 on this warp's 32 columns,
+                // transposed through shared memory so that each reduction
+                // instruction covers four contiguous 128-byte row segments.
                 int t = 0;
                 float scale = 0.0f;
                 if (valid) {
@@ -560,32 +582,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     scale = __fmul_rn(p.topk_w[f], p.alpha[e]);
                 }
                 const int sub = lane >> 3, cc = (lane & 7) * 4;
-#pragma unroll 1
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    const int cbase = 64 * half + 32 * c2;
-                    float v[32];
-                    tmem_ld16(col0 + cbase, v);
-                    tmem_ld16(col0 + cbase + 16, v + 16);
-                    tmem_wait_ld();
-                    if (c2 == 1) {
-                        tc_fence_before();
-                        mbar_arrive(&acc_empty[acc]);
-                    }
+                const int cbase = 32 * half;
+                float v[32];
+                tmem_ld16(col0 + cbase, v);
+                tmem_ld16(col0 + cbase + 16, v + 16);
+                tmem_wait_ld(v);
+                tc_fence_before();
+                mbar_arrive(&acc_empty[acc]);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) xp[lane * XPOSE_LD + i] = v[i] * scale;
-                    __syncwarp();
+                for (int i = 0; i < 32; ++i) xp[lane * XPOSE_LD + i] = v[i] * scale;
+                __syncwarp();
 #pragma unroll
-                    for (int it = 0; it < 8; ++it) {
-                        const int rr = it * 4 + sub;
-                        const int t_r = __shfl_sync(0xffffffffu, t, rr);
-                        const int ok_r = __shfl_sync(0xffffffffu, (int)valid, rr);
-                        const float *src = xp + rr * XPOSE_LD + cc;
-                        if (ok_r)
-                            red_add_v4(p.out + (size_t)t_r * p.H + nt * 128 + cbase + cc, src[0], src[1], src[2],
-                                       src[3]);
-                    }
-                    __syncwarp();
+                for (int it = 0; it < 8; ++it) {
+                    const int rr = it * 4 + sub;
+                    const int t_r = __shfl_sync(0xffffffffu, t, rr);
+                    const int ok_r = __shfl_sync(0xffffffffu, (int)valid, rr);
+                    const float *src = xp + rr * XPOSE_LD + cc;
+                    if (ok_r)
+                        red_add_v4(p.out + (size_t)t_r * p.H + nt * 128 + cbase + cc, src[0], src[1], src[2],
+                                   src[3]);
                 }
+                __syncwarp();
             }
             if (++acc == ACC_BUFS) {
                 acc = 0;
@@ -670,7 +687,7 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
     const long long tiles = (long long)a.mtiles_cap * nt;
     int grid = sm_count();
     if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
-    moe_gemm_kernel<EPI><<<grid, NUM_THREADS, Plan<EPI>::SMEM_BYTES, st>>>(ma, mb, a, div_table());
+    moe_gemm_kernel<EPI><<<grid, Plan<EPI>::NUM_THREADS, Plan<EPI>::SMEM_BYTES, st>>>(ma, mb, a, div_table());
     return cudaGetLastError();
 }
 
