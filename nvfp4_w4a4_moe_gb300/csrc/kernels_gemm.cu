@@ -56,15 +56,17 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 //       releases it before computing; a 4-stage ring of 54 KB stages.
 //       Eight epilogue warps, two per TMEM lane quarter.
 //  w2:  tiles of 128 x 128, M128 N128 MMAs into two alternating accumulators,
-//       a 4-stage ring, and sixteen epilogue warps (four per lane quarter, 32
-//       columns each) so that enough of them are issuing the combine's
-//       reductions while others wait on TMEM; each has a transpose buffer.
+//       a 4-stage ring, and sixteen epilogue warps in two groups of eight that
+//       take alternate tiles (one accumulator each), so one group is issuing
+//       the combine's reductions while the other waits on TMEM and fetches
+//       its rows' tokens and weights; each warp has a transpose buffer.
 template <int EPI>
 struct Plan {
     static constexpr int BN = EPI == 0 ? 256 : 128;  // widest tile (MMA N)
     static constexpr int STAGES = 4;
     static constexpr int NUM_EPI_WARPS = EPI == 0 ? 8 : 16;
     static constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
+    static constexpr int EPI_GROUPS = EPI == 0 ? 1 : 2;  // w2: one group of eight warps per accumulator
     static constexpr int SCALE_WARP0 = 2 + NUM_EPI_WARPS;  // then the four scale writers
     static constexpr int NUM_THREADS = 64 + EPI_THREADS + 32 * NUM_SCALE_WARPS;
     static constexpr int ACC_BUFS = EPI == 0 ? 1 : 2;
@@ -84,6 +86,7 @@ struct Plan {
     static constexpr int XPOSE_BYTES = EPI == 1 ? NUM_EPI_WARPS * 32 * XPOSE_LD * 4 : 0;
     static constexpr int SMEM_BYTES = OFF_XPOSE + XPOSE_BYTES + 1024;  // + alignment slack
     static_assert(SF_TMEM_COL + STAGES * SF_COLS <= TMEM_COLS, "scale slots exceed TMEM");
+    static_assert(EPI_GROUPS == ACC_BUFS, "each epilogue group owns one accumulator");
     static_assert(SMEM_BYTES + (EPI == 0 ? (int)sizeof(DivTable2) : 0) <= 232448,
                   "shared memory plan exceeds the opt-in limit");
 };
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                   OFF_SFA = P::OFF_SFA, OFF_SFB = P::OFF_SFB, OFF_BAR = P::OFF_BAR, OFF_MISC = P::OFF_MISC,
                   OFF_XPOSE = P::OFF_XPOSE, B_BYTES = P::B_BYTES, SFB_BYTES = P::SFB_BYTES,
                   SFB_STEP = P::SFB_STEP, SF_COLS = P::SF_COLS, SF_TMEM_COL = P::SF_TMEM_COL,
-                  EPI_THREADS = P::EPI_THREADS, SCALE_WARP0 = P::SCALE_WARP0;
+                  EPI_THREADS = P::EPI_THREADS, SCALE_WARP0 = P::SCALE_WARP0, EPI_GROUPS = P::EPI_GROUPS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ DivTable2 tab;
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -292,7 +295,7 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         }
         for (int i = 0; i < ACC_BUFS; ++i) {
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], EPI_THREADS);
+            mbar_init(&acc_empty[i], EPI_THREADS / EPI_GROUPS);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -475,9 +478,10 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         }
     } else if (warp >= 2 && warp < SCALE_WARP0) {
         // ------------------------------------------------ epilogue
-        const int ew = warp - 2;          // 0 .. epilogue warps - 1
-        const int quarter = warp & 3;     // TMEM lanes this warp may read
-        const int half = ew >> 2;         // w13: which half of the tile's columns it owns; w2: which quarter
+        const int ew = warp - 2;                         // 0 .. epilogue warps - 1
+        const int group = ew / (P::NUM_EPI_WARPS / EPI_GROUPS);  // w2: tiles of this group's parity
+        const int quarter = warp & 3;                    // TMEM lanes this warp may read
+        const int half = (ew >> 2) & 1;                  // which half of the tile's columns it owns
         const int r_in = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         if (EPI == 0 && p.zero_out) {
@@ -491,13 +495,29 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                 z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         float *xp = reinterpret_cast<float *>(smem + OFF_XPOSE) + ew * 32 * XPOSE_LD;
-        uint32_t acc = 0, acc_phase = 0;
+        const uint32_t acc = EPI_GROUPS == 2 ? (uint32_t)group : 0u;
+        uint32_t acc_phase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        for (int tile = blockIdx.x + group * gridDim.x; tile < ntiles; tile += EPI_GROUPS * gridDim.x) {
+            // everything the tile needs besides the accumulator is fetched
+            // before waiting for it
             const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT);
             const int e = ti.e, nt = ti.nt;
             const int row = ti.mt * BM + r_in;
-            const bool valid = row < p.pad_off[e] + p.counts[e];
+            bool valid;
+            float s0, s1;  // w13: alpha, g2; w2: routing weight * alpha2
+            int t = 0;     // w2: token of the row
+            if (EPI == 0) {
+                valid = row < p.pad_off[e] + p.counts[e];
+                s0 = p.alpha[e];
+                s1 = p.g2[e];
+            } else {
+                const int f = p.row_src[row];  // -1 on padding rows
+                valid = f >= 0;
+                s0 = valid ? __fmul_rn(p.topk_w[f], p.alpha[e]) : 0.0f;
+                s1 = 0.0f;
+                t = valid ? f / p.k : 0;
+            }
             if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
                 ok = false;
                 break;
@@ -510,7 +530,7 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                 // hc + w0...  h = SiLU(alpha * gate) * (alpha * up) is formed
                 // 32 columns at a time and the accumulator released once all
                 // of it is in registers.
-                const float alpha = p.alpha[e], g2 = p.g2[e];
+                const float alpha = s0, g2 = s1;
                 const f32x2 aa = pack_f32x2(alpha, alpha);
                 const int hw = ti.hc >> 1, w0 = half * hw;
                 const int nblocks = hw >> 4;  // 4 or 2 blocks of 16
@@ -571,43 +591,40 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                             *reinterpret_cast<uint32_t *>(p.sf2 + swz_sf_offset(row, cc, p.kc2)) = 0u;
                 }
             } else {
-                // out[t, cols] += w[t, j] * alpha2 * y2 on this warp's 32 columns,
-                // transposed through shared memory so that each reduction
-                // instruction covers four contiguous 128-byte row segments.
-                int t = 0;
-                float scale = 0.0f;
-                if (valid) {
-                    const int f = p.row_src[row];
-                    t = f / p.k;
-                    scale = __fmul_rn(p.topk_w[f], p.alpha[e]);
-                }
+                // out[t, cols] += w[t, j] * alpha2 * y2 on this warp's 64 columns,
+                // 32 at a time, transposed through shared memory so that each
+                // reduction instruction covers four contiguous 128-byte row
+                // segments.
+                const float scale = s0;
                 const int sub = lane >> 3, cc = (lane & 7) * 4;
-                const int cbase = 32 * half;
-                float v[32];
-                tmem_ld16(col0 + cbase, v);
-                tmem_ld16(col0 + cbase + 16, v + 16);
-                tmem_wait_ld(v);
-                tc_fence_before();
-                mbar_arrive(&acc_empty[acc]);
+#pragma unroll 1
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int cbase = 64 * half + 32 * c2;
+                    float v[32];
+                    tmem_ld16(col0 + cbase, v);
+                    tmem_ld16(col0 + cbase + 16, v + 16);
+                    tmem_wait_ld(v);
+                    if (c2 == 1) {
+                        tc_fence_before();
+                        mbar_arrive(&acc_empty[acc]);
+                    }
 #pragma unroll
-                for (int i = 0; i < 32; ++i) xp[lane * XPOSE_LD + i] = v[i] * scale;
-                __syncwarp();
+                    for (int i = 0; i < 32; ++i) xp[lane * XPOSE_LD + i] = v[i] * scale;
+                    __syncwarp();
 #pragma unroll
-                for (int it = 0; it < 8; ++it) {
-                    const int rr = it * 4 + sub;
-                    const int t_r = __shfl_sync(0xffffffffu, t, rr);
-                    const int ok_r = __shfl_sync(0xffffffffu, (int)valid, rr);
-                    const float *src = xp + rr * XPOSE_LD + cc;
-                    if (ok_r)
-                        red_add_v4(p.out + (size_t)t_r * p.H + nt * 128 + cbase + cc, src[0], src[1], src[2],
-                                   src[3]);
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = it * 4 + sub;
+                        const int t_r = __shfl_sync(0xffffffffu, t, rr);
+                        const int ok_r = __shfl_sync(0xffffffffu, (int)valid, rr);
+                        const float *src = xp + rr * XPOSE_LD + cc;
+                        if (ok_r)
+                            red_add_v4(p.out + (size_t)t_r * p.H + nt * 128 + cbase + cc, src[0], src[1], src[2],
+                                       src[3]);
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
-            if (++acc == ACC_BUFS) {
-                acc = 0;
-                acc_phase ^= 1u;
-            }
+            acc_phase ^= 1u;  // each group owns one accumulator
         }
         if (!ok) {
             *abort_flag = 1;
