@@ -368,11 +368,18 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
             if (issued & (1u << s)) mbar_wait(&full[s], (last_parity >> s) & 1u, nullptr, kDrainLimitNs);
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
+        // The issuing warp shares its scheduler with busy epilogue warps, so
+        // the loop is kept short: descriptors advance by constants (a 64-K
+        // step is 32 bytes = 2 descriptor units; a stage is a fixed stride)
+        // and a full stage's four MMAs are unrolled.
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool ok = true;
+        const uint64_t da0 = desc_sw128(su32(smem + OFF_A)), db0 = desc_sw128(su32(smem + OFF_B));
+        const uint32_t sf0 = tmem + SF_TMEM_COL;
+        const int k_full = p.K / BK;  // stages with four 64-K steps
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT);
-            const uint32_t idesc = idesc_for(EPI == 0 ? 2 * ti.hc : 128);
+            const int nt = tile % NT;
+            const uint32_t idesc = idesc_for(EPI == 0 ? 2 * min(128, p.gate_up_I - 128 * nt) : 128);
             if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
                 ok = false;
                 break;
@@ -387,13 +394,19 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const int ksteps = min(4, (p.K - kt * BK + 63) / 64);
-                const uint32_t sfa_t = tmem + SF_TMEM_COL + stage * SF_COLS, sfb_t = sfa_t + 16;
-                const uint32_t sa = su32(smem + OFF_A + stage * A_BYTES);
-                const uint32_t sb = su32(smem + OFF_B + stage * B_BYTES);
-                for (int j = 0; j < ksteps; ++j)
-                    tc_mma(d, desc_sw128(sa + 32 * j), desc_sw128(sb + 32 * j), idesc, sfa_t + 4 * j,
-                           sfb_t + SFB_STEP * j, (kt | j) != 0);
+                const uint64_t da = da0 + (uint64_t)(stage * (A_BYTES >> 4));
+                const uint64_t db = db0 + (uint64_t)(stage * (B_BYTES >> 4));
+                const uint32_t sfa = sf0 + stage * SF_COLS, sfb = sfa + 16;
+                if (kt < k_full) {
+                    tc_mma(d, da, db, idesc, sfa, sfb, kt != 0);
+                    tc_mma(d, da + 2, db + 2, idesc, sfa + 4, sfb + SFB_STEP, 1u);
+                    tc_mma(d, da + 4, db + 4, idesc, sfa + 8, sfb + 2 * SFB_STEP, 1u);
+                    tc_mma(d, da + 6, db + 6, idesc, sfa + 12, sfb + 3 * SFB_STEP, 1u);
+                } else {
+                    const int ksteps = (p.K - kt * BK) / 64;
+                    for (int j = 0; j < ksteps; ++j)
+                        tc_mma(d, da + 2 * j, db + 2 * j, idesc, sfa + 4 * j, sfb + SFB_STEP * j, (kt | j) != 0);
+                }
                 tc_commit(&empty[stage]);
                 if (++stage == STAGES) {
                     stage = 0;
