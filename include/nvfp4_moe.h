@@ -241,10 +241,18 @@ int nvfp4_moe_forward_profiled(const nvfp4_moe_weights *w, const void *prepared,
 /*
  * nvfp4_moe_forward_host -- the same layer with HOST activations and routing:
  * copies x_host [T, H] BF16, topk_ids_host [T, k], topk_weights_host [T, k]
- * into the workspace, runs nvfp4_moe_forward and copies out [T, H] FP32 back
- * to out_host.  Host buffers should be page-locked for the copies to be
- * asynchronous.  SYNCHRONOUS: returns after out_host is written.
- * Workspace: nvfp4_moe_host_workspace_size(T, H, I, E, k) bytes.
+ * into the workspace, runs the layer and copies out [T, H] FP32 back to
+ * out_host.  From 4096 tokens on, the tokens are processed in up to 8 chunks
+ * (2048 first and last, up to 4096 between), each chunk's copy-in and the
+ * previous chunk's copy-out overlapping the layer on other streams (tokens
+ * are independent, so the result is that of one call).  Host buffers should
+ * be page-locked for the copies to overlap.  SYNCHRONOUS: returns after
+ * out_host is written and no copy of the call is in flight, also on error.
+ * The scale check follows `flags` for the first chunk and runs on the device
+ * for every chunk; a failure in any chunk is returned (its part of out_host
+ * is then unspecified).  Not reentrant per device: concurrent calls on one
+ * device serialise.  Workspace: nvfp4_moe_host_workspace_size(T, H, I, E, k)
+ * bytes.
  */
 size_t nvfp4_moe_host_workspace_size(int T, int H, int I, int E, int k);
 int nvfp4_moe_forward_host(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x_host,

@@ -135,6 +135,7 @@ WsLayout make_layout(int T, int H, int I, int E, int k)
     L.ids_stage = take(sizeof(int32_t) * (size_t)R);
     L.w_stage = take(sizeof(float) * (size_t)R);
     L.out_stage = take(sizeof(float) * (size_t)T * H);
+    L.status_stage = take(sizeof(DevHeader) * (size_t)kMaxHostChunks);
     L.host_end = o;
     return L;
 }
@@ -570,6 +571,46 @@ int nvfp4_moe_forward_profiled(const nvfp4_moe_weights *w, const void *prepared,
                         (cudaStream_t)stream, events);
 }
 
+// Token chunks of the pipelined host entry point.  Tokens are independent, so
+// the layer runs chunk by chunk while the next chunk's inputs are copied in
+// and the previous chunk's output is copied out.  Small first and last chunks
+// shorten the copy-in head and the copy-out tail that nothing overlaps; the
+// middle chunks are large enough to keep the GEMMs efficient.
+static std::vector<std::pair<int, int>> host_chunks(int T)
+{
+    std::vector<std::pair<int, int>> c;
+    constexpr int kEdge = 2048, kMid = 4096;
+    if (T < 2 * kEdge) {
+        c.push_back({0, T});
+        return c;
+    }
+    const int mid = T - 2 * kEdge;
+    int nmid = mid == 0 ? 0 : (mid + kMid - 1) / kMid;
+    if (nmid > kMaxHostChunks - 2) nmid = kMaxHostChunks - 2;
+    c.push_back({0, kEdge});
+    int t0 = kEdge;
+    for (int i = 0; i < nmid; ++i) {
+        const int n = (mid - (t0 - kEdge) + (nmid - i) - 1) / (nmid - i);
+        c.push_back({t0, n});
+        t0 += n;
+    }
+    c.push_back({t0, kEdge});
+    return c;
+}
+
+namespace {
+// Copy streams and events of the host entry point, one set per device,
+// created on first use.  A call holds the device's mutex from its first
+// enqueue to its final synchronisation, so sets are never shared by two calls.
+struct HostPipe {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, in_done[kMaxHostChunks], fwd_done[kMaxHostChunks], out_done[kMaxHostChunks];
+};
+HostPipe g_pipes[64];
+}  // namespace
+
 int nvfp4_moe_forward_host(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x_host, int T,
                            const int32_t *topk_ids_host, const float *topk_weights_host, int k, float *out_host,
                            void *ws, size_t ws_bytes, unsigned flags, nvfp4_stream_t stream)
@@ -584,24 +625,91 @@ int nvfp4_moe_forward_host(const nvfp4_moe_weights *w, const void *prepared, con
     if (ws_bytes < L.host_end)
         return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "host workspace %zu < %zu", ws_bytes, L.host_end);
     if (T == 0) return NVFP4_OK;
+    int dev = 0;
+    NV_CUDA(cudaGetDevice(&dev), "querying the device");
+    if (dev < 0 || dev >= 64) return fail(NVFP4_ERR_CUDA, "device %d out of range", dev);
+    HostPipe &P = g_pipes[dev];
+    std::lock_guard<std::mutex> lock(P.mu);
+    if (!P.ready) {
+        NV_CUDA(cudaStreamCreateWithFlags(&P.in, cudaStreamNonBlocking), "creating a copy stream");
+        NV_CUDA(cudaStreamCreateWithFlags(&P.out, cudaStreamNonBlocking), "creating a copy stream");
+        NV_CUDA(cudaEventCreateWithFlags(&P.start, cudaEventDisableTiming), "creating an event");
+        for (int i = 0; i < kMaxHostChunks; ++i) {
+            NV_CUDA(cudaEventCreateWithFlags(&P.in_done[i], cudaEventDisableTiming), "creating an event");
+            NV_CUDA(cudaEventCreateWithFlags(&P.fwd_done[i], cudaEventDisableTiming), "creating an event");
+            NV_CUDA(cudaEventCreateWithFlags(&P.out_done[i], cudaEventDisableTiming), "creating an event");
+        }
+        P.ready = true;
+    }
     cudaStream_t st = (cudaStream_t)stream;
     uint8_t *base = static_cast<uint8_t *>(ws);
     uint16_t *x = reinterpret_cast<uint16_t *>(base + L.x_stage);
     int32_t *ids = reinterpret_cast<int32_t *>(base + L.ids_stage);
     float *tw = reinterpret_cast<float *>(base + L.w_stage);
     float *out = reinterpret_cast<float *>(base + L.out_stage);
-    const size_t R = (size_t)T * k;
-    NV_CUDA(cudaMemcpyAsync(x, x_host, sizeof(uint16_t) * (size_t)T * w->H, cudaMemcpyHostToDevice, st), "copying x");
-    NV_CUDA(cudaMemcpyAsync(ids, topk_ids_host, sizeof(int32_t) * R, cudaMemcpyHostToDevice, st), "copying ids");
-    NV_CUDA(cudaMemcpyAsync(tw, topk_weights_host, sizeof(float) * R, cudaMemcpyHostToDevice, st), "copying weights");
-    rc = forward_impl(w, prepared, x, T, ids, tw, k, out, ws, ws_bytes, flags & ~NVFP4_DEBUG_KEEP_H, st);
-    if (rc) return rc;
-    NV_CUDA(cudaMemcpyAsync(out_host, out, sizeof(float) * (size_t)T * w->H, cudaMemcpyDeviceToHost, st),
-            "copying out");
-    DevHeader h;
-    rc = read_header(base + L.hdr, st, &h);
-    if (rc) return rc;
-    return header_status(h, nullptr);
+    DevHeader *status = reinterpret_cast<DevHeader *>(base + L.status_stage);
+    const size_t H = (size_t)w->H;
+    const std::vector<std::pair<int, int>> chunks = host_chunks(T);
+    const int n = (int)chunks.size();
+
+    // Everything already on the caller's stream (earlier users of this
+    // workspace) completes before the copy streams touch it.
+    NV_CUDA(cudaEventRecord(P.start, st), "recording an event");
+    NV_CUDA(cudaStreamWaitEvent(P.in, P.start, 0), "ordering the copy stream");
+    NV_CUDA(cudaStreamWaitEvent(P.out, P.start, 0), "ordering the copy stream");
+    for (int c = 0; c < n; ++c) {
+        const size_t t0 = (size_t)chunks[c].first, tc = (size_t)chunks[c].second;
+        NV_CUDA(cudaMemcpyAsync(x + t0 * H, x_host + t0 * H, sizeof(uint16_t) * tc * H, cudaMemcpyHostToDevice, P.in),
+                "copying x");
+        NV_CUDA(cudaMemcpyAsync(ids + t0 * k, topk_ids_host + t0 * k, sizeof(int32_t) * tc * k,
+                                cudaMemcpyHostToDevice, P.in),
+                "copying ids");
+        NV_CUDA(cudaMemcpyAsync(tw + t0 * k, topk_weights_host + t0 * k, sizeof(float) * tc * k,
+                                cudaMemcpyHostToDevice, P.in),
+                "copying weights");
+        NV_CUDA(cudaEventRecord(P.in_done[c], P.in), "recording an event");
+    }
+    int first_rc = NVFP4_OK;
+    for (int c = 0; c < n; ++c) {
+        const size_t t0 = (size_t)chunks[c].first;
+        const int tc = chunks[c].second;
+        NV_CUDA(cudaStreamWaitEvent(st, P.in_done[c], 0), "ordering the compute stream");
+        // The first chunk checks the scales as the caller asked (with a host
+        // synchronisation unless they were pre-validated); the device keeps
+        // checking them in every chunk, and each chunk's status is saved.
+        const unsigned cf = (flags & ~(NVFP4_DEBUG_KEEP_H | NVFP4_SYNC_CHECK)) |
+                            (c > 0 ? (unsigned)NVFP4_SCALES_PREVALIDATED : 0u);
+        rc = forward_impl(w, prepared, x + t0 * H, tc, ids + t0 * k, tw + t0 * k, k, out + t0 * H, ws, ws_bytes,
+                          cf, st);
+        if (rc) {
+            first_rc = rc;
+            break;
+        }
+        NV_CUDA(cudaMemcpyAsync(status + c, base + L.hdr, sizeof(DevHeader), cudaMemcpyDeviceToDevice, st),
+                "saving the chunk status");
+        NV_CUDA(cudaEventRecord(P.fwd_done[c], st), "recording an event");
+        NV_CUDA(cudaStreamWaitEvent(P.out, P.fwd_done[c], 0), "ordering the copy stream");
+        NV_CUDA(cudaMemcpyAsync(out_host + t0 * H, out + t0 * H, sizeof(float) * (size_t)tc * H,
+                                cudaMemcpyDeviceToHost, P.out),
+                "copying out");
+        NV_CUDA(cudaEventRecord(P.out_done[c], P.out), "recording an event");
+    }
+    // Nothing of this call is left in flight when it returns: the caller may
+    // reuse its host buffers at once, also after an error.
+    NV_CUDA(cudaStreamSynchronize(P.in), "synchronising the copy stream");
+    NV_CUDA(cudaStreamSynchronize(P.out), "synchronising the copy stream");
+    if (first_rc) {
+        NV_CUDA(cudaStreamSynchronize(st), "synchronising the stream");
+        return first_rc;
+    }
+    DevHeader h[kMaxHostChunks];
+    NV_CUDA(cudaMemcpyAsync(h, status, sizeof(DevHeader) * n, cudaMemcpyDeviceToHost, st), "reading the status");
+    NV_CUDA(cudaStreamSynchronize(st), "synchronising the stream");
+    for (int c = 0; c < n; ++c) {
+        rc = header_status(h[c], nullptr);
+        if (rc) return rc;
+    }
+    return NVFP4_OK;
 }
 
 int nvfp4_moe_status(const void *ws, nvfp4_stream_t stream, int *first_bad_host)

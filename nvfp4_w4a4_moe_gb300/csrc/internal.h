@@ -19,8 +19,10 @@ struct WsLayout {
     size_t hdr, g1, g2, alpha1, alpha2, counts, offsets, pad_off, chunk_hist, row_of, perm, row_src,
         tile_expert, a1q, sf1, a2q, sf2, end;
     // forward_host staging (after `end`), and the optional FP32 h dump
-    size_t x_stage, ids_stage, w_stage, out_stage, host_end;
+    size_t x_stage, ids_stage, w_stage, out_stage, status_stage, host_end;
 };
+
+constexpr int kMaxHostChunks = 8;  // token chunks of the pipelined host entry point
 
 constexpr int kRouteChunk = 2048;  // routed rows per routing CTA
 

@@ -153,6 +153,30 @@ def test_host_entry_point_matches_device_path(m):
     assert_close(out_h.numpy(), host(out_d).astype(np.float64), "host vs device entry point")
 
 
+def test_host_entry_point_chunked_prefill(m, prefill):
+    """From 4096 tokens on the host entry point runs the layer in token chunks
+    with the copies overlapped; the result equals the device entry point's
+    (up to the order of the combine's FP32 additions), and an out-of-range
+    expert id in the last chunk is still reported."""
+    layer, W = prefill
+    w = device_weights(W)
+    out_d, _ = m.moe_forward(w, dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w), flags=m.SYNC_CHECK)
+    xh = torch.from_numpy(layer.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ih = torch.from_numpy(layer.topk_ids).pin_memory()
+    wh = torch.from_numpy(layer.topk_w).pin_memory()
+    out_h, ws = m.moe_forward_host(w, xh, ih, wh)
+    got, ref = out_h.numpy().astype(np.float64), host(out_d).astype(np.float64)
+    assert np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max()
+    toks = np.sort(np.random.default_rng([layer.seed, 2]).choice(layer.T, 16, replace=False))
+    assert_close(got[toks], oracle.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W, tokens=toks)["out"][toks],
+                 "chunked host entry point")
+    bad = layer.topk_ids.copy()
+    bad[-1, 0] = layer.E
+    with pytest.raises(m.Nvfp4Error) as ei:
+        m.moe_forward_host(w, xh, torch.from_numpy(bad).pin_memory(), wh, ws=ws)
+    assert ei.value.status == m.ERR_INVALID_ARG
+
+
 def test_weight_quantiser_matches_oracle_weight_path(m):
     """The device weight quantiser against the oracle's static weight path."""
     r = np.random.default_rng(11)
