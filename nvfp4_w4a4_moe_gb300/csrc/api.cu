@@ -175,7 +175,7 @@ static int header_status(const DevHeader &h, int *first_bad)
                     h.first_bad);
     if (h.status == 3 || (h.error_flags & kErrBadExpertId))
         return fail(NVFP4_ERR_INVALID_ARG, "an expert id is outside [0, E)");
-    if (h.error_flags & (kErrTimeoutProducer | kErrTimeoutMma | kErrTimeoutEpilogue))
+    if (h.status == 5 || (h.error_flags & (kErrTimeoutProducer | kErrTimeoutMma | kErrTimeoutEpilogue | kErrTimeoutRoute)))
         return fail(NVFP4_ERR_DEVICE_TIMEOUT, "a device-side wait expired (flags 0x%x)", h.error_flags);
     return NVFP4_OK;
 }

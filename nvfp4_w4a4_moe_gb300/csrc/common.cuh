@@ -36,7 +36,7 @@ constexpr float kFltMax = 3.40282346638528859812e+38f;
 
 // Device-side status block at the start of every workspace.
 struct DevHeader {
-    int status;          // 0 = ok, 2 = a scale slot failed validation, 3 = bad expert id
+    int status;          // 0 = ok, 2 = a scale slot failed validation, 3 = bad expert id, 5 = device timeout
     int bad_count;       // number of bad scale slots
     int first_bad;       // lowest bad slot index (INT_MAX when none)
     int error_flags;     // kErr* bits below
@@ -51,6 +51,7 @@ enum : int {
     kErrTimeoutProducer = 2,
     kErrTimeoutMma = 4,
     kErrTimeoutEpilogue = 8,
+    kErrTimeoutRoute = 16,
 };
 
 // RN, saturating FP32 -> E4M3 (t >= 0): the byte of the second source.

@@ -65,48 +65,84 @@ __global__ void __launch_bounds__(256) validate_kernel(ValidateArgs a)
 // GEMMs run as one grouped GEMM.  Order inside an expert: ascending routed
 // row f = t*k + j (stable), which makes the permutation unique.
 //
-// route_hist_kernel: per-chunk expert histogram; the last CTA to finish scans
-// them (exclusive over chunks per expert, then over experts), producing the
-// compact offsets, the 128-row-padded offsets used by the grouped GEMM, the
-// m-tile -> expert map and the padding entries of row_src.
-__global__ void __launch_bounds__(256) route_hist_kernel(RouteArgs a)
+// One cooperative launch (every CTA resident) over chunks of kRouteChunk
+// routed rows, in two phases around a grid barrier:
+//   1. per-chunk expert histograms (shared-memory atomics) -> chunk_hist;
+//      an out-of-range id raises kErrBadExpertId.
+//   2. every CTA reads all chunk histograms and forms, by warp scans, the
+//      compact and 128-row-padded expert offsets (identical in every CTA); the
+//      CTAs share out the m-tile -> expert map and the padding entries of
+//      row_src; then each chunk is scattered: its warps own contiguous 256-row
+//      slices, per-warp histograms give each warp's first rank per expert, and
+//      equal experts inside a 32-row step are ranked with __match_any_sync.
+// The barrier counter is the header's done_count, cleared by the scale check
+// that precedes every routing launch; its wait is bounded.
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kRouteSlice = kRouteChunk / kRouteWarps;  // rows per warp per chunk
+constexpr int kRouteIdsPerLane = kRouteSlice / 32;
+
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
 {
     extern __shared__ int sh[];
-    __shared__ int s_last;
-    int *hist = sh;
+    __shared__ int s_fail;
     const int E = a.E;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-    __syncthreads();
-    if (a.hdr->status != 0) return;
-    const int f0 = blockIdx.x * kRouteChunk, f1 = min(a.R, f0 + kRouteChunk);
-    for (int f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
-        const int e = a.ids[f];
-        if (e < 0 || e >= E)
-            atomicOr(&a.hdr->error_flags, kErrBadExpertId);
-        else
-            atomicAdd(&hist[e], 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (a.hdr->status != 0) return;  // same value in every CTA (set by the previous kernel)
+
+    // ---- phase 1: chunk histograms
+    int *hist = sh;  // [E]
+    for (int c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
+        for (int e = tid; e < E; e += kRouteThreads) hist[e] = 0;
+        __syncthreads();
+        const int f0 = c * kRouteChunk, f1 = min(a.R, f0 + kRouteChunk);
+        for (int f = f0 + tid; f < f1; f += kRouteThreads) {
+            const int e = a.ids[f];
+            if (e < 0 || e >= E)
+                atomicOr(&a.hdr->error_flags, kErrBadExpertId);
+            else
+                atomicAdd(&hist[e], 1);
+        }
+        __syncthreads();
+        for (int e = tid; e < E; e += kRouteThreads) a.chunk_hist[(size_t)c * E + e] = hist[e];
+        __syncthreads();
+    }
+
+    // ---- grid barrier
+    if (tid == 0) {
+        s_fail = 0;
+        __threadfence();
+        atomicAdd(&a.hdr->done_count, 1u);
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+            unsigned v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(&a.hdr->done_count) : "memory");
+            if (v >= gridDim.x) break;
+            if (global_timer_ns() - t0 > 1000000000ull) {
+                atomicOr(&a.hdr->error_flags, kErrTimeoutRoute);
+                a.hdr->status = 5;
+                s_fail = 1;
+                break;
+            }
+        }
+        __threadfence();
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) a.chunk_hist[(size_t)blockIdx.x * E + e] = hist[e];
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = (atomicAdd(&a.hdr->done_count, 1u) == gridDim.x - 1);
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
+    if (s_fail) return;
     if (__ldcg(&a.hdr->error_flags) & kErrBadExpertId) {
-        if (threadIdx.x == 0) a.hdr->status = 3;  // nothing after this writes
+        if (blockIdx.x == 0 && tid == 0) a.hdr->status = 3;  // nothing after this writes
         return;
     }
 
-    int *cnt = sh;            // [E]
-    int *off = sh + E;        // [E + 1]
-    int *poff = sh + 2 * E + 1;  // [E + 1]
-    // Per expert, exclusive prefix over the chunks.  The chunk counts are all
-    // loaded before any is rewritten, so the loads overlap instead of forming
-    // a chain of dependent round trips.
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = 0;
+    // ---- phase 2: offsets (every CTA), this CTA's chunk prefixes
+    const int own = (a.nchunks - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // chunks of this CTA
+    int *cnt = sh;                    // [E]
+    int *off = cnt + E;               // [E + 1]
+    int *poff = off + E + 1;          // [E + 1]
+    int *wbase = poff + E + 1;        // [kRouteWarps][E]
+    int *cpre = wbase + kRouteWarps * E;  // [own][E]: chunk's first rank per expert
+    for (int e = tid; e < E; e += kRouteThreads) {
+        int run = 0, next_own = (int)blockIdx.x, i_own = 0;
         for (int c0 = 0; c0 < a.nchunks; c0 += 16) {
             int v[16];
             const int n = min(16, a.nchunks - c0);
@@ -114,18 +150,21 @@ __global__ void __launch_bounds__(256) route_hist_kernel(RouteArgs a)
             for (int i = 0; i < 16; ++i) v[i] = i < n ? __ldcg(&a.chunk_hist[(size_t)(c0 + i) * E + e]) : 0;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                if (i < n) a.chunk_hist[(size_t)(c0 + i) * E + e] = run;
+                if (c0 + i == next_own && i < n) {
+                    cpre[i_own * E + e] = run;
+                    ++i_own;
+                    next_own += gridDim.x;
+                }
                 run += v[i];
             }
         }
         cnt[e] = run;
-        a.counts[e] = run;
+        if (blockIdx.x == 0) a.counts[e] = run;
     }
     __syncthreads();
-    // Exclusive scans over experts (compact, and padded to 128-row tiles) by
-    // warp 0, 32 experts per step.
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
+    // exclusive scans over experts (compact, and padded to 128-row tiles) by
+    // warp 0, 32 experts per step
+    if (warp == 0) {
         int base_o = 0, base_p = 0;
         for (int e0 = 0; e0 < E; e0 += 32) {
             const int e = e0 + lane;
@@ -150,22 +189,24 @@ __global__ void __launch_bounds__(256) route_hist_kernel(RouteArgs a)
         if (lane == 0) {
             off[E] = base_o;
             poff[E] = base_p;
-            a.hdr->num_mtiles = base_p >> 7;
+            if (blockIdx.x == 0) a.hdr->num_mtiles = base_p >> 7;
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-        a.offsets[e] = off[e];
-        a.pad_off[e] = poff[e];
-        if (a.offsets_out) a.offsets_out[e] = off[e];
+    if (blockIdx.x == 0) {
+        for (int e = tid; e <= E; e += kRouteThreads) {
+            a.offsets[e] = off[e];
+            a.pad_off[e] = poff[e];
+            if (a.offsets_out) a.offsets_out[e] = off[e];
+        }
     }
-    // m-tile -> expert map: every thread takes m-tiles and finds the expert
-    // whose padded range holds the tile (binary search over the offsets).
+    // m-tile -> expert map, shared out over the grid: binary search for the
+    // last expert whose padded range starts at or before the tile
     if (a.tile_expert) {
         const int ntile = poff[E] >> 7;
-        for (int mtile = threadIdx.x; mtile < ntile; mtile += blockDim.x) {
+        for (int mtile = blockIdx.x * kRouteThreads + tid; mtile < ntile; mtile += gridDim.x * kRouteThreads) {
             const int row = mtile << 7;
-            int lo = 0, hi = E - 1;  // last e with poff[e] <= row
+            int lo = 0, hi = E - 1;
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
                 if (poff[mid] <= row)
@@ -176,61 +217,59 @@ __global__ void __launch_bounds__(256) route_hist_kernel(RouteArgs a)
             a.tile_expert[mtile] = lo;
         }
     }
-    // padding rows of each expert's last tile: one warp per expert at a time
+    // padding rows of each expert's last tile: one warp per expert
     if (a.row_src) {
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-        for (int e = warp; e < E; e += nwarps)
+        for (int e = blockIdx.x * kRouteWarps + warp; e < E; e += gridDim.x * kRouteWarps)
             for (int r = poff[e] + cnt[e] + lane; r < poff[e + 1]; r += 32) a.row_src[r] = -1;
     }
-}
 
-// route_scatter_kernel: stable ranks.  Each of the 8 warps owns a contiguous
-// 256-row slice of the chunk; per-warp histograms give each warp's starting
-// rank per expert, and the warp walks its slice in order, ranking equal
-// experts inside each 32-row step with __match_any_sync.
-__global__ void __launch_bounds__(256) route_scatter_kernel(RouteArgs a)
-{
-    extern __shared__ int sh[];  // [8][E]
-    const int E = a.E;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int *wb = sh + warp * E;
-    for (int e = lane; e < E; e += 32) wb[e] = 0;
-    __syncthreads();
-    if (a.hdr->status != 0) return;
-    const int f0 = blockIdx.x * kRouteChunk;
-    const int wf0 = f0 + warp * (kRouteChunk / 8);
-    const int wf1 = min(a.R, wf0 + kRouteChunk / 8);
-    for (int f = wf0 + lane; f < wf1; f += 32) {
-        const int e = a.ids[f];
-        if (e >= 0 && e < E) atomicAdd(&wb[e], 1);
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = a.chunk_hist[(size_t)blockIdx.x * E + e];
-        for (int w = 0; w < 8; ++w) {
-            const int v = sh[w * E + e];
-            sh[w * E + e] = run;
-            run += v;
+    // ---- phase 2: scatter this CTA's chunks
+    int *wb = wbase + warp * E;
+    int i_own = 0;
+    for (int c = blockIdx.x; c < a.nchunks; c += gridDim.x, ++i_own) {
+        const int wf0 = c * kRouteChunk + warp * kRouteSlice;
+        int ids[kRouteIdsPerLane];
+#pragma unroll
+        for (int i = 0; i < kRouteIdsPerLane; ++i) {
+            const int f = wf0 + 32 * i + lane;
+            ids[i] = f < a.R ? a.ids[f] : -1;  // ids are valid here (checked above)
         }
-    }
-    __syncthreads();
-    for (int base = wf0; base < wf1; base += 32) {
-        const int f = base + lane;
-        int e = (f < wf1) ? a.ids[f] : -1;
-        if (e >= E) e = -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int rank = __popc(peers & ((1u << lane) - 1u));
-        const int pos = (e >= 0) ? wb[e] + rank : 0;
+        for (int e = lane; e < E; e += 32) wb[e] = 0;
         __syncwarp();
-        if (e >= 0 && rank == 0) wb[e] += __popc(peers);
-        __syncwarp();
-        if (e >= 0) {
-            const int compact = a.offsets[e] + pos;
-            const int padded = a.pad_off[e] + pos;
-            a.row_of[f] = a.padded ? padded : compact;
-            if (a.perm) a.perm[compact] = f;
-            if (a.row_src) a.row_src[padded] = f;
+#pragma unroll
+        for (int i = 0; i < kRouteIdsPerLane; ++i)
+            if (ids[i] >= 0) atomicAdd(&wb[ids[i]], 1);
+        __syncthreads();
+        // each warp's first rank per expert: the chunk's rank plus the
+        // earlier warps' counts
+        for (int e = tid; e < E; e += kRouteThreads) {
+            int run = cpre[i_own * E + e];
+            for (int w = 0; w < kRouteWarps; ++w) {
+                const int v = wbase[w * E + e];
+                wbase[w * E + e] = run;
+                run += v;
+            }
         }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kRouteIdsPerLane; ++i) {
+            const int f = wf0 + 32 * i + lane;
+            const int e = ids[i];
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            const int pos = (e >= 0) ? wb[e] + rank : 0;
+            __syncwarp();
+            if (e >= 0 && rank == 0) wb[e] += __popc(peers);
+            __syncwarp();
+            if (e >= 0) {
+                const int compact = off[e] + pos;
+                const int padded = poff[e] + pos;
+                a.row_of[f] = a.padded ? padded : compact;
+                if (a.perm) a.perm[compact] = f;
+                if (a.row_src) a.row_src[padded] = f;
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -451,13 +490,32 @@ cudaError_t launch_validate(const ValidateArgs &a, cudaStream_t st)
 
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st)
 {
-    const size_t sh1 = sizeof(int) * (3 * (size_t)a.E + 2);
-    route_hist_kernel<<<a.nchunks, 256, sh1, st>>>(a);
-    cudaError_t err = cudaGetLastError();
+    // A cooperative launch of at most as many CTAs as can be resident at
+    // once, each taking every gridDim-th chunk.
+    static int resident[64] = {0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const size_t sh2 = sizeof(int) * 8 * (size_t)a.E;
-    route_scatter_kernel<<<a.nchunks, 256, sh2, st>>>(a);
-    return cudaGetLastError();
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    const int max_own = 8;  // chunks per CTA the shared-memory plan allows for
+    auto smem_for = [&](int E) { return sizeof(int) * ((3 + kRouteWarps + max_own) * (size_t)E + 2); };
+    const size_t smem = smem_for(a.E);
+    if (!resident[dev]) {
+        // sized once for the largest expert count, so any call fits
+        const size_t smem_max = smem_for(1024);
+        err = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
+        if (err != cudaSuccess) return err;
+        int per_sm = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_kernel, kRouteThreads, smem_max);
+        if (err != cudaSuccess) return err;
+        resident[dev] = (per_sm < 1 ? 1 : per_sm) * sm_count();
+    }
+    int grid = a.nchunks < resident[dev] ? a.nchunks : resident[dev];
+    if (grid < 1) grid = 1;
+    if ((a.nchunks + grid - 1) / grid > max_own) return cudaErrorInvalidConfiguration;
+    RouteArgs args = a;
+    void *params[] = {&args};
+    return cudaLaunchCooperativeKernel((const void *)route_kernel, dim3(grid), dim3(kRouteThreads), params, smem, st);
 }
 
 cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st)
