@@ -494,7 +494,8 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         const int ew = warp - 2;                         // 0 .. epilogue warps - 1
         const int group = ew / (P::NUM_EPI_WARPS / EPI_GROUPS);  // w2: tiles of this group's parity
         const int quarter = warp & 3;                    // TMEM lanes this warp may read
-        const int half = (ew >> 2) & 1;                  // which half of the tile's columns it owns
+        const int half = (ew >> 2) & 1;                  // w2: which half of the tile's columns it owns
+        const int part = ew >> 2;                        // w13: which slice of the tile's h columns
         const int r_in = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         if (EPI == 0 && p.zero_out) {
@@ -545,8 +546,8 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                 // of it is in registers.
                 const float alpha = s0, g2 = s1;
                 const f32x2 aa = pack_f32x2(alpha, alpha);
-                const int hw = ti.hc >> 1, w0 = half * hw;
-                const int nblocks = hw >> 4;  // 4 or 2 blocks of 16
+                const int hw = ti.hc / (P::NUM_EPI_WARPS / 4), w0 = part * hw;
+                const int nblocks = hw >> 4;  // blocks of 16 of this warp
                 f32x2 h[4][8];
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -597,9 +598,11 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                     uint8_t *sfp = p.sf2 + swz_sf_offset(row, hcol_tile >> 6, p.kc2) + ((hcol_tile & 63) >> 4);
                     if (nblocks == 4)
                         *reinterpret_cast<uint32_t *>(sfp) = sfw;
-                    else
+                    else if (nblocks == 2)
                         *reinterpret_cast<uint16_t *>(sfp) = (uint16_t)sfw;
-                    if (nt == NT - 1 && half == 0)
+                    else
+                        *sfp = (uint8_t)sfw;
+                    if (nt == NT - 1 && part == 0)
                         for (int cc = p.I >> 6; cc < p.kc2; ++cc)
                             *reinterpret_cast<uint32_t *>(p.sf2 + swz_sf_offset(row, cc, p.kc2)) = 0u;
                 }
