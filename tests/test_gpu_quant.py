@@ -112,6 +112,27 @@ def test_single_expert_and_ragged(m):
     run_and_compare(m, x, ids, np.full(4, 1e-3, np.float32), 4)
 
 
+def test_routing_more_chunks_than_resident_ctas(m):
+    """1.2 M routed rows: the routing kernel's cooperative grid is smaller
+    than its 2048-row chunk count, so CTAs take several chunks each."""
+    r = np.random.default_rng(21)
+    T, k, E = 150000, 8, 128
+    x = S.normal_bf16(r, (T, 64), 1.0)
+    ids, _ = S.uniform_topk(r, T, E, k)
+    scale = np.exp(r.uniform(-8, -4, E)).astype(np.float32)
+    run_and_compare(m, x, ids, scale, E, layouts=(0,))
+
+
+def test_routing_max_experts(m):
+    """E = 1024 with top-32 (the largest routing shared-memory plan)."""
+    r = np.random.default_rng(22)
+    T, k, E = 300, 32, 1024
+    x = S.normal_bf16(r, (T, 64), 1.0)
+    ids = np.stack([r.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    scale = np.exp(r.uniform(-8, -4, E)).astype(np.float32)
+    run_and_compare(m, x, ids, scale, E)
+
+
 def test_empty_batch(m):
     x = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
     ids = torch.zeros((0, 2), dtype=torch.int32, device="cuda")

@@ -73,9 +73,20 @@ def test_stack_of_30_layers():
             xo = oracle.residual_rmsnorm(x_orc[tokens], ref["out"][tokens].astype(np.float32), 1e-6)
             xg = host(x_next.view(torch.int16)).view(np.uint16)[tokens]
             gf, of = S.f32_from_bf16_bits(xg), S.f32_from_bf16_bits(xo)
-            # the two sides' FP32 outputs differ in the last bits, so a BF16 rounding
-            # of the next input may land one step apart, rarely
-            assert np.all(np.abs(gf - of) <= np.abs(of) * 2.0 ** -7 * 1.0001), f"layer {layer}: next input"
+            # The two sides' FP32 outputs differ in the last bits.  That difference
+            # passes through the normalisation as an absolute one (|d out| times the
+            # row's 1/rms), and each side then rounds to BF16: the next inputs may be
+            # one BF16 step apart plus that propagated difference (which dominates
+            # only where x + out nearly cancels), plus FP32 arithmetic noise.
+            o_gpu = host(out_gpu)[tokens].astype(np.float64)
+            o_ref = ref["out"][tokens].astype(np.float64)
+            s = S.f32_from_bf16_bits(x_orc[tokens]).astype(np.float64) + o_ref
+            rinv = 1.0 / np.sqrt((s * s).mean(axis=1, keepdims=True) + 1e-6)
+            bound = (np.maximum(np.abs(gf), np.abs(of)) * 2.0 ** -7 * 1.0001 + np.abs(o_gpu - o_ref) * rinv * 1.01
+                     + 1e-6)
+            over = np.abs(gf - of) - bound
+            assert np.all(over <= 0), (f"layer {layer}: next input, {(over > 0).sum()} values beyond the bound, "
+                                       f"worst |d| {np.abs(gf - of).flat[over.argmax()]:.3e} vs {bound.flat[over.argmax()]:.3e}")
             assert (xg != xo).mean() <= 1e-3, f"layer {layer}: {(xg != xo).mean():.2e} of next-input values differ"
             rows.append((layer, round(mx, 7), round(fro, 9), float((xg != xo).mean())))
             x_orc[tokens] = xo
