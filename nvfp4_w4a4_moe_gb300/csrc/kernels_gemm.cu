@@ -242,11 +242,22 @@ struct TileInfo {
     int nblk;  // 128-row scale blocks of the B tile (w13 full: 2, else 1)
 };
 template <int EPI>
-__device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, int NT)
+__device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, int NT, int MT)
 {
     TileInfo<EPI> ti;
-    ti.mt = tile / NT;
-    ti.nt = tile - ti.mt * NT;
+    if (EPI == 0) {
+        // m-tile major: the CTAs working at one time share a few A tiles
+        ti.mt = tile / NT;
+        ti.nt = tile - ti.mt * NT;
+    } else {
+        // column-block major: at any time the combine's reductions touch one or
+        // two 128-column blocks of `out` (4 MB at 8192 tokens), which stay in
+        // L2 instead of being evicted and re-read from HBM between the k
+        // contributions to each row; an expert's m-tiles stay adjacent, so its
+        // B tile is reused from L2
+        ti.nt = tile / MT;
+        ti.mt = tile - ti.nt * MT;
+    }
     ti.e = p.tile_expert[ti.mt];
     if (EPI == 0) {
         ti.hc = min(128, p.gate_up_I - 128 * ti.nt);
@@ -282,7 +293,8 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (p.hdr->status != 0) return;
     const int NT = EPI == 0 ? (p.gate_up_I + 127) / 128 : p.N / 128;
-    const int ntiles = p.hdr->num_mtiles * NT;
+    const int MT = p.hdr->num_mtiles;
+    const int ntiles = MT * NT;
     if ((int)blockIdx.x >= ntiles) return;
     const int KT = (p.K + BK - 1) / BK;
 
@@ -321,7 +333,7 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         bool ok = true;
         const size_t b_sf_expert = (size_t)(p.N / 128) * p.b_kc * SF_TILE;  // prepared scale bytes per expert
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT);
+            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT, MT);
             const uint8_t *b_sf = p.b_sf + (size_t)ti.e * b_sf_expert +
                                   (size_t)(EPI == 0 ? 2 * ti.nt : ti.nt) * p.b_kc * SF_TILE;
             const uint32_t b_bytes = EPI == 0 ? (uint32_t)ti.hc * 2 * (BK / 2) : (uint32_t)B_BYTES;
@@ -444,7 +456,7 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         uint32_t stage = 0, phase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT);
+            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT, MT);
             for (int kt = 0; kt < KT; ++kt) {
                 if (!mbar_wait(&full[stage], phase, abort_flag, kWaitLimitNs)) {
                     ok = false;
@@ -515,7 +527,7 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         for (int tile = blockIdx.x + group * gridDim.x; tile < ntiles; tile += EPI_GROUPS * gridDim.x) {
             // everything the tile needs besides the accumulator is fetched
             // before waiting for it
-            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT);
+            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT, MT);
             const int e = ti.e, nt = ti.nt;
             const int row = ti.mt * BM + r_in;
             bool valid;
