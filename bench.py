@@ -40,6 +40,33 @@ FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
 # kernels one layer step launches: scale check, token reorder, a1 quantiser, w13 GEMM, w2 GEMM
 LAUNCHES_PER_STEP = 5
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the two GEMM kernels
+# on the 8192-token prefill layer, from one ncu capture (profiles/moe_gemm_prefill8192_dram.md).
+# It holds for the kernel source it was taken on: any change to these files makes it null.
+NCU_TRAFFIC = {
+    "tokens": 8192,
+    "source_sha1": {"nvfp4_w4a4_moe_gb300/csrc/kernels_gemm.cu": "a26baa8040ec68a93ac5d49a8b6dfa912b93b1a6",
+                    "nvfp4_w4a4_moe_gb300/csrc/common.cuh": "5682b9898c256b93a3a8fa14f68dde76ff313ab0"},
+    "bytes": {"gemm_w13": 384558080 + 116169472, "gemm_w2": 267339776 + 68121088},
+}
+
+
+def measured_traffic(kernel: str, tokens: int):
+    """The ncu DRAM bytes per launch of `kernel`, or None when there is no
+    capture for it, for this token count, or for the current kernel source."""
+    import hashlib
+    if tokens != NCU_TRAFFIC["tokens"] or kernel not in NCU_TRAFFIC["bytes"]:
+        return None
+    root = os.path.dirname(os.path.abspath(__file__))
+    for rel, digest in NCU_TRAFFIC["source_sha1"].items():
+        try:
+            with open(os.path.join(root, rel), "rb") as f:
+                if hashlib.sha1(f.read()).hexdigest() != digest:
+                    return None
+        except OSError:
+            return None
+    return NCU_TRAFFIC["bytes"][kernel]
+
 
 def peaks():
     p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
@@ -268,7 +295,8 @@ def run_ours(args, rank, world):
     else:
         roof = {"bound": "hbm", "achieved": a["bytes"] / t_s / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = measured_traffic(dom, T)
+    roof["traffic_unit"] = "bytes per launch (ncu dram read + write)"
     roof["kernel"] = dom
     roof["peak_source"] = (f"{pk['source']} HBM copy" if roof["bound"] == "hbm" else
                            f"{pk['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4:BF16)")
