@@ -514,7 +514,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     ga.I = I;
     ga.kc2 = L.kc2;
     ga.h_dump = keep_h ? reinterpret_cast<float *>(base + L.host_end) : nullptr;
-    ga.zero_out = out;  // the w13 kernel clears out for the w2 kernel's reductions
+    ga.zero_out = out;  // cleared by the w13 kernel for the w2 kernel's reductions
     ga.zero_floats = (long long)T * H;
     ga.k = k;
     ga.H = H;
@@ -535,8 +535,6 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     gb.gate_up_I = 0;
     gb.alpha = alpha2;
     gb.h_dump = nullptr;
-    gb.zero_out = nullptr;
-    gb.zero_floats = 0;
     gb.row_src = ra.row_src;
     gb.topk_w = topk_w;
     gb.out = out;

@@ -93,7 +93,7 @@ struct GemmArgs {
     uint8_t *a2q, *sf2;
     int I, kc2;
     float *h_dump;
-    float *zero_out;  // w13 kernel: [T, H] FP32 output zeroed by the epilogue warps before the first tile
+    float *zero_out;  // w13 kernel: [T, H] FP32 output cleared for the w2 kernel's reductions (nullable)
     long long zero_floats;
     // w2 epilogue (weighted combine)
     const int *row_src;

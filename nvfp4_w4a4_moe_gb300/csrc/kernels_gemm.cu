@@ -24,8 +24,7 @@
 //              then either SiLU(gate)*up + NVFP4 requantisation (w13) or the
 //              weighted scatter-add into the token-order output (w2),
 //              transposed through shared memory so the FP32 reductions are
-//              coalesced.  In the w13 kernel they first clear the output for
-//              w2.
+//              coalesced.
 //   last 4     scale writers, one per TMEM lane quarter: per stage they move
 //              both operands' scale tiles smem -> registers -> TMEM
 //              (tcgen05.st).
@@ -510,20 +509,25 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         const int part = ew >> 2;                        // w13: which slice of the tile's h columns
         const int r_in = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        if (EPI == 0 && p.zero_out) {
-            // Clear the FP32 output for the w2 kernel's reductions while the
-            // first accumulator is being produced.
-            const long long active = min((long long)gridDim.x, (long long)ntiles);
-            const long long n4 = p.zero_floats >> 2;
-            float4 *z = reinterpret_cast<float4 *>(p.zero_out);
-            for (long long i = (long long)blockIdx.x * EPI_THREADS + (threadIdx.x - 64); i < n4;
-                 i += active * EPI_THREADS)
-                z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
         float *xp = reinterpret_cast<float *>(smem + OFF_XPOSE) + ew * 32 * XPOSE_LD;
         const uint32_t acc = EPI_GROUPS == 2 ? (uint32_t)group : 0u;
         uint32_t acc_phase = 0;
         bool ok = true;
+        // w13: the FP32 output is cleared for the w2 kernel's reductions, a
+        // slice after each tile, so that the stores use the HBM bandwidth the
+        // GEMM leaves idle instead of delaying the first accumulator.  Each
+        // active CTA owns a contiguous range of it.
+        long long z_next = 0, z_end = 0, z_slice = 0;
+        float4 *z4 = reinterpret_cast<float4 *>(p.zero_out);
+        if (EPI == 0 && p.zero_out) {
+            const long long n4 = p.zero_floats >> 2;
+            const long long active = min((long long)gridDim.x, (long long)ntiles);
+            const long long per_cta = (n4 + active - 1) / active;
+            const long long my_tiles = (ntiles - (long long)blockIdx.x + gridDim.x - 1) / gridDim.x;
+            z_next = min(n4, (long long)blockIdx.x * per_cta);
+            z_end = min(n4, z_next + per_cta);
+            z_slice = (per_cta + my_tiles - 1) / my_tiles;
+        }
         for (int tile = blockIdx.x + group * gridDim.x; tile < ntiles; tile += EPI_GROUPS * gridDim.x) {
             // everything the tile needs besides the accumulator is fetched
             // before waiting for it
@@ -651,6 +655,12 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                     }
                     __syncwarp();
                 }
+            }
+            if (EPI == 0 && z_next < z_end) {
+                const long long stop = min(z_end, z_next + z_slice);
+                for (long long i = z_next + (threadIdx.x - 64); i < stop; i += EPI_THREADS)
+                    z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                z_next = stop;
             }
             acc_phase ^= 1u;  // each group owns one accumulator
         }

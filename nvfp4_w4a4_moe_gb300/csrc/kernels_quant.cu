@@ -133,7 +133,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
         if (blockIdx.x == 0 && tid == 0) a.hdr->status = 3;  // nothing after this writes
         return;
     }
-
     // ---- phase 2: offsets (every CTA), this CTA's chunk prefixes
     const int own = (a.nchunks - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // chunks of this CTA
     int *cnt = sh;                    // [E]
