@@ -19,6 +19,7 @@ namespace {
 __global__ void __launch_bounds__(256) validate_kernel(ValidateArgs a)
 {
     __shared__ int s_bad, s_first;
+    __shared__ float s_recip[4][1024];  // reciprocals for alpha (forward: 4 arrays, E <= 1024)
     if (threadIdx.x == 0) {
         s_bad = 0;
         s_first = INT_MAX;
@@ -36,6 +37,7 @@ __global__ void __launch_bounds__(256) validate_kernel(ValidateArgs a)
         const float ar = fabsf(r);
         if (!(ar <= FLT_MAX) || ar < FLT_MIN) ok = false;
         if (a.recip[arr]) a.recip[arr][e] = r;
+        if (arr < 4 && e < 1024) s_recip[arr][e] = r;  // the forward's alpha needs E <= 1024, 4 arrays
         if (!ok) {
             atomicAdd(&s_bad, 1);
             atomicMin(&s_first, i);
@@ -46,8 +48,8 @@ __global__ void __launch_bounds__(256) validate_kernel(ValidateArgs a)
     // figure: the GEMM's scaling takes in both FP32 global scales].
     if (a.alpha1 && a.narrays == 4) {
         for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
-            a.alpha1[e] = __frcp_rn(__fmul_rn(a.recip[0][e], a.recip[2][e]));
-            a.alpha2[e] = __frcp_rn(__fmul_rn(a.recip[1][e], a.recip[3][e]));
+            a.alpha1[e] = __frcp_rn(__fmul_rn(s_recip[0][e], s_recip[2][e]));
+            a.alpha2[e] = __frcp_rn(__fmul_rn(s_recip[1][e], s_recip[3][e]));
         }
     }
     if (threadIdx.x == 0) {
@@ -81,6 +83,7 @@ constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kRouteSlice = kRouteChunk / kRouteWarps;  // rows per warp per chunk
 constexpr int kRouteIdsPerLane = kRouteSlice / 32;
+constexpr int kRouteMaxOwn = 8;  // chunks per CTA the shared-memory plan allows for
 
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
 {
@@ -90,18 +93,37 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (a.hdr->status != 0) return;  // same value in every CTA (set by the previous kernel)
 
-    // ---- phase 1: chunk histograms
+    // ---- phase 1: chunk histograms.  Each thread reads its ids in the
+    // scatter's mapping (warp w: rows [256 w, 256 w + 256) of the chunk, lane l:
+    // rows 32 i + l) all at once, and keeps those of its first chunk in
+    // registers for the scatter.
     int *hist = sh;  // [E]
+    int ids_first[kRouteIdsPerLane];
     for (int c = blockIdx.x; c < a.nchunks; c += gridDim.x) {
         for (int e = tid; e < E; e += kRouteThreads) hist[e] = 0;
+        const int wf0 = c * kRouteChunk + warp * kRouteSlice;
+        int idv[kRouteIdsPerLane];
+#pragma unroll
+        for (int i = 0; i < kRouteIdsPerLane; ++i) {
+            const int f = wf0 + 32 * i + lane;
+            idv[i] = f < a.R ? a.ids[f] : 0;
+        }
         __syncthreads();
-        const int f0 = c * kRouteChunk, f1 = min(a.R, f0 + kRouteChunk);
-        for (int f = f0 + tid; f < f1; f += kRouteThreads) {
-            const int e = a.ids[f];
-            if (e < 0 || e >= E)
-                atomicOr(&a.hdr->error_flags, kErrBadExpertId);
-            else
-                atomicAdd(&hist[e], 1);
+        bool bad = false;
+#pragma unroll
+        for (int i = 0; i < kRouteIdsPerLane; ++i) {
+            if (wf0 + 32 * i + lane >= a.R) {
+                idv[i] = -1;  // past the end: no row
+            } else if (idv[i] < 0 || idv[i] >= E) {
+                bad = true;
+            } else {
+                atomicAdd(&hist[idv[i]], 1);
+            }
+        }
+        if (bad) atomicOr(&a.hdr->error_flags, kErrBadExpertId);
+        if (c == (int)blockIdx.x) {
+#pragma unroll
+            for (int i = 0; i < kRouteIdsPerLane; ++i) ids_first[i] = idv[i];
         }
         __syncthreads();
         for (int e = tid; e < E; e += kRouteThreads) a.chunk_hist[(size_t)c * E + e] = hist[e];
@@ -140,25 +162,46 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
     int *poff = off + E + 1;          // [E + 1]
     int *wbase = poff + E + 1;        // [kRouteWarps][E]
     int *cpre = wbase + kRouteWarps * E;  // [own][E]: chunk's first rank per expert
-    for (int e = tid; e < E; e += kRouteThreads) {
-        int run = 0, next_own = (int)blockIdx.x, i_own = 0;
-        for (int c0 = 0; c0 < a.nchunks; c0 += 16) {
+    int *psum = cpre + kRouteMaxOwn * E;  // [parts][E]
+    // Per expert, the exclusive prefix over chunks.  With few experts the chunk
+    // range is split into `parts` runs summed by different threads (one batch
+    // of loads each), then the runs' sums are chained.
+    const int parts = E >= kRouteThreads ? 1 : min(kRouteThreads / E, 16);
+    const int csz = (a.nchunks + parts - 1) / parts;
+    for (int t = tid; t < parts * E; t += kRouteThreads) {
+        const int e = t % E, part = t / E;
+        const int c_lo = part * csz, c_hi = min(a.nchunks, c_lo + csz);
+        // this CTA's chunks are blockIdx.x + j * gridDim.x; the first at or after c_lo
+        int j = c_lo <= (int)blockIdx.x ? 0 : (c_lo - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+        int next_own = (int)blockIdx.x + j * (int)gridDim.x;
+        int run = 0;
+        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
             int v[16];
-            const int n = min(16, a.nchunks - c0);
+            const int n = min(16, c_hi - c0);
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = i < n ? __ldcg(&a.chunk_hist[(size_t)(c0 + i) * E + e]) : 0;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                if (c0 + i == next_own && i < n) {
-                    cpre[i_own * E + e] = run;
-                    ++i_own;
+                if (i < n && c0 + i == next_own) {
+                    cpre[j * E + e] = run;  // prefix within this run, completed below
+                    ++j;
                     next_own += gridDim.x;
                 }
                 run += v[i];
             }
         }
-        cnt[e] = run;
-        if (blockIdx.x == 0) a.counts[e] = run;
+        psum[part * E + e] = run;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kRouteThreads) {
+        int before = 0, j = 0;
+        for (int part = 0; part < parts; ++part) {
+            const int c_hi = min(a.nchunks, (part + 1) * csz);
+            for (; j < own && (int)blockIdx.x + j * (int)gridDim.x < c_hi; ++j) cpre[j * E + e] += before;
+            before += psum[part * E + e];
+        }
+        cnt[e] = before;
+        if (blockIdx.x == 0) a.counts[e] = before;
     }
     __syncthreads();
     // exclusive scans over experts (compact, and padded to 128-row tiles) by
@@ -231,7 +274,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
 #pragma unroll
         for (int i = 0; i < kRouteIdsPerLane; ++i) {
             const int f = wf0 + 32 * i + lane;
-            ids[i] = f < a.R ? a.ids[f] : -1;  // ids are valid here (checked above)
+            ids[i] = i_own == 0 ? ids_first[i] : f < a.R ? a.ids[f] : -1;  // valid here (checked above)
         }
         for (int e = lane; e < E; e += 32) wb[e] = 0;
         __syncwarp();
@@ -496,8 +539,11 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t st)
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    const int max_own = 8;  // chunks per CTA the shared-memory plan allows for
-    auto smem_for = [&](int E) { return sizeof(int) * ((3 + kRouteWarps + max_own) * (size_t)E + 2); };
+    const int max_own = kRouteMaxOwn;
+    // cnt, off, poff, per-warp bases, per-chunk prefixes, per-run sums
+    auto smem_for = [&](int E) {
+        return sizeof(int) * ((3 + kRouteWarps + max_own) * (size_t)E + 2 + (E > kRouteThreads ? E : kRouteThreads));
+    };
     const size_t smem = smem_for(a.E);
     if (!resident[dev]) {
         // sized once for the largest expert count, so any call fits
