@@ -7,6 +7,10 @@ experts, hidden 2816, intermediate 704, top-8 with Zipf(1.1) routing.  Inputs
 are synthetic and seeded; weights are N(0, 0.02) BF16 draws quantised to NVFP4
 on the device.  Prints one JSON line (rank 0).
 
+The throughput comes from K timed steps of the plain forward; the per-kernel
+split (and the roofline's kernel time) from a second timed region of K steps
+that records an event around every kernel.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 --impl reference times the CPU oracle on a bounded sample of the same
@@ -245,15 +249,27 @@ def run_ours(args, rank, world):
         uuid = "GPU-" + str(torch.cuda.get_device_properties(0).uuid)
     except Exception:
         uuid = None
+    # Two timed regions of K steps each.  The first runs the layer as a user
+    # does and gives the throughput; the second records six events per step
+    # (before and after every kernel) for the per-kernel times, which the
+    # records themselves lengthen by about 2 us each, so it does not set value.
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pstart, pstop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(uuid if rank == 0 else None) as clocks:
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
         start.record(stream)
         for i in range(K):
-            m.moe_forward_profiled(w, x, ids, tw, evs[i], out=out, ws=ws, flags=flags)
+            m.moe_forward(w, x, ids, tw, out=out, ws=ws, flags=flags)
         stop.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        pstart.record(stream)
+        for i in range(K):
+            m.moe_forward_profiled(w, x, ids, tw, evs[i], out=out, ws=ws, flags=flags)
+        pstop.record(stream)
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
@@ -262,6 +278,7 @@ def run_ours(args, rank, world):
     if status != m.OK:
         raise RuntimeError(f"device status {status} after the timed steps")
     ms_step, value = combine_ranks(total_ms, T, K, dist)
+    ms_step_profiled = pstart.elapsed_time(pstop) / K
     stage_ms = {name: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
                 for j, name in enumerate(m.STAGES)}
 
@@ -322,6 +339,9 @@ def run_ours(args, rank, world):
                    "ms_per_step_with_host_scale_check": ms_checked},
         "roofline": roof,
         "kernels": {n: {"ms": v, "share": v / sum(stage_ms.values())} for n, v in stage_ms.items()},
+        "kernels_note": (f"per-kernel CUDA-event times from a second timed region of {K} steps with six "
+                         f"events per step ({ms_step_profiled:.4f} ms per step there, against "
+                         f"{ms_step:.4f} ms without the events)"),
         "gemm": {
             "w13_tflops": alg["gemm_w13"]["flops"] / (stage_ms["gemm_w13"] * 1e-3) / 1e12,
             "w2_tflops": alg["gemm_w2"]["flops"] / (stage_ms["gemm_w2"] * 1e-3) / 1e12,
