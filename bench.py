@@ -299,6 +299,7 @@ def run_ours(args, rank, world):
 
     # e2e: host buffers in, host buffers out, through the host entry point
     e2e = e2e_host(m, torch, w, layer, args)
+    decode = decode_leg(m, torch, w, args)
 
     pk = peaks()
     n_active = int((np.bincount(layer.topk_ids.ravel(), minlength=E) > 0).sum())
@@ -350,6 +351,7 @@ def run_ours(args, rank, world):
             "w2_frac_fp4_peak": alg["gemm_w2"]["flops"] / (stage_ms["gemm_w2"] * 1e-3) / 1e12 / fp4_peak,
         },
         "quant": qres,
+        "decode": decode,
         "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * K,
         "clocks": clocks.summary(),
@@ -389,6 +391,71 @@ def quant_workload(m, torch, w, args):
             "ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
             "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
             "note": "bytes = x read once + codes and scales written + routing reads"}
+
+
+def decode_leg(m, torch, w, args):
+    """The decode-shaped layers (same experts, 1-64 tokens): latency per call
+    of the plain forward and of a CUDA-graph replay of it, tokens/s, and the
+    bandwidth over the weight bytes of the experts the batch touches (codes +
+    block scales of w13 and w2)."""
+    H, I, E = w.H, w.I, w.E
+    per_expert = 2 * I * H // 2 + 2 * I * H // 16 + H * I // 2 + H * I // 16
+    res = {}
+    for T in (1, 8, 32, 64):
+        L = S.decode(T)
+        k = L.k
+        x = torch.from_numpy(L.x.view(np.int16)).cuda().view(torch.bfloat16)
+        ids = torch.from_numpy(L.topk_ids).cuda()
+        tw = torch.from_numpy(L.topk_w).cuda()
+        wd = m.MoEWeights(E, H, I, w.w13_q, w.w13_sf, w.w13_scale2, torch.from_numpy(L.w13_input_scale).cuda(),
+                          w.w2_q, w.w2_sf, w.w2_scale2, w.w2_input_scale)
+        wd.prepared = w.prepared
+        out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        ws = torch.empty(m.moe_workspace_size(T, H, I, E, k), dtype=torch.uint8, device="cuda")
+        m.moe_forward(wd, x, ids, tw, out=out, ws=ws, flags=m.SYNC_CHECK)
+        n = 500
+        flags = m.SCALES_PREVALIDATED
+        for _ in range(20):
+            m.moe_forward(wd, x, ids, tw, out=out, ws=ws, flags=flags)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(n):
+            m.moe_forward(wd, x, ids, tw, out=out, ws=ws, flags=flags)
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) / n * 1e3
+        graph_us, graph_err = None, None
+        try:
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                m.moe_forward(wd, x, ids, tw, out=out, ws=ws, flags=flags)
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g, stream=s):
+                    m.moe_forward(wd, x, ids, tw, out=out, ws=ws, flags=flags, stream=s)
+            torch.cuda.current_stream().wait_stream(s)
+            for _ in range(20):
+                g.replay()
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(n):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            graph_us = a.elapsed_time(b) / n * 1e3
+            st, _ = m.moe_status(ws)
+            if st != m.OK:
+                graph_us, graph_err = None, f"device status {st} after graph replays"
+        except Exception as ex:  # capture support depends on the driver; report, do not fail the run
+            graph_err = f"{type(ex).__name__}: {ex}"[:200]
+        touched = len(np.unique(L.topk_ids))
+        best = graph_us if graph_us is not None else us
+        res[str(T)] = {"us_per_call": us, "us_per_graph_replay": graph_us, "graph_error": graph_err,
+                       "tokens_per_s": T / (best * 1e-6), "experts_touched": touched,
+                       "weight_gbs": touched * per_expert / (best * 1e-6) / 1e9}
+    return res
 
 
 def e2e_host(m, torch, w, layer, args):
