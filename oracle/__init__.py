@@ -70,6 +70,7 @@ def _load_locked(path):
         "orc_quant_rows": (None, [P, I64, I64, P, P, P, ctypes.c_int]),
         "orc_validate_scales": (I64, [P, P, I64, P]),
         "orc_route": (ctypes.c_int, [P, I64, I32, I32, P, P]),
+        "orc_router": (ctypes.c_int, [P, I64, I32, I32, P, P]),
         "orc_gemm_nvfp4": (ctypes.c_int, [P, P, P, I64, P, P, F32, I64, I64, P, ctypes.c_int]),
         "orc_silu_mul": (None, [P, I64, I64, P]),
         "orc_residual_rmsnorm": (None, [P, P, I64, I64, F64, P]),
@@ -250,6 +251,19 @@ def route(topk_ids: np.ndarray, E: int):
     if rc != 0:
         raise ValueError("expert id outside [0, E)")
     return offsets, perm
+
+
+def router(logits: np.ndarray, k: int):
+    """(topk_ids [T, k] int32, topk_weights [T, k] f32) of the softmax / top-k /
+    renormalise router over FP32 logits [T, E]."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float32)
+    rc = _L().orc_router(_p(lg), T, E, k, _p(ids), _p(w))
+    if rc != 0:
+        raise ValueError("router: bad shape")
+    return ids, w
 
 
 def gemm(aq, asf, ga_rows, wq, wsf, gw) -> np.ndarray:

@@ -333,6 +333,63 @@ int orc_route(const int32_t *ids, int64_t T, int32_t k, int32_t E, int32_t *offs
 }
 
 /* ------------------------------------------------------------------------ */
+/* Router: softmax over the experts, top-k, renormalised                      */
+/* ------------------------------------------------------------------------ */
+
+/* [page "Gemma 4 NVFP4 MoE 空输出", §矩阵融合 "MoE FFN": the routing result
+ * decides which experts a token visits, and the expert outputs are summed with
+ * the routing weights; page "genesis-vllm-patches" (mlqm.cn), §3.3 patch P31:
+ * the router's softmax and top-k run on logits upcast to FP32].  Per token,
+ * from FP32 logits l[0..E):
+ *   1. p_e = exp(l_e) / sum_e' exp(l_e')     softmax, fp64 (shifted by max l)
+ *   2. the k experts of largest p, largest first, ties to the lower index
+ *   3. w_j = p_ids[j] / sum_i p_ids[i]        renormalised over the k, stored FP32
+ * Reading for step 3: the pages do not say whether the k weights are
+ * renormalised; renormalising over the selected k (weights sum to 1) is the
+ * reading taken.  Reading for step 2: softmax is strictly increasing in the
+ * logit, so the exact probability order is the order of the FP32 logits; the
+ * selection compares the logits themselves (an fp64 probability can tie where
+ * two logits differ by less than its rounding).  Ties between equal logits go
+ * to the lower index.  Returns 0, -1 for a bad shape, -2 if out of memory. */
+int orc_router(const float *logits, int64_t T, int32_t E, int32_t k, int32_t *ids, float *w)
+{
+    if (E < 1 || k < 1 || k > E) return -1;
+    double *p = (double *)malloc(sizeof(double) * (size_t)E);
+    uint8_t *taken = (uint8_t *)malloc((size_t)E);
+    if (!p || !taken) {
+        free(p);
+        free(taken);
+        return -2;
+    }
+    for (int64_t t = 0; t < T; ++t) {
+        const float *l = logits + t * E;
+        double lmax = l[0];
+        for (int32_t e = 1; e < E; ++e)
+            if (l[e] > lmax) lmax = l[e];
+        double z = 0.0;
+        for (int32_t e = 0; e < E; ++e) {
+            p[e] = exp((double)l[e] - lmax);
+            z += p[e];
+        }
+        for (int32_t e = 0; e < E; ++e) p[e] /= z;
+        memset(taken, 0, (size_t)E);
+        double zk = 0.0;
+        for (int32_t j = 0; j < k; ++j) {
+            int32_t best = -1;
+            for (int32_t e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || l[e] > l[best])) best = e;
+            taken[best] = 1;
+            ids[t * k + j] = best;
+            zk += p[best];
+        }
+        for (int32_t j = 0; j < k; ++j) w[t * k + j] = (float)(p[ids[t * k + j]] / zk);
+    }
+    free(p);
+    free(taken);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Block-scaled FP4 GEMM, exact                                               */
 /* ------------------------------------------------------------------------ */
 

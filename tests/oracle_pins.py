@@ -251,6 +251,50 @@ def pin_route_bruteforce(orc):
         assert list(offsets) == [0] + list(np.cumsum(counts))
 
 
+def pin_router(orc):
+    """Router pins: k = E is SciPy's softmax in the stable descending order of the
+    logits; for k < E the renormalised weights are the softmax of the selected
+    logits (an identity of renormalisation, checked with SciPy); hand cases for
+    ties, equal logits and a dominant logit; brute-force selection on tiny
+    inputs; shift invariance."""
+    from scipy.special import softmax
+    r = _rng(21)
+    lg = r.standard_normal((16, 9)).astype(np.float32)
+    ids, w = orc.router(lg, 9)
+    assert np.array_equal(ids, np.argsort(-lg, axis=1, kind="stable"))
+    ref = softmax(lg.astype(np.float64), axis=1)
+    assert np.allclose(w, np.take_along_axis(ref, ids, axis=1), rtol=2e-7, atol=0)
+    for k in (1, 3, 5):
+        ids, w = orc.router(lg, k)
+        sub = softmax(np.take_along_axis(lg, ids, axis=1).astype(np.float64), axis=1)
+        assert np.allclose(w, sub, rtol=2e-7, atol=0)
+        assert np.all(np.diff(w, axis=1) <= 0)
+    # ties go to the lower index; equal logits share the weight exactly
+    ids, w = orc.router(np.array([[0.0, 5.0, 5.0, 1.0]], np.float32), 2)
+    assert ids.tolist() == [[1, 2]] and w.tolist() == [[0.5, 0.5]]
+    ids, w = orc.router(np.zeros((3, 8), np.float32), 4)
+    assert ids.tolist() == [[0, 1, 2, 3]] * 3 and np.all(w == 0.25)
+    # a dominant logit takes all the weight
+    big = r.standard_normal((1, 32)).astype(np.float32)
+    big[0, 17] = 60.0
+    ids, w = orc.router(big, 1)
+    assert ids.tolist() == [[17]] and w.tolist() == [[1.0]]
+    # logits whose fp64 probabilities tie are ordered by the logits themselves
+    ids, _ = orc.router(np.array([[0.0, 1e-30, 0.0, 2e-30]], np.float32), 2)
+    assert ids.tolist() == [[3, 1]]
+    # brute-force selection on tiny inputs with many duplicate values
+    for _ in range(50):
+        E = int(r.integers(1, 7))
+        k = int(r.integers(1, E + 1))
+        row = r.integers(-2, 3, E).astype(np.float32)
+        ids, _ = orc.router(row[None, :], k)
+        assert ids[0].tolist() == sorted(range(E), key=lambda e: (-row[e], e))[:k]
+    # shifting every logit changes nothing but rounding
+    ids0, w0 = orc.router(lg, 4)
+    ids1, w1 = orc.router(lg + np.float32(2.0), 4)
+    assert np.array_equal(ids0, ids1) and np.allclose(w0, w1, rtol=1e-6, atol=0)
+
+
 # ---------------------------------------------------------------------------
 # GEMM, activation, combine
 # ---------------------------------------------------------------------------
@@ -451,5 +495,5 @@ ALL_PINS = [
     pin_e2m1_table, pin_e2m1_ties, pin_e2m1_boundaries, pin_e4m3_roundtrip, pin_e4m3_frexp,
     pin_e4m3_torch, pin_block_worked, pin_identity_2688, pin_block_invariances,
     pin_route_bruteforce, pin_gemm_fraction, pin_gemm_fp64, pin_silu_mul, pin_combine_special,
-    pin_forward_stepwise, pin_validate, pin_rmsnorm,
+    pin_forward_stepwise, pin_validate, pin_rmsnorm, pin_router,
 ]

@@ -32,6 +32,9 @@ MUTANTS = [
      "for (int64_t f = R - 1; f >= 0; --f) perm[cursor[ids[f]]++] = (int32_t)f;", 0),
     ("validate_no_reciprocal_check", "if (!isfinite(r) || !isnormal(r)) ok = 0;", "(void)r;", 0),
     ("rmsnorm_eps_outside", "sqrt(ss / (double)H + eps)", "(sqrt(ss / (double)H) + eps)", 0),
+    ("router_ties_to_higher", "(best < 0 || l[e] > l[best])", "(best < 0 || l[e] >= l[best])", 0),
+    ("router_smallest_first", "(best < 0 || l[e] > l[best])", "(best < 0 || l[e] < l[best])", 0),
+    ("router_not_renormalised", "(float)(p[ids[t * k + j]] / zk)", "(float)(p[ids[t * k + j]])", 0),
 ]
 
 
