@@ -300,6 +300,7 @@ def run_ours(args, rank, world):
     # e2e: host buffers in, host buffers out, through the host entry point
     e2e = e2e_host(m, torch, w, layer, args)
     decode = decode_leg(m, torch, w, args)
+    router = router_leg(m, torch, args)
 
     pk = peaks()
     n_active = int((np.bincount(layer.topk_ids.ravel(), minlength=E) > 0).sum())
@@ -352,6 +353,7 @@ def run_ours(args, rank, world):
         },
         "quant": qres,
         "decode": decode,
+        "router": router,
         "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * K,
         "clocks": clocks.summary(),
@@ -456,6 +458,60 @@ def decode_leg(m, torch, w, args):
                        "tokens_per_s": T / (best * 1e-6), "experts_touched": touched,
                        "weight_gbs": touched * per_expert / (best * 1e-6) / 1e9}
     return res
+
+
+def router_leg(m, torch, args):
+    """The router (softmax / top-k / renormalise) on N(0,1) FP32 logits of the
+    layer's shape (128 experts, top-8), at the prefill and the decode token
+    counts.  Two times per launch: back-to-back calls through the binding
+    (host-bound at small sizes), and launches replayed from a CUDA graph of
+    50 launches (the device's own time per launch).  Bandwidth is over the
+    router's bytes (logits read, ids and weights written); the logits (4 MB
+    at 8192 tokens) stay in L2 between launches, so it is a latency figure."""
+    E, k = 128, 8
+    per_graph, reps = 50, 10
+    res = {}
+    for T in (args.tokens, 64, 1):
+        lg = torch.from_numpy(np.random.default_rng([7100, T]).standard_normal((T, E)).astype(np.float32)).cuda()
+        ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        tw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        for _ in range(20):
+            m.router_topk(lg, k, ids, tw)
+        n = 500
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(n):
+            m.router_topk(lg, k, ids, tw)
+        b.record()
+        torch.cuda.synchronize()
+        us_call = a.elapsed_time(b) / n * 1e3
+        us_graph, graph_err = None, None
+        try:
+            g = torch.cuda.CUDAGraph()
+            st = torch.cuda.Stream()
+            st.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(st):
+                with torch.cuda.graph(g, stream=st):
+                    for _ in range(per_graph):
+                        m.router_topk(lg, k, ids, tw, stream=st)
+            torch.cuda.current_stream().wait_stream(st)
+            g.replay()
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(reps):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            us_graph = a.elapsed_time(b) / (reps * per_graph) * 1e3
+        except Exception as ex:  # capture support depends on the driver; report, do not fail the run
+            graph_err = f"{type(ex).__name__}: {ex}"[:200]
+        nbytes = T * E * 4 + T * k * 8
+        best = us_graph if us_graph is not None else us_call
+        res[str(T)] = {"us_per_call": us_call, "us_per_launch_in_graph": us_graph, "graph_error": graph_err,
+                       "bytes": nbytes, "gbs": nbytes / (best * 1e-6) / 1e9}
+    return {"E": E, "k": k, "logits": "fp32 ~N(0,1)", "tokens": res,
+            "note": "not part of the timed step: the step's routing is an input of the expert path"}
 
 
 def e2e_host(m, torch, w, layer, args):

@@ -71,6 +71,9 @@ typedef enum {
 
 enum { NVFP4_SF_LINEAR = 0, NVFP4_SF_SWIZZLED = 1 };
 
+/* Element type of the router's logits (nvfp4_router_topk). */
+enum { NVFP4_LOGITS_F32 = 0, NVFP4_LOGITS_BF16 = 1 };
+
 /* Flags of nvfp4_moe_forward / nvfp4_moe_forward_host. */
 enum {
     /* Skip the synchronous host check of the scales.  The device still
@@ -300,6 +303,28 @@ int nvfp4_moe_intermediates_of(void *ws, int T, int H, int I, int E, int k,
  */
 int nvfp4_residual_rmsnorm(const uint16_t *x, const float *out, int T, int H, float eps,
                            uint16_t *x_next, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_router_topk -- the MoE router [page "Gemma 4 NVFP4 MoE 空输出",
+ * §矩阵融合 "MoE FFN": the routing result picks each token's experts and the
+ * expert outputs are summed with the routing weights; page
+ * "genesis-vllm-patches" (mlqm.cn), §3.3 patch P31: softmax and top-k on
+ * logits upcast to FP32].  Per token t:
+ *   topk_ids[t, 0..k)     the k experts of largest softmax probability, largest
+ *                         first; equal logits go to the lower expert index
+ *   topk_weights[t, 0..k) their probabilities renormalised over the k (they sum
+ *                         to 1), i.e. the softmax of the k selected logits, FP32
+ * logits: device, [T, E] row-major, FP32 (logits_dtype NVFP4_LOGITS_F32) or
+ * BF16 (NVFP4_LOGITS_BF16, widened exactly to FP32); finite values (NaN or inf
+ * logits give unspecified results).  topk_ids [T, k] int32 and
+ * topk_weights [T, k] FP32 are device buffers owned by the caller, in the
+ * layout nvfp4_moe_forward() reads.  Limits: T >= 0, 1 <= E <= 1024,
+ * 1 <= k <= min(32, E).  Needs no workspace; asynchronous on `stream`.
+ * Returns NVFP4_OK (T = 0 launches nothing), NVFP4_ERR_INVALID_ARG (shape,
+ * dtype, null or misaligned pointer), NVFP4_ERR_CUDA (launch failure).
+ */
+int nvfp4_router_topk(const void *logits, int logits_dtype, int T, int E, int k, int32_t *topk_ids,
+                      float *topk_weights, nvfp4_stream_t stream);
 
 /*
  * nvfp4_quantize_weights -- static weight quantisation on the device

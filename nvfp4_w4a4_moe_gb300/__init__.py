@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libnvfp4moe.so")
 OK, ERR_INVALID_ARG, ERR_SCALE_INVALID, ERR_UNSUPPORTED_SHAPE, ERR_CUDA, ERR_DEVICE_TIMEOUT, \
     ERR_WORKSPACE_TOO_SMALL = range(7)
 SF_LINEAR, SF_SWIZZLED = 0, 1
+LOGITS_F32, LOGITS_BF16 = 0, 1
 SCALES_PREVALIDATED, SYNC_CHECK, DEBUG_KEEP_H = 1, 2, 4
 
 _lib = None
@@ -79,6 +80,7 @@ def load():
             "nvfp4_moe_status": (I, [P, P, P]),
             "nvfp4_moe_intermediates_of": (I, [P, I, I, I, I, I, P]),
             "nvfp4_residual_rmsnorm": (I, [P, P, I, I, ctypes.c_float, P, P]),
+            "nvfp4_router_topk": (I, [P, I, I, I, I, P, P, P]),
             "nvfp4_quantize_weights_workspace_size": (SZ, [I]),
             "nvfp4_quantize_weights": (I, [P, I, I, I, P, P, P, P, SZ, P]),
             "nvfp4_selftest_block_division": (ctypes.c_longlong, [I]),
@@ -326,6 +328,28 @@ def residual_rmsnorm(x: torch.Tensor, out: torch.Tensor, eps: float = 1e-6, x_ne
         x_next = torch.empty_like(x)
     _check(load().nvfp4_residual_rmsnorm(_ptr(x), _ptr(out), T, H, float(eps), _ptr(x_next), _stream(stream)))
     return x_next
+
+
+def router_topk(logits: torch.Tensor, k: int, topk_ids: torch.Tensor | None = None,
+                topk_weights: torch.Tensor | None = None, stream=None):
+    """logits [T, E] fp32 or bf16 (device) -> (topk_ids [T, k] int32, topk_weights [T, k] f32):
+    softmax over the experts, the k largest (ties to the lower index), renormalised."""
+    T, E = logits.shape
+    if logits.dtype == torch.float32:
+        dt = LOGITS_F32
+    elif logits.dtype == torch.bfloat16:
+        dt = LOGITS_BF16
+    else:
+        raise Nvfp4Error(ERR_INVALID_ARG, f"router_topk: logits must be float32 or bfloat16, not {logits.dtype}")
+    if not logits.is_contiguous():
+        raise Nvfp4Error(ERR_INVALID_ARG, "router_topk: logits must be contiguous")
+    if topk_ids is None:
+        topk_ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+    if topk_weights is None:
+        topk_weights = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _check(load().nvfp4_router_topk(_ptr(logits), dt, T, E, k, _ptr(topk_ids), _ptr(topk_weights),
+                                    _stream(stream)))
+    return topk_ids, topk_weights
 
 
 def quantize_weights(w: torch.Tensor, stream=None):

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libnvfp4moe.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "kernels_quant.cu", "kernels_gemm.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "kernels_quant.cu", "kernels_gemm.cu", "kernels_router.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

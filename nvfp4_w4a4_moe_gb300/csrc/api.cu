@@ -746,6 +746,23 @@ int nvfp4_residual_rmsnorm(const uint16_t *x, const float *out, int T, int H, fl
     return NVFP4_OK;
 }
 
+int nvfp4_router_topk(const void *logits, int logits_dtype, int T, int E, int k, int32_t *topk_ids,
+                      float *topk_weights, nvfp4_stream_t stream)
+{
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E)
+        return fail(NVFP4_ERR_INVALID_ARG, "router_topk: need T >= 0, 1 <= E <= 1024, 1 <= k <= min(32, E)");
+    if (logits_dtype != NVFP4_LOGITS_F32 && logits_dtype != NVFP4_LOGITS_BF16)
+        return fail(NVFP4_ERR_INVALID_ARG, "router_topk: logits_dtype must be NVFP4_LOGITS_F32 or NVFP4_LOGITS_BF16");
+    if (T == 0) return NVFP4_OK;
+    if (!logits || !topk_ids || !topk_weights) return fail(NVFP4_ERR_INVALID_ARG, "router_topk: null pointer");
+    if (!aligned(logits, logits_dtype == NVFP4_LOGITS_F32 ? 4 : 2) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4))
+        return fail(NVFP4_ERR_INVALID_ARG, "router_topk: misaligned pointer");
+    NV_CUDA(launch_router_topk(logits, logits_dtype == NVFP4_LOGITS_BF16, T, E, k, topk_ids, topk_weights,
+                               (cudaStream_t)stream),
+            "launching the router");
+    return NVFP4_OK;
+}
+
 size_t nvfp4_quantize_weights_workspace_size(int count) { return count > 0 ? up256(sizeof(unsigned) * count) : 0; }
 
 int nvfp4_quantize_weights(const uint16_t *w, int count, int N, int K, uint8_t *q, uint8_t *sf, float *scale2,

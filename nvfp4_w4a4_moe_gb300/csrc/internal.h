@@ -76,6 +76,10 @@ cudaError_t launch_prep_sf(const PrepArgs &a, cudaStream_t st);
 cudaError_t launch_rmsnorm(const uint16_t *x, const float *out, int T, int H, float eps, uint16_t *xn,
                            cudaStream_t st);
 
+// Router: softmax / top-k / renormalise over logits [T, E] (FP32, or BF16 when bf16 != 0).
+cudaError_t launch_router_topk(const void *logits, int bf16, int T, int E, int k, int32_t *ids, float *w,
+                               cudaStream_t st);
+
 cudaError_t launch_quantize_weights(const uint16_t *w, int count, int N, int K, uint8_t *q, uint8_t *sf,
                                     float *scale2, unsigned *amax_bits, cudaStream_t st);
 

@@ -97,6 +97,12 @@ def test_argument_errors_need_no_gpu(lib):
     # validate: null result pointers
     rc = lib.nvfp4_validate_scales(P(256), None, 4, P(256), None, None, None)
     assert rc == m.ERR_INVALID_ARG
+    # router: k outside [1, min(32, E)], E outside [1, 1024], unknown dtype, null or misaligned logits
+    for E, k, dt in ((128, 0, 0), (128, 33, 0), (4, 8, 0), (1025, 8, 0), (0, 1, 0), (128, 8, 2)):
+        assert lib.nvfp4_router_topk(P(256), dt, 1, E, k, P(256), P(256), None) == m.ERR_INVALID_ARG, (E, k, dt)
+    assert lib.nvfp4_router_topk(None, 0, 1, 128, 8, P(256), P(256), None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_router_topk(P(258), 0, 1, 128, 8, P(256), P(256), None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_router_topk(None, 0, 0, 128, 8, None, None, None) == m.OK  # T = 0 launches nothing
 
 
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
