@@ -123,7 +123,8 @@ int nvfp4_validate_scales(const float *scales, const uint8_t *written, int n, vo
  * check; a bad slot returns NVFP4_ERR_SCALE_INVALID with no output written.
  * The call also waits for the quantiser and returns NVFP4_ERR_INVALID_ARG,
  * with no output written, if an expert id is outside [0, E).  Pointer
- * alignment: x 16 B, q_out 8 B, sf_out 4 B.  Workspace:
+ * alignment: x 16 B, q_out 16 B, sf_out 4 B.  T*k*H/16 (the scale bytes)
+ * must stay below 2^32 (else NVFP4_ERR_UNSUPPORTED_SHAPE).  Workspace:
  * nvfp4_quantize_workspace_size(T, k, E) bytes of device memory, 256-byte
  * aligned.
  */

@@ -151,6 +151,14 @@ static size_t prepared_w2_bytes(int E, int H, int I)
 
 static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The activation quantiser addresses its outputs with 32-bit offsets: scale
+// bytes (both layouts, rows rounded up to 128) must stay below 2^32.
+static bool quant_offsets_fit(long long rows, int H)
+{
+    const long long kc = (H + 63) / 64;
+    return ((rows + 127) / 128) * kc * 512 < (1ll << 32);
+}
+
 static int check_layer_shape(int E, int H, int I, int k)
 {
     if (E < 1 || E > 1024) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "E=%d outside [1, 1024]", E);
@@ -278,8 +286,11 @@ int nvfp4_quantize_experts(const uint16_t *x, int T, int H, const int32_t *topk_
         return fail(NVFP4_ERR_INVALID_ARG, "unknown scale layout %d", sf_layout);
     if (!input_scale || !expert_offsets || !ws || (T > 0 && (!x || !topk_ids || !q_out || !sf_out || !perm)))
         return fail(NVFP4_ERR_INVALID_ARG, "quantize: null pointer");
-    if (!aligned(ws, 256) || (T > 0 && (!aligned(x, 16) || !aligned(q_out, 8) || !aligned(sf_out, 4))))
-        return fail(NVFP4_ERR_INVALID_ARG, "quantize: misaligned pointer (x 16 B, q 8 B, sf 4 B, ws 256 B)");
+    if (!aligned(ws, 256) || (T > 0 && (!aligned(x, 16) || !aligned(q_out, 16) || !aligned(sf_out, 4))))
+        return fail(NVFP4_ERR_INVALID_ARG, "quantize: misaligned pointer (x 16 B, q 16 B, sf 4 B, ws 256 B)");
+    if (!quant_offsets_fit((long long)T * k, H))
+        return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "quantize: T*k*H/16 = %lld scale bytes exceed 2^32",
+                    (long long)T * k * (H / 16));
     const size_t need = nvfp4_quantize_workspace_size(T, k, E);
     if (ws_bytes < need) return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "quantize: workspace %zu < %zu", ws_bytes, need);
     cudaStream_t st = (cudaStream_t)stream;
@@ -411,6 +422,8 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     const int E = w->E, H = w->H, I = w->I;
     if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "T=%d < 0", T);
     if ((long long)T * k >= (1ll << 31) / 2) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "T*k too large");
+    if (!quant_offsets_fit(make_layout(T, H, I, E, k).rows_cap, H))
+        return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "T*k too large for 32-bit scale offsets at H=%d", H);
     if (!prepared || !ws || (T > 0 && (!x || !ids || !topk_w || !out)))
         return fail(NVFP4_ERR_INVALID_ARG, "forward: null pointer");
     if (!aligned(ws, 256) || !aligned(prepared, 256) || (T > 0 && (!aligned(x, 16) || !aligned(out, 16))))

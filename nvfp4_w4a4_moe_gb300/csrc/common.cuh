@@ -68,67 +68,51 @@ __device__ __forceinline__ float div_by_scale(float y, float2 z)
     return __fmaf_rn(y, z.x, __fmul_rn(y, z.y));
 }
 
-// Packed FP32x2 arithmetic on 64-bit register pairs (one instruction, two
-// IEEE round-to-nearest results); element 0 in the low half.
-typedef unsigned long long f32x2;
+// Packed FP32x2 arithmetic (one instruction, two IEEE round-to-nearest
+// results) through the compiler's float2 builtins, so register pairs are
+// allocated and scheduled like any other value; element 0 in .x.
+typedef float2 f32x2;
 
-__device__ __forceinline__ f32x2 pack_f32x2(float lo, float hi)
-{
-    f32x2 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ f32x2 mul_f32x2(f32x2 a, f32x2 b)
-{
-    f32x2 r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ f32x2 fma_f32x2(f32x2 a, f32x2 b, f32x2 c)
-{
-    f32x2 r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ float lo_f32(f32x2 v) { return __uint_as_float((uint32_t)v); }
-__device__ __forceinline__ float hi_f32(f32x2 v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ f32x2 pack_f32x2(float lo, float hi) { return make_float2(lo, hi); }
+__device__ __forceinline__ f32x2 mul_f32x2(f32x2 a, f32x2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ f32x2 fma_f32x2(f32x2 a, f32x2 b, f32x2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float lo_f32(f32x2 v) { return v.x; }
+__device__ __forceinline__ float hi_f32(f32x2 v) { return v.y; }
 
 // Two BF16 values (one 32-bit word, element 0 in the low half) widened to FP32.
 __device__ __forceinline__ f32x2 bf16x2_to_f32x2(uint32_t w)
 {
-    return ((f32x2)(w & 0xFFFF0000u) << 32) | (f32x2)(w << 16);
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-// Four quotient pairs -> 32 bits of codes (pair i in byte i, the low element
+// Four quotient pairs -> 32 bits of codes (pair i in byte i, the .x element
 // of each pair in the low nibble).
 __device__ __forceinline__ uint32_t e2m1_rn_sat8(f32x2 a, f32x2 b, f32x2 c, f32x2 d)
 {
     uint32_t r;
-    asm("{\n\t.reg .f32 a0, a1, b0, b1, c0, c1, d0, d1;\n\t.reg .b8 ba, bb, bc, bd;\n\t.reg .b16 lo, hi;\n\t"
-        "mov.b64 {a0, a1}, %1;\n\tmov.b64 {b0, b1}, %2;\n\tmov.b64 {c0, c1}, %3;\n\tmov.b64 {d0, d1}, %4;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 ba, a1, a0;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 bb, b1, b0;\n\t"
-        "mov.b16 lo, {ba, bb};\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 bc, c1, c0;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 bd, d1, d0;\n\t"
-        "mov.b16 hi, {bc, bd};\n\t"
-        "mov.b32 %0, {lo, hi};\n\t}"
+    asm("{\n\t.reg .b8 ba, bb, bc, bd;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 ba, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 bb, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 bc, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 bd, %8, %7;\n\t"
+        "mov.b32 %0, {ba, bb, bc, bd};\n\t}"
         : "=r"(r)
-        : "l"(a), "l"(b), "l"(c), "l"(d));
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y), "f"(d.x), "f"(d.y));
     return r;
 }
 
 // The division table in the form the kernels keep in shared memory: the two
-// constants of each E4M3 divisor duplicated into FP32x2 pairs, and those of 6.
+// constants of each E4M3 divisor duplicated into pairs, (zh, zh, zl, zl), and
+// those of 6.
 struct DivTable2 {
-    ulonglong2 z[128];
+    float4 z[128];
     float2 six;
 };
 __device__ __forceinline__ void load_div_table(DivTable2 *dst, const DivTable &src)
 {
     for (int i = threadIdx.x; i < 128; i += blockDim.x) {
         const float2 z = src.z[i];
-        dst->z[i] = make_ulonglong2(pack_f32x2(z.x, z.x), pack_f32x2(z.y, z.y));
+        dst->z[i] = make_float4(z.x, z.x, z.y, z.y);
     }
     if (threadIdx.x == 0) dst->six = src.z[kE4M3Six];
 }
@@ -149,12 +133,13 @@ __device__ __forceinline__ uint2 quant_block16(const f32x2 (&x)[8], float amax, 
             sf_byte = 0;
             return make_uint2(0u, 0u);
         }
-        const ulonglong2 z = tab->z[sb];  // (zh, zh), (zl, zl)
+        const float4 z = tab->z[sb];  // (zh, zh, zl, zl)
+        const f32x2 zh = make_float2(z.x, z.y), zl = make_float2(z.z, z.w);
         const f32x2 gg = pack_f32x2(g, g);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const f32x2 y = mul_f32x2(x[i], gg);
-            q[i] = fma_f32x2(y, z.x, mul_f32x2(y, z.y));
+            q[i] = fma_f32x2(y, zh, mul_f32x2(y, zl));
         }
     } else {
         // g * amax overflowed: the scale saturates to 448 and the rare block

@@ -317,61 +317,108 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
 
 // ------------------------------------------------------------------ quantiser
 // [page, §NVFP4 runtime-order figure; MoE section: SFScale[expert_idx]]:
-// one thread per (token, 16-element block).  The block's BF16 values and amax
-// are read once and quantised for each of the token's k experts with that
-// expert's global scale, into the expert's permuted row.  The token's k
-// destination rows and global scales are loaded up front (KMAX >= k, so the
-// expert loop unrolls and its loads overlap).
-template <int KMAX>
-__global__ void __launch_bounds__(256) quant_experts_kernel(QuantArgs a, DivTable tab_in)
+// one warp per (token, 1024-element chunk), each lane two consecutive
+// 16-element blocks.  The blocks' BF16 values and amax are read once and
+// quantised for each of the token's k experts with that expert's global
+// scale, into the expert's permuted row: 16 bytes of codes and two scale
+// bytes per lane and expert.  Lane j < k loads expert j's destination row and
+// global scale once per item and turns the row into the row's part of both
+// output offsets; the expert loop broadcasts the three values by shuffle and
+// adds the lane's own part, so it holds no per-row address arithmetic.
+// Offsets are 32-bit (codes in 16-byte units, scales in bytes); the host
+// keeps every call within that range.
+
+// max |x| over 16 BF16 values in 8 words: signs cleared, the two halves
+// compared as unsigned 16-bit integers (the magnitudes of non-negative
+// floats order like their bit patterns), then the two halves.  As FP32.
+__device__ __forceinline__ float amax16_bf16(const uint32_t *w)
+{
+    uint32_t m = w[0] & 0x7FFF7FFFu;
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+        const uint32_t v = w[i] & 0x7FFF7FFFu;
+        asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(v));
+    }
+    return __uint_as_float(max(m << 16, m & 0xFFFF0000u));
+}
+
+constexpr int kQuantThreads = 128;  // 5 CTAs (20 warps) per SM at <= 96 registers
+
+// SWZ: scales in the swizzled tensor-core layout (else linear [rows, H/16]).
+template <bool SWZ>
+__global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantArgs a, DivTable tab_in)
 {
     __shared__ DivTable2 tab;
     load_div_table(&tab, tab_in);
     __syncthreads();
     if (a.hdr && a.hdr->status != 0) return;
-    const int nb = a.H >> 4;
-    const int k = a.k;
-    const long long total = (long long)a.T * nb;
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    const int32_t *__restrict__ ids = a.ids;
-    const int *__restrict__ row_of = a.row_of;
-    const float *__restrict__ gsc = a.g;
-    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
-        const int t = (int)(idx / nb);
-        const int b = (int)(idx - (long long)t * nb);
-        int rows[KMAX];
-        float gs[KMAX];
-#pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            rows[j] = 0;
-            gs[j] = 1.0f;
-            if (j < k) {
-                const int f = t * k + j;
-                rows[j] = __ldg(row_of + f);
-                gs[j] = __ldg(gsc + __ldg(ids + f));
-            }
+    const int lane = threadIdx.x & 31;
+    const int k = a.k, H = a.H;
+    const int npair = H >> 5;              // block pairs (32 elements) per row
+    const int nchunk = (npair + 31) >> 5;  // warp items per row
+    uint4 *const q16 = reinterpret_cast<uint4 *>(a.q);
+    // items (t, c) = warp index + n * (warps in the grid), walked without dividing per item
+    const int wpb = blockDim.x >> 5;
+    const int warps = gridDim.x * wpb;
+    const int w0 = blockIdx.x * wpb + (threadIdx.x >> 5);
+    const int dt = warps / nchunk, dc = warps - dt * nchunk;
+    int t = w0 / nchunk, c = w0 - (w0 / nchunk) * nchunk;
+    while (t < a.T) {
+        const int pair = c * 32 + lane;
+        uint32_t my_q = 0, my_s = 0;  // lane j < k: row parts of expert j's code and scale offsets
+        float my_g = 1.0f;
+        if (lane < k) {
+            const int f = t * k + lane;
+            const uint32_t row = (uint32_t)__ldg(a.row_of + f);
+            my_g = __ldg(a.g + __ldg(a.ids + f));
+            my_q = row * (uint32_t)npair;
+            my_s = SWZ ? ((row >> 7) * (uint32_t)a.sf_kc * 512u + (row & 31u) * 16u + ((row >> 5) & 3u) * 4u)
+                       : row * (uint32_t)(H >> 4);
         }
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + (size_t)b * 16);
-        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        f32x2 x[8];
-        uint32_t amax_bits = 0;  // max |x| on the bit patterns (non-negative floats order as integers)
+        const bool active = pair < npair;
+        const int b = 2 * pair;  // even: both scale bytes share one aligned 16-bit word
+        const uint32_t lane_s = SWZ ? (uint32_t)(b >> 2) * 512u + (uint32_t)(b & 3) : (uint32_t)b;
+        uint32_t w[16];
+        if (active) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + (size_t)pair * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v = __ldg(src + i);
+                w[4 * i] = v.x;
+                w[4 * i + 1] = v.y;
+                w[4 * i + 2] = v.z;
+                w[4 * i + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = 0u;
+        }
+        f32x2 x0[8], x1[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            x[i] = bf16x2_to_f32x2(w[i]);
-            amax_bits = max(amax_bits, max((w[i] << 16) & 0x7FFFFFFFu, w[i] & 0x7FFF0000u));
+            x0[i] = bf16x2_to_f32x2(w[i]);
+            x1[i] = bf16x2_to_f32x2(w[8 + i]);
         }
-        const float amax = __uint_as_float(amax_bits);
-#pragma unroll
-        for (int j = 0; j < KMAX; ++j) {
-            if (j >= k) break;
-            uint32_t sb;
-            const uint2 pk = quant_block16(x, amax, gs[j], &tab, sb);
-            const int row = rows[j];
-            *reinterpret_cast<uint2 *>(a.q + (size_t)row * (a.H >> 1) + (size_t)b * 8) = pk;
-            uint8_t *dst = a.sf_swizzled ? a.sf + swz_sf_offset(row, b >> 2, a.sf_kc) + (b & 3)
-                                         : a.sf + (size_t)row * nb + b;
-            *dst = (uint8_t)sb;
+        const float amax0 = amax16_bf16(w), amax1 = amax16_bf16(w + 8);
+        // not unrolled: the compact loop runs faster than eight inlined copies
+#pragma unroll 1
+        for (int j = 0; j < k; ++j) {
+            const uint32_t qo = __shfl_sync(0xffffffffu, my_q, j) + (uint32_t)pair;
+            const uint32_t so = __shfl_sync(0xffffffffu, my_s, j) + lane_s;
+            const float g = __shfl_sync(0xffffffffu, my_g, j);
+            if (active) {
+                uint32_t s0, s1;
+                const uint2 p0 = quant_block16(x0, amax0, g, &tab, s0);
+                const uint2 p1 = quant_block16(x1, amax1, g, &tab, s1);
+                q16[qo] = make_uint4(p0.x, p0.y, p1.x, p1.y);
+                *reinterpret_cast<uint16_t *>(a.sf + so) = (uint16_t)(s0 | (s1 << 8));
+            }
+        }
+        t += dt;
+        c += dc;
+        if (c >= nchunk) {
+            c -= nchunk;
+            ++t;
         }
     }
 }
@@ -565,28 +612,23 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t st)
 
 cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st)
 {
-    const long long work = (long long)a.T * (a.H >> 4);
+    const long long work = (long long)a.T * ((a.H / 32 + 31) / 32) * 32;  // one lane per block pair
     // One full wave of resident CTAs, grid-striding over the work.
     auto launch = [&](auto kernel) {
         int per_sm = 1;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0) != cudaSuccess || per_sm < 1)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kQuantThreads, 0) != cudaSuccess ||
+            per_sm < 1)
             per_sm = 1;
         long long grid = (long long)sm_count() * per_sm;
-        const long long need = (work + 255) / 256;
+        const long long need = (work + kQuantThreads - 1) / kQuantThreads;
         if (grid > need) grid = need;
         if (grid < 1) grid = 1;
-        kernel<<<(int)grid, 256, 0, st>>>(a, div_table());
+        kernel<<<(int)grid, kQuantThreads, 0, st>>>(a, div_table());
     };
-    if (a.k <= 1)
-        launch(quant_experts_kernel<1>);
-    else if (a.k <= 2)
-        launch(quant_experts_kernel<2>);
-    else if (a.k <= 4)
-        launch(quant_experts_kernel<4>);
-    else if (a.k <= 8)
-        launch(quant_experts_kernel<8>);
+    if (a.sf_swizzled)
+        launch(quant_experts_kernel<true>);
     else
-        launch(quant_experts_kernel<32>);
+        launch(quant_experts_kernel<false>);
     return cudaGetLastError();
 }
 
