@@ -50,8 +50,8 @@ LAUNCHES_PER_STEP = 5
 NCU_TRAFFIC = {
     "tokens": 8192,
     "source_sha1": {"nvfp4_w4a4_moe_gb300/csrc/kernels_gemm.cu": "2549ac09dff52d41bfff1904b666f72ff1a13f19",
-                    "nvfp4_w4a4_moe_gb300/csrc/common.cuh": "5682b9898c256b93a3a8fa14f68dde76ff313ab0"},
-    "bytes": {"gemm_w13": 383486976 + 101337344, "gemm_w2": 267535104 + 67844096},
+                    "nvfp4_w4a4_moe_gb300/csrc/common.cuh": "cd0438b935211e7a4d13568e2c81bc78fbe11871"},
+    "bytes": {"gemm_w13": 383488256 + 101186304, "gemm_w2": 267173120 + 68059136},
 }
 
 
