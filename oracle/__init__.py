@@ -68,6 +68,10 @@ def _load_locked(path):
         "orc_e4m3_encode_array": (None, [P, I64, P, ctypes.c_int]),
         "orc_quant_block16": (ctypes.c_int, [P, F32, P]),
         "orc_quant_rows": (None, [P, I64, I64, P, P, P, ctypes.c_int]),
+        "orc_ue8m0_value": (F64, [ctypes.c_int]),
+        "orc_ue8m0_encode": (ctypes.c_int, [F32]),
+        "orc_quant_block16_ue8m0": (ctypes.c_int, [P, F32, P]),
+        "orc_quant_rows_ue8m0": (None, [P, I64, I64, P, P, P, ctypes.c_int]),
         "orc_validate_scales": (I64, [P, P, I64, P]),
         "orc_route": (ctypes.c_int, [P, I64, I32, I32, P, P]),
         "orc_router": (ctypes.c_int, [P, I64, I32, I32, P, P]),
@@ -166,18 +170,34 @@ def reciprocal_f32(s: np.ndarray) -> np.ndarray:
         return (np.float32(1.0) / s).astype(np.float32)
 
 
-def quant_block16(x16: np.ndarray, g: float):
-    """One micro-block: returns (scale byte, 16 codes)."""
+def ue8m0_value(byte: int) -> float:
+    return float(_L().orc_ue8m0_value(int(byte)))
+
+
+def ue8m0_encode(t: float) -> int:
+    return int(_L().orc_ue8m0_encode(np.float32(t)))
+
+
+def ue8m0_values(bytes_: np.ndarray) -> np.ndarray:
+    table = np.array([ue8m0_value(b) for b in range(256)], dtype=np.float64)
+    return table[np.asarray(bytes_, dtype=np.uint8)]
+
+
+def quant_block16(x16: np.ndarray, g: float, ue8m0: bool = False):
+    """One micro-block: returns (scale byte, 16 codes); the scale is E4M3, or
+    UE8M0 when ue8m0 is set."""
     x = np.ascontiguousarray(x16, dtype=np.float32)
     assert x.size == 16
     codes = np.empty(16, dtype=np.uint8)
-    sb = _L().orc_quant_block16(_p(x), np.float32(g), _p(codes))
+    fn = _L().orc_quant_block16_ue8m0 if ue8m0 else _L().orc_quant_block16
+    sb = fn(_p(x), np.float32(g), _p(codes))
     return int(sb), codes
 
 
-def quant_rows(x: np.ndarray, g_row: np.ndarray):
+def quant_rows(x: np.ndarray, g_row: np.ndarray, ue8m0: bool = False):
     """Quantise rows of FP32 values (K % 16 == 0), row r with global scale
-    g_row[r].  Returns (q [rows, K/2] packed, sf [rows, K/16] E4M3 bytes)."""
+    g_row[r].  Returns (q [rows, K/2] packed, sf [rows, K/16] scale bytes,
+    E4M3 or, with ue8m0, UE8M0)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     rows, K = x.shape
     assert K % 16 == 0
@@ -185,7 +205,8 @@ def quant_rows(x: np.ndarray, g_row: np.ndarray):
     q = np.empty((rows, K // 2), dtype=np.uint8)
     sf = np.empty((rows, K // 16), dtype=np.uint8)
     if rows:
-        _L().orc_quant_rows(_p(x), rows, K, _p(g), _p(q), _p(sf), 0)
+        fn = _L().orc_quant_rows_ue8m0 if ue8m0 else _L().orc_quant_rows
+        fn(_p(x), rows, K, _p(g), _p(q), _p(sf), 0)
     return q, sf
 
 
@@ -198,24 +219,26 @@ def unpack_codes(q: np.ndarray) -> np.ndarray:
     return out
 
 
-def dequant(q: np.ndarray, sf: np.ndarray, g) -> np.ndarray:
+def dequant(q: np.ndarray, sf: np.ndarray, g, ue8m0: bool = False) -> np.ndarray:
     """fp64 dequantisation code * scale / g (g per row or scalar)."""
     codes = unpack_codes(q)
     K = codes.shape[-1]
-    v = e2m1_values(codes) * np.repeat(e4m3_values(sf), 16, axis=-1)[..., :K]
+    scales = ue8m0_values(sf) if ue8m0 else e4m3_values(sf)
+    v = e2m1_values(codes) * np.repeat(scales, 16, axis=-1)[..., :K]
     g = np.asarray(g, dtype=np.float64)
     if g.ndim == 1:
         g = g[:, None]
     return v / g
 
 
-def quantize_weight(w_bf16: np.ndarray):
+def quantize_weight(w_bf16: np.ndarray, ue8m0: bool = False):
     """Static weight quantisation of one (expert, projection) tensor [N, K]
     (page "Gemma 4 NVFP4 MoE 空输出", glossary "Static weight quantization":
     packed FP4 weight + E4M3 weight_scale + FP32 weight_scale_2).
     Reading: weight_scale_2 = fl(amax / 2688) over the whole tensor (the 2688 =
     6 * 448 range of §NVFP4), and the quantiser's global scale is its FP32
     reciprocal, exactly as for activations.
+    With ue8m0 the block scales are UE8M0 bytes (same weight_scale_2).
     Returns (q [N, K/2], sf [N, K/16], weight_scale_2 float32)."""
     wf = (np.asarray(w_bf16, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
     amax = np.float32(np.abs(wf).max())
@@ -224,7 +247,7 @@ def quantize_weight(w_bf16: np.ndarray):
         return np.zeros((N, K // 2), np.uint8), np.zeros((N, K // 16), np.uint8), np.float32(0.0)
     scale2 = np.float32(amax / np.float32(2688.0))
     g = reciprocal_f32(np.array([scale2]))[0]
-    q, sf = quant_rows(wf, np.full(wf.shape[0], g, dtype=np.float32))
+    q, sf = quant_rows(wf, np.full(wf.shape[0], g, dtype=np.float32), ue8m0=ue8m0)
     return q, sf, scale2
 
 

@@ -232,6 +232,55 @@ int orc_quant_block16(const float *x, float g, uint8_t *codes16)
     return sb;
 }
 
+/* ------------------------------------------------------------------------ */
+/* UE8M0 block scales (the variant the quantiser's UE8M0_SF flag selects)     */
+/* ------------------------------------------------------------------------ */
+
+/* [page, MoE section: the expert quantiser is a template with a UE8M0_SF
+ * flag] -- the page names the flag and nothing more.  Reading: UE8M0 is the
+ * MX-style scale byte, an unsigned biased exponent: byte b in 0..254 has value
+ * 2^(b - 127) and 255 is NaN. */
+double orc_ue8m0_value(int byte)
+{
+    if (byte == 255) return NAN;
+    return ldexp(1.0, byte - 127);
+}
+
+/* Reading for the encoding: the block scale is the same t as in the E4M3 path,
+ * rounded up to a power of two, so that the block's largest element, divided
+ * by the scale, stays at or below 6 and does not saturate; t = 0 and values
+ * below the range take the smallest byte (2^-127), values above it the largest
+ * finite one (2^127).  The scan visits the bytes in value order. */
+int orc_ue8m0_encode(float t)
+{
+    double a = (double)t;
+    for (int b = 0; b < 255; ++b)
+        if (ldexp(1.0, b - 127) >= a) return b;
+    return 254;
+}
+
+/* orc_quant_block16 with a UE8M0 scale: steps 1, 2 and 4 as there, step 3
+ * rounds t up to the UE8M0 scale s.  s is a power of two, so fl(y / s) is
+ * the exact quotient rounded once.  Returns the scale byte. */
+int orc_quant_block16_ue8m0(const float *x, float g, uint8_t *codes16)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax) amax = a;
+    }
+    float ga = g * amax;
+    float t = ga / 6.0f;
+    int sb = orc_ue8m0_encode(t);
+    double s = orc_ue8m0_value(sb);
+    for (int i = 0; i < 16; ++i) {
+        float y = x[i] * g;
+        float q = (float)((double)y / s); /* the quotient is exact in double */
+        codes16[i] = (uint8_t)orc_e2m1_encode(q);
+    }
+    return sb;
+}
+
 /* Packing [page, §NVFP4, conversion listing and glossary "Packing"]: two E2M1
  * values per byte.  Reading of the listing's operand order under the PTX
  * definition of the x2 conversion (first source to the upper half): element
@@ -246,6 +295,7 @@ typedef struct {
     int64_t K;
     const float *g_row;
     uint8_t *q, *sf;
+    int ue8m0;
 } quant_ctx;
 
 static void quant_range(int64_t lo, int64_t hi, void *p)
@@ -255,7 +305,9 @@ static void quant_range(int64_t lo, int64_t hi, void *p)
     for (int64_t r = lo; r < hi; ++r) {
         const float *xr = c->x + r * c->K;
         for (int64_t b = 0; b < c->K / 16; ++b) {
-            c->sf[r * (c->K / 16) + b] = (uint8_t)orc_quant_block16(xr + 16 * b, c->g_row[r], codes);
+            c->sf[r * (c->K / 16) + b] =
+                (uint8_t)(c->ue8m0 ? orc_quant_block16_ue8m0(xr + 16 * b, c->g_row[r], codes)
+                                   : orc_quant_block16(xr + 16 * b, c->g_row[r], codes));
             for (int i = 0; i < 8; ++i)
                 c->q[r * (c->K / 2) + 8 * b + i] = pack2(codes[2 * i], codes[2 * i + 1]);
         }
@@ -268,7 +320,15 @@ static void quant_range(int64_t lo, int64_t hi, void *p)
 void orc_quant_rows(const float *x, int64_t rows, int64_t K, const float *g_row, uint8_t *q,
                     uint8_t *sf, int nthreads)
 {
-    quant_ctx c = {x, K, g_row, q, sf};
+    quant_ctx c = {x, K, g_row, q, sf, 0};
+    parallel_for(rows, nthreads, quant_range, &c);
+}
+
+/* orc_quant_rows with UE8M0 block scales (sf holds UE8M0 bytes). */
+void orc_quant_rows_ue8m0(const float *x, int64_t rows, int64_t K, const float *g_row, uint8_t *q,
+                          uint8_t *sf, int nthreads)
+{
+    quant_ctx c = {x, K, g_row, q, sf, 1};
     parallel_for(rows, nthreads, quant_range, &c);
 }
 

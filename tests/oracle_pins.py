@@ -251,6 +251,65 @@ def pin_route_bruteforce(orc):
         assert list(offsets) == [0] + list(np.cumsum(counts))
 
 
+def pin_ue8m0(orc):
+    """UE8M0 block scales.  Byte values against FP32 bit patterns (a float whose
+    exponent field is b and mantissa 0 is 2^(b-127); 2^-127 is the subnormal
+    0x00400000).  The encoding is the smallest power of two at or above t,
+    checked with frexp on powers of two, their neighbours and log-uniform
+    values.  Blocks: hand cases; against a numpy FP32 recomputation of
+    x*g/s; no element saturates and the largest reaches at least 3; sign
+    symmetry; the zero block."""
+    for b in range(1, 255):
+        assert orc.ue8m0_value(b) == float(np.uint32(b << 23).view(np.float32)), b
+    assert orc.ue8m0_value(0) == float(np.uint32(0x00400000).view(np.float32))
+    assert math.isnan(orc.ue8m0_value(255))
+
+    def by_frexp(t):
+        if not t > 2.0 ** -127:
+            return 0
+        if math.isinf(t):
+            return 254
+        m, e = math.frexp(t)  # t = m * 2^e, 0.5 <= m < 1
+        return min((e - 1 if m == 0.5 else e) + 127, 254)
+
+    r = _rng(31)
+    ts = [0.0, float(np.finfo(np.float32).max), float("inf"), 2.0 ** -149, 2.0 ** -127, 2.0 ** 127]
+    for k in range(-149, 128):
+        p2 = np.float32(2.0) ** np.float32(k) if k > -127 else np.float32(2.0 ** k)
+        ts += [float(p2), float(np.nextafter(p2, np.float32(np.inf))), float(np.nextafter(p2, np.float32(0)))]
+    with np.errstate(over="ignore"):  # values beyond FP32 become inf, which is a case too
+        ts += list(np.exp(r.uniform(-100, 100, 4000)).astype(np.float32).astype(float))
+    for t in ts:
+        assert orc.ue8m0_encode(t) == by_frexp(float(np.float32(t))), t
+
+    table = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, 0, -0.5, -1, -1.5, -2, -3, -4, -6], np.float32)
+    sb, codes = orc.quant_block16(table, 1.0, ue8m0=True)
+    assert sb == 127 and codes.tolist() == [0, 1, 2, 3, 4, 5, 6, 7, 0, 9, 10, 11, 12, 13, 14, 15]
+    sb, codes = orc.quant_block16(table * 2, 1.0, ue8m0=True)
+    assert sb == 128 and codes.tolist() == [0, 1, 2, 3, 4, 5, 6, 7, 0, 9, 10, 11, 12, 13, 14, 15]
+    sb, codes = orc.quant_block16(np.full(16, 7.0, np.float32), 1.0, ue8m0=True)
+    assert sb == 128 and np.all(codes == 6)  # t = 7/6 -> s = 2; 3.5 ties to the even code, 4.0
+    sb, codes = orc.quant_block16(np.zeros(16, np.float32), 3.0, ue8m0=True)
+    assert sb == 0 and np.all(codes == 0)
+    for _ in range(3000):
+        x = (r.standard_normal(16) * np.exp(r.uniform(-20, 20))).astype(np.float32)
+        g = np.float32(np.exp(r.uniform(-10, 10)))
+        sb, codes = orc.quant_block16(x, g, ue8m0=True)
+        amax = np.float32(np.abs(x).max())
+        t = np.float32(np.float32(g * amax) / np.float32(6.0))
+        s = orc.ue8m0_value(sb)
+        assert s >= t and (sb == 0 or s / 2 < t)
+        y = (x * g).astype(np.float32)
+        q = (y.astype(np.float64) / s).astype(np.float32)
+        assert np.array_equal(codes, orc.e2m1_encode(q))
+        vals = orc.e2m1_values(codes)
+        assert np.all(np.abs(vals) <= 6)
+        if sb > 0:
+            assert np.abs(vals).max() >= 3
+        sb2, codes2 = orc.quant_block16(-x, g, ue8m0=True)
+        assert sb2 == sb and np.array_equal(codes2, codes ^ 8)
+
+
 def pin_router(orc):
     """Router pins: k = E is SciPy's softmax in the stable descending order of the
     logits; for k < E the renormalised weights are the softmax of the selected
@@ -495,5 +554,5 @@ ALL_PINS = [
     pin_e2m1_table, pin_e2m1_ties, pin_e2m1_boundaries, pin_e4m3_roundtrip, pin_e4m3_frexp,
     pin_e4m3_torch, pin_block_worked, pin_identity_2688, pin_block_invariances,
     pin_route_bruteforce, pin_gemm_fraction, pin_gemm_fp64, pin_silu_mul, pin_combine_special,
-    pin_forward_stepwise, pin_validate, pin_rmsnorm, pin_router,
+    pin_forward_stepwise, pin_validate, pin_rmsnorm, pin_router, pin_ue8m0,
 ]

@@ -34,6 +34,9 @@ MUTANTS = [
     ("rmsnorm_eps_outside", "sqrt(ss / (double)H + eps)", "(sqrt(ss / (double)H) + eps)", 0),
     ("router_ties_to_higher", "(best < 0 || l[e] > l[best])", "(best < 0 || l[e] >= l[best])", 0),
     ("router_smallest_first", "(best < 0 || l[e] > l[best])", "(best < 0 || l[e] < l[best])", 0),
+    ("ue8m0_round_to_nearest", "if (ldexp(1.0, b - 127) >= a) return b;", "if (1.5 * ldexp(1.0, b - 127) >= a) return b;", 0),
+    ("ue8m0_bias_126", "return ldexp(1.0, byte - 127);", "return ldexp(1.0, byte - 126);", 0),
+    ("ue8m0_no_global_scale", "float y = x[i] * g;", "float y = x[i];", 1),
     ("router_not_renormalised", "(float)(p[ids[t * k + j]] / zk)", "(float)(p[ids[t * k + j]])", 0),
 ]
 
