@@ -301,6 +301,7 @@ def run_ours(args, rank, world):
     e2e = e2e_host(m, torch, w, layer, args)
     decode = decode_leg(m, torch, w, args)
     router = router_leg(m, torch, args)
+    ue8m0 = ue8m0_leg(m, torch, args)
 
     pk = peaks()
     n_active = int((np.bincount(layer.topk_ids.ravel(), minlength=E) > 0).sum())
@@ -354,6 +355,7 @@ def run_ours(args, rank, world):
         "quant": qres,
         "decode": decode,
         "router": router,
+        "ue8m0": ue8m0,
         "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * K,
         "clocks": clocks.summary(),
@@ -458,6 +460,33 @@ def decode_leg(m, torch, w, args):
                        "tokens_per_s": T / (best * 1e-6), "experts_touched": touched,
                        "weight_gbs": touched * per_expert / (best * 1e-6) / 1e9}
     return res
+
+
+def ue8m0_leg(m, torch, args):
+    """The activation quantiser with E4M3 and with UE8M0 block scales on the
+    quantiser workload (4096 x 2816, 128 experts, uniform top-8), through the
+    stand-alone entry point: each call runs the scale check (with its host
+    synchronisation), the token reorder and the quantiser, so the difference
+    between the two is the quantiser's."""
+    L = S.quantiser()
+    x = torch.from_numpy(L.x.view(np.int16)).cuda().view(torch.bfloat16)
+    ids = torch.from_numpy(L.topk_ids).cuda()
+    scale = torch.from_numpy(L.w13_input_scale).cuda()
+    ws = torch.empty(m.quantize_workspace_size(L.T, L.k, L.E), dtype=torch.uint8, device="cuda")
+    res = {}
+    for name, fmt in (("e4m3", 0), ("ue8m0", m.SF_UE8M0)):
+        layout = m.SF_SWIZZLED | fmt
+        for _ in range(5):
+            m.quantize_experts(x, ids, scale, L.E, sf_layout=layout, ws=ws)
+        n = 50
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            m.quantize_experts(x, ids, scale, L.E, sf_layout=layout, ws=ws)
+        torch.cuda.synchronize()
+        res[name] = {"us_per_call": (time.perf_counter() - t0) / n * 1e6}
+    return {"workload": "4096 tokens x 2816, 128 experts, uniform top-8", "calls": res,
+            "note": "synchronous calls: scale check + token reorder + quantiser each"}
 
 
 def router_leg(m, torch, args):

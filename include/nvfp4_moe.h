@@ -71,6 +71,16 @@ typedef enum {
 
 enum { NVFP4_SF_LINEAR = 0, NVFP4_SF_SWIZZLED = 1 };
 
+/* OR'ed into a quantiser's scale layout (or passed as sf_format): block scales
+ * as UE8M0 bytes instead of E4M3 [page "Gemma 4 NVFP4 MoE 空输出", MoE section:
+ * the quantiser template's UE8M0_SF flag].  A UE8M0 byte b is the power of
+ * two 2^(b - 127) (255 is NaN, never written).  The scale of a block is the
+ * E4M3 path's t = fl(fl(g*amax)/6) rounded up to a power of two, clamped to
+ * 2^-127 .. 2^127, so no element of the block saturates; the codes are then
+ * e2m1(fl(fl(x*g)/s)) as in the E4M3 path.  The tensor-core GEMMs of
+ * nvfp4_moe_forward take E4M3 block scales only. */
+enum { NVFP4_SF_UE8M0 = 4 };
+
 /* Element type of the router's logits (nvfp4_router_topk). */
 enum { NVFP4_LOGITS_F32 = 0, NVFP4_LOGITS_BF16 = 1 };
 
@@ -116,7 +126,8 @@ int nvfp4_validate_scales(const float *scales, const uint8_t *written, int n, vo
  * per 16-block, s = e4m3(fl(fl(g*amax)/6)), q = e2m1(fl(fl(x*g)/s)), with
  * round-to-nearest-even and saturation; an all-zero-scale block gets code 0.
  * Outputs: q_out [R, H/2] packed codes; sf_out scales in `sf_layout`
- * (LINEAR: [R, H/16]; SWIZZLED: ceil(R/128) * ceil(H/64) * 512 bytes);
+ * (LINEAR: [R, H/16]; SWIZZLED: ceil(R/128) * ceil(H/64) * 512 bytes),
+ * E4M3 bytes, or UE8M0 bytes when NVFP4_SF_UE8M0 is OR'ed into sf_layout;
  * expert_offsets [E+1] (first permuted row of each expert, [E] = R);
  * perm [R] (permuted row -> f).
  * SYNCHRONOUS: input_scale is validated first and the call waits for the
@@ -339,6 +350,15 @@ int nvfp4_router_topk(const void *logits, int logits_dtype, int T, int E, int k,
 size_t nvfp4_quantize_weights_workspace_size(int count);
 int nvfp4_quantize_weights(const uint16_t *w, int count, int N, int K, uint8_t *q, uint8_t *sf,
                            float *scale2, void *ws, size_t ws_bytes, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_quantize_weights_format -- nvfp4_quantize_weights with the block-scale
+ * format chosen: sf_format 0 writes E4M3 scales (as nvfp4_quantize_weights),
+ * NVFP4_SF_UE8M0 writes UE8M0 scales (see NVFP4_SF_UE8M0; weight_scale_2 and
+ * the codes' rule are unchanged).  Any other sf_format: NVFP4_ERR_INVALID_ARG.
+ */
+int nvfp4_quantize_weights_format(const uint16_t *w, int count, int N, int K, int sf_format, uint8_t *q,
+                                  uint8_t *sf, float *scale2, void *ws, size_t ws_bytes, nvfp4_stream_t stream);
 
 /*
  * nvfp4_selftest_block_division -- host-side exhaustive check of the exact

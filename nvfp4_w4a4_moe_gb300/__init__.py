@@ -21,6 +21,7 @@ OK, ERR_INVALID_ARG, ERR_SCALE_INVALID, ERR_UNSUPPORTED_SHAPE, ERR_CUDA, ERR_DEV
     ERR_WORKSPACE_TOO_SMALL = range(7)
 SF_LINEAR, SF_SWIZZLED = 0, 1
 LOGITS_F32, LOGITS_BF16 = 0, 1
+SF_UE8M0 = 4
 SCALES_PREVALIDATED, SYNC_CHECK, DEBUG_KEEP_H = 1, 2, 4
 
 _lib = None
@@ -83,6 +84,7 @@ def load():
             "nvfp4_router_topk": (I, [P, I, I, I, I, P, P, P]),
             "nvfp4_quantize_weights_workspace_size": (SZ, [I]),
             "nvfp4_quantize_weights": (I, [P, I, I, I, P, P, P, P, SZ, P]),
+            "nvfp4_quantize_weights_format": (I, [P, I, I, I, I, P, P, P, P, SZ, P]),
             "nvfp4_selftest_block_division": (ctypes.c_longlong, [I]),
         }
         for name, (res, args) in sig.items():
@@ -137,13 +139,14 @@ def quantize_workspace_size(T: int, k: int, E: int) -> int:
 def quantize_experts(x: torch.Tensor, topk_ids: torch.Tensor, input_scale: torch.Tensor, E: int,
                      sf_layout: int = SF_LINEAR, ws: torch.Tensor | None = None, stream=None):
     """x [T, H] bf16, topk_ids [T, k] int32, input_scale [E] f32 (device).
+    sf_layout: SF_LINEAR or SF_SWIZZLED, optionally | SF_UE8M0 for UE8M0 scales.
     Returns (q [R, H/2] u8, sf u8, expert_offsets [E+1] i32, perm [R] i32)."""
     T, H = x.shape
     k = topk_ids.shape[1]
     R = T * k
     dev = x.device
     q = torch.empty((R, H // 2), dtype=torch.uint8, device=dev)
-    if sf_layout == SF_SWIZZLED:
+    if (sf_layout & ~SF_UE8M0) == SF_SWIZZLED:
         sf = torch.empty(((R + 127) // 128) * ((H + 63) // 64) * 512, dtype=torch.uint8, device=dev)
     else:
         sf = torch.empty((R, H // 16), dtype=torch.uint8, device=dev)
@@ -168,7 +171,7 @@ def quantize_experts_static_scratch(x: torch.Tensor, topk_ids: torch.Tensor, inp
     R = T * k
     dev = x.device
     q = torch.empty((R, H // 2), dtype=torch.uint8, device=dev)
-    if sf_layout == SF_SWIZZLED:
+    if (sf_layout & ~SF_UE8M0) == SF_SWIZZLED:
         sf = torch.empty(((R + 127) // 128) * ((H + 63) // 64) * 512, dtype=torch.uint8, device=dev)
     else:
         sf = torch.empty((R, H // 16), dtype=torch.uint8, device=dev)
@@ -352,8 +355,9 @@ def router_topk(logits: torch.Tensor, k: int, topk_ids: torch.Tensor | None = No
     return topk_ids, topk_weights
 
 
-def quantize_weights(w: torch.Tensor, stream=None):
-    """w [count, N, K] bf16 (device) -> (q [count, N, K/2] u8, sf [count, N, K/16] u8, scale2 [count] f32)."""
+def quantize_weights(w: torch.Tensor, stream=None, ue8m0: bool = False):
+    """w [count, N, K] bf16 (device) -> (q [count, N, K/2] u8, sf [count, N, K/16] u8, scale2 [count] f32);
+    the block scales are E4M3, or UE8M0 with ue8m0."""
     count, N, K = w.shape
     dev = w.device
     q = torch.empty((count, N, K // 2), dtype=torch.uint8, device=dev)
@@ -361,6 +365,6 @@ def quantize_weights(w: torch.Tensor, stream=None):
     s2 = torch.empty(count, dtype=torch.float32, device=dev)
     n = int(load().nvfp4_quantize_weights_workspace_size(count))
     ws = _empty_ws(n, dev)
-    _check(load().nvfp4_quantize_weights(_ptr(w), count, N, K, _ptr(q), _ptr(sf), _ptr(s2), _ptr(ws), ws.numel(),
-                                         _stream(stream)))
+    _check(load().nvfp4_quantize_weights_format(_ptr(w), count, N, K, SF_UE8M0 if ue8m0 else 0, _ptr(q), _ptr(sf),
+                                                _ptr(s2), _ptr(ws), ws.numel(), _stream(stream)))
     return q, sf, s2

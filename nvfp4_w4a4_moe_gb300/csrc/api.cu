@@ -282,6 +282,8 @@ int nvfp4_quantize_experts(const uint16_t *x, int T, int H, const int32_t *topk_
     if (E < 1 || E > 1024 || k < 1 || k > 32 || k > E || T < 0)
         return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "quantize: E=%d k=%d T=%d unsupported", E, k, T);
     if (H <= 0 || H % 64 != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "quantize: H=%d is not a multiple of 64", H);
+    const int sf_ue8m0 = (sf_layout & NVFP4_SF_UE8M0) != 0;
+    sf_layout &= ~NVFP4_SF_UE8M0;
     if (sf_layout != NVFP4_SF_LINEAR && sf_layout != NVFP4_SF_SWIZZLED)
         return fail(NVFP4_ERR_INVALID_ARG, "unknown scale layout %d", sf_layout);
     if (!input_scale || !expert_offsets || !ws || (T > 0 && (!x || !topk_ids || !q_out || !sf_out || !perm)))
@@ -352,6 +354,7 @@ int nvfp4_quantize_experts(const uint16_t *x, int T, int H, const int32_t *topk_
     qa.sf = sf_out;
     qa.sf_swizzled = sf_layout == NVFP4_SF_SWIZZLED;
     qa.sf_kc = kc;
+    qa.sf_ue8m0 = sf_ue8m0;
     qa.hdr = hdr;
     NV_CUDA(launch_quant_experts(qa, st), "launching the quantiser");
     rc = read_header(hdr, st, &h);
@@ -499,6 +502,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     qa.sf = base + L.sf1;
     qa.sf_swizzled = 1;
     qa.sf_kc = L.kc1;
+    qa.sf_ue8m0 = 0;  // the tensor-core GEMM takes E4M3 block scales
     qa.hdr = hdr;
     NV_CUDA(launch_quant_experts(qa, st), "launching the a1 quantiser");
     NV_CUDA(mark(3), "recording an event");
@@ -781,13 +785,21 @@ size_t nvfp4_quantize_weights_workspace_size(int count) { return count > 0 ? up2
 int nvfp4_quantize_weights(const uint16_t *w, int count, int N, int K, uint8_t *q, uint8_t *sf, float *scale2,
                            void *ws, size_t ws_bytes, nvfp4_stream_t stream)
 {
+    return nvfp4_quantize_weights_format(w, count, N, K, 0, q, sf, scale2, ws, ws_bytes, stream);
+}
+
+int nvfp4_quantize_weights_format(const uint16_t *w, int count, int N, int K, int sf_format, uint8_t *q,
+                                  uint8_t *sf, float *scale2, void *ws, size_t ws_bytes, nvfp4_stream_t stream)
+{
+    if (sf_format != 0 && sf_format != NVFP4_SF_UE8M0)
+        return fail(NVFP4_ERR_INVALID_ARG, "quantize_weights: sf_format must be 0 (E4M3) or NVFP4_SF_UE8M0");
     if (count < 1 || count > 65535 || N < 1 || K < 16 || K % 16 != 0 || !w || !q || !sf || !scale2 || !ws)
         return fail(NVFP4_ERR_INVALID_ARG, "quantize_weights: bad arguments");
     if (!aligned(q, 8)) return fail(NVFP4_ERR_INVALID_ARG, "quantize_weights: q must be 8-byte aligned");
     if (ws_bytes < nvfp4_quantize_weights_workspace_size(count))
         return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "quantize_weights: workspace too small");
     NV_CUDA(launch_quantize_weights(w, count, N, K, q, sf, scale2, static_cast<unsigned *>(ws),
-                                    (cudaStream_t)stream),
+                                    sf_format == NVFP4_SF_UE8M0, (cudaStream_t)stream),
             "launching the weight quantiser");
     return NVFP4_OK;
 }

@@ -61,6 +61,7 @@ struct QuantArgs {
     uint8_t *q;
     uint8_t *sf;
     int sf_swizzled, sf_kc;
+    int sf_ue8m0;  // block scales as UE8M0 powers of two (else E4M3)
     const DevHeader *hdr;
 };
 cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st);
@@ -81,7 +82,7 @@ cudaError_t launch_router_topk(const void *logits, int bf16, int T, int E, int k
                                cudaStream_t st);
 
 cudaError_t launch_quantize_weights(const uint16_t *w, int count, int N, int K, uint8_t *q, uint8_t *sf,
-                                    float *scale2, unsigned *amax_bits, cudaStream_t st);
+                                    float *scale2, unsigned *amax_bits, int ue8m0, cudaStream_t st);
 
 struct GemmArgs {
     // A: activations [rows_cap, K/2]; B: weights [E * Nrows, K/2]

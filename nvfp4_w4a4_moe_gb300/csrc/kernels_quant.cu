@@ -315,6 +315,44 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
     }
 }
 
+// ------------------------------------------------------------------ UE8M0 block scales
+// UE8M0 block scale of t >= 0 (t from the same fl(fl(g*amax)/6) as the E4M3
+// path): the byte of the smallest power of two at or above t, clamped to the
+// finite range 2^-127 .. 2^127 (bytes 0 .. 254).  Read off t's exponent field:
+// a zero mantissa means t is itself a power of two.
+__device__ __forceinline__ uint32_t ue8m0_round_up(float t)
+{
+    const uint32_t b = __float_as_uint(t);
+    const uint32_t e = b >> 23, m = b & 0x7FFFFFu;
+    if (e == 0) return m > 0x400000u ? 1u : 0u;  // subnormal t: 2^-127 covers up to 0x400000 * 2^-149
+    const uint32_t c = e + (m != 0u ? 1u : 0u);
+    return c > 254u ? 254u : c;                // also t = inf (e = 255)
+}
+
+// 1 / value(byte) = 2^(127 - byte), exact: a normal float for bytes 0 .. 253,
+// the subnormal 2^-127 for byte 254.
+__device__ __forceinline__ float ue8m0_reciprocal(uint32_t byte)
+{
+    return __uint_as_float(byte == 254u ? 0x00400000u : (254u - byte) << 23);
+}
+
+// quant_block16 with a UE8M0 block scale: the scale is t rounded up to a power
+// of two, so fl(fl(x*g) / s) is one exact product by 1/s, rounded once.
+__device__ __forceinline__ uint2 quant_block16_ue8m0(const f32x2 (&x)[8], float amax, float g, uint32_t &sf_byte)
+{
+    // fl(ga / 6) by the IEEE division: unlike the E4M3 path, the result matters
+    // down to FP32 subnormals here
+    const float t = __fdiv_rn(__fmul_rn(g, amax), 6.0f);
+    const uint32_t sb = ue8m0_round_up(t);
+    const float r = ue8m0_reciprocal(sb);
+    const f32x2 gg = pack_f32x2(g, g), rr = pack_f32x2(r, r);
+    f32x2 q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = mul_f32x2(mul_f32x2(x[i], gg), rr);
+    sf_byte = sb;
+    return make_uint2(e2m1_rn_sat8(q[0], q[1], q[2], q[3]), e2m1_rn_sat8(q[4], q[5], q[6], q[7]));
+}
+
 // ------------------------------------------------------------------ quantiser
 // [page, §NVFP4 runtime-order figure; MoE section: SFScale[expert_idx]]:
 // one warp per (token, 1024-element chunk), each lane two consecutive
@@ -344,8 +382,9 @@ __device__ __forceinline__ float amax16_bf16(const uint32_t *w)
 
 constexpr int kQuantThreads = 128;  // 5 CTAs (20 warps) per SM at <= 96 registers
 
-// SWZ: scales in the swizzled tensor-core layout (else linear [rows, H/16]).
-template <bool SWZ>
+// SWZ: scales in the swizzled tensor-core layout (else linear [rows, H/16]);
+// UE: UE8M0 block scales (else E4M3).
+template <bool SWZ, bool UE>
 __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantArgs a, DivTable tab_in)
 {
     __shared__ DivTable2 tab;
@@ -408,8 +447,8 @@ __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantAr
             const float g = __shfl_sync(0xffffffffu, my_g, j);
             if (active) {
                 uint32_t s0, s1;
-                const uint2 p0 = quant_block16(x0, amax0, g, &tab, s0);
-                const uint2 p1 = quant_block16(x1, amax1, g, &tab, s1);
+                const uint2 p0 = UE ? quant_block16_ue8m0(x0, amax0, g, s0) : quant_block16(x0, amax0, g, &tab, s0);
+                const uint2 p1 = UE ? quant_block16_ue8m0(x1, amax1, g, s1) : quant_block16(x1, amax1, g, &tab, s1);
                 q16[qo] = make_uint4(p0.x, p0.y, p1.x, p1.y);
                 *reinterpret_cast<uint16_t *>(a.sf + so) = (uint16_t)(s0 | (s1 << 8));
             }
@@ -523,6 +562,7 @@ __global__ void __launch_bounds__(256) weight_amax_kernel(const uint16_t *w, lon
 // the same block quantisation as activations.  A tensor of zeros has no
 // usable scale: it gets weight_scale_2 = 0 (rejected by validation) and zero
 // codes and scales.
+template <bool UE>
 __global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t *w, int N, int K, uint8_t *q,
                                                            uint8_t *sf, float *scale2,
                                                            const unsigned *amax_bits, DivTable tab_in)
@@ -554,7 +594,7 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const uint16_t *w, in
         }
         uint32_t sb = 0;
         uint2 pk = make_uint2(0u, 0u);
-        if (amax_t > 0.0f) pk = quant_block16(x, amax, g, &tab, sb);
+        if (amax_t > 0.0f) pk = UE ? quant_block16_ue8m0(x, amax, g, sb) : quant_block16(x, amax, g, &tab, sb);
         *reinterpret_cast<uint2 *>(qc + (size_t)n * (K >> 1) + (size_t)b * 8) = pk;
         sfc[(size_t)n * nb + b] = (uint8_t)sb;
     }
@@ -625,10 +665,17 @@ cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st)
         if (grid < 1) grid = 1;
         kernel<<<(int)grid, kQuantThreads, 0, st>>>(a, div_table());
     };
-    if (a.sf_swizzled)
-        launch(quant_experts_kernel<true>);
-    else
-        launch(quant_experts_kernel<false>);
+    if (a.sf_ue8m0) {
+        if (a.sf_swizzled)
+            launch(quant_experts_kernel<true, true>);
+        else
+            launch(quant_experts_kernel<false, true>);
+    } else {
+        if (a.sf_swizzled)
+            launch(quant_experts_kernel<true, false>);
+        else
+            launch(quant_experts_kernel<false, false>);
+    }
     return cudaGetLastError();
 }
 
@@ -647,7 +694,7 @@ cudaError_t launch_rmsnorm(const uint16_t *x, const float *out, int T, int H, fl
 }
 
 cudaError_t launch_quantize_weights(const uint16_t *w, int count, int N, int K, uint8_t *q, uint8_t *sf,
-                                    float *scale2, unsigned *amax_bits, cudaStream_t st)
+                                    float *scale2, unsigned *amax_bits, int ue8m0, cudaStream_t st)
 {
     cudaError_t err = cudaMemsetAsync(amax_bits, 0, sizeof(unsigned) * (size_t)count, st);
     if (err != cudaSuccess) return err;
@@ -657,7 +704,10 @@ cudaError_t launch_quantize_weights(const uint16_t *w, int count, int N, int K, 
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     dim3 g2(grid_for((long long)N * (K / 16), 256, 4), count);
-    weight_quant_kernel<<<g2, 256, 0, st>>>(w, N, K, q, sf, scale2, amax_bits, div_table());
+    if (ue8m0)
+        weight_quant_kernel<true><<<g2, 256, 0, st>>>(w, N, K, q, sf, scale2, amax_bits, div_table());
+    else
+        weight_quant_kernel<false><<<g2, 256, 0, st>>>(w, N, K, q, sf, scale2, amax_bits, div_table());
     return cudaGetLastError();
 }
 

@@ -359,7 +359,7 @@ def quantize_layer_weights(layer, experts=None) -> Weights:
     return W
 
 
-def quantize_experts(x_bf16, topk_ids, input_scale, E):
+def quantize_experts(x_bf16, topk_ids, input_scale, E, ue8m0: bool = False):
     """Activation quantisation for the routed rows, in permuted order
     (page "Gemma 4 NVFP4 MoE 空输出", MoE section: the per-expert global scale
     SFScale[expert_idx] chosen by the router's expert index).
@@ -369,7 +369,7 @@ def quantize_experts(x_bf16, topk_ids, input_scale, E):
     g = reciprocal_f32(input_scale)
     xf = (np.asarray(x_bf16, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
     row_e = np.repeat(np.arange(E, dtype=np.int32), np.diff(offsets))
-    q, sf = quant_rows(xf[perm // k], g[row_e])
+    q, sf = quant_rows(xf[perm // k], g[row_e], ue8m0=ue8m0)
     return q, sf, offsets, perm
 
 

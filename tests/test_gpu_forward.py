@@ -177,18 +177,21 @@ def test_host_entry_point_chunked_prefill(m, prefill):
     assert ei.value.status == m.ERR_INVALID_ARG
 
 
-def test_weight_quantiser_matches_oracle_weight_path(m):
-    """The device weight quantiser against the oracle's static weight path."""
+@pytest.mark.parametrize("ue8m0", [False, True], ids=["e4m3", "ue8m0"])
+def test_weight_quantiser_matches_oracle_weight_path(m, ue8m0):
+    """The device weight quantiser against the oracle's static weight path,
+    with E4M3 and with UE8M0 block scales."""
     r = np.random.default_rng(11)
     layer = S.decode(1)
     w = np.stack([layer.weight_bf16(0, "w13"), layer.weight_bf16(1, "w13")])
     small = S.normal_bf16(r, (3, 64, 256), 0.02)
     small[2] = 0  # a tensor of zeros
+    small[1, :8] = S.normal_bf16(r, (8, 256), 1e-30)  # blocks whose scales reach FP32 subnormals
     for t in (w, small):
-        q, sf, s2 = m.quantize_weights(dev_bf16(t))
+        q, sf, s2 = m.quantize_weights(dev_bf16(t), ue8m0=ue8m0)
         torch.cuda.synchronize()
         for c in range(t.shape[0]):
-            q_ref, sf_ref, s2_ref = oracle.quantize_weight(t[c])
+            q_ref, sf_ref, s2_ref = oracle.quantize_weight(t[c], ue8m0=ue8m0)
             assert host(s2)[c] == s2_ref
             assert np.array_equal(host(q)[c], q_ref) and np.array_equal(host(sf)[c], sf_ref)
 

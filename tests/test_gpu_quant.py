@@ -19,13 +19,14 @@ def m():
     return mod
 
 
-def run_and_compare(m, x_bits, ids, scale, E, layouts=(0, 1)):
+def run_and_compare(m, x_bits, ids, scale, E, layouts=(0, 1), ue8m0=False):
     T, H = x_bits.shape
     k = ids.shape[1]
     R = T * k
-    q_ref, sf_ref, off_ref, perm_ref = oracle.quantize_experts(x_bits, ids, scale, E)
+    q_ref, sf_ref, off_ref, perm_ref = oracle.quantize_experts(x_bits, ids, scale, E, ue8m0=ue8m0)
     for layout in layouts:
-        q, sf, off, perm = m.quantize_experts(dev_bf16(x_bits), dev(ids), dev(scale), E, sf_layout=layout)
+        q, sf, off, perm = m.quantize_experts(dev_bf16(x_bits), dev(ids), dev(scale), E,
+                                              sf_layout=layout | (m.SF_UE8M0 if ue8m0 else 0))
         torch.cuda.synchronize()
         assert np.array_equal(host(off), off_ref), "expert offsets"
         assert np.array_equal(host(perm), perm_ref), "permutation"
@@ -44,20 +45,27 @@ def run_and_compare(m, x_bits, ids, scale, E, layouts=(0, 1)):
         assert np.array_equal(sfh, sf_ref), "scale bytes"
 
 
-def test_tiny(m):
+FORMATS = pytest.mark.parametrize("ue8m0", [False, True], ids=["e4m3", "ue8m0"])
+
+
+@FORMATS
+def test_tiny(m, ue8m0):
     L = S.tiny()
-    run_and_compare(m, L.x, L.topk_ids, L.w13_input_scale, L.E)
+    run_and_compare(m, L.x, L.topk_ids, L.w13_input_scale, L.E, ue8m0=ue8m0)
 
 
-def test_quantiser_workload_full_size(m):
+@FORMATS
+def test_quantiser_workload_full_size(m, ue8m0):
     L = S.quantiser()
-    run_and_compare(m, L.x, L.topk_ids, L.w13_input_scale, L.E)
+    run_and_compare(m, L.x, L.topk_ids, L.w13_input_scale, L.E, ue8m0=ue8m0)
 
 
 @pytest.mark.parametrize("T", [1, 8, 32, 64])
 def test_decode_shapes(m, T):
     L = S.decode(T)
     run_and_compare(m, L.x, L.topk_ids, L.w13_input_scale, L.E)
+    if T == 64:
+        run_and_compare(m, L.x, L.topk_ids, L.w13_input_scale, L.E, ue8m0=True)
 
 
 def test_prefill_zipf_full_size(m):
@@ -65,7 +73,8 @@ def test_prefill_zipf_full_size(m):
     run_and_compare(m, L.x, L.topk_ids, L.w13_input_scale, L.E, layouts=(1,))
 
 
-def test_rounding_edges(m):
+@FORMATS
+def test_rounding_edges(m, ue8m0):
     """Blocks built so that x*g/s lands on every E2M1 tie, on both sides of
     it, on signed zeros, tiny negatives, huge values and saturation, and
     scales that land on E4M3 ties, underflow and saturate."""
@@ -96,7 +105,31 @@ def test_rounding_edges(m):
     # global scales: 1 (ties stay exact), a few odd values, huge and tiny
     scale = np.array([1.0, 1 / 3.0, 1e-3, 7.0, 2.0 ** -100, 2.0 ** 100], np.float32)
     ids = np.array([[0, 1, 2, 3, 4, 5]] * 4, np.int32)
-    run_and_compare(m, x, ids, scale, E)
+    run_and_compare(m, x, ids, scale, E, ue8m0=ue8m0)
+
+
+def test_ue8m0_scale_edges(m):
+    """UE8M0 scales at their decision points: amax = 6 * 2^k (t an exact power
+    of two) and one BF16 step either side, for k across the range, with global
+    scales that push t into FP32 subnormals and to the top of the range."""
+    def bf(v):
+        return S.bf16_bits_from_f32(np.asarray(v, np.float32))
+
+    r = np.random.default_rng(5)
+    rows = []
+    for k in range(-30, 31, 3):
+        top = int(bf([6.0 * 2.0 ** k])[0])  # exact in BF16
+        for bits in (top, top + 1, top - 1):  # and the BF16 neighbours either side
+            amax = S.f32_from_bf16_bits(np.array([bits], np.uint16))[0]
+            body = bf(r.uniform(-1, 1, 15).astype(np.float32) * amax)
+            rows.append(np.concatenate([np.array([bits], np.uint16), body]))
+    H = 64 * ((len(rows) * 16 + 63) // 64)
+    x = np.concatenate(rows).astype(np.uint16)
+    x = np.concatenate([x, bf(r.standard_normal(H - x.size))]).reshape(1, H)
+    x = np.repeat(x, 3, axis=0)
+    scale = np.array([1.0, 2.0 ** 100, 2.0 ** -100, 3.0, 2.0 ** 120], np.float32)
+    ids = np.array([[0, 1, 2, 3, 4]] * 3, np.int32)
+    run_and_compare(m, x, ids, scale, 5, ue8m0=True)
 
 
 def test_single_expert_and_ragged(m):
