@@ -69,6 +69,7 @@ def _load_locked(path):
         "orc_quant_block16": (ctypes.c_int, [P, F32, P]),
         "orc_quant_rows": (None, [P, I64, I64, P, P, P, ctypes.c_int]),
         "orc_ue8m0_value": (F64, [ctypes.c_int]),
+        "orc_silu_mul_bf16": (None, [P, I64, I64, P]),
         "orc_ue8m0_encode": (ctypes.c_int, [F32]),
         "orc_quant_block16_ue8m0": (ctypes.c_int, [P, F32, P]),
         "orc_quant_rows_ue8m0": (None, [P, I64, I64, P, P, P, ctypes.c_int]),
@@ -419,3 +420,71 @@ def moe_forward(x_bf16, topk_ids, topk_w, W: Weights, tokens=None):
     np.add.at(out, t_of, wts[:, None] * y2)
     return dict(out=out, rows=rows, a1q=a1q, sf1=sf1, h=h, a2q=a2q, sf2=sf2, y2=y2,
                 offsets=offsets, perm=perm, row_expert=row_e)
+
+
+# ---------------------------------------------------------------------------
+# W4A16: NVFP4 weights, BF16 activations
+# ---------------------------------------------------------------------------
+
+def dequant_weight(q: np.ndarray, sf: np.ndarray, scale2) -> np.ndarray:
+    """fp64 weights [N, K] = e2m1(code) * e4m3(block scale) * weight_scale_2
+    (page "Gemma 4 NVFP4 MoE 空输出", §NVFP4 two-level scale: FP4 data, FP8
+    block scale and FP32 global scale reconstruct the value); every product
+    is exact in fp64."""
+    codes = unpack_codes(q)
+    K = codes.shape[-1]
+    return e2m1_values(codes) * np.repeat(e4m3_values(sf), 16, axis=-1)[..., :K] * float(np.float32(scale2))
+
+
+def silu_mul_bf16(y1: np.ndarray) -> np.ndarray:
+    """h [M, I] BF16 bits = bf16(SiLU(gate) * up) from fp64 y1 [M, 2I], one rounding."""
+    y1 = np.ascontiguousarray(y1, dtype=np.float64)
+    M, I2 = y1.shape
+    h = np.empty((M, I2 // 2), dtype=np.uint16)
+    if M:
+        _L().orc_silu_mul_bf16(_p(y1), M, I2 // 2, _p(h))
+    return h
+
+
+def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def moe_forward_w4a16(x_bf16, topk_ids, topk_w, W: Weights, tokens=None):
+    """The W4A16 expert forward (page "Gemma 4 NVFP4 MoE 空输出", backend
+    figure: the MARLIN path executes the NVFP4 checkpoint as W4A16 and reads
+    no activation input_scale) for the tokens in `tokens` (all if None):
+    gate/up = x . W13^T and y2 = h . W2^T in fp64 over the dequantised
+    weights, h = bf16(SiLU(gate) * up), out[t] = sum_j w[t, j] y2.
+    Returns out [T, H] fp64 (rows outside `tokens` are 0), h (BF16 bits of the
+    computed permuted rows), rows, offsets, perm, row_expert."""
+    T, k = topk_ids.shape
+    E, H, I = W.E, W.H, W.I
+    for s in (W.w13_scale2, W.w2_scale2):
+        bad, first = validate_scales(s)
+        if bad:
+            raise ValueError(f"invalid weight scale slot {first}")
+    offsets, perm = route(topk_ids, E)
+    row_e = np.repeat(np.arange(E, dtype=np.int32), np.diff(offsets))
+    if tokens is None:
+        rows = np.arange(T * k, dtype=np.int64)
+    else:
+        keep = np.zeros(T, dtype=bool)
+        keep[np.asarray(tokens, dtype=np.int64)] = True
+        rows = np.nonzero(keep[perm // k])[0]
+    xf = bf16_bits_to_f64(x_bf16)
+    nr = len(rows)
+    h = np.zeros((nr, I), np.uint16)
+    y2 = np.zeros((nr, H), np.float64)
+    re = row_e[rows]
+    for e in np.unique(re):
+        sel = np.nonzero(re == e)[0]
+        X = xf[perm[rows[sel]] // k]
+        y1 = X @ dequant_weight(W.w13_q[e], W.w13_sf[e], W.w13_scale2[e]).T
+        h[sel] = silu_mul_bf16(y1)
+        y2[sel] = bf16_bits_to_f64(h[sel]) @ dequant_weight(W.w2_q[e], W.w2_sf[e], W.w2_scale2[e]).T
+    out = np.zeros((T, H), np.float64)
+    f = perm[rows]
+    wts = np.asarray(topk_w, dtype=np.float32).reshape(-1)[f].astype(np.float64)
+    np.add.at(out, f // k, wts[:, None] * y2)
+    return dict(out=out, rows=rows, h=h, y2=y2, offsets=offsets, perm=perm, row_expert=row_e)

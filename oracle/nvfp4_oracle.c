@@ -581,6 +581,22 @@ static uint16_t bf16_nearest(double d)
     return (uint16_t)(u >> 16);
 }
 
+/* W4A16 activation step [page, backend figure: the MARLIN path executes the
+ * checkpoint as W4A16, so the activations stay 16-bit].  Reading: the
+ * intermediate h = SiLU(gate) * up is formed from the fp64 gate/up of the
+ * first GEMM and rounded once to BF16, the second GEMM's input.  y1 is
+ * [M, 2I] (gate columns then up columns); h [M, I] BF16 bits. */
+void orc_silu_mul_bf16(const double *y1, int64_t M, int64_t I, uint16_t *h)
+{
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t i = 0; i < I; ++i) {
+            double gate = y1[m * 2 * I + i];
+            double up = y1[m * 2 * I + I + i];
+            double silu = gate / (1.0 + exp(-gate));
+            h[m * I + i] = bf16_nearest(silu * up);
+        }
+}
+
 /* Between stacked layers (not on the page; the stacked-layer workload adds it):
  *   r = x + out,  x' = bf16( r / sqrt(mean(r^2) + eps) ),  gamma = 1,
  * in fp64.  x is BF16 bits [T, H], out is FP32 [T, H]. */

@@ -310,6 +310,83 @@ def pin_ue8m0(orc):
         assert sb2 == sb and np.array_equal(codes2, codes ^ 8)
 
 
+def _bf16_round_fraction(v: Fraction) -> Fraction:
+    """Nearest BF16 value (8 significant bits, ties to even), by exact
+    rational arithmetic."""
+    if v == 0:
+        return Fraction(0)
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    step = Fraction(2) ** (e - 7)          # spacing of 8-bit significands at this binade
+    q, rem = divmod(a, step)
+    if rem * 2 > step or (rem * 2 == step and q % 2 == 1):
+        q += 1
+    return (q * step) if v > 0 else -(q * step)
+
+
+def pin_w4a16(orc):
+    """The W4A16 layer on a tiny case against exact rational arithmetic: the
+    weights decoded from the page's E2M1 table (golden file) and an E4M3
+    formula written here, times weight_scale_2; both GEMMs and the combine as
+    exact sums; h = SiLU(gate) * up in double, rounded to BF16 by a rational
+    round-to-nearest-even.  Catches a dropped scale, swapped gate/up,
+    transposed operands, an h that skips its BF16 rounding and wrong weights
+    in the combine."""
+    r = _rng(41)
+    E, H, I, T, k = 2, 32, 32, 3, 2
+
+    class W:
+        pass
+
+    W.E, W.H, W.I = E, H, I
+    W.w13_q = r.integers(0, 256, (E, 2 * I, H // 2)).astype(np.uint8)
+    W.w13_sf = r.integers(0x28, 0x48, (E, 2 * I, H // 16)).astype(np.uint8)
+    W.w13_scale2 = np.array([0.75, 1.0 / 3.0], np.float32)
+    W.w2_q = r.integers(0, 256, (E, H, I // 2)).astype(np.uint8)
+    W.w2_sf = r.integers(0x28, 0x48, (E, H, I // 16)).astype(np.uint8)
+    W.w2_scale2 = np.array([0.5, 1.25], np.float32)
+    x = (r.standard_normal((T, H)) * 0.25).astype(np.float32)
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)  # truncated to BF16 bits: any BF16 input will do
+    ids = np.array([[0, 1], [1, 0], [0, 1]], np.int32)
+    tw = np.array([[0.75, 0.25], [0.5, 0.5], [1.0, 0.0]], np.float32)
+    got = orc.moe_forward_w4a16(xb, ids, tw, W)
+
+    def e4m3(b):
+        ex, m = (b >> 3) & 15, b & 7
+        return Fraction(m, 512) if ex == 0 else Fraction(8 + m, 8) * Fraction(2) ** (ex - 7)
+
+    def weights(q, sf, s2):
+        N, K = q.shape[0], q.shape[1] * 2
+        out = [[Fraction(0)] * K for _ in range(N)]
+        for n in range(N):
+            for kk in range(K):
+                byte = int(q[n, kk // 2])
+                code = byte & 15 if kk % 2 == 0 else byte >> 4
+                out[n][kk] = Fraction(E2M1[code]) * e4m3(int(sf[n, kk // 16])) * Fraction(float(s2))
+        return out
+
+    w13 = [weights(W.w13_q[e], W.w13_sf[e], W.w13_scale2[e]) for e in range(E)]
+    w2 = [weights(W.w2_q[e], W.w2_sf[e], W.w2_scale2[e]) for e in range(E)]
+    xf = [[Fraction(float(np.uint32(int(b) << 16).view(np.float32))) for b in row] for row in xb]
+    for t in range(T):
+        acc = [Fraction(0)] * H
+        for j in range(k):
+            e, wt = int(ids[t, j]), Fraction(float(tw[t, j]))
+            y1 = [sum(xf[t][kk] * w13[e][n][kk] for kk in range(H)) for n in range(2 * I)]
+            h = []
+            for i in range(I):
+                g, u = float(y1[i]), float(y1[I + i])
+                h.append(_bf16_round_fraction(Fraction(g / (1.0 + math.exp(-g)) * u)))
+            for n in range(H):
+                acc[n] += wt * sum(h[i] * w2[e][n][i] for i in range(I))
+        want = np.array([float(a) for a in acc])
+        assert np.allclose(got["out"][t], want, rtol=1e-12, atol=1e-300), (t, np.abs(got["out"][t] - want).max())
+
+
 def pin_router(orc):
     """Router pins: k = E is SciPy's softmax in the stable descending order of the
     logits; for k < E the renormalised weights are the softmax of the selected
@@ -554,5 +631,5 @@ ALL_PINS = [
     pin_e2m1_table, pin_e2m1_ties, pin_e2m1_boundaries, pin_e4m3_roundtrip, pin_e4m3_frexp,
     pin_e4m3_torch, pin_block_worked, pin_identity_2688, pin_block_invariances,
     pin_route_bruteforce, pin_gemm_fraction, pin_gemm_fp64, pin_silu_mul, pin_combine_special,
-    pin_forward_stepwise, pin_validate, pin_rmsnorm, pin_router, pin_ue8m0,
+    pin_forward_stepwise, pin_validate, pin_rmsnorm, pin_router, pin_ue8m0, pin_w4a16,
 ]

@@ -37,6 +37,8 @@ MUTANTS = [
     ("ue8m0_round_to_nearest", "if (ldexp(1.0, b - 127) >= a) return b;", "if (1.5 * ldexp(1.0, b - 127) >= a) return b;", 0),
     ("ue8m0_bias_126", "return ldexp(1.0, byte - 127);", "return ldexp(1.0, byte - 126);", 0),
     ("ue8m0_no_global_scale", "float y = x[i] * g;", "float y = x[i];", 1),
+    ("w4a16_silu_sign", "double silu = gate / (1.0 + exp(-gate));", "double silu = gate / (1.0 + exp(gate));", 1),
+    ("w4a16_sum_not_product", "bf16_nearest(silu * up)", "bf16_nearest(silu + up)", 0),
     ("router_not_renormalised", "(float)(p[ids[t * k + j]] / zk)", "(float)(p[ids[t * k + j]])", 0),
 ]
 
