@@ -317,6 +317,39 @@ int nvfp4_residual_rmsnorm(const uint16_t *x, const float *out, int T, int H, fl
                            uint16_t *x_next, nvfp4_stream_t stream);
 
 /*
+ * W4A16 expert forward -- the same layer with the weights kept NVFP4 and the
+ * activations BF16 [page "Gemma 4 NVFP4 MoE 空输出", backend figure: the
+ * MARLIN path executes the NVFP4 checkpoint as W4A16 and consumes no
+ * activation input_scale].  Per routed row (token t, expert e):
+ *   gate, up = x[t] . W13[e]^T,  W = e2m1(code) * e4m3(block scale) * weight_scale_2
+ *   h        = bf16( SiLU(gate) * up )      (the activations stay 16-bit)
+ *   out[t]  += topk_weights[t, j] * (h . W2[e]^T)
+ * BF16 x BF16 tensor-core products with FP32 accumulation; out [T, H] FP32.
+ * w13_input_scale / w2_input_scale are not read (they may be null); the
+ * weight_scale_2 slots are validated as in nvfp4_moe_forward.
+ *
+ * nvfp4_w4a16_prepared_size / nvfp4_prepare_weights_w4a16: the weights' block
+ * scales rearranged for this path ([E * N / 64][K / 64][64 rows][4 bytes] per
+ * projection); device memory, 256-byte aligned, owned by the caller, valid
+ * while the weights are unchanged.  Asynchronous on `stream`.
+ * nvfp4_moe_w4a16_workspace_size: device workspace of the forward (256-byte
+ * aligned).  nvfp4_moe_forward_w4a16: arguments, flags, synchronisation and
+ * errors as nvfp4_moe_forward (the same shape limits apply).
+ * nvfp4_moe_w4a16_intermediates_of: pointers, inside a workspace, to the
+ * gathered BF16 rows [rows_cap, H] and to h [rows_cap, I] (padded permuted
+ * row order, as nvfp4_moe_intermediates_of describes).
+ */
+size_t nvfp4_w4a16_prepared_size(int E, int H, int I);
+int nvfp4_prepare_weights_w4a16(const nvfp4_moe_weights *w, void *prepared, size_t prepared_bytes,
+                                nvfp4_stream_t stream);
+size_t nvfp4_moe_w4a16_workspace_size(int T, int H, int I, int E, int k);
+int nvfp4_moe_forward_w4a16(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x, int T,
+                            const int32_t *topk_ids, const float *topk_weights, int k, float *out, void *ws,
+                            size_t ws_bytes, unsigned flags, nvfp4_stream_t stream);
+int nvfp4_moe_w4a16_intermediates_of(void *ws, int T, int H, int I, int E, int k, uint16_t **a16,
+                                     uint16_t **h16);
+
+/*
  * nvfp4_router_topk -- the MoE router [page "Gemma 4 NVFP4 MoE 空输出",
  * §矩阵融合 "MoE FFN": the routing result picks each token's experts and the
  * expert outputs are summed with the routing weights; page

@@ -82,6 +82,11 @@ def load():
             "nvfp4_moe_intermediates_of": (I, [P, I, I, I, I, I, P]),
             "nvfp4_residual_rmsnorm": (I, [P, P, I, I, ctypes.c_float, P, P]),
             "nvfp4_router_topk": (I, [P, I, I, I, I, P, P, P]),
+            "nvfp4_w4a16_prepared_size": (SZ, [I, I, I]),
+            "nvfp4_prepare_weights_w4a16": (I, [P, P, SZ, P]),
+            "nvfp4_moe_w4a16_workspace_size": (SZ, [I, I, I, I, I]),
+            "nvfp4_moe_forward_w4a16": (I, [P, P, P, I, P, P, I, P, P, SZ, U, P]),
+            "nvfp4_moe_w4a16_intermediates_of": (I, [P, I, I, I, I, I, P, P]),
             "nvfp4_quantize_weights_workspace_size": (SZ, [I]),
             "nvfp4_quantize_weights": (I, [P, I, I, I, P, P, P, P, SZ, P]),
             "nvfp4_quantize_weights_format": (I, [P, I, I, I, I, P, P, P, P, SZ, P]),
@@ -194,6 +199,7 @@ class MoEWeights:
         self.w2_q, self.w2_sf, self.w2_scale2, self.w2_input_scale = w2_q, w2_sf, w2_scale2, w2_input_scale
         self.w13_input_written, self.w2_input_written = w13_input_written, w2_input_written
         self.prepared = None
+        self.prepared_w4a16 = None
 
     def cstruct(self) -> _Weights:
         return _Weights(self.E, self.H, self.I, _ptr(self.w13_q), _ptr(self.w13_sf), _ptr(self.w13_scale2),
@@ -240,6 +246,52 @@ def moe_forward(w: MoEWeights, x: torch.Tensor, topk_ids: torch.Tensor, topk_wei
     _check(load().nvfp4_moe_forward(ctypes.byref(cw), _ptr(w.prepared), _ptr(x), T, _ptr(topk_ids),
                                     _ptr(topk_weights), k, _ptr(out), _ptr(ws), ws.numel(), flags, _stream(stream)))
     return out, ws
+
+
+def prepare_weights_w4a16(w: MoEWeights, stream=None) -> torch.Tensor:
+    """The block scales rearranged for the W4A16 path (kept on w)."""
+    n = int(load().nvfp4_w4a16_prepared_size(w.E, w.H, w.I))
+    prep = torch.empty(max(n, 1), dtype=torch.uint8, device=w.w13_q.device)
+    cw = w.cstruct()
+    _check(load().nvfp4_prepare_weights_w4a16(ctypes.byref(cw), _ptr(prep), n, _stream(stream)))
+    w.prepared_w4a16 = prep
+    return prep
+
+
+def moe_w4a16_workspace_size(T: int, H: int, I: int, E: int, k: int) -> int:
+    return int(load().nvfp4_moe_w4a16_workspace_size(T, H, I, E, k))
+
+
+def moe_forward_w4a16(w: MoEWeights, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                      out: torch.Tensor | None = None, ws: torch.Tensor | None = None, flags: int = 0, stream=None):
+    """out [T, H] f32 = the expert path with NVFP4 weights and BF16 activations."""
+    T, H = x.shape
+    k = topk_ids.shape[1]
+    if w.prepared_w4a16 is None:
+        prepare_weights_w4a16(w, stream)
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = _empty_ws(moe_w4a16_workspace_size(T, H, w.I, w.E, k), x.device)
+    cw = w.cstruct()
+    _check(load().nvfp4_moe_forward_w4a16(ctypes.byref(cw), _ptr(w.prepared_w4a16), _ptr(x), T, _ptr(topk_ids),
+                                          _ptr(topk_weights), k, _ptr(out), _ptr(ws), ws.numel(), flags,
+                                          _stream(stream)))
+    return out, ws
+
+
+def w4a16_intermediates_of(ws: torch.Tensor, T: int, H: int, I: int, E: int, k: int) -> dict:
+    """Views of the W4A16 workspace: gathered BF16 rows and h (BF16 bits as int16)."""
+    a16, h16 = ctypes.c_void_p(), ctypes.c_void_p()
+    _check(load().nvfp4_moe_w4a16_intermediates_of(_ptr(ws), T, H, I, E, k, ctypes.byref(a16), ctypes.byref(h16)))
+    rc = intermediates_rows_cap(T, E, k)
+    base = ws.data_ptr()
+
+    def view(addr, n, shape):
+        off = addr - base
+        return ws[off:off + 2 * n].view(torch.int16).view(shape)
+
+    return dict(rows_cap=rc, a16=view(a16.value, rc * H, (rc, H)), h16=view(h16.value, rc * I, (rc, I)))
 
 
 STAGES = ("validate", "route", "quant_a1", "gemm_w13", "gemm_w2")

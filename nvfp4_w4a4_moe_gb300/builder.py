@@ -17,8 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libnvfp4moe.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "kernels_quant.cu", "kernels_gemm.cu", "kernels_router.cu", "noalloc.cu"]
-HEADERS = ["common.cuh", "internal.h"]
+SOURCES = ["api.cu", "kernels_quant.cu", "kernels_gemm.cu", "kernels_w4a16.cu", "kernels_router.cu", "noalloc.cu"]
+HEADERS = ["common.cuh", "internal.h", "tc_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

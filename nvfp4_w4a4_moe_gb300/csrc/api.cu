@@ -753,6 +753,185 @@ int nvfp4_moe_intermediates_of(void *ws, int T, int H, int I, int E, int k, nvfp
     return NVFP4_OK;
 }
 
+// ---------------------------------------------------------------- W4A16
+static int check_weights_w16(const nvfp4_moe_weights *w)
+{
+    if (!w) return fail(NVFP4_ERR_INVALID_ARG, "weights struct is null");
+    if (!w->w13_q || !w->w13_sf || !w->w13_scale2 || !w->w2_q || !w->w2_sf || !w->w2_scale2)
+        return fail(NVFP4_ERR_INVALID_ARG, "a weight or weight-scale pointer is null");
+    if (!aligned(w->w13_q, 16) || !aligned(w->w2_q, 16) || !aligned(w->w13_sf, 4) || !aligned(w->w2_sf, 4))
+        return fail(NVFP4_ERR_INVALID_ARG, "weight codes must be 16-byte aligned, scales 4-byte aligned");
+    return NVFP4_OK;
+}
+
+static size_t w16_w13_sf_bytes(int E, int H, int I) { return (size_t)E * 2 * I * (H / 16); }
+
+size_t nvfp4_w4a16_prepared_size(int E, int H, int I)
+{
+    if (E < 1 || H <= 0 || I <= 0 || H % 64 || I % 64) return 0;
+    return up256(w16_w13_sf_bytes(E, H, I)) + up256((size_t)E * H * (I / 16));
+}
+
+int nvfp4_prepare_weights_w4a16(const nvfp4_moe_weights *w, void *prepared, size_t prepared_bytes,
+                                nvfp4_stream_t stream)
+{
+    int rc = check_weights_w16(w);
+    if (rc) return rc;
+    rc = check_layer_shape(w->E, w->H, w->I, 1);
+    if (rc) return rc;
+    if (!prepared || !aligned(prepared, 256)) return fail(NVFP4_ERR_INVALID_ARG, "prepared: null or not 256-byte aligned");
+    if (prepared_bytes < nvfp4_w4a16_prepared_size(w->E, w->H, w->I))
+        return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "prepared buffer too small");
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *base = static_cast<uint8_t *>(prepared);
+    NV_CUDA(launch_prep_sf_w16(w->w13_sf, base, w->E, 2 * w->I, w->H, st), "launching the w13 scale layout");
+    NV_CUDA(launch_prep_sf_w16(w->w2_sf, base + up256(w16_w13_sf_bytes(w->E, w->H, w->I)), w->E, w->H, w->I, st),
+            "launching the w2 scale layout");
+    return NVFP4_OK;
+}
+
+// W4A16 workspace: the routing regions of the W4A4 layout, then A (gathered
+// BF16 rows, [rows_cap, H]) and h ([rows_cap, I] BF16) in place of the W4A4
+// activation buffers.
+struct W16Layout {
+    size_t a16, h16, end;
+};
+static W16Layout make_w16_layout(const WsLayout &L, int H, int I)
+{
+    W16Layout w;
+    w.a16 = L.a1q;
+    w.h16 = w.a16 + up256((size_t)L.rows_cap * H * 2);
+    w.end = w.h16 + up256((size_t)L.rows_cap * I * 2);
+    return w;
+}
+
+size_t nvfp4_moe_w4a16_workspace_size(int T, int H, int I, int E, int k)
+{
+    if (T < 0 || H <= 0 || I <= 0 || E < 1 || k < 1) return 0;
+    const WsLayout L = make_layout(T, H, I, E, k);
+    return make_w16_layout(L, H, I).end;
+}
+
+int nvfp4_moe_forward_w4a16(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x, int T,
+                            const int32_t *topk_ids, const float *topk_weights, int k, float *out, void *ws,
+                            size_t ws_bytes, unsigned flags, nvfp4_stream_t stream)
+{
+    int rc = check_weights_w16(w);
+    if (rc) return rc;
+    rc = check_layer_shape(w->E, w->H, w->I, k);
+    if (rc) return rc;
+    const int E = w->E, H = w->H, I = w->I;
+    if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "T=%d < 0", T);
+    if ((long long)T * k >= (1ll << 31) / 2) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "T*k too large");
+    if (!prepared || !ws || (T > 0 && (!x || !topk_ids || !topk_weights || !out)))
+        return fail(NVFP4_ERR_INVALID_ARG, "w4a16 forward: null pointer");
+    if (!aligned(ws, 256) || !aligned(prepared, 256) || (T > 0 && (!aligned(x, 16) || !aligned(out, 16))))
+        return fail(NVFP4_ERR_INVALID_ARG, "w4a16 forward: misaligned pointer (x, out 16 B; ws, prepared 256 B)");
+    const WsLayout L = make_layout(T, H, I, E, k);
+    const W16Layout W = make_w16_layout(L, H, I);
+    if (ws_bytes < W.end) return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu", ws_bytes, W.end);
+    if (T == 0) return NVFP4_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    DevHeader *hdr = reinterpret_cast<DevHeader *>(base + L.hdr);
+
+    // only the weight_scale_2 slots are consumed (no activation scale)
+    ValidateArgs va;
+    std::memset(&va, 0, sizeof(va));
+    va.s[0] = w->w13_scale2;
+    va.s[1] = w->w2_scale2;
+    va.E = E;
+    va.narrays = 2;
+    va.hdr = hdr;
+    NV_CUDA(launch_validate(va, st), "launching the scale check");
+    if (!(flags & NVFP4_SCALES_PREVALIDATED)) {
+        DevHeader h;
+        rc = read_header(hdr, st, &h);
+        if (rc) return rc;
+        if (h.status) return header_status(h, nullptr);
+    }
+
+    RouteArgs ra;
+    std::memset(&ra, 0, sizeof(ra));
+    ra.ids = topk_ids;
+    ra.R = T * k;
+    ra.k = k;
+    ra.E = E;
+    ra.nchunks = L.nchunks;
+    ra.chunk_hist = reinterpret_cast<int *>(base + L.chunk_hist);
+    ra.counts = reinterpret_cast<int *>(base + L.counts);
+    ra.offsets = reinterpret_cast<int *>(base + L.offsets);
+    ra.pad_off = reinterpret_cast<int *>(base + L.pad_off);
+    ra.tile_expert = reinterpret_cast<int *>(base + L.tile_expert);
+    ra.row_of = reinterpret_cast<int *>(base + L.row_of);
+    ra.perm = reinterpret_cast<int *>(base + L.perm);
+    ra.row_src = reinterpret_cast<int *>(base + L.row_src);
+    ra.padded = 1;
+    ra.hdr = hdr;
+    NV_CUDA(launch_route(ra, st), "launching the token reorder");
+
+    uint16_t *a16 = reinterpret_cast<uint16_t *>(base + W.a16);
+    uint16_t *h16 = reinterpret_cast<uint16_t *>(base + W.h16);
+    NV_CUDA(launch_gather_rows(x, H, k, ra.row_src, hdr, L.rows_cap, a16, out, (long long)T * H, st),
+            "launching the row gather");
+
+    const uint8_t *pw = static_cast<const uint8_t *>(prepared);
+    W16Args wa;
+    std::memset(&wa, 0, sizeof(wa));
+    wa.a = a16;
+    wa.b_q = w->w13_q;
+    wa.b_sfp = pw;
+    wa.rows_cap = L.rows_cap;
+    wa.K = H;
+    wa.N = 2 * I;
+    wa.E = E;
+    wa.gate_up_I = I;
+    wa.tile_expert = ra.tile_expert;
+    wa.pad_off = ra.pad_off;
+    wa.counts = ra.counts;
+    wa.row_src = ra.row_src;
+    wa.scale2 = w->w13_scale2;
+    wa.h = h16;
+    wa.I = I;
+    wa.k = k;
+    wa.H = H;
+    wa.hdr = hdr;
+    wa.mtiles_cap = L.mtiles_cap;
+    NV_CUDA(launch_w16_w13(wa, st), "launching the W4A16 w13 GEMM");
+
+    W16Args wb = wa;
+    wb.a = h16;
+    wb.b_q = w->w2_q;
+    wb.b_sfp = pw + up256(w16_w13_sf_bytes(E, H, I));
+    wb.K = I;
+    wb.N = H;
+    wb.gate_up_I = 0;
+    wb.scale2 = w->w2_scale2;
+    wb.h = nullptr;
+    wb.topk_w = topk_weights;
+    wb.out = out;
+    NV_CUDA(launch_w16_w2(wb, st), "launching the W4A16 w2 GEMM");
+
+    if (flags & NVFP4_SYNC_CHECK) {
+        DevHeader h;
+        rc = read_header(hdr, st, &h);
+        if (rc) return rc;
+        return header_status(h, nullptr);
+    }
+    return NVFP4_OK;
+}
+
+int nvfp4_moe_w4a16_intermediates_of(void *ws, int T, int H, int I, int E, int k, uint16_t **a16, uint16_t **h16)
+{
+    if (!ws || T < 0 || H <= 0 || I <= 0 || E < 1 || k < 1 || !a16 || !h16)
+        return fail(NVFP4_ERR_INVALID_ARG, "w4a16 intermediates: bad arguments");
+    const WsLayout L = make_layout(T, H, I, E, k);
+    const W16Layout W = make_w16_layout(L, H, I);
+    *a16 = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + W.a16);
+    *h16 = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + W.h16);
+    return NVFP4_OK;
+}
+
 int nvfp4_residual_rmsnorm(const uint16_t *x, const float *out, int T, int H, float eps, uint16_t *x_next,
                            nvfp4_stream_t stream)
 {

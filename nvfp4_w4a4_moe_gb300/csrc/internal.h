@@ -111,6 +111,36 @@ struct GemmArgs {
 cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st);
 cudaError_t launch_gemm_w2(const GemmArgs &a, cudaStream_t st);
 
+// W4A16 expert GEMMs: BF16 activation rows against NVFP4 weights.
+struct W16Args {
+    const uint16_t *a;       // A: BF16 rows [rows_cap, K]
+    const uint8_t *b_q;      // B: FP4 codes [E * N, K/2]
+    const uint8_t *b_sfp;    // B scales, prepared: [E][N/64][K/64][64 rows][4 bytes]
+    int rows_cap, K, N, E;
+    int gate_up_I;           // w13: I (B tile = up to 128 gate rows + the matching up rows); w2: 0
+    const int *tile_expert, *pad_off, *counts, *row_src;
+    const float *scale2;     // weight_scale_2 per expert: the epilogue's multiplier
+    uint16_t *h;             // w13: h [rows_cap, I] BF16
+    int I;
+    const float *topk_w;     // w2: combine
+    int k, H;
+    float *out;
+    DevHeader *hdr;
+    int mtiles_cap;
+};
+cudaError_t launch_w16_w13(const W16Args &a, cudaStream_t st);
+cudaError_t launch_w16_w2(const W16Args &a, cudaStream_t st);
+// A rows of the W4A16 path: padded permuted row p holds x[row_src[p] / k] (zero on padding rows);
+// also clears out [out_floats] (a multiple of 4) when the device status is clean.
+cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int *row_src, const DevHeader *hdr,
+                               int rows_cap, uint16_t *a, float *out, long long out_floats, cudaStream_t st);
+// W4A16 weight-scale layout: canonical [E, N, K/16] -> [E][N/64][K/64][64][4].
+cudaError_t launch_prep_sf_w16(const uint8_t *sf, uint8_t *out, int E, int N, int K, cudaStream_t st);
+
+// 2-D byte tensor map [rows, row_bytes], box (box_bytes x box_rows), 128-byte swizzle or none.
+bool make_tensor_map_2d(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes,
+                        uint32_t box_rows, bool swizzle128);
+
 // ---------------------------------------------------------------- helpers
 const DivTable &div_table();
 int sm_count();

@@ -1,0 +1,568 @@
+// W4A16 expert GEMMs: NVFP4 weights (E2M1 codes, E4M3 block scales, FP32
+// weight_scale_2) against BF16 activations, on the tcgen05 tensor cores.
+//
+// Page cited: "Gemma 4 NVFP4 MoE 空输出" (taking-lying-flat.github.io):
+//   backend overview: the MARLIN path runs NVFP4 checkpoints as W4A16, the
+//   weights stay 4-bit and the activations 16-bit, and it consumes no
+//   activation input_scale; §矩阵融合 "Gated FFN" / "MoE FFN": the same
+//   gate/up GEMM, act(gate) * up, down GEMM and weighted combine as the W4A4
+//   path.
+//
+// The weights stay FP4 in memory.  Each stage, converter warps expand the
+// stage's FP4 weight tile into a BF16 tile in shared memory, in the 128-byte
+// swizzled K-major layout the MMA reads: code value times E4M3 block scale
+// has at most 6 significant bits, so the product is exact in BF16, and the
+// FP32 weight_scale_2 is applied in the epilogue.  The MMA is
+// tcgen05.mma.kind::f16 with BF16 A and B and FP32 accumulators; with no
+// block scales in TMEM, two accumulators fit in both kernels.
+//
+// Kernel shape (one persistent CTA per SM):
+//   warp 0     TMA producer: per 64-K stage the A tile (128 BF16 rows x 128 B,
+//              128-byte swizzle), the FP4 codes of the B tile (64-row boxes of
+//              32 B) and its scales (256-byte bulk copies of the prepared
+//              layout).
+//   warp 1     TMEM owner and MMA issuer: 4 x kind::f16 K16 per stage, M128 x
+//              N256 (w13: 128 gate + 128 up rows) or N128 (w2).
+//   warps 2-5  converters: FP4 codes x block scale -> BF16 tile, then a proxy
+//              fence and an arrive on the stage's "ready" barrier.
+//   the rest   epilogue: w13 forms h = SiLU(s2 gate) (s2 up) and stores it as
+//              BF16 (the second GEMM's A operand); w2 scatters
+//              w * s2 * y2 into the token-order FP32 output with vector
+//              reductions, as in the W4A4 path.
+// Every wait is bounded (%globaltimer); on expiry the kernel records the
+// error in the workspace header, drains what it has in flight and exits.
+#include <climits>
+
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace nvfp4 {
+namespace {
+
+using namespace tc;
+
+constexpr int WBM = 128, WBK = 64;         // K per stage: one 128-byte row of BF16
+constexpr int W_A_BYTES = WBM * WBK * 2;   // 16 KB
+constexpr int W_TMEM_COLS = 512;
+constexpr int kConvWarps = 4;
+constexpr int kXposeLd = 33;
+constexpr uint64_t kWLimitNs = 1000000000ull;
+constexpr uint64_t kWDrainNs = 200000000ull;
+
+template <int EPI>
+struct WPlan {
+    static constexpr int BN = EPI == 0 ? 256 : 128;
+    static constexpr int STAGES = EPI == 0 ? 3 : 4;
+    static constexpr int NUM_EPI_WARPS = EPI == 0 ? 8 : 16;
+    static constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
+    static constexpr int EPI_GROUPS = EPI == 0 ? 1 : 2;
+    static constexpr int CONV_WARP0 = 2;
+    static constexpr int EPI_WARP0 = CONV_WARP0 + kConvWarps;
+    static constexpr int NUM_THREADS = 32 * EPI_WARP0 + EPI_THREADS;
+    static constexpr int ACC_BUFS = 2;
+    static constexpr int B16_BYTES = BN * WBK * 2;  // BF16 B tile: BN rows x 128 B
+    static constexpr int BQ_BYTES = BN * WBK / 2;   // FP4 codes: BN rows x 32 B
+    static constexpr int SQ_BYTES = BN * 4;         // E4M3 scales: BN rows x 4
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B16 = OFF_A + STAGES * W_A_BYTES;
+    static constexpr int OFF_BQ = OFF_B16 + STAGES * B16_BYTES;
+    static constexpr int OFF_SQ = OFF_BQ + STAGES * BQ_BYTES;
+    static constexpr int OFF_LUT = OFF_SQ + STAGES * SQ_BYTES;  // 256 x u32 codes, 128 x u32 scales
+    static constexpr int OFF_BAR = OFF_LUT + 384 * 4;
+    static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_BUFS + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_XPOSE = (OFF_MISC + 16 + 15) & ~15;
+    static constexpr int XPOSE_BYTES = EPI == 1 ? NUM_EPI_WARPS * 32 * kXposeLd * 4 : 0;
+    static constexpr int SMEM_BYTES = OFF_XPOSE + XPOSE_BYTES + 1024;  // + alignment slack
+    static_assert(ACC_BUFS * BN <= W_TMEM_COLS, "accumulators exceed TMEM");
+    static_assert(W_A_BYTES % 1024 == 0 && B16_BYTES % 1024 == 0, "swizzled tiles keep 1024-byte alignment");
+    static_assert(SMEM_BYTES <= 232448, "shared memory plan exceeds the opt-in limit");
+};
+
+// Instruction descriptor, kind::f16: FP32 accumulator (bits 4-5 = 1), BF16 A
+// and B (code 1 at bits 7-9 and 10-12), K-major both, N>>3 at 17-22, M>>4 at
+// 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16(int n)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(WBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Two BF16 products, each exact here (at most 6 significant bits).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Two FP32 values rounded to nearest-even BF16, packed (first in the low half).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float silu_w16(float z) { return __fdividef(z, 1.0f + __expf(fminf(-z, 80.0f))); }
+
+// Tile geometry (as in the W4A4 kernels).  w13: tile t covers h columns
+// [128 nt, 128 nt + hc), hc = min(128, I - 128 nt), B rows = hc gate rows then
+// hc up rows, m-tile major.  w2: output columns [128 nt, 128 nt + 128),
+// output-column-block major.
+struct WTile {
+    int mt, nt, e, hc;
+};
+template <int EPI>
+__device__ __forceinline__ WTile w_tile(const W16Args &p, int tile, int NT, int MT)
+{
+    WTile t;
+    if (EPI == 0) {
+        t.mt = tile / NT;
+        t.nt = tile - t.mt * NT;
+        t.hc = min(128, p.gate_up_I - 128 * t.nt);
+    } else {
+        t.nt = tile / MT;
+        t.mt = tile - t.nt * MT;
+        t.hc = 128;
+    }
+    t.e = p.tile_expert[t.mt];
+    return t;
+}
+
+// BF16 bits of an E2M1 code (the page's 16-entry table: magnitudes 0, 0.5,
+// 1, 1.5, 2, 3, 4, 6; codes 8..15 negative, 8 is -0).
+__device__ __forceinline__ uint32_t e2m1_bf16(uint32_t code)
+{
+    const uint32_t mag[8] = {0x0000u, 0x3F00u, 0x3F80u, 0x3FC0u, 0x4000u, 0x4040u, 0x4080u, 0x40C0u};
+    return mag[code & 7u] | ((code & 8u) << 12);
+}
+// BF16 bits of a non-negative E4M3 scale byte (exact: at most 4 significant bits).
+__device__ __forceinline__ uint32_t e4m3_bf16(uint32_t b)
+{
+    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+    if (e == 15u && m == 7u) return 0x7FC0u;  // NaN
+    const float v = e == 0u ? (float)m * 0x1p-9f : ldexpf((float)(8u + m), (int)e - 10);
+    return __float_as_uint(v) >> 16;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
+    w16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const W16Args p)
+{
+    using P = WPlan<EPI>;
+    constexpr int STAGES = P::STAGES, ACC_BUFS = P::ACC_BUFS, BN = P::BN, EPI_GROUPS = P::EPI_GROUPS,
+                  EPI_THREADS = P::EPI_THREADS;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::OFF_BAR);
+    uint64_t *full = bars, *ready = bars + STAGES, *empty = bars + 2 * STAGES, *acc_full = bars + 3 * STAGES,
+             *acc_empty = acc_full + ACC_BUFS, *drain = acc_empty + ACC_BUFS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P::OFF_MISC + 4);
+    uint32_t *lut_code = reinterpret_cast<uint32_t *>(smem + P::OFF_LUT);  // byte -> its two codes as BF16x2
+    uint32_t *lut_scale = lut_code + 256;                                 // E4M3 byte -> (s, s) as BF16x2
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (p.hdr->status != 0) return;
+    const int NT = EPI == 0 ? (p.gate_up_I + 127) / 128 : p.N / 128;
+    const int MT = p.hdr->num_mtiles;
+    const int ntiles = MT * NT;
+    if ((int)blockIdx.x >= ntiles) return;
+    const int KT = p.K / WBK;
+
+    for (int i = threadIdx.x; i < 384; i += blockDim.x) {
+        if (i < 256) {
+            lut_code[i] = e2m1_bf16((uint32_t)i & 15u) | (e2m1_bf16((uint32_t)i >> 4) << 16);
+        } else {
+            const uint32_t s = e4m3_bf16((uint32_t)(i - 256));
+            lut_scale[i - 256] = s | (s << 16);
+        }
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&ready[s], kConvWarps);
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < ACC_BUFS; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], EPI_THREADS / EPI_GROUPS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                     "r"(W_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer
+        uint32_t stage = 0, phase = 0, issued = 0, last_parity = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            const WTile ti = w_tile<EPI>(p, tile, NT, MT);
+            const int rows_b = EPI == 0 ? 2 * ti.hc : 128;
+            const uint32_t bytes = (uint32_t)W_A_BYTES + (uint32_t)rows_b * 36u;  // + 32 B codes, 4 B scales per row
+            // first B row of each 64-row box: w13 gate rows then the matching up rows
+            int brow[4];
+            int nbox = 0;
+            if (EPI == 0) {
+                const int gate = ti.e * 2 * p.gate_up_I + 128 * ti.nt;
+                for (int r = 0; r < ti.hc; r += 64) brow[nbox++] = gate + r;
+                for (int r = 0; r < ti.hc; r += 64) brow[nbox++] = gate + p.gate_up_I + r;
+            } else {
+                brow[nbox++] = ti.e * p.N + 128 * ti.nt;
+                brow[nbox++] = ti.e * p.N + 128 * ti.nt + 64;
+            }
+            for (int kt = 0; kt < KT; ++kt) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kWLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                uint64_t *fb = &full[stage];
+                mbar_expect_tx(fb, bytes);
+                tma_2d(smem + P::OFF_A + stage * W_A_BYTES, &tmap_a, kt * (WBK * 2), ti.mt * WBM, fb);
+                uint8_t *bq = smem + P::OFF_BQ + stage * P::BQ_BYTES;
+                uint8_t *sq = smem + P::OFF_SQ + stage * P::SQ_BYTES;
+                for (int b = 0; b < nbox; ++b) {
+                    tma_2d(bq + b * 64 * (WBK / 2), &tmap_b, kt * (WBK / 2), brow[b], fb);
+                    bulk_g2s(sq + b * 64 * 4, p.b_sfp + ((size_t)(brow[b] / 64) * KT + kt) * 256, 256u, fb);
+                }
+                issued |= 1u << stage;
+                last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            atomicOr(&p.hdr->error_flags, kErrTimeoutProducer);
+        }
+        for (int s = 0; s < STAGES; ++s)
+            if (issued & (1u << s)) mbar_wait(&full[s], (last_parity >> s) & 1u, nullptr, kWDrainNs);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------ MMA issuer
+        uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+        bool ok = true;
+        const uint64_t da0 = desc_sw128(su32(smem + P::OFF_A)), db0 = desc_sw128(su32(smem + P::OFF_B16));
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            const int nt = tile % NT;
+            const uint32_t idesc = idesc_f16(EPI == 0 ? 2 * min(128, p.gate_up_I - 128 * nt) : 128);
+            if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, kWLimitNs)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem + acc * BN;
+            for (int kt = 0; kt < KT; ++kt) {
+                // the converters arrive on ready[stage] only after they have
+                // seen the stage's loads land and written its BF16 B tile
+                if (!mbar_wait(&ready[stage], phase, abort_flag, kWLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t da = da0 + (uint64_t)(stage * (W_A_BYTES >> 4));
+                const uint64_t db = db0 + (uint64_t)(stage * (P::B16_BYTES >> 4));
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tc_mma_f16(d, da + 2 * j, db + 2 * j, idesc, (kt | j) != 0);
+                tc_commit(&empty[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            tc_commit(&acc_full[acc]);
+            if (++acc == ACC_BUFS) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            atomicOr(&p.hdr->error_flags, kErrTimeoutMma);
+        }
+        tc_commit(drain);
+        mbar_wait(drain, 0, nullptr, kWDrainNs);
+    } else if (warp >= P::CONV_WARP0 && warp < P::EPI_WARP0) {
+        // ------------------------------------------------ converters
+        // 16-byte output chunk j of B row r holds K elements 8j..8j+7: codes
+        // bytes 4j..4j+3 of the row, block scale j/2; it is stored at chunk
+        // j ^ (r & 7) of the row, the 128-byte swizzle the descriptor names.
+        const int ct = threadIdx.x - 32 * P::CONV_WARP0;
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+            const int nt = tile % NT;
+            const int rows_b = EPI == 0 ? 2 * min(128, p.gate_up_I - 128 * nt) : 128;
+            for (int kt = 0; kt < KT; ++kt) {
+                if (!mbar_wait(&full[stage], phase, abort_flag, kWLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t *bq = reinterpret_cast<const uint32_t *>(smem + P::OFF_BQ + stage * P::BQ_BYTES);
+                const uint8_t *sq = smem + P::OFF_SQ + stage * P::SQ_BYTES;
+                uint8_t *b16 = smem + P::OFF_B16 + stage * P::B16_BYTES;
+                for (int i = ct; i < rows_b * 8; i += 32 * kConvWarps) {
+                    const int r = i >> 3, j = i & 7;
+                    const uint32_t cw = bq[r * 8 + j];
+                    const uint32_t s2 = lut_scale[sq[r * 4 + (j >> 1)] & 127u];
+                    uint4 o;
+                    o.x = bf16x2_mul(lut_code[cw & 0xFFu], s2);
+                    o.y = bf16x2_mul(lut_code[(cw >> 8) & 0xFFu], s2);
+                    o.z = bf16x2_mul(lut_code[(cw >> 16) & 0xFFu], s2);
+                    o.w = bf16x2_mul(lut_code[cw >> 24], s2);
+                    *reinterpret_cast<uint4 *>(b16 + r * 128 + ((j ^ (r & 7)) << 4)) = o;
+                }
+                // generic-proxy stores -> visible to the tensor core's reads
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ready[stage]);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicOr(&p.hdr->error_flags, kErrTimeoutMma);
+        }
+    } else if (warp >= P::EPI_WARP0) {
+        // ------------------------------------------------ epilogue
+        const int ew = warp - P::EPI_WARP0;
+        const int group = ew / (P::NUM_EPI_WARPS / EPI_GROUPS);
+        const int quarter = warp & 3;   // TMEM lanes this warp may read
+        const int part = ew >> 2;       // w13: which half of the tile's h columns
+        const int half = (ew >> 2) & 1; // w2: which half of the tile's columns
+        const int r_in = quarter * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        float *xp = reinterpret_cast<float *>(smem + P::OFF_XPOSE) + ew * 32 * kXposeLd;
+        uint32_t acc = EPI_GROUPS == 2 ? (uint32_t)group : 0u, acc_phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x + group * gridDim.x; tile < ntiles; tile += EPI_GROUPS * gridDim.x) {
+            const WTile ti = w_tile<EPI>(p, tile, NT, MT);
+            const int e = ti.e;
+            const int row = ti.mt * WBM + r_in;
+            bool valid;
+            float s0;  // w13: weight_scale_2; w2: routing weight * weight_scale_2
+            int t = 0;
+            if (EPI == 0) {
+                valid = row < p.pad_off[e] + p.counts[e];
+                s0 = p.scale2[e];
+            } else {
+                const int f = p.row_src[row];
+                valid = f >= 0;
+                s0 = valid ? __fmul_rn(p.topk_w[f], p.scale2[e]) : 0.0f;
+                t = valid ? f / p.k : 0;
+            }
+            if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, kWLimitNs)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t col0 = lane_base + acc * BN;
+            if (EPI == 0) {
+                // h columns [w0, w0 + hw) of the tile, 32 at a time: gate at
+                // accumulator column w0.., up at hc + w0..; the accumulator is
+                // released once the last columns are in registers.
+                const int hw = ti.hc / 2, w0 = part * hw;
+                for (int c = 0; 32 * c < hw; ++c) {
+                    float gate[32], up[32];
+                    tmem_ld16(col0 + w0 + 32 * c, gate);
+                    tmem_ld16(col0 + w0 + 32 * c + 16, gate + 16);
+                    tmem_ld16(col0 + ti.hc + w0 + 32 * c, up);
+                    tmem_ld16(col0 + ti.hc + w0 + 32 * c + 16, up + 16);
+                    tmem_wait_ld(gate, up);
+                    if (32 * (c + 1) >= hw) {
+                        tc_fence_before();
+                        mbar_arrive(&acc_empty[acc]);
+                    }
+                    uint32_t hb[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float h0 = silu_w16(s0 * gate[2 * i]) * (s0 * up[2 * i]);
+                        const float h1 = silu_w16(s0 * gate[2 * i + 1]) * (s0 * up[2 * i + 1]);
+                        hb[i] = pack_bf16x2(h0, h1);
+                    }
+                    if (valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.h + (size_t)row * p.I + 128 * ti.nt + w0 + 32 * c);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
+                    }
+                }
+                if (++acc == ACC_BUFS) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            } else {
+                // out[t, cols] += w * s2 * y2 on this warp's 64 columns, 32 at
+                // a time, transposed through shared memory so each reduction
+                // covers four contiguous 128-byte row segments
+                const int sub = lane >> 3, cc = (lane & 7) * 4;
+#pragma unroll 1
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int cbase = 64 * half + 32 * c2;
+                    float v[32];
+                    tmem_ld16(col0 + cbase, v);
+                    tmem_ld16(col0 + cbase + 16, v + 16);
+                    tmem_wait_ld(v);
+                    if (c2 == 1) {
+                        tc_fence_before();
+                        mbar_arrive(&acc_empty[acc]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) xp[lane * kXposeLd + i] = v[i] * s0;
+                    __syncwarp();
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = it * 4 + sub;
+                        const int t_r = __shfl_sync(0xffffffffu, t, rr);
+                        const int ok_r = __shfl_sync(0xffffffffu, (int)valid, rr);
+                        const float *src = xp + rr * kXposeLd + cc;
+                        if (ok_r)
+                            red_add_v4(p.out + (size_t)t_r * p.H + ti.nt * 128 + cbase + cc, src[0], src[1], src[2],
+                                       src[3]);
+                    }
+                    __syncwarp();
+                }
+                acc_phase ^= 1u;  // each group owns one accumulator
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            atomicOr(&p.hdr->error_flags, kErrTimeoutEpilogue);
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(W_TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// Padded permuted row p of the A operand = x[row_src[p] / k], zero on padding
+// rows; one warp per row, 16 bytes per lane and step.  The FP32 output is
+// cleared here for the w2 kernel's reductions, after the status check, so a
+// refused call writes nothing.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *__restrict__ x, int H, int k,
+                                                          const int *__restrict__ row_src, const DevHeader *hdr,
+                                                          uint16_t *__restrict__ a, float4 *__restrict__ out,
+                                                          long long out4)
+{
+    if (hdr->status != 0) return;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < out4;
+         i += (long long)gridDim.x * blockDim.x)
+        out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const long long rows = (long long)hdr->num_mtiles * WBM;
+    const int lane = threadIdx.x & 31;
+    const int n16 = H / 8;  // 16-byte chunks per row
+    for (long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows;
+         r += ((long long)gridDim.x * blockDim.x) >> 5) {
+        const int f = row_src[r];
+        uint4 *dst = reinterpret_cast<uint4 *>(a + (size_t)r * H);
+        if (f >= 0) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(f / k) * H);
+            for (int i = lane; i < n16; i += 32) dst[i] = __ldg(src + i);
+        } else {
+            for (int i = lane; i < n16; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+}
+
+// [E, N, K/16] scale bytes -> [E*N/64][K/64][64 rows][4 bytes]: the four
+// scales of one 64-K step for 64 consecutive rows are one 256-byte run.
+__global__ void __launch_bounds__(256) prep_sf_w16_kernel(const uint8_t *__restrict__ sf, uint8_t *__restrict__ out,
+                                                          long long groups, int K)
+{
+    const int KT = K / 64, nsf = K / 16;
+    const long long words = groups * KT * 64;
+    for (long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x; w < words;
+         w += (long long)gridDim.x * blockDim.x) {
+        const long long g = w / ((long long)KT * 64);
+        const int rem = (int)(w - g * KT * 64);
+        const int kt = rem >> 6, rr = rem & 63;
+        const long long row = g * 64 + rr;
+        reinterpret_cast<uint32_t *>(out)[w] = *reinterpret_cast<const uint32_t *>(sf + row * nsf + 4 * kt);
+    }
+}
+
+template <int EPI>
+cudaError_t launch_w16(const W16Args &a, cudaStream_t st)
+{
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t err = cudaFuncSetAttribute(w16_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               WPlan<EPI>::SMEM_BYTES);
+        if (err != cudaSuccess) return err;
+        attr_set = true;
+    }
+    CUtensorMap ma, mb;
+    if (!make_tensor_map_2d(&ma, a.a, (uint64_t)a.K * 2, (uint64_t)a.rows_cap, 128, WBM, true))
+        return cudaErrorInvalidValue;
+    if (!make_tensor_map_2d(&mb, a.b_q, (uint64_t)a.K / 2, (uint64_t)a.E * (uint64_t)a.N, WBK / 2, 64, false))
+        return cudaErrorInvalidValue;
+    const long long nt = EPI == 0 ? (a.gate_up_I + 127) / 128 : a.N / 128;
+    const long long tiles = (long long)a.mtiles_cap * nt;
+    int grid = sm_count();
+    if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
+    w16_gemm_kernel<EPI><<<grid, WPlan<EPI>::NUM_THREADS, WPlan<EPI>::SMEM_BYTES, st>>>(ma, mb, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_w16_w13(const W16Args &a, cudaStream_t st) { return launch_w16<0>(a, st); }
+cudaError_t launch_w16_w2(const W16Args &a, cudaStream_t st) { return launch_w16<1>(a, st); }
+
+cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int *row_src, const DevHeader *hdr,
+                               int rows_cap, uint16_t *a, float *out, long long out_floats, cudaStream_t st)
+{
+    const long long warps = rows_cap > 0 ? rows_cap : 1;
+    long long grid = (warps * 32 + 255) / 256;
+    const long long cap = (long long)sm_count() * 8;
+    if (grid > cap) grid = cap;
+    gather_rows_kernel<<<(int)grid, 256, 0, st>>>(x, H, k, row_src, hdr, a, reinterpret_cast<float4 *>(out),
+                                                  out_floats / 4);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep_sf_w16(const uint8_t *sf, uint8_t *out, int E, int N, int K, cudaStream_t st)
+{
+    const long long groups = (long long)E * N / 64;
+    const long long words = groups * (K / 64) * 64;
+    long long grid = (words + 255) / 256;
+    const long long cap = (long long)sm_count() * 16;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    prep_sf_w16_kernel<<<(int)grid, 256, 0, st>>>(sf, out, groups, K);
+    return cudaGetLastError();
+}
+
+}  // namespace nvfp4
