@@ -49,9 +49,10 @@ LAUNCHES_PER_STEP = 5
 # It holds for the kernel source it was taken on: any change to these files makes it null.
 NCU_TRAFFIC = {
     "tokens": 8192,
-    "source_sha1": {"nvfp4_w4a4_moe_gb300/csrc/kernels_gemm.cu": "2549ac09dff52d41bfff1904b666f72ff1a13f19",
+    "source_sha1": {"nvfp4_w4a4_moe_gb300/csrc/kernels_gemm.cu": "4dc4391912f598237be9dfe3c08c2a851c0278df",
+                    "nvfp4_w4a4_moe_gb300/csrc/tc_common.cuh": "8b48f3cc1e817c11a7683255ae42b63797adf749",
                     "nvfp4_w4a4_moe_gb300/csrc/common.cuh": "cd0438b935211e7a4d13568e2c81bc78fbe11871"},
-    "bytes": {"gemm_w13": 383488256 + 101186304, "gemm_w2": 267173120 + 68059136},
+    "bytes": {"gemm_w13": 383503104 + 101355776, "gemm_w2": 268049664 + 67787264},
 }
 
 
@@ -282,6 +283,11 @@ def run_ours(args, rank, world):
     stage_ms = {name: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
                 for j, name in enumerate(m.STAGES)}
 
+    if args.only_w4a16:
+        res = w4a16_leg(m, torch, w, layer, x, ids, tw, args)
+        return {"metric": METRIC, "value": res["prefill"]["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+                "config": {"T": T, "path": "w4a16"}, "w4a16": res, "note": "W4A16 only (profiling run)"}
+
     if args.only_layer:
         return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": K, "warmup": W, "ms_per_step": ms_step, "config": {"T": T},
@@ -302,6 +308,7 @@ def run_ours(args, rank, world):
     decode = decode_leg(m, torch, w, args)
     router = router_leg(m, torch, args)
     ue8m0 = ue8m0_leg(m, torch, args)
+    w4a16 = w4a16_leg(m, torch, w, layer, x, ids, tw, args)
 
     pk = peaks()
     n_active = int((np.bincount(layer.topk_ids.ravel(), minlength=E) > 0).sum())
@@ -356,6 +363,7 @@ def run_ours(args, rank, world):
         "decode": decode,
         "router": router,
         "ue8m0": ue8m0,
+        "w4a16": w4a16,
         "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * K,
         "clocks": clocks.summary(),
@@ -459,6 +467,85 @@ def decode_leg(m, torch, w, args):
         res[str(T)] = {"us_per_call": us, "us_per_graph_replay": graph_us, "graph_error": graph_err,
                        "tokens_per_s": T / (best * 1e-6), "experts_touched": touched,
                        "weight_gbs": touched * per_expert / (best * 1e-6) / 1e9}
+    return res
+
+
+def w4a16_leg(m, torch, w, layer, x, ids, tw, args):
+    """The W4A16 path (NVFP4 weights, BF16 activations, kind::f16 tensor
+    cores) on the same prefill layer and on the decode shapes: time per call
+    (CUDA events around back-to-back calls; decode also from a CUDA graph),
+    tokens/s, the GEMMs' BF16 TFLOP/s against the measured BF16 peak, and the
+    decode weight bandwidth over the touched experts' codes and scales."""
+    T, H, I, E, k = layer.T, layer.H, layer.I, layer.E, layer.k
+    m.prepare_weights_w4a16(w)
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(m.moe_w4a16_workspace_size(T, H, I, E, k), dtype=torch.uint8, device="cuda")
+    m.moe_forward_w4a16(w, x, ids, tw, out=out, ws=ws, flags=m.SYNC_CHECK)
+    flags = m.SCALES_PREVALIDATED
+    for _ in range(3):
+        m.moe_forward_w4a16(w, x, ids, tw, out=out, ws=ws, flags=flags)
+    n = 20
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(n):
+        m.moe_forward_w4a16(w, x, ids, tw, out=out, ws=ws, flags=flags)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    status, _ = m.moe_status(ws)
+    if status != m.OK:
+        raise RuntimeError(f"W4A16 device status {status}")
+    flops = 6.0 * T * k * H * I  # gate/up (2 x 2I x H) + down (2 x H x I) per routed row
+    pk = peaks()
+    res = {"prefill": {"T": T, "ms_per_call": ms, "tokens_per_s": T / (ms * 1e-3),
+                       "layer_tflops": flops / (ms * 1e-3) / 1e12,
+                       "frac_bf16_peak": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+                       "note": "whole call (scale check, reorder, row gather, both GEMMs) against the BF16 burst peak"}}
+    per_expert = 2 * I * H // 2 + 2 * I * H // 16 + H * I // 2 + H * I // 16
+    dec = {}
+    for Td in (1, 64):
+        L = S.decode(Td)
+        xd = torch.from_numpy(L.x.view(np.int16)).cuda().view(torch.bfloat16)
+        idd, twd = torch.from_numpy(L.topk_ids).cuda(), torch.from_numpy(L.topk_w).cuda()
+        od = torch.empty((Td, H), dtype=torch.float32, device="cuda")
+        wsd = torch.empty(m.moe_w4a16_workspace_size(Td, H, I, E, L.k), dtype=torch.uint8, device="cuda")
+        m.moe_forward_w4a16(w, xd, idd, twd, out=od, ws=wsd, flags=m.SYNC_CHECK)
+        for _ in range(20):
+            m.moe_forward_w4a16(w, xd, idd, twd, out=od, ws=wsd, flags=flags)
+        nd = 300
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(nd):
+            m.moe_forward_w4a16(w, xd, idd, twd, out=od, ws=wsd, flags=flags)
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) / nd * 1e3
+        graph_us, graph_err = None, None
+        try:
+            g = torch.cuda.CUDAGraph()
+            st = torch.cuda.Stream()
+            st.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(st):
+                with torch.cuda.graph(g, stream=st):
+                    m.moe_forward_w4a16(w, xd, idd, twd, out=od, ws=wsd, flags=flags, stream=st)
+            torch.cuda.current_stream().wait_stream(st)
+            for _ in range(20):
+                g.replay()
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(nd):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            graph_us = a.elapsed_time(b) / nd * 1e3
+        except Exception as ex:  # capture support depends on the driver; report, do not fail the run
+            graph_err = f"{type(ex).__name__}: {ex}"[:200]
+        touched = len(np.unique(L.topk_ids))
+        best = graph_us if graph_us is not None else us
+        dec[str(Td)] = {"us_per_call": us, "us_per_graph_replay": graph_us, "graph_error": graph_err,
+                        "experts_touched": touched, "weight_gbs": touched * per_expert / (best * 1e-6) / 1e9}
+    res["decode"] = dec
     return res
 
 
@@ -640,6 +727,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=8192,
                     help="prefill tokens (8192 is the benchmark workload; smaller values for ncu captures)")
+    ap.add_argument("--only-w4a16", action="store_true",
+                    help="time only the W4A16 path on the prefill layer (for profiling runs)")
     ap.add_argument("--only-layer", action="store_true",
                     help="time only the layer steps (no quantiser workload, e2e or CPU baseline)")
     args = ap.parse_args()
