@@ -910,6 +910,16 @@ int nvfp4_moe_forward_w4a16(const nvfp4_moe_weights *w, const void *prepared, co
     wb.h = nullptr;
     wb.topk_w = topk_weights;
     wb.out = out;
+    // column blocks per group: the largest divisor of H/128 whose output slice
+    // (T rows x 128 G columns of FP32) stays within about 48 MB of L2
+    const int nblk = H / 128;
+    const long long per_blk = (long long)T * 128 * 4;
+    wb.col_group = 1;
+    for (int G = nblk; G >= 1; --G)
+        if (nblk % G == 0 && (long long)G * per_blk <= (48ll << 20)) {
+            wb.col_group = G;
+            break;
+        }
     NV_CUDA(launch_w16_w2(wb, st), "launching the W4A16 w2 GEMM");
 
     if (flags & NVFP4_SYNC_CHECK) {

@@ -127,6 +127,7 @@ struct W16Args {
     float *out;
     DevHeader *hdr;
     int mtiles_cap;
+    int col_group;           // w2: output column blocks per tile group (divides N / 128)
 };
 cudaError_t launch_w16_w13(const W16Args &a, cudaStream_t st);
 cudaError_t launch_w16_w2(const W16Args &a, cudaStream_t st);

@@ -20,12 +20,15 @@
 //   warp 0     TMA producer: per 64-K stage the A tile (128 BF16 rows x 128 B,
 //              128-byte swizzle), the FP4 codes of the B tile (64-row boxes of
 //              32 B) and its scales (256-byte bulk copies of the prepared
-//              layout).
+//              layout), into a ring of 6 (w13) or 5 (w2) stages.
 //   warp 1     TMEM owner and MMA issuer: 4 x kind::f16 K16 per stage, M128 x
 //              N256 (w13: 128 gate + 128 up rows) or N128 (w2).
-//   warps 2-5  converters: FP4 codes x block scale -> BF16 tile, then a proxy
-//              fence and an arrive on the stage's "ready" barrier.
-//   the rest   epilogue: w13 forms h = SiLU(s2 gate) (s2 up) and stores it as
+//   warps 2-17 converters: FP4 codes x block scale -> BF16 tile in a second,
+//              two-slot ring (byte permutes on register-held tables, then
+//              BF16 products), a proxy fence and an arrive on the slot's
+//              "ready" barrier; the MMA frees both rings' slots by commits.
+//   the rest   epilogue (4 warps for w13, 2 x 4 for w2): w13 forms
+//              h = SiLU(s2 gate) (s2 up) and stores it as
 //              BF16 (the second GEMM's A operand); w2 scatters
 //              w * s2 * y2 into the token-order FP32 output with vector
 //              reductions, as in the W4A4 path.
@@ -36,6 +39,20 @@
 #include "internal.h"
 #include "tc_common.cuh"
 
+// Warp counts: the conversion is latency-bound per warp (measured 1.88 ms
+// per prefill call with 4 converter warps, 1.45 with 8, 1.31 with 16), so the
+// converters take most of the CTA; with two accumulators one epilogue warp
+// per TMEM lane quarter (w13) or two groups of four (w2) keep up.
+#ifndef W16_CONV_WARPS
+#define W16_CONV_WARPS 16
+#endif
+#ifndef W16_EPI13
+#define W16_EPI13 4
+#endif
+#ifndef W16_EPI2
+#define W16_EPI2 8
+#endif
+
 namespace nvfp4 {
 namespace {
 
@@ -44,16 +61,20 @@ using namespace tc;
 constexpr int WBM = 128, WBK = 64;         // K per stage: one 128-byte row of BF16
 constexpr int W_A_BYTES = WBM * WBK * 2;   // 16 KB
 constexpr int W_TMEM_COLS = 512;
-constexpr int kConvWarps = 4;
+constexpr int kConvWarps = W16_CONV_WARPS;
 constexpr int kXposeLd = 33;
 constexpr uint64_t kWLimitNs = 1000000000ull;
 constexpr uint64_t kWDrainNs = 200000000ull;
 
+// Two rings: NS stages of the TMA-loaded tiles (A, FP4 codes, scales; small,
+// so the loads run well ahead) and NB stages of converted BF16 B tiles.
 template <int EPI>
 struct WPlan {
     static constexpr int BN = EPI == 0 ? 256 : 128;
-    static constexpr int STAGES = EPI == 0 ? 3 : 4;
-    static constexpr int NUM_EPI_WARPS = EPI == 0 ? 8 : 16;
+    static constexpr int NS = EPI == 0 ? 6 : 5;
+    static constexpr int NB = 2;
+    static constexpr int NUM_EPI_WARPS = EPI == 0 ? W16_EPI13 : W16_EPI2;
+    static constexpr int Q_PARTS = NUM_EPI_WARPS / (4 * (EPI == 0 ? 1 : 2));  // warps per TMEM lane quarter and group
     static constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
     static constexpr int EPI_GROUPS = EPI == 0 ? 1 : 2;
     static constexpr int CONV_WARP0 = 2;
@@ -64,12 +85,12 @@ struct WPlan {
     static constexpr int BQ_BYTES = BN * WBK / 2;   // FP4 codes: BN rows x 32 B
     static constexpr int SQ_BYTES = BN * 4;         // E4M3 scales: BN rows x 4
     static constexpr int OFF_A = 0;
-    static constexpr int OFF_B16 = OFF_A + STAGES * W_A_BYTES;
-    static constexpr int OFF_BQ = OFF_B16 + STAGES * B16_BYTES;
-    static constexpr int OFF_SQ = OFF_BQ + STAGES * BQ_BYTES;
-    static constexpr int OFF_LUT = OFF_SQ + STAGES * SQ_BYTES;  // 256 x u32 codes, 128 x u32 scales
-    static constexpr int OFF_BAR = OFF_LUT + 384 * 4;
-    static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_BUFS + 1;
+    static constexpr int OFF_B16 = OFF_A + NS * W_A_BYTES;
+    static constexpr int OFF_BQ = OFF_B16 + NB * B16_BYTES;
+    static constexpr int OFF_SQ = OFF_BQ + NS * BQ_BYTES;
+    static constexpr int OFF_LUT = OFF_SQ + NS * SQ_BYTES;  // 128 x u32: E4M3 scale -> BF16x2
+    static constexpr int OFF_BAR = OFF_LUT + 128 * 4;
+    static constexpr int NUM_BARS = 2 * NS + 2 * NB + 2 * ACC_BUFS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_XPOSE = (OFF_MISC + 16 + 15) & ~15;
     static constexpr int XPOSE_BYTES = EPI == 1 ? NUM_EPI_WARPS * 32 * kXposeLd * 4 : 0;
@@ -114,10 +135,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 
 __device__ __forceinline__ float silu_w16(float z) { return __fdividef(z, 1.0f + __expf(fminf(-z, 80.0f))); }
 
-// Tile geometry (as in the W4A4 kernels).  w13: tile t covers h columns
-// [128 nt, 128 nt + hc), hc = min(128, I - 128 nt), B rows = hc gate rows then
-// hc up rows, m-tile major.  w2: output columns [128 nt, 128 nt + 128),
-// output-column-block major.
+// Tile geometry.  w13: tile t covers h columns [128 nt, 128 nt + hc), hc =
+// min(128, I - 128 nt), B rows = hc gate rows then hc up rows, m-tile major.
+// w2: output columns [128 nt, 128 nt + 128), in groups of col_group column
+// blocks: within a group the m-tiles are walked with the group's column
+// blocks adjacent.  A group's slice of the FP32 output stays in L2 for the
+// combine's reductions, and each BF16 A tile is read once per group rather
+// than once per column block.
 struct WTile {
     int mt, nt, e, hc;
 };
@@ -130,20 +154,38 @@ __device__ __forceinline__ WTile w_tile(const W16Args &p, int tile, int NT, int 
         t.nt = tile - t.mt * NT;
         t.hc = min(128, p.gate_up_I - 128 * t.nt);
     } else {
-        t.nt = tile / MT;
-        t.mt = tile - t.nt * MT;
+        const int G = p.col_group;
+        const int grp = tile / (MT * G), rem = tile - grp * (MT * G);
+        t.mt = rem / G;
+        t.nt = grp * G + (rem - t.mt * G);
         t.hc = 128;
     }
     t.e = p.tile_expert[t.mt];
     return t;
 }
 
-// BF16 bits of an E2M1 code (the page's 16-entry table: magnitudes 0, 0.5,
-// 1, 1.5, 2, 3, 4, 6; codes 8..15 negative, 8 is -0).
-__device__ __forceinline__ uint32_t e2m1_bf16(uint32_t code)
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
 {
-    const uint32_t mag[8] = {0x0000u, 0x3F00u, 0x3F80u, 0x3FC0u, 0x4000u, 0x4040u, 0x4080u, 0x40C0u};
-    return mag[code & 7u] | ((code & 8u) << 12);
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Four E2M1 codes (the low 16 bits of c, code i in nibble i) -> their BF16
+// values as two BF16x2 words (codes 0, 1 in o0; 2, 3 in o1), in registers.
+// The page's table has magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6, i.e. BF16 bits
+// 0000 3F00 3F80 3FC0 4000 4040 4080 40C0; the low and high bytes of those
+// eight values are held in two 8-byte tables, and byte permutes index them
+// with each code's three magnitude bits.  The sign (code bit 3) is the top
+// bit of a byte of c or of c << 4, which a sign-replicating permute spreads
+// to the high bytes.
+__device__ __forceinline__ void e2m1x4_bf16(uint32_t c, uint32_t &o0, uint32_t &o1)
+{
+    const uint32_t sel = c & 0x7777u;
+    const uint32_t lo = prmt(0xC0800000u, 0xC0804000u, sel);
+    const uint32_t hi = prmt(0x3F3F3F00u, 0x40404040u, sel) | (prmt(c << 4, c, 0xD9C8u) & 0x80808080u);
+    o0 = prmt(lo, hi, 0x5140u);
+    o1 = prmt(lo, hi, 0x7362u);
 }
 // BF16 bits of a non-negative E4M3 scale byte (exact: at most 4 significant bits).
 __device__ __forceinline__ uint32_t e4m3_bf16(uint32_t b)
@@ -160,17 +202,17 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
                     const W16Args p)
 {
     using P = WPlan<EPI>;
-    constexpr int STAGES = P::STAGES, ACC_BUFS = P::ACC_BUFS, BN = P::BN, EPI_GROUPS = P::EPI_GROUPS,
+    constexpr int NS = P::NS, NB = P::NB, ACC_BUFS = P::ACC_BUFS, BN = P::BN, EPI_GROUPS = P::EPI_GROUPS,
                   EPI_THREADS = P::EPI_THREADS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::OFF_BAR);
-    uint64_t *full = bars, *ready = bars + STAGES, *empty = bars + 2 * STAGES, *acc_full = bars + 3 * STAGES,
+    // full / empty: the TMA ring; ready / bfree: the BF16 ring
+    uint64_t *full = bars, *empty = bars + NS, *ready = bars + 2 * NS, *bfree = ready + NB, *acc_full = bfree + NB,
              *acc_empty = acc_full + ACC_BUFS, *drain = acc_empty + ACC_BUFS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + P::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P::OFF_MISC + 4);
-    uint32_t *lut_code = reinterpret_cast<uint32_t *>(smem + P::OFF_LUT);  // byte -> its two codes as BF16x2
-    uint32_t *lut_scale = lut_code + 256;                                 // E4M3 byte -> (s, s) as BF16x2
+    uint32_t *lut_scale = reinterpret_cast<uint32_t *>(smem + P::OFF_LUT);  // E4M3 byte -> (s, s) as BF16x2
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (p.hdr->status != 0) return;
@@ -180,19 +222,18 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
     if ((int)blockIdx.x >= ntiles) return;
     const int KT = p.K / WBK;
 
-    for (int i = threadIdx.x; i < 384; i += blockDim.x) {
-        if (i < 256) {
-            lut_code[i] = e2m1_bf16((uint32_t)i & 15u) | (e2m1_bf16((uint32_t)i >> 4) << 16);
-        } else {
-            const uint32_t s = e4m3_bf16((uint32_t)(i - 256));
-            lut_scale[i - 256] = s | (s << 16);
-        }
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+        const uint32_t s = e4m3_bf16((uint32_t)i);
+        lut_scale[i] = s | (s << 16);
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&ready[s], kConvWarps);
             mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < NB; ++s) {
+            mbar_init(&ready[s], kConvWarps);
+            mbar_init(&bfree[s], 1);
         }
         for (int i = 0; i < ACC_BUFS; ++i) {
             mbar_init(&acc_full[i], 1);
@@ -249,7 +290,7 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
                 }
                 issued |= 1u << stage;
                 last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == STAGES) {
+                if (++stage == NS) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -259,11 +300,11 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
             *abort_flag = 1;
             atomicOr(&p.hdr->error_flags, kErrTimeoutProducer);
         }
-        for (int s = 0; s < STAGES; ++s)
+        for (int s = 0; s < NS; ++s)
             if (issued & (1u << s)) mbar_wait(&full[s], (last_parity >> s) & 1u, nullptr, kWDrainNs);
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
-        uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+        uint32_t ts = 0, bs = 0, bphase = 0, acc = 0, acc_phase = 0;
         bool ok = true;
         const uint64_t da0 = desc_sw128(su32(smem + P::OFF_A)), db0 = desc_sw128(su32(smem + P::OFF_B16));
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
@@ -276,21 +317,23 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
             tc_fence_after();
             const uint32_t d = tmem + acc * BN;
             for (int kt = 0; kt < KT; ++kt) {
-                // the converters arrive on ready[stage] only after they have
-                // seen the stage's loads land and written its BF16 B tile
-                if (!mbar_wait(&ready[stage], phase, abort_flag, kWLimitNs)) {
+                // the converters arrive on ready[bs] only after they have seen
+                // the TMA stage land and written its BF16 B tile
+                if (!mbar_wait(&ready[bs], bphase, abort_flag, kWLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t da = da0 + (uint64_t)(stage * (W_A_BYTES >> 4));
-                const uint64_t db = db0 + (uint64_t)(stage * (P::B16_BYTES >> 4));
+                const uint64_t da = da0 + (uint64_t)(ts * (W_A_BYTES >> 4));
+                const uint64_t db = db0 + (uint64_t)(bs * (P::B16_BYTES >> 4));
 #pragma unroll
                 for (int j = 0; j < 4; ++j) tc_mma_f16(d, da + 2 * j, db + 2 * j, idesc, (kt | j) != 0);
-                tc_commit(&empty[stage]);
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+                tc_commit(&empty[ts]);  // A tile read (the converters finished with the codes before ready)
+                tc_commit(&bfree[bs]);  // BF16 B tile read
+                if (++ts == NS) ts = 0;
+                if (++bs == NB) {
+                    bs = 0;
+                    bphase ^= 1u;
                 }
             }
             if (!ok) break;
@@ -311,38 +354,57 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
         // 16-byte output chunk j of B row r holds K elements 8j..8j+7: codes
         // bytes 4j..4j+3 of the row, block scale j/2; it is stored at chunk
         // j ^ (r & 7) of the row, the 128-byte swizzle the descriptor names.
+        // An item is one 16-element block: chunks 2jj and 2jj+1, scale jj.
         const int ct = threadIdx.x - 32 * P::CONV_WARP0;
-        uint32_t stage = 0, phase = 0;
+        uint32_t ts = 0, tphase = 0, bs = 0, bphase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
             const int nt = tile % NT;
             const int rows_b = EPI == 0 ? 2 * min(128, p.gate_up_I - 128 * nt) : 128;
             for (int kt = 0; kt < KT; ++kt) {
-                if (!mbar_wait(&full[stage], phase, abort_flag, kWLimitNs)) {
+                if (!mbar_wait(&full[ts], tphase, abort_flag, kWLimitNs) ||
+                    !mbar_wait(&bfree[bs], bphase ^ 1u, abort_flag, kWLimitNs)) {
                     ok = false;
                     break;
                 }
-                const uint32_t *bq = reinterpret_cast<const uint32_t *>(smem + P::OFF_BQ + stage * P::BQ_BYTES);
-                const uint8_t *sq = smem + P::OFF_SQ + stage * P::SQ_BYTES;
-                uint8_t *b16 = smem + P::OFF_B16 + stage * P::B16_BYTES;
-                for (int i = ct; i < rows_b * 8; i += 32 * kConvWarps) {
-                    const int r = i >> 3, j = i & 7;
-                    const uint32_t cw = bq[r * 8 + j];
-                    const uint32_t s2 = lut_scale[sq[r * 4 + (j >> 1)] & 127u];
-                    uint4 o;
-                    o.x = bf16x2_mul(lut_code[cw & 0xFFu], s2);
-                    o.y = bf16x2_mul(lut_code[(cw >> 8) & 0xFFu], s2);
-                    o.z = bf16x2_mul(lut_code[(cw >> 16) & 0xFFu], s2);
-                    o.w = bf16x2_mul(lut_code[cw >> 24], s2);
-                    *reinterpret_cast<uint4 *>(b16 + r * 128 + ((j ^ (r & 7)) << 4)) = o;
+                const uint32_t *bq = reinterpret_cast<const uint32_t *>(smem + P::OFF_BQ + ts * P::BQ_BYTES);
+                const uint8_t *sq = smem + P::OFF_SQ + ts * P::SQ_BYTES;
+                uint8_t *b16 = smem + P::OFF_B16 + bs * P::B16_BYTES;
+                // one 16-element block (two 16-byte output chunks, one scale) per item
+                const int items = rows_b * 4;
+#pragma unroll 4
+                for (int i = ct; i < items; i += 32 * kConvWarps) {
+                    const int r = i >> 2, jj = i & 3;
+                    const uint2 cw = reinterpret_cast<const uint2 *>(bq)[r * 4 + jj];
+                    const uint32_t s2 = lut_scale[sq[r * 4 + jj] & 127u];
+                    uint4 o0, o1;
+                    e2m1x4_bf16(cw.x, o0.x, o0.y);
+                    e2m1x4_bf16(cw.x >> 16, o0.z, o0.w);
+                    e2m1x4_bf16(cw.y, o1.x, o1.y);
+                    e2m1x4_bf16(cw.y >> 16, o1.z, o1.w);
+                    o0.x = bf16x2_mul(o0.x, s2);
+                    o0.y = bf16x2_mul(o0.y, s2);
+                    o0.z = bf16x2_mul(o0.z, s2);
+                    o0.w = bf16x2_mul(o0.w, s2);
+                    o1.x = bf16x2_mul(o1.x, s2);
+                    o1.y = bf16x2_mul(o1.y, s2);
+                    o1.z = bf16x2_mul(o1.z, s2);
+                    o1.w = bf16x2_mul(o1.w, s2);
+                    uint8_t *row = b16 + r * 128;
+                    *reinterpret_cast<uint4 *>(row + (((2 * jj) ^ (r & 7)) << 4)) = o0;
+                    *reinterpret_cast<uint4 *>(row + (((2 * jj + 1) ^ (r & 7)) << 4)) = o1;
                 }
                 // generic-proxy stores -> visible to the tensor core's reads
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ready[stage]);
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
+                if (lane == 0) mbar_arrive(&ready[bs]);
+                if (++ts == NS) {
+                    ts = 0;
+                    tphase ^= 1u;
+                }
+                if (++bs == NB) {
+                    bs = 0;
+                    bphase ^= 1u;
                 }
             }
         }
@@ -355,8 +417,7 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
         const int ew = warp - P::EPI_WARP0;
         const int group = ew / (P::NUM_EPI_WARPS / EPI_GROUPS);
         const int quarter = warp & 3;   // TMEM lanes this warp may read
-        const int part = ew >> 2;       // w13: which half of the tile's h columns
-        const int half = (ew >> 2) & 1; // w2: which half of the tile's columns
+        const int part = (ew >> 2) % P::Q_PARTS;  // which slice of the tile's columns
         const int r_in = quarter * 32 + lane;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
         float *xp = reinterpret_cast<float *>(smem + P::OFF_XPOSE) + ew * 32 * kXposeLd;
@@ -388,7 +449,7 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
                 // h columns [w0, w0 + hw) of the tile, 32 at a time: gate at
                 // accumulator column w0.., up at hc + w0..; the accumulator is
                 // released once the last columns are in registers.
-                const int hw = ti.hc / 2, w0 = part * hw;
+                const int hw = ti.hc / P::Q_PARTS, w0 = part * hw;
                 for (int c = 0; 32 * c < hw; ++c) {
                     float gate[32], up[32];
                     tmem_ld16(col0 + w0 + 32 * c, gate);
@@ -424,13 +485,14 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
                 // covers four contiguous 128-byte row segments
                 const int sub = lane >> 3, cc = (lane & 7) * 4;
 #pragma unroll 1
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    const int cbase = 64 * half + 32 * c2;
+                constexpr int CW = 128 / P::Q_PARTS;  // columns of this warp
+                for (int c2 = 0; c2 < CW / 32; ++c2) {
+                    const int cbase = CW * part + 32 * c2;
                     float v[32];
                     tmem_ld16(col0 + cbase, v);
                     tmem_ld16(col0 + cbase + 16, v + 16);
                     tmem_wait_ld(v);
-                    if (c2 == 1) {
+                    if (c2 == CW / 32 - 1) {
                         tc_fence_before();
                         mbar_arrive(&acc_empty[acc]);
                     }
