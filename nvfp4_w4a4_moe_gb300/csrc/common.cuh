@@ -153,6 +153,15 @@ __device__ __forceinline__ uint2 quant_block16(const f32x2 (&x)[8], float amax, 
     return make_uint2(e2m1_rn_sat8(q[0], q[1], q[2], q[3]), e2m1_rn_sat8(q[4], q[5], q[6], q[7]));
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may be
+// scheduled while its predecessor on the stream is still running: pdl_wait()
+// blocks until the predecessor has completed and its memory is visible, and
+// must come before anything it wrote is read.  pdl_trigger() lets the next
+// kernel on the stream be scheduled once every CTA of this one has called it
+// or exited.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

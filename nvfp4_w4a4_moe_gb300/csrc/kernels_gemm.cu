@@ -176,6 +176,8 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();  // the previous kernel's outputs (A operand, row maps, status)
     if (p.hdr->status != 0) return;
     const int NT = EPI == 0 ? (p.gate_up_I + 127) / 128 : p.N / 128;
     const int MT = p.hdr->num_mtiles;
@@ -591,8 +593,9 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
     const long long tiles = (long long)a.mtiles_cap * nt;
     int grid = sm_count();
     if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
-    moe_gemm_kernel<EPI><<<grid, Plan<EPI>::NUM_THREADS, Plan<EPI>::SMEM_BYTES, st>>>(ma, mb, a, div_table());
-    return cudaGetLastError();
+    const cudaError_t err = launch_pdl(moe_gemm_kernel<EPI>, dim3(grid), dim3(Plan<EPI>::NUM_THREADS),
+                                       Plan<EPI>::SMEM_BYTES, st, ma, mb, a, div_table());
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace

@@ -87,6 +87,7 @@ constexpr int kRouteMaxOwn = 8;  // chunks per CTA the shared-memory plan allows
 
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
 {
+    pdl_trigger();  // the quantiser may be scheduled; it waits for this kernel to finish
     extern __shared__ int sh[];
     __shared__ int s_fail;
     const int E = a.E;
@@ -388,8 +389,10 @@ template <bool SWZ, bool UE>
 __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantArgs a, DivTable tab_in)
 {
     __shared__ DivTable2 tab;
+    pdl_trigger();
     load_div_table(&tab, tab_in);
     __syncthreads();
+    pdl_wait();  // the routing kernel's row map and status
     if (a.hdr && a.hdr->status != 0) return;
     const int lane = threadIdx.x & 31;
     const int k = a.k, H = a.H;
@@ -663,20 +666,14 @@ cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st)
         const long long need = (work + kQuantThreads - 1) / kQuantThreads;
         if (grid > need) grid = need;
         if (grid < 1) grid = 1;
-        kernel<<<(int)grid, kQuantThreads, 0, st>>>(a, div_table());
+        return launch_pdl(kernel, dim3((int)grid), dim3(kQuantThreads), 0, st, a, div_table());
     };
-    if (a.sf_ue8m0) {
-        if (a.sf_swizzled)
-            launch(quant_experts_kernel<true, true>);
-        else
-            launch(quant_experts_kernel<false, true>);
-    } else {
-        if (a.sf_swizzled)
-            launch(quant_experts_kernel<true, false>);
-        else
-            launch(quant_experts_kernel<false, false>);
-    }
-    return cudaGetLastError();
+    cudaError_t err;
+    if (a.sf_ue8m0)
+        err = a.sf_swizzled ? launch(quant_experts_kernel<true, true>) : launch(quant_experts_kernel<false, true>);
+    else
+        err = a.sf_swizzled ? launch(quant_experts_kernel<true, false>) : launch(quant_experts_kernel<false, false>);
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 cudaError_t launch_prep_sf(const PrepArgs &a, cudaStream_t st)

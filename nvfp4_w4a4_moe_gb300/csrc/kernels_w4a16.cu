@@ -215,6 +215,8 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
     uint32_t *lut_scale = reinterpret_cast<uint32_t *>(smem + P::OFF_LUT);  // E4M3 byte -> (s, s) as BF16x2
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();  // the previous kernel's outputs (A operand, row maps, status)
     if (p.hdr->status != 0) return;
     const int NT = EPI == 0 ? (p.gate_up_I + 127) / 128 : p.N / 128;
     const int MT = p.hdr->num_mtiles;
@@ -538,6 +540,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *__rest
                                                           uint16_t *__restrict__ a, float4 *__restrict__ out,
                                                           long long out4)
 {
+    pdl_trigger();
+    pdl_wait();  // the routing kernel's row map and status
     if (hdr->status != 0) return;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < out4;
          i += (long long)gridDim.x * blockDim.x)
@@ -594,8 +598,9 @@ cudaError_t launch_w16(const W16Args &a, cudaStream_t st)
     const long long tiles = (long long)a.mtiles_cap * nt;
     int grid = sm_count();
     if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
-    w16_gemm_kernel<EPI><<<grid, WPlan<EPI>::NUM_THREADS, WPlan<EPI>::SMEM_BYTES, st>>>(ma, mb, a);
-    return cudaGetLastError();
+    const cudaError_t err = launch_pdl(w16_gemm_kernel<EPI>, dim3(grid), dim3(WPlan<EPI>::NUM_THREADS),
+                                       WPlan<EPI>::SMEM_BYTES, st, ma, mb, a);
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace
@@ -610,9 +615,9 @@ cudaError_t launch_gather_rows(const uint16_t *x, int H, int k, const int *row_s
     long long grid = (warps * 32 + 255) / 256;
     const long long cap = (long long)sm_count() * 8;
     if (grid > cap) grid = cap;
-    gather_rows_kernel<<<(int)grid, 256, 0, st>>>(x, H, k, row_src, hdr, a, reinterpret_cast<float4 *>(out),
-                                                  out_floats / 4);
-    return cudaGetLastError();
+    const cudaError_t err = launch_pdl(gather_rows_kernel, dim3((int)grid), dim3(256), 0, st, x, H, k, row_src,
+                                       hdr, a, reinterpret_cast<float4 *>(out), out_floats / 4);
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 cudaError_t launch_prep_sf_w16(const uint8_t *sf, uint8_t *out, int E, int N, int K, cudaStream_t st)
