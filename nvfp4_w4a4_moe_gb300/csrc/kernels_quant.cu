@@ -18,6 +18,8 @@ namespace {
 // written, finite, positive and normal, and so must its FP32 reciprocal.
 __global__ void __launch_bounds__(256) validate_kernel(ValidateArgs a)
 {
+    pdl_trigger();
+    pdl_wait();  // whatever ran before on the stream (a previous call may still read the header)
     __shared__ int s_bad, s_first;
     __shared__ float s_recip[4][1024];  // reciprocals for alpha (forward: 4 arrays, E <= 1024)
     if (threadIdx.x == 0) {
@@ -88,6 +90,7 @@ constexpr int kRouteMaxOwn = 8;  // chunks per CTA the shared-memory plan allows
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
 {
     pdl_trigger();  // the quantiser may be scheduled; it waits for this kernel to finish
+    pdl_wait();     // the scale check (status, reset barrier counter)
     extern __shared__ int sh[];
     __shared__ int s_fail;
     const int E = a.E;
@@ -616,8 +619,8 @@ int grid_for(long long work, int per_block, int waves_cap)
 
 cudaError_t launch_validate(const ValidateArgs &a, cudaStream_t st)
 {
-    validate_kernel<<<1, 256, 0, st>>>(a);
-    return cudaGetLastError();
+    const cudaError_t err = launch_pdl(validate_kernel, dim3(1), dim3(256), 0, st, a);
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st)
@@ -649,6 +652,12 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t st)
     if (grid < 1) grid = 1;
     if ((a.nchunks + grid - 1) / grid > max_own) return cudaErrorInvalidConfiguration;
     RouteArgs args = a;
+    if (grid == 1) {
+        // one CTA: the grid barrier is trivial, so a plain launch (which may
+        // overlap the scale check's tail) does
+        const cudaError_t e = launch_pdl(route_kernel, dim3(1), dim3(kRouteThreads), smem, st, args);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     void *params[] = {&args};
     return cudaLaunchCooperativeKernel((const void *)route_kernel, dim3(grid), dim3(kRouteThreads), params, smem, st);
 }
