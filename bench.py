@@ -86,7 +86,9 @@ def peaks():
 
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples (200 ms) while the timed region runs."""
+    """nvidia-smi samples (every 20 ms) around the timed region; each sample is
+    stamped on arrival, and the summary keeps those between mark_start() and
+    mark_end() (all of them if none fell inside)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -95,10 +97,17 @@ class ClockSampler:
     def __init__(self, uuid: str | None):
         self.uuid = uuid
         self.proc = None
-        self.lines = []
+        self.lines = []  # (arrival time, line)
+        self.t_start = self.t_end = None
+
+    def mark_start(self):
+        self.t_start = time.monotonic()
+
+    def mark_end(self):
+        self.t_end = time.monotonic()
 
     def __enter__(self):
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "20"]
         if self.uuid:
             cmd += ["-i", self.uuid]
         try:
@@ -112,7 +121,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
     def __exit__(self, *exc):
         if self.proc:
@@ -127,7 +136,9 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
+        inside = [ln for t, ln in self.lines
+                  if self.t_start is not None and self.t_end is not None and self.t_start <= t <= self.t_end]
+        for ln in inside or [ln for _, ln in self.lines]:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -142,7 +153,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_in_timed_region": len(inside)}
 
 
 # --------------------------------------------------------------------------- workload
@@ -260,6 +271,7 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
+        clocks.mark_start()
         start.record(stream)
         for i in range(K):
             m.moe_forward(w, x, ids, tw, out=out, ws=ws, flags=flags)
@@ -272,6 +284,7 @@ def run_ours(args, rank, world):
             m.moe_forward_profiled(w, x, ids, tw, evs[i], out=out, ws=ws, flags=flags)
         pstop.record(stream)
         torch.cuda.synchronize()
+        clocks.mark_end()
         if dist:
             dist.barrier()
     total_ms = start.elapsed_time(stop)

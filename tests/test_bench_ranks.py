@@ -66,3 +66,23 @@ def test_reference_arm_only_on_rank_zero():
     class Args:
         steps, warmup, gpus, tokens, cpu_tokens = 1, 0, 2, 8192, 16
     assert bench.run_reference(Args(), rank=1, world=2) is None
+
+
+def test_clock_summary_keeps_the_timed_region():
+    """Samples outside [mark_start, mark_end] are dropped; throttle reasons
+    seen inside are reported (host-side parsing only, no nvidia-smi)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    c = bench.ClockSampler(None)
+    idle = "1200, 2070, 150.0, 0x1, Not Active, Not Active, Not Active, Not Active"
+    busy = "2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active"
+    capped = "1980, 2070, 1400.0, 0x4, Not Active, Not Active, Not Active, Active"
+    c.lines = [(0.0, idle), (1.0, busy), (1.1, capped), (1.2, busy), (2.0, idle)]
+    c.t_start, c.t_end = 0.5, 1.5
+    s = c.summary()
+    assert s["samples_in_timed_region"] == 3 and s["samples"] == 3
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+    c.t_start, c.t_end = 5.0, 6.0  # nothing inside: every sample is summarised
+    s = c.summary()
+    assert s["samples_in_timed_region"] == 0 and s["samples"] == 5
