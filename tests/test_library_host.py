@@ -105,6 +105,43 @@ def test_argument_errors_need_no_gpu(lib):
     assert lib.nvfp4_router_topk(None, 0, 0, 128, 8, None, None, None) == m.OK  # T = 0 launches nothing
 
 
+def test_w4a16_and_format_argument_errors_need_no_gpu(lib):
+    import nvfp4_w4a4_moe_gb300 as m
+    P = ctypes.c_void_p
+    H, I, E, k = 2816, 704, 128, 8
+    # sizes: the prepared scales are as many bytes as the weights' scales, rearranged
+    assert m.load().nvfp4_w4a16_prepared_size(E, H, I) == E * 2 * I * (H // 16) + E * H * (I // 16)
+    assert m.load().nvfp4_w4a16_prepared_size(E, H, 700) == 0
+    n = m.moe_w4a16_workspace_size(64, H, I, E, k)
+    assert n % 256 == 0 and n >= 64 * k * H * 2  # holds at least the gathered BF16 rows
+    assert m.moe_w4a16_workspace_size(-1, H, I, E, k) == 0
+    # forward: null weights, unsupported shape, workspace too small, misaligned output
+    assert lib.nvfp4_moe_forward_w4a16(None, P(256), P(256), 4, P(256), P(256), k, P(256), P(256), 1 << 30, 0,
+                                       None) == m.ERR_INVALID_ARG
+    w = m._Weights(E, H, 700, *([P(256)] * 10))
+    assert lib.nvfp4_moe_forward_w4a16(ctypes.byref(w), P(256), P(256), 4, P(256), P(256), k, P(256), P(256),
+                                       1 << 30, 0, None) == m.ERR_UNSUPPORTED_SHAPE
+    w = m._Weights(E, H, I, *([P(256)] * 10))
+    assert lib.nvfp4_moe_forward_w4a16(ctypes.byref(w), P(256), P(256), 64, P(256), P(256), k, P(256), P(256),
+                                       1024, 0, None) == m.ERR_WORKSPACE_TOO_SMALL
+    assert lib.nvfp4_moe_forward_w4a16(ctypes.byref(w), P(256), P(256), 64, P(256), P(256), k, P(264), P(256),
+                                       1 << 40, 0, None) == m.ERR_INVALID_ARG
+    # input scales may be null on this path; weight scales may not
+    w = m._Weights(E, H, I, P(256), P(256), P(256), None, None, P(256), P(256), P(256), None, None)
+    assert lib.nvfp4_moe_forward_w4a16(ctypes.byref(w), P(256), P(256), 0, P(256), P(256), k, P(256), P(256),
+                                       1 << 30, 0, None) == m.OK  # T = 0 launches nothing
+    w = m._Weights(E, H, I, P(256), P(256), None, None, None, P(256), P(256), P(256), None, None)
+    assert lib.nvfp4_moe_forward_w4a16(ctypes.byref(w), P(256), P(256), 0, P(256), P(256), k, P(256), P(256),
+                                       1 << 30, 0, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_prepare_weights_w4a16(None, P(256), 1 << 30, None) == m.ERR_INVALID_ARG
+    # weight quantiser: unknown scale format
+    assert lib.nvfp4_quantize_weights_format(P(256), 1, 64, 64, 3, P(256), P(256), P(256), P(256), 1 << 20,
+                                             None) == m.ERR_INVALID_ARG
+    # activation quantiser: a layout with an unknown bit
+    assert lib.nvfp4_quantize_experts(P(256), 4, 256, P(256), 2, 4, P(256), P(256), P(256), 2 | m.SF_UE8M0,
+                                      P(256), P(256), P(256), 1 << 20, None) == m.ERR_INVALID_ARG
+
+
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     import nvfp4_w4a4_moe_gb300 as m
     monkeypatch.setattr(m, "_lib", None)
