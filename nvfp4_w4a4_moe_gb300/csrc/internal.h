@@ -51,6 +51,9 @@ struct RouteArgs {
     DevHeader *hdr;
 };
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st);
+// The scale check then the routing: one kernel when the routing takes one CTA
+// (at most kRouteChunk routed rows), else the two launches above.
+cudaError_t launch_validate_route(const ValidateArgs &v, const RouteArgs &a, cudaStream_t st);
 
 struct QuantArgs {
     const uint16_t *x;

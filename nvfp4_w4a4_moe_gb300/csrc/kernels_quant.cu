@@ -16,10 +16,9 @@ namespace {
 // [page, ROOT CAUSE]: a per-expert scale slot left unwritten by the loader is
 // reciprocated into an inf / NaN / garbage global scale.  Every slot must be
 // written, finite, positive and normal, and so must its FP32 reciprocal.
-__global__ void __launch_bounds__(256) validate_kernel(ValidateArgs a)
+// Run by one CTA of 256 threads; ends with the header written by thread 0.
+__device__ __forceinline__ void validate_body(const ValidateArgs &a)
 {
-    pdl_trigger();
-    pdl_wait();  // whatever ran before on the stream (a previous call may still read the header)
     __shared__ int s_bad, s_first;
     __shared__ float s_recip[4][1024];  // reciprocals for alpha (forward: 4 arrays, E <= 1024)
     if (threadIdx.x == 0) {
@@ -64,6 +63,13 @@ __global__ void __launch_bounds__(256) validate_kernel(ValidateArgs a)
     }
 }
 
+__global__ void __launch_bounds__(256) validate_kernel(ValidateArgs a)
+{
+    pdl_trigger();
+    pdl_wait();  // whatever ran before on the stream (a previous call may still read the header)
+    validate_body(a);
+}
+
 // ------------------------------------------------------------------ routing
 // [page, §矩阵融合 "MoE FFN"]: rows are reordered by expert so all experts'
 // GEMMs run as one grouped GEMM.  Order inside an expert: ascending routed
@@ -80,22 +86,23 @@ __global__ void __launch_bounds__(256) validate_kernel(ValidateArgs a)
 //      slices, per-warp histograms give each warp's first rank per expert, and
 //      equal experts inside a 32-row step are ranked with __match_any_sync.
 // The barrier counter is the header's done_count, cleared by the scale check
-// that precedes every routing launch; its wait is bounded.
+// that precedes every routing launch; its wait is bounded.  A single CTA
+// (up to kRouteChunk routed rows) needs no barrier, and then runs in the same
+// kernel as the scale check (validate_route_kernel).
 constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kRouteSlice = kRouteChunk / kRouteWarps;  // rows per warp per chunk
 constexpr int kRouteIdsPerLane = kRouteSlice / 32;
 constexpr int kRouteMaxOwn = 8;  // chunks per CTA the shared-memory plan allows for
 
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
+__device__ __forceinline__ void route_body(const RouteArgs &a)
 {
-    pdl_trigger();  // the quantiser may be scheduled; it waits for this kernel to finish
-    pdl_wait();     // the scale check (status, reset barrier counter)
     extern __shared__ int sh[];
     __shared__ int s_fail;
     const int E = a.E;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (a.hdr->status != 0) return;  // same value in every CTA (set by the previous kernel)
+    if (a.hdr->status != 0) return;  // same value in every CTA (set by the scale check)
+    if (tid == 0) s_fail = 0;
 
     // ---- phase 1: chunk histograms.  Each thread reads its ids in the
     // scatter's mapping (warp w: rows [256 w, 256 w + 256) of the chunk, lane l:
@@ -134,9 +141,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
         __syncthreads();
     }
 
-    // ---- grid barrier
-    if (tid == 0) {
-        s_fail = 0;
+    // ---- grid barrier (with one CTA, the block barrier below is enough: its
+    // own global writes are visible to all its threads after it)
+    if (tid == 0 && gridDim.x > 1) {
         __threadfence();
         atomicAdd(&a.hdr->done_count, 1u);
         const uint64_t t0 = global_timer_ns();
@@ -317,6 +324,24 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
         }
         __syncthreads();
     }
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a)
+{
+    pdl_trigger();  // the quantiser may be scheduled; it waits for this kernel to finish
+    pdl_wait();     // the scale check (status, reset barrier counter)
+    route_body(a);
+}
+
+// The scale check and a one-CTA routing in one launch: the routing reads the
+// status the check has just written, after a block barrier.
+__global__ void __launch_bounds__(kRouteThreads) validate_route_kernel(ValidateArgs v, RouteArgs a)
+{
+    pdl_trigger();
+    pdl_wait();  // whatever ran before on the stream (a previous call may still read the header)
+    validate_body(v);
+    __syncthreads();
+    route_body(a);
 }
 
 // ------------------------------------------------------------------ UE8M0 block scales
@@ -623,25 +648,28 @@ cudaError_t launch_validate(const ValidateArgs &a, cudaStream_t st)
     return err != cudaSuccess ? err : cudaGetLastError();
 }
 
-cudaError_t launch_route(const RouteArgs &a, cudaStream_t st)
+namespace {
+// Routing launch shape: a cooperative grid of at most as many CTAs as can be
+// resident at once, each taking every gridDim-th chunk.
+size_t route_smem(int E)
 {
-    // A cooperative launch of at most as many CTAs as can be resident at
-    // once, each taking every gridDim-th chunk.
+    // cnt, off, poff, per-warp bases, per-chunk prefixes, per-run sums
+    return sizeof(int) * ((3 + kRouteWarps + kRouteMaxOwn) * (size_t)E + 2 + (E > kRouteThreads ? E : kRouteThreads));
+}
+
+cudaError_t route_plan(const RouteArgs &a, int *grid_out)
+{
     static int resident[64] = {0};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    const int max_own = kRouteMaxOwn;
-    // cnt, off, poff, per-warp bases, per-chunk prefixes, per-run sums
-    auto smem_for = [&](int E) {
-        return sizeof(int) * ((3 + kRouteWarps + max_own) * (size_t)E + 2 + (E > kRouteThreads ? E : kRouteThreads));
-    };
-    const size_t smem = smem_for(a.E);
     if (!resident[dev]) {
         // sized once for the largest expert count, so any call fits
-        const size_t smem_max = smem_for(1024);
+        const size_t smem_max = route_smem(1024);
         err = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
+        if (err != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(validate_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
         if (err != cudaSuccess) return err;
         int per_sm = 0;
         err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_kernel, kRouteThreads, smem_max);
@@ -650,16 +678,40 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t st)
     }
     int grid = a.nchunks < resident[dev] ? a.nchunks : resident[dev];
     if (grid < 1) grid = 1;
-    if ((a.nchunks + grid - 1) / grid > max_own) return cudaErrorInvalidConfiguration;
+    if ((a.nchunks + grid - 1) / grid > kRouteMaxOwn) return cudaErrorInvalidConfiguration;
+    *grid_out = grid;
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t launch_route(const RouteArgs &a, cudaStream_t st)
+{
+    int grid = 0;
+    const cudaError_t err = route_plan(a, &grid);
+    if (err != cudaSuccess) return err;
+    const size_t smem = route_smem(a.E);
     RouteArgs args = a;
     if (grid == 1) {
-        // one CTA: the grid barrier is trivial, so a plain launch (which may
-        // overlap the scale check's tail) does
+        // one CTA: no grid barrier, so a plain launch (which may overlap the
+        // scale check's tail) does
         const cudaError_t e = launch_pdl(route_kernel, dim3(1), dim3(kRouteThreads), smem, st, args);
         return e != cudaSuccess ? e : cudaGetLastError();
     }
     void *params[] = {&args};
     return cudaLaunchCooperativeKernel((const void *)route_kernel, dim3(grid), dim3(kRouteThreads), params, smem, st);
+}
+
+cudaError_t launch_validate_route(const ValidateArgs &v, const RouteArgs &a, cudaStream_t st)
+{
+    int grid = 0;
+    cudaError_t err = route_plan(a, &grid);
+    if (err != cudaSuccess) return err;
+    if (grid > 1) {
+        err = launch_validate(v, st);
+        return err != cudaSuccess ? err : launch_route(a, st);
+    }
+    err = launch_pdl(validate_route_kernel, dim3(1), dim3(kRouteThreads), route_smem(a.E), st, v, a);
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st)
