@@ -176,15 +176,11 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Set-up that reads nothing the previous kernel writes runs before the
+    // dependency wait, overlapping that kernel's tail: the division table (a
+    // kernel parameter), the barriers, the TMEM allocation and the tensor-map
+    // prefetch.
     pdl_trigger();
-    pdl_wait();  // the previous kernel's outputs (A operand, row maps, status)
-    if (p.hdr->status != 0) return;
-    const int NT = EPI == 0 ? (p.gate_up_I + 127) / 128 : p.N / 128;
-    const int MT = p.hdr->num_mtiles;
-    const int ntiles = MT * NT;
-    if ((int)blockIdx.x >= ntiles) return;
-    const int KT = (p.K + BK - 1) / BK;
-
     if (EPI == 0) load_div_table(&tab, tab_in);
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -200,6 +196,8 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
@@ -210,6 +208,20 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+
+    pdl_wait();  // the previous kernel's outputs (A operand, row maps, status)
+    const int NT = EPI == 0 ? (p.gate_up_I + 127) / 128 : p.N / 128;
+    const int MT = p.hdr->num_mtiles;
+    const int ntiles = MT * NT;
+    if (p.hdr->status != 0 || (int)blockIdx.x >= ntiles) {
+        // nothing to do (same decision in every thread): give TMEM back
+        if (warp == 1)
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot), "r"(TMEM_COLS)
+                         : "memory");
+        return;
+    }
+    const int KT = (p.K + BK - 1) / BK;
+
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 && lane == 0) {

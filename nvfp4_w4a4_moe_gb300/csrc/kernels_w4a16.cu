@@ -215,15 +215,9 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
     uint32_t *lut_scale = reinterpret_cast<uint32_t *>(smem + P::OFF_LUT);  // E4M3 byte -> (s, s) as BF16x2
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Set-up that reads nothing the previous kernel writes runs before the
+    // dependency wait, overlapping that kernel's tail.
     pdl_trigger();
-    pdl_wait();  // the previous kernel's outputs (A operand, row maps, status)
-    if (p.hdr->status != 0) return;
-    const int NT = EPI == 0 ? (p.gate_up_I + 127) / 128 : p.N / 128;
-    const int MT = p.hdr->num_mtiles;
-    const int ntiles = MT * NT;
-    if ((int)blockIdx.x >= ntiles) return;
-    const int KT = p.K / WBK;
-
     for (int i = threadIdx.x; i < 128; i += blockDim.x) {
         const uint32_t s = e4m3_bf16((uint32_t)i);
         lut_scale[i] = s | (s << 16);
@@ -245,6 +239,8 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
@@ -255,6 +251,19 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+
+    pdl_wait();  // the previous kernel's outputs (A operand, row maps, status)
+    const int NT = EPI == 0 ? (p.gate_up_I + 127) / 128 : p.N / 128;
+    const int MT = p.hdr->num_mtiles;
+    const int ntiles = MT * NT;
+    if (p.hdr->status != 0 || (int)blockIdx.x >= ntiles) {
+        // nothing to do (same decision in every thread): give TMEM back
+        if (warp == 1)
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot), "r"(W_TMEM_COLS)
+                         : "memory");
+        return;
+    }
+    const int KT = p.K / WBK;
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 && lane == 0) {

@@ -47,6 +47,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile
 }
 
 // ---------------------------------------------------------------- copies
+// Prefetch a tensor map (a __grid_constant__ kernel parameter) into the
+// descriptor cache ahead of its first TMA.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
 __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar)
 {
     asm volatile(
