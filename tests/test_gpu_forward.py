@@ -104,6 +104,28 @@ def test_prefill_unwritten_slots_rejected_before_launch(m, prefill):
     assert bool((out == 7.0).all())
 
 
+def test_decode_refused_on_device_then_clean_call(m):
+    """At decode sizes the scale check and the routing share one kernel.  With
+    the host check skipped, a bad scale still stops the call on the device:
+    the GEMM kernels find the bad status, give back their TMEM and leave, and
+    out keeps its contents.  A following call on the same workspace is exact."""
+    layer, W = layer_with_weights(S.decode(8))
+    bad = device_weights(W)
+    bad.w2_scale2 = bad.w2_scale2.clone()
+    bad.w2_scale2[int(layer.topk_ids[0, 0])] = float("nan")
+    out = torch.full((layer.T, layer.H), 9.0, device="cuda")
+    _, ws = m.moe_forward(bad, dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w), out=out,
+                          flags=m.SCALES_PREVALIDATED)
+    torch.cuda.synchronize()
+    assert m.moe_status(ws)[0] == m.ERR_SCALE_INVALID
+    assert bool((out == 9.0).all())
+    out2, _ = m.moe_forward(device_weights(W), dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w),
+                            ws=ws, flags=m.SYNC_CHECK)
+    torch.cuda.synchronize()
+    ref = oracle.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W)
+    assert_close(host(out2), ref["out"], "out")
+
+
 def test_bad_expert_id_refused_on_device(m):
     layer, W = layer_with_weights(S.tiny())
     ids = layer.topk_ids.copy()

@@ -26,9 +26,9 @@ def m():
     return mod
 
 
-def check_w4a16(m, layer, W, tokens=None, w=None):
+def check_w4a16(m, layer, W, tokens=None, w=None, ws=None):
     w = device_weights(W) if w is None else w
-    out, ws = m.moe_forward_w4a16(w, dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w),
+    out, ws = m.moe_forward_w4a16(w, dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w), ws=ws,
                                   flags=m.SYNC_CHECK)
     torch.cuda.synchronize()
     ref = oracle.moe_forward_w4a16(layer.x, layer.topk_ids, layer.topk_w, W, tokens=tokens)
@@ -100,6 +100,23 @@ def test_bad_weight_scale_rejected(m):
     assert ei.value.status == m.ERR_SCALE_INVALID
     torch.cuda.synchronize()
     assert bool((out == 3.0).all())
+
+
+def test_bad_scale_refused_on_device_then_clean_call(m):
+    """With the host check skipped, the device check still stops the call (the
+    row gather and both GEMMs leave at once, out untouched); the next call on
+    the same workspace is exact."""
+    layer, W = layer_with_weights(S.decode(8))
+    bad = device_weights(W)
+    bad.w13_scale2 = bad.w13_scale2.clone()
+    bad.w13_scale2[int(layer.topk_ids[0, 0])] = 0.0
+    out = torch.full((layer.T, layer.H), 4.0, device="cuda")
+    _, ws = m.moe_forward_w4a16(bad, dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w), out=out,
+                                flags=m.SCALES_PREVALIDATED)
+    torch.cuda.synchronize()
+    assert m.moe_status(ws)[0] == m.ERR_SCALE_INVALID
+    assert bool((out == 4.0).all())
+    check_w4a16(m, layer, W, ws=ws)
 
 
 def test_bad_expert_id_writes_nothing(m):
