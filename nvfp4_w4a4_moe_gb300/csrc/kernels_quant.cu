@@ -424,6 +424,10 @@ __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantAr
     if (a.hdr && a.hdr->status != 0) return;
     const int lane = threadIdx.x & 31;
     const int k = a.k, H = a.H;
+    // blockIdx.y takes a share of each token's k experts: small batches spread
+    // the expert loop over more CTAs instead of running it in one
+    const int kper = (k + (int)gridDim.y - 1) / (int)gridDim.y;
+    const int j0 = (int)blockIdx.y * kper, j1 = min(k, j0 + kper);
     const int npair = H >> 5;              // block pairs (32 elements) per row
     const int nchunk = (npair + 31) >> 5;  // warp items per row
     uint4 *const q16 = reinterpret_cast<uint4 *>(a.q);
@@ -472,7 +476,7 @@ __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantAr
         const float amax0 = amax16_bf16(w), amax1 = amax16_bf16(w + 8);
         // not unrolled: the compact loop runs faster than eight inlined copies
 #pragma unroll 1
-        for (int j = 0; j < k; ++j) {
+        for (int j = j0; j < j1; ++j) {
             const uint32_t qo = __shfl_sync(0xffffffffu, my_q, j) + (uint32_t)pair;
             const uint32_t so = __shfl_sync(0xffffffffu, my_s, j) + lane_s;
             const float g = __shfl_sync(0xffffffffu, my_g, j);
@@ -723,11 +727,17 @@ cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st)
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kQuantThreads, 0) != cudaSuccess ||
             per_sm < 1)
             per_sm = 1;
-        long long grid = (long long)sm_count() * per_sm;
+        const long long wave = (long long)sm_count() * per_sm;
+        long long grid = wave;
         const long long need = (work + kQuantThreads - 1) / kQuantThreads;
         if (grid > need) grid = need;
         if (grid < 1) grid = 1;
-        return launch_pdl(kernel, dim3((int)grid), dim3(kQuantThreads), 0, st, a, div_table());
+        // a batch that fills less than a wave splits each token's experts
+        // over gridDim.y, up to one expert per CTA
+        long long ysplit = wave / grid;
+        if (ysplit > a.k) ysplit = a.k;
+        if (ysplit < 1) ysplit = 1;
+        return launch_pdl(kernel, dim3((int)grid, (int)ysplit), dim3(kQuantThreads), 0, st, a, div_table());
     };
     cudaError_t err;
     if (a.sf_ue8m0)
