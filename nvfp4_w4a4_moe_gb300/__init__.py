@@ -118,6 +118,65 @@ def _empty_ws(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
+def _arg(t, name: str, dtypes, shape=None, numel=None, where: str | None = "cuda", nullable: bool = False,
+         cur: int = -1):
+    """Refuse a tensor that the C entry point would misread.  The library takes
+    bare pointers to dense row-major data of one element type on the current
+    device (or in host memory for the host entry point), so a wrong dtype, a
+    strided or broadcast view, a wrong shape or another device would make its
+    kernels read or write past the tensor.  Checked before any library call.
+    `where` None skips the memory check; `cur` is the current device when the
+    caller already has it."""
+    if t is None:
+        if nullable:
+            return
+        raise Nvfp4Error(ERR_INVALID_ARG, f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise Nvfp4Error(ERR_INVALID_ARG, f"{name} must be a torch.Tensor, not {type(t).__name__}")
+    dt = t.dtype
+    if dt is not dtypes and not (isinstance(dtypes, tuple) and dt in dtypes):
+        want = " or ".join(str(d) for d in dtypes) if isinstance(dtypes, tuple) else str(dtypes)
+        raise Nvfp4Error(ERR_INVALID_ARG, f"{name} must be {want}, not {dt}")
+    if not t.is_contiguous():
+        raise Nvfp4Error(ERR_INVALID_ARG, f"{name} must be contiguous")
+    if shape is not None and t.shape != shape:
+        raise Nvfp4Error(ERR_INVALID_ARG, f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if numel is not None and t.numel() != numel:
+        raise Nvfp4Error(ERR_INVALID_ARG, f"{name} has {t.numel()} elements, expected {numel}")
+    if where is None:
+        return
+    d = t.get_device()  # -1 in host memory
+    if where == "cuda":
+        if d < 0:
+            raise Nvfp4Error(ERR_INVALID_ARG, f"{name} must be a CUDA tensor, not on {t.device}")
+        if cur < 0:
+            cur = torch.cuda.current_device()
+        if d != cur:
+            raise Nvfp4Error(ERR_INVALID_ARG, f"{name} is on {t.device}, the current device is cuda:{cur}")
+    elif d >= 0:
+        raise Nvfp4Error(ERR_INVALID_ARG, f"{name} must be a host tensor, not on {t.device}")
+
+
+def _ws_arg(ws, name: str = "ws"):
+    _arg(ws, name, torch.uint8)  # its numel() is passed as its size in bytes
+
+
+def _layer_args(w, x, topk_ids, topk_weights, out, where: str = "cuda"):
+    """x [T, w.H] BF16, topk_ids [T, k] int32, topk_weights [T, k] FP32 and
+    out [T, w.H] FP32 (when given), all on `where`; returns (T, k)."""
+    cur = torch.cuda.current_device() if where == "cuda" and torch.cuda.is_available() else -1
+    _arg(x, "x", torch.bfloat16, where=where, cur=cur)
+    if x.dim() != 2 or x.shape[1] != w.H:
+        raise Nvfp4Error(ERR_INVALID_ARG, f"x has shape {tuple(x.shape)}, expected [T, {w.H}]")
+    _arg(topk_ids, "topk_ids", torch.int32, where=where, cur=cur)
+    if topk_ids.dim() != 2 or topk_ids.shape[0] != x.shape[0]:
+        raise Nvfp4Error(ERR_INVALID_ARG, f"topk_ids has shape {tuple(topk_ids.shape)}, expected [{x.shape[0]}, k]")
+    T, k = topk_ids.shape
+    _arg(topk_weights, "topk_weights", torch.float32, shape=(T, k), where=where, cur=cur)
+    _arg(out, "out", torch.float32, shape=(T, w.H), where=where, nullable=True, cur=cur)
+    return T, k
+
+
 def version() -> int:
     return int(load().nvfp4_version())
 
@@ -130,7 +189,10 @@ def selftest_block_division(nthreads: int = 0) -> int:
 def validate_scales(scales: torch.Tensor, written: torch.Tensor | None = None, ws: torch.Tensor | None = None,
                     stream=None):
     """Returns (bad_count, first_bad or -1).  Synchronous."""
+    _arg(scales, "scales", torch.float32)
+    _arg(written, "written", torch.uint8, numel=scales.numel(), nullable=True)
     ws = _empty_ws(256, scales.device) if ws is None else ws
+    _ws_arg(ws)
     bad, first = ctypes.c_int(0), ctypes.c_int(0)
     _check(load().nvfp4_validate_scales(_ptr(scales), _ptr(written), scales.numel(), _ptr(ws), _stream(stream),
                                         ctypes.byref(bad), ctypes.byref(first)))
@@ -146,8 +208,13 @@ def quantize_experts(x: torch.Tensor, topk_ids: torch.Tensor, input_scale: torch
     """x [T, H] bf16, topk_ids [T, k] int32, input_scale [E] f32 (device).
     sf_layout: SF_LINEAR or SF_SWIZZLED, optionally | SF_UE8M0 for UE8M0 scales.
     Returns (q [R, H/2] u8, sf u8, expert_offsets [E+1] i32, perm [R] i32)."""
+    _arg(x, "x", torch.bfloat16)
+    if x.dim() != 2 or topk_ids.dim() != 2:
+        raise Nvfp4Error(ERR_INVALID_ARG, "x must be [T, H] and topk_ids [T, k]")
     T, H = x.shape
     k = topk_ids.shape[1]
+    _arg(topk_ids, "topk_ids", torch.int32, shape=(T, k))
+    _arg(input_scale, "input_scale", torch.float32, numel=E)
     R = T * k
     dev = x.device
     q = torch.empty((R, H // 2), dtype=torch.uint8, device=dev)
@@ -159,6 +226,7 @@ def quantize_experts(x: torch.Tensor, topk_ids: torch.Tensor, input_scale: torch
     perm = torch.empty(max(R, 1), dtype=torch.int32, device=dev)
     need = quantize_workspace_size(T, k, E)
     ws = _empty_ws(need, dev) if ws is None else ws
+    _ws_arg(ws)
     _check(load().nvfp4_quantize_experts(_ptr(x), T, H, _ptr(topk_ids), k, E, _ptr(input_scale), _ptr(q), _ptr(sf),
                                          sf_layout, _ptr(offsets), _ptr(perm), _ptr(ws), ws.numel(),
                                          _stream(stream)))
@@ -171,8 +239,13 @@ def quantize_experts_static_scratch(x: torch.Tensor, topk_ids: torch.Tensor, inp
     device memory, the library's fixed per-device scratch array is used (see
     nvfp4_quantize_experts_static_scratch in the C header for its limit and
     the rule that overlapping calls race).  Outputs are still the caller's."""
+    _arg(x, "x", torch.bfloat16)
+    if x.dim() != 2 or topk_ids.dim() != 2:
+        raise Nvfp4Error(ERR_INVALID_ARG, "x must be [T, H] and topk_ids [T, k]")
     T, H = x.shape
     k = topk_ids.shape[1]
+    _arg(topk_ids, "topk_ids", torch.int32, shape=(T, k))
+    _arg(input_scale, "input_scale", torch.float32, numel=E)
     R = T * k
     dev = x.device
     q = torch.empty((R, H // 2), dtype=torch.uint8, device=dev)
@@ -201,7 +274,42 @@ class MoEWeights:
         self.prepared = None
         self.prepared_w4a16 = None
 
+    def __setattr__(self, name, value):
+        # assigning any field (not an in-place write) re-arms the argument check
+        object.__setattr__(self, name, value)
+        if name not in ("_checked_on", "_cstruct"):
+            object.__setattr__(self, "_checked_on", None)
+            object.__setattr__(self, "_cstruct", None)
+
+    def check(self):
+        """Every tensor dense, of its dtype and size, on the current device
+        (the input scales and the written masks may be None).  All layouts
+        are checked before the first memory location.  The result holds until
+        a field is assigned again."""
+        cur = torch.cuda.current_device() if torch.cuda.is_available() else None
+        if cur is not None and self._checked_on == cur:
+            return
+        E, H, I = self.E, self.H, self.I
+        spec = [("w13_q", torch.uint8, E * 2 * I * H // 2, False), ("w13_sf", torch.uint8, E * 2 * I * H // 16, False),
+                ("w13_scale2", torch.float32, E, False), ("w13_input_scale", torch.float32, E, True),
+                ("w13_input_written", torch.uint8, E, True),
+                ("w2_q", torch.uint8, E * H * I // 2, False), ("w2_sf", torch.uint8, E * H * I // 16, False),
+                ("w2_scale2", torch.float32, E, False), ("w2_input_scale", torch.float32, E, True),
+                ("w2_input_written", torch.uint8, E, True)]
+        for where in (None, "cuda"):
+            for name, dtype, n, nullable in spec:
+                _arg(getattr(self, name), name, dtype, numel=n, where=where, nullable=nullable,
+                     cur=-1 if cur is None else cur)
+        self._checked_on = cur
+
     def cstruct(self) -> _Weights:
+        """The C struct of the weight pointers, rebuilt after any assignment."""
+        self.check()
+        if self._cstruct is None:
+            self._cstruct = self._make_cstruct()
+        return self._cstruct
+
+    def _make_cstruct(self) -> _Weights:
         return _Weights(self.E, self.H, self.I, _ptr(self.w13_q), _ptr(self.w13_sf), _ptr(self.w13_scale2),
                         _ptr(self.w13_input_scale), _ptr(self.w13_input_written), _ptr(self.w2_q), _ptr(self.w2_sf),
                         _ptr(self.w2_scale2), _ptr(self.w2_input_scale), _ptr(self.w2_input_written))
@@ -231,8 +339,9 @@ def moe_host_workspace_size(T: int, H: int, I: int, E: int, k: int) -> int:
 def moe_forward(w: MoEWeights, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
                 out: torch.Tensor | None = None, ws: torch.Tensor | None = None, flags: int = 0, stream=None):
     """out [T, H] f32 = the expert path of one layer (device tensors)."""
-    T, H = x.shape
-    k = topk_ids.shape[1]
+    w.check()
+    T, k = _layer_args(w, x, topk_ids, topk_weights, out)
+    H = w.H
     if w.prepared is None:
         prepare_weights(w, stream)
     if out is None:
@@ -242,6 +351,8 @@ def moe_forward(w: MoEWeights, x: torch.Tensor, topk_ids: torch.Tensor, topk_wei
         if flags & DEBUG_KEEP_H:
             n = moe_host_workspace_size(T, H, w.I, w.E, k) + intermediates_rows_cap(T, w.E, k) * w.I * 4
         ws = _empty_ws(n, x.device)
+    _ws_arg(ws)
+    _arg(w.prepared, "prepared weights", torch.uint8)
     cw = w.cstruct()
     _check(load().nvfp4_moe_forward(ctypes.byref(cw), _ptr(w.prepared), _ptr(x), T, _ptr(topk_ids),
                                     _ptr(topk_weights), k, _ptr(out), _ptr(ws), ws.numel(), flags, _stream(stream)))
@@ -265,14 +376,17 @@ def moe_w4a16_workspace_size(T: int, H: int, I: int, E: int, k: int) -> int:
 def moe_forward_w4a16(w: MoEWeights, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
                       out: torch.Tensor | None = None, ws: torch.Tensor | None = None, flags: int = 0, stream=None):
     """out [T, H] f32 = the expert path with NVFP4 weights and BF16 activations."""
-    T, H = x.shape
-    k = topk_ids.shape[1]
+    w.check()
+    T, k = _layer_args(w, x, topk_ids, topk_weights, out)
+    H = w.H
     if w.prepared_w4a16 is None:
         prepare_weights_w4a16(w, stream)
     if out is None:
         out = torch.empty((T, H), dtype=torch.float32, device=x.device)
     if ws is None:
         ws = _empty_ws(moe_w4a16_workspace_size(T, H, w.I, w.E, k), x.device)
+    _ws_arg(ws)
+    _arg(w.prepared_w4a16, "prepared W4A16 weights", torch.uint8)
     cw = w.cstruct()
     _check(load().nvfp4_moe_forward_w4a16(ctypes.byref(cw), _ptr(w.prepared_w4a16), _ptr(x), T, _ptr(topk_ids),
                                           _ptr(topk_weights), k, _ptr(out), _ptr(ws), ws.numel(), flags,
@@ -282,6 +396,7 @@ def moe_forward_w4a16(w: MoEWeights, x: torch.Tensor, topk_ids: torch.Tensor, to
 
 def w4a16_intermediates_of(ws: torch.Tensor, T: int, H: int, I: int, E: int, k: int) -> dict:
     """Views of the W4A16 workspace: gathered BF16 rows and h (BF16 bits as int16)."""
+    _ws_arg(ws)
     a16, h16 = ctypes.c_void_p(), ctypes.c_void_p()
     _check(load().nvfp4_moe_w4a16_intermediates_of(_ptr(ws), T, H, I, E, k, ctypes.byref(a16), ctypes.byref(h16)))
     rc = intermediates_rows_cap(T, E, k)
@@ -301,8 +416,12 @@ def moe_forward_profiled(w: MoEWeights, x: torch.Tensor, topk_ids: torch.Tensor,
                          events, out: torch.Tensor, ws: torch.Tensor, flags: int = 0, stream=None):
     """moe_forward recording six torch.cuda.Event (enable_timing) around its
     stages on the launching stream; stage i lasts events[i] -> events[i + 1]."""
-    T, H = x.shape
-    k = topk_ids.shape[1]
+    w.check()
+    T, k = _layer_args(w, x, topk_ids, topk_weights, out)
+    _ws_arg(ws)
+    _arg(w.prepared, "prepared weights", torch.uint8)
+    if len(events) != 6:
+        raise Nvfp4Error(ERR_INVALID_ARG, f"{len(events)} events given, 6 needed")
     for e in events:  # torch creates the CUDA event on its first record
         if e.cuda_event == 0:
             e.record(stream)
@@ -318,14 +437,17 @@ def moe_forward_host(w: MoEWeights, x_host: torch.Tensor, topk_ids_host: torch.T
                      topk_weights_host: torch.Tensor, out_host: torch.Tensor | None = None,
                      ws: torch.Tensor | None = None, flags: int = 0, stream=None):
     """Same layer from host (ideally pinned) tensors; returns out_host [T, H] f32."""
-    T, H = x_host.shape
-    k = topk_ids_host.shape[1]
+    w.check()
+    T, k = _layer_args(w, x_host, topk_ids_host, topk_weights_host, out_host, where="cpu")
+    H = w.H
     if w.prepared is None:
         prepare_weights(w, stream)
     if out_host is None:
         out_host = torch.empty((T, H), dtype=torch.float32, pin_memory=True)
     if ws is None:
         ws = _empty_ws(moe_host_workspace_size(T, H, w.I, w.E, k), w.w13_q.device)
+    _ws_arg(ws)
+    _arg(w.prepared, "prepared weights", torch.uint8)
     cw = w.cstruct()
     _check(load().nvfp4_moe_forward_host(ctypes.byref(cw), _ptr(w.prepared), _ptr(x_host), T, _ptr(topk_ids_host),
                                          _ptr(topk_weights_host), k, _ptr(out_host), _ptr(ws), ws.numel(), flags,
@@ -334,7 +456,9 @@ def moe_forward_host(w: MoEWeights, x_host: torch.Tensor, topk_ids_host: torch.T
 
 
 def moe_status(ws: torch.Tensor, stream=None):
-    """(status, first_bad) of the last forward on ws.  Synchronous; does not raise."""
+    """(status, first_bad) of the last forward on ws.  Synchronous; does not
+    raise on a device status (a bad workspace argument does raise)."""
+    _ws_arg(ws)
     first = ctypes.c_int(-1)
     rc = load().nvfp4_moe_status(_ptr(ws), _stream(stream), ctypes.byref(first))
     return int(rc), first.value
@@ -349,6 +473,7 @@ def intermediates_rows_cap(T: int, E: int, k: int) -> int:
 
 def intermediates_of(ws: torch.Tensor, T: int, H: int, I: int, E: int, k: int) -> dict:
     """Views (device tensors) of the workspace intermediates of the last forward."""
+    _ws_arg(ws)
     o = _Intermediates()
     _check(load().nvfp4_moe_intermediates_of(_ptr(ws), T, H, I, E, k, ctypes.byref(o)))
     base = ws.data_ptr()
@@ -378,9 +503,15 @@ def intermediates_of(ws: torch.Tensor, T: int, H: int, I: int, E: int, k: int) -
 
 def residual_rmsnorm(x: torch.Tensor, out: torch.Tensor, eps: float = 1e-6, x_next: torch.Tensor | None = None,
                      stream=None) -> torch.Tensor:
+    """x_next = RMSNorm(x + out) in BF16 (no weight), x [T, H] BF16, out [T, H] FP32."""
+    _arg(x, "x", torch.bfloat16)
+    if x.dim() != 2:
+        raise Nvfp4Error(ERR_INVALID_ARG, f"x has shape {tuple(x.shape)}, expected [T, H]")
     T, H = x.shape
+    _arg(out, "out", torch.float32, shape=(T, H))
     if x_next is None:
         x_next = torch.empty_like(x)
+    _arg(x_next, "x_next", torch.bfloat16, shape=(T, H))
     _check(load().nvfp4_residual_rmsnorm(_ptr(x), _ptr(out), T, H, float(eps), _ptr(x_next), _stream(stream)))
     return x_next
 
@@ -389,19 +520,18 @@ def router_topk(logits: torch.Tensor, k: int, topk_ids: torch.Tensor | None = No
                 topk_weights: torch.Tensor | None = None, stream=None):
     """logits [T, E] fp32 or bf16 (device) -> (topk_ids [T, k] int32, topk_weights [T, k] f32):
     softmax over the experts, the k largest (ties to the lower index), renormalised."""
+    cur = torch.cuda.current_device() if torch.cuda.is_available() else -1
+    _arg(logits, "logits", (torch.float32, torch.bfloat16), cur=cur)
+    if logits.dim() != 2:
+        raise Nvfp4Error(ERR_INVALID_ARG, f"logits has shape {tuple(logits.shape)}, expected [T, E]")
     T, E = logits.shape
-    if logits.dtype == torch.float32:
-        dt = LOGITS_F32
-    elif logits.dtype == torch.bfloat16:
-        dt = LOGITS_BF16
-    else:
-        raise Nvfp4Error(ERR_INVALID_ARG, f"router_topk: logits must be float32 or bfloat16, not {logits.dtype}")
-    if not logits.is_contiguous():
-        raise Nvfp4Error(ERR_INVALID_ARG, "router_topk: logits must be contiguous")
+    dt = LOGITS_F32 if logits.dtype == torch.float32 else LOGITS_BF16
     if topk_ids is None:
         topk_ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
     if topk_weights is None:
         topk_weights = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+    _arg(topk_ids, "topk_ids", torch.int32, shape=(T, k), cur=cur)
+    _arg(topk_weights, "topk_weights", torch.float32, shape=(T, k), cur=cur)
     _check(load().nvfp4_router_topk(_ptr(logits), dt, T, E, k, _ptr(topk_ids), _ptr(topk_weights),
                                     _stream(stream)))
     return topk_ids, topk_weights
@@ -410,6 +540,9 @@ def router_topk(logits: torch.Tensor, k: int, topk_ids: torch.Tensor | None = No
 def quantize_weights(w: torch.Tensor, stream=None, ue8m0: bool = False):
     """w [count, N, K] bf16 (device) -> (q [count, N, K/2] u8, sf [count, N, K/16] u8, scale2 [count] f32);
     the block scales are E4M3, or UE8M0 with ue8m0."""
+    _arg(w, "w", torch.bfloat16)
+    if w.dim() != 3:
+        raise Nvfp4Error(ERR_INVALID_ARG, f"w has shape {tuple(w.shape)}, expected [count, N, K]")
     count, N, K = w.shape
     dev = w.device
     q = torch.empty((count, N, K // 2), dtype=torch.uint8, device=dev)
