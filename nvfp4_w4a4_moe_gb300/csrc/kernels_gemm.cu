@@ -589,12 +589,17 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t row
 template <int EPI>
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
 {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               Plan<EPI>::SMEM_BYTES);
-        if (err != cudaSuccess) return err;
-        attr_set = true;
+    // function attributes are per device: set once on each
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaError_t aerr = cudaGetDevice(&dev);
+    if (aerr != cudaSuccess) return aerr;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        aerr = cudaFuncSetAttribute(moe_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Plan<EPI>::SMEM_BYTES);
+        if (aerr != cudaSuccess) return aerr;
+        attr_set[dev] = true;
     }
     CUtensorMap ma, mb;
     const uint64_t kbytes = (uint64_t)a.K / 2;
@@ -616,19 +621,19 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+static EncodeTiledFn query_encode_fn()
+{
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return reinterpret_cast<EncodeTiledFn>(p);
+    return nullptr;
+}
+
 static EncodeTiledFn encode_fn()
 {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
+    static const EncodeTiledFn fn = query_encode_fn();  // initialised once, thread-safe
     return fn;
 }
 

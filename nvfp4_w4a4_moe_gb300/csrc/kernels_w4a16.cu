@@ -591,12 +591,17 @@ __global__ void __launch_bounds__(256) prep_sf_w16_kernel(const uint8_t *__restr
 template <int EPI>
 cudaError_t launch_w16(const W16Args &a, cudaStream_t st)
 {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t err = cudaFuncSetAttribute(w16_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               WPlan<EPI>::SMEM_BYTES);
-        if (err != cudaSuccess) return err;
-        attr_set = true;
+    // function attributes are per device: set once on each
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaError_t aerr = cudaGetDevice(&dev);
+    if (aerr != cudaSuccess) return aerr;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        aerr = cudaFuncSetAttribute(w16_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    WPlan<EPI>::SMEM_BYTES);
+        if (aerr != cudaSuccess) return aerr;
+        attr_set[dev] = true;
     }
     CUtensorMap ma, mb;
     if (!make_tensor_map_2d(&ma, a.a, (uint64_t)a.K * 2, (uint64_t)a.rows_cap, 128, WBM, true))
