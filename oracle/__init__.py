@@ -73,6 +73,7 @@ def _load_locked(path):
         "orc_ue8m0_encode": (ctypes.c_int, [F32]),
         "orc_quant_block16_ue8m0": (ctypes.c_int, [P, F32, P]),
         "orc_quant_rows_ue8m0": (None, [P, I64, I64, P, P, P, ctypes.c_int]),
+        "orc_gemm_nvfp4_ue8m0": (ctypes.c_int, [P, P, P, I64, P, P, F32, I64, I64, P, ctypes.c_int]),
         "orc_validate_scales": (I64, [P, P, I64, P]),
         "orc_route": (ctypes.c_int, [P, I64, I32, I32, P, P]),
         "orc_router": (ctypes.c_int, [P, I64, I32, I32, P, P]),
@@ -306,6 +307,23 @@ def gemm(aq, asf, ga_rows, wq, wsf, gw) -> np.ndarray:
     return y
 
 
+def gemm_ue8m0(aq, asf, ga_rows, wq, wsf, gw) -> np.ndarray:
+    """y [M, N] fp64 = (sum_k qa*sa*qw*sw) / (g_a*g_w), as gemm() with UE8M0
+    block scales on both operands (see orc_gemm_nvfp4_ue8m0)."""
+    aq = np.ascontiguousarray(aq, dtype=np.uint8)
+    asf = np.ascontiguousarray(asf, dtype=np.uint8)
+    wq = np.ascontiguousarray(wq, dtype=np.uint8)
+    wsf = np.ascontiguousarray(wsf, dtype=np.uint8)
+    M, K = aq.shape[0], aq.shape[1] * 2
+    N = wq.shape[0]
+    ga = np.ascontiguousarray(np.broadcast_to(np.asarray(ga_rows, dtype=np.float32), (M,)))
+    y = np.empty((M, N), dtype=np.float64)
+    if M and N:
+        rc = _L().orc_gemm_nvfp4_ue8m0(_p(aq), _p(asf), _p(ga), M, _p(wq), _p(wsf), np.float32(gw), N, K, _p(y), 0)
+        assert rc == 0
+    return y
+
+
 def silu_mul(y1: np.ndarray) -> np.ndarray:
     """[M, 2I] fp64 (gate columns first) -> h [M, I] FP32."""
     y1 = np.ascontiguousarray(y1, dtype=np.float64)
@@ -343,16 +361,19 @@ class Weights:
         self.w2_q = np.zeros((E, H, I // 2), np.uint8)
         self.w2_sf = np.zeros((E, H, I // 16), np.uint8)
         self.w2_scale2 = np.zeros(E, np.float32)
+        self.ue8m0 = False  # block scales of w13_sf / w2_sf: E4M3, or UE8M0 when set
         self.w13_input_scale = np.ones(E, np.float32)
         self.w2_input_scale = np.ones(E, np.float32)
 
 
-def quantize_layer_weights(layer, experts=None) -> Weights:
-    """The oracle's weight path applied to a synthetic layer's BF16 weights."""
+def quantize_layer_weights(layer, experts=None, ue8m0: bool = False) -> Weights:
+    """The oracle's weight path applied to a synthetic layer's BF16 weights
+    (UE8M0 block scales with ue8m0)."""
     W = Weights(layer.E, layer.H, layer.I)
+    W.ue8m0 = ue8m0
     for e in (range(layer.E) if experts is None else experts):
-        W.w13_q[e], W.w13_sf[e], W.w13_scale2[e] = quantize_weight(layer.weight_bf16(e, "w13"))
-        W.w2_q[e], W.w2_sf[e], W.w2_scale2[e] = quantize_weight(layer.weight_bf16(e, "w2"))
+        W.w13_q[e], W.w13_sf[e], W.w13_scale2[e] = quantize_weight(layer.weight_bf16(e, "w13"), ue8m0=ue8m0)
+        W.w2_q[e], W.w2_sf[e], W.w2_scale2[e] = quantize_weight(layer.weight_bf16(e, "w2"), ue8m0=ue8m0)
     if layer.w13_input_scale is not None:
         W.w13_input_scale = layer.w13_input_scale.copy()
     if layer.w2_input_scale is not None:
@@ -379,7 +400,12 @@ def moe_forward(x_bf16, topk_ids, topk_w, W: Weights, tokens=None):
 
     Returns a dict with out [T, H] fp64 (rows outside `tokens` are 0) and the
     intermediates of the permuted rows it computed: rows (permuted row
-    indices), a1q, sf1, h, a2q, sf2, y2, plus offsets and perm."""
+    indices), a1q, sf1, h, a2q, sf2, y2, plus offsets and perm.
+
+    With W.ue8m0 the whole layer takes UE8M0 block scales (reading: the
+    page's UE8M0_SF flag selects power-of-two block scales; the variant keeps
+    every other step, so the weights, a1 and a2 all carry UE8M0 scales and
+    both GEMMs take them)."""
     T, k = topk_ids.shape
     E, H, I = W.E, W.H, W.I
     for s in (W.w13_input_scale, W.w2_input_scale, W.w13_scale2, W.w2_scale2):
@@ -400,7 +426,9 @@ def moe_forward(x_bf16, topk_ids, topk_w, W: Weights, tokens=None):
         rows = np.nonzero(keep[perm // k])[0]
     xf = (np.asarray(x_bf16, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
     nr = len(rows)
-    a1q, sf1 = quant_rows(xf[perm[rows] // k], g1[row_e[rows]])
+    ue = bool(getattr(W, "ue8m0", False))
+    mm = gemm_ue8m0 if ue else gemm
+    a1q, sf1 = quant_rows(xf[perm[rows] // k], g1[row_e[rows]], ue8m0=ue)
     h = np.zeros((nr, I), np.float32)
     y2 = np.zeros((nr, H), np.float64)
     a2q = np.zeros((nr, I // 2), np.uint8)
@@ -408,11 +436,11 @@ def moe_forward(x_bf16, topk_ids, topk_w, W: Weights, tokens=None):
     re = row_e[rows]
     for e in np.unique(re):
         sel = np.nonzero(re == e)[0]
-        y1 = gemm(a1q[sel], sf1[sel], g1[e], W.w13_q[e], W.w13_sf[e], gw13[e])
+        y1 = mm(a1q[sel], sf1[sel], g1[e], W.w13_q[e], W.w13_sf[e], gw13[e])
         h[sel] = silu_mul(y1)
-        q2, s2 = quant_rows(h[sel], np.full(len(sel), g2[e], np.float32))
+        q2, s2 = quant_rows(h[sel], np.full(len(sel), g2[e], np.float32), ue8m0=ue)
         a2q[sel], sf2[sel] = q2, s2
-        y2[sel] = gemm(q2, s2, g2[e], W.w2_q[e], W.w2_sf[e], gw2[e])
+        y2[sel] = mm(q2, s2, g2[e], W.w2_q[e], W.w2_sf[e], gw2[e])
     out = np.zeros((T, H), np.float64)
     f = perm[rows]
     t_of = f // k

@@ -537,6 +537,79 @@ int orc_gemm_nvfp4(const uint8_t *aq, const uint8_t *asf, const float *ga, int64
     return 0;
 }
 
+/* y[M, N] = dequant(A) . dequant(W)^T with UE8M0 block scales on both
+ * operands [page, MoE section: the expert quantiser's UE8M0_SF flag].
+ * Reading: the variant keeps the GEMM above, y = (sum_k qa*sa*qw*sw) /
+ * (g_a * g_w), with every block scale s = 2^(byte - 127).  A term
+ * code * 2^e is exact in fp64 (an E2M1 value has two significant bits and
+ * e lies in [-127, 127]), so is each product of two terms; the sum runs in
+ * fp64 in k order, and the result takes one multiply by 1/(g_a * g_w). */
+typedef struct {
+    const uint8_t *aq, *asf;
+    const float *ga;
+    const double *wd; /* [N, K] dequantised weights, code * scale */
+    float gw;
+    int64_t N, K;
+    double *y;
+} gemm_ue_ctx;
+
+static double deq_ue8m0(uint8_t code, uint8_t sfb) { return orc_e2m1_value(code) * orc_ue8m0_value(sfb); }
+
+static void gemm_ue_range(int64_t lo, int64_t hi, void *p)
+{
+    gemm_ue_ctx *c = (gemm_ue_ctx *)p;
+    int64_t K = c->K;
+    double *arow = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    if (!arow) return;
+    for (int64_t m = lo; m < hi; ++m) {
+        for (int64_t kk = 0; kk < K; ++kk) {
+            uint8_t byte = c->aq[m * (K / 2) + kk / 2];
+            uint8_t code = (kk & 1) ? (byte >> 4) : (byte & 15);
+            arow[kk] = deq_ue8m0(code, c->asf[m * (K / 16) + kk / 16]);
+        }
+        double alpha = 1.0 / ((double)c->ga[m] * (double)c->gw);
+        for (int64_t n = 0; n < c->N; ++n) {
+            const double *wr = c->wd + n * K;
+            double acc = 0.0;
+            for (int64_t kk = 0; kk < K; ++kk) acc += arow[kk] * wr[kk];
+            c->y[m * c->N + n] = acc * alpha;
+        }
+    }
+    free(arow);
+}
+
+typedef struct {
+    const uint8_t *wq, *wsf;
+    int64_t K;
+    double *wd;
+} deq_ue_ctx;
+
+static void deq_ue_range(int64_t lo, int64_t hi, void *p)
+{
+    deq_ue_ctx *c = (deq_ue_ctx *)p;
+    int64_t K = c->K;
+    for (int64_t n = lo; n < hi; ++n)
+        for (int64_t kk = 0; kk < K; ++kk) {
+            uint8_t byte = c->wq[n * (K / 2) + kk / 2];
+            uint8_t code = (kk & 1) ? (byte >> 4) : (byte & 15);
+            c->wd[n * K + kk] = deq_ue8m0(code, c->wsf[n * (K / 16) + kk / 16]);
+        }
+}
+
+int orc_gemm_nvfp4_ue8m0(const uint8_t *aq, const uint8_t *asf, const float *ga, int64_t M, const uint8_t *wq,
+                         const uint8_t *wsf, float gw, int64_t N, int64_t K, double *y, int nthreads)
+{
+    if (K % 16 != 0) return -1;
+    double *wd = (double *)malloc(sizeof(double) * (size_t)(N * K > 0 ? N * K : 1));
+    if (!wd) return -2;
+    deq_ue_ctx dc = {wq, wsf, K, wd};
+    parallel_for(N, nthreads, deq_ue_range, &dc);
+    gemm_ue_ctx gc = {aq, asf, ga, wd, gw, N, K, y};
+    parallel_for(M, nthreads, gemm_ue_range, &gc);
+    free(wd);
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Gated activation                                                           */
 /* ------------------------------------------------------------------------ */

@@ -496,6 +496,62 @@ def pin_gemm_fp64(orc):
     assert np.allclose(y, want, rtol=1e-12, atol=1e-12 * np.abs(want).max())
 
 
+def _ue8m0_fraction(b: int) -> Fraction:
+    # UE8M0 byte b encodes 2^(b - 127) (255 is NaN and never produced)
+    return Fraction(2) ** (int(b) - 127)
+
+
+def pin_gemm_ue8m0_fraction(orc):
+    """The UE8M0 GEMM against exact rational arithmetic, with global scales
+    spread over 2^-60 .. 2^60 so that the block scale bytes lie far from the
+    bias and a wrong bias, a dropped scale or a swapped nibble shows."""
+    r = _rng(21)
+    M, N, K = 3, 4, 48
+    x = r.standard_normal((M, K)).astype(np.float32)
+    w = (r.standard_normal((N, K)) * 0.02).astype(np.float32)
+    ga = np.exp2(r.uniform(-60, 60, M)).astype(np.float32)
+    gw = np.float32(np.exp2(r.uniform(-40, 40)))
+    aq, asf = orc.quant_rows(x, ga, ue8m0=True)
+    wq, wsf = orc.quant_rows(w, np.full(N, gw, np.float32), ue8m0=True)
+    assert asf.min() < 100 or asf.max() > 150  # far from the bias
+    y = orc.gemm_ue8m0(aq, asf, ga, wq, wsf, gw)
+
+    def row_values(q, sf):
+        return [Fraction(E2M1[(int(q[i // 2]) >> (4 * (i % 2))) & 15]) * _ue8m0_fraction(sf[i // 16])
+                for i in range(len(q) * 2)]
+
+    for m in range(M):
+        a = row_values(aq[m], asf[m])
+        for n in range(N):
+            b = row_values(wq[n], wsf[n])
+            want = sum(p * q for p, q in zip(a, b)) / (Fraction(float(ga[m])) * Fraction(float(gw)))
+            assert abs(y[m, n] - float(want)) <= 1e-15 * abs(float(want)) + 1e-300, (m, n, y[m, n], float(want))
+
+
+def pin_gemm_ue8m0_matches_e4m3(orc):
+    """On block scales that are powers of two inside E4M3's range (2^-9 ..
+    2^8), the same operands written with E4M3 and with UE8M0 scale bytes give
+    the same GEMM: the UE8M0 GEMM against the rationally pinned E4M3 one.
+    The bytes come from test-side encoders of 2^k."""
+    r = _rng(22)
+    M, N, K = 9, 7, 96
+
+    def e4m3_pow2(k):
+        return ((k + 7) << 3) if k >= -6 else (1 << (k + 9))
+
+    ka = r.integers(-9, 9, (M, K // 16))
+    kw = r.integers(-9, 9, (N, K // 16))
+    aq = r.integers(0, 256, (M, K // 2)).astype(np.uint8)
+    wq = r.integers(0, 256, (N, K // 2)).astype(np.uint8)
+    ga = np.exp(r.uniform(-2, 2, M)).astype(np.float32)
+    gw = np.float32(3.0)
+    enc = np.vectorize(e4m3_pow2)
+    assert all(e4m3_value_ocp(e4m3_pow2(k)) == 2.0 ** k for k in range(-9, 9))
+    y_e4 = orc.gemm(aq, enc(ka).astype(np.uint8), ga, wq, enc(kw).astype(np.uint8), gw)
+    y_ue = orc.gemm_ue8m0(aq, (ka + 127).astype(np.uint8), ga, wq, (kw + 127).astype(np.uint8), gw)
+    assert np.allclose(y_ue, y_e4, rtol=1e-15, atol=1e-15 * np.abs(y_e4).max())
+
+
 def pin_silu_mul(orc):
     from scipy.special import expit
     r = _rng(9)
@@ -585,6 +641,66 @@ def pin_forward_stepwise(orc):
         assert np.allclose(res["y2"][sel], a2 @ w2.T, rtol=1e-12, atol=1e-12 * np.abs(res["y2"]).max())
 
 
+def pin_forward_stepwise_ue8m0(orc):
+    """The forward with UE8M0 block scales throughout: every scale byte of a1
+    and a2 is the smallest power of two at or above fl(fl(g*amax)/6), and each
+    GEMM stage matches an fp64 numpy matmul of operands decoded on the test
+    side (2^(b - 127) scales)."""
+    from scipy.special import expit
+    r = _rng(23)
+    E, H, I, T, k = 2, 64, 32, 8, 2
+    W = orc.Weights(E, H, I)
+    W.ue8m0 = True
+    for e in range(E):
+        for name, shape in (("w13", (2 * I, H)), ("w2", (H, I))):
+            wv = (r.standard_normal(shape) * 0.02).astype(np.float32)
+            q, sf, s2 = orc.quantize_weight((wv.view(np.uint32) >> 16).astype(np.uint16), ue8m0=True)
+            getattr(W, name + "_q")[e], getattr(W, name + "_sf")[e] = q, sf
+            getattr(W, name + "_scale2")[e] = s2
+    W.w13_input_scale = np.exp(r.uniform(-9, -6, E)).astype(np.float32)
+    W.w2_input_scale = np.exp(r.uniform(-9, -6, E)).astype(np.float32)
+    x = (r.standard_normal((T, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    ids = np.stack([r.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    w = r.uniform(0, 1, (T, k)).astype(np.float32)
+    res = orc.moe_forward(x, ids, w, W)
+    tab = np.array([E2M1[c] for c in range(16)])
+
+    def deq(q, sf, g):
+        codes = np.empty((q.shape[0], q.shape[1] * 2), np.int64)
+        codes[:, 0::2], codes[:, 1::2] = q & 15, q >> 4
+        return tab[codes] * np.repeat(np.exp2(sf.astype(np.float64) - 127), 16, axis=1) / np.float64(g)
+
+    def check_scales(vals, sf, g):
+        # vals [rows, K] FP32 values that were quantised with global scale g per row
+        for i in range(vals.shape[0]):
+            for b in range(sf.shape[1]):
+                amax = np.float32(np.abs(vals[i, 16 * b:16 * b + 16]).max())
+                t = np.float32(np.float32(np.float32(g[i]) * amax) / np.float32(6))
+                if t == 0:
+                    continue
+                s = 2.0 ** (int(sf[i, b]) - 127)
+                assert s >= t and s / 2 < t, (i, b, s, t)
+
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    g1 = np.float32(1) / W.w13_input_scale
+    g2 = np.float32(1) / W.w2_input_scale
+    rows = res["rows"]
+    re = res["row_expert"][rows]
+    check_scales(xf[res["perm"][rows] // k], res["sf1"], g1[re])
+    check_scales(res["h"], res["sf2"], g2[re])
+    for e in range(E):
+        sel = re == e
+        a1 = deq(res["a1q"][sel], res["sf1"][sel], g1[e])
+        w13 = deq(W.w13_q[e], W.w13_sf[e], np.float32(1) / W.w13_scale2[e])
+        y1 = a1 @ w13.T
+        gate, up = y1[:, :I], y1[:, I:]
+        assert np.allclose(res["h"][sel], (gate * expit(gate) * up).astype(np.float32), rtol=1e-6,
+                           atol=1e-6 * np.abs(res["h"][sel]).max())
+        a2 = deq(res["a2q"][sel], res["sf2"][sel], g2[e])
+        w2 = deq(W.w2_q[e], W.w2_sf[e], np.float32(1) / W.w2_scale2[e])
+        assert np.allclose(res["y2"][sel], a2 @ w2.T, rtol=1e-12, atol=1e-12 * np.abs(res["y2"]).max())
+
+
 # ---------------------------------------------------------------------------
 # validation, residual + RMSNorm
 # ---------------------------------------------------------------------------
@@ -632,4 +748,5 @@ ALL_PINS = [
     pin_e4m3_torch, pin_block_worked, pin_identity_2688, pin_block_invariances,
     pin_route_bruteforce, pin_gemm_fraction, pin_gemm_fp64, pin_silu_mul, pin_combine_special,
     pin_forward_stepwise, pin_validate, pin_rmsnorm, pin_router, pin_ue8m0, pin_w4a16,
+    pin_gemm_ue8m0_fraction, pin_gemm_ue8m0_matches_e4m3, pin_forward_stepwise_ue8m0,
 ]

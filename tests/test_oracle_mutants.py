@@ -40,6 +40,10 @@ MUTANTS = [
     ("w4a16_silu_sign", "double silu = gate / (1.0 + exp(-gate));", "double silu = gate / (1.0 + exp(gate));", 1),
     ("w4a16_sum_not_product", "bf16_nearest(silu * up)", "bf16_nearest(silu + up)", 0),
     ("router_not_renormalised", "(float)(p[ids[t * k + j]] / zk)", "(float)(p[ids[t * k + j]])", 0),
+    ("gemm_ue8m0_e4m3_decode", "orc_e2m1_value(code) * orc_ue8m0_value(sfb)", "orc_e2m1_value(code) * orc_e4m3_value(sfb)", 0),
+    ("gemm_ue8m0_block_index", "deq_ue8m0(code, c->asf[m * (K / 16) + kk / 16])",
+     "deq_ue8m0(code, c->asf[m * (K / 16) + kk / 32])", 0),
+    ("gemm_ue8m0_weight_scale_dropped", "((double)c->ga[m] * (double)c->gw)", "((double)c->ga[m])", 1),
 ]
 
 
