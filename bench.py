@@ -157,17 +157,19 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- workload
-def make_layer_device(layer, m, torch, seed: int):
-    """Device weights: N(0, 0.02) BF16 draws quantised on the device."""
+def make_layer_device(layer, m, torch, seed: int, ue8m0: bool = False):
+    """Device weights: N(0, 0.02) BF16 draws quantised on the device (UE8M0
+    block scales with ue8m0)."""
     E, H, I = layer.E, layer.H, layer.I
     gen = torch.Generator(device="cuda")
     gen.manual_seed(seed)
     w13 = (torch.randn((E, 2 * I, H), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
     w2 = (torch.randn((E, H, I), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
-    q13, sf13, s13 = m.quantize_weights(w13)
-    q2, sf2, s2 = m.quantize_weights(w2)
+    q13, sf13, s13 = m.quantize_weights(w13, ue8m0=ue8m0)
+    q2, sf2, s2 = m.quantize_weights(w2, ue8m0=ue8m0)
     in13 = torch.from_numpy(layer.w13_input_scale).cuda()
-    w = m.MoEWeights(E, H, I, q13, sf13, s13, in13, q2, sf2, s2, torch.ones(E, device="cuda"))
+    w = m.MoEWeights(E, H, I, q13, sf13, s13, in13, q2, sf2, s2, torch.ones(E, device="cuda"),
+                     sf_format=m.SF_UE8M0 if ue8m0 else m.SF_E4M3)
     return w, (w13, w2)
 
 
@@ -585,8 +587,38 @@ def ue8m0_leg(m, torch, args):
             m.quantize_experts(x, ids, scale, L.E, sf_layout=layout, ws=ws)
         torch.cuda.synchronize()
         res[name] = {"us_per_call": (time.perf_counter() - t0) / n * 1e6}
-    return {"workload": "4096 tokens x 2816, 128 experts, uniform top-8", "calls": res,
-            "note": "synchronous calls: scale check + token reorder + quantiser each"}
+    out = {"workload": "4096 tokens x 2816, 128 experts, uniform top-8", "calls": res,
+           "note": "synchronous calls: scale check + token reorder + quantiser each"}
+
+    # the prefill layer with UE8M0 block scales on the weights, a1 and a2
+    layer = S.prefill(args.tokens)
+    wu, bf = make_layer_device(layer, m, torch, seed=1003, ue8m0=True)
+    del bf
+    xl = torch.from_numpy(layer.x.view(np.int16)).cuda().view(torch.bfloat16)
+    idl = torch.from_numpy(layer.topk_ids).cuda()
+    twl = torch.from_numpy(layer.topk_w).cuda()
+    calibrate_w2_on_device(m, torch, wu, xl, idl, twl, layer)
+    outl = torch.empty((layer.T, layer.H), device="cuda")
+    wsl = torch.empty(m.moe_workspace_size(layer.T, layer.H, layer.I, layer.E, layer.k), dtype=torch.uint8,
+                      device="cuda")
+    m.moe_forward(wu, xl, idl, twl, out=outl, ws=wsl, flags=m.SYNC_CHECK)
+    for _ in range(5):
+        m.moe_forward(wu, xl, idl, twl, out=outl, ws=wsl, flags=m.SCALES_PREVALIDATED)
+    n = 50
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(n):
+        m.moe_forward(wu, xl, idl, twl, out=outl, ws=wsl, flags=m.SCALES_PREVALIDATED)
+    e.record()
+    torch.cuda.synchronize()
+    st, _ = m.moe_status(wsl)
+    ms = s.elapsed_time(e) / n
+    out["prefill_layer"] = {"T": layer.T, "ms_per_call": ms, "tokens_per_s": layer.T / (ms * 1e-3), "status": st,
+                            "note": "UE8M0 block scales throughout (weights, a1, a2), carried to the tensor "
+                                    "cores as E4M3 powers of two"}
+    del wu, outl, wsl
+    return out
 
 
 def router_leg(m, torch, args):

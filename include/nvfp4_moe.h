@@ -67,9 +67,13 @@ typedef enum {
     NVFP4_ERR_CUDA = 4,                /* a CUDA runtime / driver call failed */
     NVFP4_ERR_DEVICE_TIMEOUT = 5,      /* a bounded device-side wait expired */
     NVFP4_ERR_WORKSPACE_TOO_SMALL = 6, /* ws_bytes below the size query's answer */
+    NVFP4_ERR_SCALE_RANGE = 7,         /* NVFP4_UE8M0_SCALES: a block scale above 2^11 (see there) */
 } nvfp4_status;
 
 enum { NVFP4_SF_LINEAR = 0, NVFP4_SF_SWIZZLED = 1 };
+
+/* Block-scale format of a weight set (nvfp4_prepare_weights_format). */
+enum { NVFP4_SF_E4M3 = 0 };
 
 /* OR'ed into a quantiser's scale layout (or passed as sf_format): block scales
  * as UE8M0 bytes instead of E4M3 [page "Gemma 4 NVFP4 MoE 空输出", MoE section:
@@ -77,8 +81,8 @@ enum { NVFP4_SF_LINEAR = 0, NVFP4_SF_SWIZZLED = 1 };
  * two 2^(b - 127) (255 is NaN, never written).  The scale of a block is the
  * E4M3 path's t = fl(fl(g*amax)/6) rounded up to a power of two, clamped to
  * 2^-127 .. 2^127, so no element of the block saturates; the codes are then
- * e2m1(fl(fl(x*g)/s)) as in the E4M3 path.  The tensor-core GEMMs of
- * nvfp4_moe_forward take E4M3 block scales only. */
+ * e2m1(fl(fl(x*g)/s)) as in the E4M3 path.  nvfp4_moe_forward runs with
+ * UE8M0 block scales throughout under NVFP4_UE8M0_SCALES. */
 enum { NVFP4_SF_UE8M0 = 4 };
 
 /* Element type of the router's logits (nvfp4_router_topk). */
@@ -93,6 +97,22 @@ enum {
     /* Synchronise at the end of the call and report device-side errors
      * (a bad scale slot or an expired wait) in the return value. */
     NVFP4_SYNC_CHECK = 2u,
+    /* The UE8M0 variant [page "Gemma 4 NVFP4 MoE 空输出", MoE section: the
+     * quantiser's UE8M0_SF flag]: the weights carry UE8M0 block scales (from
+     * nvfp4_quantize_weights_format, prepared with nvfp4_prepare_weights_format
+     * and NVFP4_SF_UE8M0), and both activation quantisations take UE8M0 scales
+     * (see NVFP4_SF_UE8M0); every other step is unchanged.  The block-scaled
+     * FP4 tensor-core MMA is fed E4M3 scale bytes, so a UE8M0 scale 2^e travels
+     * as the E4M3 value 2^(e-3), exact for 2^-6 <= 2^e <= 2^11, and the GEMM
+     * output scales take the factor 2^3 of each operand back.  A block whose
+     * scale is below 2^-6 contributes zero (its values are below 6 * 2^-6 / g
+     * in magnitude).  An activation scale above 2^11 (values more than about
+     * 4.6 times the calibration amax) stops the call on the device with
+     * NVFP4_ERR_SCALE_RANGE; raised by the second quantisation, `out` may then
+     * hold zeros.  Weight scale bytes above 2^11 travel as NaN.  The prepared
+     * weights must match the flag (else NVFP4_ERR_INVALID_ARG on the device,
+     * nothing written).  Not accepted by nvfp4_moe_forward_w4a16. */
+    NVFP4_UE8M0_SCALES = 8u,
 };
 
 /* One-line description of the last error raised on the calling thread. */
@@ -213,6 +233,17 @@ typedef struct {
 size_t nvfp4_prepared_weights_size(int E, int H, int I);
 int nvfp4_prepare_weights(const nvfp4_moe_weights *w, void *prepared, size_t prepared_bytes,
                           nvfp4_stream_t stream);
+
+/*
+ * nvfp4_prepare_weights_format -- nvfp4_prepare_weights for weights whose
+ * block scales are in `format`: NVFP4_SF_E4M3 (as nvfp4_prepare_weights) or
+ * NVFP4_SF_UE8M0, whose bytes are converted to the E4M3 encoding the tensor
+ * cores take (see NVFP4_UE8M0_SCALES).  The last 256 bytes of `prepared` record
+ * the format; nvfp4_moe_forward checks it against its flags.  Any other
+ * format: NVFP4_ERR_INVALID_ARG.  Asynchronous.
+ */
+int nvfp4_prepare_weights_format(const nvfp4_moe_weights *w, void *prepared, size_t prepared_bytes, int format,
+                                 nvfp4_stream_t stream);
 
 /*
  * nvfp4_moe_forward -- the expert path of one MoE layer.

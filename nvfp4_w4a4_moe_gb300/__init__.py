@@ -18,11 +18,12 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libnvfp4moe.so")
 
 OK, ERR_INVALID_ARG, ERR_SCALE_INVALID, ERR_UNSUPPORTED_SHAPE, ERR_CUDA, ERR_DEVICE_TIMEOUT, \
-    ERR_WORKSPACE_TOO_SMALL = range(7)
+    ERR_WORKSPACE_TOO_SMALL, ERR_SCALE_RANGE = range(8)
 SF_LINEAR, SF_SWIZZLED = 0, 1
+SF_E4M3 = 0
 LOGITS_F32, LOGITS_BF16 = 0, 1
 SF_UE8M0 = 4
-SCALES_PREVALIDATED, SYNC_CHECK, DEBUG_KEEP_H = 1, 2, 4
+SCALES_PREVALIDATED, SYNC_CHECK, DEBUG_KEEP_H, UE8M0_SCALES = 1, 2, 4, 8
 
 _lib = None
 _lock = threading.Lock()
@@ -73,6 +74,7 @@ def load():
             "nvfp4_quantize_experts_static_scratch": (I, [P, I, I, P, I, I, P, P, P, I, P, P, P]),
             "nvfp4_prepared_weights_size": (SZ, [I, I, I]),
             "nvfp4_prepare_weights": (I, [P, P, SZ, P]),
+            "nvfp4_prepare_weights_format": (I, [P, P, SZ, I, P]),
             "nvfp4_moe_workspace_size": (SZ, [I, I, I, I, I]),
             "nvfp4_moe_forward": (I, [P, P, P, I, P, P, I, P, P, SZ, U, P]),
             "nvfp4_moe_forward_profiled": (I, [P, P, P, I, P, P, I, P, P, SZ, U, P, P]),
@@ -263,10 +265,15 @@ def quantize_experts_static_scratch(x: torch.Tensor, topk_ids: torch.Tensor, inp
 
 class MoEWeights:
     """Device tensors of one layer's NVFP4 expert weights (canonical layout,
-    see nvfp4_moe_weights in the C header) plus their prepared scale layout."""
+    see nvfp4_moe_weights in the C header) plus their prepared scale layout.
+    sf_format: the block scales of w13_sf / w2_sf, SF_E4M3 or SF_UE8M0 (the
+    UE8M0 variant: the forward then runs with UE8M0_SCALES)."""
 
     def __init__(self, E, H, I, w13_q, w13_sf, w13_scale2, w13_input_scale, w2_q, w2_sf, w2_scale2,
-                 w2_input_scale, w13_input_written=None, w2_input_written=None):
+                 w2_input_scale, w13_input_written=None, w2_input_written=None, sf_format=SF_E4M3):
+        if sf_format not in (SF_E4M3, SF_UE8M0):
+            raise Nvfp4Error(ERR_INVALID_ARG, f"unknown block-scale format {sf_format}")
+        self.sf_format = sf_format
         self.E, self.H, self.I = E, H, I
         self.w13_q, self.w13_sf, self.w13_scale2, self.w13_input_scale = w13_q, w13_sf, w13_scale2, w13_input_scale
         self.w2_q, self.w2_sf, self.w2_scale2, self.w2_input_scale = w2_q, w2_sf, w2_scale2, w2_input_scale
@@ -323,9 +330,13 @@ def prepare_weights(w: MoEWeights, stream=None) -> torch.Tensor:
     n = prepared_weights_size(w.E, w.H, w.I)
     prep = torch.empty(n, dtype=torch.uint8, device=w.w13_q.device)
     cw = w.cstruct()
-    _check(load().nvfp4_prepare_weights(ctypes.byref(cw), _ptr(prep), n, _stream(stream)))
+    _check(load().nvfp4_prepare_weights_format(ctypes.byref(cw), _ptr(prep), n, w.sf_format, _stream(stream)))
     w.prepared = prep
     return prep
+
+
+def _forward_flags(w: MoEWeights, flags: int) -> int:
+    return flags | (UE8M0_SCALES if w.sf_format == SF_UE8M0 else 0)
 
 
 def moe_workspace_size(T: int, H: int, I: int, E: int, k: int) -> int:
@@ -355,7 +366,8 @@ def moe_forward(w: MoEWeights, x: torch.Tensor, topk_ids: torch.Tensor, topk_wei
     _arg(w.prepared, "prepared weights", torch.uint8)
     cw = w.cstruct()
     _check(load().nvfp4_moe_forward(ctypes.byref(cw), _ptr(w.prepared), _ptr(x), T, _ptr(topk_ids),
-                                    _ptr(topk_weights), k, _ptr(out), _ptr(ws), ws.numel(), flags, _stream(stream)))
+                                    _ptr(topk_weights), k, _ptr(out), _ptr(ws), ws.numel(), _forward_flags(w, flags),
+                                    _stream(stream)))
     return out, ws
 
 
@@ -376,6 +388,8 @@ def moe_w4a16_workspace_size(T: int, H: int, I: int, E: int, k: int) -> int:
 def moe_forward_w4a16(w: MoEWeights, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
                       out: torch.Tensor | None = None, ws: torch.Tensor | None = None, flags: int = 0, stream=None):
     """out [T, H] f32 = the expert path with NVFP4 weights and BF16 activations."""
+    if w.sf_format != SF_E4M3:
+        raise Nvfp4Error(ERR_INVALID_ARG, "the W4A16 path takes E4M3 weight block scales only")
     w.check()
     T, k = _layer_args(w, x, topk_ids, topk_weights, out)
     H = w.H
@@ -428,8 +442,8 @@ def moe_forward_profiled(w: MoEWeights, x: torch.Tensor, topk_ids: torch.Tensor,
     arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     cw = w.cstruct()
     _check(load().nvfp4_moe_forward_profiled(ctypes.byref(cw), _ptr(w.prepared), _ptr(x), T, _ptr(topk_ids),
-                                             _ptr(topk_weights), k, _ptr(out), _ptr(ws), ws.numel(), flags,
-                                             _stream(stream), arr))
+                                             _ptr(topk_weights), k, _ptr(out), _ptr(ws), ws.numel(),
+                                             _forward_flags(w, flags), _stream(stream), arr))
     return out
 
 
@@ -450,8 +464,8 @@ def moe_forward_host(w: MoEWeights, x_host: torch.Tensor, topk_ids_host: torch.T
     _arg(w.prepared, "prepared weights", torch.uint8)
     cw = w.cstruct()
     _check(load().nvfp4_moe_forward_host(ctypes.byref(cw), _ptr(w.prepared), _ptr(x_host), T, _ptr(topk_ids_host),
-                                         _ptr(topk_weights_host), k, _ptr(out_host), _ptr(ws), ws.numel(), flags,
-                                         _stream(stream)))
+                                         _ptr(topk_weights_host), k, _ptr(out_host), _ptr(ws), ws.numel(),
+                                         _forward_flags(w, flags), _stream(stream)))
     return out_host, ws
 
 

@@ -183,6 +183,11 @@ static int header_status(const DevHeader &h, int *first_bad)
                     h.first_bad);
     if (h.status == 3 || (h.error_flags & kErrBadExpertId))
         return fail(NVFP4_ERR_INVALID_ARG, "an expert id is outside [0, E)");
+    if (h.status == 4)
+        return fail(NVFP4_ERR_INVALID_ARG, "the prepared weights were converted for the other block-scale format");
+    if (h.status == 6 || (h.error_flags & kErrUe8m0Range))
+        return fail(NVFP4_ERR_SCALE_RANGE, "a UE8M0 block scale is above 2^%d, the largest carried to the tensor cores",
+                    8 + kUe8m0Shift);
     if (h.status == 5 || (h.error_flags & (kErrTimeoutProducer | kErrTimeoutMma | kErrTimeoutEpilogue | kErrTimeoutRoute)))
         return fail(NVFP4_ERR_DEVICE_TIMEOUT, "a device-side wait expired (flags 0x%x)", h.error_flags);
     return NVFP4_OK;
@@ -362,10 +367,18 @@ int nvfp4_quantize_experts(const uint16_t *x, int T, int H, const int32_t *topk_
     return header_status(h, nullptr);
 }
 
+// The prepared buffer ends with a 256-byte slot whose first word names the
+// block-scale format the scales were converted from; the forward checks it.
+constexpr uint32_t kPrepTagE4M3 = 0xE4E4E4E4u, kPrepTagUE8M0 = 0x5E5E5E5Eu;
+static size_t prep_tag_offset(int E, int H, int I)
+{
+    return up256(prepared_w13_bytes(E, H, I)) + up256(prepared_w2_bytes(E, H, I));
+}
+
 size_t nvfp4_prepared_weights_size(int E, int H, int I)
 {
     if (E < 1 || H <= 0 || I <= 0) return 0;
-    return up256(prepared_w13_bytes(E, H, I)) + up256(prepared_w2_bytes(E, H, I));
+    return prep_tag_offset(E, H, I) + 256;
 }
 
 static int check_weights(const nvfp4_moe_weights *w)
@@ -381,6 +394,15 @@ static int check_weights(const nvfp4_moe_weights *w)
 
 int nvfp4_prepare_weights(const nvfp4_moe_weights *w, void *prepared, size_t prepared_bytes, nvfp4_stream_t stream)
 {
+    return nvfp4_prepare_weights_format(w, prepared, prepared_bytes, NVFP4_SF_E4M3, stream);
+}
+
+int nvfp4_prepare_weights_format(const nvfp4_moe_weights *w, void *prepared, size_t prepared_bytes, int format,
+                                 nvfp4_stream_t stream)
+{
+    if (format != NVFP4_SF_E4M3 && format != NVFP4_SF_UE8M0)
+        return fail(NVFP4_ERR_INVALID_ARG, "prepare: unknown block-scale format %d", format);
+    const int ue = format == NVFP4_SF_UE8M0;
     int rc = check_weights(w);
     if (rc) return rc;
     rc = check_layer_shape(w->E, w->H, w->I, 1);
@@ -391,11 +413,13 @@ int nvfp4_prepare_weights(const nvfp4_moe_weights *w, void *prepared, size_t pre
         return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "prepared buffer %zu < %zu", prepared_bytes, need);
     cudaStream_t st = (cudaStream_t)stream;
     uint8_t *base = static_cast<uint8_t *>(prepared);
-    PrepArgs a13 = {w->w13_sf, base, w->E, 2 * w->I, w->H, 4 * ((w->H + 255) / 256), w->I};
+    PrepArgs a13 = {w->w13_sf, base, w->E, 2 * w->I, w->H, 4 * ((w->H + 255) / 256), w->I, ue};
     NV_CUDA(launch_prep_sf(a13, st), "launching the w13 scale conversion");
     PrepArgs a2 = {w->w2_sf, base + up256(prepared_w13_bytes(w->E, w->H, w->I)), w->E, w->H, w->I,
-                   4 * ((w->I + 255) / 256), 0};
+                   4 * ((w->I + 255) / 256), 0, ue};
     NV_CUDA(launch_prep_sf(a2, st), "launching the w2 scale conversion");
+    NV_CUDA(cudaMemsetAsync(base + prep_tag_offset(w->E, w->H, w->I), ue ? 0x5E : 0xE4, 4, st),
+            "writing the format word");
     return NVFP4_OK;
 }
 
@@ -434,6 +458,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     const WsLayout L = make_layout(T, H, I, E, k);
     if (ws_bytes < L.end) return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu", ws_bytes, L.end);
     const bool keep_h = (flags & NVFP4_DEBUG_KEEP_H) != 0;
+    const bool ue = (flags & NVFP4_UE8M0_SCALES) != 0;
     if (keep_h && ws_bytes < L.host_end + (size_t)L.rows_cap * I * sizeof(float))
         return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "NVFP4_DEBUG_KEEP_H needs the host workspace size + rows_cap*I*4");
     if (T == 0) return NVFP4_OK;
@@ -457,6 +482,10 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     va.narrays = 4;
     va.alpha1 = alpha1;
     va.alpha2 = alpha2;
+    va.alpha_pow2 = ue ? (float)(1 << (2 * kUe8m0Shift)) : 1.0f;  // both operands' scales were divided
+    va.prep_tag = reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(prepared) +
+                                                     prep_tag_offset(E, H, I));
+    va.prep_tag_want = ue ? kPrepTagUE8M0 : kPrepTagE4M3;
     va.hdr = hdr;
     const int R = T * k;
     RouteArgs ra;
@@ -508,7 +537,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     qa.sf = base + L.sf1;
     qa.sf_swizzled = 1;
     qa.sf_kc = L.kc1;
-    qa.sf_ue8m0 = 0;  // the tensor-core GEMM takes E4M3 block scales
+    qa.sf_ue8m0 = ue ? 2 : 0;  // the tensor cores take E4M3 bytes: UE8M0 scales travel as E4M3 powers of two
     qa.hdr = hdr;
     NV_CUDA(launch_quant_experts(qa, st), "launching the a1 quantiser");
     NV_CUDA(mark(3), "recording an event");
@@ -537,6 +566,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     ga.I = I;
     ga.kc2 = L.kc2;
     ga.h_dump = keep_h ? reinterpret_cast<float *>(base + L.host_end) : nullptr;
+    ga.ue8m0 = ue ? 1 : 0;
     ga.zero_out = out;  // cleared by the w13 kernel for the w2 kernel's reductions
     ga.zero_floats = (long long)T * H;
     ga.k = k;
@@ -828,6 +858,8 @@ int nvfp4_moe_forward_w4a16(const nvfp4_moe_weights *w, const void *prepared, co
     if (rc) return rc;
     const int E = w->E, H = w->H, I = w->I;
     if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "T=%d < 0", T);
+    if (flags & NVFP4_UE8M0_SCALES)
+        return fail(NVFP4_ERR_INVALID_ARG, "w4a16 forward: UE8M0 weight scales are not supported");
     if ((long long)T * k >= (1ll << 31) / 2) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "T*k too large");
     if (!prepared || !ws || (T > 0 && (!x || !topk_ids || !topk_weights || !out)))
         return fail(NVFP4_ERR_INVALID_ARG, "w4a16 forward: null pointer");

@@ -36,7 +36,8 @@ constexpr float kFltMax = 3.40282346638528859812e+38f;
 
 // Device-side status block at the start of every workspace.
 struct DevHeader {
-    int status;          // 0 = ok, 2 = a scale slot failed validation, 3 = bad expert id, 5 = device timeout
+    int status;          // 0 = ok, 2 = a scale slot failed validation, 3 = bad expert id, 4 = prepared weights in
+                         // the other scale format, 5 = device timeout, 6 = a UE8M0 scale above the carried range
     int bad_count;       // number of bad scale slots
     int first_bad;       // lowest bad slot index (INT_MAX when none)
     int error_flags;     // kErr* bits below
@@ -52,6 +53,7 @@ enum : int {
     kErrTimeoutMma = 4,
     kErrTimeoutEpilogue = 8,
     kErrTimeoutRoute = 16,
+    kErrUe8m0Range = 32,
 };
 
 // RN, saturating FP32 -> E4M3 (t >= 0): the byte of the second source.
@@ -151,6 +153,63 @@ __device__ __forceinline__ uint2 quant_block16(const f32x2 (&x)[8], float amax, 
     }
     sf_byte = sb;
     return make_uint2(e2m1_rn_sat8(q[0], q[1], q[2], q[3]), e2m1_rn_sat8(q[4], q[5], q[6], q[7]));
+}
+
+// UE8M0 block scales.
+// UE8M0 block scale of t >= 0 (t from the same fl(fl(g*amax)/6) as the E4M3
+// path): the byte of the smallest power of two at or above t, clamped to the
+// finite range 2^-127 .. 2^127 (bytes 0 .. 254).  Read off t's exponent field:
+// a zero mantissa means t is itself a power of two.
+__device__ __forceinline__ uint32_t ue8m0_round_up(float t)
+{
+    const uint32_t b = __float_as_uint(t);
+    const uint32_t e = b >> 23, m = b & 0x7FFFFFu;
+    if (e == 0) return m > 0x400000u ? 1u : 0u;  // subnormal t: 2^-127 covers up to 0x400000 * 2^-149
+    const uint32_t c = e + (m != 0u ? 1u : 0u);
+    return c > 254u ? 254u : c;                // also t = inf (e = 255)
+}
+
+// 1 / value(byte) = 2^(127 - byte), exact: a normal float for bytes 0 .. 253,
+// the subnormal 2^-127 for byte 254.
+__device__ __forceinline__ float ue8m0_reciprocal(uint32_t byte)
+{
+    return __uint_as_float(byte == 254u ? 0x00400000u : (254u - byte) << 23);
+}
+
+// quant_block16 with a UE8M0 block scale: the scale is t rounded up to a power
+// of two, so fl(fl(x*g) / s) is one exact product by 1/s, rounded once.
+__device__ __forceinline__ uint2 quant_block16_ue8m0(const f32x2 (&x)[8], float amax, float g, uint32_t &sf_byte)
+{
+    // fl(ga / 6) by the IEEE division: unlike the E4M3 path, the result matters
+    // down to FP32 subnormals here
+    const float t = __fdiv_rn(__fmul_rn(g, amax), 6.0f);
+    const uint32_t sb = ue8m0_round_up(t);
+    const float r = ue8m0_reciprocal(sb);
+    const f32x2 gg = pack_f32x2(g, g), rr = pack_f32x2(r, r);
+    f32x2 q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = mul_f32x2(mul_f32x2(x[i], gg), rr);
+    sf_byte = sb;
+    return make_uint2(e2m1_rn_sat8(q[0], q[1], q[2], q[3]), e2m1_rn_sat8(q[4], q[5], q[6], q[7]));
+}
+
+// UE8M0 scales carried to the tensor cores.  The block-scaled FP4 MMA is
+// given E4M3 scale bytes; a UE8M0 scale 2^(b-127) travels as the E4M3
+// encoding of 2^(b-127-kUe8m0Shift), exact while that lies in E4M3's powers of
+// two 2^-9 .. 2^8, and the GEMM's output scale takes 2^kUe8m0Shift per
+// operand back.  With the shift of 3 the scales 2^-6 .. 2^11 travel exactly.
+// A smaller scale gives 0: such a block lies below 2^-6 * 6 / g in magnitude.
+// A larger one cannot travel: kUe8m0TooLarge (an E4M3 NaN) is returned, and
+// the caller reports it.
+constexpr int kUe8m0Shift = 3;
+constexpr uint32_t kUe8m0TooLarge = 0x7Fu;
+__device__ __forceinline__ uint32_t e4m3_of_ue8m0(uint32_t b)
+{
+    const int k = (int)b - 127 - kUe8m0Shift;
+    if (k > 8) return kUe8m0TooLarge;
+    if (k >= -6) return (uint32_t)(k + 7) << 3;  // normal: exponent field k + 7, mantissa 0
+    if (k >= -9) return 1u << (k + 9);           // subnormal: mantissa 2^(k+9) x 2^-9
+    return 0u;
 }
 
 // Programmatic dependent launch.  A kernel launched with launch_pdl may be

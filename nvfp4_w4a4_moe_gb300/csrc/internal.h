@@ -35,6 +35,9 @@ struct ValidateArgs {
     float *recip[4];  // FP32 reciprocal of each slot (nullable per array)
     int E, narrays;
     float *alpha1, *alpha2;  // 1/(g_a * g_w) per expert (forward only; nullable)
+    float alpha_pow2;        // power of two the alphas are multiplied by (0 means 1)
+    const uint32_t *prep_tag;  // format word of the prepared weights (nullable)
+    uint32_t prep_tag_want;    // the value it must hold, else status 4
     DevHeader *hdr;
 };
 cudaError_t launch_validate(const ValidateArgs &a, cudaStream_t st);
@@ -64,8 +67,8 @@ struct QuantArgs {
     uint8_t *q;
     uint8_t *sf;
     int sf_swizzled, sf_kc;
-    int sf_ue8m0;  // block scales as UE8M0 powers of two (else E4M3)
-    const DevHeader *hdr;
+    int sf_ue8m0;  // 0: E4M3 block scales; 1: UE8M0 bytes; 2: UE8M0 carried as E4M3 (e4m3_of_ue8m0)
+    DevHeader *hdr;  // read for the status; mode 2 writes a range error into it
 };
 cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st);
 
@@ -74,6 +77,7 @@ struct PrepArgs {
     uint8_t *out;       // [E][N/128 blocks][kc][512]; w13 blocks of one tile interleaved per K step
     int E, N, K, kc;
     int gate_up_I;      // w13: I > 0 (blocks of 128 gate rows and 128 up rows; a 64 + 64 tail block)
+    int ue8m0;          // the canonical bytes are UE8M0: written carried as E4M3 (e4m3_of_ue8m0)
 };
 cudaError_t launch_prep_sf(const PrepArgs &a, cudaStream_t st);
 
@@ -101,6 +105,7 @@ struct GemmArgs {
     uint8_t *a2q, *sf2;
     int I, kc2;
     float *h_dump;
+    int ue8m0;        // w13 kernel: a2 takes UE8M0 block scales, carried as E4M3 (e4m3_of_ue8m0)
     float *zero_out;  // w13 kernel: [T, H] FP32 output cleared for the w2 kernel's reductions (nullable)
     long long zero_floats;
     // w2 epilogue (weighted combine)

@@ -155,7 +155,9 @@ __device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, 
 }
 
 // ---------------------------------------------------------------- kernel
-template <int EPI>  // 0: w13 (SiLU*up + requantise), 1: w2 (weighted combine)
+// EPI 0: w13 (SiLU*up + requantise), 1: w2 (weighted combine).  UE (w13):
+// the requantisation takes UE8M0 block scales, carried as E4M3.
+template <int EPI, bool UE>
 __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const GemmArgs p, const DivTable tab_in)
@@ -504,7 +506,18 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                                                 hi_f32(h[b][2 * i + 1]));
                     }
                     uint32_t sb;
-                    const uint2 pk = quant_block16(h[b], amax, g2, &tab, sb);
+                    uint2 pk;
+                    if (UE) {
+                        pk = quant_block16_ue8m0(h[b], amax, g2, sb);
+                        sb = e4m3_of_ue8m0(sb);
+                        if (sb == kUe8m0TooLarge && valid) {
+                            // the w2 kernel finds the status and does not run
+                            atomicOr(&p.hdr->error_flags, kErrUe8m0Range);
+                            p.hdr->status = 6;
+                        }
+                    } else {
+                        pk = quant_block16(h[b], amax, g2, &tab, sb);
+                    }
                     if (valid) *reinterpret_cast<uint2 *>(p.a2q + (size_t)row * (p.I >> 1) + (hcol >> 1)) = pk;
                     sfw |= sb << (8 * b);
                 }
@@ -586,7 +599,7 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t row
     return make_tensor_map_2d(m, base, row_bytes, rows, 128, box_rows, true);
 }
 
-template <int EPI>
+template <int EPI, bool UE>
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
 {
     // function attributes are per device: set once on each
@@ -596,7 +609,7 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
     if (aerr != cudaSuccess) return aerr;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        aerr = cudaFuncSetAttribute(moe_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        aerr = cudaFuncSetAttribute(moe_gemm_kernel<EPI, UE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Plan<EPI>::SMEM_BYTES);
         if (aerr != cudaSuccess) return aerr;
         attr_set[dev] = true;
@@ -610,7 +623,7 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
     const long long tiles = (long long)a.mtiles_cap * nt;
     int grid = sm_count();
     if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
-    const cudaError_t err = launch_pdl(moe_gemm_kernel<EPI>, dim3(grid), dim3(Plan<EPI>::NUM_THREADS),
+    const cudaError_t err = launch_pdl(moe_gemm_kernel<EPI, UE>, dim3(grid), dim3(Plan<EPI>::NUM_THREADS),
                                        Plan<EPI>::SMEM_BYTES, st, ma, mb, a, div_table());
     return err != cudaSuccess ? err : cudaGetLastError();
 }
@@ -660,7 +673,10 @@ bool make_tensor_map_2d(CUtensorMap *m, const void *base, uint64_t row_bytes, ui
     return true;
 }
 
-cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st) { return launch_gemm<0>(a, st); }
-cudaError_t launch_gemm_w2(const GemmArgs &a, cudaStream_t st) { return launch_gemm<1>(a, st); }
+cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st)
+{
+    return a.ue8m0 ? launch_gemm<0, true>(a, st) : launch_gemm<0, false>(a, st);
+}
+cudaError_t launch_gemm_w2(const GemmArgs &a, cudaStream_t st) { return launch_gemm<1, false>(a, st); }
 
 }  // namespace nvfp4

@@ -47,16 +47,20 @@ __device__ __forceinline__ void validate_body(const ValidateArgs &a)
     __syncthreads();
     // GEMM output scale 1/(g_a * g_w) per expert [page, §NVFP4 runtime-order
     // figure: the GEMM's scaling takes in both FP32 global scales].
+    // With UE8M0 scales carried as E4M3 (each operand's scales divided by
+    // 2^kUe8m0Shift) the alphas take that power of two back: an exact product.
     if (a.alpha1 && a.narrays == 4) {
+        const float ap = a.alpha_pow2 > 0.0f ? a.alpha_pow2 : 1.0f;
         for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
-            a.alpha1[e] = __frcp_rn(__fmul_rn(s_recip[0][e], s_recip[2][e]));
-            a.alpha2[e] = __frcp_rn(__fmul_rn(s_recip[1][e], s_recip[3][e]));
+            a.alpha1[e] = __fmul_rn(__frcp_rn(__fmul_rn(s_recip[0][e], s_recip[2][e])), ap);
+            a.alpha2[e] = __fmul_rn(__frcp_rn(__fmul_rn(s_recip[1][e], s_recip[3][e])), ap);
         }
     }
     if (threadIdx.x == 0) {
+        const bool tag_bad = a.prep_tag && *a.prep_tag != a.prep_tag_want;
         a.hdr->bad_count = s_bad;
         a.hdr->first_bad = s_first;
-        a.hdr->status = s_bad ? 2 : 0;
+        a.hdr->status = s_bad ? 2 : tag_bad ? 4 : 0;
         a.hdr->error_flags = 0;
         a.hdr->num_mtiles = 0;
         a.hdr->done_count = 0u;
@@ -344,44 +348,6 @@ __global__ void __launch_bounds__(kRouteThreads) validate_route_kernel(ValidateA
     route_body(a);
 }
 
-// ------------------------------------------------------------------ UE8M0 block scales
-// UE8M0 block scale of t >= 0 (t from the same fl(fl(g*amax)/6) as the E4M3
-// path): the byte of the smallest power of two at or above t, clamped to the
-// finite range 2^-127 .. 2^127 (bytes 0 .. 254).  Read off t's exponent field:
-// a zero mantissa means t is itself a power of two.
-__device__ __forceinline__ uint32_t ue8m0_round_up(float t)
-{
-    const uint32_t b = __float_as_uint(t);
-    const uint32_t e = b >> 23, m = b & 0x7FFFFFu;
-    if (e == 0) return m > 0x400000u ? 1u : 0u;  // subnormal t: 2^-127 covers up to 0x400000 * 2^-149
-    const uint32_t c = e + (m != 0u ? 1u : 0u);
-    return c > 254u ? 254u : c;                // also t = inf (e = 255)
-}
-
-// 1 / value(byte) = 2^(127 - byte), exact: a normal float for bytes 0 .. 253,
-// the subnormal 2^-127 for byte 254.
-__device__ __forceinline__ float ue8m0_reciprocal(uint32_t byte)
-{
-    return __uint_as_float(byte == 254u ? 0x00400000u : (254u - byte) << 23);
-}
-
-// quant_block16 with a UE8M0 block scale: the scale is t rounded up to a power
-// of two, so fl(fl(x*g) / s) is one exact product by 1/s, rounded once.
-__device__ __forceinline__ uint2 quant_block16_ue8m0(const f32x2 (&x)[8], float amax, float g, uint32_t &sf_byte)
-{
-    // fl(ga / 6) by the IEEE division: unlike the E4M3 path, the result matters
-    // down to FP32 subnormals here
-    const float t = __fdiv_rn(__fmul_rn(g, amax), 6.0f);
-    const uint32_t sb = ue8m0_round_up(t);
-    const float r = ue8m0_reciprocal(sb);
-    const f32x2 gg = pack_f32x2(g, g), rr = pack_f32x2(r, r);
-    f32x2 q[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = mul_f32x2(mul_f32x2(x[i], gg), rr);
-    sf_byte = sb;
-    return make_uint2(e2m1_rn_sat8(q[0], q[1], q[2], q[3]), e2m1_rn_sat8(q[4], q[5], q[6], q[7]));
-}
-
 // ------------------------------------------------------------------ quantiser
 // [page, §NVFP4 runtime-order figure; MoE section: SFScale[expert_idx]]:
 // one warp per (token, 1024-element chunk), each lane two consecutive
@@ -412,8 +378,9 @@ __device__ __forceinline__ float amax16_bf16(const uint32_t *w)
 constexpr int kQuantThreads = 128;  // 5 CTAs (20 warps) per SM at <= 96 registers
 
 // SWZ: scales in the swizzled tensor-core layout (else linear [rows, H/16]);
-// UE: UE8M0 block scales (else E4M3).
-template <bool SWZ, bool UE>
+// SF: block scales E4M3 (0), UE8M0 bytes (1), or UE8M0 carried as E4M3
+// powers of two for the tensor cores (2, see e4m3_of_ue8m0).
+template <bool SWZ, int SF>
 __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantArgs a, DivTable tab_in)
 {
     __shared__ DivTable2 tab;
@@ -482,8 +449,17 @@ __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantAr
             const float g = __shfl_sync(0xffffffffu, my_g, j);
             if (active) {
                 uint32_t s0, s1;
-                const uint2 p0 = UE ? quant_block16_ue8m0(x0, amax0, g, s0) : quant_block16(x0, amax0, g, &tab, s0);
-                const uint2 p1 = UE ? quant_block16_ue8m0(x1, amax1, g, s1) : quant_block16(x1, amax1, g, &tab, s1);
+                const uint2 p0 = SF ? quant_block16_ue8m0(x0, amax0, g, s0) : quant_block16(x0, amax0, g, &tab, s0);
+                const uint2 p1 = SF ? quant_block16_ue8m0(x1, amax1, g, s1) : quant_block16(x1, amax1, g, &tab, s1);
+                if (SF == 2) {
+                    s0 = e4m3_of_ue8m0(s0);
+                    s1 = e4m3_of_ue8m0(s1);
+                    if (s0 == kUe8m0TooLarge || s1 == kUe8m0TooLarge) {
+                        // the GEMMs find the status and do not run
+                        atomicOr(&a.hdr->error_flags, kErrUe8m0Range);
+                        a.hdr->status = 6;
+                    }
+                }
                 q16[qo] = make_uint4(p0.x, p0.y, p1.x, p1.y);
                 *reinterpret_cast<uint16_t *>(a.sf + so) = (uint16_t)(s0 | (s1 << 8));
             }
@@ -541,7 +517,7 @@ __global__ void __launch_bounds__(256) prep_sf_kernel(PrepArgs a)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int col = 4 * c + j;
-            if (col < nsf) word |= (uint32_t)src[col] << (8 * j);
+            if (col < nsf) word |= (a.ue8m0 ? e4m3_of_ue8m0(src[col]) : (uint32_t)src[col]) << (8 * j);
         }
         uint8_t *dst = a.out + (size_t)e * NT * a.kc * 512 + blk_off + (size_t)(v & 31) * 16 + (v >> 5) * 4;
         *reinterpret_cast<uint32_t *>(dst) = word;
@@ -740,10 +716,12 @@ cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st)
         return launch_pdl(kernel, dim3((int)grid, (int)ysplit), dim3(kQuantThreads), 0, st, a, div_table());
     };
     cudaError_t err;
-    if (a.sf_ue8m0)
-        err = a.sf_swizzled ? launch(quant_experts_kernel<true, true>) : launch(quant_experts_kernel<false, true>);
+    if (a.sf_ue8m0 == 2)
+        err = a.sf_swizzled ? launch(quant_experts_kernel<true, 2>) : cudaErrorInvalidValue;
+    else if (a.sf_ue8m0)
+        err = a.sf_swizzled ? launch(quant_experts_kernel<true, 1>) : launch(quant_experts_kernel<false, 1>);
     else
-        err = a.sf_swizzled ? launch(quant_experts_kernel<true, false>) : launch(quant_experts_kernel<false, false>);
+        err = a.sf_swizzled ? launch(quant_experts_kernel<true, 0>) : launch(quant_experts_kernel<false, 0>);
     return err != cudaSuccess ? err : cudaGetLastError();
 }
 

@@ -50,11 +50,12 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str = ""):
 
 
 @functools.lru_cache(maxsize=4)
-def oracle_weights(name: str, seed: int, E: int, H: int, I: int):
-    """Oracle-quantised expert weights of a synthetic layer (cached by seed)."""
+def oracle_weights(name: str, seed: int, E: int, H: int, I: int, ue8m0: bool = False):
+    """Oracle-quantised expert weights of a synthetic layer (cached by seed);
+    UE8M0 block scales with ue8m0."""
     layer = S.Layer(name, E, H, I, 0, 1, seed, np.zeros((0, H), np.uint16), np.zeros((0, 1), np.int32),
                     np.zeros((0, 1), np.float32))
-    return oracle.quantize_layer_weights(layer)
+    return oracle.quantize_layer_weights(layer, ue8m0=ue8m0)
 
 
 def calibrate_w2(layer: S.Layer, W: oracle.Weights, max_rows: int | None = None) -> np.ndarray:
@@ -75,8 +76,10 @@ def calibrate_w2(layer: S.Layer, W: oracle.Weights, max_rows: int | None = None)
             continue
         if max_rows is not None and len(rows) > max_rows:
             rows = np.sort(rng.choice(rows, max_rows, replace=False))
-        q, sf = oracle.quant_rows(xf[rows // k], np.full(len(rows), g1[e], np.float32))
-        h = oracle.silu_mul(oracle.gemm(q, sf, g1[e], W.w13_q[e], W.w13_sf[e], gw13[e]))
+        ue = bool(getattr(W, "ue8m0", False))
+        q, sf = oracle.quant_rows(xf[rows // k], np.full(len(rows), g1[e], np.float32), ue8m0=ue)
+        mm = oracle.gemm_ue8m0 if ue else oracle.gemm
+        h = oracle.silu_mul(mm(q, sf, g1[e], W.w13_q[e], W.w13_sf[e], gw13[e]))
         amax[e] = np.abs(h).max()
         got[e] = True
     fallback = amax[got].max() if got.any() else np.float32(1.0)
@@ -88,13 +91,16 @@ def device_weights(W: oracle.Weights, w13_in=None, w2_in=None):
     import nvfp4_w4a4_moe_gb300 as m
     return m.MoEWeights(W.E, W.H, W.I, dev(W.w13_q), dev(W.w13_sf), dev(W.w13_scale2),
                         dev(W.w13_input_scale if w13_in is None else w13_in), dev(W.w2_q), dev(W.w2_sf),
-                        dev(W.w2_scale2), dev(W.w2_input_scale if w2_in is None else w2_in))
+                        dev(W.w2_scale2), dev(W.w2_input_scale if w2_in is None else w2_in),
+                        sf_format=m.SF_UE8M0 if getattr(W, "ue8m0", False) else m.SF_E4M3)
 
 
-def layer_with_weights(layer: S.Layer, max_rows: int | None = None):
-    """(layer, oracle weights with the layer's calibrated input scales)."""
-    base = oracle_weights(layer.name.split("_T")[0], layer.seed, layer.E, layer.H, layer.I)
+def layer_with_weights(layer: S.Layer, max_rows: int | None = None, ue8m0: bool = False):
+    """(layer, oracle weights with the layer's calibrated input scales); the
+    whole layer takes UE8M0 block scales with ue8m0."""
+    base = oracle_weights(layer.name.split("_T")[0], layer.seed, layer.E, layer.H, layer.I, ue8m0)
     W = oracle.Weights(layer.E, layer.H, layer.I)
+    W.ue8m0 = ue8m0
     for f in ("w13_q", "w13_sf", "w13_scale2", "w2_q", "w2_sf", "w2_scale2"):
         setattr(W, f, getattr(base, f))
     W.w13_input_scale = layer.w13_input_scale.copy()

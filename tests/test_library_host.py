@@ -58,7 +58,8 @@ def test_workspace_sizes(lib):
     R = 8192 * k
     assert m.intermediates_rows_cap(8192, E, k) >= R + E * 127
     assert m.intermediates_rows_cap(1, E, k) == 8 * 128
-    assert m.prepared_weights_size(E, H, I) == E * 11 * 44 * 512 + E * 22 * 12 * 512
+    # the two scale sets in the tensor-core layout, then a 256-byte slot for the format word
+    assert m.prepared_weights_size(E, H, I) == E * 11 * 44 * 512 + E * 22 * 12 * 512 + 256
     assert m.quantize_workspace_size(4096, 8, 128) > 0
     assert m.moe_workspace_size(-1, H, I, E, k) == 0
 
@@ -140,6 +141,13 @@ def test_w4a16_and_format_argument_errors_need_no_gpu(lib):
     # activation quantiser: a layout with an unknown bit
     assert lib.nvfp4_quantize_experts(P(256), 4, 256, P(256), 2, 4, P(256), P(256), P(256), 2 | m.SF_UE8M0,
                                       P(256), P(256), P(256), 1 << 20, None) == m.ERR_INVALID_ARG
+    # weight preparation: unknown scale format; the W4A16 path refuses the UE8M0 variant
+    assert lib.nvfp4_prepare_weights_format(None, P(256), 1 << 30, 3, None) == m.ERR_INVALID_ARG
+    assert b"format" in lib.nvfp4_last_error_string()
+    w = m._Weights(E, H, I, *([P(256)] * 10))
+    assert lib.nvfp4_moe_forward_w4a16(ctypes.byref(w), P(256), P(256), 0, P(256), P(256), k, P(256), P(256),
+                                       1 << 30, m.UE8M0_SCALES, None) == m.ERR_INVALID_ARG
+    assert b"UE8M0" in lib.nvfp4_last_error_string()
 
 
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
