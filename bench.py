@@ -721,7 +721,16 @@ def oracle_sample_setup(n_tokens: int):
 
 
 def cpu_baseline(args):
-    orc, layer, W, toks = oracle_sample_setup(args.cpu_tokens)
+    """The oracle on the first tokens of the prefill workload, as many as take
+    about args.cpu_seconds of CPU work.  The sample is sized from a run on
+    args.cpu_tokens tokens: each expert a sample touches costs a fixed weight
+    decoding, so a much smaller calibration would understate the rate."""
+    orc, layer, W, toks = oracle_sample_setup(8192)  # every token of the prefill layer
+    n0 = min(len(toks), args.cpu_tokens)
+    t0 = time.perf_counter()
+    orc.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W, tokens=toks[:n0])
+    rate = n0 / (time.perf_counter() - t0)
+    toks = toks[:int(min(len(toks), max(n0, rate * args.cpu_seconds)))]
     t0 = time.perf_counter()
     orc.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W, tokens=toks)
     dt = time.perf_counter() - t0
@@ -768,7 +777,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--cpu-tokens", type=int, default=1024)  # reference arm: largest token sample per step
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)  # cpu_baseline: CPU work to time
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=8192,
                     help="prefill tokens (8192 is the benchmark workload; smaller values for ncu captures)")
