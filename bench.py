@@ -778,7 +778,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-tokens", type=int, default=1024)  # reference arm: largest token sample per step
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)  # cpu_baseline: CPU work to time
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)  # cpu_baseline: CPU work to time
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=8192,
                     help="prefill tokens (8192 is the benchmark workload; smaller values for ncu captures)")

@@ -436,6 +436,19 @@ int nvfp4_quantize_weights_format(const uint16_t *w, int count, int N, int K, in
  */
 long long nvfp4_selftest_block_division(int nthreads);
 
+/*
+ * nvfp4_selftest_device_wait -- the failure path of the device-side waits,
+ * run on purpose.  One small kernel waits on a barrier that nothing arrives
+ * on: one thread gives up after limit_us microseconds (1 .. 10^6), a second,
+ * with a ten times longer limit, gives up as soon as the first raises the
+ * CTA's abort flag.  They record the expiry in the status block at the start
+ * of `ws` (device, 256-byte aligned, at least 256 bytes) as the GEMM kernels
+ * do, so nvfp4_moe_status(ws) then returns NVFP4_ERR_DEVICE_TIMEOUT and the
+ * context stays usable.  Asynchronous; NVFP4_ERR_INVALID_ARG for a bad ws or
+ * limit.
+ */
+int nvfp4_selftest_device_wait(void *ws, size_t ws_bytes, unsigned limit_us, nvfp4_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -93,6 +93,7 @@ def load():
             "nvfp4_quantize_weights": (I, [P, I, I, I, P, P, P, P, SZ, P]),
             "nvfp4_quantize_weights_format": (I, [P, I, I, I, I, P, P, P, P, SZ, P]),
             "nvfp4_selftest_block_division": (ctypes.c_longlong, [I]),
+            "nvfp4_selftest_device_wait": (I, [P, SZ, U, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -185,6 +186,15 @@ def version() -> int:
 
 def selftest_block_division(nthreads: int = 0) -> int:
     return int(load().nvfp4_selftest_block_division(nthreads))
+
+
+def selftest_device_wait(ws: torch.Tensor | None = None, limit_us: int = 2000, stream=None) -> torch.Tensor:
+    """Run a kernel whose bounded waits expire on purpose; afterwards
+    moe_status(ws) reports ERR_DEVICE_TIMEOUT.  Returns ws."""
+    ws = _empty_ws(256, torch.device("cuda", torch.cuda.current_device())) if ws is None else ws
+    _ws_arg(ws)
+    _check(load().nvfp4_selftest_device_wait(_ptr(ws), ws.numel(), int(limit_us), _stream(stream)))
+    return ws
 
 
 # ---------------------------------------------------------------------------

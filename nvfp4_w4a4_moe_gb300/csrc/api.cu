@@ -249,6 +249,19 @@ int nvfp4_version(void) { return 100; }
 
 long long nvfp4_selftest_block_division(int nthreads) { return selftest_division(nthreads); }
 
+int nvfp4_selftest_device_wait(void *ws, size_t ws_bytes, unsigned limit_us, nvfp4_stream_t stream)
+{
+    if (!ws || !aligned(ws, 256) || ws_bytes < sizeof(DevHeader))
+        return fail(NVFP4_ERR_INVALID_ARG, "selftest: workspace null, misaligned or below 256 bytes");
+    if (limit_us == 0 || limit_us > 1000000u)
+        return fail(NVFP4_ERR_INVALID_ARG, "selftest: limit %u us outside [1, 10^6]", limit_us);
+    cudaStream_t st = (cudaStream_t)stream;
+    NV_CUDA(cudaMemsetAsync(ws, 0, sizeof(DevHeader), st), "clearing the status block");
+    NV_CUDA(launch_wait_selftest(static_cast<DevHeader *>(ws), (uint64_t)limit_us * 1000u, st),
+            "launching the wait self-test");
+    return NVFP4_OK;
+}
+
 int nvfp4_validate_scales(const float *scales, const uint8_t *written, int n, void *ws, nvfp4_stream_t stream,
                           int *bad_count_host, int *first_bad_host)
 {

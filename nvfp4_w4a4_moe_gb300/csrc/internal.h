@@ -83,6 +83,8 @@ cudaError_t launch_prep_sf(const PrepArgs &a, cudaStream_t st);
 
 cudaError_t launch_rmsnorm(const uint16_t *x, const float *out, int T, int H, float eps, uint16_t *xn,
                            cudaStream_t st);
+// A kernel whose bounded waits run out by design (status 5 in hdr).
+cudaError_t launch_wait_selftest(DevHeader *hdr, uint64_t limit_ns, cudaStream_t st);
 
 // Router: softmax / top-k / renormalise over logits [T, E] (FP32, or BF16 when bf16 != 0).
 cudaError_t launch_router_topk(const void *logits, int bf16, int T, int E, int k, int32_t *ids, float *w,

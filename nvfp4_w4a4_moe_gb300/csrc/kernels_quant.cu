@@ -8,6 +8,7 @@
 #include <cfloat>
 
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace nvfp4 {
 namespace {
@@ -524,6 +525,34 @@ __global__ void __launch_bounds__(256) prep_sf_kernel(PrepArgs a)
     }
 }
 
+// ------------------------------------------------------------------ bounded waits
+// The waits of the tensor-core kernels, made to run out: thread 0 waits on an
+// mbarrier that nothing arrives on and gives up after limit_ns; thread 32
+// waits on the same barrier with a limit ten times longer and gives up when
+// thread 0 raises the CTA's abort flag.  Both record what happened in the
+// status block as the GEMM kernels do (status 5 and their error bits).
+__global__ void wait_selftest_kernel(DevHeader *hdr, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    volatile int *abort_v = &abort_flag;
+    if (threadIdx.x == 0) {
+        if (!tc::mbar_wait(&bar, 0, nullptr, limit_ns)) {
+            *abort_v = 1;
+            atomicOr(&hdr->error_flags, kErrTimeoutMma);
+            hdr->status = 5;
+        }
+    } else if (threadIdx.x == 32) {
+        if (!tc::mbar_wait(&bar, 0, abort_v, 10 * limit_ns)) atomicOr(&hdr->error_flags, kErrTimeoutEpilogue);
+    }
+}
+
 // ------------------------------------------------------------------ residual + RMSNorm
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t *x, const float *out, int H, float eps,
                                                        uint16_t *xn)
@@ -729,6 +758,12 @@ cudaError_t launch_prep_sf(const PrepArgs &a, cudaStream_t st)
 {
     const long long work = (long long)a.E * (a.N / 128) * a.kc * 128;
     prep_sf_kernel<<<grid_for(work, 256, 16), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(DevHeader *hdr, uint64_t limit_ns, cudaStream_t st)
+{
+    wait_selftest_kernel<<<1, 64, 0, st>>>(hdr, limit_ns);
     return cudaGetLastError();
 }
 

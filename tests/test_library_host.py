@@ -148,6 +148,12 @@ def test_w4a16_and_format_argument_errors_need_no_gpu(lib):
     assert lib.nvfp4_moe_forward_w4a16(ctypes.byref(w), P(256), P(256), 0, P(256), P(256), k, P(256), P(256),
                                        1 << 30, m.UE8M0_SCALES, None) == m.ERR_INVALID_ARG
     assert b"UE8M0" in lib.nvfp4_last_error_string()
+    # the device-wait self-test: bad workspace or limit
+    assert lib.nvfp4_selftest_device_wait(None, 256, 1000, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_selftest_device_wait(P(264), 256, 1000, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_selftest_device_wait(P(256), 128, 1000, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_selftest_device_wait(P(256), 256, 0, None) == m.ERR_INVALID_ARG
+    assert lib.nvfp4_selftest_device_wait(P(256), 256, 2000000, None) == m.ERR_INVALID_ARG
 
 
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
