@@ -46,7 +46,11 @@ constexpr int SF_TILE = 512;                 // one 128x4-scale tile: 128 rows x
 constexpr int SFA_BYTES = 4 * SF_TILE;       // 256 K per stage
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_SCALE_WARPS = 4;  // one per TMEM lane quarter
-constexpr int XPOSE_LD = 33;  // padded row of the per-warp 32 x 32 transpose buffer
+// Row of the per-warp 32 x 32 transpose buffer: 32 floats in eight 16-byte
+// chunks, logical chunk j of row r stored at chunk j ^ (r & 7).  A row written
+// by one lane and four rows read by 8 lanes each are then 128-bit accesses
+// that take the minimum four wavefronts.
+constexpr int XPOSE_LD = 32;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 
@@ -58,7 +62,10 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 //       releases it before computing; a 4-stage ring of 54 KB stages.
 //       Eight epilogue warps, two per TMEM lane quarter.
 //  w2:  tiles of 128 x 128, M128 N128 MMAs into two alternating accumulators,
-//       a 4-stage ring, and sixteen epilogue warps in two groups of eight that
+//       a 4-stage ring of B and scales, A in three slots of its own (one per
+//       256-K stage) filled once per pair of tiles that share the m-tile (two
+//       adjacent output column blocks, run back to back), and sixteen
+//       epilogue warps in two groups of eight that
 //       take alternate tiles (one accumulator each), so one group is issuing
 //       the combine's reductions while the other waits on TMEM and fetches
 //       its rows' tokens and weights; each warp has a transpose buffer.
@@ -73,15 +80,25 @@ struct Plan {
     static constexpr int NUM_THREADS = 64 + EPI_THREADS + 32 * NUM_SCALE_WARPS;
     static constexpr int ACC_BUFS = EPI == 0 ? 1 : 2;
     static constexpr int B_BYTES = BN * BK / 2;
+    // w2: A lives in a ring of slots of its own, outside the B ring, so that a
+    // tile pair (two column blocks of one m-tile) loads it once.  Fill f (one
+    // 256-K stage of one m-tile) takes slot f % A_SLOTS and completes on the
+    // B ring stage it is issued with.  No barrier of its own is needed: before
+    // fill f + A_SLOTS is issued the producer has waited for the MMAs of a ring
+    // stage at or after the last one reading fill f (checked for every K depth
+    // a pair can have, 1 .. A_SLOTS stages, and for unpaired tiles).
+    static constexpr int A_SLOTS = EPI == 1 ? 5 : 0;
+    static constexpr int RING_A_BYTES = EPI == 1 ? 0 : A_BYTES;
     static constexpr int SFB_BYTES = (BN / 128) * 4 * SF_TILE;
     static constexpr int SFB_STEP = BN / 32;               // TMEM columns per 64-K step of B scales
     static constexpr int SF_COLS = 16 + 4 * SFB_STEP;      // TMEM scale columns per stage
     static constexpr int SF_TMEM_COL = ACC_BUFS * BN;      // scale slots after the accumulator(s)
     static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_B = OFF_A + STAGES * RING_A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr int OFF_AS = OFF_SFB + STAGES * SFB_BYTES;  // the A slots (w2)
+    static constexpr int OFF_BAR = OFF_AS + A_SLOTS * A_BYTES;
     static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_XPOSE = (OFF_MISC + 16 + 15) & ~15;
@@ -89,6 +106,8 @@ struct Plan {
     static constexpr int SMEM_BYTES = OFF_XPOSE + XPOSE_BYTES + 1024;  // + alignment slack
     static_assert(SF_TMEM_COL + STAGES * SF_COLS <= TMEM_COLS, "scale slots exceed TMEM");
     static_assert(EPI_GROUPS == ACC_BUFS, "each epilogue group owns one accumulator");
+    static_assert(OFF_B % 1024 == 0 && OFF_AS % 1024 == 0, "128-byte-swizzled operands start on 1024 bytes");
+    static_assert(EPI == 0 || (A_SLOTS == 5 && STAGES == 4), "the A-slot reuse argument is for 5 slots, 4 stages");
     static_assert(SMEM_BYTES + (EPI == 0 ? (int)sizeof(DivTable2) : 0) <= 232448,
                   "shared memory plan exceeds the opt-in limit");
 };
@@ -154,6 +173,28 @@ __device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, 
     return ti;
 }
 
+// The CTA's i-th tile.  w13, and w2 when a tile pair does not fit the A
+// slots: tile blockIdx + i * gridDim of tile_info's order.  w2 paired: units
+// (m-tile, pair of adjacent output column blocks) in column-pair-major order,
+// unit (i/2) * gridDim + blockIdx, column block 2 * pair + (i & 1); the two
+// tiles of a unit run back to back and share the A operand.
+template <int EPI>
+__device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int NT, int MT, bool paired)
+{
+    if (EPI == 1 && paired) {
+        const int u = (i >> 1) * (int)gridDim.x + (int)blockIdx.x;
+        const int g = u / MT;
+        TileInfo<EPI> ti;
+        ti.mt = u - g * MT;
+        ti.nt = 2 * g + (i & 1);
+        ti.e = p.tile_expert[ti.mt];
+        ti.hc = 0;
+        ti.nblk = 1;
+        return ti;
+    }
+    return tile_info<EPI>(p, (int)blockIdx.x + i * (int)gridDim.x, NT, MT);
+}
+
 // ---------------------------------------------------------------- kernel
 // EPI 0: w13 (SiLU*up + requantise), 1: w2 (weighted combine).  UE (w13):
 // the requantisation takes UE8M0 block scales, carried as E4M3.
@@ -215,14 +256,23 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
     const int NT = EPI == 0 ? (p.gate_up_I + 127) / 128 : p.N / 128;
     const int MT = p.hdr->num_mtiles;
     const int ntiles = MT * NT;
-    if (p.hdr->status != 0 || (int)blockIdx.x >= ntiles) {
+    const int KT = (p.K + BK - 1) / BK;
+    const int G = (int)gridDim.x, b = (int)blockIdx.x;
+    // w2: tile pairs share A when all of a tile's A stages fit the slots, and
+    // when pairing (units of two tiles) adds at most 1/32 to the busiest CTA's
+    // tile count: with few tiles per CTA, as in decode, that tail costs more
+    // than the A loads it saves
+    const int per_cta = (ntiles + G - 1) / G, per_cta_paired = 2 * ((MT * (NT / 2) + G - 1) / G);
+    const bool paired = EPI == 1 && KT <= P::A_SLOTS && NT % 2 == 0 && per_cta_paired * 32 <= per_cta * 33;
+    const int nunits = paired ? MT * (NT / 2) : ntiles;
+    const int n_i = nunits > b ? ((nunits - b + G - 1) / G) * (paired ? 2 : 1) : 0;  // this CTA's tiles
+    if (p.hdr->status != 0 || n_i == 0) {
         // nothing to do (same decision in every thread): give TMEM back
         if (warp == 1)
             asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot), "r"(TMEM_COLS)
                          : "memory");
         return;
     }
-    const int KT = (p.K + BK - 1) / BK;
 
     const uint32_t tmem = *tmem_slot;
 
@@ -233,23 +283,29 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         uint32_t last_parity = 0;      // bit s: parity of that last load's phase
         bool ok = true;
         const size_t b_sf_expert = (size_t)(p.N / 128) * p.b_kc * SF_TILE;  // prepared scale bytes per expert
-        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT, MT);
+        for (int i = 0; i < n_i && ok; ++i) {
+            const TileInfo<EPI> ti = seq_tile<EPI>(p, i, NT, MT, paired);
+            const bool fill_a = !paired || (i & 1) == 0;  // w2: the first tile of a pair brings A
             const uint8_t *b_sf = p.b_sf + (size_t)ti.e * b_sf_expert +
                                   (size_t)(EPI == 0 ? 2 * ti.nt : ti.nt) * p.b_kc * SF_TILE;
             const uint32_t b_bytes = EPI == 0 ? (uint32_t)ti.hc * 2 * (BK / 2) : (uint32_t)B_BYTES;
             const uint32_t sfb_bytes = (uint32_t)ti.nblk * 4 * SF_TILE;
             for (int kt = 0; kt < KT; ++kt) {
+                const int kx = kt * (BK / 2);
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 uint64_t *fb = &full[stage];
-                mbar_expect_tx(fb, A_BYTES + b_bytes + SFA_BYTES + sfb_bytes);
-                const int kx = kt * (BK / 2);
-                uint8_t *sa = smem + OFF_A + stage * A_BYTES;
+                const bool a_now = EPI == 0 || fill_a;
+                mbar_expect_tx(fb, (a_now ? A_BYTES : 0u) + b_bytes + SFA_BYTES + sfb_bytes);
                 uint8_t *sb = smem + OFF_B + stage * B_BYTES;
-                tma_2d(sa, &tmap_a, kx, ti.mt * BM, fb);
+                if constexpr (EPI == 0) {
+                    tma_2d(smem + OFF_A + stage * A_BYTES, &tmap_a, kx, ti.mt * BM, fb);
+                } else if (fill_a) {
+                    const int f = (paired ? (i >> 1) : i) * KT + kt;  // A fill f goes to slot f % A_SLOTS
+                    tma_2d(smem + P::OFF_AS + (f % P::A_SLOTS) * A_BYTES, &tmap_a, kx, ti.mt * BM, fb);
+                }
                 if (EPI == 0) {
                     // hc gate rows, then the hc matching up rows, in 64-row boxes
                     const int gate = ti.e * 2 * p.gate_up_I + 128 * ti.nt;
@@ -287,11 +343,13 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         // and a full stage's four MMAs are unrolled.
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool ok = true;
-        const uint64_t da0 = desc_sw128(su32(smem + OFF_A)), db0 = desc_sw128(su32(smem + OFF_B));
+        const uint64_t da0 = desc_sw128(su32(smem + (EPI == 1 ? P::OFF_AS : OFF_A))),
+                       db0 = desc_sw128(su32(smem + OFF_B));
         const uint32_t sf0 = tmem + SF_TMEM_COL;
         const int k_full = p.K / BK;  // stages with four 64-K steps
-        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            const int nt = tile % NT;
+
+        for (int i = 0; i < n_i && ok; ++i) {
+            const int nt = (b + i * G) % NT;  // w13: the tile's width (w2 takes N128 throughout)
             const uint32_t idesc = idesc_for(EPI == 0 ? 2 * min(128, p.gate_up_I - 128 * nt) : 128);
             if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
                 ok = false;
@@ -307,7 +365,11 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint64_t da = da0 + (uint64_t)(stage * (A_BYTES >> 4));
+                // w2: the A fill this stage reads (landed with this tile's, or
+                // for the second of a pair the first's, ring stage)
+                int sl = stage;
+                if constexpr (EPI == 1) sl = ((paired ? (i >> 1) : i) * KT + kt) % P::A_SLOTS;
+                const uint64_t da = da0 + (uint64_t)(sl * (A_BYTES >> 4));
                 const uint64_t db = db0 + (uint64_t)(stage * (B_BYTES >> 4));
                 const uint32_t sfa = sf0 + stage * SF_COLS, sfb = sfa + 16;
                 if (kt < k_full) {
@@ -356,8 +418,8 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         uint32_t stage = 0, phase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT, MT);
+        for (int i = 0; i < n_i && ok; ++i) {
+            const TileInfo<EPI> ti = seq_tile<EPI>(p, i, NT, MT, paired);
             for (int kt = 0; kt < KT; ++kt) {
                 if (!mbar_wait(&full[stage], phase, abort_flag, kWaitLimitNs)) {
                     ok = false;
@@ -425,15 +487,15 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
             const long long n4 = p.zero_floats >> 2;
             const long long active = min((long long)gridDim.x, (long long)ntiles);
             const long long per_cta = (n4 + active - 1) / active;
-            const long long my_tiles = (ntiles - (long long)blockIdx.x + gridDim.x - 1) / gridDim.x;
+            const long long my_tiles = n_i;
             z_next = min(n4, (long long)blockIdx.x * per_cta);
             z_end = min(n4, z_next + per_cta);
             z_slice = (per_cta + my_tiles - 1) / my_tiles;
         }
-        for (int tile = blockIdx.x + group * gridDim.x; tile < ntiles; tile += EPI_GROUPS * gridDim.x) {
+        for (int i = group; i < n_i; i += EPI_GROUPS) {
             // everything the tile needs besides the accumulator is fetched
             // before waiting for it
-            const TileInfo<EPI> ti = tile_info<EPI>(p, tile, NT, MT);
+            const TileInfo<EPI> ti = seq_tile<EPI>(p, i, NT, MT, paired);
             const int e = ti.e, nt = ti.nt;
             const int row = ti.mt * BM + r_in;
             bool valid;
@@ -553,18 +615,22 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                         tc_fence_before();
                         mbar_arrive(&acc_empty[acc]);
                     }
+                    float4 *xrow = reinterpret_cast<float4 *>(xp + lane * XPOSE_LD);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) xp[lane * XPOSE_LD + i] = v[i] * scale;
+                    for (int j = 0; j < 8; ++j)
+                        xrow[j ^ (lane & 7)] = make_float4(v[4 * j] * scale, v[4 * j + 1] * scale,
+                                                           v[4 * j + 2] * scale, v[4 * j + 3] * scale);
                     __syncwarp();
 #pragma unroll
                     for (int it = 0; it < 8; ++it) {
                         const int rr = it * 4 + sub;
                         const int t_r = __shfl_sync(0xffffffffu, t, rr);
                         const int ok_r = __shfl_sync(0xffffffffu, (int)valid, rr);
-                        const float *src = xp + rr * XPOSE_LD + cc;
+                        const float4 src =
+                            reinterpret_cast<const float4 *>(xp + rr * XPOSE_LD)[(lane & 7) ^ (rr & 7)];
                         if (ok_r)
-                            red_add_v4(p.out + (size_t)t_r * p.H + nt * 128 + cbase + cc, src[0], src[1], src[2],
-                                       src[3]);
+                            red_add_v4(p.out + (size_t)t_r * p.H + nt * 128 + cbase + cc, src.x, src.y, src.z,
+                                       src.w);
                     }
                     __syncwarp();
                 }

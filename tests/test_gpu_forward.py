@@ -74,6 +74,17 @@ def test_decode_layer(m, T):
     check_layer(m, layer, W)
 
 
+@pytest.mark.parametrize("I", [1280, 1536])
+def test_long_intermediate(m, I):
+    """The w2 GEMM's K is I.  With 5 stages of 256 a tile pair's A fills every
+    A slot; with 6 the A slots are a plain ring refilled for every tile.  Enough
+    m-tiles that each CTA runs several pairs, so the slots wrap around."""
+    layer, W = layer_with_weights(S._softmax_layer(f"wideI{I}", seed=1010, E=8, H=2816, I=I, T=512, k=8),
+                                  max_rows=16)
+    tokens = np.sort(np.random.default_rng([layer.seed, 4]).choice(layer.T, 12, replace=False))
+    check_layer(m, layer, W, tokens=tokens)
+
+
 @pytest.fixture(scope="module")
 def prefill(m):
     return layer_with_weights(S.prefill(), max_rows=32)
