@@ -14,7 +14,8 @@
 // Kernel shape (one persistent CTA per SM):
 //   warp 0     TMA producer: per 256-K stage the A tile (128 rows, 128-byte
 //              swizzle), the B tile, and the 128x4-scale tiles of both (plain
-//              bulk copies) into a 4-stage ring.
+//              bulk copies) into a 4-stage ring; for w2 the A tile goes to a
+//              ring of five slots of its own, once per pair of tiles.
 //   warp 1     TMEM owner (512 columns) and MMA issuer: per stage, 4 x
 //              tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (K64):
 //              M128 N256 into one accumulator (w13), M128 N128 into one of two
