@@ -74,6 +74,14 @@ def test_decode_layer(m, T):
     check_layer(m, layer, W)
 
 
+def test_most_experts_and_top_k(m):
+    """E = 1024 and k = 32, the largest the library takes: 2560 routed rows in
+    two routing chunks (the cooperative launch with the largest shared-memory
+    plan), about a thousand m-tiles of one to a few rows each."""
+    layer, W = layer_with_weights(S._softmax_layer("maxEk", seed=1011, E=1024, H=256, I=128, T=80, k=32))
+    check_layer(m, layer, W)
+
+
 @pytest.mark.parametrize("I", [1280, 1536])
 def test_long_intermediate(m, I):
     """The w2 GEMM's K is I.  With 5 stages of 256 a tile pair's A fills every
