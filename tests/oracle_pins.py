@@ -702,6 +702,115 @@ def pin_forward_stepwise_ue8m0(orc):
 
 
 # ---------------------------------------------------------------------------
+# composition: routed rows in permuted order, token subsets
+# ---------------------------------------------------------------------------
+
+def _order_by_sort(ids):
+    """The permuted order by brute force: flat routed rows f = t*k + j sorted
+    by (expert, f) (the page's reorder by expert; stable within an expert)."""
+    flat = np.asarray(ids).ravel()
+    return sorted(range(flat.size), key=lambda f: (int(flat[f]), f))
+
+
+def _row_by_blocks(orc, xrow, g, ue8m0=False):
+    """One row quantised block by block with the pinned single-block routine,
+    codes packed two per byte, element 2i in the low nibble."""
+    H = xrow.size
+    q = np.zeros(H // 2, np.uint8)
+    sf = np.zeros(H // 16, np.uint8)
+    for b in range(H // 16):
+        sb, codes = orc.quant_block16(xrow[16 * b:16 * b + 16], g, ue8m0=ue8m0)
+        sf[b] = sb
+        c = np.asarray(codes, np.uint8)
+        q[8 * b:8 * b + 8] = c[0::2] | (c[1::2] << 4)
+    return q, sf
+
+
+def _ragged_routing(r, T, k, E, skip=()):
+    """Distinct experts per token, some experts left empty (ragged groups)."""
+    allowed = np.array([e for e in range(E) if e not in skip])
+    return np.stack([r.choice(allowed, k, replace=False) for _ in range(T)]).astype(np.int32)
+
+
+def pin_quantize_experts_rows(orc):
+    """Routed-row quantisation: permuted row p is token perm[p] // k
+    quantised with the global scale fl(1/input_scale[e]) of the expert e that
+    row belongs to (page "Gemma 4 NVFP4 MoE 空输出", MoE section: the expert
+    index selects SFScale; §矩阵融合 "MoE FFN": rows reordered by expert).
+    The permutation, each row's token and each row's scale are recomputed
+    here from the routing alone; T, k are chosen so that f % k and f // k
+    differ for most rows."""
+    r = _rng(31)
+    for ue in (False, True):
+        for T, k, E, skip in ((7, 3, 5, (2,)), (11, 2, 6, (0, 4)), (3, 1, 2, ())):
+            H = 48
+            x = (r.standard_normal((T, H)).astype(np.float32) * np.float32(3)).view(np.uint32)
+            x = (x >> 16).astype(np.uint16)
+            # one token made large so a wrong token shows in every scale byte
+            x[T // 2] = ((x[T // 2].astype(np.uint32) << 16).view(np.float32) * np.float32(64)).view(np.uint32) >> 16
+            ids = _ragged_routing(r, T, k, E, skip)
+            scales = np.exp(r.uniform(-4, 2, E)).astype(np.float32)
+            q, sf, offsets, perm = orc.quantize_experts(x, ids, scales, E, ue8m0=ue)
+            order = _order_by_sort(ids)
+            assert list(perm) == order
+            flat = ids.ravel()
+            assert list(offsets) == [0] + list(np.cumsum(np.bincount(flat, minlength=E)))
+            xf = (x.astype(np.uint32) << 16).view(np.float32)
+            for p, f in enumerate(order):
+                e = int(flat[f])
+                g = np.float32(np.float32(1.0) / scales[e])
+                wq, wsf = _row_by_blocks(orc, xf[f // k], g, ue8m0=ue)
+                assert np.array_equal(q[p], wq), (ue, T, k, p)
+                assert np.array_equal(sf[p], wsf), (ue, T, k, p)
+
+
+def pin_forward_token_subset(orc):
+    """The forward restricted to a token subset S (a test-size device of the
+    oracle: the full-size checks compute sampled tokens only).  Restoring the
+    token order and summing with the routing weights (page "Gemma 4 NVFP4 MoE
+    空输出", §矩阵融合 pipeline figure) is per token, so out on S must equal
+    the full run's out on S exactly and be 0 elsewhere; the computed rows must
+    be exactly the permuted rows whose token is in S, each intermediate row
+    equal to the full run's row; and the a1 codes of every row must be its
+    token's row quantised with its expert's scale."""
+    r = _rng(32)
+    E, H, I, T, k = 4, 32, 16, 9, 3
+    W = _small_weights(orc, r, E, H, I)
+    x = (r.standard_normal((T, H)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    ids = _ragged_routing(r, T, k, E)
+    w = r.uniform(0.1, 1, (T, k)).astype(np.float32)
+    full = orc.moe_forward(x, ids, w, W)
+    order = _order_by_sort(ids)
+    assert list(full["perm"]) == order
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    g1 = (np.float32(1) / W.w13_input_scale).astype(np.float32)
+    flat = ids.ravel()
+    for p, f in enumerate(order):
+        wq, wsf = _row_by_blocks(orc, xf[f // k], g1[flat[f]])
+        assert np.array_equal(full["a1q"][p], wq) and np.array_equal(full["sf1"][p], wsf), p
+    for S in ([0], [T - 1, 2], [1, 4, 5, 8], list(range(T))):
+        sub = orc.moe_forward(x, ids, w, W, tokens=S)
+        want_rows = [p for p, f in enumerate(order) if f // k in S]
+        assert list(sub["rows"]) == want_rows, S
+        keep = np.zeros(T, bool)
+        keep[S] = True
+        assert np.array_equal(sub["out"][keep], full["out"][keep]), S
+        assert not sub["out"][~keep].any(), S
+        for name in ("a1q", "sf1", "h", "a2q", "sf2", "y2"):
+            assert np.array_equal(sub[name], full[name][want_rows]), (S, name)
+    # the W4A16 forward's subset path, likewise
+    full16 = orc.moe_forward_w4a16(x, ids, w, W)
+    for S in ([3], [0, 7, 8]):
+        sub = orc.moe_forward_w4a16(x, ids, w, W, tokens=S)
+        want_rows = [p for p, f in enumerate(order) if f // k in S]
+        assert list(sub["rows"]) == want_rows, S
+        keep = np.zeros(T, bool)
+        keep[S] = True
+        assert np.array_equal(sub["out"][keep], full16["out"][keep]) and not sub["out"][~keep].any(), S
+        assert np.array_equal(sub["h"], full16["h"][want_rows]), S
+
+
+# ---------------------------------------------------------------------------
 # validation, residual + RMSNorm
 # ---------------------------------------------------------------------------
 
@@ -749,4 +858,5 @@ ALL_PINS = [
     pin_route_bruteforce, pin_gemm_fraction, pin_gemm_fp64, pin_silu_mul, pin_combine_special,
     pin_forward_stepwise, pin_validate, pin_rmsnorm, pin_router, pin_ue8m0, pin_w4a16,
     pin_gemm_ue8m0_fraction, pin_gemm_ue8m0_matches_e4m3, pin_forward_stepwise_ue8m0,
+    pin_quantize_experts_rows, pin_forward_token_subset,
 ]

@@ -1,8 +1,10 @@
-"""Plant a plausible mistake in a copy of the C oracle and check that at least
-one pin fails on it.  The mistakes are planted on the CPU, in a temporary build
-of the oracle; the real oracle is untouched."""
+"""Plant a plausible mistake in a copy of the oracle and check that at least
+one pin fails on it.  The mistakes are planted on the CPU: in a temporary build
+of the C oracle, or in a copy of the Python module that composes its steps,
+loaded under another name; the real oracle is untouched."""
 import os
 import subprocess
+import types
 
 import pytest
 
@@ -10,6 +12,7 @@ from oracle_pins import ALL_PINS
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "nvfp4_oracle.c")
+PY_SRC = os.path.join(ROOT, "oracle", "__init__.py")
 
 # (name, text in the oracle source, replacement, which occurrence (0-based))
 MUTANTS = [
@@ -73,3 +76,49 @@ def test_mutant_is_caught(orc, tmp_path, name, old, new, which):
             except Exception:  # an AssertionError, or a crash of the broken maths
                 failed.append(pin.__name__)
     assert failed, f"no pin caught mutant {name}"
+
+
+# Mistakes in the composition (oracle/__init__.py): which token a permuted row
+# reads, which expert's scale it takes, which rows a token subset keeps.
+PY_MUTANTS = [
+    ("quantize_experts_token_mod_k", "q, sf = quant_rows(xf[perm // k], g[row_e]", "q, sf = quant_rows(xf[perm % k], g[row_e]", 0),
+    ("quantize_experts_unpermuted_expert", "q, sf = quant_rows(xf[perm // k], g[row_e]",
+     "q, sf = quant_rows(xf[perm // k], g[np.asarray(topk_ids).reshape(-1)]", 0),
+    ("quantize_experts_unpermuted_token", "q, sf = quant_rows(xf[perm // k], g[row_e]",
+     "q, sf = quant_rows(xf[np.arange(T * k) // k], g[row_e]", 0),
+    ("forward_subset_filter_mod_k", "rows = np.nonzero(keep[perm // k])[0]", "rows = np.nonzero(keep[perm % k])[0]", 0),
+    ("forward_subset_unpermuted", "rows = np.nonzero(keep[perm // k])[0]", "rows = np.nonzero(keep[np.arange(T * k) // k])[0]", 0),
+    ("forward_row_token_unpermuted", "a1q, sf1 = quant_rows(xf[perm[rows] // k]", "a1q, sf1 = quant_rows(xf[rows // k]", 0),
+    ("w4a16_subset_filter_mod_k", "rows = np.nonzero(keep[perm // k])[0]", "rows = np.nonzero(keep[perm % k])[0]", 1),
+]
+
+
+def _load_module_copy(text):
+    mod = types.ModuleType("oracle_mutant")
+    mod.__file__ = PY_SRC  # the copy builds and loads the same C library
+    exec(compile(text, PY_SRC, "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name,old,new,which", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_composition_mutant_is_caught(orc, name, old, new, which):
+    with open(PY_SRC, encoding="utf-8") as f:
+        src = f.read()
+    mutated = _mutate(src, old, new, which)
+    assert mutated != src
+    mod = _load_module_copy(mutated)
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(mod)
+        except Exception:
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught mutant {name}"
+
+
+def test_unmutated_module_copy_passes(orc):
+    """The loader itself changes nothing: the unmodified copy passes every pin."""
+    with open(PY_SRC, encoding="utf-8") as f:
+        mod = _load_module_copy(f.read())
+    for pin in ALL_PINS:
+        pin(mod)
