@@ -45,8 +45,8 @@ FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor ratio on GB300
 LAUNCHES_PER_STEP = 5
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the two GEMM kernels
-# on the 8192-token prefill layer, from one ncu capture (profiles/moe_gemm_prefill8192_dram.md).
-# It holds for the kernel source it was taken on: any change to these files makes it null.
+# on the 8192-token prefill layer, from one ncu capture of the two GEMM kernels with those two
+# counters.  It holds for the kernel source it was taken on: any change to these files makes it null.
 NCU_TRAFFIC = {
     "tokens": 8192,
     "source_sha1": {"nvfp4_w4a4_moe_gb300/csrc/kernels_gemm.cu": "c26dea127f6426c3cbc207b3ab3b917d13fc377c",

@@ -182,7 +182,14 @@ int nvfp4_quantize_experts(const uint16_t *x, int T, int H, const int32_t *topk_
  * cudaMalloc, cudaFree or other allocating routine on this path.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The cached address belongs
+ *     to the device's primary context: after cudaDeviceReset on a device that
+ *     has called this entry point, the process must not call it again on that
+ *     device (the library's module, and the array, would be reloaded at
+ *     another address).
+ *   - Shapes the workspace entry point refuses are refused here with the
+ *     same status (NVFP4_ERR_UNSUPPORTED_SHAPE); only the size limit above
+ *     is particular to this entry point.
  *   - Every call on a device shares the one array, which keeps the last
  *     call's contents (each call resets what it needs).  Calls whose work
  *     overlaps on the GPU -- e.g. from two host threads or on two streams --

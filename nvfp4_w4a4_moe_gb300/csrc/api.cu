@@ -1,6 +1,7 @@
 // C ABI of libnvfp4moe: argument checks, workspace layout and the launch
 // sequence of the NVFP4 MoE expert path.  Declared in include/nvfp4_moe.h.
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -159,6 +160,17 @@ static bool quant_offsets_fit(long long rows, int H)
     return ((rows + 127) / 128) * kc * 512 < (1ll << 32);
 }
 
+int quantize_shape_status(int T, int H, int k, int E)
+{
+    if (E < 1 || E > 1024 || k < 1 || k > 32 || k > E || T < 0)
+        return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "quantize: E=%d k=%d T=%d unsupported", E, k, T);
+    if (H <= 0 || H % 64 != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "quantize: H=%d is not a multiple of 64", H);
+    if (!quant_offsets_fit((long long)T * k, H))
+        return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "quantize: T*k*H/16 = %lld scale bytes exceed 2^32",
+                    (long long)T * k * (H / 16));
+    return NVFP4_OK;
+}
+
 static int check_layer_shape(int E, int H, int I, int k)
 {
     if (E < 1 || E > 1024) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "E=%d outside [1, 1024]", E);
@@ -288,7 +300,7 @@ int nvfp4_validate_scales(const float *scales, const uint8_t *written, int n, vo
 
 size_t nvfp4_quantize_workspace_size(int T, int k, int E)
 {
-    if (T < 0 || k < 1 || E < 1) return 0;
+    if (T < 0 || k < 1 || E < 1 || (long long)T * k > INT_MAX) return 0;
     return make_layout(T, 256, 64, E, k).row_src;  // header .. perm
 }
 
@@ -297,9 +309,8 @@ int nvfp4_quantize_experts(const uint16_t *x, int T, int H, const int32_t *topk_
                            int32_t *expert_offsets, int32_t *perm, void *ws, size_t ws_bytes,
                            nvfp4_stream_t stream)
 {
-    if (E < 1 || E > 1024 || k < 1 || k > 32 || k > E || T < 0)
-        return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "quantize: E=%d k=%d T=%d unsupported", E, k, T);
-    if (H <= 0 || H % 64 != 0) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "quantize: H=%d is not a multiple of 64", H);
+    const int shape_rc = quantize_shape_status(T, H, k, E);
+    if (shape_rc != NVFP4_OK) return shape_rc;
     const int sf_ue8m0 = (sf_layout & NVFP4_SF_UE8M0) != 0;
     sf_layout &= ~NVFP4_SF_UE8M0;
     if (sf_layout != NVFP4_SF_LINEAR && sf_layout != NVFP4_SF_SWIZZLED)
@@ -308,9 +319,6 @@ int nvfp4_quantize_experts(const uint16_t *x, int T, int H, const int32_t *topk_
         return fail(NVFP4_ERR_INVALID_ARG, "quantize: null pointer");
     if (!aligned(ws, 256) || (T > 0 && (!aligned(x, 16) || !aligned(q_out, 16) || !aligned(sf_out, 4))))
         return fail(NVFP4_ERR_INVALID_ARG, "quantize: misaligned pointer (x 16 B, q 16 B, sf 4 B, ws 256 B)");
-    if (!quant_offsets_fit((long long)T * k, H))
-        return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "quantize: T*k*H/16 = %lld scale bytes exceed 2^32",
-                    (long long)T * k * (H / 16));
     const size_t need = nvfp4_quantize_workspace_size(T, k, E);
     if (ws_bytes < need) return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "quantize: workspace %zu < %zu", ws_bytes, need);
     cudaStream_t st = (cudaStream_t)stream;
@@ -438,13 +446,13 @@ int nvfp4_prepare_weights_format(const nvfp4_moe_weights *w, void *prepared, siz
 
 size_t nvfp4_moe_workspace_size(int T, int H, int I, int E, int k)
 {
-    if (T < 0 || H <= 0 || I <= 0 || E < 1 || k < 1) return 0;
+    if (T < 0 || H <= 0 || I <= 0 || E < 1 || k < 1 || (long long)T * k > INT_MAX) return 0;
     return make_layout(T, H, I, E, k).end;
 }
 
 size_t nvfp4_moe_host_workspace_size(int T, int H, int I, int E, int k)
 {
-    if (T < 0 || H <= 0 || I <= 0 || E < 1 || k < 1) return 0;
+    if (T < 0 || H <= 0 || I <= 0 || E < 1 || k < 1 || (long long)T * k > INT_MAX) return 0;
     return make_layout(T, H, I, E, k).host_end;
 }
 

@@ -171,6 +171,10 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
+// The shape checks of nvfp4_quantize_experts (status and error text as that
+// entry point returns them): NVFP4_OK or NVFP4_ERR_UNSUPPORTED_SHAPE.
+int quantize_shape_status(int T, int H, int k, int E);
+
 const DivTable &div_table();
 int sm_count();
 void set_error(const char *fmt, ...);

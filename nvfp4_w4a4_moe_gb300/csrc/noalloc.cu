@@ -58,11 +58,11 @@ extern "C" int nvfp4_quantize_experts_static_scratch(const uint16_t *x, int T, i
                                                      uint8_t *sf_out, int sf_layout, int32_t *expert_offsets,
                                                      int32_t *perm, nvfp4_stream_t stream)
 {
-    const size_t need = nvfp4_quantize_workspace_size(T, k, E);
-    if (T < 0 || k < 1 || E < 1 || need == 0) {
-        nvfp4::set_error("static scratch: bad shape T=%d k=%d E=%d", T, k, E);
-        return NVFP4_ERR_INVALID_ARG;
-    }
+    // the workspace entry point's shape checks first, with its status codes,
+    // so that a shape it refuses is refused here the same way
+    const int shape_rc = nvfp4::quantize_shape_status(T, H, k, E);
+    if (shape_rc != NVFP4_OK) return shape_rc;
+    const size_t need = nvfp4_quantize_workspace_size(T, k, E);  // T * k fits an int after those checks
     if (need > kStaticScratchBytes) {
         nvfp4::set_error("static scratch: T=%d, k=%d, E=%d needs %zu bytes of scratch; the static array holds %zu "
                          "(use nvfp4_quantize_experts with a caller workspace)",

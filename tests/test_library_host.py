@@ -162,3 +162,28 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(m, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(m.Nvfp4Error):
         m.load()
+
+
+def test_static_scratch_refuses_shapes_like_the_workspace_entry_point(lib):
+    """The entry point without a workspace applies the workspace entry point's
+    shape checks first, so a shape that one refuses is refused by both with the
+    same status.  Every case returns before any CUDA call (no GPU needed)."""
+    import nvfp4_w4a4_moe_gb300 as m
+    null = ctypes.c_void_p(0)
+    cases = [  # (T, H, k, E)
+        (4, 256, 2, 1025),     # E above 1024
+        (4, 256, 33, 64),      # k above 32
+        (4, 256, 5, 4),        # k above E
+        (-1, 256, 2, 4),       # negative T
+        (4, 100, 2, 4),        # H not a multiple of 64
+        (2 ** 30, 256, 8, 128),  # T * k overflows an int
+    ]
+    for T, H, k, E in cases:
+        rc_ws = lib.nvfp4_quantize_experts(null, T, H, null, k, E, null, null, null, 0, null, null, null,
+                                           ctypes.c_size_t(0), null)
+        rc_st = lib.nvfp4_quantize_experts_static_scratch(null, T, H, null, k, E, null, null, null, 0, null, null,
+                                                          null)
+        assert rc_ws == m.ERR_UNSUPPORTED_SHAPE, (T, H, k, E, rc_ws)
+        assert rc_st == rc_ws, (T, H, k, E, rc_st)
+    assert lib.nvfp4_quantize_workspace_size(2 ** 30, 8, 128) == 0
+    assert lib.nvfp4_moe_workspace_size(2 ** 30, 2816, 704, 128, 8) == 0

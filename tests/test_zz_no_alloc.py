@@ -68,3 +68,17 @@ def test_static_scratch_refuses_oversized_requests():
     assert b"static array" in lib.nvfp4_last_error_string()
     torch.cuda.synchronize()
     assert bool((q == 0x5A).all())
+
+
+def test_static_scratch_python_wrapper_ue8m0_swizzled():
+    """The binding's wrapper (argument checks, output sizing, the UE8M0 flag
+    in the layout word) against the workspace entry point, byte for byte."""
+    import nvfp4_w4a4_moe_gb300 as m
+    layer = S.decode(32)
+    x, ids, scale = _bf16(layer.x), _dev(layer.topk_ids), _dev(layer.w13_input_scale)
+    layout = m.SF_SWIZZLED | m.SF_UE8M0
+    got = m.quantize_experts_static_scratch(x, ids, scale, layer.E, sf_layout=layout)
+    want = m.quantize_experts(x, ids, scale, layer.E, sf_layout=layout)
+    torch.cuda.synchronize()
+    for g, w in zip(got, want):
+        assert torch.equal(g.view(-1), w.view(-1))
