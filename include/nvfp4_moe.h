@@ -67,7 +67,8 @@ typedef enum {
     NVFP4_ERR_CUDA = 4,                /* a CUDA runtime / driver call failed */
     NVFP4_ERR_DEVICE_TIMEOUT = 5,      /* a bounded device-side wait expired */
     NVFP4_ERR_WORKSPACE_TOO_SMALL = 6, /* ws_bytes below the size query's answer */
-    NVFP4_ERR_SCALE_RANGE = 7,         /* NVFP4_UE8M0_SCALES: a block scale above 2^11 (see there) */
+    NVFP4_ERR_SCALE_RANGE = 7,         /* reserved; no entry point returns it (UE8M0 scales are carried
+                                          per row, see NVFP4_UE8M0_SCALES) */
 } nvfp4_status;
 
 enum { NVFP4_SF_LINEAR = 0, NVFP4_SF_SWIZZLED = 1 };
@@ -102,16 +103,19 @@ enum {
      * nvfp4_quantize_weights_format, prepared with nvfp4_prepare_weights_format
      * and NVFP4_SF_UE8M0), and both activation quantisations take UE8M0 scales
      * (see NVFP4_SF_UE8M0); every other step is unchanged.  The block-scaled
-     * FP4 tensor-core MMA is fed E4M3 scale bytes, so a UE8M0 scale 2^e travels
-     * as the E4M3 value 2^(e-3), exact for 2^-6 <= 2^e <= 2^11, and the GEMM
-     * output scales take the factor 2^3 of each operand back.  A block whose
-     * scale is below 2^-6 contributes zero (its values are below 6 * 2^-6 / g
-     * in magnitude).  An activation scale above 2^11 (values more than about
-     * 4.6 times the calibration amax) stops the call on the device with
-     * NVFP4_ERR_SCALE_RANGE; raised by the second quantisation, `out` may then
-     * hold zeros.  Weight scale bytes above 2^11 travel as NaN.  The prepared
-     * weights must match the flag (else NVFP4_ERR_INVALID_ARG on the device,
-     * nothing written).  Not accepted by nvfp4_moe_forward_w4a16. */
+     * FP4 tensor-core MMA is fed E4M3 scale bytes, whose powers of two span
+     * 18 binades (2^-9 .. 2^8), so each GEMM operand row -- a row of
+     * activations, or the weight row of one output column -- carries its
+     * UE8M0 scales relative to its own largest one: that largest scale
+     * travels as 2^8, the others as the same power of two below it, and the
+     * epilogue multiplies the row's power of two back (an exact product, per
+     * activation row and per output column).  Any scale in the UE8M0 range is
+     * accepted, whatever the calibration.  A block whose scale is more than
+     * 17 binades below the largest of its own row contributes zero (its
+     * values are below 2^-17 of that row's largest block).  The intermediates
+     * (sf1, sf2 of nvfp4_moe_intermediates_of) hold the UE8M0 bytes.  The
+     * prepared weights must match the flag (else NVFP4_ERR_INVALID_ARG on the
+     * device, nothing written).  Not accepted by nvfp4_moe_forward_w4a16. */
     NVFP4_UE8M0_SCALES = 8u,
 };
 
@@ -245,7 +249,10 @@ int nvfp4_prepare_weights(const nvfp4_moe_weights *w, void *prepared, size_t pre
  * nvfp4_prepare_weights_format -- nvfp4_prepare_weights for weights whose
  * block scales are in `format`: NVFP4_SF_E4M3 (as nvfp4_prepare_weights) or
  * NVFP4_SF_UE8M0, whose bytes are converted to the E4M3 encoding the tensor
- * cores take (see NVFP4_UE8M0_SCALES).  The last 256 bytes of `prepared` record
+ * cores take, relative to the largest scale of each weight row, with each
+ * row's power of two stored after the scale tiles (see NVFP4_UE8M0_SCALES;
+ * nvfp4_prepared_weights_size includes that room for either format).  The
+ * last 256 bytes of `prepared` record
  * the format; nvfp4_moe_forward checks it against its flags.  Any other
  * format: NVFP4_ERR_INVALID_ARG.  Asynchronous.
  */
@@ -442,6 +449,18 @@ int nvfp4_quantize_weights_format(const uint16_t *w, int count, int N, int K, in
  * nthreads <= 0 uses every host core.  Runs on the CPU only.
  */
 long long nvfp4_selftest_block_division(int nthreads);
+
+/*
+ * nvfp4_selftest_ue8m0_carry -- the per-row carry of UE8M0 scales to the
+ * tensor cores (NVFP4_UE8M0_SCALES), for every byte b and row shift c in
+ * 0 .. 255: out (device, 131072 bytes, 4-byte aligned) receives
+ * out[c * 256 + b] from the one-byte routine the weight preparation uses and
+ * out[65536 + c * 256 + b] from the four-byte routine the GEMM uses.  The
+ * carried byte is the E4M3 encoding of 2^(b - c - 10) when 1 <= b - c <= 18,
+ * and 0 when b <= c.  Synchronous.  NVFP4_ERR_INVALID_ARG for a null or
+ * misaligned `out`.
+ */
+int nvfp4_selftest_ue8m0_carry(uint8_t *out, nvfp4_stream_t stream);
 
 /*
  * nvfp4_selftest_device_wait -- the failure path of the device-side waits,

@@ -94,6 +94,7 @@ def load():
             "nvfp4_quantize_weights_format": (I, [P, I, I, I, I, P, P, P, P, SZ, P]),
             "nvfp4_selftest_block_division": (ctypes.c_longlong, [I]),
             "nvfp4_selftest_device_wait": (I, [P, SZ, U, P]),
+            "nvfp4_selftest_ue8m0_carry": (I, [P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

@@ -127,6 +127,7 @@ WsLayout make_layout(int T, int H, int I, int E, int k)
     L.perm = take(sizeof(int) * (size_t)R);
     L.row_src = take(sizeof(int) * (size_t)L.rows_cap);
     L.tile_expert = take(sizeof(int) * (size_t)L.mtiles_cap);
+    L.row_max = take(sizeof(int) * 2 * (size_t)L.rows_cap);  // UE8M0: a1 rows, then a2 rows
     L.a1q = take((size_t)L.rows_cap * (H / 2));
     L.sf1 = take((size_t)L.mtiles_cap * L.kc1 * 512);
     L.a2q = take((size_t)L.rows_cap * (I / 2));
@@ -197,9 +198,6 @@ static int header_status(const DevHeader &h, int *first_bad)
         return fail(NVFP4_ERR_INVALID_ARG, "an expert id is outside [0, E)");
     if (h.status == 4)
         return fail(NVFP4_ERR_INVALID_ARG, "the prepared weights were converted for the other block-scale format");
-    if (h.status == 6 || (h.error_flags & kErrUe8m0Range))
-        return fail(NVFP4_ERR_SCALE_RANGE, "a UE8M0 block scale is above 2^%d, the largest carried to the tensor cores",
-                    8 + kUe8m0Shift);
     if (h.status == 5 || (h.error_flags & (kErrTimeoutProducer | kErrTimeoutMma | kErrTimeoutEpilogue | kErrTimeoutRoute)))
         return fail(NVFP4_ERR_DEVICE_TIMEOUT, "a device-side wait expired (flags 0x%x)", h.error_flags);
     return NVFP4_OK;
@@ -260,6 +258,16 @@ const char *nvfp4_last_error_string(void) { return g_err; }
 int nvfp4_version(void) { return 100; }
 
 long long nvfp4_selftest_block_division(int nthreads) { return selftest_division(nthreads); }
+
+int nvfp4_selftest_ue8m0_carry(uint8_t *out, nvfp4_stream_t stream)
+{
+    if (!out) return fail(NVFP4_ERR_INVALID_ARG, "selftest: out is null");
+    if (!aligned(out, 4)) return fail(NVFP4_ERR_INVALID_ARG, "selftest: out must be 4-byte aligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    NV_CUDA(launch_ue8m0_carry_selftest(out, st), "launching the carry self-test");
+    NV_CUDA(cudaStreamSynchronize(st), "synchronising the stream");
+    return NVFP4_OK;
+}
 
 int nvfp4_selftest_device_wait(void *ws, size_t ws_bytes, unsigned limit_us, nvfp4_stream_t stream)
 {
@@ -391,9 +399,14 @@ int nvfp4_quantize_experts(const uint16_t *x, int T, int H, const int32_t *topk_
 // The prepared buffer ends with a 256-byte slot whose first word names the
 // block-scale format the scales were converted from; the forward checks it.
 constexpr uint32_t kPrepTagE4M3 = 0xE4E4E4E4u, kPrepTagUE8M0 = 0x5E5E5E5Eu;
-static size_t prep_tag_offset(int E, int H, int I)
+// UE8M0 weight-row factors after both scale layouts: [E, 2I] (w13) then [E, H] (w2).
+static size_t prep_factor_offset(int E, int H, int I)
 {
     return up256(prepared_w13_bytes(E, H, I)) + up256(prepared_w2_bytes(E, H, I));
+}
+static size_t prep_tag_offset(int E, int H, int I)
+{
+    return prep_factor_offset(E, H, I) + up256(sizeof(float) * (size_t)E * (2 * (size_t)I + H));
 }
 
 size_t nvfp4_prepared_weights_size(int E, int H, int I)
@@ -434,10 +447,11 @@ int nvfp4_prepare_weights_format(const nvfp4_moe_weights *w, void *prepared, siz
         return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "prepared buffer %zu < %zu", prepared_bytes, need);
     cudaStream_t st = (cudaStream_t)stream;
     uint8_t *base = static_cast<uint8_t *>(prepared);
-    PrepArgs a13 = {w->w13_sf, base, w->E, 2 * w->I, w->H, 4 * ((w->H + 255) / 256), w->I, ue};
+    float *factors = reinterpret_cast<float *>(base + prep_factor_offset(w->E, w->H, w->I));
+    PrepArgs a13 = {w->w13_sf, base, w->E, 2 * w->I, w->H, 4 * ((w->H + 255) / 256), w->I, ue, factors};
     NV_CUDA(launch_prep_sf(a13, st), "launching the w13 scale conversion");
     PrepArgs a2 = {w->w2_sf, base + up256(prepared_w13_bytes(w->E, w->H, w->I)), w->E, w->H, w->I,
-                   4 * ((w->I + 255) / 256), 0, ue};
+                   4 * ((w->I + 255) / 256), 0, ue, factors + (size_t)w->E * 2 * w->I};
     NV_CUDA(launch_prep_sf(a2, st), "launching the w2 scale conversion");
     NV_CUDA(cudaMemsetAsync(base + prep_tag_offset(w->E, w->H, w->I), ue ? 0x5E : 0xE4, 4, st),
             "writing the format word");
@@ -503,7 +517,6 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     va.narrays = 4;
     va.alpha1 = alpha1;
     va.alpha2 = alpha2;
-    va.alpha_pow2 = ue ? (float)(1 << (2 * kUe8m0Shift)) : 1.0f;  // both operands' scales were divided
     va.prep_tag = reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(prepared) +
                                                      prep_tag_offset(E, H, I));
     va.prep_tag_want = ue ? kPrepTagUE8M0 : kPrepTagE4M3;
@@ -524,6 +537,9 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     ra.row_of = reinterpret_cast<int *>(base + L.row_of);
     ra.perm = reinterpret_cast<int *>(base + L.perm);
     ra.row_src = reinterpret_cast<int *>(base + L.row_src);
+    int *row_max = reinterpret_cast<int *>(base + L.row_max);  // UE8M0: a1 rows, then a2 rows
+    ra.row_max = ue ? row_max : nullptr;
+    ra.rows_cap = L.rows_cap;
     ra.padded = 1;
     ra.hdr = hdr;
     // The routing returns at once when the check has failed, so it may be
@@ -558,7 +574,8 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     qa.sf = base + L.sf1;
     qa.sf_swizzled = 1;
     qa.sf_kc = L.kc1;
-    qa.sf_ue8m0 = ue ? 2 : 0;  // the tensor cores take E4M3 bytes: UE8M0 scales travel as E4M3 powers of two
+    qa.sf_ue8m0 = ue ? 1 : 0;  // UE8M0 bytes, carried to the tensor cores per row by the GEMM
+    qa.row_max = ue ? row_max : nullptr;
     qa.hdr = hdr;
     NV_CUDA(launch_quant_experts(qa, st), "launching the a1 quantiser");
     NV_CUDA(mark(3), "recording an event");
@@ -588,6 +605,12 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     ga.kc2 = L.kc2;
     ga.h_dump = keep_h ? reinterpret_cast<float *>(base + L.host_end) : nullptr;
     ga.ue8m0 = ue ? 1 : 0;
+    const float *factors = reinterpret_cast<const float *>(pw + prep_factor_offset(E, H, I));
+    if (ue) {
+        ga.a_row_max = row_max;
+        ga.out_row_max = row_max + L.rows_cap;
+        ga.b_row_factor = factors;
+    }
     ga.zero_out = out;  // cleared by the w13 kernel for the w2 kernel's reductions
     ga.zero_floats = (long long)T * H;
     ga.k = k;
@@ -612,6 +635,11 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     gb.row_src = ra.row_src;
     gb.topk_w = topk_w;
     gb.out = out;
+    if (ue) {
+        gb.a_row_max = row_max + L.rows_cap;
+        gb.out_row_max = nullptr;
+        gb.b_row_factor = factors + (size_t)E * 2 * I;
+    }
     NV_CUDA(launch_gemm_w2(gb, st), "launching the w2 GEMM");
     NV_CUDA(mark(5), "recording an event");
 

@@ -37,7 +37,7 @@ constexpr float kFltMax = 3.40282346638528859812e+38f;
 // Device-side status block at the start of every workspace.
 struct DevHeader {
     int status;          // 0 = ok, 2 = a scale slot failed validation, 3 = bad expert id, 4 = prepared weights in
-                         // the other scale format, 5 = device timeout, 6 = a UE8M0 scale above the carried range
+                         // the other scale format, 5 = device timeout
     int bad_count;       // number of bad scale slots
     int first_bad;       // lowest bad slot index (INT_MAX when none)
     int error_flags;     // kErr* bits below
@@ -53,7 +53,6 @@ enum : int {
     kErrTimeoutMma = 4,
     kErrTimeoutEpilogue = 8,
     kErrTimeoutRoute = 16,
-    kErrUe8m0Range = 32,
 };
 
 // RN, saturating FP32 -> E4M3 (t >= 0): the byte of the second source.
@@ -193,23 +192,45 @@ __device__ __forceinline__ uint2 quant_block16_ue8m0(const f32x2 (&x)[8], float 
     return make_uint2(e2m1_rn_sat8(q[0], q[1], q[2], q[3]), e2m1_rn_sat8(q[4], q[5], q[6], q[7]));
 }
 
-// UE8M0 scales carried to the tensor cores.  The block-scaled FP4 MMA is
-// given E4M3 scale bytes; a UE8M0 scale 2^(b-127) travels as the E4M3
-// encoding of 2^(b-127-kUe8m0Shift), exact while that lies in E4M3's powers of
-// two 2^-9 .. 2^8, and the GEMM's output scale takes 2^kUe8m0Shift per
-// operand back.  With the shift of 3 the scales 2^-6 .. 2^11 travel exactly.
-// A smaller scale gives 0: such a block lies below 2^-6 * 6 / g in magnitude.
-// A larger one cannot travel: kUe8m0TooLarge (an E4M3 NaN) is returned, and
-// the caller reports it.
-constexpr int kUe8m0Shift = 3;
-constexpr uint32_t kUe8m0TooLarge = 0x7Fu;
-__device__ __forceinline__ uint32_t e4m3_of_ue8m0(uint32_t b)
+// UE8M0 scales carried to the tensor cores, one window per GEMM row.  The
+// block-scaled FP4 MMA is given E4M3 scale bytes, whose powers of two span
+// 2^-9 .. 2^8 (18 binades).  Each operand row (a row of activations, or the
+// weight row of one output column) carries its UE8M0 bytes b relative to its
+// own largest byte m: with the row's shift c = max(m - 18, 0), byte b travels
+// as the E4M3 encoding of 2^(b - c - 10) when d = b - c lies in 1 .. 18
+// (2^-9 .. 2^8), and as 0 when d <= 0, i.e. when the block's scale is more
+// than 17 binades below the row's largest (its values are below 2^-17 of the
+// row's largest block).  The true scale is the carried one times 2^(c - 117),
+// a power of two the GEMM epilogue multiplies back per row and per column: an
+// exact product, so nothing depends on the global calibration and no scale
+// is out of range.
+__device__ __forceinline__ uint32_t ue8m0_row_shift(uint32_t row_max_byte)
 {
-    const int k = (int)b - 127 - kUe8m0Shift;
-    if (k > 8) return kUe8m0TooLarge;
-    if (k >= -6) return (uint32_t)(k + 7) << 3;  // normal: exponent field k + 7, mantissa 0
-    if (k >= -9) return 1u << (k + 9);           // subnormal: mantissa 2^(k+9) x 2^-9
-    return 0u;
+    return row_max_byte > 18u ? row_max_byte - 18u : 0u;
+}
+// 2^(c - 117) for a row shift c in 0 .. 236 (a normal float).
+__device__ __forceinline__ float ue8m0_row_factor(uint32_t c) { return __uint_as_float((c + 10u) << 23); }
+// Row shift back from its factor.
+__device__ __forceinline__ uint32_t ue8m0_shift_of_factor(float f) { return (__float_as_uint(f) >> 23) - 10u; }
+// One byte carried with row shift c.
+__device__ __forceinline__ uint32_t ue8m0_carried(uint32_t b, uint32_t c)
+{
+    uint32_t d = b > c ? b - c : 0u;
+    d = d < 18u ? d : 18u;  // b <= the row's largest byte keeps d <= 18; bytes of unused rows are clamped
+    if (d == 0u) return 0u;
+    if (d <= 3u) return 1u << (d - 1u);  // subnormal: 2^(d-10) = (1 << (d-1)) * 2^-9
+    return (d - 3u) << 3;                // normal: exponent field d - 3, mantissa 0
+}
+// Four bytes (one 32-bit word) carried with the row shift c4 (c in every byte).
+__device__ __forceinline__ uint32_t ue8m0_carried4(uint32_t w, uint32_t c4)
+{
+    uint32_t d = __vsubus4(w, c4);               // b - c, saturated at 0
+    d = __vminu4(d, 0x12121212u);                // <= 18
+    const uint32_t normal = __vsubus4(d, 0x03030303u) << 3;  // (d - 3) << 3 where d >= 4, else 0 (bytes <= 15 << 3)
+    const uint32_t le3 = __vcmpleu4(d, 0x03030303u);          // 0xFF where d <= 3
+    const uint32_t eq3 = __vcmpeq4(d, 0x03030303u);
+    const uint32_t sub = (d + (eq3 & 0x01010101u)) & le3;     // d = 1, 2, 3 -> 1, 2, 4 (d + 1 <= 4: no carry)
+    return normal | sub;
 }
 
 // Programmatic dependent launch.  A kernel launched with launch_pdl may be

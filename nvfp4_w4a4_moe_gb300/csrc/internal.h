@@ -17,7 +17,7 @@ struct WsLayout {
     int rows_cap, mtiles_cap, nchunks;
     int kc1, kc2;  // 64-element scale chunks per 128-row tile for a1 (H) and a2 (I)
     size_t hdr, g1, g2, alpha1, alpha2, counts, offsets, pad_off, chunk_hist, row_of, perm, row_src,
-        tile_expert, a1q, sf1, a2q, sf2, end;
+        tile_expert, row_max, a1q, sf1, a2q, sf2, end;
     // forward_host staging (after `end`), and the optional FP32 h dump
     size_t x_stage, ids_stage, w_stage, out_stage, status_stage, host_end;
 };
@@ -35,7 +35,6 @@ struct ValidateArgs {
     float *recip[4];  // FP32 reciprocal of each slot (nullable per array)
     int E, narrays;
     float *alpha1, *alpha2;  // 1/(g_a * g_w) per expert (forward only; nullable)
-    float alpha_pow2;        // power of two the alphas are multiplied by (0 means 1)
     const uint32_t *prep_tag;  // format word of the prepared weights (nullable)
     uint32_t prep_tag_want;    // the value it must hold, else status 4
     DevHeader *hdr;
@@ -50,6 +49,8 @@ struct RouteArgs {
     int *perm;         // compact permuted row -> f (nullable)
     int *row_src;      // padded row -> f, -1 for padding (nullable)
     int *offsets_out;  // caller copy of the compact offsets (nullable)
+    int *row_max;      // UE8M0 forward: two arrays of rows_cap ints set to 0 for every padded row (nullable)
+    int rows_cap;
     int padded;
     DevHeader *hdr;
 };
@@ -67,7 +68,8 @@ struct QuantArgs {
     uint8_t *q;
     uint8_t *sf;
     int sf_swizzled, sf_kc;
-    int sf_ue8m0;  // 0: E4M3 block scales; 1: UE8M0 bytes; 2: UE8M0 carried as E4M3 (e4m3_of_ue8m0)
+    int sf_ue8m0;  // 0: E4M3 block scales; 1: UE8M0 bytes
+    int *row_max;  // UE8M0: per padded row, the largest scale byte (atomicMax; nullable)
     DevHeader *hdr;  // read for the status; mode 2 writes a range error into it
 };
 cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st);
@@ -77,7 +79,8 @@ struct PrepArgs {
     uint8_t *out;       // [E][N/128 blocks][kc][512]; w13 blocks of one tile interleaved per K step
     int E, N, K, kc;
     int gate_up_I;      // w13: I > 0 (blocks of 128 gate rows and 128 up rows; a 64 + 64 tail block)
-    int ue8m0;          // the canonical bytes are UE8M0: written carried as E4M3 (e4m3_of_ue8m0)
+    int ue8m0;          // the canonical bytes are UE8M0: written carried per row (ue8m0_carried)
+    float *row_factor;  // UE8M0: [E * N] per weight row 2^(shift - 117), written here, read by the epilogues
 };
 cudaError_t launch_prep_sf(const PrepArgs &a, cudaStream_t st);
 
@@ -85,6 +88,9 @@ cudaError_t launch_rmsnorm(const uint16_t *x, const float *out, int T, int H, fl
                            cudaStream_t st);
 // A kernel whose bounded waits run out by design (status 5 in hdr).
 cudaError_t launch_wait_selftest(DevHeader *hdr, uint64_t limit_ns, cudaStream_t st);
+// out [2][256 shifts][256 bytes]: the UE8M0 row carry of every byte and shift, by the
+// one-byte and the four-byte routine.
+cudaError_t launch_ue8m0_carry_selftest(uint8_t *out, cudaStream_t st);
 
 // Router: softmax / top-k / renormalise over logits [T, E] (FP32, or BF16 when bf16 != 0).
 cudaError_t launch_router_topk(const void *logits, int bf16, int T, int E, int k, int32_t *ids, float *w,
@@ -107,7 +113,10 @@ struct GemmArgs {
     uint8_t *a2q, *sf2;
     int I, kc2;
     float *h_dump;
-    int ue8m0;        // w13 kernel: a2 takes UE8M0 block scales, carried as E4M3 (e4m3_of_ue8m0)
+    int ue8m0;        // UE8M0 block scales: A carried per row, B prepared per row, factors in the epilogue
+    const int *a_row_max;      // UE8M0: the A rows' largest scale bytes
+    int *out_row_max;          // UE8M0, w13: the a2 rows' largest scale bytes (atomicMax; zero on entry)
+    const float *b_row_factor; // UE8M0: [E * N] weight-row factors 2^(shift - 117)
     float *zero_out;  // w13 kernel: [T, H] FP32 output cleared for the w2 kernel's reductions (nullable)
     long long zero_floats;
     // w2 epilogue (weighted combine)

@@ -197,8 +197,13 @@ __device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int 
 }
 
 // ---------------------------------------------------------------- kernel
-// EPI 0: w13 (SiLU*up + requantise), 1: w2 (weighted combine).  UE (w13):
-// the requantisation takes UE8M0 block scales, carried as E4M3.
+// EPI 0: w13 (SiLU*up + requantise), 1: w2 (weighted combine).  UE: UE8M0
+// block scales throughout.  The A scales arrive as UE8M0 bytes and are
+// carried to the tensor cores per row (ue8m0_carried, with the row's largest
+// byte from a_row_max); the weight scales were carried per weight row when
+// prepared.  The epilogue multiplies both rows' factors back: the A row's
+// into the row scale, the weight row's per output column.  w13 then writes
+// a2 as UE8M0 bytes with each row's largest byte (out_row_max).
 template <int EPI, bool UE>
 __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -421,6 +426,14 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         bool ok = true;
         for (int i = 0; i < n_i && ok; ++i) {
             const TileInfo<EPI> ti = seq_tile<EPI>(p, i, NT, MT, paired);
+            // UE8M0: word q of this lane's 16 bytes holds row q * 32 + lane
+            // of the m-tile; its bytes are carried with that row's shift
+            uint32_t c4[4] = {0u, 0u, 0u, 0u};
+            if (UE) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    c4[q] = ue8m0_row_shift((uint32_t)__ldg(p.a_row_max + ti.mt * BM + q * 32 + lane)) * 0x01010101u;
+            }
             for (int kt = 0; kt < KT; ++kt) {
                 if (!mbar_wait(&full[stage], phase, abort_flag, kWaitLimitNs)) {
                     ok = false;
@@ -432,6 +445,12 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                 uint4 v[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) v[j] = ssfa[32 * j];
+                if (UE) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        v[j] = make_uint4(ue8m0_carried4(v[j].x, c4[0]), ue8m0_carried4(v[j].y, c4[1]),
+                                          ue8m0_carried4(v[j].z, c4[2]), ue8m0_carried4(v[j].w, c4[3]));
+                }
                 tmem_st16(sfa_t, v);
                 if (SFB_STEP == 4) {
 #pragma unroll
@@ -513,6 +532,9 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                 s1 = 0.0f;
                 t = valid ? f / p.k : 0;
             }
+            // UE8M0: the A row's carried scales take 2^(shift - 117) back (an
+            // exact product; the weight rows' factors are applied per column)
+            if (UE) s0 *= ue8m0_row_factor(ue8m0_row_shift((uint32_t)p.a_row_max[row]));
             if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
                 ok = false;
                 break;
@@ -529,6 +551,8 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                 const f32x2 aa = pack_f32x2(alpha, alpha);
                 const int hw = ti.hc / (P::NUM_EPI_WARPS / 4), w0 = part * hw;
                 const int nblocks = hw >> 4;  // blocks of 16 of this warp
+                // UE8M0: factors of the gate and up weight rows of this warp's columns
+                const float *fgate = UE ? p.b_row_factor + (size_t)e * p.N + 128 * nt + w0 : nullptr;
                 f32x2 h[4][8];
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -546,12 +570,16 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                     }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const f32x2 gs = mul_f32x2(pack_f32x2(gate[2 * i], gate[2 * i + 1]), aa);
-                        const f32x2 us = mul_f32x2(pack_f32x2(up[2 * i], up[2 * i + 1]), aa);
+                        f32x2 gs = mul_f32x2(pack_f32x2(gate[2 * i], gate[2 * i + 1]), aa);
+                        f32x2 us = mul_f32x2(pack_f32x2(up[2 * i], up[2 * i + 1]), aa);
+                        if (UE) {
+                            gs = mul_f32x2(gs, __ldg(reinterpret_cast<const float2 *>(fgate + 32 * c + 2 * i)));
+                            us = mul_f32x2(us, __ldg(reinterpret_cast<const float2 *>(fgate + p.gate_up_I + 32 * c + 2 * i)));
+                        }
                         h[2 * c + (i >> 3)][i & 7] = mul_f32x2(pack_f32x2(silu(lo_f32(gs)), silu(hi_f32(gs))), us);
                     }
                 }
-                uint32_t sfw = 0;
+                uint32_t sfw = 0, sf_max = 0;
                 const int hcol_tile = 128 * nt + w0;  // first h column of this warp
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
@@ -572,12 +600,7 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                     uint2 pk;
                     if (UE) {
                         pk = quant_block16_ue8m0(h[b], amax, g2, sb);
-                        sb = e4m3_of_ue8m0(sb);
-                        if (sb == kUe8m0TooLarge && valid) {
-                            // the w2 kernel finds the status and does not run
-                            atomicOr(&p.hdr->error_flags, kErrUe8m0Range);
-                            p.hdr->status = 6;
-                        }
+                        sf_max = max(sf_max, sb);
                     } else {
                         pk = quant_block16(h[b], amax, g2, &tab, sb);
                     }
@@ -597,6 +620,7 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                     if (nt == NT - 1 && part == 0)
                         for (int cc = p.I >> 6; cc < p.kc2; ++cc)
                             *reinterpret_cast<uint32_t *>(p.sf2 + swz_sf_offset(row, cc, p.kc2)) = 0u;
+                    if (UE) atomicMax(p.out_row_max + row, (int)sf_max);  // the w2 kernel carries a2 by it
                 }
             } else {
                 // out[t, cols] += w[t, j] * alpha2 * y2 on this warp's 64 columns,
@@ -617,10 +641,22 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                         mbar_arrive(&acc_empty[acc]);
                     }
                     float4 *xrow = reinterpret_cast<float4 *>(xp + lane * XPOSE_LD);
+                    if (UE) {
+                        // the weight rows' factors of these 32 output columns
+                        const float4 *cf =
+                            reinterpret_cast<const float4 *>(p.b_row_factor + (size_t)e * p.N + nt * 128 + cbase);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        xrow[j ^ (lane & 7)] = make_float4(v[4 * j] * scale, v[4 * j + 1] * scale,
-                                                           v[4 * j + 2] * scale, v[4 * j + 3] * scale);
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 f = __ldg(cf + j);
+                            xrow[j ^ (lane & 7)] = make_float4(v[4 * j] * scale * f.x, v[4 * j + 1] * scale * f.y,
+                                                               v[4 * j + 2] * scale * f.z, v[4 * j + 3] * scale * f.w);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            xrow[j ^ (lane & 7)] = make_float4(v[4 * j] * scale, v[4 * j + 1] * scale,
+                                                               v[4 * j + 2] * scale, v[4 * j + 3] * scale);
+                    }
                     __syncwarp();
 #pragma unroll
                     for (int it = 0; it < 8; ++it) {
@@ -744,6 +780,9 @@ cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st)
 {
     return a.ue8m0 ? launch_gemm<0, true>(a, st) : launch_gemm<0, false>(a, st);
 }
-cudaError_t launch_gemm_w2(const GemmArgs &a, cudaStream_t st) { return launch_gemm<1, false>(a, st); }
+cudaError_t launch_gemm_w2(const GemmArgs &a, cudaStream_t st)
+{
+    return a.ue8m0 ? launch_gemm<1, true>(a, st) : launch_gemm<1, false>(a, st);
+}
 
 }  // namespace nvfp4

@@ -48,13 +48,10 @@ __device__ __forceinline__ void validate_body(const ValidateArgs &a)
     __syncthreads();
     // GEMM output scale 1/(g_a * g_w) per expert [page, §NVFP4 runtime-order
     // figure: the GEMM's scaling takes in both FP32 global scales].
-    // With UE8M0 scales carried as E4M3 (each operand's scales divided by
-    // 2^kUe8m0Shift) the alphas take that power of two back: an exact product.
     if (a.alpha1 && a.narrays == 4) {
-        const float ap = a.alpha_pow2 > 0.0f ? a.alpha_pow2 : 1.0f;
         for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
-            a.alpha1[e] = __fmul_rn(__frcp_rn(__fmul_rn(s_recip[0][e], s_recip[2][e])), ap);
-            a.alpha2[e] = __fmul_rn(__frcp_rn(__fmul_rn(s_recip[1][e], s_recip[3][e])), ap);
+            a.alpha1[e] = __frcp_rn(__fmul_rn(s_recip[0][e], s_recip[2][e]));
+            a.alpha2[e] = __frcp_rn(__fmul_rn(s_recip[1][e], s_recip[3][e]));
         }
     }
     if (threadIdx.x == 0) {
@@ -278,7 +275,10 @@ __device__ __forceinline__ void route_body(const RouteArgs &a)
     // padding rows of each expert's last tile: one warp per expert
     if (a.row_src) {
         for (int e = blockIdx.x * kRouteWarps + warp; e < E; e += gridDim.x * kRouteWarps)
-            for (int r = poff[e] + cnt[e] + lane; r < poff[e + 1]; r += 32) a.row_src[r] = -1;
+            for (int r = poff[e] + cnt[e] + lane; r < poff[e + 1]; r += 32) {
+                a.row_src[r] = -1;
+                if (a.row_max) a.row_max[r] = a.row_max[a.rows_cap + r] = 0;
+            }
     }
 
     // ---- phase 2: scatter this CTA's chunks
@@ -325,6 +325,7 @@ __device__ __forceinline__ void route_body(const RouteArgs &a)
                 a.row_of[f] = a.padded ? padded : compact;
                 if (a.perm) a.perm[compact] = f;
                 if (a.row_src) a.row_src[padded] = f;
+                if (a.row_max) a.row_max[padded] = a.row_max[a.rows_cap + padded] = 0;
             }
         }
         __syncthreads();
@@ -379,8 +380,10 @@ __device__ __forceinline__ float amax16_bf16(const uint32_t *w)
 constexpr int kQuantThreads = 128;  // 5 CTAs (20 warps) per SM at <= 96 registers
 
 // SWZ: scales in the swizzled tensor-core layout (else linear [rows, H/16]);
-// SF: block scales E4M3 (0), UE8M0 bytes (1), or UE8M0 carried as E4M3
-// powers of two for the tensor cores (2, see e4m3_of_ue8m0).
+// SF: block scales E4M3 (0) or UE8M0 bytes (1).  With UE8M0 and a row_max
+// array, each routed row's largest scale byte is also recorded there
+// (atomicMax; the array is zero on entry): the GEMM carries the row's bytes
+// relative to it (ue8m0_carried).
 template <bool SWZ, int SF>
 __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantArgs a, DivTable tab_in)
 {
@@ -408,10 +411,12 @@ __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantAr
     while (t < a.T) {
         const int pair = c * 32 + lane;
         uint32_t my_q = 0, my_s = 0;  // lane j < k: row parts of expert j's code and scale offsets
+        uint32_t my_row = 0;
         float my_g = 1.0f;
         if (lane < k) {
             const int f = t * k + lane;
             const uint32_t row = (uint32_t)__ldg(a.row_of + f);
+            my_row = row;
             my_g = __ldg(a.g + __ldg(a.ids + f));
             my_q = row * (uint32_t)npair;
             my_s = SWZ ? ((row >> 7) * (uint32_t)a.sf_kc * 512u + (row & 31u) * 16u + ((row >> 5) & 3u) * 4u)
@@ -448,21 +453,17 @@ __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantAr
             const uint32_t qo = __shfl_sync(0xffffffffu, my_q, j) + (uint32_t)pair;
             const uint32_t so = __shfl_sync(0xffffffffu, my_s, j) + lane_s;
             const float g = __shfl_sync(0xffffffffu, my_g, j);
+            uint32_t s0 = 0, s1 = 0;
             if (active) {
-                uint32_t s0, s1;
                 const uint2 p0 = SF ? quant_block16_ue8m0(x0, amax0, g, s0) : quant_block16(x0, amax0, g, &tab, s0);
                 const uint2 p1 = SF ? quant_block16_ue8m0(x1, amax1, g, s1) : quant_block16(x1, amax1, g, &tab, s1);
-                if (SF == 2) {
-                    s0 = e4m3_of_ue8m0(s0);
-                    s1 = e4m3_of_ue8m0(s1);
-                    if (s0 == kUe8m0TooLarge || s1 == kUe8m0TooLarge) {
-                        // the GEMMs find the status and do not run
-                        atomicOr(&a.hdr->error_flags, kErrUe8m0Range);
-                        a.hdr->status = 6;
-                    }
-                }
                 q16[qo] = make_uint4(p0.x, p0.y, p1.x, p1.y);
                 *reinterpret_cast<uint16_t *>(a.sf + so) = (uint16_t)(s0 | (s1 << 8));
+            }
+            if (SF && a.row_max) {
+                const uint32_t m = __reduce_max_sync(0xffffffffu, max(s0, s1));
+                const uint32_t row = __shfl_sync(0xffffffffu, my_row, j);
+                if (lane == 0) atomicMax(a.row_max + row, (int)m);
             }
         }
         t += dt;
@@ -471,6 +472,24 @@ __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantAr
             c -= nchunk;
             ++t;
         }
+    }
+}
+
+// ------------------------------------------------------------------ UE8M0 weight rows
+// One warp per weight row (an output column of the GEMM): the row's largest
+// UE8M0 block-scale byte m, stored as the row's factor 2^(c - 117) with the
+// shift c = max(m - 18, 0) (see ue8m0_carried).
+__global__ void __launch_bounds__(256) sf_row_factor_kernel(const uint8_t *sf, long long rows, int nsf,
+                                                            float *row_factor)
+{
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+        const uint8_t *src = sf + r * nsf;
+        uint32_t m = 0;
+        for (int i = lane; i < nsf; i += 32) m = max(m, (uint32_t)src[i]);
+        m = __reduce_max_sync(0xffffffffu, m);
+        if (lane == 0) row_factor[r] = ue8m0_row_factor(ue8m0_row_shift(m));
     }
 }
 
@@ -514,11 +533,14 @@ __global__ void __launch_bounds__(256) prep_sf_kernel(PrepArgs a)
             blk_off = ((size_t)nt * a.kc + c) * 512;
         }
         const uint8_t *src = a.sf + ((size_t)e * a.N + row) * nsf;
+        // UE8M0: carried relative to the row's largest byte (its shift read
+        // back from the row factor that sf_row_factor_kernel wrote)
+        const uint32_t shift = a.ue8m0 ? ue8m0_shift_of_factor(a.row_factor[(size_t)e * a.N + row]) : 0u;
         uint32_t word = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int col = 4 * c + j;
-            if (col < nsf) word |= (a.ue8m0 ? e4m3_of_ue8m0(src[col]) : (uint32_t)src[col]) << (8 * j);
+            if (col < nsf) word |= (a.ue8m0 ? ue8m0_carried(src[col], shift) : (uint32_t)src[col]) << (8 * j);
         }
         uint8_t *dst = a.out + (size_t)e * NT * a.kc * 512 + blk_off + (size_t)(v & 31) * 16 + (v >> 5) * 4;
         *reinterpret_cast<uint32_t *>(dst) = word;
@@ -745,9 +767,7 @@ cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st)
         return launch_pdl(kernel, dim3((int)grid, (int)ysplit), dim3(kQuantThreads), 0, st, a, div_table());
     };
     cudaError_t err;
-    if (a.sf_ue8m0 == 2)
-        err = a.sf_swizzled ? launch(quant_experts_kernel<true, 2>) : cudaErrorInvalidValue;
-    else if (a.sf_ue8m0)
+    if (a.sf_ue8m0)
         err = a.sf_swizzled ? launch(quant_experts_kernel<true, 1>) : launch(quant_experts_kernel<false, 1>);
     else
         err = a.sf_swizzled ? launch(quant_experts_kernel<true, 0>) : launch(quant_experts_kernel<false, 0>);
@@ -756,8 +776,31 @@ cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st)
 
 cudaError_t launch_prep_sf(const PrepArgs &a, cudaStream_t st)
 {
+    if (a.ue8m0) {
+        const long long rows = (long long)a.E * a.N;
+        sf_row_factor_kernel<<<grid_for(rows * 32, 256, 16), 256, 0, st>>>(a.sf, rows, a.K / 16, a.row_factor);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     const long long work = (long long)a.E * (a.N / 128) * a.kc * 128;
     prep_sf_kernel<<<grid_for(work, 256, 16), 256, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+// Every (byte b, row shift c) pair through both carry routines: out[c][b] by
+// ue8m0_carried, out[256 + c][b] by ue8m0_carried4 (four bytes a word).
+__global__ void ue8m0_carry_selftest_kernel(uint8_t *out)
+{
+    const uint32_t c = blockIdx.x, b = threadIdx.x;
+    out[c * 256 + b] = (uint8_t)ue8m0_carried(b, c);
+    if ((b & 3) == 0) {
+        const uint32_t w = b | (b + 1) << 8 | (b + 2) << 16 | (b + 3) << 24;
+        *reinterpret_cast<uint32_t *>(out + (256 + c) * 256 + b) = ue8m0_carried4(w, c * 0x01010101u);
+    }
+}
+cudaError_t launch_ue8m0_carry_selftest(uint8_t *out, cudaStream_t st)
+{
+    ue8m0_carry_selftest_kernel<<<256, 256, 0, st>>>(out);
     return cudaGetLastError();
 }
 

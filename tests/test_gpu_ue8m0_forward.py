@@ -1,11 +1,13 @@
 """GPU parity of the UE8M0 variant of the expert forward (power-of-two block
 scales on the weights, a1 and a2) against the oracle, through the C ABI.
 
-The tensor cores take E4M3 scale bytes, so the library carries a UE8M0 scale
-2^e as the E4M3 value 2^(e-3) and takes 2^3 per operand back in the output
-scale.  Bit-exact: a1 and a2 codes, and the scale bytes the GEMMs read, which
-must be exactly that carried encoding of the oracle's UE8M0 bytes (written
-here from the two formats' definitions).  Within tolerance: h and out."""
+The tensor cores take E4M3 scale bytes, whose powers of two span 18 binades,
+so each GEMM operand row carries its UE8M0 scales relative to its own largest
+one and the epilogue multiplies that power of two back.  Bit-exact: a1 and a2
+codes and their UE8M0 scale bytes, and the carry of every (byte, row shift)
+pair against its definition.  Within tolerance: h and out, also for
+activations far from the calibration and for rows whose blocks span many
+binades (nothing is refused)."""
 import ctypes
 
 import numpy as np
@@ -19,8 +21,6 @@ from gpu_helpers import assert_close, dev, dev_bf16, device_weights, host, layer
 
 pytestmark = pytest.mark.gpu
 
-SHIFT = 3  # UE8M0 2^e travels as E4M3 2^(e - SHIFT)
-
 
 @pytest.fixture(scope="module")
 def m():
@@ -29,32 +29,37 @@ def m():
     return mod
 
 
-def carried_e4m3(ue: np.ndarray) -> np.ndarray:
-    """E4M3 bytes of 2^(b - 127 - SHIFT): normal for exponents -6 .. 8 (field
-    k + 7, mantissa 0), subnormal 2^(k + 9) * 2^-9 for -9 .. -7, else 0."""
-    k = np.asarray(ue, dtype=np.int64) - 127 - SHIFT
-    assert (k <= 8).all(), "a scale above the carried range"
-    normal = (k + 7) << 3
-    sub = np.left_shift(1, np.clip(k + 9, 0, 7))
-    return np.where(k >= -6, normal, np.where(k >= -9, sub, 0)).astype(np.uint8)
+def test_row_carry_matches_its_definition(m):
+    """Both device carry routines, for every byte b and row shift c: the E4M3
+    value of the carried byte (decoded by the oracle's E4M3 decoder) is
+    2^(b - c - 10) when 1 <= b - c <= 18 and 0 when b <= c.  (b - c > 18 does
+    not occur: the shift is the row's largest byte minus 18.)"""
+    out = torch.zeros(2 * 256 * 256, dtype=torch.uint8, device="cuda")
+    assert m.load().nvfp4_selftest_ue8m0_carry(m._ptr(out), m._stream()) == m.OK
+    got = host(out).reshape(2, 256, 256)  # [routine, c, b]
+    b = np.arange(256)[None, :]
+    c = np.arange(256)[:, None]
+    d = b - c
+    want = np.where((d >= 1) & (d <= 18), np.exp2((d - 10).astype(np.float64)), 0.0)
+    inside = d <= 18
+    for routine in range(2):
+        val = oracle.e4m3_values(got[routine])
+        assert np.array_equal(val[inside], np.broadcast_to(want, val.shape)[inside]), routine
+        assert not np.isnan(val).any()
 
 
-def test_carried_encoding_matches_e4m3():
-    """The test's encoder against the oracle's E4M3 decoding: every carried
-    byte decodes to exactly 2^(e - SHIFT), or to 0 below E4M3's range."""
-    b = np.arange(0, 139)
-    enc = carried_e4m3(b)
-    val = oracle.e4m3_values(enc)
-    want = np.where(b - 127 - SHIFT >= -9, np.exp2((b - 127 - SHIFT).astype(np.float64)), 0.0)
-    assert np.array_equal(val, want)
+def _row_shift(ue_bytes: np.ndarray) -> np.ndarray:
+    return np.maximum(ue_bytes.astype(np.int64).max(axis=1) - 18, 0)
 
 
-def check_ue8m0(m, layer, W, tokens=None):
-    w = device_weights(W)
+def check_ue8m0(m, layer, W, tokens=None, w13_in=None, w2_in=None):
+    w = device_weights(W, w13_in=w13_in, w2_in=w2_in)
     assert w.sf_format == m.SF_UE8M0
     out, ws = m.moe_forward(w, dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w),
                             flags=m.SYNC_CHECK | m.DEBUG_KEEP_H)
     torch.cuda.synchronize()
+    if w13_in is not None or w2_in is not None:
+        W = _with_input_scales(W, w13_in, w2_in)
     ref = oracle.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W, tokens=tokens)
     toks = np.arange(layer.T) if tokens is None else np.asarray(tokens)
     stats = {"out": assert_close(host(out)[toks], ref["out"][toks], "out")}
@@ -64,16 +69,25 @@ def check_ue8m0(m, layer, W, tokens=None):
     assert np.array_equal(host(it["offsets"]), ref["offsets"])
     prow = host(it["row_of"])[ref["perm"][ref["rows"]]]
     assert np.array_equal(host(it["a1q"])[prow], ref["a1q"]), "a1 codes"
-    assert np.array_equal(unswizzle(host(it["sf1"]), prow, H // 16, it["kc1"]), carried_e4m3(ref["sf1"])), \
-        "a1 scales (carried)"
+    assert np.array_equal(unswizzle(host(it["sf1"]), prow, H // 16, it["kc1"]), ref["sf1"]), "a1 UE8M0 scales"
     h_gpu = host(it["h"])[prow]
     stats["h"] = assert_close(h_gpu, ref["h"], "h")
     g2 = oracle.reciprocal_f32(W.w2_input_scale)[ref["row_expert"][ref["rows"]]]
     q2, s2 = oracle.quant_rows(h_gpu, g2, ue8m0=True)
     assert np.array_equal(host(it["a2q"])[prow], q2), "a2 codes (UE8M0 requantisation of the GPU's h)"
-    assert np.array_equal(unswizzle(host(it["sf2"]), prow, I // 16, it["kc2"]), carried_e4m3(s2)), \
-        "a2 scales (carried)"
+    assert np.array_equal(unswizzle(host(it["sf2"]), prow, I // 16, it["kc2"]), s2), "a2 UE8M0 scales"
+    stats["a1_row_span"] = int((ref["sf1"].max(axis=1).astype(int) - ref["sf1"].min(axis=1)).max())
     return stats
+
+
+def _with_input_scales(W, w13_in, w2_in):
+    import copy
+    W2 = copy.copy(W)
+    if w13_in is not None:
+        W2.w13_input_scale = np.asarray(w13_in, np.float32)
+    if w2_in is not None:
+        W2.w2_input_scale = np.asarray(w2_in, np.float32)
+    return W2
 
 
 def test_tiny_layer(m):
@@ -121,22 +135,36 @@ def test_prepared_format_must_match(m):
     assert bool((out == 2.0).all())
 
 
-def test_activation_scale_above_the_carried_range(m):
-    """An expert whose input scale is 16x too small puts its a1 block scales
-    above 2^11: the quantiser stops the call before either GEMM runs."""
+def test_activation_scales_far_from_calibration(m):
+    """Input scales 100 times too small (activations 100x the calibration
+    amax) on some experts and 10^4 times too large (10^-4 x) on others: every
+    block scale moves by the same power of two within its row, so the call is
+    computed, with the codes and scale bytes exact and out within tolerance."""
     layer, W = layer_with_weights(S.tiny(), ue8m0=True)
-    e = int(layer.topk_ids[0, 0])
     w13_in = W.w13_input_scale.copy()
-    w13_in[e] = np.float32(w13_in[e] / 16)
-    w = device_weights(W, w13_in=w13_in)
-    out = torch.full((layer.T, layer.H), 3.0, device="cuda")
-    with pytest.raises(m.Nvfp4Error) as ei:
-        m.moe_forward(w, dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w), out=out, flags=m.SYNC_CHECK)
-    assert ei.value.status == m.ERR_SCALE_RANGE
-    torch.cuda.synchronize()
-    assert bool((out == 3.0).all())
-    # the same weights with the calibrated scale run clean on the same device state
-    check_ue8m0(m, layer, W)
+    w2_in = W.w2_input_scale.copy()
+    w13_in[0] = np.float32(w13_in[0] / 100)
+    w13_in[1] = np.float32(w13_in[1] * 1e4)
+    w2_in[2] = np.float32(w2_in[2] / 100)
+    w2_in[3] = np.float32(w2_in[3] * 1e4)
+    check_ue8m0(m, layer, W, w13_in=w13_in, w2_in=w2_in)
+
+
+def test_rows_spanning_many_binades(m):
+    """Tokens whose 16-element blocks are scaled by 2^0, 2^-1, ..., 2^-20 along
+    the row: each row's scales span about 20 binades, so its smallest blocks
+    fall more than 17 binades below its largest and are carried as zero; their
+    share of out is below the tolerance, and every code and scale byte is
+    still exact."""
+    layer, W = layer_with_weights(S.tiny(), ue8m0=True)
+    x = (layer.x.astype(np.uint32) << 16).view(np.float32).copy()
+    nb = layer.H // 16
+    steps = np.exp2(-np.round(np.linspace(0, 20, nb))).astype(np.float32)
+    for t in range(0, layer.T, 3):
+        x[t] = (x[t].reshape(nb, 16) * steps[:, None]).reshape(-1)
+    layer.x = (x.view(np.uint32) >> 16).astype(np.uint16)  # exact: powers of two
+    stats = check_ue8m0(m, layer, W)
+    assert stats["a1_row_span"] >= 19, stats
 
 
 def test_host_entry_point(m):

@@ -59,7 +59,9 @@ def test_workspace_sizes(lib):
     assert m.intermediates_rows_cap(8192, E, k) >= R + E * 127
     assert m.intermediates_rows_cap(1, E, k) == 8 * 128
     # the two scale sets in the tensor-core layout, then a 256-byte slot for the format word
-    assert m.prepared_weights_size(E, H, I) == E * 11 * 44 * 512 + E * 22 * 12 * 512 + 256
+    # both scale layouts, then the UE8M0 weight-row factors (FP32 per row of w13 and w2), then the format word
+    factors = -(-(4 * E * (2 * I + H)) // 256) * 256
+    assert m.prepared_weights_size(E, H, I) == E * 11 * 44 * 512 + E * 22 * 12 * 512 + factors + 256
     assert m.quantize_workspace_size(4096, 8, 128) > 0
     assert m.moe_workspace_size(-1, H, I, E, k) == 0
 
