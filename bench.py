@@ -156,6 +156,93 @@ class ClockSampler:
                 "samples": len(sm), "samples_in_timed_region": len(inside)}
 
 
+class NvmlClockSampler:
+    """In-process, read-only NVML queries (SM clock, its maximum, and the
+    clock-event reasons) every `period_s` from a thread, stamped on arrival,
+    so that a timed region of a few milliseconds holds several samples.  No
+    setting of the GPU is changed.  `ok` is False when libnvidia-ml cannot be
+    loaded or the device is not found; the caller then falls back to
+    nvidia-smi."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, uuid: str | None, period_s: float = 0.001):
+        import ctypes
+        self.period = period_s
+        self.samples = []  # (time, sm_mhz, max_mhz, reason bits)
+        self.t_start = self.t_end = None
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            rc = (lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) if uuid
+                  else lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)))
+            if rc != 0:
+                return
+            self.lib, self.h, self.ct = lib, h, ctypes
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            self.reasons_fn = reasons or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _query(self):
+        c = self.ct
+        sm, mx, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, c.byref(sm)) != 0:  # NVML_CLOCK_SM
+            return None
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, c.byref(mx))
+        self.reasons_fn(self.h, c.byref(rs))
+        return (time.monotonic(), sm.value, mx.value, rs.value)
+
+    def _run(self):
+        while not self._stop.is_set():
+            q = self._query()
+            if q:
+                self.samples.append(q)
+            time.sleep(self.period)
+
+    def mark_start(self):
+        self.t_start = time.monotonic()
+
+    def mark_end(self):
+        self.t_end = time.monotonic()
+
+    def __enter__(self):
+        if self.ok:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+            time.sleep(0.05)
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            time.sleep(0.02)
+            self._stop.set()
+            self.thread.join(timeout=5)
+        return False
+
+    def summary(self):
+        inside = [q for q in self.samples
+                  if self.t_start is not None and self.t_end is not None and self.t_start <= q[0] <= self.t_end]
+        use = inside or self.samples
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({name for q in use for bit, name in self.REASONS.items() if q[3] & bit})
+        return {"sm_mhz": statistics.median(q[1] for q in use), "sm_max_mhz": max(q[2] for q in use),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside),
+                "source": f"NVML, in process, every {self.period * 1e3:g} ms"}
+
+
+def clock_sampler(uuid: str | None):
+    """NVML in process when available, else nvidia-smi."""
+    s = NvmlClockSampler(uuid)
+    return s if s.ok else ClockSampler(uuid)
+
+
 # --------------------------------------------------------------------------- workload
 def make_layer_device(layer, m, torch, seed: int, ue8m0: bool = False):
     """Device weights: N(0, 0.02) BF16 draws quantised on the device (UE8M0
@@ -269,7 +356,7 @@ def run_ours(args, rank, world):
     # records themselves lengthen by about 2 us each, so it does not set value.
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     pstart, pstop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(uuid if rank == 0 else None) as clocks:
+    with clock_sampler(uuid if rank == 0 else None) as clocks:
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
@@ -324,6 +411,7 @@ def run_ours(args, rank, world):
     router = router_leg(m, torch, args)
     ue8m0 = ue8m0_leg(m, torch, args)
     w4a16 = w4a16_leg(m, torch, w, layer, x, ids, tw, args)
+    stack = stack_leg(m, torch, args) if not args.no_stack else None
 
     pk = peaks()
     n_active = int((np.bincount(layer.topk_ids.ravel(), minlength=E) > 0).sum())
@@ -363,7 +451,11 @@ def run_ours(args, rank, world):
                    "scale_check": "device-side each step; host sync skipped in the timed steps",
                    "ms_per_step_with_host_scale_check": ms_checked},
         "roofline": roof,
-        "kernels": {n: {"ms": v, "share": v / sum(stage_ms.values())} for n, v in stage_ms.items()},
+        "kernels": {n: {"ms": v, "share": v / sum(stage_ms.values()),
+                        "algorithmic_bytes": alg[n]["bytes"],
+                        "gbs": alg[n]["bytes"] / (v * 1e-3) / 1e9,
+                        "frac_hbm": alg[n]["bytes"] / (v * 1e-3) / 1e9 / pk["hbm_gbs"]}
+                    for n, v in stage_ms.items()},
         "kernels_note": (f"per-kernel CUDA-event times from a second timed region of {K} steps with six "
                          f"events per step ({ms_step_profiled:.4f} ms per step there, against "
                          f"{ms_step:.4f} ms without the events)"),
@@ -379,12 +471,14 @@ def run_ours(args, rank, world):
         "router": router,
         "ue8m0": ue8m0,
         "w4a16": w4a16,
+        "stack": stack,
         "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * K,
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
+        line["cpu_baseline"]["oracle_timings"] = oracle_timings(args)
     if dist:
         dist.destroy_process_group()
     return line
@@ -616,7 +710,7 @@ def ue8m0_leg(m, torch, args):
     ms = s.elapsed_time(e) / n
     out["prefill_layer"] = {"T": layer.T, "ms_per_call": ms, "tokens_per_s": layer.T / (ms * 1e-3), "status": st,
                             "note": "UE8M0 block scales throughout (weights, a1, a2), carried to the tensor "
-                                    "cores as E4M3 powers of two"}
+                                    "cores as E4M3 powers of two relative to each operand row's largest"}
     del wu, outl, wsl
     return out
 
@@ -739,6 +833,107 @@ def cpu_baseline(args):
                       f"path, {dt:.1f} s"}
 
 
+def stack_leg(m, torch, args):
+    """The 30-layer stack: 30 decode-shaped layers (128 experts, 2816 x 704,
+    top-8) at 2048 tokens, each with its own device-drawn weights and its own
+    seeded routing (drawn independently of its input: the expert path only),
+    residual add + RMSNorm (eps 1e-6) between layers.  One step = all 30
+    layers (forward + normalisation each), timed with CUDA events; tokens/s =
+    2048 / step time."""
+    LAYERS, T = 30, 2048
+    layers = []
+    out = ws = None
+    for li in range(LAYERS):
+        L = S.stack_layer(li, T)
+        w, bf = make_layer_device(L, m, torch, seed=5004 + 100 * li)
+        del bf
+        x = torch.from_numpy(L.x.view(np.int16)).cuda().view(torch.bfloat16)
+        ids = torch.from_numpy(L.topk_ids).cuda()
+        tw = torch.from_numpy(L.topk_w).cuda()
+        calibrate_w2_on_device(m, torch, w, x, ids, tw, L)
+        m.prepare_weights(w)
+        if li == 0:
+            x0 = x
+            out = torch.empty((T, L.H), dtype=torch.float32, device="cuda")
+            ws = torch.empty(m.moe_workspace_size(T, L.H, L.I, L.E, L.k), dtype=torch.uint8, device="cuda")
+        layers.append((w, ids, tw))
+    xa, xb = x0.clone(), torch.empty_like(x0)
+    for (w, ids, tw) in layers:  # the checked pass: every layer's scale check with the host sync
+        m.moe_forward(w, xa, ids, tw, out=out, ws=ws, flags=m.SYNC_CHECK)
+        m.residual_rmsnorm(xa, out, 1e-6, x_next=xb)
+        xa, xb = xb, xa
+
+    def step():
+        nonlocal xa, xb
+        xa.copy_(x0)
+        for (w, ids, tw) in layers:
+            m.moe_forward(w, xa, ids, tw, out=out, ws=ws, flags=m.SCALES_PREVALIDATED)
+            m.residual_rmsnorm(xa, out, 1e-6, x_next=xb)
+            xa, xb = xb, xa
+
+    for _ in range(3):
+        step()
+    n = max(5, args.steps // 20)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(n):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    st, _ = m.moe_status(ws)
+    ms = a.elapsed_time(b) / n
+    res = {"layers": LAYERS, "T": T, "ms_per_stack": ms, "tokens_per_s": T / (ms * 1e-3),
+           "ms_per_layer": ms / LAYERS, "status": st, "steps": n,
+           "note": "each step: a 5.8 MB copy of the first input, then 30 x (expert forward + residual RMSNorm)"}
+    del layers, out, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def oracle_timings(args):
+    """The oracle on one core and on all cores: the tiny layer (whole path)
+    and the quantiser workload (routed-row quantisation of a bounded token
+    sample; GB/s over the same algorithmic bytes the GPU's figure uses)."""
+    import oracle as orc
+    orc.build()
+    tiny = S.tiny()
+    res = {}
+    W = orc.quantize_layer_weights(tiny)
+    q = S.quantiser()
+    ntok = min(q.T, args.oracle_quant_tokens)
+    xq, idq = q.x[:ntok], q.topk_ids[:ntok]
+    nbytes = ntok * q.H * 2 + ntok * q.k * q.H * (0.5 + 1 / 16) + ntok * q.k * 8
+    saved = os.environ.get("ORACLE_THREADS")
+    try:
+        for label, threads in (("1_core", 1), ("all_cores", 0)):
+            if threads:
+                os.environ["ORACLE_THREADS"] = str(threads)
+            elif saved is None:
+                os.environ.pop("ORACLE_THREADS", None)
+            else:
+                os.environ["ORACLE_THREADS"] = saved
+            t0 = time.perf_counter()
+            reps = 0
+            while reps < 3 or time.perf_counter() - t0 < 1.0:
+                orc.moe_forward(tiny.x, tiny.topk_ids, tiny.topk_w, W)
+                reps += 1
+            t_tiny = (time.perf_counter() - t0) / reps
+            t0 = time.perf_counter()
+            orc.quantize_experts(xq, idq, q.w13_input_scale, q.E)
+            t_q = time.perf_counter() - t0
+            res[label] = {"threads": orc.threads(),
+                          "tiny_layer": {"ms": t_tiny * 1e3, "tokens_per_s": tiny.T / t_tiny},
+                          "quantiser": {"tokens": ntok, "s": t_q, "gbs": nbytes / t_q / 1e9,
+                                        "tokens_per_s": ntok / t_q}}
+    finally:
+        if saved is None:
+            os.environ.pop("ORACLE_THREADS", None)
+        else:
+            os.environ["ORACLE_THREADS"] = saved
+    return res
+
+
 def run_reference(args, rank, world):
     """The reference arm: the CPU oracle, as it stands, on the host cores; each
     step is the whole expert path for a bounded token sample of the workload,
@@ -780,6 +975,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=1024)  # reference arm: largest token sample per step
     ap.add_argument("--cpu-seconds", type=float, default=15.0)  # cpu_baseline: CPU work to time
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stack", action="store_true")  # skip the 30-layer stack leg
+    ap.add_argument("--oracle-quant-tokens", type=int, default=512)  # oracle quantiser timing sample
     ap.add_argument("--tokens", type=int, default=8192,
                     help="prefill tokens (8192 is the benchmark workload; smaller values for ncu captures)")
     ap.add_argument("--only-w4a16", action="store_true",
