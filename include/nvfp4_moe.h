@@ -103,16 +103,16 @@ enum {
      * nvfp4_quantize_weights_format, prepared with nvfp4_prepare_weights_format
      * and NVFP4_SF_UE8M0), and both activation quantisations take UE8M0 scales
      * (see NVFP4_SF_UE8M0); every other step is unchanged.  The block-scaled
-     * FP4 tensor-core MMA is fed E4M3 scale bytes, whose powers of two span
-     * 18 binades (2^-9 .. 2^8), so each GEMM operand row -- a row of
+     * FP4 tensor-core MMA is fed E4M3 scale bytes, whose normal powers of two
+     * span 15 binades (2^-6 .. 2^8), so each GEMM operand row -- a row of
      * activations, or the weight row of one output column -- carries its
      * UE8M0 scales relative to its own largest one: that largest scale
      * travels as 2^8, the others as the same power of two below it, and the
      * epilogue multiplies the row's power of two back (an exact product, per
      * activation row and per output column).  Any scale in the UE8M0 range is
      * accepted, whatever the calibration.  A block whose scale is more than
-     * 17 binades below the largest of its own row contributes zero (its
-     * values are below 2^-17 of that row's largest block).  The intermediates
+     * 14 binades below the largest of its own row contributes zero (its
+     * values are below 2^-14 of that row's largest block).  The intermediates
      * (sf1, sf2 of nvfp4_moe_intermediates_of) hold the UE8M0 bytes.  The
      * prepared weights must match the flag (else NVFP4_ERR_INVALID_ARG on the
      * device, nothing written).  Not accepted by nvfp4_moe_forward_w4a16. */
@@ -456,7 +456,7 @@ long long nvfp4_selftest_block_division(int nthreads);
  * 0 .. 255: out (device, 131072 bytes, 4-byte aligned) receives
  * out[c * 256 + b] from the one-byte routine the weight preparation uses and
  * out[65536 + c * 256 + b] from the four-byte routine the GEMM uses.  The
- * carried byte is the E4M3 encoding of 2^(b - c - 10) when 1 <= b - c <= 18,
+ * carried byte is the E4M3 encoding of 2^(b - c - 7) when 1 <= b - c <= 15,
  * and 0 when b <= c.  Synchronous.  NVFP4_ERR_INVALID_ARG for a null or
  * misaligned `out`.
  */

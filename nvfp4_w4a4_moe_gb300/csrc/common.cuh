@@ -193,44 +193,39 @@ __device__ __forceinline__ uint2 quant_block16_ue8m0(const f32x2 (&x)[8], float 
 }
 
 // UE8M0 scales carried to the tensor cores, one window per GEMM row.  The
-// block-scaled FP4 MMA is given E4M3 scale bytes, whose powers of two span
-// 2^-9 .. 2^8 (18 binades).  Each operand row (a row of activations, or the
-// weight row of one output column) carries its UE8M0 bytes b relative to its
-// own largest byte m: with the row's shift c = max(m - 18, 0), byte b travels
-// as the E4M3 encoding of 2^(b - c - 10) when d = b - c lies in 1 .. 18
-// (2^-9 .. 2^8), and as 0 when d <= 0, i.e. when the block's scale is more
-// than 17 binades below the row's largest (its values are below 2^-17 of the
-// row's largest block).  The true scale is the carried one times 2^(c - 117),
-// a power of two the GEMM epilogue multiplies back per row and per column: an
-// exact product, so nothing depends on the global calibration and no scale
-// is out of range.
+// block-scaled FP4 MMA is given E4M3 scale bytes; its normal powers of two
+// span 2^-6 .. 2^8 (15 binades, exponent fields 1 .. 15, mantissa 0).  Each
+// operand row (a row of activations, or the weight row of one output column)
+// carries its UE8M0 bytes b relative to its own largest byte m: with the
+// row's shift c = max(m - 15, 0), byte b travels as the E4M3 byte with
+// exponent field d = b - c, i.e. the value 2^(b - c - 7), when d lies in
+// 1 .. 15, and as 0 when d <= 0 -- a block whose scale is more than 14
+// binades below the row's largest (its values are below 2^-14 of the row's
+// largest block).  The true scale is the carried one times 2^(c - 120), a
+// power of two the GEMM epilogue multiplies back per row and per column: an
+// exact product, so nothing depends on the global calibration and no scale is
+// out of range.
 __device__ __forceinline__ uint32_t ue8m0_row_shift(uint32_t row_max_byte)
 {
-    return row_max_byte > 18u ? row_max_byte - 18u : 0u;
+    return row_max_byte > 15u ? row_max_byte - 15u : 0u;
 }
-// 2^(c - 117) for a row shift c in 0 .. 236 (a normal float).
-__device__ __forceinline__ float ue8m0_row_factor(uint32_t c) { return __uint_as_float((c + 10u) << 23); }
+// 2^(c - 120) for a row shift c in 0 .. 239 (a normal float).
+__device__ __forceinline__ float ue8m0_row_factor(uint32_t c) { return __uint_as_float((c + 7u) << 23); }
 // Row shift back from its factor.
-__device__ __forceinline__ uint32_t ue8m0_shift_of_factor(float f) { return (__float_as_uint(f) >> 23) - 10u; }
-// One byte carried with row shift c.
+__device__ __forceinline__ uint32_t ue8m0_shift_of_factor(float f) { return (__float_as_uint(f) >> 23) - 7u; }
+// One byte carried with row shift c.  Bytes of a row never exceed its largest,
+// so d <= 15; the mask only bounds the bytes of unused (padding) rows.
 __device__ __forceinline__ uint32_t ue8m0_carried(uint32_t b, uint32_t c)
 {
-    uint32_t d = b > c ? b - c : 0u;
-    d = d < 18u ? d : 18u;  // b <= the row's largest byte keeps d <= 18; bytes of unused rows are clamped
-    if (d == 0u) return 0u;
-    if (d <= 3u) return 1u << (d - 1u);  // subnormal: 2^(d-10) = (1 << (d-1)) * 2^-9
-    return (d - 3u) << 3;                // normal: exponent field d - 3, mantissa 0
+    const uint32_t d = b > c ? b - c : 0u;
+    return (d & 15u) << 3;
 }
-// Four bytes (one 32-bit word) carried with the row shift c4 (c in every byte).
+// Four bytes (one 32-bit word) carried with the row shift c4 (c in every
+// byte): a saturating byte-wise subtraction, then each 4-bit result moved to
+// the exponent field (no byte overflows into its neighbour).
 __device__ __forceinline__ uint32_t ue8m0_carried4(uint32_t w, uint32_t c4)
 {
-    uint32_t d = __vsubus4(w, c4);               // b - c, saturated at 0
-    d = __vminu4(d, 0x12121212u);                // <= 18
-    const uint32_t normal = __vsubus4(d, 0x03030303u) << 3;  // (d - 3) << 3 where d >= 4, else 0 (bytes <= 15 << 3)
-    const uint32_t le3 = __vcmpleu4(d, 0x03030303u);          // 0xFF where d <= 3
-    const uint32_t eq3 = __vcmpeq4(d, 0x03030303u);
-    const uint32_t sub = (d + (eq3 & 0x01010101u)) & le3;     // d = 1, 2, 3 -> 1, 2, 4 (d + 1 <= 4: no carry)
-    return normal | sub;
+    return (__vsubus4(w, c4) & 0x0F0F0F0Fu) << 3;
 }
 
 // Programmatic dependent launch.  A kernel launched with launch_pdl may be

@@ -424,15 +424,26 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         uint32_t stage = 0, phase = 0;
         bool ok = true;
+        // UE8M0: word q of this lane's 16 bytes holds row q * 32 + lane of
+        // the m-tile; its bytes are carried with that row's shift.  The rows'
+        // largest bytes are loaded one tile ahead, off the stage's path.
+        int rmax_next[4] = {0, 0, 0, 0};
+        if (UE && n_i > 0) {
+            const int mt0 = seq_tile<EPI>(p, 0, NT, MT, paired).mt;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) rmax_next[q] = __ldg(p.a_row_max + mt0 * BM + q * 32 + lane);
+        }
         for (int i = 0; i < n_i && ok; ++i) {
             const TileInfo<EPI> ti = seq_tile<EPI>(p, i, NT, MT, paired);
-            // UE8M0: word q of this lane's 16 bytes holds row q * 32 + lane
-            // of the m-tile; its bytes are carried with that row's shift
             uint32_t c4[4] = {0u, 0u, 0u, 0u};
             if (UE) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    c4[q] = ue8m0_row_shift((uint32_t)__ldg(p.a_row_max + ti.mt * BM + q * 32 + lane)) * 0x01010101u;
+                for (int q = 0; q < 4; ++q) c4[q] = ue8m0_row_shift((uint32_t)rmax_next[q]) * 0x01010101u;
+                if (i + 1 < n_i) {
+                    const int mt1 = seq_tile<EPI>(p, i + 1, NT, MT, paired).mt;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) rmax_next[q] = __ldg(p.a_row_max + mt1 * BM + q * 32 + lane);
+                }
             }
             for (int kt = 0; kt < KT; ++kt) {
                 if (!mbar_wait(&full[stage], phase, abort_flag, kWaitLimitNs)) {
@@ -532,9 +543,29 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                 s1 = 0.0f;
                 t = valid ? f / p.k : 0;
             }
-            // UE8M0: the A row's carried scales take 2^(shift - 117) back (an
-            // exact product; the weight rows' factors are applied per column)
-            if (UE) s0 *= ue8m0_row_factor(ue8m0_row_shift((uint32_t)p.a_row_max[row]));
+            // UE8M0: the A row's carried scales take 2^(shift - 120) back (an
+            // exact product), and the weight rows' factors are applied per
+            // column.  Those are loaded here, before the accumulator wait, one
+            // column per lane: w13 lane l holds the gate and up factors of
+            // columns l and 32 + l of this warp's slice, w2 the four columns
+            // it reduces in each 32-column chunk.
+            float4 colf[2] = {make_float4(1.f, 1.f, 1.f, 1.f), make_float4(1.f, 1.f, 1.f, 1.f)};
+            if (UE) {
+                s0 *= ue8m0_row_factor(ue8m0_row_shift((uint32_t)p.a_row_max[row]));
+                if (EPI == 0) {
+                    const int w0 = part * (ti.hc / (P::NUM_EPI_WARPS / 4));
+                    const float *fg = p.b_row_factor + (size_t)e * p.N + 128 * nt + w0;
+                    const int hw = ti.hc / (P::NUM_EPI_WARPS / 4);
+                    colf[0].x = fg[lane];
+                    colf[0].y = fg[p.gate_up_I + lane];
+                    colf[0].z = hw > 32 ? fg[32 + lane] : 1.f;
+                    colf[0].w = hw > 32 ? fg[p.gate_up_I + 32 + lane] : 1.f;
+                } else {
+                    const float *fc = p.b_row_factor + (size_t)e * p.N + nt * 128 + (lane & 7) * 4;
+                    colf[0] = __ldg(reinterpret_cast<const float4 *>(fc + 64 * half));
+                    colf[1] = __ldg(reinterpret_cast<const float4 *>(fc + 64 * half + 32));
+                }
+            }
             if (!mbar_wait(&acc_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
                 ok = false;
                 break;
@@ -551,8 +582,6 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                 const f32x2 aa = pack_f32x2(alpha, alpha);
                 const int hw = ti.hc / (P::NUM_EPI_WARPS / 4), w0 = part * hw;
                 const int nblocks = hw >> 4;  // blocks of 16 of this warp
-                // UE8M0: factors of the gate and up weight rows of this warp's columns
-                const float *fgate = UE ? p.b_row_factor + (size_t)e * p.N + 128 * nt + w0 : nullptr;
                 f32x2 h[4][8];
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -573,8 +602,11 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                         f32x2 gs = mul_f32x2(pack_f32x2(gate[2 * i], gate[2 * i + 1]), aa);
                         f32x2 us = mul_f32x2(pack_f32x2(up[2 * i], up[2 * i + 1]), aa);
                         if (UE) {
-                            gs = mul_f32x2(gs, __ldg(reinterpret_cast<const float2 *>(fgate + 32 * c + 2 * i)));
-                            us = mul_f32x2(us, __ldg(reinterpret_cast<const float2 *>(fgate + p.gate_up_I + 32 * c + 2 * i)));
+                            const float fg = c == 0 ? colf[0].x : colf[0].z, fu = c == 0 ? colf[0].y : colf[0].w;
+                            gs = mul_f32x2(gs, pack_f32x2(__shfl_sync(0xffffffffu, fg, 2 * i),
+                                                          __shfl_sync(0xffffffffu, fg, 2 * i + 1)));
+                            us = mul_f32x2(us, pack_f32x2(__shfl_sync(0xffffffffu, fu, 2 * i),
+                                                          __shfl_sync(0xffffffffu, fu, 2 * i + 1)));
                         }
                         h[2 * c + (i >> 3)][i & 7] = mul_f32x2(pack_f32x2(silu(lo_f32(gs)), silu(hi_f32(gs))), us);
                     }
@@ -641,30 +673,21 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                         mbar_arrive(&acc_empty[acc]);
                     }
                     float4 *xrow = reinterpret_cast<float4 *>(xp + lane * XPOSE_LD);
-                    if (UE) {
-                        // the weight rows' factors of these 32 output columns
-                        const float4 *cf =
-                            reinterpret_cast<const float4 *>(p.b_row_factor + (size_t)e * p.N + nt * 128 + cbase);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 f = __ldg(cf + j);
-                            xrow[j ^ (lane & 7)] = make_float4(v[4 * j] * scale * f.x, v[4 * j + 1] * scale * f.y,
-                                                               v[4 * j + 2] * scale * f.z, v[4 * j + 3] * scale * f.w);
-                        }
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            xrow[j ^ (lane & 7)] = make_float4(v[4 * j] * scale, v[4 * j + 1] * scale,
-                                                               v[4 * j + 2] * scale, v[4 * j + 3] * scale);
-                    }
+                    for (int j = 0; j < 8; ++j)
+                        xrow[j ^ (lane & 7)] = make_float4(v[4 * j] * scale, v[4 * j + 1] * scale,
+                                                           v[4 * j + 2] * scale, v[4 * j + 3] * scale);
                     __syncwarp();
 #pragma unroll
                     for (int it = 0; it < 8; ++it) {
                         const int rr = it * 4 + sub;
                         const int t_r = __shfl_sync(0xffffffffu, t, rr);
                         const int ok_r = __shfl_sync(0xffffffffu, (int)valid, rr);
-                        const float4 src =
-                            reinterpret_cast<const float4 *>(xp + rr * XPOSE_LD)[(lane & 7) ^ (rr & 7)];
+                        float4 src = reinterpret_cast<const float4 *>(xp + rr * XPOSE_LD)[(lane & 7) ^ (rr & 7)];
+                        if (UE) {  // the weight rows' factors of this lane's four columns (exact products)
+                            const float4 f = c2 == 0 ? colf[0] : colf[1];
+                            src = make_float4(src.x * f.x, src.y * f.y, src.z * f.z, src.w * f.w);
+                        }
                         if (ok_r)
                             red_add_v4(p.out + (size_t)t_r * p.H + nt * 128 + cbase + cc, src.x, src.y, src.z,
                                        src.w);

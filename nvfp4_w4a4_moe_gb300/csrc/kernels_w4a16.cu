@@ -495,7 +495,6 @@ __global__ void __launch_bounds__(WPlan<EPI>::NUM_THREADS, 1)
                 // a time, transposed through shared memory so each reduction
                 // covers four contiguous 128-byte row segments
                 const int sub = lane >> 3, cc = (lane & 7) * 4;
-#pragma unroll 1
                 constexpr int CW = 128 / P::Q_PARTS;  // columns of this warp
                 for (int c2 = 0; c2 < CW / 32; ++c2) {
                     const int cbase = CW * part + 32 * c2;

@@ -1,7 +1,7 @@
 """GPU parity of the UE8M0 variant of the expert forward (power-of-two block
 scales on the weights, a1 and a2) against the oracle, through the C ABI.
 
-The tensor cores take E4M3 scale bytes, whose powers of two span 18 binades,
+The tensor cores take E4M3 scale bytes, whose normal powers of two span 15 binades,
 so each GEMM operand row carries its UE8M0 scales relative to its own largest
 one and the epilogue multiplies that power of two back.  Bit-exact: a1 and a2
 codes and their UE8M0 scale bytes, and the carry of every (byte, row shift)
@@ -32,24 +32,20 @@ def m():
 def test_row_carry_matches_its_definition(m):
     """Both device carry routines, for every byte b and row shift c: the E4M3
     value of the carried byte (decoded by the oracle's E4M3 decoder) is
-    2^(b - c - 10) when 1 <= b - c <= 18 and 0 when b <= c.  (b - c > 18 does
-    not occur: the shift is the row's largest byte minus 18.)"""
+    2^(b - c - 7) when 1 <= b - c <= 15 and 0 when b <= c.  (b - c > 15 does
+    not occur: the shift is the row's largest byte minus 15.)"""
     out = torch.zeros(2 * 256 * 256, dtype=torch.uint8, device="cuda")
     assert m.load().nvfp4_selftest_ue8m0_carry(m._ptr(out), m._stream()) == m.OK
     got = host(out).reshape(2, 256, 256)  # [routine, c, b]
     b = np.arange(256)[None, :]
     c = np.arange(256)[:, None]
     d = b - c
-    want = np.where((d >= 1) & (d <= 18), np.exp2((d - 10).astype(np.float64)), 0.0)
-    inside = d <= 18
+    want = np.where((d >= 1) & (d <= 15), np.exp2((d - 7).astype(np.float64)), 0.0)
+    inside = d <= 15
     for routine in range(2):
         val = oracle.e4m3_values(got[routine])
         assert np.array_equal(val[inside], np.broadcast_to(want, val.shape)[inside]), routine
         assert not np.isnan(val).any()
-
-
-def _row_shift(ue_bytes: np.ndarray) -> np.ndarray:
-    return np.maximum(ue_bytes.astype(np.int64).max(axis=1) - 18, 0)
 
 
 def check_ue8m0(m, layer, W, tokens=None, w13_in=None, w2_in=None):
@@ -153,7 +149,7 @@ def test_activation_scales_far_from_calibration(m):
 def test_rows_spanning_many_binades(m):
     """Tokens whose 16-element blocks are scaled by 2^0, 2^-1, ..., 2^-20 along
     the row: each row's scales span about 20 binades, so its smallest blocks
-    fall more than 17 binades below its largest and are carried as zero; their
+    fall more than 14 binades below its largest and are carried as zero; their
     share of out is below the tolerance, and every code and scale byte is
     still exact."""
     layer, W = layer_with_weights(S.tiny(), ue8m0=True)
