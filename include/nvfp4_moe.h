@@ -117,6 +117,16 @@ enum {
      * prepared weights must match the flag (else NVFP4_ERR_INVALID_ARG on the
      * device, nothing written).  Not accepted by nvfp4_moe_forward_w4a16. */
     NVFP4_UE8M0_SCALES = 8u,
+    /* The w13 GEMM form.  By default the library chooses: from 512 routed
+     * rows per expert on average (T*k >= 512*E), the tiles are computed by
+     * pairs of CTAs (thread-block clusters of two sharing each tensor-core
+     * MMA, M = 256: each CTA loads its own 128 activation rows and half of
+     * the weight tile), with every expert's rows padded to 256; below that,
+     * by single CTAs with rows padded to 128.  These flags force one form
+     * (both together: NVFP4_ERR_INVALID_ARG).  The result is the same up to
+     * the order of the FP32 accumulation inside the tensor cores. */
+    NVFP4_W13_ONE_SM = 16u,
+    NVFP4_W13_TWO_SM = 32u,
 };
 
 /* One-line description of the last error raised on the calling thread. */
@@ -337,7 +347,8 @@ int nvfp4_moe_status(const void *ws, nvfp4_stream_t stream, int *first_bad_host)
  *   a1q [rows_cap, H/2], sf1 (swizzled, ceil(H/64) tiles per 128 rows),
  *   a2q [rows_cap, I/2], sf2 (swizzled, 4*ceil(I/256) tiles per 128 rows),
  *   row_of [R] (routed row f -> padded permuted row), offsets [E+1] (compact),
- *   pad_offsets [E+1] (padded: every expert starts on a 128-row boundary),
+ *   pad_offsets [E+1] (padded: every expert starts on a 128-row boundary,
+ *   or a 256-row boundary when the w13 GEMM ran on CTA pairs),
  *   h [rows_cap, I] FP32, the SiLU(gate)*up intermediate (written only when
  *   a forward ran with NVFP4_DEBUG_KEEP_H, which needs
  *   nvfp4_moe_host_workspace_size(...) + rows_cap*I*4 bytes of workspace).

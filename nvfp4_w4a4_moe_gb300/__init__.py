@@ -24,6 +24,7 @@ SF_E4M3 = 0
 LOGITS_F32, LOGITS_BF16 = 0, 1
 SF_UE8M0 = 4
 SCALES_PREVALIDATED, SYNC_CHECK, DEBUG_KEEP_H, UE8M0_SCALES = 1, 2, 4, 8
+W13_ONE_SM, W13_TWO_SM = 16, 32  # force the w13 GEMM form (default: chosen from the rows per expert)
 
 _lib = None
 _lock = threading.Lock()
@@ -493,7 +494,7 @@ def intermediates_rows_cap(T: int, E: int, k: int) -> int:
     R = T * k
     if R == 0:
         return 0
-    return ((R + min(R, E) * 127) + 127) // 128 * 128
+    return ((R + min(R, E) * 255) + 255) // 256 * 256
 
 
 def intermediates_of(ws: torch.Tensor, T: int, H: int, I: int, E: int, k: int) -> dict:

@@ -101,8 +101,10 @@ WsLayout make_layout(int T, int H, int I, int E, int k)
     L.T = T, L.H = H, L.I = I, L.E = E, L.k = k;
     L.R = T * k;
     const long long R = L.R;
+    // rows padded per expert to 256 (the paired w13 GEMM) at most: every busy
+    // expert may end on a partial 256-row block
     const long long busy = R < E ? R : E;
-    L.rows_cap = R == 0 ? 0 : (int)(((R + busy * 127) + 127) / 128 * 128);
+    L.rows_cap = R == 0 ? 0 : (int)(((R + busy * 255) + 255) / 256 * 256);
     L.mtiles_cap = L.rows_cap / 128;
     L.nchunks = (int)((R + kRouteChunk - 1) / kRouteChunk);
     if (L.nchunks < 1) L.nchunks = 1;
@@ -127,6 +129,7 @@ WsLayout make_layout(int T, int H, int I, int E, int k)
     L.perm = take(sizeof(int) * (size_t)R);
     L.row_src = take(sizeof(int) * (size_t)L.rows_cap);
     L.tile_expert = take(sizeof(int) * (size_t)L.mtiles_cap);
+    L.live_mtiles = take(sizeof(int) * (size_t)L.mtiles_cap);
     L.row_max = take(sizeof(int) * 2 * (size_t)L.rows_cap);  // UE8M0: a1 rows, then a2 rows
     L.a1q = take((size_t)L.rows_cap * (H / 2));
     L.sf1 = take((size_t)L.mtiles_cap * L.kc1 * 512);
@@ -369,6 +372,7 @@ int nvfp4_quantize_experts(const uint16_t *x, int T, int H, const int32_t *topk_
     ra.perm = perm;
     ra.row_src = nullptr;
     ra.offsets_out = expert_offsets;
+    ra.pad_rows = 128;
     ra.padded = 0;
     ra.hdr = hdr;
     NV_CUDA(launch_route(ra, st), "launching the token reorder");
@@ -494,6 +498,14 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     if (ws_bytes < L.end) return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "workspace %zu < %zu", ws_bytes, L.end);
     const bool keep_h = (flags & NVFP4_DEBUG_KEEP_H) != 0;
     const bool ue = (flags & NVFP4_UE8M0_SCALES) != 0;
+    if ((flags & NVFP4_W13_ONE_SM) && (flags & NVFP4_W13_TWO_SM))
+        return fail(NVFP4_ERR_INVALID_ARG, "NVFP4_W13_ONE_SM and NVFP4_W13_TWO_SM together");
+    // w13 on CTA pairs when experts hold many rows on average: the rows are
+    // then padded to 256 per expert, which costs a 128-row tile of padding on
+    // about half the experts; with few rows per expert that costs more than
+    // the pairs save
+    const bool pairs = (flags & NVFP4_W13_TWO_SM) ||
+                       (!(flags & NVFP4_W13_ONE_SM) && (long long)T * k >= kPairRowsPerExpert * (long long)E);
     if (keep_h && ws_bytes < L.host_end + (size_t)L.rows_cap * I * sizeof(float))
         return fail(NVFP4_ERR_WORKSPACE_TOO_SMALL, "NVFP4_DEBUG_KEEP_H needs the host workspace size + rows_cap*I*4");
     if (T == 0) return NVFP4_OK;
@@ -540,6 +552,8 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     int *row_max = reinterpret_cast<int *>(base + L.row_max);  // UE8M0: a1 rows, then a2 rows
     ra.row_max = ue ? row_max : nullptr;
     ra.rows_cap = L.rows_cap;
+    ra.pad_rows = pairs ? 256 : 128;
+    ra.live_mtiles = pairs ? reinterpret_cast<int *>(base + L.live_mtiles) : nullptr;
     ra.padded = 1;
     ra.hdr = hdr;
     // The routing returns at once when the check has failed, so it may be
@@ -617,6 +631,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     ga.H = H;
     ga.hdr = hdr;
     ga.mtiles_cap = L.mtiles_cap;
+    ga.pairs = pairs ? 1 : 0;
     NV_CUDA(launch_gemm_w13(ga, st), "launching the w13 GEMM");
     NV_CUDA(mark(4), "recording an event");
 
@@ -635,6 +650,8 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     gb.row_src = ra.row_src;
     gb.topk_w = topk_w;
     gb.out = out;
+    gb.pairs = 0;
+    gb.live_mtiles = ra.live_mtiles;  // with 256-row padding, the m-tiles that hold rows
     if (ue) {
         gb.a_row_max = row_max + L.rows_cap;
         gb.out_row_max = nullptr;
@@ -946,6 +963,7 @@ int nvfp4_moe_forward_w4a16(const nvfp4_moe_weights *w, const void *prepared, co
     ra.row_of = reinterpret_cast<int *>(base + L.row_of);
     ra.perm = reinterpret_cast<int *>(base + L.perm);
     ra.row_src = reinterpret_cast<int *>(base + L.row_src);
+    ra.pad_rows = 128;
     ra.padded = 1;
     ra.hdr = hdr;
     NV_CUDA(launch_validate_route(va, ra, st), "launching the scale check and the token reorder");

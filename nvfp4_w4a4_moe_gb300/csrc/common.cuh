@@ -43,7 +43,8 @@ struct DevHeader {
     int error_flags;     // kErr* bits below
     int num_mtiles;      // 128-row tiles of the padded permuted rows
     unsigned done_count; // CTAs of the routing histogram that finished
-    int pad[58];
+    int num_live_mtiles; // 128-row tiles holding at least one row (fewer than num_mtiles with 256-row padding)
+    int pad[57];
 };
 static_assert(sizeof(DevHeader) == 256, "header is one 256-byte slot");
 

@@ -17,7 +17,7 @@ struct WsLayout {
     int rows_cap, mtiles_cap, nchunks;
     int kc1, kc2;  // 64-element scale chunks per 128-row tile for a1 (H) and a2 (I)
     size_t hdr, g1, g2, alpha1, alpha2, counts, offsets, pad_off, chunk_hist, row_of, perm, row_src,
-        tile_expert, row_max, a1q, sf1, a2q, sf2, end;
+        tile_expert, live_mtiles, row_max, a1q, sf1, a2q, sf2, end;
     // forward_host staging (after `end`), and the optional FP32 h dump
     size_t x_stage, ids_stage, w_stage, out_stage, status_stage, host_end;
 };
@@ -25,6 +25,13 @@ struct WsLayout {
 constexpr int kMaxHostChunks = 8;  // token chunks of the pipelined host entry point
 
 constexpr int kRouteChunk = 2048;  // routed rows per routing CTA
+
+// The w13 GEMM runs on CTA pairs (rows padded to 256 per expert) from this many
+// routed rows per expert on average; below it, on single CTAs.  Measured on the
+// 128-expert layer: pairs take 156 us against 160 at 8192 tokens (512 rows per
+// expert), but 107 against 100 at 4096 and 84 against 71 at 2048, where the
+// padding to 256 rows costs more than the pairs save.
+constexpr long long kPairRowsPerExpert = 512;
 
 WsLayout make_layout(int T, int H, int I, int E, int k);
 
@@ -51,6 +58,8 @@ struct RouteArgs {
     int *offsets_out;  // caller copy of the compact offsets (nullable)
     int *row_max;      // UE8M0 forward: two arrays of rows_cap ints set to 0 for every padded row (nullable)
     int rows_cap;
+    int pad_rows;      // expert row padding: 128, or 256 for the 2-SM w13 GEMM (m-tile pairs of one expert)
+    int *live_mtiles;  // the 128-row m-tiles that hold rows, in order (nullable); count in hdr->num_live_mtiles
     int padded;
     DevHeader *hdr;
 };
@@ -126,6 +135,8 @@ struct GemmArgs {
     float *out;
     DevHeader *hdr;
     int mtiles_cap;
+    int pairs;                 // w13: CTA pairs on m-tile pairs (rows padded to 256 per expert)
+    const int *live_mtiles;    // w2: the m-tiles holding rows, in order (nullable: all m-tiles)
 };
 cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st);
 cudaError_t launch_gemm_w2(const GemmArgs &a, cudaStream_t st);

@@ -70,17 +70,29 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 //       take alternate tiles (one accumulator each), so one group is issuing
 //       the combine's reductions while the other waits on TMEM and fetches
 //       its rows' tokens and weights; each warp has a transpose buffer.
-template <int EPI>
+//  w13, CTA2: the same tiles computed by a pair of CTAs (a cluster of two) on
+//       two m-tiles of one expert: one M256 N256 MMA per 64-K step
+//       (tcgen05 .cta_group::2, issued by rank 0).  Each CTA loads its own
+//       m-tile's A and scales, half of B (rank 0 the gate rows, rank 1 the up
+//       rows) and all of B's scales (the pair MMA reads the B scales of all N
+//       from each CTA's tensor memory); its accumulator holds its 128 rows.
+//       38 KB per stage per CTA instead of 54, a 5-stage ring, and sixteen
+//       epilogue warps.
+template <int EPI, bool CTA2 = false>
 struct Plan {
     static constexpr int BN = EPI == 0 ? 256 : 128;  // widest tile (MMA N)
-    static constexpr int STAGES = 4;
-    static constexpr int NUM_EPI_WARPS = EPI == 0 ? 8 : 16;
+    static constexpr int STAGES = CTA2 ? 5 : 4;
+    // w13 pairs: 16 epilogue warps of 32 columns each, so every warp releases
+    // the accumulator after a single TMEM load (the pair form's stages are
+    // shorter, and the release gates the next tile's MMAs); 8 for w13 on
+    // single CTAs, where 16 measured no faster
+    static constexpr int NUM_EPI_WARPS = EPI == 0 ? (CTA2 ? 16 : 8) : 16;
     static constexpr int EPI_THREADS = 32 * NUM_EPI_WARPS;
     static constexpr int EPI_GROUPS = EPI == 0 ? 1 : 2;  // w2: one group of eight warps per accumulator
     static constexpr int SCALE_WARP0 = 2 + NUM_EPI_WARPS;  // then the four scale writers
     static constexpr int NUM_THREADS = 64 + EPI_THREADS + 32 * NUM_SCALE_WARPS;
     static constexpr int ACC_BUFS = EPI == 0 ? 1 : 2;
-    static constexpr int B_BYTES = BN * BK / 2;
+    static constexpr int B_BYTES = (CTA2 ? BN / 2 : BN) * BK / 2;  // B rows this CTA loads per stage
     // w2: A lives in a ring of slots of its own, outside the B ring, so that a
     // tile pair (two column blocks of one m-tile) loads it once.  Fill f (one
     // 256-K stage of one m-tile) takes slot f % A_SLOTS and completes on the
@@ -109,6 +121,7 @@ struct Plan {
     static_assert(EPI_GROUPS == ACC_BUFS, "each epilogue group owns one accumulator");
     static_assert(OFF_B % 1024 == 0 && OFF_AS % 1024 == 0, "128-byte-swizzled operands start on 1024 bytes");
     static_assert(EPI == 0 || (A_SLOTS == 5 && STAGES == 4), "the A-slot reuse argument is for 5 slots, 4 stages");
+    static_assert(!CTA2 || EPI == 0, "CTA pairs: w13 only");
     static_assert(SMEM_BYTES + (EPI == 0 ? (int)sizeof(DivTable2) : 0) <= 232448,
                   "shared memory plan exceeds the opt-in limit");
 };
@@ -116,9 +129,9 @@ struct Plan {
 // Instruction descriptor, block-scaled kinds: E2M1 A and B (code 1 at bits
 // 7-9 and 10-12), K-major both, N>>3 at 17-22, scale type UE4M3 (bit 23 = 0),
 // M>>4 at 24-28, scale-factor ids 0.
-__host__ __device__ constexpr uint32_t idesc_for(int n)
+__host__ __device__ constexpr uint32_t idesc_for(int n, int m = BM)
 {
-    return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+    return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
@@ -127,6 +140,19 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+}
+// The pair's form (.cta_group::2, M256): A from both CTAs' shared memory at
+// the same offsets (128 rows each), B half from each, D and the scale
+// factors in each CTA's tensor memory at the same addresses.
+__device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                            uint32_t sfb, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
             d),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
         : "memory");
@@ -146,6 +172,10 @@ struct TileInfo {
     int hc;    // w13: h columns of the tile (128 or 64)
     int nblk;  // 128-row scale blocks of the B tile (w13 full: 2, else 1)
 };
+// w2 walks the m-tiles that hold rows (live_mtiles, when the rows are padded
+// to 256 for the paired w13) in order.
+__device__ __forceinline__ int mtile_of(const GemmArgs &p, int mi) { return p.live_mtiles ? p.live_mtiles[mi] : mi; }
+
 template <int EPI>
 __device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, int NT, int MT)
 {
@@ -161,7 +191,7 @@ __device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, 
         // contributions to each row; an expert's m-tiles stay adjacent, so its
         // B tile is reused from L2
         ti.nt = tile / MT;
-        ti.mt = tile - ti.nt * MT;
+        ti.mt = mtile_of(p, tile - ti.nt * MT);
     }
     ti.e = p.tile_expert[ti.mt];
     if (EPI == 0) {
@@ -179,14 +209,22 @@ __device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, 
 // (m-tile, pair of adjacent output column blocks) in column-pair-major order,
 // unit (i/2) * gridDim + blockIdx, column block 2 * pair + (i & 1); the two
 // tiles of a unit run back to back and share the A operand.
-template <int EPI>
+template <int EPI, bool CTA2 = false>
 __device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int NT, int MT, bool paired)
 {
+    if (CTA2) {
+        // unit (m-tile pair, column tile), pair-major; this CTA's m-tile of the pair
+        const int G = (int)gridDim.x >> 1, b = (int)blockIdx.x >> 1;
+        TileInfo<EPI> ti = tile_info<EPI>(p, b + i * G, NT, MT);
+        ti.mt = 2 * ti.mt + (int)(blockIdx.x & 1);
+        ti.e = p.tile_expert[ti.mt];
+        return ti;
+    }
     if (EPI == 1 && paired) {
         const int u = (i >> 1) * (int)gridDim.x + (int)blockIdx.x;
         const int g = u / MT;
         TileInfo<EPI> ti;
-        ti.mt = u - g * MT;
+        ti.mt = mtile_of(p, u - g * MT);
         ti.nt = 2 * g + (i & 1);
         ti.e = p.tile_expert[ti.mt];
         ti.hc = 0;
@@ -204,12 +242,12 @@ __device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int 
 // prepared.  The epilogue multiplies both rows' factors back: the A row's
 // into the row scale, the weight row's per output column.  w13 then writes
 // a2 as UE8M0 bytes with each row's largest byte (out_row_max).
-template <int EPI, bool UE>
-__global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
+template <int EPI, bool UE, bool CTA2>
+__global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const GemmArgs p, const DivTable tab_in)
 {
-    using P = Plan<EPI>;
+    using P = Plan<EPI, CTA2>;
     constexpr int STAGES = P::STAGES, ACC_BUFS = P::ACC_BUFS, OFF_A = P::OFF_A, OFF_B = P::OFF_B,
                   OFF_SFA = P::OFF_SFA, OFF_SFB = P::OFF_SFB, OFF_BAR = P::OFF_BAR, OFF_MISC = P::OFF_MISC,
                   OFF_XPOSE = P::OFF_XPOSE, B_BYTES = P::B_BYTES, SFB_BYTES = P::SFB_BYTES,
@@ -231,15 +269,18 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
     // prefetch.
     pdl_trigger();
     if (EPI == 0) load_div_table(&tab, tab_in);
+    // CTA pairs: rank 0 issues the MMAs; its sf_ready and acc_empty barriers
+    // take the arrivals of both CTAs' scale writers and epilogue warps.
+    const uint32_t rank = CTA2 ? cluster_rank() : 0u;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&sf_ready[s], NUM_SCALE_WARPS);
+            mbar_init(&sf_ready[s], CTA2 ? 2 * NUM_SCALE_WARPS : NUM_SCALE_WARPS);
         }
         for (int i = 0; i < ACC_BUFS; ++i) {
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], EPI_THREADS / EPI_GROUPS);
+            mbar_init(&acc_empty[i], CTA2 ? 2 * P::NUM_EPI_WARPS : EPI_THREADS / EPI_GROUPS);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -249,21 +290,32 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         prefetch_tmap(&tmap_b);
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (CTA2) {
+            // one warp of each CTA of the pair, together: the same columns in both
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (CTA2) cluster_sync_all();  // the peer's barriers are initialised before any arrival on them
 
     pdl_wait();  // the previous kernel's outputs (A operand, row maps, status)
     const int NT = EPI == 0 ? (p.gate_up_I + 127) / 128 : p.N / 128;
-    const int MT = p.hdr->num_mtiles;
+    // w13 pairs: units of two m-tiles; w2: the m-tiles that hold rows
+    const int MT = CTA2 ? p.hdr->num_mtiles / 2 : (EPI == 1 && p.live_mtiles) ? p.hdr->num_live_mtiles : p.hdr->num_mtiles;
     const int ntiles = MT * NT;
     const int KT = (p.K + BK - 1) / BK;
-    const int G = (int)gridDim.x, b = (int)blockIdx.x;
+    // work is shared out per CTA, or per CTA pair
+    const int G = (int)gridDim.x >> (CTA2 ? 1 : 0), b = (int)blockIdx.x >> (CTA2 ? 1 : 0);
     // w2: tile pairs share A when all of a tile's A stages fit the slots, and
     // when pairing (units of two tiles) adds at most 1/32 to the busiest CTA's
     // tile count: with few tiles per CTA, as in decode, that tail costs more
@@ -273,10 +325,18 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
     const int nunits = paired ? MT * (NT / 2) : ntiles;
     const int n_i = nunits > b ? ((nunits - b + G - 1) / G) * (paired ? 2 : 1) : 0;  // this CTA's tiles
     if (p.hdr->status != 0 || n_i == 0) {
-        // nothing to do (same decision in every thread): give TMEM back
-        if (warp == 1)
-            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot), "r"(TMEM_COLS)
-                         : "memory");
+        // nothing to do (same decision in every thread, and in both CTAs of a
+        // pair): give TMEM back
+        if (warp == 1) {
+            if (CTA2)
+                asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot),
+                             "r"(TMEM_COLS)
+                             : "memory");
+            else
+                asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot),
+                             "r"(TMEM_COLS)
+                             : "memory");
+        }
         return;
     }
 
@@ -290,14 +350,16 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         bool ok = true;
         const size_t b_sf_expert = (size_t)(p.N / 128) * p.b_kc * SF_TILE;  // prepared scale bytes per expert
         for (int i = 0; i < n_i && ok; ++i) {
-            const TileInfo<EPI> ti = seq_tile<EPI>(p, i, NT, MT, paired);
+            const TileInfo<EPI> ti = seq_tile<EPI, CTA2>(p, i, NT, MT, paired);
             const bool fill_a = !paired || (i & 1) == 0;  // w2: the first tile of a pair brings A
             const uint8_t *b_sf = p.b_sf + (size_t)ti.e * b_sf_expert +
                                   (size_t)(EPI == 0 ? 2 * ti.nt : ti.nt) * p.b_kc * SF_TILE;
-            const uint32_t b_bytes = EPI == 0 ? (uint32_t)ti.hc * 2 * (BK / 2) : (uint32_t)B_BYTES;
+            // w13: hc gate rows and hc up rows (a pair: rank 0 the gate rows, rank 1 the up rows)
+            const uint32_t b_bytes = EPI == 0 ? (uint32_t)ti.hc * (CTA2 ? 1 : 2) * (BK / 2) : (uint32_t)B_BYTES;
             const uint32_t sfb_bytes = (uint32_t)ti.nblk * 4 * SF_TILE;
             for (int kt = 0; kt < KT; ++kt) {
                 const int kx = kt * (BK / 2);
+                // (a pair: released by rank 0's commit to both CTAs)
                 if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
                     ok = false;
                     break;
@@ -312,7 +374,12 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                     const int f = (paired ? (i >> 1) : i) * KT + kt;  // A fill f goes to slot f % A_SLOTS
                     tma_2d(smem + P::OFF_AS + (f % P::A_SLOTS) * A_BYTES, &tmap_a, kx, ti.mt * BM, fb);
                 }
-                if (EPI == 0) {
+                if (EPI == 0 && CTA2) {
+                    // this CTA's half of the B tile: the hc gate rows (rank 0)
+                    // or the hc up rows (rank 1), in 64-row boxes
+                    const int first = ti.e * 2 * p.gate_up_I + 128 * ti.nt + (rank ? p.gate_up_I : 0);
+                    for (int r = 0; r < ti.hc; r += 64) tma_2d(sb + r * (BK / 2), &tmap_b, kx, first + r, fb);
+                } else if (EPI == 0) {
                     // hc gate rows, then the hc matching up rows, in 64-row boxes
                     const int gate = ti.e * 2 * p.gate_up_I + 128 * ti.nt;
                     for (int r = 0; r < ti.hc; r += 64) {
@@ -341,8 +408,10 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         // Drain: every issued load has landed before the CTA exits.
         for (int s = 0; s < STAGES; ++s)
             if (issued & (1u << s)) mbar_wait(&full[s], (last_parity >> s) & 1u, nullptr, kDrainLimitNs);
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1 && lane == 0 && rank == 0) {
         // ------------------------------------------------ MMA issuer
+        // (a pair: rank 0 issues the M256 MMAs for both CTAs, waits on barriers
+        // both CTAs arrive on, and commits to the barriers of both)
         // The issuing warp shares its scheduler with busy epilogue warps, so
         // the loop is kept short: descriptors advance by constants (a 64-K
         // step is 32 bytes = 2 descriptor units; a stage is a fixed stride)
@@ -356,7 +425,7 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
 
         for (int i = 0; i < n_i && ok; ++i) {
             const int nt = (b + i * G) % NT;  // w13: the tile's width (w2 takes N128 throughout)
-            const uint32_t idesc = idesc_for(EPI == 0 ? 2 * min(128, p.gate_up_I - 128 * nt) : 128);
+            const uint32_t idesc = idesc_for(EPI == 0 ? 2 * min(128, p.gate_up_I - 128 * nt) : 128, CTA2 ? 2 * BM : BM);
             if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
                 ok = false;
                 break;
@@ -378,24 +447,42 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                 const uint64_t da = da0 + (uint64_t)(sl * (A_BYTES >> 4));
                 const uint64_t db = db0 + (uint64_t)(stage * (B_BYTES >> 4));
                 const uint32_t sfa = sf0 + stage * SF_COLS, sfb = sfa + 16;
-                if (kt < k_full) {
-                    tc_mma(d, da, db, idesc, sfa, sfb, kt != 0);
-                    tc_mma(d, da + 2, db + 2, idesc, sfa + 4, sfb + SFB_STEP, 1u);
-                    tc_mma(d, da + 4, db + 4, idesc, sfa + 8, sfb + 2 * SFB_STEP, 1u);
-                    tc_mma(d, da + 6, db + 6, idesc, sfa + 12, sfb + 3 * SFB_STEP, 1u);
+                if constexpr (CTA2) {
+                    if (kt < k_full) {
+                        tc_mma_pair(d, da, db, idesc, sfa, sfb, kt != 0);
+                        tc_mma_pair(d, da + 2, db + 2, idesc, sfa + 4, sfb + SFB_STEP, 1u);
+                        tc_mma_pair(d, da + 4, db + 4, idesc, sfa + 8, sfb + 2 * SFB_STEP, 1u);
+                        tc_mma_pair(d, da + 6, db + 6, idesc, sfa + 12, sfb + 3 * SFB_STEP, 1u);
+                    } else {
+                        const int ksteps = (p.K - kt * BK) / 64;
+                        for (int j = 0; j < ksteps; ++j)
+                            tc_mma_pair(d, da + 2 * j, db + 2 * j, idesc, sfa + 4 * j, sfb + SFB_STEP * j,
+                                        (kt | j) != 0);
+                    }
+                    tc_commit_pair(&empty[stage]);
                 } else {
-                    const int ksteps = (p.K - kt * BK) / 64;
-                    for (int j = 0; j < ksteps; ++j)
-                        tc_mma(d, da + 2 * j, db + 2 * j, idesc, sfa + 4 * j, sfb + SFB_STEP * j, (kt | j) != 0);
+                    if (kt < k_full) {
+                        tc_mma(d, da, db, idesc, sfa, sfb, kt != 0);
+                        tc_mma(d, da + 2, db + 2, idesc, sfa + 4, sfb + SFB_STEP, 1u);
+                        tc_mma(d, da + 4, db + 4, idesc, sfa + 8, sfb + 2 * SFB_STEP, 1u);
+                        tc_mma(d, da + 6, db + 6, idesc, sfa + 12, sfb + 3 * SFB_STEP, 1u);
+                    } else {
+                        const int ksteps = (p.K - kt * BK) / 64;
+                        for (int j = 0; j < ksteps; ++j)
+                            tc_mma(d, da + 2 * j, db + 2 * j, idesc, sfa + 4 * j, sfb + SFB_STEP * j, (kt | j) != 0);
+                    }
+                    tc_commit(&empty[stage]);
                 }
-                tc_commit(&empty[stage]);
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            tc_commit(&acc_full[acc]);
+            if (CTA2)
+                tc_commit_pair(&acc_full[acc]);
+            else
+                tc_commit(&acc_full[acc]);
             if (++acc == ACC_BUFS) {
                 acc = 0;
                 acc_phase ^= 1u;
@@ -405,9 +492,15 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
             *abort_flag = 1;
             atomicOr(&p.hdr->error_flags, kErrTimeoutMma);
         }
-        // Drain: all issued tcgen05 work completes before TMEM is released.
-        tc_commit(drain);
-        mbar_wait(drain, 0, nullptr, kDrainLimitNs);
+        // Drain: all issued tcgen05 work completes before TMEM is released
+        // (a pair: both CTAs wait for it below, before either releases its
+        // tensor memory or shared memory).
+        if (CTA2) {
+            tc_commit_pair(drain);
+        } else {
+            tc_commit(drain);
+            mbar_wait(drain, 0, nullptr, kDrainLimitNs);
+        }
     } else if (warp >= SCALE_WARP0) {
         // ------------------------------------------------ scale writers
         // Each warp owns one TMEM lane quarter and writes the stage's scales
@@ -429,18 +522,18 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         // largest bytes are loaded one tile ahead, off the stage's path.
         int rmax_next[4] = {0, 0, 0, 0};
         if (UE && n_i > 0) {
-            const int mt0 = seq_tile<EPI>(p, 0, NT, MT, paired).mt;
+            const int mt0 = seq_tile<EPI, CTA2>(p, 0, NT, MT, paired).mt;
 #pragma unroll
             for (int q = 0; q < 4; ++q) rmax_next[q] = __ldg(p.a_row_max + mt0 * BM + q * 32 + lane);
         }
         for (int i = 0; i < n_i && ok; ++i) {
-            const TileInfo<EPI> ti = seq_tile<EPI>(p, i, NT, MT, paired);
+            const TileInfo<EPI> ti = seq_tile<EPI, CTA2>(p, i, NT, MT, paired);
             uint32_t c4[4] = {0u, 0u, 0u, 0u};
             if (UE) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) c4[q] = ue8m0_row_shift((uint32_t)rmax_next[q]) * 0x01010101u;
                 if (i + 1 < n_i) {
-                    const int mt1 = seq_tile<EPI>(p, i + 1, NT, MT, paired).mt;
+                    const int mt1 = seq_tile<EPI, CTA2>(p, i + 1, NT, MT, paired).mt;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) rmax_next[q] = __ldg(p.a_row_max + mt1 * BM + q * 32 + lane);
                 }
@@ -484,7 +577,12 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sf_ready[stage]);
+                if (lane == 0) {
+                    if (CTA2)
+                        mbar_arrive_rank0(&sf_ready[stage]);  // both CTAs' scales feed rank 0's MMA
+                    else
+                        mbar_arrive(&sf_ready[stage]);
+                }
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -516,7 +614,7 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         float4 *z4 = reinterpret_cast<float4 *>(p.zero_out);
         if (EPI == 0 && p.zero_out) {
             const long long n4 = p.zero_floats >> 2;
-            const long long active = min((long long)gridDim.x, (long long)ntiles);
+            const long long active = min((long long)gridDim.x, (long long)ntiles << (CTA2 ? 1 : 0));
             const long long per_cta = (n4 + active - 1) / active;
             const long long my_tiles = n_i;
             z_next = min(n4, (long long)blockIdx.x * per_cta);
@@ -526,7 +624,7 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
         for (int i = group; i < n_i; i += EPI_GROUPS) {
             // everything the tile needs besides the accumulator is fetched
             // before waiting for it
-            const TileInfo<EPI> ti = seq_tile<EPI>(p, i, NT, MT, paired);
+            const TileInfo<EPI> ti = seq_tile<EPI, CTA2>(p, i, NT, MT, paired);
             const int e = ti.e, nt = ti.nt;
             const int row = ti.mt * BM + r_in;
             bool valid;
@@ -593,9 +691,15 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
                     tmem_ld16(col0 + ti.hc + w0 + 32 * c + 16, up + 16);
                     tmem_wait_ld(gate, up);
                     if (32 * (c + 1) >= hw) {
-                        // the whole accumulator slice is in registers
+                        // the whole accumulator slice is in registers (a pair:
+                        // one arrival per warp, on rank 0's barrier)
                         tc_fence_before();
-                        mbar_arrive(&acc_empty[acc]);
+                        if (CTA2) {
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive_rank0(&acc_empty[acc]);
+                        } else {
+                            mbar_arrive(&acc_empty[acc]);
+                        }
                     }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -708,13 +812,20 @@ __global__ void __launch_bounds__(Plan<EPI>::NUM_THREADS, 1)
             atomicOr(&p.hdr->error_flags, kErrTimeoutEpilogue);
         }
     }
+    // a pair: every MMA rank 0 issued has completed (they read both CTAs'
+    // shared and tensor memory) before either CTA releases anything
+    if (CTA2 && warp == 1 && lane == 0) mbar_wait(drain, 0, nullptr, kDrainLimitNs);
     __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
-                     : "memory");
+        if (CTA2)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                         : "memory");
     }
 }
 
@@ -725,19 +836,40 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t row
     return make_tensor_map_2d(m, base, row_bytes, rows, 128, box_rows, true);
 }
 
-template <int EPI, bool UE>
+template <int EPI, bool UE, bool CTA2>
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
 {
-    // function attributes are per device: set once on each
+    using P = Plan<EPI, CTA2>;
+    auto kernel = moe_gemm_kernel<EPI, UE, CTA2>;
+    // function attributes and the pair form's resident cluster count are per
+    // device: taken once on each
     static bool attr_set[64] = {false};
+    static int clusters[64] = {0};
     int dev = 0;
     cudaError_t aerr = cudaGetDevice(&dev);
     if (aerr != cudaSuccess) return aerr;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        aerr = cudaFuncSetAttribute(moe_gemm_kernel<EPI, UE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Plan<EPI>::SMEM_BYTES);
+        aerr = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM_BYTES);
         if (aerr != cudaSuccess) return aerr;
+        if (CTA2) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(2 * (sm_count() / 2));
+            q.blockDim = dim3(P::NUM_THREADS);
+            q.dynamicSmemBytes = P::SMEM_BYTES;
+            cudaLaunchAttribute ca[1];
+            ca[0].id = cudaLaunchAttributeClusterDimension;
+            ca[0].val.clusterDim.x = 2;
+            ca[0].val.clusterDim.y = 1;
+            ca[0].val.clusterDim.z = 1;
+            q.attrs = ca;
+            q.numAttrs = 1;
+            int n = 0;
+            aerr = cudaOccupancyMaxActiveClusters(&n, kernel, &q);
+            if (aerr != cudaSuccess) return aerr;
+            if (n < 1) return cudaErrorInvalidConfiguration;
+            clusters[dev] = n;
+        }
         attr_set[dev] = true;
     }
     CUtensorMap ma, mb;
@@ -746,11 +878,33 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
     const uint64_t brows = (uint64_t)a.E * (uint64_t)a.N;
     if (!make_map(&mb, a.b_q, kbytes, brows, a.gate_up_I > 0 ? 64 : 128)) return cudaErrorInvalidValue;
     const long long nt = EPI == 0 ? (a.gate_up_I + 127) / 128 : a.N / 128;
-    const long long tiles = (long long)a.mtiles_cap * nt;
-    int grid = sm_count();
-    if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
-    const cudaError_t err = launch_pdl(moe_gemm_kernel<EPI, UE>, dim3(grid), dim3(Plan<EPI>::NUM_THREADS),
-                                       Plan<EPI>::SMEM_BYTES, st, ma, mb, a, div_table());
+    cudaError_t err;
+    if (CTA2) {
+        // one resident cluster of two CTAs per SM pair; units are m-tile pairs
+        const long long units = (long long)(a.mtiles_cap / 2) * nt;
+        int nc = clusters[dev];
+        if (units < nc) nc = (int)(units > 0 ? units : 1);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * nc);
+        cfg.blockDim = dim3(P::NUM_THREADS);
+        cfg.dynamicSmemBytes = P::SMEM_BYTES;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        err = cudaLaunchKernelEx(&cfg, kernel, ma, mb, a, div_table());
+    } else {
+        const long long tiles = (long long)a.mtiles_cap * nt;
+        int grid = sm_count();
+        if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
+        err = launch_pdl(kernel, dim3(grid), dim3(P::NUM_THREADS), P::SMEM_BYTES, st, ma, mb, a, div_table());
+    }
     return err != cudaSuccess ? err : cudaGetLastError();
 }
 
@@ -801,11 +955,12 @@ bool make_tensor_map_2d(CUtensorMap *m, const void *base, uint64_t row_bytes, ui
 
 cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st)
 {
-    return a.ue8m0 ? launch_gemm<0, true>(a, st) : launch_gemm<0, false>(a, st);
+    if (a.pairs) return a.ue8m0 ? launch_gemm<0, true, true>(a, st) : launch_gemm<0, false, true>(a, st);
+    return a.ue8m0 ? launch_gemm<0, true, false>(a, st) : launch_gemm<0, false, false>(a, st);
 }
 cudaError_t launch_gemm_w2(const GemmArgs &a, cudaStream_t st)
 {
-    return a.ue8m0 ? launch_gemm<1, true>(a, st) : launch_gemm<1, false>(a, st);
+    return a.ue8m0 ? launch_gemm<1, true, false>(a, st) : launch_gemm<1, false, false>(a, st);
 }
 
 }  // namespace nvfp4

@@ -176,6 +176,7 @@ __device__ __forceinline__ void route_body(const RouteArgs &a)
     int *wbase = poff + E + 1;        // [kRouteWarps][E]
     int *cpre = wbase + kRouteWarps * E;  // [own][E]: chunk's first rank per expert
     int *psum = cpre + kRouteMaxOwn * E;  // [parts][E]
+    int *loff = psum + (E > kRouteThreads ? E : kRouteThreads);  // [E + 1]: first live 128-row tile per expert
     // Per expert, the exclusive prefix over chunks.  With few experts the chunk
     // range is split into `parts` runs summed by different threads (one batch
     // of loads each), then the runs' sums are chained.
@@ -217,34 +218,46 @@ __device__ __forceinline__ void route_body(const RouteArgs &a)
         if (blockIdx.x == 0) a.counts[e] = before;
     }
     __syncthreads();
-    // exclusive scans over experts (compact, and padded to 128-row tiles) by
-    // warp 0, 32 experts per step
+    // exclusive scans over experts by warp 0, 32 experts per step: compact,
+    // padded to the pad_rows granularity (128, or 256 so that the 2-SM GEMM's
+    // m-tile pairs belong to one expert), and the live 128-row tiles
+    // (ceil(count / 128) per expert, the tiles holding rows)
+    const int padm = (a.pad_rows == 256 ? 256 : 128) - 1;
     if (warp == 0) {
-        int base_o = 0, base_p = 0;
+        int base_o = 0, base_p = 0, base_l = 0;
         for (int e0 = 0; e0 < E; e0 += 32) {
             const int e = e0 + lane;
             const int c = e < E ? cnt[e] : 0;
-            const int cp = (c + 127) & ~127;
-            int io = c, ip = cp;  // inclusive warp scans
+            const int cp = (c + padm) & ~padm;
+            const int cl = (c + 127) >> 7;
+            int io = c, ip = cp, il = cl;  // inclusive warp scans
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const int to = __shfl_up_sync(0xffffffffu, io, o), tp = __shfl_up_sync(0xffffffffu, ip, o);
+                const int to = __shfl_up_sync(0xffffffffu, io, o), tp = __shfl_up_sync(0xffffffffu, ip, o),
+                          tl = __shfl_up_sync(0xffffffffu, il, o);
                 if (lane >= o) {
                     io += to;
                     ip += tp;
+                    il += tl;
                 }
             }
             if (e < E) {
                 off[e] = base_o + io - c;
                 poff[e] = base_p + ip - cp;
+                loff[e] = base_l + il - cl;
             }
             base_o += __shfl_sync(0xffffffffu, io, 31);
             base_p += __shfl_sync(0xffffffffu, ip, 31);
+            base_l += __shfl_sync(0xffffffffu, il, 31);
         }
         if (lane == 0) {
             off[E] = base_o;
             poff[E] = base_p;
-            if (blockIdx.x == 0) a.hdr->num_mtiles = base_p >> 7;
+            loff[E] = base_l;
+            if (blockIdx.x == 0) {
+                a.hdr->num_mtiles = base_p >> 7;
+                a.hdr->num_live_mtiles = base_l;
+            }
         }
     }
     __syncthreads();
@@ -270,6 +283,21 @@ __device__ __forceinline__ void route_body(const RouteArgs &a)
                     hi = mid - 1;
             }
             a.tile_expert[mtile] = lo;
+        }
+        // live tiles in order: live tile j of expert e is m-tile poff[e]/128 + (j - loff[e])
+        if (a.live_mtiles) {
+            const int nlive = loff[E];
+            for (int j = blockIdx.x * kRouteThreads + tid; j < nlive; j += gridDim.x * kRouteThreads) {
+                int lo = 0, hi = E - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (loff[mid] <= j)
+                        lo = mid;
+                    else
+                        hi = mid - 1;
+                }
+                a.live_mtiles[j] = (poff[lo] >> 7) + (j - loff[lo]);
+            }
         }
     }
     // padding rows of each expert's last tile: one warp per expert
@@ -684,8 +712,9 @@ namespace {
 // resident at once, each taking every gridDim-th chunk.
 size_t route_smem(int E)
 {
-    // cnt, off, poff, per-warp bases, per-chunk prefixes, per-run sums
-    return sizeof(int) * ((3 + kRouteWarps + kRouteMaxOwn) * (size_t)E + 2 + (E > kRouteThreads ? E : kRouteThreads));
+    // cnt, off, poff, per-warp bases, per-chunk prefixes, per-run sums, live-tile offsets
+    return sizeof(int) *
+           ((4 + kRouteWarps + kRouteMaxOwn) * (size_t)E + 3 + (E > kRouteThreads ? E : kRouteThreads));
 }
 
 cudaError_t route_plan(const RouteArgs &a, int *grid_out)

@@ -46,6 +46,34 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, volatile
     }
 }
 
+// ---------------------------------------------------------------- CTA pairs
+// A pair of CTAs (a cluster of two) sharing each MMA (tcgen05 .cta_group::2):
+// rank 0 issues the MMAs; barriers it waits on receive arrivals from both CTAs.
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Both CTAs of the cluster: every thread's earlier writes (barrier
+// initialisation) visible to the peer before either goes on.  The CTAs of a
+// cluster are scheduled together, so both arrive.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive on the barrier at the same shared-memory offset in the rank-0 CTA
+// (the rank-0 CTA's own threads arrive on their own barrier the same way).
+// The arrival has the default (release, CTA) semantics; what it publishes to
+// rank 0's tensor-core work -- the TMA data and the tensor-memory stores of
+// this CTA -- is ordered by the tcgen05 fences around it.
+__device__ __forceinline__ void mbar_arrive_rank0(uint64_t *b)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(remote) : "r"(su32(b)));
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
 // ---------------------------------------------------------------- copies
 // Prefetch a tensor map (a __grid_constant__ kernel parameter) into the
 // descriptor cache ahead of its first TMA.
@@ -70,48 +98,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                  : "memory");
 }
 
-// ---------------------------------------------------------------- L2 policies
-// Per-instruction L2 eviction priorities (createpolicy + .L2::cache_hint): a
-// hint on the accesses that carry it, no device setting.  evict_first for
-// data read once that streams through L2; evict_last for lines that are
-// written now and reduced into later.
-__device__ __forceinline__ uint64_t l2_policy_evict_first()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ void tma_2d_hint(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
-                                            uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
-        "[%1, {%2, %3}], [%4], %5;" ::"r"(su32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar)), "l"(policy)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                              uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
-        "%4;" ::"r"(su32(dst)),
-        "l"(src), "r"(bytes), "r"(su32(bar)), "l"(policy)
-        : "memory");
-}
-__device__ __forceinline__ void st_v4_hint(float4 *p, float4 v, uint64_t policy)
-{
-    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y),
-                 "f"(v.z), "f"(v.w), "l"(policy)
-                 : "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -119,6 +105,16 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
                  : "memory");
+}
+// The pair's form: arrives on the barrier at the same offset in both CTAs
+// once the MMAs this thread issued have completed.
+__device__ __forceinline__ void tc_commit_pair(uint64_t *bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            su32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
 }
 // K-major operand tile, 128-byte swizzle: 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr)
@@ -171,12 +167,6 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d)
 {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
-__device__ __forceinline__ void red_add_v4_hint(float *p, float a, float b, float c, float d, uint64_t policy)
-{
-    asm volatile("red.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a), "f"(b),
-                 "f"(c), "f"(d), "l"(policy)
                  : "memory");
 }
 

@@ -32,8 +32,17 @@ def run_gpu(m, layer, W, flags=None, w=None):
     return out, ws, w
 
 
-def check_layer(m, layer, W, tokens=None):
-    out, ws, _ = run_gpu(m, layer, W)
+def w13_pairs(m, layer, flags):
+    """Whether the forward runs w13 on CTA pairs (rows padded to 256 per
+    expert): forced by a flag, else from 512 routed rows per expert on
+    average."""
+    if flags & m.W13_TWO_SM:
+        return True
+    return not (flags & m.W13_ONE_SM) and layer.T * layer.k >= 512 * layer.E
+
+
+def check_layer(m, layer, W, tokens=None, extra_flags=0):
+    out, ws, _ = run_gpu(m, layer, W, flags=m.SYNC_CHECK | m.DEBUG_KEEP_H | extra_flags)
     ref = oracle.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W, tokens=tokens)
     toks = np.arange(layer.T) if tokens is None else np.asarray(tokens)
     stats = {"out": assert_close(host(out)[toks], ref["out"][toks], "out")}
@@ -43,9 +52,11 @@ def check_layer(m, layer, W, tokens=None):
     assert np.array_equal(host(it["offsets"]), ref["offsets"])
     row_of = host(it["row_of"])
     prow = row_of[ref["perm"][ref["rows"]]]
-    # padded layout: each expert starts on a 128-row tile, rows keep the oracle's order
+    # padded layout: each expert starts on a 128-row tile (256 with CTA pairs),
+    # rows keep the oracle's order
+    g = 256 if w13_pairs(m, layer, extra_flags) else 128
     pad = host(it["pad_offsets"])
-    assert np.all(pad[1:] - pad[:-1] == ((np.diff(ref["offsets"]) + 127) // 128) * 128)
+    assert np.all(pad[1:] - pad[:-1] == ((np.diff(ref["offsets"]) + g - 1) // g) * g)
     assert np.array_equal(host(it["a1q"])[prow], ref["a1q"]), "a1 codes"
     assert np.array_equal(unswizzle(host(it["sf1"]), prow, H // 16, it["kc1"]), ref["sf1"]), "a1 scales"
     h_gpu = host(it["h"])[prow]
@@ -100,8 +111,42 @@ def prefill(m):
 
 def test_prefill_layer_sampled_tokens(m, prefill):
     layer, W = prefill
+    assert w13_pairs(m, layer, 0), "the prefill layer takes the CTA-pair w13 by default"
     tokens = np.sort(np.random.default_rng([layer.seed, 1]).choice(layer.T, 48, replace=False))
     check_layer(m, layer, W, tokens=tokens)
+
+
+def test_prefill_layer_single_cta_w13(m, prefill):
+    """The same layer with the w13 GEMM forced onto single CTAs (rows padded
+    to 128): the same tokens, the same checks."""
+    layer, W = prefill
+    tokens = np.sort(np.random.default_rng([layer.seed, 1]).choice(layer.T, 48, replace=False))
+    check_layer(m, layer, W, tokens=tokens, extra_flags=m.W13_ONE_SM)
+
+
+def test_w13_pairs_forced_on_small_layers(m):
+    """CTA pairs where the default takes single CTAs: most pairs' second
+    m-tile holds padding only, the last tile of I = 128 is a full one, and the
+    w2 GEMM walks the m-tiles that hold rows."""
+    layer, W = layer_with_weights(S.tiny())
+    check_layer(m, layer, W, extra_flags=m.W13_TWO_SM)
+    for T in (1, 64):
+        layer, W = layer_with_weights(S.decode(T))
+        check_layer(m, layer, W, extra_flags=m.W13_TWO_SM)
+
+
+def test_w13_pairs_forced_most_experts(m):
+    """E = 1024, k = 32 on CTA pairs: about a thousand pairs, each one expert's
+    one to a few rows plus a tile of padding."""
+    layer, W = layer_with_weights(S._softmax_layer("maxEk", seed=1011, E=1024, H=256, I=128, T=80, k=32))
+    check_layer(m, layer, W, extra_flags=m.W13_TWO_SM)
+
+
+def test_w13_form_flags_exclusive(m):
+    layer, W = layer_with_weights(S.tiny())
+    with pytest.raises(m.Nvfp4Error) as ei:
+        run_gpu(m, layer, W, flags=m.SYNC_CHECK | m.W13_ONE_SM | m.W13_TWO_SM)
+    assert ei.value.status == m.ERR_INVALID_ARG
 
 
 def test_prefill_unwritten_slots_rejected_before_launch(m, prefill):

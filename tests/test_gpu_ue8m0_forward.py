@@ -48,11 +48,11 @@ def test_row_carry_matches_its_definition(m):
         assert not np.isnan(val).any()
 
 
-def check_ue8m0(m, layer, W, tokens=None, w13_in=None, w2_in=None):
+def check_ue8m0(m, layer, W, tokens=None, w13_in=None, w2_in=None, extra_flags=0):
     w = device_weights(W, w13_in=w13_in, w2_in=w2_in)
     assert w.sf_format == m.SF_UE8M0
     out, ws = m.moe_forward(w, dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w),
-                            flags=m.SYNC_CHECK | m.DEBUG_KEEP_H)
+                            flags=m.SYNC_CHECK | m.DEBUG_KEEP_H | extra_flags)
     torch.cuda.synchronize()
     if w13_in is not None or w2_in is not None:
         W = _with_input_scales(W, w13_in, w2_in)
@@ -97,10 +97,19 @@ def test_decode_layer(m, T):
     check_ue8m0(m, layer, W)
 
 
-def test_prefill_layer_sampled_tokens(m):
+@pytest.mark.parametrize("form", ["default", "single"])
+def test_prefill_layer_sampled_tokens(m, form):
+    """The prefill layer takes the CTA-pair w13 by default; also forced onto
+    single CTAs."""
     layer, W = layer_with_weights(S.prefill(), max_rows=32, ue8m0=True)
     tokens = np.sort(np.random.default_rng([layer.seed, 3]).choice(layer.T, 32, replace=False))
-    check_ue8m0(m, layer, W, tokens=tokens)
+    check_ue8m0(m, layer, W, tokens=tokens, extra_flags=m.W13_ONE_SM if form == "single" else 0)
+
+
+def test_w13_pairs_forced_small_layers(m):
+    for L in (S.tiny(), S.decode(8)):
+        layer, W = layer_with_weights(L, ue8m0=True)
+        check_ue8m0(m, layer, W, extra_flags=m.W13_TWO_SM)
 
 
 def test_prepared_format_must_match(m):
