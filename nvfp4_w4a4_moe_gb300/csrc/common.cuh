@@ -155,6 +155,24 @@ __device__ __forceinline__ uint2 quant_block16(const f32x2 (&x)[8], float amax, 
     return make_uint2(e2m1_rn_sat8(q[0], q[1], q[2], q[3]), e2m1_rn_sat8(q[4], q[5], q[6], q[7]));
 }
 
+// max |x| over 16 BF16 values in 8 words: signs cleared, the two halves
+// compared as unsigned 16-bit integers (the magnitudes of non-negative
+// floats order like their bit patterns), then the two halves.  As FP32.
+__device__ __forceinline__ float amax16_bf16(const uint32_t *w)
+{
+    uint32_t m = w[0] & 0x7FFF7FFFu;
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+        const uint32_t v = w[i] & 0x7FFF7FFFu;
+        asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(v));
+    }
+    return __uint_as_float(max(m << 16, m & 0xFFFF0000u));
+}
+
+// z * sigmoid(z) with the fast exponential and division (a few ulp; the
+// requantisation that follows is exact for whatever FP32 h results).
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(fminf(-z, 80.0f))); }
+
 // UE8M0 block scales.
 // UE8M0 block scale of t >= 0 (t from the same fl(fl(g*amax)/6) as the E4M3
 // path): the byte of the smallest power of two at or above t, clamped to the

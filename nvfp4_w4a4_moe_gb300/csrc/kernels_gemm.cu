@@ -157,9 +157,6 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, 
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
         : "memory");
 }
-// z * sigmoid(z) with the fast exponential and division (a few ulp; the
-// requantisation that follows is exact for whatever FP32 h results).
-__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(fminf(-z, 80.0f))); }
 
 // ---------------------------------------------------------------- tiles
 // Tile geometry shared by every role.  w13: tile t covers h columns

@@ -17,10 +17,11 @@ namespace {
 // [page, ROOT CAUSE]: a per-expert scale slot left unwritten by the loader is
 // reciprocated into an inf / NaN / garbage global scale.  Every slot must be
 // written, finite, positive and normal, and so must its FP32 reciprocal.
-// Run by one CTA of 256 threads; ends with the header written by thread 0.
-__device__ __forceinline__ void validate_body(const ValidateArgs &a)
+// Run by one CTA of 256 threads; ends with the header written by thread 0
+// and returns the status it wrote (every thread, after a block barrier).
+__device__ __forceinline__ int validate_body(const ValidateArgs &a)
 {
-    __shared__ int s_bad, s_first;
+    __shared__ int s_bad, s_first, s_status;
     __shared__ float s_recip[4][1024];  // reciprocals for alpha (forward: 4 arrays, E <= 1024)
     if (threadIdx.x == 0) {
         s_bad = 0;
@@ -56,13 +57,17 @@ __device__ __forceinline__ void validate_body(const ValidateArgs &a)
     }
     if (threadIdx.x == 0) {
         const bool tag_bad = a.prep_tag && *a.prep_tag != a.prep_tag_want;
+        const int status = s_bad ? 2 : tag_bad ? 4 : 0;
         a.hdr->bad_count = s_bad;
         a.hdr->first_bad = s_first;
-        a.hdr->status = s_bad ? 2 : tag_bad ? 4 : 0;
+        a.hdr->status = status;
         a.hdr->error_flags = 0;
         a.hdr->num_mtiles = 0;
         a.hdr->done_count = 0u;
+        s_status = status;
     }
+    __syncthreads();
+    return s_status;
 }
 
 __global__ void __launch_bounds__(256) validate_kernel(ValidateArgs a)
@@ -378,6 +383,129 @@ __global__ void __launch_bounds__(kRouteThreads) validate_route_kernel(ValidateA
     route_body(a);
 }
 
+// The scale check and the routing of a small batch (at most kRouteThreads
+// routed rows, rows padded to 128 per expert) in one CTA: one routed row per
+// thread, its rank among equal experts from a warp match and the per-warp
+// counts, the offsets from one block scan.  The same outputs as route_body.
+__global__ void __launch_bounds__(kRouteThreads) validate_route_tiny_kernel(ValidateArgs v, RouteArgs a)
+{
+    extern __shared__ int sh[];
+    __shared__ int s_bad;
+    __shared__ int s_wsum[2][kRouteWarps];
+    pdl_trigger();
+    pdl_wait();  // whatever ran before on the stream (a previous call may still read the header)
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, E = a.E;
+    const int f = tid;
+    const bool live = f < a.R;
+    const int id = live ? a.ids[f] : -1;  // in flight during the scale check
+    int *wcnt = sh;                     // [kRouteWarps][E]: a warp's rows per expert, then its first rank
+    int *off = wcnt + kRouteWarps * E;  // [E + 1]: counts, then compact offsets
+    int *poff = off + E + 1;            // [E + 1]: padded offsets
+    for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) wcnt[i] = 0;
+    if (tid == 0) s_bad = 0;
+    if (validate_body(v) != 0) return;  // (its block barriers order the clearing above)
+    const bool ok = live && id >= 0 && id < E;
+    if (live && !ok) s_bad = 1;
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? id : -1 - lane);
+    const int wrank = __popc(peers & ((1u << lane) - 1u));
+    if (ok && wrank == 0) wcnt[warp * E + id] = __popc(peers);
+    __syncthreads();
+    if (s_bad) {
+        if (tid == 0) {
+            atomicOr(&a.hdr->error_flags, kErrBadExpertId);
+            a.hdr->status = 3;  // nothing after this writes
+        }
+        return;
+    }
+    for (int e = tid; e < E; e += kRouteThreads) {
+        int run = 0;
+        for (int w = 0; w < kRouteWarps; ++w) {
+            const int c = wcnt[w * E + e];
+            wcnt[w * E + e] = run;
+            run += c;
+        }
+        off[e] = run;
+    }
+    __syncthreads();
+    // exclusive scans of the counts and of the counts padded to 128 rows;
+    // thread t owns experts [per t, per t + per)
+    constexpr int kMaxPer = 1024 / kRouteThreads;
+    const int per = (E + kRouteThreads - 1) / kRouteThreads, e0 = tid * per;
+    int cl[kMaxPer], so = 0, sp = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) {
+        const int e = e0 + i;
+        cl[i] = (i < per && e < E) ? off[e] : 0;
+        so += cl[i];
+        sp += (cl[i] + 127) & ~127;
+    }
+    int io = so, ip = sp;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int to = __shfl_up_sync(0xffffffffu, io, o), tp = __shfl_up_sync(0xffffffffu, ip, o);
+        if (lane >= o) {
+            io += to;
+            ip += tp;
+        }
+    }
+    if (lane == 31) {
+        s_wsum[0][warp] = io;
+        s_wsum[1][warp] = ip;
+    }
+    __syncthreads();
+    int xo = io - so, xp = ip - sp;
+    for (int w = 0; w < warp; ++w) {
+        xo += s_wsum[0][w];
+        xp += s_wsum[1][w];
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxPer; ++i) {
+        const int e = e0 + i;
+        if (i < per && e < E) {
+            off[e] = xo;
+            poff[e] = xp;
+        }
+        xo += cl[i];
+        xp += (cl[i] + 127) & ~127;
+    }
+    if (tid == kRouteThreads - 1) {
+        off[E] = xo;
+        poff[E] = xp;
+    }
+    __syncthreads();
+    const int npad = poff[E];
+    for (int e = tid; e <= E; e += kRouteThreads) {
+        if (e < E) a.counts[e] = off[e + 1] - off[e];
+        a.offsets[e] = off[e];
+        a.pad_off[e] = poff[e];
+        if (a.offsets_out) a.offsets_out[e] = off[e];
+        if (e < E && a.tile_expert)
+            for (int t = poff[e] >> 7; t < poff[e + 1] >> 7; ++t) a.tile_expert[t] = e;
+    }
+    if (tid == 0) {
+        a.hdr->num_mtiles = npad >> 7;
+        a.hdr->num_live_mtiles = npad >> 7;
+    }
+    // every padded row: no source (and UE8M0 row maxima 0); the routed rows'
+    // sources are written after the barrier
+    const int4 none = make_int4(-1, -1, -1, -1), zero = make_int4(0, 0, 0, 0);
+    for (int r4 = tid; r4 < (npad >> 2); r4 += kRouteThreads) {
+        if (a.row_src) reinterpret_cast<int4 *>(a.row_src)[r4] = none;
+        if (a.row_max) {
+            reinterpret_cast<int4 *>(a.row_max)[r4] = zero;
+            reinterpret_cast<int4 *>(a.row_max + a.rows_cap)[r4] = zero;
+        }
+    }
+    __syncthreads();
+    if (ok) {
+        const int pos = wcnt[warp * E + id] + wrank;
+        const int compact = off[id] + pos, padded = poff[id] + pos;
+        a.row_of[f] = a.padded ? padded : compact;
+        if (a.perm) a.perm[compact] = f;
+        if (a.row_src) a.row_src[padded] = f;
+    }
+}
+
 // ------------------------------------------------------------------ quantiser
 // [page, §NVFP4 runtime-order figure; MoE section: SFScale[expert_idx]]:
 // one warp per (token, 1024-element chunk), each lane two consecutive
@@ -390,20 +518,6 @@ __global__ void __launch_bounds__(kRouteThreads) validate_route_kernel(ValidateA
 // adds the lane's own part, so it holds no per-row address arithmetic.
 // Offsets are 32-bit (codes in 16-byte units, scales in bytes); the host
 // keeps every call within that range.
-
-// max |x| over 16 BF16 values in 8 words: signs cleared, the two halves
-// compared as unsigned 16-bit integers (the magnitudes of non-negative
-// floats order like their bit patterns), then the two halves.  As FP32.
-__device__ __forceinline__ float amax16_bf16(const uint32_t *w)
-{
-    uint32_t m = w[0] & 0x7FFF7FFFu;
-#pragma unroll
-    for (int i = 1; i < 8; ++i) {
-        const uint32_t v = w[i] & 0x7FFF7FFFu;
-        asm("max.u16x2 %0, %0, %1;" : "+r"(m) : "r"(v));
-    }
-    return __uint_as_float(max(m << 16, m & 0xFFFF0000u));
-}
 
 constexpr int kQuantThreads = 128;  // 5 CTAs (20 warps) per SM at <= 96 registers
 
@@ -710,6 +824,8 @@ cudaError_t launch_validate(const ValidateArgs &a, cudaStream_t st)
 namespace {
 // Routing launch shape: a cooperative grid of at most as many CTAs as can be
 // resident at once, each taking every gridDim-th chunk.
+size_t tiny_route_smem(int E) { return sizeof(int) * ((size_t)kRouteWarps * E + 2 * ((size_t)E + 1)); }
+
 size_t route_smem(int E)
 {
     // cnt, off, poff, per-warp bases, per-chunk prefixes, per-run sums, live-tile offsets
@@ -763,6 +879,21 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t st)
 
 cudaError_t launch_validate_route(const ValidateArgs &v, const RouteArgs &a, cudaStream_t st)
 {
+    if (a.R <= kRouteThreads && a.pad_rows != 256 && !a.live_mtiles) {
+        static bool attr_set[64] = {false};
+        int dev = 0;
+        cudaError_t err = cudaGetDevice(&dev);
+        if (err != cudaSuccess) return err;
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!attr_set[dev]) {
+            err = cudaFuncSetAttribute(validate_route_tiny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)tiny_route_smem(1024));
+            if (err != cudaSuccess) return err;
+            attr_set[dev] = true;
+        }
+        err = launch_pdl(validate_route_tiny_kernel, dim3(1), dim3(kRouteThreads), tiny_route_smem(a.E), st, v, a);
+        return err != cudaSuccess ? err : cudaGetLastError();
+    }
     int grid = 0;
     cudaError_t err = route_plan(a, &grid);
     if (err != cudaSuccess) return err;

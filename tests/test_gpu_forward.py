@@ -93,6 +93,14 @@ def test_most_experts_and_top_k(m):
     check_layer(m, layer, W)
 
 
+def test_small_batch_routing_most_experts(m):
+    """240 routed rows over E = 1024 experts: the scale check and the routing
+    of a batch of at most 256 rows run in one CTA (each thread one routed
+    row, four experts per thread in the offset scan)."""
+    layer, W = layer_with_weights(S._softmax_layer("maxE_small", seed=1012, E=1024, H=256, I=128, T=60, k=4))
+    check_layer(m, layer, W)
+
+
 @pytest.mark.parametrize("I", [1280, 1536])
 def test_long_intermediate(m, I):
     """The w2 GEMM's K is I.  With 5 stages of 256 a tile pair's A fills every
