@@ -45,8 +45,9 @@ def check_layer(m, layer, W, tokens=None, extra_flags=0):
     out, ws, _ = run_gpu(m, layer, W, flags=m.SYNC_CHECK | m.DEBUG_KEEP_H | extra_flags)
     ref = oracle.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W, tokens=tokens)
     toks = np.arange(layer.T) if tokens is None else np.asarray(tokens)
-    stats = {"out": assert_close(host(out)[toks], ref["out"][toks], "out")}
+    stats = {}
 
+    # the routing and the intermediates first, then the output they feed
     T, H, I, E, k = layer.T, layer.H, layer.I, layer.E, layer.k
     it = m.intermediates_of(ws, T, H, I, E, k)
     assert np.array_equal(host(it["offsets"]), ref["offsets"])
@@ -71,6 +72,7 @@ def check_layer(m, layer, W, tokens=None, extra_flags=0):
     diff = (oracle.unpack_codes(a2q) != oracle.unpack_codes(ref["a2q"])).mean()
     assert diff <= 1e-3, f"{diff:.2e} of a2 codes differ from the oracle's"
     stats["a2_code_diff"] = diff
+    stats["out"] = assert_close(host(out)[toks], ref["out"][toks], "out")
     return stats
 
 
