@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <thread>
@@ -632,6 +633,16 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     ga.hdr = hdr;
     ga.mtiles_cap = L.mtiles_cap;
     ga.pairs = pairs ? 1 : 0;
+    // the small-batch plan when its waves of 64-column tiles (over at most
+    // min(R, E) busy experts) take less time than the wide plan's waves; a
+    // narrow tile's K loop takes about 0.55 of a wide one's
+    {
+        const long long busy = std::min<long long>((long long)T * k, E), sms = sm_count();
+        const long long small_waves = (busy * ((I + 63) / 64) + sms - 1) / sms;
+        const long long wide_waves = (busy * ((I + 127) / 128) + sms - 1) / sms;
+        ga.small = !pairs && !ue && !(flags & NVFP4_W13_ONE_SM) && (long long)T * k <= kSmallPlanRows &&
+                   100 * small_waves < 182 * wide_waves;
+    }
     NV_CUDA(launch_gemm_w13(ga, st), "launching the w13 GEMM");
     NV_CUDA(mark(4), "recording an event");
 
@@ -651,6 +662,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     gb.topk_w = topk_w;
     gb.out = out;
     gb.pairs = 0;
+    gb.small = 0;
     gb.live_mtiles = ra.live_mtiles;  // with 256-row padding, the m-tiles that hold rows
     if (ue) {
         gb.a_row_max = row_max + L.rows_cap;

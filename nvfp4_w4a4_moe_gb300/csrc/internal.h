@@ -33,6 +33,11 @@ constexpr int kRouteChunk = 2048;  // routed rows per routing CTA
 // padding to 256 rows costs more than the pairs save.
 constexpr long long kPairRowsPerExpert = 512;
 
+// Up to this many routed rows (T*k), the w13 GEMM takes its small-batch plan:
+// 64-column tiles, the A stage holding an m-tile's first 32 rows (no m-tile
+// can hold more), and a deeper ring.
+constexpr long long kSmallPlanRows = 32;
+
 WsLayout make_layout(int T, int H, int I, int E, int k);
 
 // ---------------------------------------------------------------- kernels
@@ -136,6 +141,7 @@ struct GemmArgs {
     DevHeader *hdr;
     int mtiles_cap;
     int pairs;                 // w13: CTA pairs on m-tile pairs (rows padded to 256 per expert)
+    int small;                 // w13: the small-batch plan (at most kSmallPlanRows routed rows, E4M3 scales)
     const int *live_mtiles;    // w2: the m-tiles holding rows, in order (nullable: all m-tiles)
 };
 cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st);

@@ -78,10 +78,19 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 //       from each CTA's tensor memory); its accumulator holds its 128 rows.
 //       38 KB per stage per CTA instead of 54, a 5-stage ring, and sixteen
 //       epilogue warps.
-template <int EPI, bool CTA2 = false>
+//  w13, small batches (at most kSmallPlanRows routed rows, so that no
+//       m-tile holds more): tiles of 64 h columns (64 gate + 64 up weight
+//       rows, N128; the B scales cut from the block's two 128-row scale
+//       tiles), the A stage only the m-tile's first kSmallPlanRows rows, and a
+//       7-stage ring.  At these sizes a tile's K loop is paced by the ring's
+//       round trip, not by its bytes: more stages in flight, on twice the
+//       tiles.
+constexpr int kDecRows = (int)kSmallPlanRows;
+static_assert(kDecRows % 16 == 0, "A is loaded in 16-row boxes");
+template <int EPI, bool CTA2 = false, bool DEC = false>
 struct Plan {
-    static constexpr int BN = EPI == 0 ? 256 : 128;  // widest tile (MMA N)
-    static constexpr int STAGES = CTA2 ? 5 : 4;
+    static constexpr int BN = DEC ? 128 : EPI == 0 ? 256 : 128;  // widest tile (MMA N)
+    static constexpr int STAGES = DEC ? 7 : CTA2 ? 5 : 4;
     // w13 pairs: 16 epilogue warps of 32 columns each, so every warp releases
     // the accumulator after a single TMEM load (the pair form's stages are
     // shorter, and the release gates the next tile's MMAs); 8 for w13 on
@@ -101,13 +110,18 @@ struct Plan {
     // stage at or after the last one reading fill f (checked for every K depth
     // a pair can have, 1 .. A_SLOTS stages, and for unpaired tiles).
     static constexpr int A_SLOTS = EPI == 1 ? 5 : 0;
-    static constexpr int RING_A_BYTES = EPI == 1 ? 0 : A_BYTES;
-    static constexpr int SFB_BYTES = (BN / 128) * 4 * SF_TILE;
+    // A ring stages sit A_STRIDE apart; the MMA reads 128 rows from each
+    // stage's start, so in the small-batch plan the rows past the loaded ones
+    // read the following stages (their outputs are never stored), and the
+    // region ends a full A tile after the last stage's start
+    static constexpr int A_STRIDE = DEC ? kDecRows * BK / 2 : A_BYTES;
+    static constexpr int RING_A_REGION = EPI == 1 ? 0 : (STAGES - 1) * A_STRIDE + A_BYTES;
+    static constexpr int SFB_BYTES = DEC ? 2 * 4 * SF_TILE : (BN / 128) * 4 * SF_TILE;
     static constexpr int SFB_STEP = BN / 32;               // TMEM columns per 64-K step of B scales
     static constexpr int SF_COLS = 16 + 4 * SFB_STEP;      // TMEM scale columns per stage
     static constexpr int SF_TMEM_COL = ACC_BUFS * BN;      // scale slots after the accumulator(s)
     static constexpr int OFF_A = 0;
-    static constexpr int OFF_B = OFF_A + STAGES * RING_A_BYTES;
+    static constexpr int OFF_B = OFF_A + RING_A_REGION;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_AS = OFF_SFB + STAGES * SFB_BYTES;  // the A slots (w2)
@@ -122,6 +136,7 @@ struct Plan {
     static_assert(OFF_B % 1024 == 0 && OFF_AS % 1024 == 0, "128-byte-swizzled operands start on 1024 bytes");
     static_assert(EPI == 0 || (A_SLOTS == 5 && STAGES == 4), "the A-slot reuse argument is for 5 slots, 4 stages");
     static_assert(!CTA2 || EPI == 0, "CTA pairs: w13 only");
+    static_assert(!DEC || (EPI == 0 && !CTA2), "the small-batch plan: w13 on single CTAs");
     static_assert(SMEM_BYTES + (EPI == 0 ? (int)sizeof(DivTable2) : 0) <= 232448,
                   "shared memory plan exceeds the opt-in limit");
 };
@@ -166,15 +181,21 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, 
 template <int EPI>
 struct TileInfo {
     int mt, nt, e;
-    int hc;    // w13: h columns of the tile (128 or 64)
-    int nblk;  // 128-row scale blocks of the B tile (w13 full: 2, else 1)
+    int hc;       // w13: h columns of the tile (128 or 64)
+    int hc0;      // w13: its first h column
+    int nblk;     // 128-row scale tiles per 64-K step of the tile's scale block (w13 full block: 2, else 1)
+    int compose;  // w13 64-column tile cut from a full block: 1 + which half of its two tiles; else 0
 };
 // w2 walks the m-tiles that hold rows (live_mtiles, when the rows are padded
 // to 256 for the paired w13) in order.
 __device__ __forceinline__ int mtile_of(const GemmArgs &p, int mi) { return p.live_mtiles ? p.live_mtiles[mi] : mi; }
 
+// W: w13 tile width in h columns (128, or 64 in the small-batch plan).  The
+// tile's scales are those of the 128-column block holding it: per 64-K step
+// a gate and an up 128-row tile (a full block), or one tile of 64 gate + 64
+// up rows (the last block when I is an odd multiple of 64).
 template <int EPI>
-__device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, int NT, int MT)
+__device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, int NT, int MT, int W = 128)
 {
     TileInfo<EPI> ti;
     if (EPI == 0) {
@@ -192,10 +213,13 @@ __device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, 
     }
     ti.e = p.tile_expert[ti.mt];
     if (EPI == 0) {
-        ti.hc = min(128, p.gate_up_I - 128 * ti.nt);
-        ti.nblk = ti.hc == 128 ? 2 : 1;
+        ti.hc0 = W * ti.nt;
+        ti.hc = min(W, p.gate_up_I - ti.hc0);
+        const bool full_block = (ti.hc0 & ~127) + 128 <= p.gate_up_I;
+        ti.nblk = full_block ? 2 : 1;
+        ti.compose = W == 64 && full_block ? 1 + (ti.nt & 1) : 0;
     } else {
-        ti.hc = 0;
+        ti.hc = ti.hc0 = ti.compose = 0;
         ti.nblk = 1;
     }
     return ti;
@@ -207,7 +231,7 @@ __device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, 
 // unit (i/2) * gridDim + blockIdx, column block 2 * pair + (i & 1); the two
 // tiles of a unit run back to back and share the A operand.
 template <int EPI, bool CTA2 = false>
-__device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int NT, int MT, bool paired)
+__device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int NT, int MT, bool paired, int W)
 {
     if (CTA2) {
         // unit (m-tile pair, column tile), pair-major; this CTA's m-tile of the pair
@@ -224,11 +248,11 @@ __device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int 
         ti.mt = mtile_of(p, u - g * MT);
         ti.nt = 2 * g + (i & 1);
         ti.e = p.tile_expert[ti.mt];
-        ti.hc = 0;
+        ti.hc = ti.hc0 = ti.compose = 0;
         ti.nblk = 1;
         return ti;
     }
-    return tile_info<EPI>(p, (int)blockIdx.x + i * (int)gridDim.x, NT, MT);
+    return tile_info<EPI>(p, (int)blockIdx.x + i * (int)gridDim.x, NT, MT, W);
 }
 
 // ---------------------------------------------------------------- kernel
@@ -239,12 +263,12 @@ __device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int 
 // prepared.  The epilogue multiplies both rows' factors back: the A row's
 // into the row scale, the weight row's per output column.  w13 then writes
 // a2 as UE8M0 bytes with each row's largest byte (out_row_max).
-template <int EPI, bool UE, bool CTA2>
-__global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
+template <int EPI, bool UE, bool CTA2, bool DEC>
+__global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                    const GemmArgs p, const DivTable tab_in)
+                    const __grid_constant__ CUtensorMap tmap_a16, const GemmArgs p, const DivTable tab_in)
 {
-    using P = Plan<EPI, CTA2>;
+    using P = Plan<EPI, CTA2, DEC>;
     constexpr int STAGES = P::STAGES, ACC_BUFS = P::ACC_BUFS, OFF_A = P::OFF_A, OFF_B = P::OFF_B,
                   OFF_SFA = P::OFF_SFA, OFF_SFB = P::OFF_SFB, OFF_BAR = P::OFF_BAR, OFF_MISC = P::OFF_MISC,
                   OFF_XPOSE = P::OFF_XPOSE, B_BYTES = P::B_BYTES, SFB_BYTES = P::SFB_BYTES,
@@ -285,6 +309,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         prefetch_tmap(&tmap_a);
         prefetch_tmap(&tmap_b);
+        if (DEC) prefetch_tmap(&tmap_a16);
     }
     if (warp == 1) {
         if (CTA2) {
@@ -306,7 +331,8 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
     if (CTA2) cluster_sync_all();  // the peer's barriers are initialised before any arrival on them
 
     pdl_wait();  // the previous kernel's outputs (A operand, row maps, status)
-    const int NT = EPI == 0 ? (p.gate_up_I + 127) / 128 : p.N / 128;
+    constexpr int W = DEC ? 64 : 128;  // w13 tile width in h columns
+    const int NT = EPI == 0 ? (p.gate_up_I + W - 1) / W : p.N / 128;
     // w13 pairs: units of two m-tiles; w2: the m-tiles that hold rows
     const int MT = CTA2 ? p.hdr->num_mtiles / 2 : (EPI == 1 && p.live_mtiles) ? p.hdr->num_live_mtiles : p.hdr->num_mtiles;
     const int ntiles = MT * NT;
@@ -347,10 +373,10 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
         bool ok = true;
         const size_t b_sf_expert = (size_t)(p.N / 128) * p.b_kc * SF_TILE;  // prepared scale bytes per expert
         for (int i = 0; i < n_i && ok; ++i) {
-            const TileInfo<EPI> ti = seq_tile<EPI, CTA2>(p, i, NT, MT, paired);
+            const TileInfo<EPI> ti = seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
             const bool fill_a = !paired || (i & 1) == 0;  // w2: the first tile of a pair brings A
             const uint8_t *b_sf = p.b_sf + (size_t)ti.e * b_sf_expert +
-                                  (size_t)(EPI == 0 ? 2 * ti.nt : ti.nt) * p.b_kc * SF_TILE;
+                                  (size_t)(EPI == 0 ? 2 * (ti.hc0 >> 7) : ti.nt) * p.b_kc * SF_TILE;
             // w13: hc gate rows and hc up rows (a pair: rank 0 the gate rows, rank 1 the up rows)
             const uint32_t b_bytes = EPI == 0 ? (uint32_t)ti.hc * (CTA2 ? 1 : 2) * (BK / 2) : (uint32_t)B_BYTES;
             const uint32_t sfb_bytes = (uint32_t)ti.nblk * 4 * SF_TILE;
@@ -363,10 +389,17 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
                 }
                 uint64_t *fb = &full[stage];
                 const bool a_now = EPI == 0 || fill_a;
-                mbar_expect_tx(fb, (a_now ? A_BYTES : 0u) + b_bytes + SFA_BYTES + sfb_bytes);
+                // A: the whole m-tile, or (small-batch plan) its first kDecRows rows
+                const uint32_t a_bytes = DEC ? (uint32_t)(kDecRows * BK / 2) : (uint32_t)A_BYTES;
+                mbar_expect_tx(fb, (a_now ? a_bytes : 0u) + b_bytes + SFA_BYTES + sfb_bytes);
                 uint8_t *sb = smem + OFF_B + stage * B_BYTES;
                 if constexpr (EPI == 0) {
-                    tma_2d(smem + OFF_A + stage * A_BYTES, &tmap_a, kx, ti.mt * BM, fb);
+                    if (DEC) {
+                        for (int r = 0; r < kDecRows; r += 16)
+                            tma_2d(smem + OFF_A + stage * P::A_STRIDE + r * (BK / 2), &tmap_a16, kx, ti.mt * BM + r, fb);
+                    } else {
+                        tma_2d(smem + OFF_A + stage * A_BYTES, &tmap_a, kx, ti.mt * BM, fb);
+                    }
                 } else if (fill_a) {
                     const int f = (paired ? (i >> 1) : i) * KT + kt;  // A fill f goes to slot f % A_SLOTS
                     tma_2d(smem + P::OFF_AS + (f % P::A_SLOTS) * A_BYTES, &tmap_a, kx, ti.mt * BM, fb);
@@ -374,11 +407,11 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
                 if (EPI == 0 && CTA2) {
                     // this CTA's half of the B tile: the hc gate rows (rank 0)
                     // or the hc up rows (rank 1), in 64-row boxes
-                    const int first = ti.e * 2 * p.gate_up_I + 128 * ti.nt + (rank ? p.gate_up_I : 0);
+                    const int first = ti.e * 2 * p.gate_up_I + ti.hc0 + (rank ? p.gate_up_I : 0);
                     for (int r = 0; r < ti.hc; r += 64) tma_2d(sb + r * (BK / 2), &tmap_b, kx, first + r, fb);
                 } else if (EPI == 0) {
                     // hc gate rows, then the hc matching up rows, in 64-row boxes
-                    const int gate = ti.e * 2 * p.gate_up_I + 128 * ti.nt;
+                    const int gate = ti.e * 2 * p.gate_up_I + ti.hc0;
                     for (int r = 0; r < ti.hc; r += 64) {
                         tma_2d(sb + r * (BK / 2), &tmap_b, kx, gate + r, fb);
                         tma_2d(sb + (ti.hc + r) * (BK / 2), &tmap_b, kx, gate + p.gate_up_I + r, fb);
@@ -422,7 +455,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
 
         for (int i = 0; i < n_i && ok; ++i) {
             const int nt = (b + i * G) % NT;  // w13: the tile's width (w2 takes N128 throughout)
-            const uint32_t idesc = idesc_for(EPI == 0 ? 2 * min(128, p.gate_up_I - 128 * nt) : 128, CTA2 ? 2 * BM : BM);
+            const uint32_t idesc = idesc_for(EPI == 0 ? 2 * min(W, p.gate_up_I - W * nt) : 128, CTA2 ? 2 * BM : BM);
             if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
                 ok = false;
                 break;
@@ -441,7 +474,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
                 // for the second of a pair the first's, ring stage)
                 int sl = stage;
                 if constexpr (EPI == 1) sl = ((paired ? (i >> 1) : i) * KT + kt) % P::A_SLOTS;
-                const uint64_t da = da0 + (uint64_t)(sl * (A_BYTES >> 4));
+                const uint64_t da = da0 + (uint64_t)(sl * ((EPI == 1 ? A_BYTES : P::A_STRIDE) >> 4));
                 const uint64_t db = db0 + (uint64_t)(stage * (B_BYTES >> 4));
                 const uint32_t sfa = sf0 + stage * SF_COLS, sfb = sfa + 16;
                 if constexpr (CTA2) {
@@ -519,18 +552,18 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
         // largest bytes are loaded one tile ahead, off the stage's path.
         int rmax_next[4] = {0, 0, 0, 0};
         if (UE && n_i > 0) {
-            const int mt0 = seq_tile<EPI, CTA2>(p, 0, NT, MT, paired).mt;
+            const int mt0 = seq_tile<EPI, CTA2>(p, 0, NT, MT, paired, W).mt;
 #pragma unroll
             for (int q = 0; q < 4; ++q) rmax_next[q] = __ldg(p.a_row_max + mt0 * BM + q * 32 + lane);
         }
         for (int i = 0; i < n_i && ok; ++i) {
-            const TileInfo<EPI> ti = seq_tile<EPI, CTA2>(p, i, NT, MT, paired);
+            const TileInfo<EPI> ti = seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
             uint32_t c4[4] = {0u, 0u, 0u, 0u};
             if (UE) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) c4[q] = ue8m0_row_shift((uint32_t)rmax_next[q]) * 0x01010101u;
                 if (i + 1 < n_i) {
-                    const int mt1 = seq_tile<EPI, CTA2>(p, i + 1, NT, MT, paired).mt;
+                    const int mt1 = seq_tile<EPI, CTA2>(p, i + 1, NT, MT, paired, W).mt;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) rmax_next[q] = __ldg(p.a_row_max + mt1 * BM + q * 32 + lane);
                 }
@@ -553,7 +586,22 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
                                           ue8m0_carried4(v[j].z, c4[2]), ue8m0_carried4(v[j].w, c4[3]));
                 }
                 tmem_st16(sfa_t, v);
-                if (SFB_STEP == 4) {
+                if (DEC) {
+                    // 64-column tiles, four columns per 64-K step: the tile's
+                    // 64 gate rows are words 2c, 2c+1 of the gate tile's 16
+                    // bytes (rows 64c + lane, 64c + 32 + lane), its 64 up rows
+                    // the same words of the up tile; a native 64 + 64 tile as is
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (ti.compose) {
+                            const uint4 g = ssfb[32 * (2 * j)], u = ssfb[32 * (2 * j + 1)];
+                            v[j] = ti.compose == 1 ? make_uint4(g.x, g.y, u.x, u.y) : make_uint4(g.z, g.w, u.z, u.w);
+                        } else {
+                            v[j] = ssfb[32 * j];
+                        }
+                    }
+                    tmem_st16(sfb_t, v);
+                } else if (SFB_STEP == 4) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) v[j] = ssfb[32 * j];
                     tmem_st16(sfb_t, v);
@@ -621,7 +669,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
         for (int i = group; i < n_i; i += EPI_GROUPS) {
             // everything the tile needs besides the accumulator is fetched
             // before waiting for it
-            const TileInfo<EPI> ti = seq_tile<EPI, CTA2>(p, i, NT, MT, paired);
+            const TileInfo<EPI> ti = seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
             const int e = ti.e, nt = ti.nt;
             const int row = ti.mt * BM + r_in;
             bool valid;
@@ -649,7 +697,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
                 s0 *= ue8m0_row_factor(ue8m0_row_shift((uint32_t)p.a_row_max[row]));
                 if (EPI == 0) {
                     const int w0 = part * (ti.hc / (P::NUM_EPI_WARPS / 4));
-                    const float *fg = p.b_row_factor + (size_t)e * p.N + 128 * nt + w0;
+                    const float *fg = p.b_row_factor + (size_t)e * p.N + ti.hc0 + w0;
                     const int hw = ti.hc / (P::NUM_EPI_WARPS / 4);
                     colf[0].x = fg[lane];
                     colf[0].y = fg[p.gate_up_I + lane];
@@ -713,7 +761,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2>::NUM_THREADS, 1)
                     }
                 }
                 uint32_t sfw = 0, sf_max = 0;
-                const int hcol_tile = 128 * nt + w0;  // first h column of this warp
+                const int hcol_tile = ti.hc0 + w0;  // first h column of this warp
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
                     if (b >= nblocks) break;
@@ -833,11 +881,11 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t row
     return make_tensor_map_2d(m, base, row_bytes, rows, 128, box_rows, true);
 }
 
-template <int EPI, bool UE, bool CTA2>
+template <int EPI, bool UE, bool CTA2, bool DEC = false>
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
 {
-    using P = Plan<EPI, CTA2>;
-    auto kernel = moe_gemm_kernel<EPI, UE, CTA2>;
+    using P = Plan<EPI, CTA2, DEC>;
+    auto kernel = moe_gemm_kernel<EPI, UE, CTA2, DEC>;
     // function attributes and the pair form's resident cluster count are per
     // device: taken once on each
     static bool attr_set[64] = {false};
@@ -869,12 +917,13 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
         }
         attr_set[dev] = true;
     }
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, ma16;  // ma16: A in 16-row boxes (the small-batch plan)
     const uint64_t kbytes = (uint64_t)a.K / 2;
     if (!make_map(&ma, a.a_q, kbytes, (uint64_t)a.rows_cap, 128)) return cudaErrorInvalidValue;
+    if (!make_map(&ma16, a.a_q, kbytes, (uint64_t)a.rows_cap, 16)) return cudaErrorInvalidValue;
     const uint64_t brows = (uint64_t)a.E * (uint64_t)a.N;
     if (!make_map(&mb, a.b_q, kbytes, brows, a.gate_up_I > 0 ? 64 : 128)) return cudaErrorInvalidValue;
-    const long long nt = EPI == 0 ? (a.gate_up_I + 127) / 128 : a.N / 128;
+    const long long nt = EPI == 0 ? (a.gate_up_I + (DEC ? 63 : 127)) / (DEC ? 64 : 128) : a.N / 128;
     cudaError_t err;
     if (CTA2) {
         // one resident cluster of two CTAs per SM pair; units are m-tile pairs
@@ -895,12 +944,12 @@ cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
         attr[1].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        err = cudaLaunchKernelEx(&cfg, kernel, ma, mb, a, div_table());
+        err = cudaLaunchKernelEx(&cfg, kernel, ma, mb, ma16, a, div_table());
     } else {
         const long long tiles = (long long)a.mtiles_cap * nt;
         int grid = sm_count();
         if (tiles < grid) grid = (int)(tiles > 0 ? tiles : 1);
-        err = launch_pdl(kernel, dim3(grid), dim3(P::NUM_THREADS), P::SMEM_BYTES, st, ma, mb, a, div_table());
+        err = launch_pdl(kernel, dim3(grid), dim3(P::NUM_THREADS), P::SMEM_BYTES, st, ma, mb, ma16, a, div_table());
     }
     return err != cudaSuccess ? err : cudaGetLastError();
 }
@@ -953,6 +1002,7 @@ bool make_tensor_map_2d(CUtensorMap *m, const void *base, uint64_t row_bytes, ui
 cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st)
 {
     if (a.pairs) return a.ue8m0 ? launch_gemm<0, true, true>(a, st) : launch_gemm<0, false, true>(a, st);
+    if (a.small && !a.ue8m0) return launch_gemm<0, false, false, true>(a, st);
     return a.ue8m0 ? launch_gemm<0, true, false>(a, st) : launch_gemm<0, false, false>(a, st);
 }
 cudaError_t launch_gemm_w2(const GemmArgs &a, cudaStream_t st)

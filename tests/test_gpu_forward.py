@@ -95,6 +95,22 @@ def test_most_experts_and_top_k(m):
     check_layer(m, layer, W)
 
 
+def test_small_batch_plan(m):
+    """The w13 GEMM's small-batch plan (at most 32 routed rows: 64-column
+    tiles, A stages of an m-tile's first 32 rows, a 7-stage ring; taken when
+    its waves of tiles are short enough): 32 rows on the tiny layer's 4
+    experts (I = 128, one scale block cut into two tiles) and 8 on E = 1024
+    (H = 2816, I = 704: five blocks cut in two and a last native 64 + 64
+    block), and the tiny and 1-token layers with the wide tiles forced."""
+    layer, W = layer_with_weights(S._softmax_layer("tiny_small", seed=1016, E=4, H=256, I=128, T=16, k=2))
+    check_layer(m, layer, W)
+    check_layer(m, layer, W, extra_flags=m.W13_ONE_SM)
+    layer, W = layer_with_weights(S._softmax_layer("maxE_small1", seed=1017, E=1024, H=2816, I=704, T=1, k=8))
+    check_layer(m, layer, W)
+    layer, W = layer_with_weights(S.decode(1))
+    check_layer(m, layer, W, extra_flags=m.W13_ONE_SM)
+
+
 def test_small_batch_routing_most_experts(m):
     """240 routed rows over E = 1024 experts: the scale check and the routing
     of a batch of at most 256 rows run in one CTA (each thread one routed
@@ -178,12 +194,14 @@ def test_prefill_unwritten_slots_rejected_before_launch(m, prefill):
     assert bool((out == 7.0).all())
 
 
-def test_decode_refused_on_device_then_clean_call(m):
-    """At decode sizes the scale check and the routing share one kernel.  With
-    the host check skipped, a bad scale still stops the call on the device:
-    the GEMM kernels find the bad status, give back their TMEM and leave, and
-    out keeps its contents.  A following call on the same workspace is exact."""
-    layer, W = layer_with_weights(S.decode(8))
+@pytest.mark.parametrize("T", [1, 8])
+def test_decode_refused_on_device_then_clean_call(m, T):
+    """At decode sizes the scale check and the routing share one kernel (at
+    one token also the a1 quantiser).  With the host check skipped, a bad
+    scale still stops the call on the device: the GEMM kernels find the bad
+    status, give back their TMEM and leave, and out keeps its contents.  A
+    following call on the same workspace is exact."""
+    layer, W = layer_with_weights(S.decode(T))
     bad = device_weights(W)
     bad.w2_scale2 = bad.w2_scale2.clone()
     bad.w2_scale2[int(layer.topk_ids[0, 0])] = float("nan")
@@ -200,10 +218,16 @@ def test_decode_refused_on_device_then_clean_call(m):
     assert_close(host(out2), ref["out"], "out")
 
 
-def test_bad_expert_id_refused_on_device(m):
-    layer, W = layer_with_weights(S.tiny())
+@pytest.mark.parametrize("T", [64, 2])
+def test_bad_expert_id_refused_on_device(m, T):
+    """An expert id outside [0, E) stops the call on the device, out
+    untouched: 128 routed rows, and 4 (the routing CTA also quantises)."""
+    base = S.tiny()
+    layer = base if T == base.T else S._softmax_layer("tiny_T2", seed=base.seed, E=base.E, H=base.H, I=base.I,
+                                                      T=T, k=base.k)
+    layer, W = layer_with_weights(layer)
     ids = layer.topk_ids.copy()
-    ids[3, 0] = -1
+    ids[T // 2, 0] = -1
     out = torch.full((layer.T, layer.H), 5.0, device="cuda")
     with pytest.raises(m.Nvfp4Error) as ei:
         m.moe_forward(device_weights(W), dev_bf16(layer.x), dev(ids), dev(layer.topk_w), out=out,
