@@ -662,7 +662,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     gb.topk_w = topk_w;
     gb.out = out;
     gb.pairs = 0;
-    gb.small = 0;
+    gb.small = !ue && (long long)T * k <= kSmallPlanRowsW2;
     gb.live_mtiles = ra.live_mtiles;  // with 256-row padding, the m-tiles that hold rows
     if (ue) {
         gb.a_row_max = row_max + L.rows_cap;

@@ -37,6 +37,10 @@ constexpr long long kPairRowsPerExpert = 512;
 // 64-column tiles, the A stage holding an m-tile's first 32 rows (no m-tile
 // can hold more), and a deeper ring.
 constexpr long long kSmallPlanRows = 32;
+// Up to this many routed rows the w2 GEMM takes its small-batch plan: A in
+// the ring (an m-tile's first 64 rows), a deeper ring, the combine from
+// registers.
+constexpr long long kSmallPlanRowsW2 = 64;
 
 WsLayout make_layout(int T, int H, int I, int E, int k);
 
@@ -141,7 +145,7 @@ struct GemmArgs {
     DevHeader *hdr;
     int mtiles_cap;
     int pairs;                 // w13: CTA pairs on m-tile pairs (rows padded to 256 per expert)
-    int small;                 // w13: the small-batch plan (at most kSmallPlanRows routed rows, E4M3 scales)
+    int small;                 // the small-batch plan (w13: at most kSmallPlanRows routed rows, w2: kSmallPlanRowsW2)
     const int *live_mtiles;    // w2: the m-tiles holding rows, in order (nullable: all m-tiles)
 };
 cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st);

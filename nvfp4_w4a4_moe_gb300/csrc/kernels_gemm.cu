@@ -85,10 +85,15 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 //       7-stage ring.  At these sizes a tile's K loop is paced by the ring's
 //       round trip, not by its bytes: more stages in flight, on twice the
 //       tiles.
-constexpr int kDecRows = (int)kSmallPlanRows;
-static_assert(kDecRows % 16 == 0, "A is loaded in 16-row boxes");
+//  w2, small batches (at most kSmallPlanRowsW2 routed rows): A in the ring
+//       (an m-tile's first kSmallPlanRowsW2 rows, no tile pairs), a 7-stage
+//       ring, and the combine added from registers (a tile holds one or two
+//       live rows; no transpose buffer).
+constexpr int kDecRows = (int)kSmallPlanRows, kDecRowsW2 = (int)kSmallPlanRowsW2;
+static_assert(kDecRows % 16 == 0 && kDecRowsW2 % 16 == 0, "A is loaded in 16-row boxes");
 template <int EPI, bool CTA2 = false, bool DEC = false>
 struct Plan {
+    static constexpr int DEC_ROWS = EPI == 0 ? kDecRows : kDecRowsW2;  // small-batch plan: A rows per stage
     static constexpr int BN = DEC ? 128 : EPI == 0 ? 256 : 128;  // widest tile (MMA N)
     static constexpr int STAGES = DEC ? 7 : CTA2 ? 5 : 4;
     // w13 pairs: 16 epilogue warps of 32 columns each, so every warp releases
@@ -109,14 +114,14 @@ struct Plan {
     // fill f + A_SLOTS is issued the producer has waited for the MMAs of a ring
     // stage at or after the last one reading fill f (checked for every K depth
     // a pair can have, 1 .. A_SLOTS stages, and for unpaired tiles).
-    static constexpr int A_SLOTS = EPI == 1 ? 5 : 0;
+    static constexpr int A_SLOTS = EPI == 1 && !DEC ? 5 : 0;
     // A ring stages sit A_STRIDE apart; the MMA reads 128 rows from each
     // stage's start, so in the small-batch plan the rows past the loaded ones
     // read the following stages (their outputs are never stored), and the
     // region ends a full A tile after the last stage's start
-    static constexpr int A_STRIDE = DEC ? kDecRows * BK / 2 : A_BYTES;
-    static constexpr int RING_A_REGION = EPI == 1 ? 0 : (STAGES - 1) * A_STRIDE + A_BYTES;
-    static constexpr int SFB_BYTES = DEC ? 2 * 4 * SF_TILE : (BN / 128) * 4 * SF_TILE;
+    static constexpr int A_STRIDE = DEC ? DEC_ROWS * BK / 2 : A_BYTES;
+    static constexpr int RING_A_REGION = A_SLOTS > 0 ? 0 : (STAGES - 1) * A_STRIDE + A_BYTES;
+    static constexpr int SFB_BYTES = DEC && EPI == 0 ? 2 * 4 * SF_TILE : (BN / 128) * 4 * SF_TILE;
     static constexpr int SFB_STEP = BN / 32;               // TMEM columns per 64-K step of B scales
     static constexpr int SF_COLS = 16 + 4 * SFB_STEP;      // TMEM scale columns per stage
     static constexpr int SF_TMEM_COL = ACC_BUFS * BN;      // scale slots after the accumulator(s)
@@ -129,14 +134,14 @@ struct Plan {
     static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_XPOSE = (OFF_MISC + 16 + 15) & ~15;
-    static constexpr int XPOSE_BYTES = EPI == 1 ? NUM_EPI_WARPS * 32 * XPOSE_LD * 4 : 0;
+    static constexpr int XPOSE_BYTES = EPI == 1 && !DEC ? NUM_EPI_WARPS * 32 * XPOSE_LD * 4 : 0;
     static constexpr int SMEM_BYTES = OFF_XPOSE + XPOSE_BYTES + 1024;  // + alignment slack
     static_assert(SF_TMEM_COL + STAGES * SF_COLS <= TMEM_COLS, "scale slots exceed TMEM");
     static_assert(EPI_GROUPS == ACC_BUFS, "each epilogue group owns one accumulator");
     static_assert(OFF_B % 1024 == 0 && OFF_AS % 1024 == 0, "128-byte-swizzled operands start on 1024 bytes");
-    static_assert(EPI == 0 || (A_SLOTS == 5 && STAGES == 4), "the A-slot reuse argument is for 5 slots, 4 stages");
+    static_assert(EPI == 0 || DEC || (A_SLOTS == 5 && STAGES == 4), "the A-slot reuse argument is for 5 slots, 4 stages");
     static_assert(!CTA2 || EPI == 0, "CTA pairs: w13 only");
-    static_assert(!DEC || (EPI == 0 && !CTA2), "the small-batch plan: w13 on single CTAs");
+    static_assert(!DEC || !CTA2, "the small-batch plans: single CTAs");
     static_assert(SMEM_BYTES + (EPI == 0 ? (int)sizeof(DivTable2) : 0) <= 232448,
                   "shared memory plan exceeds the opt-in limit");
 };
@@ -344,7 +349,8 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
     // tile count: with few tiles per CTA, as in decode, that tail costs more
     // than the A loads it saves
     const int per_cta = (ntiles + G - 1) / G, per_cta_paired = 2 * ((MT * (NT / 2) + G - 1) / G);
-    const bool paired = EPI == 1 && KT <= P::A_SLOTS && NT % 2 == 0 && per_cta_paired * 32 <= per_cta * 33;
+    const bool paired =
+        EPI == 1 && !DEC && KT <= P::A_SLOTS && NT % 2 == 0 && per_cta_paired * 32 <= per_cta * 33;
     const int nunits = paired ? MT * (NT / 2) : ntiles;
     const int n_i = nunits > b ? ((nunits - b + G - 1) / G) * (paired ? 2 : 1) : 0;  // this CTA's tiles
     if (p.hdr->status != 0 || n_i == 0) {
@@ -389,17 +395,15 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
                 }
                 uint64_t *fb = &full[stage];
                 const bool a_now = EPI == 0 || fill_a;
-                // A: the whole m-tile, or (small-batch plan) its first kDecRows rows
-                const uint32_t a_bytes = DEC ? (uint32_t)(kDecRows * BK / 2) : (uint32_t)A_BYTES;
-                mbar_expect_tx(fb, (a_now ? a_bytes : 0u) + b_bytes + SFA_BYTES + sfb_bytes);
+                // A: the whole m-tile, or (small-batch plans) its first DEC_ROWS rows
+                const uint32_t a_bytes = DEC ? (uint32_t)(P::DEC_ROWS * BK / 2) : (uint32_t)A_BYTES;
+                mbar_expect_tx(fb, (a_now || DEC ? a_bytes : 0u) + b_bytes + SFA_BYTES + sfb_bytes);
                 uint8_t *sb = smem + OFF_B + stage * B_BYTES;
-                if constexpr (EPI == 0) {
-                    if (DEC) {
-                        for (int r = 0; r < kDecRows; r += 16)
-                            tma_2d(smem + OFF_A + stage * P::A_STRIDE + r * (BK / 2), &tmap_a16, kx, ti.mt * BM + r, fb);
-                    } else {
-                        tma_2d(smem + OFF_A + stage * A_BYTES, &tmap_a, kx, ti.mt * BM, fb);
-                    }
+                if constexpr (DEC) {
+                    for (int r = 0; r < P::DEC_ROWS; r += 16)
+                        tma_2d(smem + OFF_A + stage * P::A_STRIDE + r * (BK / 2), &tmap_a16, kx, ti.mt * BM + r, fb);
+                } else if constexpr (EPI == 0) {
+                    tma_2d(smem + OFF_A + stage * A_BYTES, &tmap_a, kx, ti.mt * BM, fb);
                 } else if (fill_a) {
                     const int f = (paired ? (i >> 1) : i) * KT + kt;  // A fill f goes to slot f % A_SLOTS
                     tma_2d(smem + P::OFF_AS + (f % P::A_SLOTS) * A_BYTES, &tmap_a, kx, ti.mt * BM, fb);
@@ -448,7 +452,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
         // and a full stage's four MMAs are unrolled.
         uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
         bool ok = true;
-        const uint64_t da0 = desc_sw128(su32(smem + (EPI == 1 ? P::OFF_AS : OFF_A))),
+        const uint64_t da0 = desc_sw128(su32(smem + (P::A_SLOTS > 0 ? P::OFF_AS : OFF_A))),
                        db0 = desc_sw128(su32(smem + OFF_B));
         const uint32_t sf0 = tmem + SF_TMEM_COL;
         const int k_full = p.K / BK;  // stages with four 64-K steps
@@ -473,8 +477,8 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
                 // w2: the A fill this stage reads (landed with this tile's, or
                 // for the second of a pair the first's, ring stage)
                 int sl = stage;
-                if constexpr (EPI == 1) sl = ((paired ? (i >> 1) : i) * KT + kt) % P::A_SLOTS;
-                const uint64_t da = da0 + (uint64_t)(sl * ((EPI == 1 ? A_BYTES : P::A_STRIDE) >> 4));
+                if constexpr (P::A_SLOTS > 0) sl = ((paired ? (i >> 1) : i) * KT + kt) % P::A_SLOTS;
+                const uint64_t da = da0 + (uint64_t)(sl * (P::A_STRIDE >> 4));
                 const uint64_t db = db0 + (uint64_t)(stage * (B_BYTES >> 4));
                 const uint32_t sfa = sf0 + stage * SF_COLS, sfb = sfa + 16;
                 if constexpr (CTA2) {
@@ -810,8 +814,31 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
                 // segments.
                 const float scale = s0;
                 const int sub = lane >> 3, cc = (lane & 7) * 4;
+                if (DEC) {
+                    // a tile holds one or two live rows: each valid lane adds
+                    // its own row's 32 columns, from registers
 #pragma unroll 1
-                for (int c2 = 0; c2 < 2; ++c2) {
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        const int cbase = 64 * half + 32 * c2;
+                        float v[32];
+                        tmem_ld16(col0 + cbase, v);
+                        tmem_ld16(col0 + cbase + 16, v + 16);
+                        tmem_wait_ld(v);
+                        if (c2 == 1) {
+                            tc_fence_before();
+                            mbar_arrive(&acc_empty[acc]);
+                        }
+                        if (valid) {
+                            float *o = p.out + (size_t)t * p.H + nt * 128 + cbase;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                red_add_v4(o + 4 * j, v[4 * j] * scale, v[4 * j + 1] * scale, v[4 * j + 2] * scale,
+                                           v[4 * j + 3] * scale);
+                        }
+                    }
+                }
+#pragma unroll 1
+                for (int c2 = 0; c2 < (DEC ? 0 : 2); ++c2) {
                     const int cbase = 64 * half + 32 * c2;
                     float v[32];
                     tmem_ld16(col0 + cbase, v);
@@ -1007,6 +1034,7 @@ cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st)
 }
 cudaError_t launch_gemm_w2(const GemmArgs &a, cudaStream_t st)
 {
+    if (a.small && !a.ue8m0) return launch_gemm<1, false, false, true>(a, st);
     return a.ue8m0 ? launch_gemm<1, true, false>(a, st) : launch_gemm<1, false, false>(a, st);
 }
 

@@ -111,6 +111,15 @@ def test_small_batch_plan(m):
     check_layer(m, layer, W, extra_flags=m.W13_ONE_SM)
 
 
+def test_small_batch_plan_w2_full_stage(m):
+    """w2's small-batch plan (at most 64 routed rows: A stages of an m-tile's
+    first 64 rows, the combine from registers) with all 64 rows in one
+    m-tile (one expert, k = 1), and 64 rows over two experts."""
+    for E, k, T in ((1, 1, 64), (2, 2, 32)):
+        layer, W = layer_with_weights(S._softmax_layer(f"few_experts{E}", seed=1018, E=E, H=256, I=128, T=T, k=k))
+        check_layer(m, layer, W)
+
+
 def test_small_batch_routing_most_experts(m):
     """240 routed rows over E = 1024 experts: the scale check and the routing
     of a batch of at most 256 rows run in one CTA (each thread one routed
