@@ -516,9 +516,11 @@ def quant_workload(m, torch, w, args):
 
 def decode_leg(m, torch, w, args):
     """The decode-shaped layers (same experts, 1-64 tokens): latency per call
-    of the plain forward and of a CUDA-graph replay of it, tokens/s, and the
-    bandwidth over the weight bytes of the experts the batch touches (codes +
-    block scales of w13 and w2)."""
+    of the plain forward, of a CUDA-graph replay of one call, and per call
+    inside a graph of ten back-to-back calls (as in a captured multi-layer
+    decode step, where one call's first kernel overlaps the previous call's
+    tail), tokens/s, and the bandwidth over the weight bytes of the experts
+    the batch touches (codes + block scales of w13 and w2)."""
     H, I, E = w.H, w.I, w.E
     per_expert = 2 * I * H // 2 + 2 * I * H // 16 + H * I // 2 + H * I // 16
     res = {}
@@ -546,7 +548,7 @@ def decode_leg(m, torch, w, args):
         b.record()
         torch.cuda.synchronize()
         us = a.elapsed_time(b) / n * 1e3
-        graph_us, graph_err = None, None
+        graph_us, graph_err, graph10_us = None, None, None
         try:
             g = torch.cuda.CUDAGraph()
             s = torch.cuda.Stream()
@@ -569,11 +571,28 @@ def decode_leg(m, torch, w, args):
             st, _ = m.moe_status(ws)
             if st != m.OK:
                 graph_us, graph_err = None, f"device status {st} after graph replays"
+            # ten calls captured in one graph: the steady per-call time
+            g10 = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g10, stream=s):
+                    for _ in range(10):
+                        m.moe_forward(wd, x, ids, tw, out=out, ws=ws, flags=flags, stream=s)
+            torch.cuda.current_stream().wait_stream(s)
+            for _ in range(3):
+                g10.replay()
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(n // 10):
+                g10.replay()
+            b.record()
+            torch.cuda.synchronize()
+            graph10_us = a.elapsed_time(b) / (n // 10 * 10) * 1e3
         except Exception as ex:  # capture support depends on the driver; report, do not fail the run
             graph_err = f"{type(ex).__name__}: {ex}"[:200]
         touched = len(np.unique(L.topk_ids))
         best = graph_us if graph_us is not None else us
-        res[str(T)] = {"us_per_call": us, "us_per_graph_replay": graph_us, "graph_error": graph_err,
+        res[str(T)] = {"us_per_call": us, "us_per_graph_replay": graph_us,
+                       "us_per_call_in_graph_of_10": graph10_us, "graph_error": graph_err,
                        "tokens_per_s": T / (best * 1e-6), "experts_touched": touched,
                        "weight_gbs": touched * per_expert / (best * 1e-6) / 1e9}
     return res

@@ -383,10 +383,13 @@ __global__ void __launch_bounds__(kRouteThreads) validate_route_kernel(ValidateA
     route_body(a);
 }
 
-// The scale check and the routing of a small batch (at most kRouteThreads
-// routed rows, rows padded to 128 per expert) in one CTA: one routed row per
-// thread, its rank among equal experts from a warp match and the per-warp
-// counts, the offsets from one block scan.  The same outputs as route_body.
+// The scale check and the routing of a small batch (at most kTinyRouteRows
+// routed rows, rows padded to 128 per expert) in one CTA: up to four routed
+// rows per thread (row f = tid + 256 i), each row's rank among equal experts
+// from a warp match within its 32-row step and the per-step counts, the
+// offsets from one block scan.  The same outputs as route_body.
+constexpr int kTinyRouteRowsPerThread = 4;
+constexpr int kTinyRouteRows = kRouteThreads * kTinyRouteRowsPerThread;
 __global__ void __launch_bounds__(kRouteThreads) validate_route_tiny_kernel(ValidateArgs v, RouteArgs a)
 {
     extern __shared__ int sh[];
@@ -395,20 +398,31 @@ __global__ void __launch_bounds__(kRouteThreads) validate_route_tiny_kernel(Vali
     pdl_trigger();
     pdl_wait();  // whatever ran before on the stream (a previous call may still read the header)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, E = a.E;
-    const int f = tid;
-    const bool live = f < a.R;
-    const int id = live ? a.ids[f] : -1;  // in flight during the scale check
-    int *wcnt = sh;                     // [kRouteWarps][E]: a warp's rows per expert, then its first rank
-    int *off = wcnt + kRouteWarps * E;  // [E + 1]: counts, then compact offsets
-    int *poff = off + E + 1;            // [E + 1]: padded offsets
-    for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) wcnt[i] = 0;
+    const int nsteps = (a.R + 31) >> 5;  // 32-row steps; step s holds rows [32 s, 32 s + 32)
+    int id[kTinyRouteRowsPerThread];
+#pragma unroll
+    for (int i = 0; i < kTinyRouteRowsPerThread; ++i) {
+        const int f = tid + kRouteThreads * i;
+        id[i] = f < a.R ? a.ids[f] : -1;  // in flight during the scale check
+    }
+    int *wcnt = sh;                // [nsteps][E]: a step's rows per expert, then its first rank
+    int *off = wcnt + nsteps * E;  // [E + 1]: counts, then compact offsets
+    int *poff = off + E + 1;       // [E + 1]: padded offsets
+    for (int i = tid; i < nsteps * E; i += kRouteThreads) wcnt[i] = 0;
     if (tid == 0) s_bad = 0;
     if (validate_body(v) != 0) return;  // (its block barriers order the clearing above)
-    const bool ok = live && id >= 0 && id < E;
-    if (live && !ok) s_bad = 1;
-    const unsigned peers = __match_any_sync(0xffffffffu, ok ? id : -1 - lane);
-    const int wrank = __popc(peers & ((1u << lane) - 1u));
-    if (ok && wrank == 0) wcnt[warp * E + id] = __popc(peers);
+    bool ok[kTinyRouteRowsPerThread];
+    int wrank[kTinyRouteRowsPerThread];
+#pragma unroll
+    for (int i = 0; i < kTinyRouteRowsPerThread; ++i) {
+        const int f = tid + kRouteThreads * i, step = f >> 5;
+        const bool live = f < a.R;
+        ok[i] = live && id[i] >= 0 && id[i] < E;
+        if (live && !ok[i]) s_bad = 1;
+        const unsigned peers = __match_any_sync(0xffffffffu, ok[i] ? id[i] : -1 - lane);
+        wrank[i] = __popc(peers & ((1u << lane) - 1u));
+        if (ok[i] && wrank[i] == 0) wcnt[step * E + id[i]] = __popc(peers);
+    }
     __syncthreads();
     if (s_bad) {
         if (tid == 0) {
@@ -419,9 +433,9 @@ __global__ void __launch_bounds__(kRouteThreads) validate_route_tiny_kernel(Vali
     }
     for (int e = tid; e < E; e += kRouteThreads) {
         int run = 0;
-        for (int w = 0; w < kRouteWarps; ++w) {
-            const int c = wcnt[w * E + e];
-            wcnt[w * E + e] = run;
+        for (int st = 0; st < nsteps; ++st) {
+            const int c = wcnt[st * E + e];
+            wcnt[st * E + e] = run;
             run += c;
         }
         off[e] = run;
@@ -497,9 +511,12 @@ __global__ void __launch_bounds__(kRouteThreads) validate_route_tiny_kernel(Vali
         }
     }
     __syncthreads();
-    if (ok) {
-        const int pos = wcnt[warp * E + id] + wrank;
-        const int compact = off[id] + pos, padded = poff[id] + pos;
+#pragma unroll
+    for (int i = 0; i < kTinyRouteRowsPerThread; ++i) {
+        if (!ok[i]) continue;
+        const int f = tid + kRouteThreads * i;
+        const int pos = wcnt[(f >> 5) * E + id[i]] + wrank[i];
+        const int compact = off[id[i]] + pos, padded = poff[id[i]] + pos;
         a.row_of[f] = a.padded ? padded : compact;
         if (a.perm) a.perm[compact] = f;
         if (a.row_src) a.row_src[padded] = f;
@@ -824,7 +841,9 @@ cudaError_t launch_validate(const ValidateArgs &a, cudaStream_t st)
 namespace {
 // Routing launch shape: a cooperative grid of at most as many CTAs as can be
 // resident at once, each taking every gridDim-th chunk.
-size_t tiny_route_smem(int E) { return sizeof(int) * ((size_t)kRouteWarps * E + 2 * ((size_t)E + 1)); }
+// per-step counts for R routed rows, and the two offset arrays
+size_t tiny_route_smem(int R, int E) { return sizeof(int) * ((size_t)((R + 31) / 32) * E + 2 * ((size_t)E + 1)); }
+constexpr size_t kTinyRouteSmemMax = 96 * 1024;
 
 size_t route_smem(int E)
 {
@@ -879,7 +898,7 @@ cudaError_t launch_route(const RouteArgs &a, cudaStream_t st)
 
 cudaError_t launch_validate_route(const ValidateArgs &v, const RouteArgs &a, cudaStream_t st)
 {
-    if (a.R <= kRouteThreads && a.pad_rows != 256 && !a.live_mtiles) {
+    if (a.R <= kTinyRouteRows && a.pad_rows != 256 && !a.live_mtiles && tiny_route_smem(a.R, a.E) <= kTinyRouteSmemMax) {
         static bool attr_set[64] = {false};
         int dev = 0;
         cudaError_t err = cudaGetDevice(&dev);
@@ -887,11 +906,12 @@ cudaError_t launch_validate_route(const ValidateArgs &v, const RouteArgs &a, cud
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
         if (!attr_set[dev]) {
             err = cudaFuncSetAttribute(validate_route_tiny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)tiny_route_smem(1024));
+                                       (int)kTinyRouteSmemMax);
             if (err != cudaSuccess) return err;
             attr_set[dev] = true;
         }
-        err = launch_pdl(validate_route_tiny_kernel, dim3(1), dim3(kRouteThreads), tiny_route_smem(a.E), st, v, a);
+        err = launch_pdl(validate_route_tiny_kernel, dim3(1), dim3(kRouteThreads), tiny_route_smem(a.R, a.E), st, v,
+                         a);
         return err != cudaSuccess ? err : cudaGetLastError();
     }
     int grid = 0;

@@ -122,9 +122,17 @@ def test_small_batch_plan_w2_full_stage(m):
 
 def test_small_batch_routing_most_experts(m):
     """240 routed rows over E = 1024 experts: the scale check and the routing
-    of a batch of at most 256 rows run in one CTA (each thread one routed
-    row, four experts per thread in the offset scan)."""
+    of a small batch run in one CTA (each thread one routed row, four experts
+    per thread in the offset scan)."""
     layer, W = layer_with_weights(S._softmax_layer("maxE_small", seed=1012, E=1024, H=256, I=128, T=60, k=4))
+    check_layer(m, layer, W)
+
+
+@pytest.mark.parametrize("E,T", [(512, 120), (128, 128)])
+def test_small_batch_routing_four_rows_per_thread(m, E, T):
+    """960 and 1024 routed rows (top-8) in the one-CTA routing: four routed
+    rows per thread, ranks from 30 or 32 steps of 32 rows."""
+    layer, W = layer_with_weights(S._softmax_layer(f"route4_E{E}", seed=1019, E=E, H=256, I=128, T=T, k=8))
     check_layer(m, layer, W)
 
 
