@@ -520,9 +520,14 @@ def decode_leg(m, torch, w, args):
     inside a graph of ten back-to-back calls (as in a captured multi-layer
     decode step, where one call's first kernel overlaps the previous call's
     tail), tokens/s, and the bandwidth over the weight bytes of the experts
-    the batch touches (codes + block scales of w13 and w2)."""
+    the batch touches (codes + block scales of w13 and w2).  A replayed call
+    finds the weights it touched in L2 (26.8 MB at one token), so one more
+    figure takes the calls of a graph over eight copies of the weights at
+    other addresses (3.4 GB), as in a decode step through eight layers: each
+    call's weights come from HBM."""
     H, I, E = w.H, w.I, w.E
     per_expert = 2 * I * H // 2 + 2 * I * H // 16 + H * I // 2 + H * I // 16
+    copies = [(w.w13_q.clone(), w.w2_q.clone(), w.prepared.clone()) for _ in range(8)]
     res = {}
     for T in (1, 8, 32, 64):
         L = S.decode(T)
@@ -548,7 +553,7 @@ def decode_leg(m, torch, w, args):
         b.record()
         torch.cuda.synchronize()
         us = a.elapsed_time(b) / n * 1e3
-        graph_us, graph_err, graph10_us = None, None, None
+        graph_us, graph_err, graph10_us, copies_us = None, None, None, None
         try:
             g = torch.cuda.CUDAGraph()
             s = torch.cuda.Stream()
@@ -587,12 +592,38 @@ def decode_leg(m, torch, w, args):
             b.record()
             torch.cuda.synchronize()
             graph10_us = a.elapsed_time(b) / (n // 10 * 10) * 1e3
+            # one call per weight copy in one graph
+            wcs = []
+            for w13q, w2q, prep in copies:
+                wc = m.MoEWeights(E, H, I, w13q, w.w13_sf, w.w13_scale2, wd.w13_input_scale, w2q, w.w2_sf,
+                                  w.w2_scale2, w.w2_input_scale)
+                wc.prepared = prep
+                wcs.append(wc)
+            g8 = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g8, stream=s):
+                    for wc in wcs:
+                        m.moe_forward(wc, x, ids, tw, out=out, ws=ws, flags=flags, stream=s)
+            torch.cuda.current_stream().wait_stream(s)
+            for _ in range(3):
+                g8.replay()
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(n // 8):
+                g8.replay()
+            b.record()
+            torch.cuda.synchronize()
+            copies_us = a.elapsed_time(b) / (n // 8 * 8) * 1e3
+            st, _ = m.moe_status(ws)
+            if st != m.OK:
+                copies_us, graph_err = None, f"device status {st} after the weight-copy graph"
         except Exception as ex:  # capture support depends on the driver; report, do not fail the run
             graph_err = f"{type(ex).__name__}: {ex}"[:200]
         touched = len(np.unique(L.topk_ids))
         best = graph_us if graph_us is not None else us
         res[str(T)] = {"us_per_call": us, "us_per_graph_replay": graph_us,
-                       "us_per_call_in_graph_of_10": graph10_us, "graph_error": graph_err,
+                       "us_per_call_in_graph_of_10": graph10_us,
+                       "us_per_call_over_8_weight_copies": copies_us, "graph_error": graph_err,
                        "tokens_per_s": T / (best * 1e-6), "experts_touched": touched,
                        "weight_gbs": touched * per_expert / (best * 1e-6) / 1e9}
     return res

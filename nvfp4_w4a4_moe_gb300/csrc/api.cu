@@ -204,6 +204,8 @@ static int header_status(const DevHeader &h, int *first_bad)
         return fail(NVFP4_ERR_INVALID_ARG, "the prepared weights were converted for the other block-scale format");
     if (h.status == 5 || (h.error_flags & (kErrTimeoutProducer | kErrTimeoutMma | kErrTimeoutEpilogue | kErrTimeoutRoute)))
         return fail(NVFP4_ERR_DEVICE_TIMEOUT, "a device-side wait expired (flags 0x%x)", h.error_flags);
+    if (h.error_flags & kErrPlan)
+        return fail(NVFP4_ERR_CUDA, "a GEMM was launched outside its plan's conditions (flags 0x%x)", h.error_flags);
     return NVFP4_OK;
 }
 
@@ -576,23 +578,42 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
         if (h.status) return header_status(h, nullptr);
     }
 
-    QuantArgs qa;
-    std::memset(&qa, 0, sizeof(qa));
-    qa.x = x;
-    qa.ids = ids;
-    qa.row_of = ra.row_of;
-    qa.g = g;
-    qa.T = T;
-    qa.H = H;
-    qa.k = k;
-    qa.q = base + L.a1q;
-    qa.sf = base + L.sf1;
-    qa.sf_swizzled = 1;
-    qa.sf_kc = L.kc1;
-    qa.sf_ue8m0 = ue ? 1 : 0;  // UE8M0 bytes, carried to the tensor cores per row by the GEMM
-    qa.row_max = ue ? row_max : nullptr;
-    qa.hdr = hdr;
-    NV_CUDA(launch_quant_experts(qa, st), "launching the a1 quantiser");
+    // The w13 GEMM's small-batch plan when its waves of 64-column tiles (over
+    // at most min(R, E) busy experts) take less time than the wide plan's
+    // waves; a narrow tile's K loop takes about 0.55 of a wide one's.  It
+    // quantises A itself when every CTA gets one tile (m-tiles x 64-column
+    // tiles within the SM count) and K fits its persistent A buffer.
+    const long long sms = sm_count();
+    bool small_w13, a_inline;
+    {
+        const long long busy = std::min<long long>((long long)R, E);
+        const long long small_waves = (busy * ((I + 63) / 64) + sms - 1) / sms;
+        const long long wide_waves = (busy * ((I + 127) / 128) + sms - 1) / sms;
+        small_w13 = !pairs && !ue && !(flags & NVFP4_W13_ONE_SM) && (long long)R <= kSmallPlanRows &&
+                    100 * small_waves < 182 * wide_waves;
+        // (at most kSmallPlanRows <= 128 rows: one m-tile per busy expert)
+        a_inline = small_w13 && busy * ((I + 63) / 64) <= sms && (long long)H <= kInlineQuantMaxK;
+    }
+
+    if (!a_inline) {
+        QuantArgs qa;
+        std::memset(&qa, 0, sizeof(qa));
+        qa.x = x;
+        qa.ids = ids;
+        qa.row_of = ra.row_of;
+        qa.g = g;
+        qa.T = T;
+        qa.H = H;
+        qa.k = k;
+        qa.q = base + L.a1q;
+        qa.sf = base + L.sf1;
+        qa.sf_swizzled = 1;
+        qa.sf_kc = L.kc1;
+        qa.sf_ue8m0 = ue ? 1 : 0;  // UE8M0 bytes, carried to the tensor cores per row by the GEMM
+        qa.row_max = ue ? row_max : nullptr;
+        qa.hdr = hdr;
+        NV_CUDA(launch_quant_experts(qa, st), "launching the a1 quantiser");
+    }
     NV_CUDA(mark(3), "recording an event");
 
     const uint8_t *pw = static_cast<const uint8_t *>(prepared);
@@ -633,16 +654,11 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     ga.hdr = hdr;
     ga.mtiles_cap = L.mtiles_cap;
     ga.pairs = pairs ? 1 : 0;
-    // the small-batch plan when its waves of 64-column tiles (over at most
-    // min(R, E) busy experts) take less time than the wide plan's waves; a
-    // narrow tile's K loop takes about 0.55 of a wide one's
-    {
-        const long long busy = std::min<long long>((long long)T * k, E), sms = sm_count();
-        const long long small_waves = (busy * ((I + 63) / 64) + sms - 1) / sms;
-        const long long wide_waves = (busy * ((I + 127) / 128) + sms - 1) / sms;
-        ga.small = !pairs && !ue && !(flags & NVFP4_W13_ONE_SM) && (long long)T * k <= kSmallPlanRows &&
-                   100 * small_waves < 182 * wide_waves;
-    }
+    ga.small = small_w13 ? 1 : 0;
+    ga.a_inline = a_inline ? 1 : 0;
+    ga.x = x;
+    ga.g1 = g;
+    ga.row_src = ra.row_src;
     NV_CUDA(launch_gemm_w13(ga, st), "launching the w13 GEMM");
     NV_CUDA(mark(4), "recording an event");
 
@@ -659,6 +675,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     gb.alpha = alpha2;
     gb.h_dump = nullptr;
     gb.row_src = ra.row_src;
+    gb.a_inline = 0;
     gb.topk_w = topk_w;
     gb.out = out;
     gb.pairs = 0;

@@ -54,6 +54,7 @@ enum : int {
     kErrTimeoutMma = 4,
     kErrTimeoutEpilogue = 8,
     kErrTimeoutRoute = 16,
+    kErrPlan = 32,  // a kernel was launched outside the conditions of its plan
 };
 
 // RN, saturating FP32 -> E4M3 (t >= 0): the byte of the second source.

@@ -41,6 +41,10 @@ constexpr long long kSmallPlanRows = 32;
 // the ring (an m-tile's first 64 rows), a deeper ring, the combine from
 // registers.
 constexpr long long kSmallPlanRowsW2 = 64;
+// The w13 small-batch plan quantises its A rows itself (no a1 quantiser
+// launch) when every CTA gets one tile and K is at most this: the m-tile's
+// 32 rows of all K slices stay in shared memory for the whole kernel.
+constexpr long long kInlineQuantMaxK = 3072;
 
 WsLayout make_layout(int T, int H, int I, int E, int k);
 
@@ -146,6 +150,9 @@ struct GemmArgs {
     int mtiles_cap;
     int pairs;                 // w13: CTA pairs on m-tile pairs (rows padded to 256 per expert)
     int small;                 // the small-batch plan (w13: at most kSmallPlanRows routed rows, w2: kSmallPlanRowsW2)
+    int a_inline;              // w13 small-batch plan: A quantised in the kernel from x (also written to a_q / a_sf)
+    const uint16_t *x;         // a_inline: BF16 tokens [T, K]
+    const float *g1;           // a_inline: per-expert global scale of the A rows
     const int *live_mtiles;    // w2: the m-tiles holding rows, in order (nullable: all m-tiles)
 };
 cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st);

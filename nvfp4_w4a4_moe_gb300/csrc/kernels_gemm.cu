@@ -89,13 +89,21 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 //       (an m-tile's first kSmallPlanRowsW2 rows, no tile pairs), a 7-stage
 //       ring, and the combine added from registers (a tile holds one or two
 //       live rows; no transpose buffer).
+//  w13, small batches where every CTA holds one tile (QA): the small-batch
+//       plan with A quantised in the kernel.  The epilogue warps, idle until
+//       the first accumulator, quantise the m-tile's rows (the quantiser's
+//       block routine) into a persistent buffer of all its K slices, in the
+//       layout a TMA 128-byte-swizzled load leaves, and their scales into
+//       persistent scale tiles; the producer streams only the weights, and
+//       the a1 quantiser launch goes.  A 6-stage ring.
 constexpr int kDecRows = (int)kSmallPlanRows, kDecRowsW2 = (int)kSmallPlanRowsW2;
 static_assert(kDecRows % 16 == 0 && kDecRowsW2 % 16 == 0, "A is loaded in 16-row boxes");
-template <int EPI, bool CTA2 = false, bool DEC = false>
+constexpr int kQaSlices = (int)kInlineQuantMaxK / BK;  // K slices of the persistent A buffer
+template <int EPI, bool CTA2 = false, bool DEC = false, bool QA = false>
 struct Plan {
     static constexpr int DEC_ROWS = EPI == 0 ? kDecRows : kDecRowsW2;  // small-batch plan: A rows per stage
     static constexpr int BN = DEC ? 128 : EPI == 0 ? 256 : 128;  // widest tile (MMA N)
-    static constexpr int STAGES = DEC ? 7 : CTA2 ? 5 : 4;
+    static constexpr int STAGES = QA ? 6 : DEC ? 7 : CTA2 ? 5 : 4;
     // w13 pairs: 16 epilogue warps of 32 columns each, so every warp releases
     // the accumulator after a single TMEM load (the pair form's stages are
     // shorter, and the release gates the next tile's MMAs); 8 for w13 on
@@ -120,7 +128,9 @@ struct Plan {
     // read the following stages (their outputs are never stored), and the
     // region ends a full A tile after the last stage's start
     static constexpr int A_STRIDE = DEC ? DEC_ROWS * BK / 2 : A_BYTES;
-    static constexpr int RING_A_REGION = A_SLOTS > 0 ? 0 : (STAGES - 1) * A_STRIDE + A_BYTES;
+    static constexpr int RING_A_REGION =
+        A_SLOTS > 0 ? 0 : ((QA ? kQaSlices : STAGES) - 1) * A_STRIDE + A_BYTES;  // QA: the persistent A slices
+    static constexpr int SFA_REGION = (QA ? kQaSlices : STAGES) * SFA_BYTES;      // QA: persistent A scale tiles
     static constexpr int SFB_BYTES = DEC && EPI == 0 ? 2 * 4 * SF_TILE : (BN / 128) * 4 * SF_TILE;
     static constexpr int SFB_STEP = BN / 32;               // TMEM columns per 64-K step of B scales
     static constexpr int SF_COLS = 16 + 4 * SFB_STEP;      // TMEM scale columns per stage
@@ -128,10 +138,10 @@ struct Plan {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + RING_A_REGION;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+    static constexpr int OFF_SFB = OFF_SFA + SFA_REGION;
     static constexpr int OFF_AS = OFF_SFB + STAGES * SFB_BYTES;  // the A slots (w2)
     static constexpr int OFF_BAR = OFF_AS + A_SLOTS * A_BYTES;
-    static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_BUFS + 1;
+    static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_BUFS + 2;  // + drain, QA's A-ready
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_XPOSE = (OFF_MISC + 16 + 15) & ~15;
     static constexpr int XPOSE_BYTES = EPI == 1 && !DEC ? NUM_EPI_WARPS * 32 * XPOSE_LD * 4 : 0;
@@ -142,6 +152,7 @@ struct Plan {
     static_assert(EPI == 0 || DEC || (A_SLOTS == 5 && STAGES == 4), "the A-slot reuse argument is for 5 slots, 4 stages");
     static_assert(!CTA2 || EPI == 0, "CTA pairs: w13 only");
     static_assert(!DEC || !CTA2, "the small-batch plans: single CTAs");
+    static_assert(!QA || (DEC && EPI == 0 && DEC_ROWS == 32), "A quantised in the kernel: w13's small-batch plan");
     static_assert(SMEM_BYTES + (EPI == 0 ? (int)sizeof(DivTable2) : 0) <= 232448,
                   "shared memory plan exceeds the opt-in limit");
 };
@@ -268,12 +279,12 @@ __device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int 
 // prepared.  The epilogue multiplies both rows' factors back: the A row's
 // into the row scale, the weight row's per output column.  w13 then writes
 // a2 as UE8M0 bytes with each row's largest byte (out_row_max).
-template <int EPI, bool UE, bool CTA2, bool DEC>
-__global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
+template <int EPI, bool UE, bool CTA2, bool DEC, bool QA>
+__global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_a16, const GemmArgs p, const DivTable tab_in)
 {
-    using P = Plan<EPI, CTA2, DEC>;
+    using P = Plan<EPI, CTA2, DEC, QA>;
     constexpr int STAGES = P::STAGES, ACC_BUFS = P::ACC_BUFS, OFF_A = P::OFF_A, OFF_B = P::OFF_B,
                   OFF_SFA = P::OFF_SFA, OFF_SFB = P::OFF_SFB, OFF_BAR = P::OFF_BAR, OFF_MISC = P::OFF_MISC,
                   OFF_XPOSE = P::OFF_XPOSE, B_BYTES = P::B_BYTES, SFB_BYTES = P::SFB_BYTES,
@@ -284,7 +295,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint64_t *full = bars, *empty = bars + STAGES, *sf_ready = bars + 2 * STAGES, *acc_full = bars + 3 * STAGES,
-             *acc_empty = acc_full + ACC_BUFS, *drain = acc_empty + ACC_BUFS;
+             *acc_empty = acc_full + ACC_BUFS, *drain = acc_empty + ACC_BUFS, *qa_ready = drain + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
 
@@ -309,6 +320,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
             mbar_init(&acc_empty[i], CTA2 ? 2 * P::NUM_EPI_WARPS : EPI_THREADS / EPI_GROUPS);
         }
         mbar_init(drain, 1);
+        if (QA) mbar_init(qa_ready, P::NUM_EPI_WARPS);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -353,7 +365,10 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
         EPI == 1 && !DEC && KT <= P::A_SLOTS && NT % 2 == 0 && per_cta_paired * 32 <= per_cta * 33;
     const int nunits = paired ? MT * (NT / 2) : ntiles;
     const int n_i = nunits > b ? ((nunits - b + G - 1) / G) * (paired ? 2 : 1) : 0;  // this CTA's tiles
-    if (p.hdr->status != 0 || n_i == 0) {
+    // QA keeps one m-tile's A for the whole kernel: the host takes it only
+    // when no CTA gets a second tile (a broken promise is reported, not run)
+    if (QA && n_i > 1 && threadIdx.x == 0) atomicOr(&p.hdr->error_flags, kErrPlan);
+    if (p.hdr->status != 0 || n_i == 0 || (QA && n_i > 1)) {
         // nothing to do (same decision in every thread, and in both CTAs of a
         // pair): give TMEM back
         if (warp == 1) {
@@ -396,10 +411,13 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
                 uint64_t *fb = &full[stage];
                 const bool a_now = EPI == 0 || fill_a;
                 // A: the whole m-tile, or (small-batch plans) its first DEC_ROWS rows
+                // (QA: neither A nor its scales, quantised in the kernel)
                 const uint32_t a_bytes = DEC ? (uint32_t)(P::DEC_ROWS * BK / 2) : (uint32_t)A_BYTES;
-                mbar_expect_tx(fb, (a_now || DEC ? a_bytes : 0u) + b_bytes + SFA_BYTES + sfb_bytes);
+                mbar_expect_tx(fb, QA ? b_bytes + sfb_bytes
+                                      : (a_now || DEC ? a_bytes : 0u) + b_bytes + SFA_BYTES + sfb_bytes);
                 uint8_t *sb = smem + OFF_B + stage * B_BYTES;
-                if constexpr (DEC) {
+                if constexpr (QA) {
+                } else if constexpr (DEC) {
                     for (int r = 0; r < P::DEC_ROWS; r += 16)
                         tma_2d(smem + OFF_A + stage * P::A_STRIDE + r * (BK / 2), &tmap_a16, kx, ti.mt * BM + r, fb);
                 } else if constexpr (EPI == 0) {
@@ -423,8 +441,9 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
                 } else {
                     tma_2d(sb, &tmap_b, kx, ti.e * p.N + ti.nt * 128, fb);
                 }
-                bulk_g2s(smem + OFF_SFA + stage * SFA_BYTES,
-                         p.a_sf + ((size_t)ti.mt * p.a_kc + 4 * kt) * SF_TILE, SFA_BYTES, fb);
+                if (!QA)
+                    bulk_g2s(smem + OFF_SFA + stage * SFA_BYTES,
+                             p.a_sf + ((size_t)ti.mt * p.a_kc + 4 * kt) * SF_TILE, SFA_BYTES, fb);
                 bulk_g2s(smem + OFF_SFB + stage * SFB_BYTES, b_sf + (size_t)4 * kt * ti.nblk * SF_TILE, sfb_bytes,
                          fb);
                 issued |= 1u << stage;
@@ -456,6 +475,9 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
                        db0 = desc_sw128(su32(smem + OFF_B));
         const uint32_t sf0 = tmem + SF_TMEM_COL;
         const int k_full = p.K / BK;  // stages with four 64-K steps
+        // QA: the A slices are written by the epilogue warps (generic proxy,
+        // fenced to the async proxy before their arrival)
+        if (QA && !mbar_wait(qa_ready, 0, abort_flag, kWaitLimitNs)) ok = false;
 
         for (int i = 0; i < n_i && ok; ++i) {
             const int nt = (b + i * G) % NT;  // w13: the tile's width (w2 takes N128 throughout)
@@ -476,7 +498,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
                 tc_fence_after();
                 // w2: the A fill this stage reads (landed with this tile's, or
                 // for the second of a pair the first's, ring stage)
-                int sl = stage;
+                int sl = QA ? kt : stage;  // QA: the persistent slice of this K step
                 if constexpr (P::A_SLOTS > 0) sl = ((paired ? (i >> 1) : i) * KT + kt) % P::A_SLOTS;
                 const uint64_t da = da0 + (uint64_t)(sl * (P::A_STRIDE >> 4));
                 const uint64_t db = db0 + (uint64_t)(stage * (B_BYTES >> 4));
@@ -555,6 +577,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
         // the m-tile; its bytes are carried with that row's shift.  The rows'
         // largest bytes are loaded one tile ahead, off the stage's path.
         int rmax_next[4] = {0, 0, 0, 0};
+        if (QA && !mbar_wait(qa_ready, 0, abort_flag, kWaitLimitNs)) ok = false;  // the A scale tiles
         if (UE && n_i > 0) {
             const int mt0 = seq_tile<EPI, CTA2>(p, 0, NT, MT, paired, W).mt;
 #pragma unroll
@@ -578,7 +601,8 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
                     break;
                 }
                 const uint32_t sfa_t = tmem + lane_off + SF_TMEM_COL + stage * SF_COLS, sfb_t = sfa_t + 16;
-                const uint4 *ssfa = reinterpret_cast<const uint4 *>(smem + OFF_SFA + stage * SFA_BYTES) + lane;
+                const uint4 *ssfa =
+                    reinterpret_cast<const uint4 *>(smem + OFF_SFA + (QA ? kt : (int)stage) * SFA_BYTES) + lane;
                 const uint4 *ssfb = reinterpret_cast<const uint4 *>(smem + OFF_SFB + stage * SFB_BYTES) + lane;
                 uint4 v[4];
 #pragma unroll
@@ -669,6 +693,47 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC>::NUM_THREADS, 1)
             z_next = min(n4, (long long)blockIdx.x * per_cta);
             z_end = min(n4, z_next + per_cta);
             z_slice = (per_cta + my_tiles - 1) / my_tiles;
+        }
+        if constexpr (QA) {
+            // The m-tile's live rows (its first ones) quantised into the
+            // persistent A slices, one 16-element block per thread and item,
+            // by the a1 quantiser's block routine, at the bytes a 128-byte-
+            // swizzled TMA load of 16-row boxes would fill; their scale bytes
+            // into the persistent scale tiles.  The m-tile's first tile (one
+            // CTA per m-tile) also writes them to the A operand in memory.
+            const TileInfo<EPI> ti0 = seq_tile<EPI, CTA2>(p, 0, NT, MT, paired, W);
+            const int row0 = ti0.mt * BM;
+            const int nlive = min(p.pad_off[ti0.e] + p.counts[ti0.e] - row0, P::DEC_ROWS);
+            const int nblk = p.K >> 4;
+            const float g = p.g1[ti0.e];
+            uint8_t *const aq = const_cast<uint8_t *>(p.a_q);  // the workspace's A operand
+            uint8_t *const asf = const_cast<uint8_t *>(p.a_sf);
+            for (int it = ew * 32 + lane; it < nlive * nblk; it += EPI_THREADS) {
+                const int r = it / nblk, kb = it - r * nblk;
+                const int f = __ldg(p.row_src + row0 + r);
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)(f / p.k) * p.K + kb * 16);
+                const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                f32x2 xv[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) xv[j] = bf16x2_to_f32x2(wv[j]);
+                uint32_t sb;
+                const uint2 q = quant_block16(xv, amax16_bf16(wv), g, &tab, sb);
+                const int kt = kb >> 4, kb16 = kb & 15;
+                *reinterpret_cast<uint2 *>(smem + OFF_A + kt * P::A_STRIDE + r * (BK / 2) +
+                                           (((kb16 >> 1) ^ (r & 7)) << 4) + ((kb16 & 1) << 3)) = q;
+                smem[OFF_SFA + kt * SFA_BYTES + (kb16 >> 2) * SF_TILE + (r & 31) * 16 + (r >> 5) * 4 + (kb16 & 3)] =
+                    (uint8_t)sb;
+                if (ti0.nt == 0) {
+                    const int row = row0 + r;
+                    *reinterpret_cast<uint2 *>(aq + (size_t)row * (p.K >> 1) + kb * 8) = q;
+                    asf[((size_t)(row >> 7) * p.a_kc + (kb >> 2)) * SF_TILE + (row & 31) * 16 + ((row >> 5) & 3) * 4 +
+                        (kb & 3)] = (uint8_t)sb;
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the MMAs' reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qa_ready);
         }
         for (int i = group; i < n_i; i += EPI_GROUPS) {
             // everything the tile needs besides the accumulator is fetched
@@ -908,11 +973,11 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t row
     return make_tensor_map_2d(m, base, row_bytes, rows, 128, box_rows, true);
 }
 
-template <int EPI, bool UE, bool CTA2, bool DEC = false>
+template <int EPI, bool UE, bool CTA2, bool DEC = false, bool QA = false>
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
 {
-    using P = Plan<EPI, CTA2, DEC>;
-    auto kernel = moe_gemm_kernel<EPI, UE, CTA2, DEC>;
+    using P = Plan<EPI, CTA2, DEC, QA>;
+    auto kernel = moe_gemm_kernel<EPI, UE, CTA2, DEC, QA>;
     // function attributes and the pair form's resident cluster count are per
     // device: taken once on each
     static bool attr_set[64] = {false};
@@ -1029,7 +1094,9 @@ bool make_tensor_map_2d(CUtensorMap *m, const void *base, uint64_t row_bytes, ui
 cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st)
 {
     if (a.pairs) return a.ue8m0 ? launch_gemm<0, true, true>(a, st) : launch_gemm<0, false, true>(a, st);
-    if (a.small && !a.ue8m0) return launch_gemm<0, false, false, true>(a, st);
+    if (a.small && !a.ue8m0)
+        return a.a_inline ? launch_gemm<0, false, false, true, true>(a, st) : launch_gemm<0, false, false, true>(a, st);
+    if (a.a_inline) return cudaErrorInvalidValue;  // A is quantised in the kernel by the small-batch plan only
     return a.ue8m0 ? launch_gemm<0, true, false>(a, st) : launch_gemm<0, false, false>(a, st);
 }
 cudaError_t launch_gemm_w2(const GemmArgs &a, cudaStream_t st)

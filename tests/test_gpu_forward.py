@@ -111,6 +111,21 @@ def test_small_batch_plan(m):
     check_layer(m, layer, W, extra_flags=m.W13_ONE_SM)
 
 
+def test_small_batch_plan_a_in_kernel(m):
+    """The small-batch plan quantises A in the GEMM when every CTA gets one
+    tile (busy experts x 64-column tiles within the SM count) and H is at most
+    3072: the tiny and 1-token layers above take it.  Here H = 3072 (all twelve
+    K slices of the in-kernel A buffer, several live rows per m-tile), then
+    H = 3328 (over the limit: the quantiser runs, same plan) and the 4-token
+    decode layer (32 experts x 11 tiles: more tiles than SMs, the quantiser
+    runs)."""
+    for H in (3072, 3328):
+        layer, W = layer_with_weights(S._softmax_layer(f"inlineA_H{H}", seed=1020, E=6, H=H, I=192, T=8, k=4))
+        check_layer(m, layer, W)
+    layer, W = layer_with_weights(S._softmax_layer("decode_shape_T4", seed=1021, E=128, H=2816, I=704, T=4, k=8))
+    check_layer(m, layer, W)
+
+
 def test_small_batch_plan_w2_full_stage(m):
     """w2's small-batch plan (at most 64 routed rows: A stages of an m-tile's
     first 64 rows, the combine from registers) with all 64 rows in one
