@@ -559,6 +559,26 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     ra.live_mtiles = pairs ? reinterpret_cast<int *>(base + L.live_mtiles) : nullptr;
     ra.padded = 1;
     ra.hdr = hdr;
+
+    // The w13 GEMM's small-batch plan when its waves of 64-column tiles (over
+    // at most min(R, E) busy experts) take less time than the wide plan's
+    // waves; a narrow tile's K loop takes about 0.55 of a wide one's.  It
+    // quantises A itself, routing its own tile, when every CTA gets one tile
+    // (busy experts x 64-column tiles within the SM count; at most
+    // kSmallPlanRows <= 128 rows: one m-tile per busy expert), K fits its
+    // persistent A buffer, and the routing runs as one kernel (not in timed
+    // calls, which separate the scale check from the routing).
+    const long long sms = sm_count();
+    bool small_w13, a_inline;
+    {
+        const long long busy = std::min<long long>((long long)R, E);
+        const long long small_waves = (busy * ((I + 63) / 64) + sms - 1) / sms;
+        const long long wide_waves = (busy * ((I + 127) / 128) + sms - 1) / sms;
+        small_w13 = !pairs && !ue && !(flags & NVFP4_W13_ONE_SM) && (long long)R <= kSmallPlanRows &&
+                    100 * small_waves < 182 * wide_waves;
+        a_inline = small_w13 && !events && busy * ((I + 63) / 64) <= sms && (long long)H <= kInlineQuantMaxK;
+    }
+    ra.trigger_after_wait = a_inline ? 1 : 0;  // w13 reads the call's inputs before its dependency wait
     // The routing returns at once when the check has failed, so it may be
     // queued before the host reads the status.  Timed calls keep the two
     // launches apart so that each has its own interval.
@@ -576,23 +596,6 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
         rc = read_header(hdr, st, &h);
         if (rc) return rc;
         if (h.status) return header_status(h, nullptr);
-    }
-
-    // The w13 GEMM's small-batch plan when its waves of 64-column tiles (over
-    // at most min(R, E) busy experts) take less time than the wide plan's
-    // waves; a narrow tile's K loop takes about 0.55 of a wide one's.  It
-    // quantises A itself when every CTA gets one tile (m-tiles x 64-column
-    // tiles within the SM count) and K fits its persistent A buffer.
-    const long long sms = sm_count();
-    bool small_w13, a_inline;
-    {
-        const long long busy = std::min<long long>((long long)R, E);
-        const long long small_waves = (busy * ((I + 63) / 64) + sms - 1) / sms;
-        const long long wide_waves = (busy * ((I + 127) / 128) + sms - 1) / sms;
-        small_w13 = !pairs && !ue && !(flags & NVFP4_W13_ONE_SM) && (long long)R <= kSmallPlanRows &&
-                    100 * small_waves < 182 * wide_waves;
-        // (at most kSmallPlanRows <= 128 rows: one m-tile per busy expert)
-        a_inline = small_w13 && busy * ((I + 63) / 64) <= sms && (long long)H <= kInlineQuantMaxK;
     }
 
     if (!a_inline) {
@@ -657,8 +660,11 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     ga.small = small_w13 ? 1 : 0;
     ga.a_inline = a_inline ? 1 : 0;
     ga.x = x;
-    ga.g1 = g;
-    ga.row_src = ra.row_src;
+    ga.ids = ids;
+    ga.R = R;
+    ga.in_scale1 = w->w13_input_scale;
+    ga.in_scale2 = w->w2_input_scale;
+    ga.w13_scale2 = w->w13_scale2;
     NV_CUDA(launch_gemm_w13(ga, st), "launching the w13 GEMM");
     NV_CUDA(mark(4), "recording an event");
 

@@ -75,6 +75,10 @@ struct RouteArgs {
     int *live_mtiles;  // the 128-row m-tiles that hold rows, in order (nullable); count in hdr->num_live_mtiles
     int padded;
     DevHeader *hdr;
+    // one-CTA routing: let the next kernel be scheduled only after this one's
+    // dependency wait, so that it may read the call's inputs before its own
+    // (the w13 GEMM that routes itself)
+    int trigger_after_wait;
 };
 cudaError_t launch_route(const RouteArgs &a, cudaStream_t st);
 // The scale check then the routing: one kernel when the routing takes one CTA
@@ -150,9 +154,15 @@ struct GemmArgs {
     int mtiles_cap;
     int pairs;                 // w13: CTA pairs on m-tile pairs (rows padded to 256 per expert)
     int small;                 // the small-batch plan (w13: at most kSmallPlanRows routed rows, w2: kSmallPlanRowsW2)
-    int a_inline;              // w13 small-batch plan: A quantised in the kernel from x (also written to a_q / a_sf)
-    const uint16_t *x;         // a_inline: BF16 tokens [T, K]
-    const float *g1;           // a_inline: per-expert global scale of the A rows
+    // w13 small-batch plan, a_inline: the kernel routes its own tile from the
+    // call's inputs (ids, the input and weight scales), quantises A from x
+    // (also writing it to a_q / a_sf), and runs its loads and MMAs before its
+    // dependency wait; only its writes wait for the scale check and routing
+    int a_inline;
+    const uint16_t *x;         // BF16 tokens [T, K]
+    const int32_t *ids;        // top-k ids [R]
+    int R;
+    const float *in_scale1, *in_scale2, *w13_scale2;  // w13_input_scale, w2_input_scale, w13 weight_scale_2 [E]
     const int *live_mtiles;    // w2: the m-tiles holding rows, in order (nullable: all m-tiles)
 };
 cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st);

@@ -95,7 +95,14 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 //       block routine) into a persistent buffer of all its K slices, in the
 //       layout a TMA 128-byte-swizzled load leaves, and their scales into
 //       persistent scale tiles; the producer streams only the weights, and
-//       the a1 quantiser launch goes.  A 6-stage ring.
+//       the a1 quantiser launch goes.  A 6-stage ring.  The CTA also routes
+//       its own tile from the call's ids (at most 32 routed rows: one m-tile
+//       per busy expert, in expert order, rows in flat order, as the routing
+//       kernel lays them out) and forms its expert's scales from the input and
+//       weight scales as the scale check does, so that the loads, the A
+//       quantisation and the MMAs need nothing the routing kernel writes and
+//       run before the dependency wait; the epilogue's writes come after it,
+//       and only when the scale check and routing passed.
 constexpr int kDecRows = (int)kSmallPlanRows, kDecRowsW2 = (int)kSmallPlanRowsW2;
 static_assert(kDecRows % 16 == 0 && kDecRowsW2 % 16 == 0, "A is loaded in 16-row boxes");
 constexpr int kQaSlices = (int)kInlineQuantMaxK / BK;  // K slices of the persistent A buffer
@@ -143,7 +150,8 @@ struct Plan {
     static constexpr int OFF_BAR = OFF_AS + A_SLOTS * A_BYTES;
     static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_BUFS + 2;  // + drain, QA's A-ready
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-    static constexpr int OFF_XPOSE = (OFF_MISC + 16 + 15) & ~15;
+    static constexpr int OFF_QAR = (OFF_MISC + 16 + 15) & ~15;  // QA: the tile's own routing (QaRoute)
+    static constexpr int OFF_XPOSE = (OFF_QAR + (QA ? 256 : 0) + 15) & ~15;
     static constexpr int XPOSE_BYTES = EPI == 1 && !DEC ? NUM_EPI_WARPS * 32 * XPOSE_LD * 4 : 0;
     static constexpr int SMEM_BYTES = OFF_XPOSE + XPOSE_BYTES + 1024;  // + alignment slack
     static_assert(SF_TMEM_COL + STAGES * SF_COLS <= TMEM_COLS, "scale slots exceed TMEM");
@@ -202,6 +210,65 @@ struct TileInfo {
     int nblk;     // 128-row scale tiles per 64-K step of the tile's scale block (w13 full block: 2, else 1)
     int compose;  // w13 64-column tile cut from a full block: 1 + which half of its two tiles; else 0
 };
+// QA: the CTA's own tile, routed from the call's ids in the prologue (one
+// warp), and its expert's scales.
+struct QaRoute {
+    int f[32];           // the m-tile's live rows: their flat indices t * k + j, in order
+    int e;               // the tile's expert; -1: no tile for this CTA
+    int mt, nt;          // m-tile (the expert's rank among the busy experts) and 64-column tile
+    int nlive;           // live rows of the m-tile
+    int mtiles;          // busy experts: one m-tile each
+    int bad;             // an id outside [0, E) (the routing kernel refuses the call)
+    float g1, g2, alpha; // 1/w13_input_scale, 1/w2_input_scale, 1/(g1 * 1/w13 weight_scale_2)
+};
+static_assert(sizeof(QaRoute) <= 256, "QA routing block");
+
+// Up to 32 routed rows (one per lane): each busy expert holds one m-tile (at
+// most 32 rows of 128), m-tiles in ascending expert order, an expert's rows in
+// ascending flat index: the layout the routing kernel writes.  The scales are
+// the scale check's reciprocals and alpha, by the same operations.
+__device__ __forceinline__ void qa_route(const GemmArgs &p, QaRoute *q, int lane)
+{
+    const unsigned full = 0xffffffffu;
+    int id = lane < p.R ? ld_cg(p.ids + lane) : -1;
+    const bool live = lane < p.R && id >= 0 && id < p.E;
+    const bool anybad = __ballot_sync(full, lane < p.R && !live) != 0u;
+    if (!live) id = -1;
+    const unsigned peers = __match_any_sync(full, live ? id : -1 - lane);
+    const bool first = live && __ffs(peers) - 1 == lane;  // the expert's first row
+    int rank = 0;  // busy experts below this row's
+    for (int j = 0; j < 32; ++j) {
+        const int idj = __shfl_sync(full, id, j);
+        const int fj = __shfl_sync(full, first ? 1 : 0, j);
+        rank += (fj != 0 && idj < id) ? 1 : 0;
+    }
+    const unsigned firsts = __ballot_sync(full, first);
+    const int NTq = (p.gate_up_I + 63) / 64;
+    const int mt = (int)blockIdx.x / NTq, nt = (int)blockIdx.x - mt * NTq;
+    const unsigned hit = __ballot_sync(full, first && rank == mt);
+    const int eid = __shfl_sync(full, id, hit ? __ffs(hit) - 1 : 0);
+    const int e = (hit != 0u && !anybad) ? eid : -1;
+    const unsigned rows = __ballot_sync(full, live && id == e);
+    if ((rows >> lane) & 1u) q->f[__popc(rows & ((1u << lane) - 1u))] = lane;
+    if (lane == 0) {
+        q->e = e;
+        q->mt = mt;
+        q->nt = nt;
+        q->nlive = __popc(rows);
+        q->mtiles = __popc(firsts);
+        q->bad = anybad ? 1 : 0;
+        float g1 = 1.0f, g2 = 1.0f, alpha = 1.0f;
+        if (e >= 0) {
+            g1 = __frcp_rn(ld_cg(p.in_scale1 + e));
+            g2 = __frcp_rn(ld_cg(p.in_scale2 + e));
+            alpha = __frcp_rn(__fmul_rn(g1, __frcp_rn(ld_cg(p.w13_scale2 + e))));
+        }
+        q->g1 = g1;
+        q->g2 = g2;
+        q->alpha = alpha;
+    }
+}
+
 // w2 walks the m-tiles that hold rows (live_mtiles, when the rows are padded
 // to 256 for the paired w13) in order.
 __device__ __forceinline__ int mtile_of(const GemmArgs &p, int mi) { return p.live_mtiles ? p.live_mtiles[mi] : mi; }
@@ -269,6 +336,22 @@ __device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int 
         return ti;
     }
     return tile_info<EPI>(p, (int)blockIdx.x + i * (int)gridDim.x, NT, MT, W);
+}
+
+// QA: the tile qa_route chose (w13, 64-column tiles)
+template <int EPI>
+__device__ __forceinline__ TileInfo<EPI> qa_tile(const GemmArgs &p, const QaRoute *q)
+{
+    TileInfo<EPI> ti;
+    ti.mt = q->mt;
+    ti.nt = q->nt;
+    ti.e = q->e;
+    ti.hc0 = 64 * ti.nt;
+    ti.hc = min(64, p.gate_up_I - ti.hc0);
+    const bool full_block = (ti.hc0 & ~127) + 128 <= p.gate_up_I;
+    ti.nblk = full_block ? 2 : 1;
+    ti.compose = full_block ? 1 + (ti.nt & 1) : 0;
+    return ti;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -342,16 +425,22 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
             asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
         }
     }
+    // QA: the CTA's tile from the call's inputs (no dependency wait)
+    const QaRoute *qr = reinterpret_cast<const QaRoute *>(smem + P::OFF_QAR);
+    if (QA && warp == 2) qa_route(p, reinterpret_cast<QaRoute *>(smem + P::OFF_QAR), lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (CTA2) cluster_sync_all();  // the peer's barriers are initialised before any arrival on them
 
-    pdl_wait();  // the previous kernel's outputs (A operand, row maps, status)
+    if (!QA) pdl_wait();  // the previous kernel's outputs (A operand, row maps, status)
     constexpr int W = DEC ? 64 : 128;  // w13 tile width in h columns
     const int NT = EPI == 0 ? (p.gate_up_I + W - 1) / W : p.N / 128;
     // w13 pairs: units of two m-tiles; w2: the m-tiles that hold rows
-    const int MT = CTA2 ? p.hdr->num_mtiles / 2 : (EPI == 1 && p.live_mtiles) ? p.hdr->num_live_mtiles : p.hdr->num_mtiles;
+    const int MT = QA     ? (qr->bad ? 0 : qr->mtiles)
+                   : CTA2 ? p.hdr->num_mtiles / 2
+                   : (EPI == 1 && p.live_mtiles) ? p.hdr->num_live_mtiles
+                                                 : p.hdr->num_mtiles;
     const int ntiles = MT * NT;
     const int KT = (p.K + BK - 1) / BK;
     // work is shared out per CTA, or per CTA pair
@@ -367,10 +456,15 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
     const int n_i = nunits > b ? ((nunits - b + G - 1) / G) * (paired ? 2 : 1) : 0;  // this CTA's tiles
     // QA keeps one m-tile's A for the whole kernel: the host takes it only
     // when no CTA gets a second tile (a broken promise is reported, not run)
-    if (QA && n_i > 1 && threadIdx.x == 0) atomicOr(&p.hdr->error_flags, kErrPlan);
-    if (p.hdr->status != 0 || n_i == 0 || (QA && n_i > 1)) {
+    const bool plan_broken = QA && n_i > 1;
+    if ((!QA && p.hdr->status != 0) || n_i == 0 || plan_broken) {
         // nothing to do (same decision in every thread, and in both CTAs of a
-        // pair): give TMEM back
+        // pair): give TMEM back.  QA: after the dependency wait, so that this
+        // grid completes after the routing kernel.
+        if (QA) {
+            pdl_wait();
+            if (plan_broken && threadIdx.x == 0) atomicOr(&p.hdr->error_flags, kErrPlan);
+        }
         if (warp == 1) {
             if (CTA2)
                 asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot),
@@ -394,7 +488,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
         bool ok = true;
         const size_t b_sf_expert = (size_t)(p.N / 128) * p.b_kc * SF_TILE;  // prepared scale bytes per expert
         for (int i = 0; i < n_i && ok; ++i) {
-            const TileInfo<EPI> ti = seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
+            const TileInfo<EPI> ti = QA ? qa_tile<EPI>(p, qr) : seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
             const bool fill_a = !paired || (i & 1) == 0;  // w2: the first tile of a pair brings A
             const uint8_t *b_sf = p.b_sf + (size_t)ti.e * b_sf_expert +
                                   (size_t)(EPI == 0 ? 2 * (ti.hc0 >> 7) : ti.nt) * p.b_kc * SF_TILE;
@@ -584,7 +678,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
             for (int q = 0; q < 4; ++q) rmax_next[q] = __ldg(p.a_row_max + mt0 * BM + q * 32 + lane);
         }
         for (int i = 0; i < n_i && ok; ++i) {
-            const TileInfo<EPI> ti = seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
+            const TileInfo<EPI> ti = QA ? qa_tile<EPI>(p, qr) : seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
             uint32_t c4[4] = {0u, 0u, 0u, 0u};
             if (UE) {
 #pragma unroll
@@ -694,25 +788,21 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
             z_end = min(n4, z_next + per_cta);
             z_slice = (per_cta + my_tiles - 1) / my_tiles;
         }
+        int n_epi = n_i;  // tiles whose results this CTA writes
         if constexpr (QA) {
-            // The m-tile's live rows (its first ones) quantised into the
-            // persistent A slices, one 16-element block per thread and item,
-            // by the a1 quantiser's block routine, at the bytes a 128-byte-
-            // swizzled TMA load of 16-row boxes would fill; their scale bytes
-            // into the persistent scale tiles.  The m-tile's first tile (one
-            // CTA per m-tile) also writes them to the A operand in memory.
-            const TileInfo<EPI> ti0 = seq_tile<EPI, CTA2>(p, 0, NT, MT, paired, W);
-            const int row0 = ti0.mt * BM;
-            const int nlive = min(p.pad_off[ti0.e] + p.counts[ti0.e] - row0, P::DEC_ROWS);
-            const int nblk = p.K >> 4;
-            const float g = p.g1[ti0.e];
-            uint8_t *const aq = const_cast<uint8_t *>(p.a_q);  // the workspace's A operand
-            uint8_t *const asf = const_cast<uint8_t *>(p.a_sf);
+            // The m-tile's live rows quantised into the persistent A slices,
+            // one 16-element block per thread and item, by the a1 quantiser's
+            // block routine, at the bytes a 128-byte-swizzled TMA load of
+            // 16-row boxes would fill; their scale bytes into the persistent
+            // scale tiles.  x is an input of the call: it was complete before
+            // this kernel could start (the routing kernel lets it start only
+            // after its own dependency wait).
+            const int nlive = qr->nlive, nblk = p.K >> 4;
+            const float g = qr->g1;
             for (int it = ew * 32 + lane; it < nlive * nblk; it += EPI_THREADS) {
                 const int r = it / nblk, kb = it - r * nblk;
-                const int f = __ldg(p.row_src + row0 + r);
-                const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)(f / p.k) * p.K + kb * 16);
-                const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)(qr->f[r] / p.k) * p.K + kb * 16);
+                const uint4 v0 = ld_cg(src), v1 = ld_cg(src + 1);
                 const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
                 f32x2 xv[8];
 #pragma unroll
@@ -724,27 +814,45 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
                                            (((kb16 >> 1) ^ (r & 7)) << 4) + ((kb16 & 1) << 3)) = q;
                 smem[OFF_SFA + kt * SFA_BYTES + (kb16 >> 2) * SF_TILE + (r & 31) * 16 + (r >> 5) * 4 + (kb16 & 3)] =
                     (uint8_t)sb;
-                if (ti0.nt == 0) {
-                    const int row = row0 + r;
-                    *reinterpret_cast<uint2 *>(aq + (size_t)row * (p.K >> 1) + kb * 8) = q;
-                    asf[((size_t)(row >> 7) * p.a_kc + (kb >> 2)) * SF_TILE + (row & 31) * 16 + ((row >> 5) & 3) * 4 +
-                        (kb & 3)] = (uint8_t)sb;
-                }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // for the MMAs' reads
             __syncwarp();
             if (lane == 0) mbar_arrive(qa_ready);
+            // Writes only from here: after the scale check and routing, and
+            // only when they passed.  The m-tile's first tile (one CTA per
+            // m-tile) copies its A rows to the workspace's A operand.
+            pdl_wait();
+            if (p.hdr->status != 0) n_epi = 0;
+            if (n_epi > 0 && qr->nt == 0) {
+                const int row0 = qr->mt * BM;
+                uint8_t *const aq = const_cast<uint8_t *>(p.a_q);
+                uint8_t *const asf = const_cast<uint8_t *>(p.a_sf);
+                for (int it = ew * 32 + lane; it < nlive * nblk; it += EPI_THREADS) {
+                    const int r = it / nblk, kb = it - r * nblk, row = row0 + r;
+                    const int kt = kb >> 4, kb16 = kb & 15;
+                    *reinterpret_cast<uint2 *>(aq + (size_t)row * (p.K >> 1) + kb * 8) =
+                        *reinterpret_cast<const uint2 *>(smem + OFF_A + kt * P::A_STRIDE + r * (BK / 2) +
+                                                         (((kb16 >> 1) ^ (r & 7)) << 4) + ((kb16 & 1) << 3));
+                    asf[((size_t)(row >> 7) * p.a_kc + (kb >> 2)) * SF_TILE + (row & 31) * 16 + ((row >> 5) & 3) * 4 +
+                        (kb & 3)] = smem[OFF_SFA + kt * SFA_BYTES + (kb16 >> 2) * SF_TILE + (r & 31) * 16 +
+                                         (r >> 5) * 4 + (kb16 & 3)];
+                }
+            }
         }
-        for (int i = group; i < n_i; i += EPI_GROUPS) {
+        for (int i = group; i < n_epi; i += EPI_GROUPS) {
             // everything the tile needs besides the accumulator is fetched
             // before waiting for it
-            const TileInfo<EPI> ti = seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
+            const TileInfo<EPI> ti = QA ? qa_tile<EPI>(p, qr) : seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
             const int e = ti.e, nt = ti.nt;
             const int row = ti.mt * BM + r_in;
             bool valid;
             float s0, s1;  // w13: alpha, g2; w2: routing weight * alpha2
             int t = 0;     // w2: token of the row
-            if (EPI == 0) {
+            if (QA) {
+                valid = r_in < qr->nlive;
+                s0 = qr->alpha;
+                s1 = qr->g2;
+            } else if (EPI == 0) {
                 valid = row < p.pad_off[e] + p.counts[e];
                 s0 = p.alpha[e];
                 s1 = p.g2[e];

@@ -395,8 +395,9 @@ __global__ void __launch_bounds__(kRouteThreads) validate_route_tiny_kernel(Vali
     extern __shared__ int sh[];
     __shared__ int s_bad;
     __shared__ int s_wsum[2][kRouteWarps];
-    pdl_trigger();
+    if (!a.trigger_after_wait) pdl_trigger();
     pdl_wait();  // whatever ran before on the stream (a previous call may still read the header)
+    if (a.trigger_after_wait) pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, E = a.E;
     const int nsteps = (a.R + 31) >> 5;  // 32-row steps; step s holds rows [32 s, 32 s + 32)
     int id[kTinyRouteRowsPerThread];
@@ -914,6 +915,7 @@ cudaError_t launch_validate_route(const ValidateArgs &v, const RouteArgs &a, cud
                          a);
         return err != cudaSuccess ? err : cudaGetLastError();
     }
+    if (a.trigger_after_wait) return cudaErrorInvalidValue;  // the one-CTA form only
     int grid = 0;
     cudaError_t err = route_plan(a, &grid);
     if (err != cudaSuccess) return err;

@@ -126,6 +126,39 @@ def test_small_batch_plan_a_in_kernel(m):
     check_layer(m, layer, W)
 
 
+def test_small_batch_plan_a_in_kernel_duplicate_ids(m):
+    """The self-routed form with an expert named twice by one token (two rows
+    of one token in one m-tile) and by two tokens, against the oracle."""
+    layer = S._softmax_layer("decode_dup", seed=1022, E=128, H=2816, I=704, T=2, k=4)
+    layer.topk_ids = layer.topk_ids.copy()
+    layer.topk_ids[0, 1] = layer.topk_ids[0, 0]
+    layer.topk_ids[1, 2] = layer.topk_ids[0, 0]
+    layer, W = layer_with_weights(layer)
+    check_layer(m, layer, W)
+
+
+def test_bad_expert_id_refused_self_routed(m):
+    """At one token the w13 GEMM routes its own tile and runs its loads and
+    MMAs before the routing kernel's status is known.  With the host check
+    skipped, an expert id outside [0, E) still stops the call: no CTA takes a
+    tile, nothing is written, out keeps its contents, the status reads
+    INVALID_ARG.  A following call on the same workspace is exact."""
+    layer, W = layer_with_weights(S.decode(1))
+    ids = layer.topk_ids.copy()
+    ids[0, 3] = layer.E
+    out = torch.full((layer.T, layer.H), 7.0, device="cuda")
+    _, ws = m.moe_forward(device_weights(W), dev_bf16(layer.x), dev(ids), dev(layer.topk_w), out=out,
+                          flags=m.SCALES_PREVALIDATED)
+    torch.cuda.synchronize()
+    assert m.moe_status(ws)[0] == m.ERR_INVALID_ARG
+    assert bool((out == 7.0).all())
+    out2, _ = m.moe_forward(device_weights(W), dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w),
+                            ws=ws, flags=m.SYNC_CHECK)
+    torch.cuda.synchronize()
+    ref = oracle.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W)
+    assert_close(host(out2), ref["out"], "out")
+
+
 def test_small_batch_plan_w2_full_stage(m):
     """w2's small-batch plan (at most 64 routed rows: A stages of an m-tile's
     first 64 rows, the combine from registers) with all 64 rows in one
@@ -229,10 +262,11 @@ def test_prefill_unwritten_slots_rejected_before_launch(m, prefill):
 @pytest.mark.parametrize("T", [1, 8])
 def test_decode_refused_on_device_then_clean_call(m, T):
     """At decode sizes the scale check and the routing share one kernel (at
-    one token also the a1 quantiser).  With the host check skipped, a bad
-    scale still stops the call on the device: the GEMM kernels find the bad
-    status, give back their TMEM and leave, and out keeps its contents.  A
-    following call on the same workspace is exact."""
+    one token the w13 GEMM quantises A and routes its own tile).  With the
+    host check skipped, a bad scale still stops the call on the device: the
+    GEMM kernels find the bad status, write nothing, give back their TMEM and
+    leave, and out keeps its contents.  A following call on the same
+    workspace is exact."""
     layer, W = layer_with_weights(S.decode(T))
     bad = device_weights(W)
     bad.w2_scale2 = bad.w2_scale2.clone()
