@@ -578,7 +578,11 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
                     100 * small_waves < 182 * wide_waves;
         a_inline = small_w13 && !events && busy * ((I + 63) / 64) <= sms && (long long)H <= kInlineQuantMaxK;
     }
-    ra.trigger_after_wait = a_inline ? 1 : 0;  // w13 reads the call's inputs before its dependency wait
+    // otherwise, with the wide tiles on single CTAs and up to kEarlyRows
+    // routed rows, w13 routes its tiles itself and starts its weight loads
+    // before its dependency wait
+    const bool early_w13 = !small_w13 && !pairs && !ue && !events && (long long)R <= kEarlyRows && E <= 1024;
+    ra.trigger_after_wait = (a_inline || early_w13) ? 1 : 0;  // w13 reads the call's inputs early
     // The routing returns at once when the check has failed, so it may be
     // queued before the host reads the status.  Timed calls keep the two
     // launches apart so that each has its own interval.
@@ -659,6 +663,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     ga.pairs = pairs ? 1 : 0;
     ga.small = small_w13 ? 1 : 0;
     ga.a_inline = a_inline ? 1 : 0;
+    ga.early = early_w13 ? 1 : 0;
     ga.x = x;
     ga.ids = ids;
     ga.R = R;
@@ -682,6 +687,7 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     gb.h_dump = nullptr;
     gb.row_src = ra.row_src;
     gb.a_inline = 0;
+    gb.early = 0;
     gb.topk_w = topk_w;
     gb.out = out;
     gb.pairs = 0;

@@ -45,6 +45,9 @@ constexpr long long kSmallPlanRowsW2 = 64;
 // launch) when every CTA gets one tile and K is at most this: the m-tile's
 // 32 rows of all K slices stay in shared memory for the whole kernel.
 constexpr long long kInlineQuantMaxK = 3072;
+// Up to this many routed rows (and E <= 1024) the w13 GEMM on single CTAs
+// routes its own tiles and starts its weight loads before its dependency wait.
+constexpr long long kEarlyRows = 128;
 
 WsLayout make_layout(int T, int H, int I, int E, int k);
 
@@ -163,6 +166,11 @@ struct GemmArgs {
     const int32_t *ids;        // top-k ids [R]
     int R;
     const float *in_scale1, *in_scale2, *w13_scale2;  // w13_input_scale, w2_input_scale, w13 weight_scale_2 [E]
+    // w13 on single CTAs, E4M3, at most kEarlyRows routed rows (E <= 1024):
+    // the kernel routes its tiles from the ids (one m-tile per busy expert)
+    // and issues the weight loads of its first ring stages before its
+    // dependency wait; their A loads and everything else follow the wait
+    int early;
     const int *live_mtiles;    // w2: the m-tiles holding rows, in order (nullable: all m-tiles)
 };
 cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st);

@@ -106,7 +106,7 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;
 constexpr int kDecRows = (int)kSmallPlanRows, kDecRowsW2 = (int)kSmallPlanRowsW2;
 static_assert(kDecRows % 16 == 0 && kDecRowsW2 % 16 == 0, "A is loaded in 16-row boxes");
 constexpr int kQaSlices = (int)kInlineQuantMaxK / BK;  // K slices of the persistent A buffer
-template <int EPI, bool CTA2 = false, bool DEC = false, bool QA = false>
+template <int EPI, bool CTA2 = false, bool DEC = false, bool QA = false, bool EARLY = false>
 struct Plan {
     static constexpr int DEC_ROWS = EPI == 0 ? kDecRows : kDecRowsW2;  // small-batch plan: A rows per stage
     static constexpr int BN = DEC ? 128 : EPI == 0 ? 256 : 128;  // widest tile (MMA N)
@@ -150,8 +150,10 @@ struct Plan {
     static constexpr int OFF_BAR = OFF_AS + A_SLOTS * A_BYTES;
     static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_BUFS + 2;  // + drain, QA's A-ready
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-    static constexpr int OFF_QAR = (OFF_MISC + 16 + 15) & ~15;  // QA: the tile's own routing (QaRoute)
-    static constexpr int OFF_XPOSE = (OFF_QAR + (QA ? 256 : 0) + 15) & ~15;
+    // the CTA's own routing: QaRoute (QA) or EarlyRoute (w13 on single CTAs)
+    static constexpr int OFF_QAR = (OFF_MISC + 16 + 15) & ~15;
+    static constexpr int QAR_BYTES = QA ? 256 : EARLY ? 1024 : 0;
+    static constexpr int OFF_XPOSE = (OFF_QAR + QAR_BYTES + 15) & ~15;
     static constexpr int XPOSE_BYTES = EPI == 1 && !DEC ? NUM_EPI_WARPS * 32 * XPOSE_LD * 4 : 0;
     static constexpr int SMEM_BYTES = OFF_XPOSE + XPOSE_BYTES + 1024;  // + alignment slack
     static_assert(SF_TMEM_COL + STAGES * SF_COLS <= TMEM_COLS, "scale slots exceed TMEM");
@@ -161,6 +163,7 @@ struct Plan {
     static_assert(!CTA2 || EPI == 0, "CTA pairs: w13 only");
     static_assert(!DEC || !CTA2, "the small-batch plans: single CTAs");
     static_assert(!QA || (DEC && EPI == 0 && DEC_ROWS == 32), "A quantised in the kernel: w13's small-batch plan");
+    static_assert(!EARLY || (EPI == 0 && !CTA2 && !DEC && !QA), "early weights: w13's wide tiles on single CTAs");
     static_assert(SMEM_BYTES + (EPI == 0 ? (int)sizeof(DivTable2) : 0) <= 232448,
                   "shared memory plan exceeds the opt-in limit");
 };
@@ -338,6 +341,45 @@ __device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int 
     return tile_info<EPI>(p, (int)blockIdx.x + i * (int)gridDim.x, NT, MT, W);
 }
 
+// Early weights (w13, at most kEarlyRows routed rows): the busy experts of
+// the call's ids, in ascending order.  Each holds one m-tile (at most 128
+// rows), in that order: the routing kernel's tile map.
+struct EarlyRoute {
+    unsigned bits[32];  // busy-expert bitmap (E <= 1024)
+    int busy[kEarlyRows];
+    int mtiles;
+    int bad;            // an id outside [0, E) (the routing kernel refuses the call)
+};
+static_assert(sizeof(EarlyRoute) <= 1024, "early routing block");
+
+__device__ __forceinline__ void early_route(const GemmArgs &p, EarlyRoute *q, int lane)
+{
+    const unsigned full = 0xffffffffu;
+    q->bits[lane] = 0u;
+    __syncwarp();
+    bool bad = false;
+    for (int f = lane; f < p.R; f += 32) {
+        const int id = ld_cg(p.ids + f);
+        if (id >= 0 && id < p.E)
+            atomicOr(&q->bits[id >> 5], 1u << (id & 31));
+        else
+            bad = true;
+    }
+    __syncwarp();
+    const unsigned w = q->bits[lane];
+    const int c = __popc(w);
+    int incl = c;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(full, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int pos = incl - c;
+    for (unsigned m = w; m != 0u && pos < kEarlyRows; m &= m - 1u) q->busy[pos++] = 32 * lane + __ffs(m) - 1;
+    const bool anybad = __any_sync(full, bad || p.R > kEarlyRows);  // (the host keeps R within kEarlyRows)
+    if (lane == 31) q->mtiles = incl;
+    if (lane == 0) q->bad = anybad ? 1 : 0;
+}
+
 // QA: the tile qa_route chose (w13, 64-column tiles)
 template <int EPI>
 __device__ __forceinline__ TileInfo<EPI> qa_tile(const GemmArgs &p, const QaRoute *q)
@@ -354,6 +396,44 @@ __device__ __forceinline__ TileInfo<EPI> qa_tile(const GemmArgs &p, const QaRout
     return ti;
 }
 
+// Early weights: tile t of the m-tile-major order, its expert from the
+// early route instead of the routing kernel's tile map.
+template <int EPI>
+__device__ __forceinline__ TileInfo<EPI> early_tile(const GemmArgs &p, const EarlyRoute *q, int t, int NT, int W)
+{
+    TileInfo<EPI> ti;
+    ti.mt = t / NT;
+    ti.nt = t - ti.mt * NT;
+    ti.e = q->busy[ti.mt];
+    ti.hc0 = W * ti.nt;
+    ti.hc = min(W, p.gate_up_I - ti.hc0);
+    const bool full_block = (ti.hc0 & ~127) + 128 <= p.gate_up_I;
+    ti.nblk = full_block ? 2 : 1;
+    ti.compose = W == 64 && full_block ? 1 + (ti.nt & 1) : 0;
+    return ti;
+}
+
+// Early weights: the A loads of the first n ring stages (stage s holds load
+// s of the CTA's sequence: tile b + (s / KT) * G, K step s % KT), issued once
+// the dependency wait has returned.
+template <class P, bool DEC>
+__device__ __forceinline__ void early_a_loads(const GemmArgs &p, uint8_t *smem, uint64_t *full, const CUtensorMap *ta,
+                                              const CUtensorMap *ta16, int n, int b, int G, int NT, int KT)
+{
+    for (int s = 0; s < n; ++s) {
+        const int mt = (b + (s / KT) * G) / NT, kt = s % KT;
+        const int kx = kt * (BK / 2);
+        if constexpr (DEC) {
+            for (int r = 0; r < P::DEC_ROWS; r += 16)
+                tma_2d(smem + P::OFF_A + s * P::A_STRIDE + r * (BK / 2), ta16, kx, mt * BM + r, &full[s]);
+        } else {
+            tma_2d(smem + P::OFF_A + s * A_BYTES, ta, kx, mt * BM, &full[s]);
+        }
+        bulk_g2s(smem + P::OFF_SFA + s * SFA_BYTES, p.a_sf + ((size_t)mt * p.a_kc + 4 * kt) * SF_TILE, SFA_BYTES,
+                 &full[s]);
+    }
+}
+
 // ---------------------------------------------------------------- kernel
 // EPI 0: w13 (SiLU*up + requantise), 1: w2 (weighted combine).  UE: UE8M0
 // block scales throughout.  The A scales arrive as UE8M0 bytes and are
@@ -362,12 +442,12 @@ __device__ __forceinline__ TileInfo<EPI> qa_tile(const GemmArgs &p, const QaRout
 // prepared.  The epilogue multiplies both rows' factors back: the A row's
 // into the row scale, the weight row's per output column.  w13 then writes
 // a2 as UE8M0 bytes with each row's largest byte (out_row_max).
-template <int EPI, bool UE, bool CTA2, bool DEC, bool QA>
-__global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
+template <int EPI, bool UE, bool CTA2, bool DEC, bool QA, bool EARLY>
+__global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA, EARLY>::NUM_THREADS, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_a16, const GemmArgs p, const DivTable tab_in)
 {
-    using P = Plan<EPI, CTA2, DEC, QA>;
+    using P = Plan<EPI, CTA2, DEC, QA, EARLY>;
     constexpr int STAGES = P::STAGES, ACC_BUFS = P::ACC_BUFS, OFF_A = P::OFF_A, OFF_B = P::OFF_B,
                   OFF_SFA = P::OFF_SFA, OFF_SFB = P::OFF_SFB, OFF_BAR = P::OFF_BAR, OFF_MISC = P::OFF_MISC,
                   OFF_XPOSE = P::OFF_XPOSE, B_BYTES = P::B_BYTES, SFB_BYTES = P::SFB_BYTES,
@@ -425,20 +505,24 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
             asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
         }
     }
-    // QA: the CTA's tile from the call's inputs (no dependency wait)
+    // QA, early weights: the CTA's tiles from the call's inputs (no dependency wait)
     const QaRoute *qr = reinterpret_cast<const QaRoute *>(smem + P::OFF_QAR);
+    const EarlyRoute *er = reinterpret_cast<const EarlyRoute *>(smem + P::OFF_QAR);
+    constexpr bool early = EARLY && !UE;
     if (QA && warp == 2) qa_route(p, reinterpret_cast<QaRoute *>(smem + P::OFF_QAR), lane);
+    if (early && warp == 2) early_route(p, reinterpret_cast<EarlyRoute *>(smem + P::OFF_QAR), lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (CTA2) cluster_sync_all();  // the peer's barriers are initialised before any arrival on them
 
-    if (!QA) pdl_wait();  // the previous kernel's outputs (A operand, row maps, status)
+    if (!QA && !early) pdl_wait();  // the previous kernel's outputs (A operand, row maps, status)
     constexpr int W = DEC ? 64 : 128;  // w13 tile width in h columns
     const int NT = EPI == 0 ? (p.gate_up_I + W - 1) / W : p.N / 128;
     // w13 pairs: units of two m-tiles; w2: the m-tiles that hold rows
-    const int MT = QA     ? (qr->bad ? 0 : qr->mtiles)
-                   : CTA2 ? p.hdr->num_mtiles / 2
+    const int MT = QA      ? (qr->bad ? 0 : qr->mtiles)
+                   : early ? (er->bad ? 0 : er->mtiles)
+                   : CTA2  ? p.hdr->num_mtiles / 2
                    : (EPI == 1 && p.live_mtiles) ? p.hdr->num_live_mtiles
                                                  : p.hdr->num_mtiles;
     const int ntiles = MT * NT;
@@ -457,11 +541,11 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
     // QA keeps one m-tile's A for the whole kernel: the host takes it only
     // when no CTA gets a second tile (a broken promise is reported, not run)
     const bool plan_broken = QA && n_i > 1;
-    if ((!QA && p.hdr->status != 0) || n_i == 0 || plan_broken) {
+    if ((!QA && !early && p.hdr->status != 0) || n_i == 0 || plan_broken) {
         // nothing to do (same decision in every thread, and in both CTAs of a
-        // pair): give TMEM back.  QA: after the dependency wait, so that this
-        // grid completes after the routing kernel.
-        if (QA) {
+        // pair): give TMEM back.  QA, early weights: after the dependency
+        // wait, so that this grid completes after the kernels before it.
+        if (QA || early) {
             pdl_wait();
             if (plan_broken && threadIdx.x == 0) atomicOr(&p.hdr->error_flags, kErrPlan);
         }
@@ -487,8 +571,15 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
         uint32_t last_parity = 0;      // bit s: parity of that last load's phase
         bool ok = true;
         const size_t b_sf_expert = (size_t)(p.N / 128) * p.b_kc * SF_TILE;  // prepared scale bytes per expert
+        // Early weights: the first ring stages (all of them, or all the loads
+        // when fewer) get their weight loads before the dependency wait and
+        // their A loads (the quantiser's output) once it returns.
+        bool waited = !early;
+        int nd = 0;  // stages loaded so far before the wait (stage s = s, tile 0 .. )
         for (int i = 0; i < n_i && ok; ++i) {
-            const TileInfo<EPI> ti = QA ? qa_tile<EPI>(p, qr) : seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
+            const TileInfo<EPI> ti = QA      ? qa_tile<EPI>(p, qr)
+                                     : early ? early_tile<EPI>(p, er, b + i * G, NT, W)
+                                             : seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
             const bool fill_a = !paired || (i & 1) == 0;  // w2: the first tile of a pair brings A
             const uint8_t *b_sf = p.b_sf + (size_t)ti.e * b_sf_expert +
                                   (size_t)(EPI == 0 ? 2 * (ti.hc0 >> 7) : ti.nt) * p.b_kc * SF_TILE;
@@ -510,7 +601,9 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
                 mbar_expect_tx(fb, QA ? b_bytes + sfb_bytes
                                       : (a_now || DEC ? a_bytes : 0u) + b_bytes + SFA_BYTES + sfb_bytes);
                 uint8_t *sb = smem + OFF_B + stage * B_BYTES;
-                if constexpr (QA) {
+                if (!waited) {
+                    ++nd;
+                } else if constexpr (QA) {
                 } else if constexpr (DEC) {
                     for (int r = 0; r < P::DEC_ROWS; r += 16)
                         tma_2d(smem + OFF_A + stage * P::A_STRIDE + r * (BK / 2), &tmap_a16, kx, ti.mt * BM + r, fb);
@@ -535,7 +628,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
                 } else {
                     tma_2d(sb, &tmap_b, kx, ti.e * p.N + ti.nt * 128, fb);
                 }
-                if (!QA)
+                if (!QA && waited)
                     bulk_g2s(smem + OFF_SFA + stage * SFA_BYTES,
                              p.a_sf + ((size_t)ti.mt * p.a_kc + 4 * kt) * SF_TILE, SFA_BYTES, fb);
                 bulk_g2s(smem + OFF_SFB + stage * SFB_BYTES, b_sf + (size_t)4 * kt * ti.nblk * SF_TILE, sfb_bytes,
@@ -546,7 +639,16 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
                     stage = 0;
                     phase ^= 1u;
                 }
+                if (!waited && nd == STAGES) {
+                    pdl_wait();
+                    waited = true;
+                    early_a_loads<P, DEC>(p, smem, full, &tmap_a, &tmap_a16, nd, b, G, NT, KT);
+                }
             }
+        }
+        if (!waited) {
+            pdl_wait();
+            early_a_loads<P, DEC>(p, smem, full, &tmap_a, &tmap_a16, nd, b, G, NT, KT);
         }
         if (!ok) {
             *abort_flag = 1;
@@ -678,7 +780,9 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
             for (int q = 0; q < 4; ++q) rmax_next[q] = __ldg(p.a_row_max + mt0 * BM + q * 32 + lane);
         }
         for (int i = 0; i < n_i && ok; ++i) {
-            const TileInfo<EPI> ti = QA ? qa_tile<EPI>(p, qr) : seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
+            const TileInfo<EPI> ti = QA      ? qa_tile<EPI>(p, qr)
+                                     : early ? early_tile<EPI>(p, er, b + i * G, NT, W)
+                                             : seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
             uint32_t c4[4] = {0u, 0u, 0u, 0u};
             if (UE) {
 #pragma unroll
@@ -789,6 +893,11 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA>::NUM_THREADS, 1)
             z_slice = (per_cta + my_tiles - 1) / my_tiles;
         }
         int n_epi = n_i;  // tiles whose results this CTA writes
+        if (early) {
+            // the routing's tile map, the quantiser's A and the status from here
+            pdl_wait();
+            if (p.hdr->status != 0) n_epi = 0;
+        }
         if constexpr (QA) {
             // The m-tile's live rows quantised into the persistent A slices,
             // one 16-element block per thread and item, by the a1 quantiser's
@@ -1081,11 +1190,11 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t row
     return make_tensor_map_2d(m, base, row_bytes, rows, 128, box_rows, true);
 }
 
-template <int EPI, bool UE, bool CTA2, bool DEC = false, bool QA = false>
+template <int EPI, bool UE, bool CTA2, bool DEC = false, bool QA = false, bool EARLY = false>
 cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t st)
 {
-    using P = Plan<EPI, CTA2, DEC, QA>;
-    auto kernel = moe_gemm_kernel<EPI, UE, CTA2, DEC, QA>;
+    using P = Plan<EPI, CTA2, DEC, QA, EARLY>;
+    auto kernel = moe_gemm_kernel<EPI, UE, CTA2, DEC, QA, EARLY>;
     // function attributes and the pair form's resident cluster count are per
     // device: taken once on each
     static bool attr_set[64] = {false};
@@ -1202,9 +1311,12 @@ bool make_tensor_map_2d(CUtensorMap *m, const void *base, uint64_t row_bytes, ui
 cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st)
 {
     if (a.pairs) return a.ue8m0 ? launch_gemm<0, true, true>(a, st) : launch_gemm<0, false, true>(a, st);
-    if (a.small && !a.ue8m0)
+    if (a.small && !a.ue8m0) {
+        if (a.early) return cudaErrorInvalidValue;  // the wide tiles only
         return a.a_inline ? launch_gemm<0, false, false, true, true>(a, st) : launch_gemm<0, false, false, true>(a, st);
+    }
     if (a.a_inline) return cudaErrorInvalidValue;  // A is quantised in the kernel by the small-batch plan only
+    if (a.early) return a.ue8m0 ? cudaErrorInvalidValue : launch_gemm<0, false, false, false, false, true>(a, st);
     return a.ue8m0 ? launch_gemm<0, true, false>(a, st) : launch_gemm<0, false, false>(a, st);
 }
 cudaError_t launch_gemm_w2(const GemmArgs &a, cudaStream_t st)

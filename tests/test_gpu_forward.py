@@ -126,10 +126,13 @@ def test_small_batch_plan_a_in_kernel(m):
     check_layer(m, layer, W)
 
 
-def test_small_batch_plan_a_in_kernel_duplicate_ids(m):
-    """The self-routed form with an expert named twice by one token (two rows
-    of one token in one m-tile) and by two tokens, against the oracle."""
-    layer = S._softmax_layer("decode_dup", seed=1022, E=128, H=2816, I=704, T=2, k=4)
+@pytest.mark.parametrize("T,k", [(2, 4), (8, 8)])
+def test_self_routed_duplicate_ids(m, T, k):
+    """The w13 forms that route their own tiles from the ids (8 routed rows:
+    the small-batch plan quantising A itself; 64: the wide tiles starting
+    their weight loads early) with an expert named twice by one token (two
+    rows of one token in one m-tile) and by two tokens, against the oracle."""
+    layer = S._softmax_layer(f"decode_dup_T{T}", seed=1022, E=128, H=2816, I=704, T=T, k=k)
     layer.topk_ids = layer.topk_ids.copy()
     layer.topk_ids[0, 1] = layer.topk_ids[0, 0]
     layer.topk_ids[1, 2] = layer.topk_ids[0, 0]
@@ -137,13 +140,15 @@ def test_small_batch_plan_a_in_kernel_duplicate_ids(m):
     check_layer(m, layer, W)
 
 
-def test_bad_expert_id_refused_self_routed(m):
-    """At one token the w13 GEMM routes its own tile and runs its loads and
-    MMAs before the routing kernel's status is known.  With the host check
-    skipped, an expert id outside [0, E) still stops the call: no CTA takes a
-    tile, nothing is written, out keeps its contents, the status reads
-    INVALID_ARG.  A following call on the same workspace is exact."""
-    layer, W = layer_with_weights(S.decode(1))
+@pytest.mark.parametrize("T", [1, 8])
+def test_bad_expert_id_refused_self_routed(m, T):
+    """At decode sizes the w13 GEMM routes its own tiles and starts loading
+    (at one token also computing) before the routing kernel's status is
+    known.  With the host check skipped, an expert id outside [0, E) still
+    stops the call: no CTA takes a tile, nothing is written, out keeps its
+    contents, the status reads INVALID_ARG.  A following call on the same
+    workspace is exact."""
+    layer, W = layer_with_weights(S.decode(T))
     ids = layer.topk_ids.copy()
     ids[0, 3] = layer.E
     out = torch.full((layer.T, layer.H), 7.0, device="cuda")
