@@ -49,10 +49,10 @@ LAUNCHES_PER_STEP = 5
 # counters.  It holds for the kernel source it was taken on: any change to these files makes it null.
 NCU_TRAFFIC = {
     "tokens": 8192,
-    "source_sha1": {"nvfp4_w4a4_moe_gb300/csrc/kernels_gemm.cu": "7c40ef2b33f99599dbd54640e3bd4d729939daa5",
+    "source_sha1": {"nvfp4_w4a4_moe_gb300/csrc/kernels_gemm.cu": "88e1c523b15443566db1dd6ecb51edce5855be41",
                     "nvfp4_w4a4_moe_gb300/csrc/tc_common.cuh": "a2ee1d30e584fa75518c2785c3cd69d7ddb8da35",
-                    "nvfp4_w4a4_moe_gb300/csrc/common.cuh": "a0a73c7d8b17232adcfd9a885f0ccca3b2b31732"},
-    "bytes": {"gemm_w13": 394249472 + 103171328, "gemm_w2": 278044928 + 64703232},
+                    "nvfp4_w4a4_moe_gb300/csrc/common.cuh": "0428d7d24646c64d83c1960a2dc5b0380bbe36ed"},
+    "bytes": {"gemm_w13": 394253824 + 103232256, "gemm_w2": 278051072 + 64794624},
 }
 
 
@@ -514,9 +514,14 @@ def quant_workload(m, torch, w, args):
             "note": "bytes = x read once + codes and scales written + routing reads"}
 
 
+# about 25 ms at the SM clock: longer than the host takes to issue 500 graph replays
+REPLAY_QUEUE_SPIN_CYCLES = 50_000_000
+
+
 def decode_leg(m, torch, w, args):
     """The decode-shaped layers (same experts, 1-64 tokens): latency per call
-    of the plain forward, of a CUDA-graph replay of one call, and per call
+    of the plain forward, of a CUDA-graph replay of one call (replays queued
+    on the GPU; also as paced by the host's launches), and per call
     inside a graph of ten back-to-back calls (as in a captured multi-layer
     decode step, where one call's first kernel overlaps the previous call's
     tail), tokens/s, and the bandwidth over the weight bytes of the experts
@@ -553,7 +558,7 @@ def decode_leg(m, torch, w, args):
         b.record()
         torch.cuda.synchronize()
         us = a.elapsed_time(b) / n * 1e3
-        graph_us, graph_err, graph10_us, copies_us = None, None, None, None
+        graph_us, graph_err, graph10_us, copies_us, graph_host_paced_us = None, None, None, None, None
         try:
             g = torch.cuda.CUDAGraph()
             s = torch.cuda.Stream()
@@ -567,6 +572,17 @@ def decode_leg(m, torch, w, args):
             for _ in range(20):
                 g.replay()
             torch.cuda.synchronize()
+            # replays issued back to back from the host: at one token the host's
+            # graph launches (about 20 us each on this machine) pace the GPU
+            a.record()
+            for _ in range(n):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            graph_host_paced_us = a.elapsed_time(b) / n * 1e3
+            # the same replays queued behind a spin kernel, so that the GPU runs
+            # them back to back: the device time of one replay
+            torch.cuda._sleep(REPLAY_QUEUE_SPIN_CYCLES)
             a.record()
             for _ in range(n):
                 g.replay()
@@ -622,6 +638,7 @@ def decode_leg(m, torch, w, args):
         touched = len(np.unique(L.topk_ids))
         best = graph_us if graph_us is not None else us
         res[str(T)] = {"us_per_call": us, "us_per_graph_replay": graph_us,
+                       "us_per_graph_replay_host_paced": graph_host_paced_us,
                        "us_per_call_in_graph_of_10": graph10_us,
                        "us_per_call_over_8_weight_copies": copies_us, "graph_error": graph_err,
                        "tokens_per_s": T / (best * 1e-6), "experts_touched": touched,

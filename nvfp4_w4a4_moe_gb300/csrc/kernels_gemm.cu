@@ -163,7 +163,8 @@ struct Plan {
     static_assert(!CTA2 || EPI == 0, "CTA pairs: w13 only");
     static_assert(!DEC || !CTA2, "the small-batch plans: single CTAs");
     static_assert(!QA || (DEC && EPI == 0 && DEC_ROWS == 32), "A quantised in the kernel: w13's small-batch plan");
-    static_assert(!EARLY || (EPI == 0 && !CTA2 && !DEC && !QA), "early weights: w13's wide tiles on single CTAs");
+    static_assert(!EARLY || (!CTA2 && !QA && (EPI == 0 ? !DEC : DEC)),
+                  "early weights: w13's wide tiles, w2's small-batch plan, single CTAs");
     static_assert(SMEM_BYTES + (EPI == 0 ? (int)sizeof(DivTable2) : 0) <= 232448,
                   "shared memory plan exceeds the opt-in limit");
 };
@@ -396,32 +397,45 @@ __device__ __forceinline__ TileInfo<EPI> qa_tile(const GemmArgs &p, const QaRout
     return ti;
 }
 
-// Early weights: tile t of the m-tile-major order, its expert from the
-// early route instead of the routing kernel's tile map.
+// Early weights: tile t of tile_info's order (w13 m-tile major, w2 column
+// block major), its expert from the early route instead of the routing
+// kernel's tile map.
 template <int EPI>
-__device__ __forceinline__ TileInfo<EPI> early_tile(const GemmArgs &p, const EarlyRoute *q, int t, int NT, int W)
+__device__ __forceinline__ TileInfo<EPI> early_tile(const GemmArgs &p, const EarlyRoute *q, int t, int NT, int MT,
+                                                    int W)
 {
     TileInfo<EPI> ti;
-    ti.mt = t / NT;
-    ti.nt = t - ti.mt * NT;
+    if (EPI == 0) {
+        ti.mt = t / NT;
+        ti.nt = t - ti.mt * NT;
+    } else {
+        ti.nt = t / MT;
+        ti.mt = t - ti.nt * MT;
+    }
     ti.e = q->busy[ti.mt];
-    ti.hc0 = W * ti.nt;
-    ti.hc = min(W, p.gate_up_I - ti.hc0);
-    const bool full_block = (ti.hc0 & ~127) + 128 <= p.gate_up_I;
-    ti.nblk = full_block ? 2 : 1;
-    ti.compose = W == 64 && full_block ? 1 + (ti.nt & 1) : 0;
+    if (EPI == 0) {
+        ti.hc0 = W * ti.nt;
+        ti.hc = min(W, p.gate_up_I - ti.hc0);
+        const bool full_block = (ti.hc0 & ~127) + 128 <= p.gate_up_I;
+        ti.nblk = full_block ? 2 : 1;
+        ti.compose = W == 64 && full_block ? 1 + (ti.nt & 1) : 0;
+    } else {
+        ti.hc = ti.hc0 = ti.compose = 0;
+        ti.nblk = 1;
+    }
     return ti;
 }
 
 // Early weights: the A loads of the first n ring stages (stage s holds load
 // s of the CTA's sequence: tile b + (s / KT) * G, K step s % KT), issued once
 // the dependency wait has returned.
-template <class P, bool DEC>
+template <int EPI, class P, bool DEC>
 __device__ __forceinline__ void early_a_loads(const GemmArgs &p, uint8_t *smem, uint64_t *full, const CUtensorMap *ta,
-                                              const CUtensorMap *ta16, int n, int b, int G, int NT, int KT)
+                                              const CUtensorMap *ta16, int n, int b, int G, int NT, int MT, int KT)
 {
     for (int s = 0; s < n; ++s) {
-        const int mt = (b + (s / KT) * G) / NT, kt = s % KT;
+        const int t = b + (s / KT) * G, kt = s % KT;
+        const int mt = EPI == 0 ? t / NT : t % MT;
         const int kx = kt * (BK / 2);
         if constexpr (DEC) {
             for (int r = 0; r < P::DEC_ROWS; r += 16)
@@ -578,7 +592,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA, EARLY>::NUM_THREADS, 
         int nd = 0;  // stages loaded so far before the wait (stage s = s, tile 0 .. )
         for (int i = 0; i < n_i && ok; ++i) {
             const TileInfo<EPI> ti = QA      ? qa_tile<EPI>(p, qr)
-                                     : early ? early_tile<EPI>(p, er, b + i * G, NT, W)
+                                     : early ? early_tile<EPI>(p, er, b + i * G, NT, MT, W)
                                              : seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
             const bool fill_a = !paired || (i & 1) == 0;  // w2: the first tile of a pair brings A
             const uint8_t *b_sf = p.b_sf + (size_t)ti.e * b_sf_expert +
@@ -642,13 +656,13 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA, EARLY>::NUM_THREADS, 
                 if (!waited && nd == STAGES) {
                     pdl_wait();
                     waited = true;
-                    early_a_loads<P, DEC>(p, smem, full, &tmap_a, &tmap_a16, nd, b, G, NT, KT);
+                    early_a_loads<EPI, P, DEC>(p, smem, full, &tmap_a, &tmap_a16, nd, b, G, NT, MT, KT);
                 }
             }
         }
         if (!waited) {
             pdl_wait();
-            early_a_loads<P, DEC>(p, smem, full, &tmap_a, &tmap_a16, nd, b, G, NT, KT);
+            early_a_loads<EPI, P, DEC>(p, smem, full, &tmap_a, &tmap_a16, nd, b, G, NT, MT, KT);
         }
         if (!ok) {
             *abort_flag = 1;
@@ -781,7 +795,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA, EARLY>::NUM_THREADS, 
         }
         for (int i = 0; i < n_i && ok; ++i) {
             const TileInfo<EPI> ti = QA      ? qa_tile<EPI>(p, qr)
-                                     : early ? early_tile<EPI>(p, er, b + i * G, NT, W)
+                                     : early ? early_tile<EPI>(p, er, b + i * G, NT, MT, W)
                                              : seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
             uint32_t c4[4] = {0u, 0u, 0u, 0u};
             if (UE) {
@@ -1321,7 +1335,9 @@ cudaError_t launch_gemm_w13(const GemmArgs &a, cudaStream_t st)
 }
 cudaError_t launch_gemm_w2(const GemmArgs &a, cudaStream_t st)
 {
-    if (a.small && !a.ue8m0) return launch_gemm<1, false, false, true>(a, st);
+    if (a.small && !a.ue8m0)
+        return a.early ? launch_gemm<1, false, false, true, false, true>(a, st) : launch_gemm<1, false, false, true>(a, st);
+    if (a.early) return cudaErrorInvalidValue;  // the small-batch plan only
     return a.ue8m0 ? launch_gemm<1, true, false>(a, st) : launch_gemm<1, false, false>(a, st);
 }
 
