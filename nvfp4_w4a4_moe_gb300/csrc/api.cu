@@ -586,7 +586,10 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
     // A loads after the wait).  Measured: 0.3-0.7 us less per 1-token call;
     // with the quantiser's path (2 to 8 tokens) up to 0.7 us more, so not there.
     const bool early_w2 = a_inline && (long long)R <= kSmallPlanRowsW2 && (long long)R <= kEarlyRows;
-    ra.trigger_after_wait = (a_inline || early_w13 || early_w2) ? 1 : 0;  // the GEMMs read the call's inputs early
+    // the a1 quantiser forms its row map from the ids and runs beside the routing
+    const bool self_quant = !a_inline && !pairs && !ue && !events && (long long)R <= kEarlyRows && E <= 1024;
+    // (the kernels above read the call's inputs before their dependency waits)
+    ra.trigger_after_wait = (a_inline || early_w13 || early_w2 || self_quant) ? 1 : 0;
     // The routing returns at once when the check has failed, so it may be
     // queued before the host reads the status.  Timed calls keep the two
     // launches apart so that each has its own interval.
@@ -623,6 +626,9 @@ static int forward_impl(const nvfp4_moe_weights *w, const void *prepared, const 
         qa.sf_ue8m0 = ue ? 1 : 0;  // UE8M0 bytes, carried to the tensor cores per row by the GEMM
         qa.row_max = ue ? row_max : nullptr;
         qa.hdr = hdr;
+        qa.self_route = self_quant ? 1 : 0;
+        qa.in_scale = w->w13_input_scale;
+        qa.E = E;
         NV_CUDA(launch_quant_experts(qa, st), "launching the a1 quantiser");
     }
     NV_CUDA(mark(3), "recording an event");

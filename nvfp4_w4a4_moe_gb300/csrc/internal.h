@@ -100,6 +100,14 @@ struct QuantArgs {
     int sf_ue8m0;  // 0: E4M3 block scales; 1: UE8M0 bytes
     int *row_max;  // UE8M0: per padded row, the largest scale byte (atomicMax; nullable)
     DevHeader *hdr;  // read for the status; mode 2 writes a range error into it
+    // forward, E4M3, at most kEarlyRows routed rows, rows padded to 128 per
+    // expert: the kernel forms the row map (one m-tile per busy expert) and
+    // the global scales (1/in_scale, as the scale check) from the call's
+    // inputs and runs beside the routing kernel, whose completion it awaits
+    // only before it exits; row_of and g are not read
+    int self_route;
+    const float *in_scale;
+    int E;
 };
 cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st);
 

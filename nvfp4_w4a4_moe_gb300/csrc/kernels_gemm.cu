@@ -223,14 +223,12 @@ struct QaRoute {
     int nlive;           // live rows of the m-tile
     int mtiles;          // busy experts: one m-tile each
     int bad;             // an id outside [0, E) (the routing kernel refuses the call)
-    float g1, g2, alpha; // 1/w13_input_scale, 1/w2_input_scale, 1/(g1 * 1/w13 weight_scale_2)
 };
 static_assert(sizeof(QaRoute) <= 256, "QA routing block");
 
 // Up to 32 routed rows (one per lane): each busy expert holds one m-tile (at
 // most 32 rows of 128), m-tiles in ascending expert order, an expert's rows in
-// ascending flat index: the layout the routing kernel writes.  The scales are
-// the scale check's reciprocals and alpha, by the same operations.
+// ascending flat index: the layout the routing kernel writes.
 __device__ __forceinline__ void qa_route(const GemmArgs &p, QaRoute *q, int lane)
 {
     const unsigned full = 0xffffffffu;
@@ -261,15 +259,6 @@ __device__ __forceinline__ void qa_route(const GemmArgs &p, QaRoute *q, int lane
         q->nlive = __popc(rows);
         q->mtiles = __popc(firsts);
         q->bad = anybad ? 1 : 0;
-        float g1 = 1.0f, g2 = 1.0f, alpha = 1.0f;
-        if (e >= 0) {
-            g1 = __frcp_rn(ld_cg(p.in_scale1 + e));
-            g2 = __frcp_rn(ld_cg(p.in_scale2 + e));
-            alpha = __frcp_rn(__fmul_rn(g1, __frcp_rn(ld_cg(p.w13_scale2 + e))));
-        }
-        q->g1 = g1;
-        q->g2 = g2;
-        q->alpha = alpha;
     }
 }
 
@@ -907,6 +896,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA, EARLY>::NUM_THREADS, 
             z_slice = (per_cta + my_tiles - 1) / my_tiles;
         }
         int n_epi = n_i;  // tiles whose results this CTA writes
+        float qa_g2 = 1.0f, qa_alpha = 1.0f;  // QA: the expert's a2 scale and alpha
         if (early) {
             // the routing's tile map, the quantiser's A and the status from here
             pdl_wait();
@@ -920,8 +910,13 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA, EARLY>::NUM_THREADS, 
             // scale tiles.  x is an input of the call: it was complete before
             // this kernel could start (the routing kernel lets it start only
             // after its own dependency wait).
-            const int nlive = qr->nlive, nblk = p.K >> 4;
-            const float g = qr->g1;
+            // (the expert's scales are the scale check's reciprocals and
+            // alpha, by the same operations; loaded with the first x rows)
+            const int nlive = qr->nlive, nblk = p.K >> 4, eq = max(qr->e, 0);
+            const float in1 = ld_cg(p.in_scale1 + eq), in2 = ld_cg(p.in_scale2 + eq), ws2 = ld_cg(p.w13_scale2 + eq);
+            const float g = __frcp_rn(in1);
+            qa_g2 = __frcp_rn(in2);
+            qa_alpha = __frcp_rn(__fmul_rn(g, __frcp_rn(ws2)));
             for (int it = ew * 32 + lane; it < nlive * nblk; it += EPI_THREADS) {
                 const int r = it / nblk, kb = it - r * nblk;
                 const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)(qr->f[r] / p.k) * p.K + kb * 16);
@@ -973,8 +968,8 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA, EARLY>::NUM_THREADS, 
             int t = 0;     // w2: token of the row
             if (QA) {
                 valid = r_in < qr->nlive;
-                s0 = qr->alpha;
-                s1 = qr->g2;
+                s0 = qa_alpha;
+                s1 = qa_g2;
             } else if (EPI == 0) {
                 valid = row < p.pad_off[e] + p.counts[e];
                 s0 = p.alpha[e];

@@ -23,6 +23,8 @@ __device__ __forceinline__ int validate_body(const ValidateArgs &a)
 {
     __shared__ int s_bad, s_first, s_status;
     __shared__ float s_recip[4][1024];  // reciprocals for alpha (forward: 4 arrays, E <= 1024)
+    // the format word is read first, so that its load overlaps the scale loads
+    const uint32_t tag = threadIdx.x == 0 && a.prep_tag ? *a.prep_tag : a.prep_tag_want;
     if (threadIdx.x == 0) {
         s_bad = 0;
         s_first = INT_MAX;
@@ -56,7 +58,7 @@ __device__ __forceinline__ int validate_body(const ValidateArgs &a)
         }
     }
     if (threadIdx.x == 0) {
-        const bool tag_bad = a.prep_tag && *a.prep_tag != a.prep_tag_want;
+        const bool tag_bad = tag != a.prep_tag_want;
         const int status = s_bad ? 2 : tag_bad ? 4 : 0;
         a.hdr->bad_count = s_bad;
         a.hdr->first_bad = s_first;
@@ -544,15 +546,58 @@ constexpr int kQuantThreads = 128;  // 5 CTAs (20 warps) per SM at <= 96 registe
 // array, each routed row's largest scale byte is also recorded there
 // (atomicMax; the array is zero on entry): the GEMM carries the row's bytes
 // relative to it (ue8m0_carried).
-template <bool SWZ, int SF>
+//
+// SELF (QuantArgs::self_route): the row map from the ids in shared memory.
+// Expert e's rows start at 128 x (busy experts below e), in flat order; an id
+// outside [0, E) gets no row.  The call's inputs were complete before this
+// kernel could start (the one-CTA routing kernel lets it start only after its
+// own dependency wait).
+template <bool SWZ, int SF, bool SELF = false>
 __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantArgs a, DivTable tab_in)
 {
     __shared__ DivTable2 tab;
     pdl_trigger();
     load_div_table(&tab, tab_in);
-    __syncthreads();
-    pdl_wait();  // the routing kernel's row map and status
-    if (a.hdr && a.hdr->status != 0) return;
+    const int *srow = nullptr;
+    if constexpr (SELF) {
+        static_assert(kQuantThreads >= kEarlyRows, "one routed row per thread");
+        __shared__ int s_ids[kEarlyRows], s_row[kEarlyRows];
+        __shared__ unsigned s_bits[32];
+        __shared__ int s_wbase[32];
+        const int R = a.T * a.k, f = threadIdx.x;
+        if (f < 32) s_bits[f] = 0u;
+        const int id = f < R ? ld_cg(a.ids + f) : -1;
+        const bool ok = f < R && id >= 0 && id < a.E;
+        if (f < R) s_ids[f] = id;
+        __syncthreads();
+        if (ok) atomicOr(&s_bits[id >> 5], 1u << (id & 31));
+        __syncthreads();
+        if (f < 32) {
+            const int c = __popc(s_bits[f]);
+            int incl = c;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (f >= o) incl += v;
+            }
+            s_wbase[f] = incl - c;
+        }
+        __syncthreads();
+        if (f < R) {
+            int row = -1;
+            if (ok) {
+                int pos = 0;  // this expert's rows before f
+                for (int j = 0; j < R; ++j) pos += (j < f && s_ids[j] == id) ? 1 : 0;
+                row = 128 * (s_wbase[id >> 5] + __popc(s_bits[id >> 5] & ((1u << (id & 31)) - 1u))) + pos;
+            }
+            s_row[f] = row;
+        }
+        __syncthreads();
+        srow = s_row;
+    } else {
+        __syncthreads();
+        pdl_wait();  // the routing kernel's row map and status
+        if (a.hdr && a.hdr->status != 0) return;
+    }
     const int lane = threadIdx.x & 31;
     const int k = a.k, H = a.H;
     // blockIdx.y takes a share of each token's k experts: small batches spread
@@ -573,11 +618,21 @@ __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantAr
         uint32_t my_q = 0, my_s = 0;  // lane j < k: row parts of expert j's code and scale offsets
         uint32_t my_row = 0;
         float my_g = 1.0f;
+        bool my_ok = true;  // SELF: the row has a valid id
         if (lane < k) {
             const int f = t * k + lane;
-            const uint32_t row = (uint32_t)__ldg(a.row_of + f);
+            int srow_f = 0;
+            if constexpr (SELF) {
+                srow_f = srow[f];
+                my_ok = srow_f >= 0;
+                srow_f = max(srow_f, 0);
+            }
+            const uint32_t row = SELF ? (uint32_t)srow_f : (uint32_t)__ldg(a.row_of + f);
             my_row = row;
-            my_g = __ldg(a.g + __ldg(a.ids + f));
+            if constexpr (SELF)
+                my_g = my_ok ? __frcp_rn(ld_cg(a.in_scale + ld_cg(a.ids + f))) : 1.0f;
+            else
+                my_g = __ldg(a.g + __ldg(a.ids + f));
             my_q = row * (uint32_t)npair;
             my_s = SWZ ? ((row >> 7) * (uint32_t)a.sf_kc * 512u + (row & 31u) * 16u + ((row >> 5) & 3u) * 4u)
                        : row * (uint32_t)(H >> 4);
@@ -590,7 +645,7 @@ __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantAr
             const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + (size_t)pair * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint4 v = __ldg(src + i);
+                const uint4 v = SELF ? ld_cg(src + i) : __ldg(src + i);
                 w[4 * i] = v.x;
                 w[4 * i + 1] = v.y;
                 w[4 * i + 2] = v.z;
@@ -613,8 +668,9 @@ __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantAr
             const uint32_t qo = __shfl_sync(0xffffffffu, my_q, j) + (uint32_t)pair;
             const uint32_t so = __shfl_sync(0xffffffffu, my_s, j) + lane_s;
             const float g = __shfl_sync(0xffffffffu, my_g, j);
+            const bool okj = SELF ? __shfl_sync(0xffffffffu, my_ok ? 1 : 0, j) != 0 : true;
             uint32_t s0 = 0, s1 = 0;
-            if (active) {
+            if (active && okj) {
                 const uint2 p0 = SF ? quant_block16_ue8m0(x0, amax0, g, s0) : quant_block16(x0, amax0, g, &tab, s0);
                 const uint2 p1 = SF ? quant_block16_ue8m0(x1, amax1, g, s1) : quant_block16(x1, amax1, g, &tab, s1);
                 q16[qo] = make_uint4(p0.x, p0.y, p1.x, p1.y);
@@ -633,6 +689,9 @@ __global__ void __launch_bounds__(kQuantThreads, 5) quant_experts_kernel(QuantAr
             ++t;
         }
     }
+    // SELF: this grid completes only after the routing kernel, so that the
+    // next kernel's dependency wait covers both
+    if constexpr (SELF) pdl_wait();
 }
 
 // ------------------------------------------------------------------ UE8M0 weight rows
@@ -949,7 +1008,12 @@ cudaError_t launch_quant_experts(const QuantArgs &a, cudaStream_t st)
         return launch_pdl(kernel, dim3((int)grid, (int)ysplit), dim3(kQuantThreads), 0, st, a, div_table());
     };
     cudaError_t err;
-    if (a.sf_ue8m0)
+    if (a.self_route) {
+        // E4M3, swizzled, a padded row map of at most kEarlyRows routed rows
+        if (a.sf_ue8m0 || !a.sf_swizzled || (long long)a.T * a.k > kEarlyRows || !a.in_scale)
+            return cudaErrorInvalidValue;
+        err = launch(quant_experts_kernel<true, 0, true>);
+    } else if (a.sf_ue8m0)
         err = a.sf_swizzled ? launch(quant_experts_kernel<true, 1>) : launch(quant_experts_kernel<false, 1>);
     else
         err = a.sf_swizzled ? launch(quant_experts_kernel<true, 0>) : launch(quant_experts_kernel<false, 0>);
