@@ -422,9 +422,14 @@ __global__ void __launch_bounds__(kRouteThreads) validate_route_tiny_kernel(Vali
         const bool live = f < a.R;
         ok[i] = live && id[i] >= 0 && id[i] < E;
         if (live && !ok[i]) s_bad = 1;
-        const unsigned peers = __match_any_sync(0xffffffffu, ok[i] ? id[i] : -1 - lane);
-        wrank[i] = __popc(peers & ((1u << lane) - 1u));
-        if (ok[i] && wrank[i] == 0) wcnt[step * E + id[i]] = __popc(peers);
+        // (a step without a valid row skips the match: it costs about 0.3 us
+        // a step, and small batches fill one or two steps of 32)
+        wrank[i] = 0;
+        if (__any_sync(0xffffffffu, ok[i])) {
+            const unsigned peers = __match_any_sync(0xffffffffu, ok[i] ? id[i] : -1 - lane);
+            wrank[i] = __popc(peers & ((1u << lane) - 1u));
+            if (ok[i] && wrank[i] == 0) wcnt[step * E + id[i]] = __popc(peers);
+        }
     }
     __syncthreads();
     if (s_bad) {
