@@ -164,6 +164,36 @@ def test_bad_expert_id_refused_self_routed(m, T):
     assert_close(host(out2), ref["out"], "out")
 
 
+@pytest.mark.parametrize("which", ["decode1", "decode8", "tiny"])
+def test_timed_call_forms(m, which):
+    """The timed entry point (an event between launches) keeps the scale
+    check and the routing apart, so it takes the forms that wait for them:
+    at one token the small-batch plan fed by the quantiser, at 8 the wide
+    tiles without early weight loads and the quantiser's routed row map."""
+    layer = {"decode1": lambda: S.decode(1), "decode8": lambda: S.decode(8), "tiny": S.tiny}[which]()
+    layer, W = layer_with_weights(layer)
+    w = device_weights(W)
+    m.prepare_weights(w)
+    out = torch.empty((layer.T, layer.H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(m.moe_workspace_size(layer.T, layer.H, layer.I, layer.E, layer.k), dtype=torch.uint8,
+                     device="cuda")
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    m.moe_forward_profiled(w, dev_bf16(layer.x), dev(layer.topk_ids), dev(layer.topk_w), evs, out=out, ws=ws,
+                           flags=m.SYNC_CHECK)
+    torch.cuda.synchronize()
+    assert m.moe_status(ws)[0] == m.OK
+    ref = oracle.moe_forward(layer.x, layer.topk_ids, layer.topk_w, W)
+    assert_close(host(out), ref["out"], "out")
+
+
+def test_self_routed_most_experts(m):
+    """128 routed rows over E = 1024 experts: the w13 wide tiles with early
+    weight loads and the quantiser, both routing from a 1024-bit busy-expert
+    map of all 32 words."""
+    layer, W = layer_with_weights(S._softmax_layer("maxE_early", seed=1023, E=1024, H=256, I=128, T=16, k=8))
+    check_layer(m, layer, W)
+
+
 def test_small_batch_plan_w2_full_stage(m):
     """w2's small-batch plan (at most 64 routed rows: A stages of an m-tile's
     first 64 rows, the combine from registers) with all 64 rows in one
