@@ -290,6 +290,11 @@ int nvfp4_prepare_weights_format(const nvfp4_moe_weights *w, void *prepared, siz
  * weight codes 16 B.  Workspace: nvfp4_moe_workspace_size(T, H, I, E, k)
  * bytes of device memory, 256-byte aligned; its contents after the call are
  * internal.  T == 0 is valid (nothing is written).
+ * Ordering: the call's kernels read x, topk_ids, topk_weights, the weights
+ * and `prepared` once the work queued before them on `stream` has completed
+ * (small batches read them before the scale check's result is known, and
+ * write only after it); those buffers must not change until the call's work
+ * on `stream` has completed.
  */
 size_t nvfp4_moe_workspace_size(int T, int H, int I, int E, int k);
 int nvfp4_moe_forward(const nvfp4_moe_weights *w, const void *prepared, const uint16_t *x, int T,
