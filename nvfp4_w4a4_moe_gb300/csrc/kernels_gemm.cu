@@ -152,7 +152,7 @@ struct Plan {
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     // the CTA's own routing: QaRoute (QA) or EarlyRoute (w13 on single CTAs)
     static constexpr int OFF_QAR = (OFF_MISC + 16 + 15) & ~15;
-    static constexpr int QAR_BYTES = QA ? 256 : EARLY ? 1024 : 0;
+    static constexpr int QAR_BYTES = QA ? 256 : (EARLY || (EPI == 1 && DEC)) ? 1024 : 0;  // (w2 small: the tile map)
     static constexpr int OFF_XPOSE = (OFF_QAR + QAR_BYTES + 15) & ~15;
     static constexpr int XPOSE_BYTES = EPI == 1 && !DEC ? NUM_EPI_WARPS * 32 * XPOSE_LD * 4 : 0;
     static constexpr int SMEM_BYTES = OFF_XPOSE + XPOSE_BYTES + 1024;  // + alignment slack
@@ -270,8 +270,10 @@ __device__ __forceinline__ int mtile_of(const GemmArgs &p, int mi) { return p.li
 // tile's scales are those of the 128-column block holding it: per 64-K step
 // a gate and an up 128-row tile (a full block), or one tile of 64 gate + 64
 // up rows (the last block when I is an odd multiple of 64).
-template <int EPI>
-__device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, int NT, int MT, int W = 128)
+// STE: the tile map is read from a shared-memory copy `ste` instead of memory.
+template <int EPI, bool STE = false>
+__device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, int NT, int MT, int W = 128,
+                                                   const int *ste = nullptr)
 {
     TileInfo<EPI> ti;
     if (EPI == 0) {
@@ -287,7 +289,7 @@ __device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, 
         ti.nt = tile / MT;
         ti.mt = mtile_of(p, tile - ti.nt * MT);
     }
-    ti.e = p.tile_expert[ti.mt];
+    ti.e = STE ? ste[ti.mt] : p.tile_expert[ti.mt];
     if (EPI == 0) {
         ti.hc0 = W * ti.nt;
         ti.hc = min(W, p.gate_up_I - ti.hc0);
@@ -306,8 +308,9 @@ __device__ __forceinline__ TileInfo<EPI> tile_info(const GemmArgs &p, int tile, 
 // (m-tile, pair of adjacent output column blocks) in column-pair-major order,
 // unit (i/2) * gridDim + blockIdx, column block 2 * pair + (i & 1); the two
 // tiles of a unit run back to back and share the A operand.
-template <int EPI, bool CTA2 = false>
-__device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int NT, int MT, bool paired, int W)
+template <int EPI, bool CTA2 = false, bool STE = false>
+__device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int NT, int MT, bool paired, int W,
+                                                  const int *ste = nullptr)
 {
     if (CTA2) {
         // unit (m-tile pair, column tile), pair-major; this CTA's m-tile of the pair
@@ -328,7 +331,7 @@ __device__ __forceinline__ TileInfo<EPI> seq_tile(const GemmArgs &p, int i, int 
         ti.nblk = 1;
         return ti;
     }
-    return tile_info<EPI>(p, (int)blockIdx.x + i * (int)gridDim.x, NT, MT, W);
+    return tile_info<EPI, STE>(p, (int)blockIdx.x + i * (int)gridDim.x, NT, MT, W, ste);
 }
 
 // Early weights (w13, at most kEarlyRows routed rows): the busy experts of
@@ -520,6 +523,20 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA, EARLY>::NUM_THREADS, 
     if (CTA2) cluster_sync_all();  // the peer's barriers are initialised before any arrival on them
 
     if (!QA && !early) pdl_wait();  // the previous kernel's outputs (A operand, row maps, status)
+    // w2's small-batch plan: the routing's tile map (at most 130 m-tiles) into
+    // shared memory beside the header read, one round trip instead of the
+    // header's then the tile's expert's
+    constexpr bool STE = EPI == 1 && DEC && !EARLY;
+    const int *ste = reinterpret_cast<const int *>(smem + P::OFF_QAR);
+    int hdr_mtiles = 0, hdr_status = 0;
+    if constexpr (STE) {
+        hdr_mtiles = p.hdr->num_mtiles;
+        hdr_status = p.hdr->status;
+        int *ste_w = reinterpret_cast<int *>(smem + P::OFF_QAR);
+        const int cap = min(p.mtiles_cap, P::QAR_BYTES / 4);
+        for (int j = threadIdx.x; j < cap; j += P::NUM_THREADS) ste_w[j] = p.tile_expert[j];
+        __syncthreads();
+    }
     constexpr int W = DEC ? 64 : 128;  // w13 tile width in h columns
     const int NT = EPI == 0 ? (p.gate_up_I + W - 1) / W : p.N / 128;
     // w13 pairs: units of two m-tiles; w2: the m-tiles that hold rows
@@ -527,7 +544,8 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA, EARLY>::NUM_THREADS, 
                    : early ? (er->bad ? 0 : er->mtiles)
                    : CTA2  ? p.hdr->num_mtiles / 2
                    : (EPI == 1 && p.live_mtiles) ? p.hdr->num_live_mtiles
-                                                 : p.hdr->num_mtiles;
+                   : STE ? hdr_mtiles
+                         : p.hdr->num_mtiles;
     const int ntiles = MT * NT;
     const int KT = (p.K + BK - 1) / BK;
     // work is shared out per CTA, or per CTA pair
@@ -543,15 +561,14 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA, EARLY>::NUM_THREADS, 
     const int n_i = nunits > b ? ((nunits - b + G - 1) / G) * (paired ? 2 : 1) : 0;  // this CTA's tiles
     // QA keeps one m-tile's A for the whole kernel: the host takes it only
     // when no CTA gets a second tile (a broken promise is reported, not run)
-    const bool plan_broken = QA && n_i > 1;
-    if ((!QA && !early && p.hdr->status != 0) || n_i == 0 || plan_broken) {
+    // (and w2's small-batch plan holds at most QAR_BYTES / 4 m-tiles in its copy of the tile map)
+    const bool plan_broken = (QA && n_i > 1) || (STE && MT > P::QAR_BYTES / 4);
+    if ((!QA && !early && (STE ? hdr_status : p.hdr->status) != 0) || n_i == 0 || plan_broken) {
         // nothing to do (same decision in every thread, and in both CTAs of a
         // pair): give TMEM back.  QA, early weights: after the dependency
         // wait, so that this grid completes after the kernels before it.
-        if (QA || early) {
-            pdl_wait();
-            if (plan_broken && threadIdx.x == 0) atomicOr(&p.hdr->error_flags, kErrPlan);
-        }
+        if (QA || early) pdl_wait();
+        if (plan_broken && threadIdx.x == 0) atomicOr(&p.hdr->error_flags, kErrPlan);
         if (warp == 1) {
             if (CTA2)
                 asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot),
@@ -582,7 +599,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA, EARLY>::NUM_THREADS, 
         for (int i = 0; i < n_i && ok; ++i) {
             const TileInfo<EPI> ti = QA      ? qa_tile<EPI>(p, qr)
                                      : early ? early_tile<EPI>(p, er, b + i * G, NT, MT, W)
-                                             : seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
+                                             : seq_tile<EPI, CTA2, STE>(p, i, NT, MT, paired, W, ste);
             const bool fill_a = !paired || (i & 1) == 0;  // w2: the first tile of a pair brings A
             const uint8_t *b_sf = p.b_sf + (size_t)ti.e * b_sf_expert +
                                   (size_t)(EPI == 0 ? 2 * (ti.hc0 >> 7) : ti.nt) * p.b_kc * SF_TILE;
@@ -785,7 +802,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA, EARLY>::NUM_THREADS, 
         for (int i = 0; i < n_i && ok; ++i) {
             const TileInfo<EPI> ti = QA      ? qa_tile<EPI>(p, qr)
                                      : early ? early_tile<EPI>(p, er, b + i * G, NT, MT, W)
-                                             : seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
+                                             : seq_tile<EPI, CTA2, STE>(p, i, NT, MT, paired, W, ste);
             uint32_t c4[4] = {0u, 0u, 0u, 0u};
             if (UE) {
 #pragma unroll
@@ -960,7 +977,7 @@ __global__ void __launch_bounds__(Plan<EPI, CTA2, DEC, QA, EARLY>::NUM_THREADS, 
         for (int i = group; i < n_epi; i += EPI_GROUPS) {
             // everything the tile needs besides the accumulator is fetched
             // before waiting for it
-            const TileInfo<EPI> ti = QA ? qa_tile<EPI>(p, qr) : seq_tile<EPI, CTA2>(p, i, NT, MT, paired, W);
+            const TileInfo<EPI> ti = QA ? qa_tile<EPI>(p, qr) : seq_tile<EPI, CTA2, STE>(p, i, NT, MT, paired, W, ste);
             const int e = ti.e, nt = ti.nt;
             const int row = ti.mt * BM + r_in;
             bool valid;
