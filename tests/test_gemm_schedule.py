@@ -1,4 +1,5 @@
-"""The w2 GEMM's A-slot schedule, replayed on the host.
+"""The GEMMs' load schedules, replayed on the host: w2's A slots, and the
+A loads deferred past the dependency wait with early weight loads.
 
 The w2 kernel keeps A in a ring of A_SLOTS shared-memory slots outside its
 STAGES-deep B ring, and gives A no barrier of its own.  A fill (one 256-K stage
@@ -73,3 +74,43 @@ def test_pairing_rule_on_the_workloads():
     assert not paired_choice(127, NT, KT)      # decode, 64 tokens: 20 vs 19
     assert paired_choice(109, NT, KT)          # decode, 32 tokens: 16 vs 16
     assert not paired_choice(540, NT, -(-1536 // 256))  # six A stages do not fit the slots
+
+
+# ---------------------------------------------------------------- early weight loads
+# With early weight loads (w13's wide tiles, w2's small-batch plan beside the
+# self-routed w13) the producer issues the weight loads of its first ring
+# stages before its dependency wait and defers their A loads.  It waits once
+# STAGES loads are outstanding, or when its loads end, and then issues the A
+# loads of stages 0 .. n-1 from a closed form: load s belongs to tile
+# b + (s // KT) * G at K step s % KT.  These tests replay the producer's
+# sequence and check that the closed form names the same m-tile and K step
+# as the deferred load in that stage, and that no stage is refilled before
+# its A load was issued.
+
+
+def producer_deferred(KT, STAGES, n_i, b, G):
+    """(stage, tile, kt) of every load issued before the wait, in order."""
+    out, stage = [], 0
+    for i in range(n_i):
+        for kt in range(KT):
+            if len(out) == STAGES:
+                return out  # the wait and the A loads come before this stage is refilled
+            out.append((stage, b + i * G, kt))
+            stage = (stage + 1) % STAGES
+    return out
+
+
+def closed_form(n, KT, b, G):
+    return [(s, b + (s // KT) * G, s % KT) for s in range(n)]
+
+
+@pytest.mark.parametrize("STAGES", [4, 6, 7])
+@pytest.mark.parametrize("KT", [1, 2, 3, 11, 12])
+@pytest.mark.parametrize("n_i", [1, 2, 3, 7])
+def test_early_a_loads_match_the_deferred_stages(STAGES, KT, n_i):
+    for b, G in ((0, 152), (5, 152), (151, 152), (3, 8)):
+        deferred = producer_deferred(KT, STAGES, n_i, b, G)
+        assert len(deferred) == min(STAGES, KT * n_i)
+        assert deferred == closed_form(len(deferred), KT, b, G)
+        # stages 0 .. n-1, each once: no stage holds two deferred loads
+        assert [s for s, _, _ in deferred] == list(range(len(deferred)))
